@@ -1,0 +1,160 @@
+"""CPU oracle of the sparse MoE feed-forward block -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it (see ``moe_oracle.c`` for the definition it evaluates and
+the passages of "Optimizing on-device inference for Apple Silicon" it follows).
+
+Arrays are numpy: bfloat16 data is passed as its uint16 bit patterns
+(``dtype=0``), float32 as float32 (``dtype=1``).  All results come back in
+float64 except the router logits (float32, the precision in which the top-k
+decision is taken).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LOCK = threading.Lock()
+_LIBS: dict[int, ctypes.CDLL] = {}
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("F", ctypes.c_int), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("n_shared", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+def lib_path(mutation: int = 0) -> str:
+    if mutation == 0:
+        return os.path.join(_HERE, "liboracle.so")
+    return os.path.join(_HERE, "_mut", f"liboracle_m{mutation}.so")
+
+
+def build(mutation: int = 0, force: bool = False) -> str:
+    """Compile moe_oracle.c with gcc (OpenMP, -O2, IEEE arithmetic)."""
+    out = lib_path(mutation)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+           f"-DORACLE_MUTATION={mutation}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(mutation: int = 0) -> ctypes.CDLL:
+    with _LOCK:
+        if mutation in _LIBS:
+            return _LIBS[mutation]
+        lib = ctypes.CDLL(build(mutation))
+        vp, ip = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_route.argtypes = [ctypes.POINTER(Dims), vp, ip, vp, vp, vp, vp, vp, vp, ip]
+        lib.oracle_route.restype = ip
+        lib.oracle_forward.argtypes = [ctypes.POINTER(Dims), vp, ip, vp, vp,
+                                       vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ip]
+        lib.oracle_forward.restype = ip
+        _LIBS[mutation] = lib
+        return lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return 0
+    if a.dtype == np.float32:
+        return 1
+    raise TypeError(f"oracle takes uint16 (bf16 bits) or float32, got {a.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dt=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if dt is not None and a.dtype != dt:
+        raise TypeError(f"expected {dt}, got {a.dtype}")
+    return a
+
+
+def _default_threads() -> int:
+    return int(os.environ.get("ORACLE_THREADS", os.cpu_count() or 1))
+
+
+def route(x, wr, k, bias=None, nthreads=None, mutation=0):
+    """Router of the block: returns (idx[T][k] int32, w[T][k] f64, logits[T][E] f32, counts[E] int32).
+
+    x: [T][d], wr: [E][d], same element type; bias: float32 [E] or None.
+    """
+    x, wr = _c(x), _c(wr)
+    dt = _dtype_code(x)
+    assert _dtype_code(wr) == dt
+    T, d = x.shape
+    E = wr.shape[0]
+    bias = _c(bias, np.float32)
+    dims = Dims(d, 1, E, k, 0, dt)
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    logits = np.zeros((T, E), np.float32)
+    counts = np.zeros((E,), np.int32)
+    rc = load(mutation).oracle_route(ctypes.byref(dims), _ptr(x), T, _ptr(wr), _ptr(bias),
+                                     _ptr(idx), _ptr(w), _ptr(logits), _ptr(counts),
+                                     nthreads or _default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_route failed: {rc}")
+    return idx, w, logits, counts
+
+
+def forward(x, wr, wg, wu, wd, k, sg=None, su=None, sd=None, bias=None, nthreads=None,
+            mutation=0):
+    """The whole block: returns (out[T][d] f64, idx, w, counts).
+
+    wg, wu: [E][F][d] arrays or length-E sequences of [F][d] arrays (None where an
+    expert is never selected); wd likewise with [d][F].  sg/su/sd: shared expert
+    ([F][d], [F][d], [d][F]) or all None for no shared expert.
+    """
+    x, wr = _c(x), _c(wr)
+    dt = _dtype_code(x)
+    T, d = x.shape
+    E = wr.shape[0]
+
+    def plist(ws):
+        arrs = [None if a is None else _c(a) for a in ws]
+        for a in arrs:
+            if a is not None:
+                assert _dtype_code(a) == dt
+        return arrs, (ctypes.c_void_p * E)(*[None if a is None else a.ctypes.data for a in arrs])
+
+    wg_a, wg_p = plist(wg)
+    wu_a, wu_p = plist(wu)
+    wd_a, wd_p = plist(wd)
+    F = next(a.shape[0] for a in wg_a if a is not None) if any(a is not None for a in wg_a) else (
+        sg.shape[0])
+    n_shared = 0 if sg is None else 1
+    sg, su, sd = _c(sg), _c(su), _c(sd)
+    bias = _c(bias, np.float32)
+    dims = Dims(d, F, E, k, n_shared, dt)
+    out = np.zeros((T, d), np.float64)
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    counts = np.zeros((E,), np.int32)
+    rc = load(mutation).oracle_forward(
+        ctypes.byref(dims), _ptr(x), T, _ptr(wr), _ptr(bias),
+        ctypes.cast(wg_p, ctypes.c_void_p), ctypes.cast(wu_p, ctypes.c_void_p),
+        ctypes.cast(wd_p, ctypes.c_void_p), _ptr(sg), _ptr(su), _ptr(sd),
+        _ptr(out), _ptr(idx), _ptr(w), _ptr(counts), nthreads or _default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_forward failed: {rc}")
+    # keep the pointed-to arrays alive until here
+    del wg_a, wu_a, wd_a
+    return out, idx, w, counts

@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs for the MoE block.
+
+This module only draws random numbers.  It holds none of the block's arithmetic
+(no routing, no projections), so both the CUDA path and the CPU oracle may take
+their inputs from it.  Every tensor comes from one ``torch.Generator`` on the
+device the tensor is made on, seeded once per call, in a fixed order:
+
+    Wr, Sg, Su, Sd, Wg, Wu, Wd        (layer_weights)
+    x                                 (tokens)
+
+Distributions follow the workloads the block is measured on: activations
+x ~ N(0, 1); every projection ~ N(0, 1/fan_in), fan_in = d for the router and
+the gate/up projections, F for the down projections.  Values are drawn in the
+storage type directly (bfloat16 or float32).
+
+A torch generator on CUDA and one on the CPU give different streams for the same
+seed; a caller that needs the same values on both sides draws once and copies.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+_DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def _dt(dtype):
+    return _DTYPES[dtype] if isinstance(dtype, str) else dtype
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=torch.device(device))
+    g.manual_seed(int(seed))
+    return g
+
+
+def _normal(shape, std, g, dtype, device):
+    t = torch.empty(shape, dtype=dtype, device=device)
+    t.normal_(0.0, std, generator=g)
+    return t
+
+
+def layer_weights(seed: int, d: int, F: int, E: int, n_shared: int = 1, dtype="bf16",
+                  device="cpu") -> dict:
+    """One layer's weights in the library's layouts.
+
+    Wr [E][d]; Wg, Wu [E][F][d]; Wd [E][d][F]; Sg, Su [F][d]; Sd [d][F]
+    (shared tensors are None when n_shared == 0).
+    """
+    dtype = _dt(dtype)
+    g = _gen(seed, device)
+    sd_in, sd_ff = 1.0 / math.sqrt(d), 1.0 / math.sqrt(F)
+    w = {"Wr": _normal((E, d), sd_in, g, dtype, device)}
+    if n_shared:
+        w["Sg"] = _normal((F, d), sd_in, g, dtype, device)
+        w["Su"] = _normal((F, d), sd_in, g, dtype, device)
+        w["Sd"] = _normal((d, F), sd_ff, g, dtype, device)
+    else:
+        w["Sg"] = w["Su"] = w["Sd"] = None
+    w["Wg"] = _normal((E, F, d), sd_in, g, dtype, device)
+    w["Wu"] = _normal((E, F, d), sd_in, g, dtype, device)
+    w["Wd"] = _normal((E, d, F), sd_ff, g, dtype, device)
+    return w
+
+
+def tokens(seed: int, T: int, d: int, dtype="bf16", device="cpu") -> torch.Tensor:
+    """x ~ N(0, 1), [T][d]."""
+    return _normal((T, d), 1.0, _gen(seed, device), _dt(dtype), device)
+
+
+def fresh_rows(seed: int, attempt: int, n: int, d: int, dtype="bf16", device="cpu") -> torch.Tensor:
+    """n fresh N(0, 1) rows for re-drawing tokens; a distinct stream per (seed, attempt)."""
+    return _normal((n, d), 1.0, _gen(seed * 1000003 + 7919 * (attempt + 1), device), _dt(dtype),
+                   device)
+
+
+def zipf_bias(seed: int, E: int, s: float = 1.2) -> torch.Tensor:
+    """Skewed-routing router bias, float32 [E] (CPU).
+
+    A seeded random permutation pi of the experts ranks them; the expert of rank
+    r (1-based) gets the bias -s * ln(r), the logarithm of a Zipf(s) weight up to
+    a constant, so a few experts draw thousands of tokens and many draw none.
+    """
+    g = _gen(seed, "cpu")
+    perm = torch.randperm(E, generator=g)
+    ranks = torch.arange(1, E + 1, dtype=torch.float64)
+    b = torch.empty(E, dtype=torch.float64)
+    b[perm] = -s * torch.log(ranks)
+    return b.to(torch.float32)

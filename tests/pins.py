@@ -1,0 +1,207 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each ``pin_*`` takes ``mutation`` (0 = the oracle as committed; n > 0 = a build of
+moe_oracle.c with planted mistake n) and raises AssertionError when the oracle
+disagrees with what the mathematics fixes:
+
+* brute force: every expert on every token, masked by a top-k taken with
+  numpy's argsort (a different selection routine than the oracle's);
+* library routines: scipy's softmax, torch's silu and matmul in float64;
+* closed forms: two-expert routing weights are a logistic function of the
+  logit gap; hand-derived tiny blocks (tests/golden/hand_cases.json);
+* invariants: routing weights sum to 1, counts sum to T*k, token-permutation
+  equivariance.
+
+The block these pins fix is the one of "Optimizing on-device inference for
+Apple Silicon", section "Qwen creates three distinct workload shapes" (router
+over 256 experts picks 8, plus one shared expert) and section "Reduce
+intermediate traffic and dispatch traffic" (gated input projections, output
+projection scaled by the routing score, shared result added).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as Fnn
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng_case(seed, T, d, F, E, n_shared=1, dtype=np.float32):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    wr = (r.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+    wg = (r.standard_normal((E, F, d)) / math.sqrt(d)).astype(np.float32)
+    wu = (r.standard_normal((E, F, d)) / math.sqrt(d)).astype(np.float32)
+    wd = (r.standard_normal((E, d, F)) / math.sqrt(F)).astype(np.float32)
+    if n_shared:
+        sg = (r.standard_normal((F, d)) / math.sqrt(d)).astype(np.float32)
+        su = (r.standard_normal((F, d)) / math.sqrt(d)).astype(np.float32)
+        sd = (r.standard_normal((d, F)) / math.sqrt(F)).astype(np.float32)
+    else:
+        sg = su = sd = None
+    return dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, sg=sg, su=su, sd=sd)
+
+
+def _topk_numpy(logits32: np.ndarray, k: int) -> np.ndarray:
+    """Per-row indices of the k largest values, ties to the lower index (stable sort of -l)."""
+    order = np.argsort(-logits32.astype(np.float64), axis=1, kind="stable")
+    return order[:, :k]
+
+
+def pin_route_vs_numpy(mutation=0):
+    """Selection, weights and counts against numpy/scipy on random inputs."""
+    c = _rng_case(11, 48, 40, 8, 24, n_shared=0)
+    k = 5
+    idx, w, logits, counts = oracle.route(c["x"], c["wr"], k, nthreads=2, mutation=mutation)
+    ref_logits = (c["x"].astype(np.float64) @ c["wr"].astype(np.float64).T)
+    assert np.allclose(logits, ref_logits, rtol=1e-6, atol=1e-6)
+    ref_idx = _topk_numpy(ref_logits.astype(np.float32), k)
+    assert np.array_equal(np.sort(idx, 1), np.sort(ref_idx, 1)), "top-k sets"
+    assert np.array_equal(idx, ref_idx), "top-k order (descending logit)"
+    p = scipy.special.softmax(ref_logits.astype(np.float32).astype(np.float64), axis=1)
+    psel = np.take_along_axis(p, ref_idx, 1)
+    assert np.allclose(w, psel / psel.sum(1, keepdims=True), rtol=1e-9, atol=1e-12)
+    assert np.array_equal(counts, np.bincount(ref_idx.ravel(), minlength=24))
+
+
+def pin_full_softmax_when_k_equals_E(mutation=0):
+    """k = E: the weights are the plain softmax over all logits (scipy)."""
+    c = _rng_case(12, 16, 24, 4, 12, n_shared=0)
+    idx, w, logits, _ = oracle.route(c["x"], c["wr"], 12, nthreads=1, mutation=mutation)
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    assert np.allclose(w, np.take_along_axis(p, idx, 1), rtol=1e-12, atol=1e-15)
+    assert np.array_equal(np.sort(idx, 1), np.tile(np.arange(12), (16, 1)))
+
+
+def pin_weights_sum_and_ratio(mutation=0):
+    """Invariants: sum_j w = 1; w_i / w_j = exp(l_i - l_j) (softmax ratio)."""
+    c = _rng_case(13, 64, 32, 4, 32, n_shared=0)
+    idx, w, logits, counts = oracle.route(c["x"], c["wr"], 8, nthreads=2, mutation=mutation)
+    assert np.allclose(w.sum(1), 1.0, atol=1e-12)
+    l = np.take_along_axis(logits.astype(np.float64), idx, 1)
+    assert np.allclose(w[:, 1:] / w[:, :1], np.exp(l[:, 1:] - l[:, :1]), rtol=1e-10)
+    assert counts.sum() == 64 * 8
+    # every chosen logit beats every unchosen one
+    mask = np.zeros_like(logits, dtype=bool)
+    np.put_along_axis(mask, idx, True, 1)
+    assert (np.where(mask, logits, np.inf).min(1) >= np.where(mask, -np.inf, logits).max(1)).all()
+
+
+def pin_two_expert_logistic(mutation=0):
+    """Closed form: E = 2, k = 2, d = 1 -> w = logistic(+-(a - b)), ordered by logit."""
+    a, b = 0.75, -0.5
+    x = np.array([[1.0]], np.float32)
+    wr = np.array([[a], [b]], np.float32)
+    idx, w, _, counts = oracle.route(x, wr, 2, nthreads=1, mutation=mutation)
+    assert idx.tolist() == [[0, 1]]
+    s = 1.0 / (1.0 + math.exp(-(a - b)))
+    assert abs(w[0, 0] - s) < 1e-12 and abs(w[0, 1] - (1 - s)) < 1e-12
+    assert counts.tolist() == [1, 1]
+
+
+def pin_bf16_widening(mutation=0):
+    """bf16 bit patterns are widened exactly: 0x3F80 = 1, 0x4000 = 2, 0xC040 = -3."""
+    x = np.array([[0x3F80]], np.uint16)
+    wr = np.array([[0x4000], [0xC040]], np.uint16)
+    idx, w, logits, _ = oracle.route(x, wr, 1, nthreads=1, mutation=mutation)
+    assert logits.tolist() == [[2.0, -3.0]] and idx.tolist() == [[0]] and w.tolist() == [[1.0]]
+
+
+def pin_bias_enters_logits(mutation=0):
+    """A router bias is added to the logits before selection."""
+    c = _rng_case(14, 8, 16, 4, 8, n_shared=0)
+    bias = np.linspace(-3, 3, 8).astype(np.float32)
+    _, _, logits, _ = oracle.route(c["x"], c["wr"], 2, bias=bias, nthreads=1, mutation=mutation)
+    ref = c["x"].astype(np.float64) @ c["wr"].astype(np.float64).T + bias
+    assert np.allclose(logits, ref, rtol=1e-6, atol=1e-6)
+
+
+def _torch_swiglu(x, wg, wu, wd):
+    x, wg, wu, wd = (torch.from_numpy(np.asarray(a, np.float64)) for a in (x, wg, wu, wd))
+    return (Fnn.silu(x @ wg.T) * (x @ wu.T)) @ wd.T
+
+
+def pin_dense_swiglu(mutation=0):
+    """E = 1, k = 1, no shared expert: the block is a dense SwiGLU MLP (torch float64)."""
+    c = _rng_case(15, 12, 24, 20, 1, n_shared=0)
+    out, idx, w, counts = oracle.forward(c["x"], c["wr"], c["wg"], c["wu"], c["wd"], 1,
+                                         nthreads=2, mutation=mutation)
+    ref = _torch_swiglu(c["x"], c["wg"][0], c["wu"][0], c["wd"][0]).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    assert (idx == 0).all() and (w == 1.0).all() and counts.tolist() == [12]
+
+
+def pin_dense_plus_shared(mutation=0):
+    """E = 1, k = 1 with the shared expert: out = E_0(x) + S(x) (torch float64)."""
+    c = _rng_case(16, 10, 16, 12, 1, n_shared=1)
+    out, *_ = oracle.forward(c["x"], c["wr"], c["wg"], c["wu"], c["wd"], 1, sg=c["sg"],
+                             su=c["su"], sd=c["sd"], nthreads=2, mutation=mutation)
+    ref = (_torch_swiglu(c["x"], c["wg"][0], c["wu"][0], c["wd"][0])
+           + _torch_swiglu(c["x"], c["sg"], c["su"], c["sd"])).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_all_experts_masked(mutation=0):
+    """Brute force: evaluate every expert on every token, mask by numpy's top-k, weight by
+    scipy's softmax renormalised over the chosen, add the shared expert."""
+    E, k, T, d, F = 16, 4, 20, 32, 12
+    c = _rng_case(17, T, d, F, E, n_shared=1)
+    out, idx, w, counts = oracle.forward(c["x"], c["wr"], c["wg"], c["wu"], c["wd"], k,
+                                         sg=c["sg"], su=c["su"], sd=c["sd"], nthreads=2,
+                                         mutation=mutation)
+    x64 = c["x"].astype(np.float64)
+    logits = (x64 @ c["wr"].astype(np.float64).T).astype(np.float32)
+    top = _topk_numpy(logits, k)
+    mask = np.zeros((T, E))
+    np.put_along_axis(mask, top, 1.0, 1)
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1) * mask
+    p /= p.sum(1, keepdims=True)
+    g = np.einsum("td,efd->tef", x64, c["wg"].astype(np.float64))
+    u = np.einsum("td,efd->tef", x64, c["wu"].astype(np.float64))
+    h = g * scipy.special.expit(g) * u
+    y = np.einsum("tef,edf->ted", h, c["wd"].astype(np.float64))
+    ref = np.einsum("te,ted->td", p, y) + _torch_swiglu(c["x"], c["sg"], c["su"], c["sd"]).numpy()
+    assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
+    assert np.array_equal(counts, np.bincount(top.ravel(), minlength=E))
+
+
+def pin_permutation_equivariance(mutation=0):
+    """Tokens are independent: out(P x) == P out(x) bit for bit."""
+    c = _rng_case(18, 24, 32, 8, 16, n_shared=1)
+    perm = np.random.default_rng(5).permutation(24)
+    args = (c["wr"], c["wg"], c["wu"], c["wd"], 4)
+    kw = dict(sg=c["sg"], su=c["su"], sd=c["sd"], nthreads=3, mutation=mutation)
+    out, idx, w, counts = oracle.forward(c["x"], *args, **kw)
+    out_p, idx_p, w_p, counts_p = oracle.forward(c["x"][perm], *args, **kw)
+    assert np.array_equal(out_p, out[perm]) and np.array_equal(idx_p, idx[perm])
+    assert np.array_equal(w_p, w[perm]) and np.array_equal(counts_p, counts)
+
+
+def pin_hand_cases(mutation=0):
+    """Hand-derived tiny blocks with closed-form outputs (tests/golden/hand_cases.json)."""
+    with open(os.path.join(GOLDEN, "hand_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        a = {k: (None if v is None else np.array(v, np.float32)) for k, v in case["inputs"].items()}
+        out, idx, w, counts = oracle.forward(a["x"], a["wr"], a["wg"], a["wu"], a["wd"],
+                                             case["k"], sg=a.get("sg"), su=a.get("su"),
+                                             sd=a.get("sd"), nthreads=1, mutation=mutation)
+        exp = case["expected"]
+        assert idx.tolist() == exp["idx"], case["name"]
+        assert np.allclose(w, np.array(exp["w"]), rtol=0, atol=1e-12), case["name"]
+        assert np.allclose(out, np.array(exp["out"]), rtol=0, atol=1e-12), case["name"]
+        assert counts.tolist() == exp["counts"], case["name"]
+
+
+ALL_PINS = [pin_route_vs_numpy, pin_full_softmax_when_k_equals_E, pin_weights_sum_and_ratio,
+            pin_two_expert_logistic, pin_bf16_widening, pin_bias_enters_logits, pin_dense_swiglu,
+            pin_dense_plus_shared, pin_all_experts_masked, pin_permutation_equivariance,
+            pin_hand_cases]

@@ -1,0 +1,29 @@
+"""Each planted mistake in the oracle (a dropped term, a wrong sign, a transposed
+operand, a wrong selection, a missing renormalisation, a wrong histogram) must
+fail at least one pin; this is what makes the pins worth trusting.  Mutations are
+compiled from oracle/moe_oracle.c with -DORACLE_MUTATION=n, on the CPU."""
+import pytest
+
+import pins
+
+MUTATIONS = {
+    1: "shared expert dropped",
+    2: "silu sign flipped",
+    3: "down projection transposed",
+    4: "no renormalisation over the chosen experts",
+    5: "smallest logits selected",
+    6: "router weight transposed",
+    7: "gated activation dropped",
+    8: "histogram counts first choice only",
+}
+
+
+@pytest.mark.parametrize("m", sorted(MUTATIONS), ids=lambda m: f"m{m}")
+def test_mutation_is_caught(m):
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(m)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutation {m} ({MUTATIONS[m]}) passed every pin"

@@ -1,0 +1,9 @@
+"""The CPU oracle against what the mathematics fixes (see tests/pins.py)."""
+import pytest
+
+import pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin(0)
