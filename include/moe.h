@@ -1,0 +1,175 @@
+/*
+ * moe.h -- C ABI of the sparse Mixture-of-Experts feed-forward block on one
+ * GB300 GPU (sm_103a).
+ *
+ * The block (from "Optimizing on-device inference for Apple Silicon",
+ * Perplexity, 2026):
+ *   section "Qwen creates three distinct workload shapes": a router scores E
+ *   experts for each token and keeps the best k; one shared expert processes
+ *   every token; experts therefore receive uneven numbers of tokens.
+ *   section "Reduce intermediate traffic and dispatch traffic": each expert is
+ *   two input projections with a gated activation followed by an output
+ *   projection, scaled by the routing score and summed with the shared
+ *   expert's result.
+ * For token x (a row of d values):
+ *   l_e   = Wr[e] . x + b_e                            (e < E)
+ *   S     = indices of the k largest l_e (ties: lower index first)
+ *   w_e   = exp(l_e) / sum_{e' in S} exp(l_e')         (= softmax over all E,
+ *                                                        renormalised over S)
+ *   E_e(x)= Wd[e] (silu(Wg[e] x) * (Wu[e] x)),  silu(z) = z / (1 + exp(-z))
+ *   out   = sum_{e in S} w_e E_e(x) + Sd (silu(Sg x) * (Su x))
+ *
+ * Every pointer named "device" below must be a CUDA device pointer on the
+ * device that was current when moe_create ran; "host" pointers are ordinary
+ * host memory.  All matrices are row-major and contiguous.  Element type of x,
+ * out and every weight is the handle's dtype (bfloat16 or float32); the
+ * router bias is always float32.
+ *
+ * Errors: every function returns MOE_OK (0) or a negative MOE_ERR_* code and
+ * leaves its outputs unspecified on error.  Device-side failures (a bounded
+ * wait that ran out, an index out of range) cannot be returned by an
+ * asynchronous call; they are recorded in a status word on the device and
+ * returned by moe_status.  No call ever traps or asserts on the device.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)    /* null pointer, negative size, bad field */
+#define MOE_ERR_ALIGNMENT (-2)      /* a pointer or row pitch is not 16-byte aligned */
+#define MOE_ERR_UNSUPPORTED (-3)    /* dimensions outside what the kernels are built for */
+#define MOE_ERR_CUDA (-4)           /* a CUDA runtime call failed */
+#define MOE_ERR_DEVICE_TIMEOUT (-5) /* a bounded device wait ran out (from moe_status) */
+#define MOE_ERR_DEVICE_BOUNDS (-6)  /* a device index check failed (from moe_status) */
+#define MOE_ERR_OUT_OF_MEMORY (-7)  /* workspace allocation failed in moe_create */
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
+
+typedef struct moe_handle moe_handle; /* opaque, owned by the library */
+
+/*
+ * Shapes and weights of one MoE layer.  Supported: d_model a multiple of 64 in
+ * [64, 16384]; d_ff a multiple of 128 in [128, 4096]; n_experts in [1, 256];
+ * top_k in [1, min(n_experts, 16)]; n_shared 0 or 1; max_tokens in
+ * [1, 65536].  The prefill kernels of the bf16 path additionally need
+ * n_experts <= 256 (the router tile holds all logits of a token).
+ *
+ * Weight layouts (all K-contiguous, i.e. the reduction index is innermost):
+ *   w_router [E][d]          (the transpose of the mathematical x.Wr shape)
+ *   w_gate   [E][F][d]       w_up [E][F][d]        w_down [E][d][F]
+ *   s_gate   [F][d]          s_up [F][d]           s_down [d][F]
+ *   router_bias [E] float32, or NULL for no bias
+ * The caller owns the weights; the library keeps the pointers (it copies
+ * nothing) so they must stay valid and unchanged until moe_destroy.
+ */
+typedef struct {
+  int d_model;    /* d */
+  int n_experts;  /* E */
+  int top_k;      /* k */
+  int d_ff;       /* F, intermediate width of every expert, shared one included */
+  int n_shared;   /* 0 or 1 */
+  int max_tokens; /* tokens per internal chunk; moe_forward splits longer inputs */
+  moe_dtype dtype;
+  const void *w_router;      /* device */
+  const void *w_gate;        /* device */
+  const void *w_up;          /* device */
+  const void *w_down;        /* device */
+  const void *s_gate;        /* device, NULL iff n_shared == 0 */
+  const void *s_up;          /* device, NULL iff n_shared == 0 */
+  const void *s_down;        /* device, NULL iff n_shared == 0 */
+  const float *router_bias;  /* device, may be NULL */
+} moe_config;
+
+/*
+ * Validate cfg, build the TMA descriptors for the weights and allocate the
+ * device workspace sized for cfg->max_tokens tokens.  This is the only call
+ * that allocates.  On success *out receives the handle.
+ * Errors: INVALID_ARG, ALIGNMENT (weight pointers must be 16-byte aligned),
+ * UNSUPPORTED, OUT_OF_MEMORY, CUDA.
+ */
+int moe_create(const moe_config *cfg, moe_handle **out);
+
+/*
+ * Routing only (the router and the routing half of the block): for T tokens
+ * x[T][d] (device) writes, all device:
+ *   topk_idx[T][k] int32   chosen experts of each token, by descending logit,
+ *                          ties to the lower index;
+ *   topk_w[T][k]   float32 their routing weights (sum to 1 per token);
+ *   counts[E]      int32   number of tokens that chose each expert.
+ * Sections "Qwen creates three distinct workload shapes" and "Keep expert
+ * routing on the GPU" (histogram of assignments per expert).
+ * Requires 1 <= T <= max_tokens (T == 0 is a no-op returning MOE_OK).
+ * cuda_stream is a cudaStream_t (NULL = legacy default stream).  Asynchronous:
+ * no host synchronisation, no allocation.
+ */
+int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *topk_w,
+              int32_t *counts, void *cuda_stream);
+
+/*
+ * The whole block: out[T][d] = MoE(x[T][d]), both device, same dtype.  T == 1
+ * takes the batch-1 decode kernels (section "Optimise the single-row weight
+ * path"); T >= 2 takes the prefill kernels (section "Prefill: reuse weights and
+ * keep routing on the GPU"), in chunks of at most max_tokens tokens (section
+ * "Bound temporary memory with request chunking"; tokens are independent so
+ * chunking does not change the result).  x and out must not overlap.
+ * Asynchronous on cuda_stream: no host synchronisation, no allocation, no
+ * device-to-host copy.  T == 0 is a no-op returning MOE_OK.
+ */
+int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream);
+
+/*
+ * Synchronise cuda_stream, then return and clear the handle's device status
+ * word: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  If
+ * detail != NULL it receives a library-defined code naming the kernel and the
+ * wait or check that failed (0 when none).
+ */
+int moe_status(moe_handle *h, void *cuda_stream, int *detail);
+
+/* Free the workspace and the handle.  NULL is accepted.  The caller must make
+ * sure no work using the handle is still running. */
+int moe_destroy(moe_handle *h);
+
+/* Static string describing an error code. */
+const char *moe_strerror(int code);
+
+/*
+ * Per-kernel timing with CUDA events recorded on the launching stream around
+ * every kernel the handle launches.  moe_profile(h, 1) resets the totals and
+ * starts recording, moe_profile(h, 0) stops.  moe_profile_read synchronises
+ * the last recorded event and writes, for kernel kind i < n (see
+ * MOE_KERNEL_*), the summed milliseconds to ms[i] and the number of launches
+ * to launches[i] (either pointer may be NULL).  Kinds that have not run read 0.
+ */
+#define MOE_KERNEL_ROUTER 0
+#define MOE_KERNEL_PERMUTE 1
+#define MOE_KERNEL_GEMM_GATE_UP 2
+#define MOE_KERNEL_GEMM_DOWN 3
+#define MOE_KERNEL_COMBINE 4
+#define MOE_KERNEL_DECODE_ROUTER 5
+#define MOE_KERNEL_DECODE_GATE_UP 6
+#define MOE_KERNEL_DECODE_DOWN 7
+#define MOE_KERNEL_KINDS 8
+int moe_profile(moe_handle *h, int enable);
+int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n);
+
+/*
+ * Test hook for the device failure path: launch one small kernel on
+ * cuda_stream that waits, with the same bounded wait the GEMM kernels use, on
+ * a barrier nothing will ever signal, giving up after about wait_us
+ * microseconds (1 <= wait_us <= 2000000).  The kernel then records
+ * MOE_ERR_DEVICE_TIMEOUT in the handle's status word and returns; the context
+ * stays usable.  Read the result with moe_status.
+ */
+int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

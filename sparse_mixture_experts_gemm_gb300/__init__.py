@@ -1,0 +1,229 @@
+"""Sparse Mixture-of-Experts feed-forward block on one GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/moe.h``: the functions below carry
+the C names and only marshal arguments (torch tensors -> device pointers,
+torch streams -> cudaStream_t).  Every step of the block runs in the CUDA
+kernels of ``libmoe.so``; if that library is not built this module raises
+instead of computing anything another way.
+
+The block ("Optimizing on-device inference for Apple Silicon", sections "Qwen
+creates three distinct workload shapes" and "Reduce intermediate traffic and
+dispatch traffic"): a router picks top-k of E experts per token, each expert is
+a SwiGLU MLP, the chosen experts' outputs are weighted by the renormalised
+routing probabilities and a shared expert's output is added.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_ALIGNMENT = -2
+MOE_ERR_UNSUPPORTED = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_DEVICE_TIMEOUT = -5
+MOE_ERR_DEVICE_BOUNDS = -6
+MOE_ERR_OUT_OF_MEMORY = -7
+
+MOE_BF16 = 0
+MOE_F32 = 1
+
+KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
+                "decode_gate_up", "decode_down"]
+
+EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_status", "moe_destroy",
+            "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("d_ff", ctypes.c_int), ("n_shared", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("dtype", ctypes.c_int),
+                ("w_router", ctypes.c_void_p), ("w_gate", ctypes.c_void_p),
+                ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
+                ("s_down", ctypes.c_void_p), ("router_bias", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libmoe.so in-tree (nvcc, sm_103a)."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m sparse_mixture_experts_gemm_gb300.buildlib`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(vp)]
+    L.moe_route.argtypes = [vp, vp, ip, vp, vp, vp, vp]
+    L.moe_forward.argtypes = [vp, vp, ip, vp, vp]
+    L.moe_status.argtypes = [vp, vp, ctypes.POINTER(ip)]
+    L.moe_destroy.argtypes = [vp]
+    L.moe_strerror.argtypes = [ip]
+    L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_profile.argtypes = [vp, ip]
+    L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
+                                   ctypes.POINTER(ctypes.c_int64), ip]
+    L.moe_debug_wait_timeout.argtypes = [vp, ip, vp]
+    for name in EXPORTED:
+        if name != "moe_strerror":
+            getattr(L, name).restype = ip
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().moe_strerror(code).decode()
+    except RuntimeError:
+        return f"error {code}"
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+    return rc
+
+
+# ----------------------------------------------------------------- C names
+def moe_create(cfg: moe_config) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().moe_create(ctypes.byref(cfg), ctypes.byref(h)), "moe_create")
+    return h.value
+
+
+def moe_route(h: int, x, T: int, topk_idx, topk_w, counts, stream=None) -> int:
+    return _check(lib().moe_route(h, _ptr(x), T, _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                  _stream(stream)), "moe_route")
+
+
+def moe_forward(h: int, x, T: int, out, stream=None) -> int:
+    return _check(lib().moe_forward(h, _ptr(x), T, _ptr(out), _stream(stream)), "moe_forward")
+
+
+def moe_status(h: int, stream=None) -> tuple[int, int]:
+    """(code, detail) of the device status word; synchronises the stream."""
+    detail = ctypes.c_int(0)
+    rc = lib().moe_status(h, _stream(stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+def moe_destroy(h: int) -> int:
+    return _check(lib().moe_destroy(h), "moe_destroy")
+
+
+def moe_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def moe_profile(h: int, enable: bool) -> int:
+    return _check(lib().moe_profile(h, 1 if enable else 0), "moe_profile")
+
+
+def moe_profile_read(h: int) -> dict:
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(lib().moe_profile_read(h, ms, cnt, n), "moe_profile_read")
+    return {name: (ms[i], cnt[i]) for i, name in enumerate(KERNEL_KINDS)}
+
+
+def moe_debug_wait_timeout(h: int, wait_us: int, stream=None) -> int:
+    return _check(lib().moe_debug_wait_timeout(h, wait_us, _stream(stream)),
+                  "moe_debug_wait_timeout")
+
+
+# ----------------------------------------------------------------- wrapper
+class MoELayer:
+    """One layer: owns the handle, keeps the caller's weight tensors alive.
+
+    weights: dict with Wr [E][d], Wg/Wu [E][F][d], Wd [E][d][F], Sg/Su [F][d],
+    Sd [d][F] (shared ones may be None), all on one CUDA device, bf16 or f32;
+    bias: float32 [E] on the device, or None.
+    """
+
+    def __init__(self, weights: dict, top_k: int, max_tokens: int, bias=None):
+        import torch
+        Wr, Wg, Wd = weights["Wr"], weights["Wg"], weights["Wd"]
+        E, d = Wr.shape
+        F = Wg.shape[1]
+        dt = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}[Wr.dtype]
+        shared = weights.get("Sg") is not None
+        self.weights = weights
+        self.bias = bias
+        self.dtype = Wr.dtype
+        self.d, self.E, self.F, self.k = d, E, F, top_k
+        cfg = moe_config(d, E, top_k, F, 1 if shared else 0, max_tokens, dt,
+                         _ptr(Wr), _ptr(Wg), _ptr(weights["Wu"]), _ptr(Wd),
+                         _ptr(weights.get("Sg")), _ptr(weights.get("Su")),
+                         _ptr(weights.get("Sd")), _ptr(bias))
+        self.cfg = cfg
+        self.handle = moe_create(cfg)
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.d), dtype=self.dtype, device=x.device)
+        moe_forward(self.handle, x, T, out, stream)
+        return out
+
+    def route(self, x, stream=None):
+        import torch
+        T = x.shape[0]
+        idx = torch.empty((T, self.k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, self.k), dtype=torch.float32, device=x.device)
+        counts = torch.empty((self.E,), dtype=torch.int32, device=x.device)
+        moe_route(self.handle, x, T, idx, w, counts, stream)
+        return idx, w, counts
+
+    def status(self, stream=None):
+        return moe_status(self.handle, stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

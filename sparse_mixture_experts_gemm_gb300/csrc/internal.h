@@ -1,0 +1,100 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// One output tile of a grouped GEMM: 128 rows x N columns of one group.
+// Groups 0..E-1 are routed experts; group E is the shared expert.
+struct GemmTile {
+  int group;    // expert id, E for the shared expert
+  int a_row;    // first row of the A operand (row of Xp, x or H)
+  int out_row;  // first output row (row of H or Yp)
+  int rows;     // valid rows, 1..128
+  int n0;       // first output column; also the row offset inside the group's B
+  int pad[3];
+};
+static_assert(sizeof(GemmTile) == 32, "tile record is 32 bytes");
+
+enum Epilogue { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_ROUTER = 2 };
+
+constexpr int kBM = 128;      // rows per tile (TMEM lanes)
+constexpr int kBN = 256;      // MMA N: B rows per tile
+constexpr int kStages = 4;    // smem pipeline depth
+constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGemmSmem = kStages * (kBM * 128 + kBN * 128) + 1024 + 1024;
+constexpr int kMaxTopK = 8;
+
+struct GemmParams {
+  const GemmTile *tiles;  // device tile list (null for the router)
+  const int *ntiles_dev;  // device tile count (null for the router)
+  int ntiles_host;        // router: number of 128-token tiles
+  int num_k_blocks;       // K / (128 bytes / element size)
+  int n_routed;           // E
+  int b_rows_per_group;   // rows of one routed group's B matrix (F or d)
+  void *out;              // H (gate/up) or Yp (down)
+  long long ldo;          // elements per output row
+  int *status;            // device status word
+  int kid;                // KernelId for failure details
+  // router epilogue
+  int T, k, E;
+  const float *bias;
+  int32_t *idx;
+  float *w;
+  int32_t *blkcnt;  // [ceil(T/128)][E], zeroed before the launch
+};
+
+// Tensor maps: A routed, A shared, B0 routed, B1 routed, B0 shared, B1 shared.
+struct GemmMaps {
+  CUtensorMap m[6];
+};
+
+// gemm.cu
+template <typename T, int EPI>
+cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
+template <typename T, int EPI>
+cudaError_t gemm_set_smem_attr();
+cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
+
+// route.cu
+template <typename T>
+cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T_tok, int d, int E,
+                               int k, int32_t *idx, float *w, int32_t *blkcnt, int *status,
+                               cudaStream_t st);
+cudaError_t launch_permute(const int32_t *idx, const int32_t *blkcnt, int T_tok, int k, int E,
+                           int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
+                           GemmTile *tiles1, GemmTile *tiles2, int *ntiles, int nt1, int nt2,
+                           int n_shared, int build_tiles, int *status, cudaStream_t st);
+template <typename T>
+cudaError_t launch_gather(const T *x, const int32_t *perm, T *xp, int A, int d, int T_tok,
+                          int *status, cudaStream_t st);
+template <typename T>
+cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
+                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);
+
+// decode.cu
+struct DecodeArgs {
+  const void *x;
+  const void *wr, *wg, *wu, *wd, *sg, *su, *sd;
+  const float *bias;
+  int d, F, E, k, n_shared;
+  float *logits;       // [E]
+  int32_t *sel;        // [k]
+  float *selw;         // [k]
+  float *h;            // [(k + 1)][F]
+  unsigned *counter;   // last-block-done ticket, zero between launches
+  void *out;           // [d]
+  int *status;
+};
+template <typename T>
+cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
+template <typename T>
+cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t st, bool pdl);
+template <typename T>
+cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl);
+template <typename T>
+cudaError_t decode_set_smem_attr(int bytes);
+
+}  // namespace moe

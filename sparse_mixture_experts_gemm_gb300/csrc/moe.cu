@@ -1,0 +1,553 @@
+// moe.cu -- host side of the C ABI declared in include/moe.h: argument
+// validation, the one workspace allocation, TMA descriptors, and the kernel
+// sequence of the prefill and decode paths.
+//
+// Prefill, per chunk of at most max_tokens tokens ("Optimizing on-device
+// inference for Apple Silicon", section "Bound temporary memory with request
+// chunking"), all on the caller's stream with no host synchronisation
+// (section "Keep expert routing on the GPU"):
+//   router (tcgen05 for bf16, SIMT for fp32) -> permute -> gather ->
+//   grouped gate/up GEMM + SiLU -> grouped down GEMM -> combine.
+// Decode (T == 1, section "Optimise the single-row weight path"):
+//   decode_router -> decode_gateup -> decode_down, chained with programmatic
+//   dependent launch.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "internal.h"
+#include "status.h"
+
+using namespace moe;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D map over a row-major [rows][cols] matrix; box = 128 bytes of columns x
+// box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct moe_handle {
+  moe_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  size_t esz = 2;
+  int nt1 = 0, nt2 = 0;  // N tiles of the gate/up and down GEMMs
+  // workspace (one allocation)
+  void *ws = nullptr;
+  int32_t *idx = nullptr, *inv = nullptr, *perm = nullptr, *counts = nullptr, *offsets = nullptr,
+          *blkcnt = nullptr, *ntiles = nullptr, *status = nullptr, *sel = nullptr;
+  float *w = nullptr, *logits = nullptr, *selw = nullptr, *hdec = nullptr;
+  unsigned *counter = nullptr;
+  void *xp = nullptr, *hbuf = nullptr, *yp = nullptr;
+  GemmTile *tiles1 = nullptr, *tiles2 = nullptr;
+  // static tensor maps
+  CUtensorMap tm_xp, tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
+  // profiling
+  bool prof = false;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_used = 0;
+};
+
+namespace {
+
+int check_cfg(const moe_config *c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0 ||
+      c->max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (!c->w_router || !c->w_gate || !c->w_up || !c->w_down) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared && (!c->s_gate || !c->s_up || !c->s_down)) return MOE_ERR_INVALID_ARG;
+  if (c->d_model % 256 != 0 || c->d_model > 16384) return MOE_ERR_UNSUPPORTED;
+  if (c->d_ff % 128 != 0 || c->d_ff > 4096) return MOE_ERR_UNSUPPORTED;
+  if (c->n_experts > 256 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens > 65536) return MOE_ERR_UNSUPPORTED;
+  const void *ptrs[] = {c->w_router, c->w_gate, c->w_up, c->w_down,
+                        c->s_gate,   c->s_up,   c->s_down, c->router_bias};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+cudaEvent_t prof_event(moe_handle *h) {
+  if (h->pool_used == h->pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->pool.push_back(e);
+  }
+  return h->pool[h->pool_used++];
+}
+
+// Records an event pair around one launch when profiling is on.
+struct ProfScope {
+  moe_handle *h;
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t b = nullptr;
+  ProfScope(moe_handle *h_, int kind_, cudaStream_t st_) : h(h_), kind(kind_), st(st_) {
+    if (h->prof) {
+      b = prof_event(h);
+      if (b) cudaEventRecord(b, st);
+    }
+  }
+  ~ProfScope() {
+    if (h->prof && b) {
+      cudaEvent_t e = prof_event(h);
+      if (e) {
+        cudaEventRecord(e, st);
+        h->recs.push_back({kind, b, e});
+      }
+    }
+  }
+};
+
+#define MOE_TRY(expr)                             \
+  do {                                            \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+template <typename T>
+int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st) {
+  const moe_config &c = h->cfg;
+  const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k;
+  const int nblk = (Tc + kBM - 1) / kBM;
+  const int A = Tc * k;
+  const int BK = static_cast<int>(128 / sizeof(T));
+
+  CUtensorMap tm_x;
+  if (!make_map(&tm_x, x, sizeof(T), Tc, d, kBM)) return MOE_ERR_CUDA;
+
+  MOE_TRY(cudaMemsetAsync(h->blkcnt, 0, sizeof(int32_t) * nblk * E, st));
+  {
+    ProfScope ps(h, MOE_KERNEL_ROUTER, st);
+    if (sizeof(T) == 2) {
+      GemmMaps m;
+      m.m[0] = m.m[1] = tm_x;
+      m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
+      GemmParams p = {};
+      p.ntiles_host = nblk;
+      p.num_k_blocks = d / BK;
+      p.n_routed = E;
+      p.status = h->status;
+      p.kid = KID_ROUTER;
+      p.T = Tc;
+      p.k = k;
+      p.E = E;
+      p.bias = c.router_bias;
+      p.idx = h->idx;
+      p.w = h->w;
+      p.blkcnt = h->blkcnt;
+      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms, st)));
+    } else {
+      MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
+                                    k, h->idx, h->w, h->blkcnt, h->status, st));
+    }
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
+    MOE_TRY(launch_permute(h->idx, h->blkcnt, Tc, k, E, h->counts, h->offsets, h->perm, h->inv,
+                           h->tiles1, h->tiles2, h->ntiles, h->nt1, h->nt2, c.n_shared, 1, h->status,
+                           st));
+    MOE_TRY(launch_gather<T>(x, h->perm, static_cast<T *>(h->xp), A, d, Tc, h->status, st));
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
+    GemmMaps m;
+    m.m[0] = h->tm_xp;
+    m.m[1] = tm_x;
+    m.m[2] = h->tm_wg;
+    m.m[3] = h->tm_wu;
+    m.m[4] = c.n_shared ? h->tm_sg : h->tm_wg;
+    m.m[5] = c.n_shared ? h->tm_su : h->tm_wu;
+    GemmParams p = {};
+    p.tiles = h->tiles1;
+    p.ntiles_dev = h->ntiles;
+    p.num_k_blocks = d / BK;
+    p.n_routed = E;
+    p.b_rows_per_group = F;
+    p.out = h->hbuf;
+    p.ldo = F;
+    p.status = h->status;
+    p.kid = KID_GEMM_GATE_UP;
+    MOE_TRY((launch_gemm<T, EPI_SWIGLU>(m, p, h->num_sms, st)));
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
+    GemmMaps m;
+    m.m[0] = m.m[1] = h->tm_h;
+    m.m[2] = m.m[3] = h->tm_wd;
+    m.m[4] = m.m[5] = c.n_shared ? h->tm_sd : h->tm_wd;
+    GemmParams p = {};
+    p.tiles = h->tiles2;
+    p.ntiles_dev = h->ntiles + 1;
+    p.num_k_blocks = F / BK;
+    p.n_routed = E;
+    p.b_rows_per_group = d;
+    p.out = h->yp;
+    p.ldo = d;
+    p.status = h->status;
+    p.kid = KID_GEMM_DOWN;
+    MOE_TRY((launch_gemm<T, EPI_STORE>(m, p, h->num_sms, st)));
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_COMBINE, st);
+    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
+                              c.n_shared, h->status, st));
+  }
+  return MOE_OK;
+}
+
+template <typename T>
+int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
+  const moe_config &c = h->cfg;
+  DecodeArgs a;
+  a.x = x;
+  a.wr = c.w_router;
+  a.wg = c.w_gate;
+  a.wu = c.w_up;
+  a.wd = c.w_down;
+  a.sg = c.s_gate;
+  a.su = c.s_up;
+  a.sd = c.s_down;
+  a.bias = c.router_bias;
+  a.d = c.d_model;
+  a.F = c.d_ff;
+  a.E = c.n_experts;
+  a.k = c.top_k;
+  a.n_shared = c.n_shared;
+  a.logits = h->logits;
+  a.sel = h->sel;
+  a.selw = h->selw;
+  a.h = h->hdec;
+  a.counter = h->counter;
+  a.out = out;
+  a.status = h->status;
+  const bool pdl = !h->prof;  // event records between kernels would break the chain
+  {
+    ProfScope ps(h, MOE_KERNEL_DECODE_ROUTER, st);
+    MOE_TRY(launch_decode_router<T>(a, st, pdl));
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_DECODE_GATE_UP, st);
+    MOE_TRY(launch_decode_gateup<T>(a, st, pdl));
+  }
+  {
+    ProfScope ps(h, MOE_KERNEL_DECODE_DOWN, st);
+    MOE_TRY(launch_decode_down<T>(a, st, pdl));
+  }
+  return MOE_OK;
+}
+
+template <typename T>
+int set_attrs(const moe_config &c) {
+  if (gemm_set_smem_attr<T, EPI_SWIGLU>() != cudaSuccess) return MOE_ERR_CUDA;
+  if (gemm_set_smem_attr<T, EPI_STORE>() != cudaSuccess) return MOE_ERR_CUDA;
+  const int dec_smem = static_cast<int>(sizeof(float)) * (c.top_k + c.n_shared) * c.d_ff;
+  if (decode_set_smem_attr<T>(dec_smem) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_ALIGNMENT: return "pointer or pitch not 16-byte aligned";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case MOE_ERR_DEVICE_BOUNDS: return "a device index check failed";
+    case MOE_ERR_OUT_OF_MEMORY: return "workspace allocation failed";
+    default: return "unknown error";
+  }
+}
+
+int moe_create(const moe_config *cfg, moe_handle **out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  moe_handle *h = new (std::nothrow) moe_handle();
+  if (!h) return MOE_ERR_OUT_OF_MEMORY;
+  h->cfg = *cfg;
+  const moe_config &c = h->cfg;
+  h->esz = c.dtype == MOE_BF16 ? 2 : 4;
+  h->nt1 = c.d_ff / kBM;
+  h->nt2 = c.d_model / kBN;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+          cudaSuccess) {
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k, Tm = c.max_tokens;
+  const size_t A = static_cast<size_t>(Tm) * k;
+  const size_t nblk = (Tm + kBM - 1) / kBM;
+  const size_t max_mt = A / kBM + E + 1 + nblk;
+  const size_t esz = h->esz;
+
+  // carve the workspace
+  struct Part {
+    void **dst;
+    size_t bytes;
+  };
+  std::vector<Part> parts = {
+      {reinterpret_cast<void **>(&h->idx), sizeof(int32_t) * A},
+      {reinterpret_cast<void **>(&h->w), sizeof(float) * A},
+      {reinterpret_cast<void **>(&h->inv), sizeof(int32_t) * A},
+      {reinterpret_cast<void **>(&h->perm), sizeof(int32_t) * A},
+      {reinterpret_cast<void **>(&h->counts), sizeof(int32_t) * E},
+      {reinterpret_cast<void **>(&h->offsets), sizeof(int32_t) * (E + 1)},
+      {reinterpret_cast<void **>(&h->blkcnt), sizeof(int32_t) * nblk * E},
+      {reinterpret_cast<void **>(&h->ntiles), sizeof(int32_t) * 4},
+      {reinterpret_cast<void **>(&h->status), sizeof(int32_t) * 4},
+      {reinterpret_cast<void **>(&h->sel), sizeof(int32_t) * kMaxTopK},
+      {reinterpret_cast<void **>(&h->selw), sizeof(float) * kMaxTopK},
+      {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
+      {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
+      {reinterpret_cast<void **>(&h->counter), sizeof(unsigned) * 4},
+      {reinterpret_cast<void **>(&h->tiles1), sizeof(GemmTile) * h->nt1 * max_mt},
+      {reinterpret_cast<void **>(&h->tiles2), sizeof(GemmTile) * h->nt2 * max_mt},
+      {&h->xp, esz * A * d},
+      {&h->hbuf, esz * (A + Tm) * F},
+      {&h->yp, esz * (A + Tm) * d},
+  };
+  size_t total = 0;
+  for (auto &p : parts) total = align_up(total, 1024) + p.bytes;
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_OUT_OF_MEMORY;
+  }
+  size_t off = 0;
+  for (auto &p : parts) {
+    off = align_up(off, 1024);
+    *p.dst = static_cast<char *>(h->ws) + off;
+    off += p.bytes;
+  }
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
+    moe_destroy(h);
+    return MOE_ERR_CUDA;
+  }
+
+  // tensor maps of the weights and the fixed workspace buffers
+  bool ok = make_map(&h->tm_xp, h->xp, esz, A, d, kBM) &&
+            make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
+            make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
+            make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
+            make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN) &&
+            make_map(&h->tm_wr, c.w_router, esz, E, d, kBN);
+  if (ok && c.n_shared)
+    ok = make_map(&h->tm_sg, c.s_gate, esz, F, d, kBM) &&
+         make_map(&h->tm_su, c.s_up, esz, F, d, kBM) && make_map(&h->tm_sd, c.s_down, esz, d, F, kBN);
+  if (!ok) {
+    moe_destroy(h);
+    return MOE_ERR_CUDA;
+  }
+  rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
+  if (rc == MOE_OK && c.dtype == MOE_BF16 &&
+      gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER>() != cudaSuccess)
+    rc = MOE_ERR_CUDA;
+  if (rc != MOE_OK) {
+    moe_destroy(h);
+    return rc;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_destroy(moe_handle *h) {
+  if (!h) return MOE_OK;
+  for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
+  int rc = MOE_OK;
+  if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = MOE_ERR_CUDA;
+  delete h;
+  return rc;
+}
+
+int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *topk_w,
+              int32_t *counts, void *cuda_stream) {
+  if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !topk_idx || !topk_w || !counts) return MOE_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const moe_config &c = h->cfg;
+  const int d = c.d_model, E = c.n_experts, k = c.top_k;
+  const int nblk = (T + kBM - 1) / kBM;
+  MOE_TRY(cudaMemsetAsync(h->blkcnt, 0, sizeof(int32_t) * nblk * E, st));
+  {
+    ProfScope ps(h, MOE_KERNEL_ROUTER, st);
+    if (c.dtype == MOE_BF16) {
+      CUtensorMap tm_x;
+      if (!make_map(&tm_x, x, 2, T, d, kBM)) return MOE_ERR_CUDA;
+      GemmMaps m;
+      m.m[0] = m.m[1] = tm_x;
+      m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
+      GemmParams p = {};
+      p.ntiles_host = nblk;
+      p.num_k_blocks = d / 64;
+      p.n_routed = E;
+      p.status = h->status;
+      p.kid = KID_ROUTER;
+      p.T = T;
+      p.k = k;
+      p.E = E;
+      p.bias = c.router_bias;
+      p.idx = topk_idx;
+      p.w = topk_w;
+      p.blkcnt = h->blkcnt;
+      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms,
+                                                      st)));
+    } else {
+      MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),
+                                        static_cast<const float *>(c.w_router), c.router_bias, T, d,
+                                        E, k, topk_idx, topk_w, h->blkcnt, h->status, st));
+    }
+  }
+  ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
+  MOE_TRY(launch_permute(topk_idx, h->blkcnt, T, k, E, counts, h->offsets, h->perm, h->inv,
+                         h->tiles1, h->tiles2, h->ntiles, h->nt1, h->nt2, c.n_shared, 0, h->status,
+                         st));
+  return MOE_OK;
+}
+
+int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream) {
+  if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+  const size_t row = h->esz * h->cfg.d_model;
+  const char *xb = static_cast<const char *>(x);
+  char *ob = static_cast<char *>(out);
+  if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (T == 1) {
+    return h->cfg.dtype == MOE_BF16
+               ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),
+                                           static_cast<__nv_bfloat16 *>(out), st)
+               : run_decode<float>(h, static_cast<const float *>(x), static_cast<float *>(out), st);
+  }
+  for (int c0 = 0; c0 < T; c0 += h->cfg.max_tokens) {
+    const int Tc = (T - c0) < h->cfg.max_tokens ? (T - c0) : h->cfg.max_tokens;
+    int rc;
+    if (h->cfg.dtype == MOE_BF16)
+      rc = run_prefill_chunk<__nv_bfloat16>(
+          h, reinterpret_cast<const __nv_bfloat16 *>(xb + row * c0), Tc,
+          reinterpret_cast<__nv_bfloat16 *>(ob + row * c0), st);
+    else
+      rc = run_prefill_chunk<float>(h, reinterpret_cast<const float *>(xb + row * c0), Tc,
+                                    reinterpret_cast<float *>(ob + row * c0), st);
+    if (rc != MOE_OK) return rc;
+  }
+  return MOE_OK;
+}
+
+int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int s[2] = {0, 0};
+  if (cudaMemcpy(s, h->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(h->status, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = s[1];
+  return s[0];
+}
+
+int moe_profile(moe_handle *h, int enable) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  h->prof = enable != 0;
+  if (h->prof) {
+    h->recs.clear();
+    h->pool_used = 0;
+  }
+  return MOE_OK;
+}
+
+int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n) {
+  if (!h || n < 0) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (ms) ms[i] = 0.0f;
+    if (launches) launches[i] = 0;
+  }
+  if (!h->recs.empty() && cudaEventSynchronize(h->recs.back().b) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (const ProfRec &r : h->recs) {
+    if (r.kind >= n) continue;
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return MOE_ERR_CUDA;
+    if (ms) ms[r.kind] += t;
+    if (launches) launches[r.kind] += 1;
+  }
+  return MOE_OK;
+}
+
+int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream) {
+  if (!h || wait_us < 1 || wait_us > 2000000) return MOE_ERR_INVALID_ARG;
+  int clk_khz = 0;
+  if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, h->device) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const long long cycles = static_cast<long long>(clk_khz) * wait_us / 1000;
+  MOE_TRY(launch_debug_wait(h->status, cycles, static_cast<cudaStream_t>(cuda_stream)));
+  return MOE_OK;
+}
+
+}  // extern "C"

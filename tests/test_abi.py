@@ -1,0 +1,91 @@
+"""The C ABI library builds, loads and exports every function include/moe.h
+declares; host-side argument validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mixture_experts_gemm_gb300 as moe
+from sparse_mixture_experts_gemm_gb300 import buildlib as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ["moe_create", "moe_route", "moe_forward", "moe_destroy", "moe_status",
+                 "moe_strerror"]:
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} declared in moe.h but not exported"
+        assert name in moe.EXPORTED
+
+
+def test_strerror(lib):
+    assert moe.strerror(0) == "ok"
+    assert "align" in moe.strerror(moe.MOE_ERR_ALIGNMENT)
+    assert moe.strerror(-99) == "unknown error"
+
+
+def _cfg(**kw):
+    base = dict(d_model=512, n_experts=16, top_k=4, d_ff=128, n_shared=1, max_tokens=64,
+                dtype=moe.MOE_BF16, w_router=0x1000, w_gate=0x2000, w_up=0x3000, w_down=0x4000,
+                s_gate=0x5000, s_up=0x6000, s_down=0x7000, router_bias=None)
+    base.update(kw)
+    c = moe.moe_config()
+    for k, v in base.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_model=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(top_k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(n_shared=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(w_gate=None), moe.MOE_ERR_INVALID_ARG),
+    (dict(s_up=None), moe.MOE_ERR_INVALID_ARG),
+    (dict(dtype=7), moe.MOE_ERR_INVALID_ARG),
+    (dict(d_model=520), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_ff=100), moe.MOE_ERR_UNSUPPORTED),
+    (dict(n_experts=257), moe.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=9, n_experts=16), moe.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=5, n_experts=4), moe.MOE_ERR_UNSUPPORTED),
+    (dict(max_tokens=70000), moe.MOE_ERR_UNSUPPORTED),
+    (dict(w_down=0x4004), moe.MOE_ERR_ALIGNMENT),
+    (dict(router_bias=0x8008), moe.MOE_ERR_ALIGNMENT),
+])
+def test_create_rejects_bad_config_on_host(lib, kw, code):
+    h = ctypes.c_void_p()
+    rc = lib.moe_create(ctypes.byref(_cfg(**kw)), ctypes.byref(h))
+    assert rc == code and h.value is None
+
+
+def test_null_handle_calls(lib):
+    assert lib.moe_forward(None, None, 4, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(None, None, 4, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_destroy(None) == moe.MOE_OK
+    assert lib.moe_create(None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.lib()

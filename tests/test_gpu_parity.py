@@ -1,0 +1,203 @@
+"""GPU path against the CPU oracle, through the C ABI.
+
+Bars: expert index sets and per-expert counts bit-exact; routing weights
+within 1e-5; block output within 1e-2 row-normwise relative error (bf16 data,
+fp32 accumulation, bf16 intermediates).  Small cases compare every output;
+full-size cases compare routing on every token and outputs on a seeded sample
+of tokens, in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import sparse_mixture_experts_gemm_gb300 as moe
+from sparse_mixture_experts_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+    moe.lib()
+    return torch.device("cuda:0")
+
+
+def to_dev(w, dev):
+    return {k: (None if v is None else v.to(dev)) for k, v in w.items()}
+
+
+def run_case(dev, seed, T, d, F, E, k, dtype="bf16", n_shared=1, max_tokens=None, bias=None,
+             rows=None, gen_device="cpu"):
+    w = synth.layer_weights(seed, d, F, E, n_shared, dtype, gen_device)
+    x = H.margined_tokens(seed + 1000, T, w["Wr"], k, dtype, bias=bias, device=gen_device)
+    wd = to_dev(w, dev)
+    xd = x.to(dev)
+    bd = None if bias is None else bias.to(dev)
+    layer = moe.MoELayer(wd, k, max_tokens=max_tokens or max(T, 1), bias=bd)
+    try:
+        if T <= layer.cfg.max_tokens:
+            idx, wts, counts = layer.route(xd)
+        out = layer.forward(xd)
+        torch.cuda.synchronize()
+        rc, detail = layer.status()
+        assert rc == 0, f"device status {rc} detail {detail}"
+        if T <= layer.cfg.max_tokens:
+            ridx, rw, _, rcounts = H.oracle.route(H.np_view(x), H.np_view(w["Wr"]), k,
+                                                  bias=None if bias is None else bias.numpy())
+            H.check_routing(idx, wts, counts, ridx, rw, rcounts)
+        ref, oidx, ow, _ = H.oracle_forward(x, w, k, bias=bias, rows=rows)
+        got = out if rows is None else out[torch.as_tensor(rows, device=dev)]
+        err = H.row_rel_err(got, ref)
+        assert err.max() <= H.OUT_TOL, f"max row rel err {err.max():.3e} at row {err.argmax()}"
+        return out, err
+    finally:
+        layer.close()
+
+
+def test_tiny_fp32_config(dev):
+    """T=32, d=512, 256 experts top-8 + shared, F=128, fp32 throughout, seed 0."""
+    _, err = run_case(dev, 0, 32, 512, 128, 256, 8, dtype="f32")
+    assert err.max() < 5e-3
+
+
+@pytest.mark.parametrize("T", [2, 3, 127, 128, 129, 300, 1000])
+def test_bf16_multi_tile_ragged(dev, T):
+    """Few experts, many rows each: several M tiles per expert with ragged tails,
+    two N tiles in both GEMMs."""
+    run_case(dev, 10 + T, T, 512, 256, 16, 4)
+
+
+def test_bf16_mostly_empty_experts(dev):
+    """256 experts, 40 tokens: most experts get no rows, some get one."""
+    run_case(dev, 20, 40, 512, 128, 256, 8)
+
+
+def test_bf16_no_shared_expert(dev):
+    run_case(dev, 21, 200, 512, 128, 32, 4, n_shared=0)
+
+
+def test_bf16_one_group_takes_every_token(dev):
+    """A bias that makes experts 0..7 win for every token: 8 groups of T rows."""
+    bias = torch.zeros(64)
+    bias[:8] = 20.0
+    run_case(dev, 22, 300, 512, 128, 64, 8, bias=bias)
+
+
+def test_fp32_multi_tile(dev):
+    run_case(dev, 23, 260, 256, 128, 8, 2, dtype="f32")
+
+
+def test_chunking_does_not_change_output(dev):
+    """Tokens are independent, so the chunk size must not change a single bit
+    ("Bound temporary memory with request chunking")."""
+    d, F, E, k, T = 512, 128, 32, 4, 700
+    w = to_dev(synth.layer_weights(30, d, F, E, 1, "bf16", "cpu"), dev)
+    x = synth.tokens(31, T, d, "bf16", "cpu").to(dev)
+    outs = []
+    for mt in (128, 333, 1024):
+        layer = moe.MoELayer(w, k, max_tokens=mt)
+        outs.append(layer.forward(x))
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+        layer.close()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_token_permutation_equivariance(dev):
+    d, F, E, k, T = 512, 128, 32, 4, 257
+    w = to_dev(synth.layer_weights(32, d, F, E, 1, "bf16", "cpu"), dev)
+    x = synth.tokens(33, T, d, "bf16", "cpu").to(dev)
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(3)).to(dev)
+    layer = moe.MoELayer(w, k, max_tokens=T)
+    a = layer.forward(x)
+    b = layer.forward(x[perm].contiguous())
+    torch.cuda.synchronize()
+    layer.close()
+    assert torch.equal(a[perm], b)
+
+
+def test_decode_full_size_layer(dev):
+    """Batch-1 path (d=2048, 256 experts top-8 + shared, F=512, bf16) for a few
+    fresh tokens; also equal to the prefill path's result for the same token."""
+    d, F, E, k = 2048, 512, 256, 8
+    w = synth.layer_weights(1, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(1001, 6, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=8)
+    outs = [layer.forward(x[i:i + 1].clone()) for i in range(6)]
+    pre = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.status()[0] == 0
+    layer.close()
+    out = torch.cat(outs)
+    ref, *_ = H.oracle_forward(x, w, k)
+    err = H.row_rel_err(out, ref)
+    assert err.max() <= H.OUT_TOL, err
+    err_pre = H.row_rel_err(pre, ref)
+    assert err_pre.max() <= H.OUT_TOL, err_pre
+
+
+def _sample_rows(T, n, seed):
+    r = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, T - 1], r.choice(T, n, replace=False)]))
+    return rows
+
+
+def test_prefill_4k_full_size(dev):
+    """T=4096, d=2048, 256 experts top-8 + shared, F=512, bf16: routing exact on
+    every token, outputs on 48 sampled tokens."""
+    T = 4096
+    run_case(dev, 2, T, 2048, 512, 256, 8, max_tokens=T, rows=_sample_rows(T, 46, 2),
+             gen_device=dev)
+
+
+def test_skewed_16k_full_size(dev):
+    """T=16384 with a Zipf(1.2) router bias: a few experts take thousands of
+    rows, many take none; routing exact on every token, outputs sampled."""
+    T = 16384
+    bias = synth.zipf_bias(3, 256, 1.2)
+    out, err = run_case(dev, 3, T, 2048, 512, 256, 8, max_tokens=T, bias=bias,
+                        rows=_sample_rows(T, 46, 3), gen_device=dev)
+
+
+def test_edge_calls(dev):
+    d, F, E, k = 256, 128, 8, 2
+    w = to_dev(synth.layer_weights(40, d, F, E, 1, "bf16", "cpu"), dev)
+    layer = moe.MoELayer(w, k, max_tokens=16)
+    x = torch.zeros((17, d), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(x)
+    assert moe.lib().moe_forward(layer.handle, x.data_ptr(), 0, out.data_ptr(), None) == 0
+    # misaligned pointer
+    rc = moe.lib().moe_forward(layer.handle, x.data_ptr() + 2, 4, out.data_ptr(), None)
+    assert rc == moe.MOE_ERR_ALIGNMENT
+    # routing more tokens than one chunk
+    idx = torch.empty((17, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((17, k), dtype=torch.float32, device=dev)
+    cnt = torch.empty((E,), dtype=torch.int32, device=dev)
+    rc = moe.lib().moe_route(layer.handle, x.data_ptr(), 17, idx.data_ptr(), wt.data_ptr(),
+                             cnt.data_ptr(), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # overlapping in/out
+    rc = moe.lib().moe_forward(layer.handle, x.data_ptr(), 4, x.data_ptr(), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    layer.close()
+
+
+def test_device_timeout_is_reported_not_trapped(dev):
+    """A bounded wait on a barrier nothing signals returns an error status and
+    leaves the context usable."""
+    d, F, E, k = 256, 128, 8, 2
+    w = to_dev(synth.layer_weights(41, d, F, E, 1, "bf16", "cpu"), dev)
+    layer = moe.MoELayer(w, k, max_tokens=64)
+    moe.moe_debug_wait_timeout(layer.handle, 2000)
+    rc, detail = layer.status()
+    assert rc == moe.MOE_ERR_DEVICE_TIMEOUT and detail == 907
+    assert layer.status()[0] == 0  # cleared by the read
+    x = synth.tokens(42, 64, d, "bf16", "cpu").to(dev)
+    layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.status()[0] == 0
+    layer.close()
