@@ -1,0 +1,510 @@
+"""Benchmark of the sparse MoE feed-forward block on GB300.
+
+Default workload (N=1): prefill of T=4096 tokens through one MoE layer
+(d=2048, 256 experts top-8 + 1 shared, F=512, bf16 weights and activations,
+fp32 accumulation), plus the batch-1 decode path over a stack of 40 distinct
+layers with a fresh token per step.  `value` is prefill tokens/s; the decode
+figures (microseconds per layer) are reported under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload prefill4k|skew16k|long128k|decode|tiny]
+
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the launching stream; a 256 MiB buffer is written between timed
+steps to flush L2 (outside the events).  Multi-GPU (torchrun): every rank runs
+its own replica (tokens are independent; no collective on the data path),
+value = all ranks' tokens / the slowest rank's time ("scaling": "weak").
+The reference arm (--impl reference) times the CPU oracle on the host cores on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import sparse_mixture_experts_gemm_gb300 as moe  # noqa: E402
+from sparse_mixture_experts_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "MoE block tokens/s (4K prefill) & decode µs/layer (batch 1); % of roofline"
+D, F, E, K = 2048, 512, 256, 8
+
+WORKLOADS = {
+    "prefill4k": dict(T=4096, chunk=4096, seed=2, zipf=False, d=D, F=F, E=E, k=K, dtype="bf16"),
+    "skew16k": dict(T=16384, chunk=16384, seed=3, zipf=True, d=D, F=F, E=E, k=K, dtype="bf16"),
+    "long128k": dict(T=131072, chunk=8192, seed=4, zipf=False, d=D, F=F, E=E, k=K, dtype="bf16"),
+    "tiny": dict(T=32, chunk=32, seed=0, zipf=False, d=512, F=128, E=256, k=8, dtype="f32"),
+}
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ helpers
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def make_layer(cfg: dict, dev, seed: int):
+    w = synth.layer_weights(seed, cfg["d"], cfg["F"], cfg["E"], 1, cfg["dtype"], dev)
+    bias = synth.zipf_bias(seed, cfg["E"], 1.2).to(dev) if cfg.get("zipf") else None
+    layer = moe.MoELayer(w, cfg["k"], max_tokens=cfg["chunk"], bias=bias)
+    return layer, w, bias
+
+
+def algorithmic_prefill(cfg: dict, counts: np.ndarray, T: int) -> dict:
+    """Algorithmic work of one prefill pass: FLOPs and the minimum HBM bytes
+    (weights of every expert with at least one row + shared + router, x read
+    once, out written once)."""
+    d, Fd, k = cfg["d"], cfg["F"], cfg["k"]
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    active = int((counts > 0).sum())
+    A = T * k
+    flops = 2 * T * d * cfg["E"] + 6 * (A + T) * d * Fd
+    w_bytes = (active + 1) * 3 * Fd * d * es + cfg["E"] * d * es
+    bytes_ = w_bytes + 2 * T * d * es
+    # gate/up GEMM alone: its weights, the rows it reads, the h it writes
+    g1_bytes = (active + 1) * 2 * Fd * d * es + (A + T) * d * es + (A + T) * Fd * es
+    g1_flops = 4 * (A + T) * d * Fd
+    return dict(flops=flops, bytes=bytes_, active=active, g1_bytes=g1_bytes, g1_flops=g1_flops)
+
+
+def flush_l2(buf):
+    buf.fill_(1)
+
+
+# ------------------------------------------------------------------ our arm
+def bench_prefill(cfg, dev, steps, warmup, flush_buf):
+    layer, w, bias = make_layer(cfg, dev, cfg["seed"])
+    T = cfg["T"]
+    x = synth.tokens(cfg["seed"] + 1000, T, cfg["d"], cfg["dtype"], dev)
+    out = torch.empty_like(x)
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    rc, det = layer.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} ({det}) after warm-up")
+    chunk_counts = []
+    for c0 in range(0, T, cfg["chunk"]):
+        _, _, cnt = layer.route(x[c0:c0 + cfg["chunk"]])
+        chunk_counts.append(cnt.cpu().numpy())
+    torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    moe.moe_profile(layer.handle, True)
+    with Clocks(dev.index or 0) as clk:
+        for i in range(steps):
+            flush_l2(flush_buf)
+            evs[i][0].record(st)
+            layer.forward(x, out)
+            evs[i][1].record(st)
+        torch.cuda.synchronize()
+    prof = moe.moe_profile_read(layer.handle)
+    moe.moe_profile(layer.handle, False)
+    rc, det = layer.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} ({det}) in timed region")
+    times = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end through the public call with host buffers
+    xh = x.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(x)
+    od = torch.empty_like(x)
+    for _ in range(max(1, warmup)):
+        xd.copy_(xh, non_blocking=True)
+        layer.forward(xd, od)
+        oh.copy_(od, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush_buf)
+        e2e_ev[i][0].record(st)
+        xd.copy_(xh, non_blocking=True)
+        layer.forward(xd, od)
+        oh.copy_(od, non_blocking=True)
+        e2e_ev[i][1].record(st)
+    torch.cuda.synchronize()
+    e2e_times = [a.elapsed_time(b) for a, b in e2e_ev]
+    res = dict(times=times, prof=prof, clocks=clk.summary(), e2e_times=e2e_times,
+               counts=chunk_counts, h2d=xh.numel() * xh.element_size(),
+               d2h=oh.numel() * oh.element_size(), layer=layer, w=w, bias=bias, x=x)
+    return res
+
+
+def bench_decode(dev, steps, warmup, n_layers=40):
+    cfg = WORKLOADS["prefill4k"]
+    layers = []
+    for l in range(n_layers):
+        layer, w, _ = make_layer(dict(cfg, chunk=1), dev, 1000 + l)
+        layers.append(layer)
+    d = cfg["d"]
+    xs = synth.tokens(1, steps + warmup, d, "bf16", dev)
+    x_in = torch.empty((1, d), dtype=torch.bfloat16, device=dev)
+    outs = [torch.empty((1, d), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        x_in.copy_(xs[0:1])
+        for l, layer in enumerate(layers):  # eager pass (also loads everything)
+            layer.forward(x_in, outs[l], stream=st)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for l, layer in enumerate(layers):
+                layer.forward(x_in, outs[l], stream=st)
+        for i in range(warmup):
+            x_in.copy_(xs[i:i + 1])
+            g.replay()
+        st.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        with Clocks(dev.index or 0) as clk:
+            for i in range(steps):
+                x_in.copy_(xs[warmup + i:warmup + i + 1])
+                evs[i][0].record(st)
+                g.replay()
+                evs[i][1].record(st)
+            st.synchronize()
+        # per-kernel split on one eager step with events between the kernels
+        for layer in layers:
+            moe.moe_profile(layer.handle, True)
+        for l, layer in enumerate(layers):
+            layer.forward(x_in, outs[l], stream=st)
+        st.synchronize()
+        split = {}
+        for layer in layers:
+            for kname, (ms, n) in moe.moe_profile_read(layer.handle).items():
+                a = split.setdefault(kname, [0.0, 0])
+                a[0] += ms
+                a[1] += n
+            moe.moe_profile(layer.handle, False)
+    for layer in layers:
+        rc, det = layer.status(st)
+        if rc != 0:
+            raise RuntimeError(f"decode device status {rc} ({det})")
+    times = [a.elapsed_time(b) for a, b in evs]
+    for layer in layers:
+        layer.close()
+    del g
+    return dict(times=times, clocks=clk.summary(), split=split, n_layers=n_layers)
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_prefill_rate(cfg, w, x, bias, n_tokens, nthreads):
+    """Oracle tokens/s on the first n_tokens of the batch (host cores)."""
+    import oracle
+    oracle.build()
+
+    def npv(t):
+        t = t.detach().contiguous().cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
+            else t.numpy()
+
+    wr, wg, wu, wd = npv(w["Wr"]), npv(w["Wg"]), npv(w["Wu"]), npv(w["Wd"])
+    sg, su, sd = npv(w["Sg"]), npv(w["Su"]), npv(w["Sd"])
+    xs = npv(x[:n_tokens])
+    b = None if bias is None else bias.detach().cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.forward(xs, wr, list(wg), list(wu), list(wd), cfg["k"], sg=sg, su=su, sd=sd, bias=b,
+                   nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill4k",
+                    choices=["prefill4k", "skew16k", "long128k", "tiny", "decode"])
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--oracle-tokens", type=int, default=2048,
+                    help="tokens of the batch the CPU baseline runs on (about 10-30 s)")
+    ap.add_argument("--reference-tokens", type=int, default=256,
+                    help="tokens per step of the reference (oracle) arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    wl_name = "prefill4k" if args.workload == "decode" else args.workload
+    cfg = WORKLOADS[wl_name]
+    pk = peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, cfg, wl_name)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.build()
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    if args.workload == "decode":
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50))
+        emit_decode_line(args, dec, pk, world)
+        return
+
+    res = bench_prefill(cfg, dev, args.steps, args.warmup, flush_buf)
+    T = cfg["T"]
+    ms = statistics.mean(res["times"])
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([sum(res["times"])], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = tt.item() / len(res["times"])
+    value = world * T / (ms_max / 1e3)
+    e2e_ms = statistics.mean(res["e2e_times"])
+
+    counts = np.sum(res["counts"], axis=0) if len(res["counts"]) == 1 else None
+    work = [algorithmic_prefill(cfg, c, min(cfg["chunk"], T - i * cfg["chunk"]))
+            for i, c in enumerate(res["counts"])]
+    flops = sum(w_["flops"] for w_ in work)
+    bytes_ = sum(w_["bytes"] for w_ in work)
+    g1_ms, g1_n = res["prof"]["gemm_gate_up"]
+    g1_avg = g1_ms / max(g1_n, 1)
+    g1_bytes = sum(w_["g1_bytes"] for w_ in work) / len(work)
+    g1_flops = sum(w_["g1_flops"] for w_ in work) / len(work)
+    achieved = g1_bytes / (g1_avg / 1e3) / 1e9
+    t_roof = max(flops / (pk["bf16"] * 1e12), bytes_ / (pk["hbm"] * 1e9))
+    launches_per_step = 6 * len(work)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": {
+            "workload": f"{wl_name}: T={T} tokens through one MoE layer, d={cfg['d']}, "
+                        f"{cfg['E']} experts top-{cfg['k']} + 1 shared, F={cfg['F']}"
+                        + (", Zipf(1.2) router bias" if cfg["zipf"] else "")
+                        + (f", chunks of {cfg['chunk']}" if cfg["chunk"] < T else ""),
+            "tokens_per_step": T, "chunk": cfg["chunk"], "d_model": cfg["d"],
+            "n_experts": cfg["E"], "top_k": cfg["k"], "d_ff": cfg["F"], "n_shared": 1,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed between timed steps (256 MiB write outside the events)",
+        },
+        "roofline": {
+            "kernel": "grouped gate/up GEMM + SiLU (gemm_kernel<bf16, EPI_SWIGLU>)",
+            "bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+            "frac": achieved / pk["hbm"], "traffic": None,
+            "peak_source": f"{pk['src']} hbm_gbs",
+            "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_ms": g1_avg,
+            "tensor_frac_of_measured_burst": g1_flops / (g1_avg / 1e3) / (pk["bf16"] * 1e12),
+        },
+        "block_roofline": {
+            "flops_per_step": flops, "bytes_per_step": bytes_,
+            "t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms,
+            "bound": "hbm" if bytes_ / (pk["hbm"] * 1e9) >= flops / (pk["bf16"] * 1e12) else "tensor",
+            "tensor_frac_of_measured_burst": flops / (ms / 1e3) / (pk["bf16"] * 1e12),
+            "hbm_frac_of_measured": bytes_ / (ms / 1e3) / (pk["hbm"] * 1e9),
+        },
+        "kernels_ms_per_step": {k_: v[0] / max(args.steps, 1) for k_, v in res["prof"].items()
+                                if v[1] > 0},
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": res["clocks"],
+    }
+    if not args.no_decode and wl_name == "prefill4k":
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50))
+        line["decode"] = decode_summary(dec, pk)
+        line["gpu_launches"] += 0  # decode launches are counted in its own object
+    if rank == 0 and not args.no_cpu:
+        nthr = host_threads()
+        n_tok = min(args.oracle_tokens, T)
+        rate, dt = oracle_prefill_rate(cfg, res["w"], res["x"], res["bias"], n_tok, nthr)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
+                                "sample": f"first {n_tok} of the {T} tokens of the same batch, "
+                                          f"{dt:.1f} s, {cpu_model()}"}
+    res["layer"].close()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def decode_summary(dec, pk) -> dict:
+    per_layer_us = [t * 1e3 / dec["n_layers"] for t in dec["times"]]
+    med = statistics.median(per_layer_us)
+    p90 = float(np.percentile(per_layer_us, 90))
+    byts = E * D * 2 + (K + 1) * 3 * F * D * 2
+    achieved = byts / (med * 1e-6) / 1e9
+    split = {k_: v[0] * 1e3 / max(v[1], 1) for k_, v in dec["split"].items() if v[1] > 0}
+    return {
+        "us_per_layer_median": med, "us_per_layer_p90": p90,
+        "tokens_per_s": 1e6 / (med * dec["n_layers"]),
+        "layers": dec["n_layers"], "steps": len(dec["times"]),
+        "workload": "batch-1 decode: one fresh token per step through 40 distinct layers "
+                    "(d=2048, 256 experts top-8 + 1 shared, F=512, bf16), CUDA graph per step",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm"], "traffic": None,
+                     "algorithmic_bytes_per_layer": byts,
+                     "peak_source": f"{pk['src']} hbm_gbs"},
+        "eager_us_per_launch": split,
+        "gpu_launches": 3 * dec["n_layers"] * len(dec["times"]),
+        "clocks": dec["clocks"],
+    }
+
+
+def emit_decode_line(args, dec, pk, world):
+    s = decode_summary(dec, pk)
+    line = {
+        "metric": METRIC, "value": s["us_per_layer_median"], "unit": "us/layer",
+        "n_gpus": world, "steps": len(dec["times"]), "warmup": max(args.warmup, 50),
+        "ms_per_step": statistics.mean(dec["times"]), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded)", "config": {"workload": s["workload"]},
+        "roofline": s["roofline"], "gpu_launches": s["gpu_launches"], "clocks": s["clocks"],
+        "decode": s,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args, cfg, wl_name):
+    """The CPU oracle on the host cores, same metric and config, bounded sample."""
+    import oracle
+    oracle.build()
+    T = cfg["T"]
+    w = synth.layer_weights(cfg["seed"], cfg["d"], cfg["F"], cfg["E"], 1, cfg["dtype"], "cpu")
+    x = synth.tokens(cfg["seed"] + 1000, T, cfg["d"], cfg["dtype"], "cpu")
+    bias = synth.zipf_bias(cfg["seed"], cfg["E"], 1.2) if cfg["zipf"] else None
+    nthr = host_threads()
+    n_tok = min(args.reference_tokens, T)
+    for _ in range(1):
+        oracle_prefill_rate(cfg, w, x, bias, min(8, T), nthr)
+    rates, dts = [], []
+    for _ in range(args.steps):
+        r, dt = oracle_prefill_rate(cfg, w, x, bias, n_tok, nthr)
+        rates.append(r)
+        dts.append(dt)
+    rate = statistics.mean(rates)
+    ms = statistics.mean(dts) * 1e3 * T / n_tok
+    sample = (f"first {n_tok} of the {T} tokens per step, {statistics.mean(dts):.2f} s per step, "
+              f"{cpu_model()}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": f"{wl_name}: T={T}, oracle on host"},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
