@@ -169,6 +169,33 @@ int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n);
  */
 int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
 
+/*
+ * Batch-1 forward of one layer that allocates no device memory, for callers
+ * that cannot call cudaMalloc (an application whose allocator owns the whole
+ * device pool, a serving loop that must not allocate after start-up, a plugin
+ * that is only handed device pointers) and so cannot use moe_create.  The
+ * pages have no counterpart to this entry point.
+ *
+ * cfg describes the layer exactly as for moe_create (max_tokens is ignored);
+ * x[d] and out[d] are device rows of cfg->dtype, 16-byte aligned, not
+ * overlapping.  Result: out = MoE(x), computed by the same decode kernels as
+ * moe_forward with T == 1.
+ *
+ * Scratch: one static device array of 66,048 bytes inside the library, which
+ * every GPU that loads the library holds until the process exits.  It limits
+ * (top_k + n_shared) * d_ff to 16384; larger layers return
+ * MOE_ERR_UNSUPPORTED, as do the limits of moe_create.  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current), so make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents (the call
+ * clears what must start at zero itself): calls that overlap on the GPU, on
+ * different streams or from different threads, race on it and must be
+ * serialised by the caller.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.  Asynchronous on
+ * cuda_stream; no host synchronisation.
+ */
+int moe_decode_noalloc(const moe_config *cfg, const void *x, void *out, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

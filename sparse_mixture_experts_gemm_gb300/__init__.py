@@ -36,7 +36,8 @@ KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "de
                 "decode_gate_up", "decode_down"]
 
 EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_status", "moe_destroy",
-            "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout"]
+            "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
+            "moe_decode_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
     L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
                                    ctypes.POINTER(ctypes.c_int64), ip]
     L.moe_debug_wait_timeout.argtypes = [vp, ip, vp]
+    L.moe_decode_noalloc.argtypes = [ctypes.POINTER(moe_config), vp, vp, vp]
     for name in EXPORTED:
         if name != "moe_strerror":
             getattr(L, name).restype = ip
@@ -168,6 +170,13 @@ def moe_profile_read(h: int) -> dict:
 def moe_debug_wait_timeout(h: int, wait_us: int, stream=None) -> int:
     return _check(lib().moe_debug_wait_timeout(h, wait_us, _stream(stream)),
                   "moe_debug_wait_timeout")
+
+
+def moe_decode_noalloc(cfg: moe_config, x, out, stream=None) -> int:
+    """Batch-1 forward without any device allocation (see include/moe.h): for
+    callers that cannot allocate device memory and so cannot create a handle."""
+    return _check(lib().moe_decode_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(out),
+                                           _stream(stream)), "moe_decode_noalloc")
 
 
 # ----------------------------------------------------------------- wrapper

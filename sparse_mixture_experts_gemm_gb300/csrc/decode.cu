@@ -328,6 +328,16 @@ cudaError_t decode_set_smem_attr(int bytes) {
 template cudaError_t decode_set_smem_attr<__nv_bfloat16>(int);
 template cudaError_t decode_set_smem_attr<float>(int);
 
+template <typename T>
+cudaError_t decode_get_smem_attr(int *bytes) {
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, decode_down_kernel<T>);
+  if (e == cudaSuccess) *bytes = fa.maxDynamicSharedSizeBytes;
+  return e;
+}
+template cudaError_t decode_get_smem_attr<__nv_bfloat16>(int *);
+template cudaError_t decode_get_smem_attr<float>(int *);
+
 template cudaError_t launch_decode_router<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
 template cudaError_t launch_decode_gateup<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
 template cudaError_t launch_decode_down<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);

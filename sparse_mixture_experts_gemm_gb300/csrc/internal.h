@@ -96,5 +96,7 @@ template <typename T>
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t decode_set_smem_attr(int bytes);
+template <typename T>
+cudaError_t decode_get_smem_attr(int *bytes);
 
 }  // namespace moe
