@@ -23,27 +23,36 @@ enum Epilogue { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_ROUTER = 2 };
 constexpr int kBM = 128;      // rows per tile (TMEM lanes)
 constexpr int kBN = 256;      // MMA N: B rows per tile
 constexpr int kStages = 4;    // smem pipeline depth
-constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kGemmSmem = kStages * (kBM * 128 + kBN * 128) + 1024 + 1024;
+constexpr int kThreads = 192; // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGemmCtrl = 4096;  // barriers, TMEM slot, row tokens, group table
+constexpr int kGemmSmem = kStages * (kBM * 128 + kBN * 128) + 1024 + kGemmCtrl;
 constexpr int kMaxTopK = 8;
 
 struct GemmParams {
-  const GemmTile *tiles;  // device tile list (null for the router)
-  const int *ntiles_dev;  // device tile count (null for the router)
-  int ntiles_host;        // router: number of 128-token tiles
-  int num_k_blocks;       // K / (128 bytes / element size)
-  int n_routed;           // E
-  int b_rows_per_group;   // rows of one routed group's B matrix (F or d)
-  void *out;              // H (gate/up) or Yp (down)
-  long long ldo;          // elements per output row
-  int *status;            // device status word
-  int kid;                // KernelId for failure details
+  // grouped GEMMs: tiles derived from the group offsets
+  const int32_t *offsets;  // [E + 1] first slot of each routed group (device)
+  int T;                   // tokens of this chunk
+  int A;                   // T * k routed assignments
+  int n_shared;            // 0 or 1: group E = the shared expert over all T tokens
+  int nt;                  // N tiles per group
+  int ntiles_host;         // router: number of 128-token tiles
+  int num_k_blocks;        // K / (128 bytes / element size)
+  int n_routed;            // E
+  int b_rows_per_group;    // rows of one routed group's B matrix (F or d)
+  // epilogue output
+  void *out;               // H (gate/up) or Y (down)
+  long long ldo;           // elements per output row
+  int *status;             // device status word
+  int kid;                 // KernelId for failure details
   // router epilogue
-  int T, k, E;
+  int k, E;
   const float *bias;
   int32_t *idx;
   float *w;
-  int32_t *blkcnt;  // [ceil(T/128)][E], zeroed before the launch
+  int32_t *counts;         // [E], zeroed before the launch
+  int32_t *rank;           // [T * k] rank of each assignment inside its group (may be null)
+  int32_t *offsets_out;    // [E + 1] written by the last CTA (may be null)
+  unsigned *done;          // CTA completion ticket, zeroed before the launch
 };
 
 // Tensor maps: A routed, A shared, B0 routed, B1 routed, B0 shared, B1 shared.
@@ -61,15 +70,12 @@ cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t 
 // route.cu
 template <typename T>
 cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T_tok, int d, int E,
-                               int k, int32_t *idx, float *w, int32_t *blkcnt, int *status,
+                               int k, int32_t *idx, float *w, int32_t *counts, int32_t *rank,
                                cudaStream_t st);
-cudaError_t launch_permute(const int32_t *idx, const int32_t *blkcnt, int T_tok, int k, int E,
-                           int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
-                           GemmTile *tiles1, GemmTile *tiles2, int *ntiles, int nt1, int nt2,
-                           int n_shared, int build_tiles, int *status, cudaStream_t st);
+cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaStream_t st);
 template <typename T>
-cudaError_t launch_gather(const T *x, const int32_t *perm, T *xp, int A, int d, int T_tok,
-                          int *status, cudaStream_t st);
+cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv, const T *x,
+                         T *xp, int A, int k, int E, int d, int *status, cudaStream_t st);
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);

@@ -6,8 +6,9 @@
 // inference for Apple Silicon", section "Bound temporary memory with request
 // chunking"), all on the caller's stream with no host synchronisation
 // (section "Keep expert routing on the GPU"):
-//   router (tcgen05 for bf16, SIMT for fp32) -> permute -> gather ->
-//   grouped gate/up GEMM + SiLU -> grouped down GEMM -> combine.
+//   router (tcgen05 for bf16, SIMT + offsets for fp32) -> place (slots and
+//   the permuted row copy Xp) -> grouped gate/up GEMM + SiLU -> grouped down
+//   GEMM -> combine.
 // Decode (T == 1, section "Optimise the single-row weight path"):
 //   decode_router -> decode_gateup -> decode_down, chained with programmatic
 //   dependent launch.
@@ -83,12 +84,12 @@ struct moe_handle {
   int nt1 = 0, nt2 = 0;  // N tiles of the gate/up and down GEMMs
   // workspace (one allocation)
   void *ws = nullptr;
-  int32_t *idx = nullptr, *inv = nullptr, *perm = nullptr, *counts = nullptr, *offsets = nullptr,
-          *blkcnt = nullptr, *ntiles = nullptr, *status = nullptr, *sel = nullptr;
+  int32_t *idx = nullptr, *inv = nullptr, *offsets = nullptr, *status = nullptr,
+          *sel = nullptr;
+  int32_t *route_ctl = nullptr;  // [256] per-expert counts, then [4] the router's CTA ticket
   float *w = nullptr, *logits = nullptr, *selw = nullptr, *hdec = nullptr;
   unsigned *counter = nullptr;
   void *xp = nullptr, *hbuf = nullptr, *yp = nullptr;
-  GemmTile *tiles1 = nullptr, *tiles2 = nullptr;
   // static tensor maps
   CUtensorMap tm_xp, tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
   // profiling
@@ -96,6 +97,8 @@ struct moe_handle {
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
   size_t pool_used = 0;
+  int32_t *counts() { return route_ctl; }
+  unsigned *done() { return reinterpret_cast<unsigned *>(route_ctl + 256); }
 };
 
 namespace {
@@ -160,68 +163,84 @@ struct ProfScope {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+// The bf16 router: tcgen05 logits with top-k, weights, ranks and the
+// per-expert histogram in the epilogue; the last CTA writes the offsets.
+int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w, int32_t *counts,
+                     int32_t *rank, int32_t *offsets, cudaStream_t st) {
+  const moe_config &c = h->cfg;
+  CUtensorMap tm_x;
+  if (!make_map(&tm_x, x, 2, T, c.d_model, kBM)) return MOE_ERR_CUDA;
+  const int nblk = (T + kBM - 1) / kBM;
+  GemmMaps m;
+  m.m[0] = m.m[1] = tm_x;
+  m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
+  GemmParams p = {};
+  p.T = T;
+  p.ntiles_host = nblk;
+  p.num_k_blocks = c.d_model / 64;
+  p.n_routed = c.n_experts;
+  p.status = h->status;
+  p.kid = KID_ROUTER;
+  p.k = c.top_k;
+  p.E = c.n_experts;
+  p.bias = c.router_bias;
+  p.idx = idx;
+  p.w = w;
+  p.counts = counts;
+  p.rank = rank;
+  p.offsets_out = offsets;
+  p.done = h->done();
+  MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms, st)));
+  return MOE_OK;
+}
+
 template <typename T>
 int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st) {
   const moe_config &c = h->cfg;
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k;
-  const int nblk = (Tc + kBM - 1) / kBM;
   const int A = Tc * k;
   const int BK = static_cast<int>(128 / sizeof(T));
 
-  CUtensorMap tm_x;
-  if (!make_map(&tm_x, x, sizeof(T), Tc, d, kBM)) return MOE_ERR_CUDA;
-
-  MOE_TRY(cudaMemsetAsync(h->blkcnt, 0, sizeof(int32_t) * nblk * E, st));
+  MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, sizeof(int32_t) * 260, st));
   {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
-      GemmMaps m;
-      m.m[0] = m.m[1] = tm_x;
-      m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
-      GemmParams p = {};
-      p.ntiles_host = nblk;
-      p.num_k_blocks = d / BK;
-      p.n_routed = E;
-      p.status = h->status;
-      p.kid = KID_ROUTER;
-      p.T = Tc;
-      p.k = k;
-      p.E = E;
-      p.bias = c.router_bias;
-      p.idx = h->idx;
-      p.w = h->w;
-      p.blkcnt = h->blkcnt;
-      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms, st)));
+      const int rc = launch_router_tc(h, x, Tc, h->idx, h->w, h->counts(), h->inv, h->offsets, st);
+      if (rc != MOE_OK) return rc;
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
-                                    k, h->idx, h->w, h->blkcnt, h->status, st));
+                                    k, h->idx, h->w, h->counts(), h->inv, st));
+      MOE_TRY(launch_offsets(h->counts(), E, h->offsets, st));
     }
   }
   {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
-    MOE_TRY(launch_permute(h->idx, h->blkcnt, Tc, k, E, h->counts, h->offsets, h->perm, h->inv,
-                           h->tiles1, h->tiles2, h->ntiles, h->nt1, h->nt2, c.n_shared, 1, h->status,
-                           st));
-    MOE_TRY(launch_gather<T>(x, h->perm, static_cast<T *>(h->xp), A, d, Tc, h->status, st));
+    MOE_TRY(launch_place<T>(h->idx, h->offsets, h->inv, x, static_cast<T *>(h->xp), A, k, E, d,
+                               h->status, st));
   }
+  GemmParams base = {};
+  base.offsets = h->offsets;
+  base.T = Tc;
+  base.A = A;
+  base.n_shared = c.n_shared;
+  base.n_routed = E;
+  base.status = h->status;
   {
     ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
     GemmMaps m;
+    // routed rows from the permuted copy, the shared expert's rows from x
     m.m[0] = h->tm_xp;
-    m.m[1] = tm_x;
+    if (!make_map(&m.m[1], x, sizeof(T), Tc, d, kBM)) return MOE_ERR_CUDA;
     m.m[2] = h->tm_wg;
     m.m[3] = h->tm_wu;
     m.m[4] = c.n_shared ? h->tm_sg : h->tm_wg;
     m.m[5] = c.n_shared ? h->tm_su : h->tm_wu;
-    GemmParams p = {};
-    p.tiles = h->tiles1;
-    p.ntiles_dev = h->ntiles;
+    GemmParams p = base;
+    p.nt = h->nt1;
     p.num_k_blocks = d / BK;
-    p.n_routed = E;
     p.b_rows_per_group = F;
     p.out = h->hbuf;
     p.ldo = F;
-    p.status = h->status;
     p.kid = KID_GEMM_GATE_UP;
     MOE_TRY((launch_gemm<T, EPI_SWIGLU>(m, p, h->num_sms, st)));
   }
@@ -231,15 +250,12 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     m.m[0] = m.m[1] = h->tm_h;
     m.m[2] = m.m[3] = h->tm_wd;
     m.m[4] = m.m[5] = c.n_shared ? h->tm_sd : h->tm_wd;
-    GemmParams p = {};
-    p.tiles = h->tiles2;
-    p.ntiles_dev = h->ntiles + 1;
+    GemmParams p = base;
+    p.nt = h->nt2;
     p.num_k_blocks = F / BK;
-    p.n_routed = E;
     p.b_rows_per_group = d;
     p.out = h->yp;
     p.ldo = d;
-    p.status = h->status;
     p.kid = KID_GEMM_DOWN;
     MOE_TRY((launch_gemm<T, EPI_STORE>(m, p, h->num_sms, st)));
   }
@@ -339,8 +355,6 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
   }
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k, Tm = c.max_tokens;
   const size_t A = static_cast<size_t>(Tm) * k;
-  const size_t nblk = (Tm + kBM - 1) / kBM;
-  const size_t max_mt = A / kBM + E + 1 + nblk;
   const size_t esz = h->esz;
 
   // carve the workspace
@@ -352,19 +366,14 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
       {reinterpret_cast<void **>(&h->idx), sizeof(int32_t) * A},
       {reinterpret_cast<void **>(&h->w), sizeof(float) * A},
       {reinterpret_cast<void **>(&h->inv), sizeof(int32_t) * A},
-      {reinterpret_cast<void **>(&h->perm), sizeof(int32_t) * A},
-      {reinterpret_cast<void **>(&h->counts), sizeof(int32_t) * E},
+      {reinterpret_cast<void **>(&h->route_ctl), sizeof(int32_t) * 260},
       {reinterpret_cast<void **>(&h->offsets), sizeof(int32_t) * (E + 1)},
-      {reinterpret_cast<void **>(&h->blkcnt), sizeof(int32_t) * nblk * E},
-      {reinterpret_cast<void **>(&h->ntiles), sizeof(int32_t) * 4},
       {reinterpret_cast<void **>(&h->status), sizeof(int32_t) * 4},
       {reinterpret_cast<void **>(&h->sel), sizeof(int32_t) * kMaxTopK},
       {reinterpret_cast<void **>(&h->selw), sizeof(float) * kMaxTopK},
       {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
       {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
       {reinterpret_cast<void **>(&h->counter), sizeof(unsigned) * 4},
-      {reinterpret_cast<void **>(&h->tiles1), sizeof(GemmTile) * h->nt1 * max_mt},
-      {reinterpret_cast<void **>(&h->tiles2), sizeof(GemmTile) * h->nt2 * max_mt},
       {&h->xp, esz * A * d},
       {&h->hbuf, esz * (A + Tm) * F},
       {&h->yp, esz * (A + Tm) * d},
@@ -432,41 +441,14 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const moe_config &c = h->cfg;
   const int d = c.d_model, E = c.n_experts, k = c.top_k;
-  const int nblk = (T + kBM - 1) / kBM;
-  MOE_TRY(cudaMemsetAsync(h->blkcnt, 0, sizeof(int32_t) * nblk * E, st));
-  {
-    ProfScope ps(h, MOE_KERNEL_ROUTER, st);
-    if (c.dtype == MOE_BF16) {
-      CUtensorMap tm_x;
-      if (!make_map(&tm_x, x, 2, T, d, kBM)) return MOE_ERR_CUDA;
-      GemmMaps m;
-      m.m[0] = m.m[1] = tm_x;
-      m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
-      GemmParams p = {};
-      p.ntiles_host = nblk;
-      p.num_k_blocks = d / 64;
-      p.n_routed = E;
-      p.status = h->status;
-      p.kid = KID_ROUTER;
-      p.T = T;
-      p.k = k;
-      p.E = E;
-      p.bias = c.router_bias;
-      p.idx = topk_idx;
-      p.w = topk_w;
-      p.blkcnt = h->blkcnt;
-      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms,
-                                                      st)));
-    } else {
-      MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),
-                                        static_cast<const float *>(c.w_router), c.router_bias, T, d,
-                                        E, k, topk_idx, topk_w, h->blkcnt, h->status, st));
-    }
-  }
-  ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
-  MOE_TRY(launch_permute(topk_idx, h->blkcnt, T, k, E, counts, h->offsets, h->perm, h->inv,
-                         h->tiles1, h->tiles2, h->ntiles, h->nt1, h->nt2, c.n_shared, 0, h->status,
-                         st));
+  MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
+  MOE_TRY(cudaMemsetAsync(h->done(), 0, sizeof(unsigned) * 4, st));
+  ProfScope ps(h, MOE_KERNEL_ROUTER, st);
+  if (c.dtype == MOE_BF16) return launch_router_tc(h, x, T, topk_idx, topk_w, counts, nullptr,
+                                                   nullptr, st);
+  MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),
+                                    static_cast<const float *>(c.w_router), c.router_bias, T, d, E,
+                                    k, topk_idx, topk_w, counts, nullptr, st));
   return MOE_OK;
 }
 

@@ -1,17 +1,22 @@
 // route.cu -- GPU-resident routing around the grouped GEMMs:
 //   router_simt   fp32 router (one warp per token): logits, top-k, weights,
-//                 per-128-token-block expert histogram;
-//   permute       expert totals, exclusive prefix scan into group offsets, the
-//                 per-expert tile lists ("block map") of both grouped GEMMs,
-//                 and the stable token -> slot permutation;
-//   gather        copies each assignment's token row into its expert group;
+//                 and each assignment's rank inside its expert group, claimed
+//                 with an atomic on the per-expert histogram;
+//   offsets       exclusive prefix scan of the histogram into group offsets
+//                 (the bf16 router does this in its last CTA instead);
+//   place         slot = offset[expert] + rank for every assignment: the
+//                 (token, choice) -> slot map read by the combine, and the
+//                 token's row copied into its group's block of Xp;
 //   combine       out[t] = sum_j w[t][j] * Y[slot(t, j)] + Y_shared[t].
 // Source: "Optimizing on-device inference for Apple Silicon", section "Keep
 // expert routing on the GPU" (histogram, prefix scan into start offsets,
-// scatter of rows into expert groups, block map of fixed-size blocks, all in
-// one submission with no CPU synchronisation) and section "Reduce
-// intermediate traffic and dispatch traffic" (routing score applied to the
-// expert output, shared-expert result added).
+// scatter of rows into expert groups, all in one submission with no CPU
+// synchronisation) and section "Reduce intermediate traffic and dispatch
+// traffic" (routing score applied to the expert output, shared-expert result
+// added).  The order of rows inside a group follows the atomics and may
+// differ between runs; every output is independent of it, since each row of
+// a group is computed on its own and the combine adds a token's terms in
+// choice order.
 #include <cuda_bf16.h>
 
 #include "../../include/moe.h"
@@ -78,23 +83,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Inclusive scan of one int per thread over a 256-thread block.
-__device__ __forceinline__ int block_incl_scan_256(int v, int *sbuf) {
-  const int tid = threadIdx.x;
-  sbuf[tid] = v;
-  __syncthreads();
-#pragma unroll
-  for (int o = 1; o < 256; o <<= 1) {
-    const int add = tid >= o ? sbuf[tid - o] : 0;
-    __syncthreads();
-    sbuf[tid] += add;
-    __syncthreads();
-  }
-  const int r = sbuf[tid];
-  __syncthreads();
-  return r;
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------- fp32 router
@@ -106,7 +94,8 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const T *__restrict__ 
                                                           const T *__restrict__ wr,
                                                           const float *__restrict__ bias, int T_tok,
                                                           int d, int E, int k, int32_t *idx,
-                                                          float *w, int32_t *blkcnt) {
+                                                          float *w, int32_t *counts,
+                                                          int32_t *rank) {
   extern __shared__ float s_logit[];  // [8 warps][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -159,183 +148,116 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const T *__restrict__ 
     for (int j = 0; j < k; ++j) {
       idx[static_cast<long long>(t) * k + j] = seli[j];
       w[static_cast<long long>(t) * k + j] = ex[j] / s;
-      atomicAdd(blkcnt + static_cast<long long>(t / kBM) * E + seli[j], 1);
+      const int rk = atomicAdd(counts + seli[j], 1);
+      if (rank) rank[static_cast<long long>(t) * k + j] = rk;
     }
   }
 }
 
 template <typename T>
 cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T_tok, int d, int E,
-                               int k, int32_t *idx, float *w, int32_t *blkcnt, int *status,
+                               int k, int32_t *idx, float *w, int32_t *counts, int32_t *rank,
                                cudaStream_t st) {
-  (void)status;
   const int grid = (T_tok + 7) / 8;
   const size_t smem = sizeof(float) * 8 * E;
-  router_simt_kernel<T><<<grid, 256, smem, st>>>(x, wr, bias, T_tok, d, E, k, idx, w, blkcnt);
+  router_simt_kernel<T><<<grid, 256, smem, st>>>(x, wr, bias, T_tok, d, E, k, idx, w, counts, rank);
   return cudaGetLastError();
 }
 template cudaError_t launch_router_simt<float>(const float *, const float *, const float *, int, int,
-                                               int, int, int32_t *, float *, int32_t *, int *,
+                                               int, int, int32_t *, float *, int32_t *, int32_t *,
                                                cudaStream_t);
 template cudaError_t launch_router_simt<__nv_bfloat16>(const __nv_bfloat16 *, const __nv_bfloat16 *,
                                                        const float *, int, int, int, int, int32_t *,
-                                                       float *, int32_t *, int *, cudaStream_t);
+                                                       float *, int32_t *, int32_t *, cudaStream_t);
 
-// ---------------------------------------------------------------- permute
-// Grid: one CTA of 256 threads per 128-token block; thread e owns expert e.
-// Every CTA recomputes the expert totals and its own block's prefix from the
-// per-block histogram, so no grid-wide synchronisation is needed.  CTA 0 also
-// writes counts, offsets and both tile lists; tiles of one expert are ordered
-// (n, m) with m innermost so tiles sharing a weight block run side by side.
-__global__ void __launch_bounds__(256) permute_kernel(
-    const int32_t *__restrict__ idx, const int32_t *__restrict__ blkcnt, int T_tok, int k, int E,
-    int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, GemmTile *tiles1,
-    GemmTile *tiles2, int *ntiles, int nt1, int nt2, int n_shared, int build_tiles, int *status) {
-  __shared__ int s_scan[256];
-  __shared__ int s_idx[kBM * kMaxTopK];
-  const int e = threadIdx.x;
-  const int b = blockIdx.x;
-  const int nblk = (T_tok + kBM - 1) / kBM;
-  int tot = 0, pre = 0;
-  if (e < E) {
-    for (int bb = 0; bb < nblk; ++bb) {
-      const int c = blkcnt[static_cast<long long>(bb) * E + e];
-      tot += c;
-      if (bb < b) pre += c;
-    }
+// ---------------------------------------------------------------- offsets
+// offsets[e] = sum_{e' < e} counts[e'], offsets[E] = total; one warp.
+__global__ void offsets_kernel(const int32_t *__restrict__ counts, int E, int32_t *offsets) {
+  const int lane = threadIdx.x;
+  const int per = (E + 31) / 32;
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int e = lane * per + q;
+    if (e < E) sum += counts[e];
   }
-  const int off = block_incl_scan_256(tot, s_scan) - tot;
-  const int A_total = T_tok * k;
-
-  if (b == 0) {
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - sum;
+  for (int q = 0; q < per; ++q) {
+    const int e = lane * per + q;
     if (e < E) {
-      if (counts) counts[e] = tot;
-      if (offsets) offsets[e] = off;
-      if (offsets && e == E - 1) offsets[E] = off + tot;
-    }
-    if (build_tiles) {
-      const int mt = (e < E) ? (tot + kBM - 1) / kBM : 0;
-      const int mt_off = block_incl_scan_256(mt, s_scan) - mt;
-      for (int n = 0; n < nt1; ++n)
-        for (int m = 0; m < mt; ++m) {
-          GemmTile t;
-          t.group = e;
-          t.a_row = off + m * kBM;
-          t.out_row = off + m * kBM;
-          t.rows = min(kBM, tot - m * kBM);
-          t.n0 = n * kBM;
-          t.pad[0] = t.pad[1] = t.pad[2] = 0;
-          tiles1[nt1 * mt_off + n * mt + m] = t;
-        }
-      for (int n = 0; n < nt2; ++n)
-        for (int m = 0; m < mt; ++m) {
-          GemmTile t;
-          t.group = e;
-          t.a_row = off + m * kBM;
-          t.out_row = off + m * kBM;
-          t.rows = min(kBM, tot - m * kBM);
-          t.n0 = n * kBN;
-          t.pad[0] = t.pad[1] = t.pad[2] = 0;
-          tiles2[nt2 * mt_off + n * mt + m] = t;
-        }
-      // total routed M-tiles = last thread's inclusive value
-      __shared__ int s_total_mt;
-      if (e == 255) s_total_mt = mt_off + mt;
-      __syncthreads();
-      const int tmt = s_total_mt;
-      const int mts = n_shared ? (T_tok + kBM - 1) / kBM : 0;
-      for (int q = e; q < nt1 * mts; q += 256) {
-        const int n = q / mts, m = q % mts;
-        GemmTile t;
-        t.group = E;
-        t.a_row = m * kBM;                // rows of x
-        t.out_row = A_total + m * kBM;    // shared rows follow the routed ones in H
-        t.rows = min(kBM, T_tok - m * kBM);
-        t.n0 = n * kBM;
-        t.pad[0] = t.pad[1] = t.pad[2] = 0;
-        tiles1[nt1 * tmt + q] = t;
-      }
-      for (int q = e; q < nt2 * mts; q += 256) {
-        const int n = q / mts, m = q % mts;
-        GemmTile t;
-        t.group = E;
-        t.a_row = A_total + m * kBM;
-        t.out_row = A_total + m * kBM;
-        t.rows = min(kBM, T_tok - m * kBM);
-        t.n0 = n * kBN;
-        t.pad[0] = t.pad[1] = t.pad[2] = 0;
-        tiles2[nt2 * tmt + q] = t;
-      }
-      if (e == 0) {
-        ntiles[0] = nt1 * (tmt + mts);
-        ntiles[1] = nt2 * (tmt + mts);
-      }
+      offsets[e] = run;
+      run += counts[e];
     }
   }
-
-  // stable placement of this block's assignments: token order, then choice order
-  const int t0 = b * kBM;
-  const int nt = min(kBM, T_tok - t0);
-  for (int i = e; i < nt * k; i += 256) s_idx[i] = idx[static_cast<long long>(t0) * k + i];
-  __syncthreads();
-  if (e < E) {
-    int slot = off + pre;
-    for (int i = 0; i < nt * k; ++i) {
-      if (s_idx[i] == e) {
-        perm[slot] = t0 + i / k;
-        inv[static_cast<long long>(t0) * k + i] = slot;
-        ++slot;
-      }
-    }
-  }
-  for (int i = e; i < nt * k; i += 256)
-    if (s_idx[i] < 0 || s_idx[i] >= E)
-      report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
+  if (lane == 31) offsets[E] = incl;
 }
 
-cudaError_t launch_permute(const int32_t *idx, const int32_t *blkcnt, int T_tok, int k, int E,
-                           int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
-                           GemmTile *tiles1, GemmTile *tiles2, int *ntiles, int nt1, int nt2,
-                           int n_shared, int build_tiles, int *status, cudaStream_t st) {
-  const int nblk = (T_tok + kBM - 1) / kBM;
-  permute_kernel<<<nblk, 256, 0, st>>>(idx, blkcnt, T_tok, k, E, counts, offsets, perm, inv, tiles1,
-                                       tiles2, ntiles, nt1, nt2, n_shared, build_tiles, status);
+cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaStream_t st) {
+  offsets_kernel<<<1, 32, 0, st>>>(counts, E, offsets);
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- gather
-// One warp per assignment slot: Xp[slot] = x[perm[slot]], 16-byte vectors.
+// ---------------------------------------------------------------- place
+// One warp per assignment i = t * k + j: slot = offsets[e] + rank, written
+// over the rank in rank_inv[i]; the token row x[t] is copied to Xp[slot] with
+// 16-byte vectors (all of a lane's loads issued before its stores), so the
+// grouped gate/up GEMM reads each group's rows as one contiguous block.
 template <typename T>
-__global__ void __launch_bounds__(256) gather_kernel(const T *__restrict__ x,
-                                                     const int32_t *__restrict__ perm, T *xp, int A,
-                                                     int d, int T_tok, int *status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
-  if (row >= A) return;
-  const int t = perm[row];
-  if (t < 0 || t >= T_tok) {
+__global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ idx,
+                                                    const int32_t *__restrict__ offsets,
+                                                    int32_t *rank_inv, const T *__restrict__ x,
+                                                    T *xp, int A, int k, int E, int d,
+                                                    int *status) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (i >= A) return;
+  const int e = idx[i];
+  if (e < 0 || e >= E) {
     if (lane == 0) report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
     return;
   }
-  const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<long long>(t) * d);
-  uint4 *dst = reinterpret_cast<uint4 *>(xp + static_cast<long long>(row) * d);
+  const int lo = offsets[e], hi = offsets[e + 1];
+  const int slot = lo + rank_inv[i];
+  if (slot < lo || slot >= hi) {
+    if (lane == 0) report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
+    return;
+  }
+  __syncwarp();
+  if (lane == 0) rank_inv[i] = slot;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<long long>(i / k) * d);
+  uint4 *dst = reinterpret_cast<uint4 *>(xp + static_cast<long long>(slot) * d);
   const int nvec = d * static_cast<int>(sizeof(T)) / 16;
-#pragma unroll 8
-  for (int i = lane; i < nvec; i += 32) dst[i] = src[i];
+  for (int base = 0; base < nvec; base += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = base + q * 32 + lane;
+      if (j < nvec) v[q] = __ldg(src + j);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = base + q * 32 + lane;
+      if (j < nvec) dst[j] = v[q];
+    }
+  }
 }
 
 template <typename T>
-cudaError_t launch_gather(const T *x, const int32_t *perm, T *xp, int A, int d, int T_tok,
-                          int *status, cudaStream_t st) {
-  const int grid = (A + 7) / 8;
-  gather_kernel<T><<<grid, 256, 0, st>>>(x, perm, xp, A, d, T_tok, status);
+cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv, const T *x,
+                         T *xp, int A, int k, int E, int d, int *status, cudaStream_t st) {
+  place_kernel<T><<<(A + 7) / 8, 256, 0, st>>>(idx, offsets, rank_inv, x, xp, A, k, E, d, status);
   return cudaGetLastError();
 }
-template cudaError_t launch_gather<float>(const float *, const int32_t *, float *, int, int, int,
-                                          int *, cudaStream_t);
-template cudaError_t launch_gather<__nv_bfloat16>(const __nv_bfloat16 *, const int32_t *,
-                                                  __nv_bfloat16 *, int, int, int, int *,
-                                                  cudaStream_t);
+template cudaError_t launch_place<float>(const int32_t *, const int32_t *, int32_t *, const float *,
+                                         float *, int, int, int, int, int *, cudaStream_t);
+template cudaError_t launch_place<__nv_bfloat16>(const int32_t *, const int32_t *, int32_t *,
+                                                 const __nv_bfloat16 *, __nv_bfloat16 *, int, int,
+                                                 int, int, int *, cudaStream_t);
 
 // ---------------------------------------------------------------- combine
 // One thread per 16-byte chunk of an output row; the k routed contributions
