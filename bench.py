@@ -308,6 +308,8 @@ def main():
     ap.add_argument("--workload", default="prefill4k",
                     choices=["prefill4k", "skew16k", "long128k", "tiny", "decode"])
     ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--decode-layers", type=int, default=40,
+                    help="distinct layers in the decode stack (40 in the benchmark; fewer for profiling)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=2048,
@@ -346,7 +348,7 @@ def main():
     torch.cuda.synchronize()
 
     if args.workload == "decode":
-        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50))
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers)
         emit_decode_line(args, dec, pk, world)
         return
 
@@ -420,7 +422,7 @@ def main():
         "clocks": res["clocks"],
     }
     if not args.no_decode and wl_name == "prefill4k":
-        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50))
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers)
         line["decode"] = decode_summary(dec, pk)
         line["gpu_launches"] += 0  # decode launches are counted in its own object
     if rank == 0 and not args.no_cpu:

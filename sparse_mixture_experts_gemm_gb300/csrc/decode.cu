@@ -1,23 +1,31 @@
 // decode.cu -- batch-1 path: one token through one MoE layer as three
 // weight-streaming kernels.  "Optimizing on-device inference for Apple
-// Silicon", section "Decode: minimise bytes moved per token" (with one row the
-// weights are read once per token, so bytes moved set the speed), section
-// "Optimise the single-row weight path" (row-parallel GEMV: a group of 32
-// threads cooperates on each output while reading different parts of the
-// weight row) and section "Reduce intermediate traffic and dispatch traffic"
+// Silicon", section "Decode: minimise bytes moved per token" (with one row
+// the weights are read once per token, so bytes moved set the speed),
+// section "Optimise the single-row weight path" (row-parallel GEMV: a group of
+// 32 threads cooperates on each output while reading different parts of the
+// weight row), section "Reduce intermediate traffic and dispatch traffic"
 // (gate/up projections fused with the activation; down projection fused with
-// the routing score and the shared-expert result).
+// the routing score and the shared-expert result) and section "Let independent
+// GPU work overlap" (work that does not depend on a result does not wait for
+// it).
 //
-//   decode_router : one warp per expert logit (16-byte streaming loads of the
-//                   router row, shuffle reduction); the last CTA to finish
-//                   takes the top-k and the softmax over the chosen logits.
-//   decode_gateup : one warp per (expert slot, intermediate row): gate and up
-//                   rows streamed together, h = silu(g) * u.
-//   decode_down   : one warp per output element: sum over the k routed slots
-//                   of w_j * (Wd_j row . h_j), plus the shared slot.
-// Each kernel may be launched with programmatic dependent launch: it calls
-// griddepcontrol.wait before reading anything the previous kernel wrote and
-// then lets its own dependents start.
+//   A  decode_router : router logits (one warp per expert) and, in other CTAs,
+//                      the shared expert's gate/up rows, which do not depend on
+//                      the routing; the last router CTA takes the top-k and
+//                      the softmax over the chosen logits.  Also prefetches the
+//                      shared down matrix into L2.
+//   B  decode_gateup : gate/up rows of the k chosen experts (one warp per row
+//                      pair), h = silu(g) * u; prefetches the k chosen down
+//                      matrices into L2.
+//   C  decode_down   : one warp per output element: sum over the routed slots
+//                      of w_j * (Wd_j row . h_j), plus the shared slot.
+// The kernels are chained with programmatic dependent launch.  Each one loads
+// the static weights it can before griddepcontrol.wait (which waits for the
+// previous kernel and makes its writes visible) and reads data produced by
+// earlier kernels only after it.  Kernel C reads the expert choice before its
+// wait: it was written by kernel A, which had completed before kernel B passed
+// its own wait and let C start.
 #include <cuda_bf16.h>
 
 #include "../../include/moe.h"
@@ -44,15 +52,18 @@ struct V16<__nv_bfloat16> {
     }
     return s;
   }
-  // weights (8 bf16) against 8 fp32 values
+  // weights (8 bf16) against 8 fp32 values (h 16-byte aligned, two 16-byte reads)
   __device__ __forceinline__ static float dotf(const uint4 &w, const float *h) {
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s = fmaf(__uint_as_float(a[i] << 16), h[2 * i], s);
-      s = fmaf(__uint_as_float(a[i] & 0xFFFF0000u), h[2 * i + 1], s);
-    }
+    const float4 h0 = reinterpret_cast<const float4 *>(h)[0];
+    const float4 h1 = reinterpret_cast<const float4 *>(h)[1];
+    float s = __uint_as_float(w.x << 16) * h0.x;
+    s = fmaf(__uint_as_float(w.x & 0xFFFF0000u), h0.y, s);
+    s = fmaf(__uint_as_float(w.y << 16), h0.z, s);
+    s = fmaf(__uint_as_float(w.y & 0xFFFF0000u), h0.w, s);
+    s = fmaf(__uint_as_float(w.z << 16), h1.x, s);
+    s = fmaf(__uint_as_float(w.z & 0xFFFF0000u), h1.y, s);
+    s = fmaf(__uint_as_float(w.w << 16), h1.z, s);
+    s = fmaf(__uint_as_float(w.w & 0xFFFF0000u), h1.w, s);
     return s;
   }
   __device__ __forceinline__ static void store(void *out, int i, float v) {
@@ -70,10 +81,11 @@ struct V16<float> {
     return s;
   }
   __device__ __forceinline__ static float dotf(const uint4 &w, const float *h) {
-    float s = __uint_as_float(w.x) * h[0];
-    s = fmaf(__uint_as_float(w.y), h[1], s);
-    s = fmaf(__uint_as_float(w.z), h[2], s);
-    s = fmaf(__uint_as_float(w.w), h[3], s);
+    const float4 hv = *reinterpret_cast<const float4 *>(h);
+    float s = __uint_as_float(w.x) * hv.x;
+    s = fmaf(__uint_as_float(w.y), hv.y, s);
+    s = fmaf(__uint_as_float(w.z), hv.z, s);
+    s = fmaf(__uint_as_float(w.w), hv.w, s);
     return s;
   }
   __device__ __forceinline__ static void store(void *out, int i, float v) {
@@ -87,48 +99,102 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// dot(row, x) over nvec 16-byte vectors; lanes stride the row, 8 loads in
-// flight per lane per round.
-template <typename T>
-__device__ __forceinline__ float row_dot(const uint4 *row, const uint4 *xv, int nvec, int lane) {
-  float acc = 0.0f;
-  for (int base = 0; base < nvec; base += 32 * 8) {
-    uint4 wv[8];
+// Up to kPre 16-byte vectors of one row held in registers per lane: vector
+// u * 32 + lane for u < kPre.  Loads issued before a dependency wait overlap
+// the previous kernel's tail.
+constexpr int kPre = 8;
+
+struct RowPre {
+  uint4 v[kPre];
+};
+
+__device__ __forceinline__ void row_prefetch(RowPre &r, const uint4 *row, int nvec, int lane) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = base + u * 32 + lane;
-      if (i < nvec) wv[u] = ld_stream16(row + i);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = base + u * 32 + lane;
-      if (i < nvec) acc += V16<T>::dot(wv[u], __ldg(xv + i));
-    }
+  for (int u = 0; u < kPre; ++u) {
+    const int i = u * 32 + lane;
+    if (i < nvec) r.v[u] = ld_stream16(row + i);
   }
+}
+
+// dot(row, x) for a row whose first 32 * kPre vectors are in r; the rest (rows
+// longer than 256 vectors) are streamed here.
+template <typename T>
+__device__ __forceinline__ float row_dot_pre(const RowPre &r, const uint4 *row, const uint4 *xv,
+                                             int nvec, int lane) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = u * 32 + lane;
+    if (i < nvec) acc += V16<T>::dot(r.v[u], __ldg(xv + i));
+  }
+  for (int i = 32 * kPre + lane; i < nvec; i += 32) acc += V16<T>::dot(ld_stream16(row + i), __ldg(xv + i));
   return acc;
+}
+
+// Bring [p, p + bytes) into L2 without waiting; bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// This CTA's share [lo, hi) of a byte range split over n CTAs in 16-byte units.
+__device__ __forceinline__ void split16(long long total, int n, int j, long long &lo,
+                                        long long &hi) {
+  const long long units = total / 16;
+  lo = units * j / n * 16;
+  hi = units * (j + 1) / n * 16;
 }
 
 }  // namespace
 
-// ---------------------------------------------------------------- router
+// ---------------------------------------------------------------- A: router
+// CTAs [0, ceil(E/8)): one warp per expert logit.  CTAs after them: one warp
+// per shared-expert intermediate row f (gate row and up row together).
 template <typename T>
 __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) {
   __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
+  const int n_rt = (a.E + 7) / 8;
+  const uint4 *xv = reinterpret_cast<const uint4 *>(a.x);
+  if (static_cast<int>(blockIdx.x) >= n_rt) {
+    const int c = blockIdx.x - n_rt;
+    const int f = c * 8 + warp;
+    if (threadIdx.x == 0) {
+      long long lo, hi;
+      split16(static_cast<long long>(a.d) * a.F * sizeof(T), gridDim.x - n_rt, c, lo, hi);
+      if (hi > lo) prefetch_l2(reinterpret_cast<const char *>(a.sd) + lo, static_cast<uint32_t>(hi - lo));
+    }
+    const uint4 *rg = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.sg) +
+                                                      static_cast<long long>(f) * a.d);
+    const uint4 *ru = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.su) +
+                                                      static_cast<long long>(f) * a.d);
+    RowPre pg, pu;
+    if (f < a.F) {
+      row_prefetch(pg, rg, nvec, lane);
+      row_prefetch(pu, ru, nvec, lane);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (f >= a.F) return;
+    float g = warp_sum(row_dot_pre<T>(pg, rg, xv, nvec, lane));
+    float u = warp_sum(row_dot_pre<T>(pu, ru, xv, nvec, lane));
+    if (lane == 0) a.h[static_cast<long long>(a.k) * a.F + f] = g / (1.0f + __expf(-g)) * u;
+    return;
+  }
+  const int e = blockIdx.x * 8 + warp;
+  const uint4 *row = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wr) +
+                                                     static_cast<long long>(e) * a.d);
+  RowPre pr;
+  if (e < a.E) row_prefetch(pr, row, nvec, lane);
   pdl_wait();
   pdl_launch_dependents();
   if (e < a.E) {
-    const uint4 *row = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wr) +
-                                                       static_cast<long long>(e) * a.d);
-    float acc = row_dot<T>(row, reinterpret_cast<const uint4 *>(a.x), nvec, lane);
-    acc = warp_sum(acc);
+    const float acc = warp_sum(row_dot_pre<T>(pr, row, xv, nvec, lane));
     if (lane == 0) a.logits[e] = acc + (a.bias ? a.bias[e] : 0.0f);
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1) ? 1 : 0;
+  if (threadIdx.x == 0) s_last = (atomicAdd(a.counter, 1u) == static_cast<unsigned>(n_rt - 1)) ? 1 : 0;
   __syncthreads();
   if (!s_last || warp != 0) return;
   __threadfence();
@@ -191,97 +257,114 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
   }
 }
 
-// ---------------------------------------------------------------- gate / up
+
+// ---------------------------------------------------------------- B: gate / up
+// One warp per (routed slot s, intermediate row f); thread 0 of each CTA
+// prefetches its share of the k chosen down matrices into L2 for kernel C.
 template <typename T>
 __global__ void __launch_bounds__(256) decode_gateup_kernel(const DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + warp;
-  const int s = gw / a.F, f = gw % a.F;
-  const int nslot = a.k + a.n_shared;
+  const int s = gw / a.F, f = gw - (gw / a.F) * a.F;
   pdl_wait();
   pdl_launch_dependents();
-  if (s >= nslot) return;
-  const T *wg, *wu;
-  if (s < a.k) {
-    const int e = a.sel[s];
-    wg = reinterpret_cast<const T *>(a.wg) + (static_cast<long long>(e) * a.F + f) * a.d;
-    wu = reinterpret_cast<const T *>(a.wu) + (static_cast<long long>(e) * a.F + f) * a.d;
-  } else {
-    wg = reinterpret_cast<const T *>(a.sg) + static_cast<long long>(f) * a.d;
-    wu = reinterpret_cast<const T *>(a.su) + static_cast<long long>(f) * a.d;
+  if (threadIdx.x == 0) {
+    const long long per = static_cast<long long>(a.d) * a.F * sizeof(T);
+    long long lo, hi;
+    split16(per * a.k, gridDim.x, blockIdx.x, lo, hi);
+    while (lo < hi) {
+      const int j = static_cast<int>(lo / per);
+      const long long off = lo - j * per;
+      const long long n = (hi - lo) < (per - off) ? (hi - lo) : (per - off);
+      prefetch_l2(reinterpret_cast<const char *>(a.wd) + a.sel[j] * per + off,
+                  static_cast<uint32_t>(n));
+      lo += n;
+    }
   }
+  if (s >= a.k) return;
+  const int e = a.sel[s];
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
+  const long long r = (static_cast<long long>(e) * a.F + f) * a.d;
+  const uint4 *rg = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wg) + r);
+  const uint4 *ru = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wu) + r);
+  RowPre pg, pu;
+  row_prefetch(pg, rg, nvec, lane);
+  row_prefetch(pu, ru, nvec, lane);
   const uint4 *xv = reinterpret_cast<const uint4 *>(a.x);
-  const uint4 *rg = reinterpret_cast<const uint4 *>(wg);
-  const uint4 *ru = reinterpret_cast<const uint4 *>(wu);
-  float g = 0.0f, u = 0.0f;
-  for (int base = 0; base < nvec; base += 32 * 8) {
-    uint4 vg[8], vu[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int i = base + q * 32 + lane;
-      if (i < nvec) {
-        vg[q] = ld_stream16(rg + i);
-        vu[q] = ld_stream16(ru + i);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int i = base + q * 32 + lane;
-      if (i < nvec) {
-        const uint4 xx = __ldg(xv + i);
-        g += V16<T>::dot(vg[q], xx);
-        u += V16<T>::dot(vu[q], xx);
-      }
-    }
-  }
-  g = warp_sum(g);
-  u = warp_sum(u);
+  const float g = warp_sum(row_dot_pre<T>(pg, rg, xv, nvec, lane));
+  const float u = warp_sum(row_dot_pre<T>(pu, ru, xv, nvec, lane));
   if (lane == 0) a.h[static_cast<long long>(s) * a.F + f] = g / (1.0f + __expf(-g)) * u;
 }
 
-// ---------------------------------------------------------------- down
+// ---------------------------------------------------------------- C: down
+// One warp per output element i.  The weight vectors of all k + 1 slots (up
+// to 64 per row, two per lane) are requested before the wait for h.
 template <typename T>
-__global__ void __launch_bounds__(256) decode_down_kernel(const DecodeArgs a) {
-  extern __shared__ float s_h[];  // [(k + n_shared)][F]
+__device__ __forceinline__ const uint4 *down_row(const DecodeArgs &a, int s, int i) {
+  const T *row = (s < a.k) ? reinterpret_cast<const T *>(a.wd) +
+                                 (static_cast<long long>(a.sel[s]) * a.d + i) * a.F
+                           : reinterpret_cast<const T *>(a.sd) + static_cast<long long>(i) * a.F;
+  return reinterpret_cast<const uint4 *>(row);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 2) decode_down_kernel(const DecodeArgs a) {
+  extern __shared__ float4 s_h4[];  // [(k + n_shared) * F / 4]
+  constexpr int NV = V16<T>::N;
+  constexpr int kSlots = kMaxTopK + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + warp;  // output element
+  const int i = blockIdx.x * 8 + warp;
   const int nslot = a.k + a.n_shared;
+  const int nvec = a.F / NV;
+  uint4 wv[kSlots][2];
+#pragma unroll
+  for (int s = 0; s < kSlots; ++s) {
+    if (s < nslot && i < a.d) {
+      const uint4 *rp = down_row<T>(a, s, i);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int v = q * 32 + lane;
+        if (v < nvec) wv[s][q] = ld_stream16(rp + v);
+      }
+    }
+  }
   pdl_wait();
   pdl_launch_dependents();
-  for (int q = threadIdx.x; q < nslot * a.F; q += blockDim.x) s_h[q] = a.h[q];
+  const int total4 = nslot * a.F / 4;
+  const float4 *hg = reinterpret_cast<const float4 *>(a.h);
+  for (int base = threadIdx.x; base < total4; base += 256 * 8) {
+    float4 t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = base + u * 256;
+      if (q < total4) t[u] = __ldcg(hg + q);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = base + u * 256;
+      if (q < total4) s_h4[q] = t[u];
+    }
+  }
   __syncthreads();
   if (i >= a.d) return;
-  constexpr int NV = V16<T>::N;
-  const int nvec = a.F / NV;
+  const float *s_h = reinterpret_cast<const float *>(s_h4);
   float acc = 0.0f;
-  for (int s = 0; s < nslot; ++s) {
-    const T *row;
-    float ws;
-    if (s < a.k) {
-      row = reinterpret_cast<const T *>(a.wd) + (static_cast<long long>(a.sel[s]) * a.d + i) * a.F;
-      ws = a.selw[s];
-    } else {
-      row = reinterpret_cast<const T *>(a.sd) + static_cast<long long>(i) * a.F;
-      ws = 1.0f;
-    }
-    const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-    const float *hs = s_h + s * a.F;
-    float part = 0.0f;
-    for (int base = 0; base < nvec; base += 32 * 4) {
-      uint4 wv[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = base + q * 32 + lane;
-        if (v < nvec) wv[q] = ld_stream16(rv + v);
-      }
+  for (int s = 0; s < kSlots; ++s) {
+    if (s < nslot) {
+      const float *hs = s_h + s * a.F;
+      float part = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = base + q * 32 + lane;
-        if (v < nvec) part += V16<T>::dotf(wv[q], hs + v * NV);
+      for (int q = 0; q < 2; ++q) {
+        const int v = q * 32 + lane;
+        if (v < nvec) part += V16<T>::dotf(wv[s][q], hs + v * NV);
       }
+      if (nvec > 64) {
+        const uint4 *rp = down_row<T>(a, s, i);
+        for (int v = 64 + lane; v < nvec; v += 32) part += V16<T>::dotf(ld_stream16(rp + v), hs + v * NV);
+      }
+      acc = fmaf(s < a.k ? a.selw[s] : 1.0f, part, acc);
     }
-    acc = fmaf(ws, part, acc);
   }
   acc = warp_sum(acc);
   if (lane == 0) V16<T>::store(a.out, i, acc);
@@ -307,12 +390,12 @@ cudaError_t launch_ex(K kern, int grid, int block, size_t smem, cudaStream_t st,
 
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  return launch_ex(decode_router_kernel<T>, (a.E + 7) / 8, 256, 0, st, pdl, a);
+  const int grid = (a.E + 7) / 8 + (a.n_shared ? (a.F + 7) / 8 : 0);
+  return launch_ex(decode_router_kernel<T>, grid, 256, 0, st, pdl, a);
 }
 template <typename T>
 cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  const int warps = (a.k + a.n_shared) * a.F;
-  return launch_ex(decode_gateup_kernel<T>, (warps + 7) / 8, 256, 0, st, pdl, a);
+  return launch_ex(decode_gateup_kernel<T>, (a.k * a.F + 7) / 8, 256, 0, st, pdl, a);
 }
 template <typename T>
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl) {
@@ -320,23 +403,15 @@ cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl) {
   return launch_ex(decode_down_kernel<T>, (a.d + 7) / 8, 256, smem, st, pdl, a);
 }
 
+// Dynamic shared memory limit of the decode kernels (set once per device): the
+// down kernel keeps h of all slots in shared memory.
 template <typename T>
-cudaError_t decode_set_smem_attr(int bytes) {
+cudaError_t decode_set_smem_attr() {
   return cudaFuncSetAttribute(decode_down_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bytes);
+                              (kMaxTopK + 1) * 4096 * static_cast<int>(sizeof(float)));
 }
-template cudaError_t decode_set_smem_attr<__nv_bfloat16>(int);
-template cudaError_t decode_set_smem_attr<float>(int);
-
-template <typename T>
-cudaError_t decode_get_smem_attr(int *bytes) {
-  cudaFuncAttributes fa;
-  const cudaError_t e = cudaFuncGetAttributes(&fa, decode_down_kernel<T>);
-  if (e == cudaSuccess) *bytes = fa.maxDynamicSharedSizeBytes;
-  return e;
-}
-template cudaError_t decode_get_smem_attr<__nv_bfloat16>(int *);
-template cudaError_t decode_get_smem_attr<float>(int *);
+template cudaError_t decode_set_smem_attr<__nv_bfloat16>();
+template cudaError_t decode_set_smem_attr<float>();
 
 template cudaError_t launch_decode_router<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
 template cudaError_t launch_decode_gateup<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);

@@ -93,6 +93,10 @@ struct DecodeArgs {
   unsigned *counter;   // last-block-done ticket, zero between launches
   void *out;           // [d]
   int *status;
+  // launch shape, filled in by the launchers
+  int rows_a;          // kernel A: router rows or shared items per CTA
+  int ring;            // kernel B: ring slots per CTA
+  int c_rows;          // kernel C: output rows per CTA (upper bound)
 };
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
@@ -100,9 +104,9 @@ template <typename T>
 cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl);
+// Raise the dynamic shared memory limit of the three decode kernels (once per
+// device, with the device current).
 template <typename T>
-cudaError_t decode_set_smem_attr(int bytes);
-template <typename T>
-cudaError_t decode_get_smem_attr(int *bytes);
+cudaError_t decode_set_smem_attr();
 
 }  // namespace moe

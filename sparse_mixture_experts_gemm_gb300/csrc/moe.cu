@@ -312,8 +312,7 @@ template <typename T>
 int set_attrs(const moe_config &c) {
   if (gemm_set_smem_attr<T, EPI_SWIGLU>() != cudaSuccess) return MOE_ERR_CUDA;
   if (gemm_set_smem_attr<T, EPI_STORE>() != cudaSuccess) return MOE_ERR_CUDA;
-  const int dec_smem = static_cast<int>(sizeof(float)) * (c.top_k + c.n_shared) * c.d_ff;
-  if (decode_set_smem_attr<T>(dec_smem) != cudaSuccess) return MOE_ERR_CUDA;
+  if (decode_set_smem_attr<T>() != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

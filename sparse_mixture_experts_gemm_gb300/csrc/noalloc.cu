@@ -11,9 +11,9 @@
 // holds until the process exits.
 //
 // Scratch layout (floats): [0, 256) router logits, [256, 264) chosen expert
-// ids (as int32), [264, 272) their weights, [272, 276) the last-block-done
-// counter, [512, 512 + kNoAllocMaxH) the intermediate h of the k routed
-// experts and the shared one.  The pages describe no allocation-free mode;
+// ids (as int32), [264, 272) their weights, [272, 276) the router's
+// last-block-done counter (cleared by every call), [512, 512 + kNoAllocMaxH)
+// the intermediate h of the k routed experts and the shared one.  The pages describe no allocation-free mode;
 // this has no counterpart there.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,21 +44,14 @@ int setup_device(int dev, float **out) {
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    // the decode kernels stage weight rows in dynamic shared memory
+    if (decode_set_smem_attr<__nv_bfloat16>() != cudaSuccess ||
+        decode_set_smem_attr<float>() != cudaSuccess)
+      return MOE_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<float *>(p);
   }
   *out = g_scratch_ptr[dev];
   return MOE_OK;
-}
-
-// The down kernel keeps h in dynamic shared memory; above the 48 KB default
-// its limit must be raised.  It is only ever raised here, never lowered.
-template <typename T>
-int ensure_down_smem(int bytes) {
-  if (bytes <= 48 * 1024) return MOE_OK;
-  int cur = 0;
-  if (decode_get_smem_attr<T>(&cur) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cur >= bytes) return MOE_OK;
-  return decode_set_smem_attr<T>(bytes) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -123,9 +116,6 @@ extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
   // the router's last-block-done counter must start at zero
   if (cudaMemsetAsync(a.counter, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
   const bool bf16 = c->dtype == MOE_BF16;
-  const int h_bytes = static_cast<int>(sizeof(float)) * (c->top_k + c->n_shared) * c->d_ff;
-  const int rc2 = bf16 ? ensure_down_smem<__nv_bfloat16>(h_bytes) : ensure_down_smem<float>(h_bytes);
-  if (rc2 != MOE_OK) return rc2;
   if ((bf16 ? launch_decode_router<__nv_bfloat16>(a, st, false)
             : launch_decode_router<float>(a, st, false)) != cudaSuccess)
     return MOE_ERR_CUDA;
