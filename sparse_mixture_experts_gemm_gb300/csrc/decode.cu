@@ -12,20 +12,22 @@
 //
 //   A  decode_router : router logits (one warp per expert) and, in other CTAs,
 //                      the shared expert's gate/up rows, which do not depend on
-//                      the routing; the last router CTA takes the top-k and
-//                      the softmax over the chosen logits.  Also prefetches the
-//                      shared down matrix into L2.
-//   B  decode_gateup : gate/up rows of the k chosen experts (one warp per row
-//                      pair), h = silu(g) * u; prefetches the k chosen down
+//                      the routing.  Also prefetches the shared down matrix
+//                      into L2.
+//   B  decode_gateup : every CTA takes the top-k of the logits and the softmax
+//                      over the chosen ones itself (one warp, two redux.sync
+//                      per choice), then one warp per (chosen expert, row) pair
+//                      computes h = silu(g) * u; prefetches the k chosen down
 //                      matrices into L2.
-//   C  decode_down   : one warp per output element: sum over the routed slots
-//                      of w_j * (Wd_j row . h_j), plus the shared slot.
+//   C  decode_down   : the same top-k, then one warp per output element: sum
+//                      over the routed slots of w_j * (Wd_j row . h_j), plus the
+//                      shared slot.
 // The kernels are chained with programmatic dependent launch.  Each one loads
 // the static weights it can before griddepcontrol.wait (which waits for the
 // previous kernel and makes its writes visible) and reads data produced by
-// earlier kernels only after it.  Kernel C reads the expert choice before its
-// wait: it was written by kernel A, which had completed before kernel B passed
-// its own wait and let C start.
+// earlier kernels only after it.  Kernel C reads the logits before its wait:
+// kernel A wrote them and had completed before kernel B passed its own wait
+// and let C start.
 #include <cuda_bf16.h>
 
 #include "../../include/moe.h"
@@ -144,6 +146,69 @@ __device__ __forceinline__ void split16(long long total, int n, int j, long long
   hi = units * (j + 1) / n * 16;
 }
 
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key; -0.0 sorts just below +0.0) and its inverse.
+__device__ __forceinline__ unsigned fkey(float v) {
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+// One warp: the k largest of E <= 256 logits (ties to the lower index) and
+// their softmax weights, into s_sel / s_selw (shared memory).  Each lane holds
+// experts lane + 32 i; a round takes the warp maximum of the keys, then the
+// lowest expert index holding it, with one redux.sync each.
+__device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int lane, int *s_sel,
+                                          float *s_selw) {
+  unsigned key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (e < E) ? fkey(__ldcg(logits + e)) : 0u;
+  }
+  float selv[kMaxTopK];
+  int seli[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    selv[j] = -INFINITY;
+    seli[j] = 0;
+    if (j < k) {
+      unsigned lm = key[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) lm = max(lm, key[i]);
+      const unsigned gm = __reduce_max_sync(0xffffffffu, lm);
+      int le = 0x7fffffff;
+#pragma unroll
+      for (int i = 7; i >= 0; --i)
+        if (key[i] == gm) le = lane + 32 * i;
+      int ge = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(le)));
+      if (ge >= E) ge = 0;  // only reachable with NaN logits; keeps every index in range
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i == ge) key[i] = 0u;
+      selv[j] = fkey_inv(gm);
+      seli[j] = ge;
+    }
+  }
+  if (lane == 0) {
+    float ex[kMaxTopK];
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      ex[j] = (j < k) ? expf(selv[j] - selv[0]) : 0.0f;
+      sum += ex[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        s_sel[j] = seli[j];
+        s_selw[j] = ex[j] / sum;
+      }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- A: router
@@ -151,7 +216,6 @@ __device__ __forceinline__ void split16(long long total, int n, int j, long long
 // per shared-expert intermediate row f (gate row and up row together).
 template <typename T>
 __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) {
-  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
   const int n_rt = (a.E + 7) / 8;
@@ -173,8 +237,8 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
       row_prefetch(pg, rg, nvec, lane);
       row_prefetch(pu, ru, nvec, lane);
     }
+    pdl_launch_dependents();  // kernel B reads nothing of ours before its wait
     pdl_wait();
-    pdl_launch_dependents();
     if (f >= a.F) return;
     float g = warp_sum(row_dot_pre<T>(pg, rg, xv, nvec, lane));
     float u = warp_sum(row_dot_pre<T>(pu, ru, xv, nvec, lane));
@@ -186,123 +250,128 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
                                                      static_cast<long long>(e) * a.d);
   RowPre pr;
   if (e < a.E) row_prefetch(pr, row, nvec, lane);
+  pdl_launch_dependents();  // kernel B reads nothing of ours before its wait
   pdl_wait();
-  pdl_launch_dependents();
   if (e < a.E) {
     const float acc = warp_sum(row_dot_pre<T>(pr, row, xv, nvec, lane));
     if (lane == 0) a.logits[e] = acc + (a.bias ? a.bias[e] : 0.0f);
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(a.counter, 1u) == static_cast<unsigned>(n_rt - 1)) ? 1 : 0;
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();
-  // last CTA: top-k over the E logits, 8 per lane at most (E <= 256)
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ee = lane + 32 * i;
-    v[i] = (ee < a.E) ? __ldcg(a.logits + ee) : -INFINITY;
-  }
-  float selv[kMaxTopK];
-  int seli[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    selv[j] = -INFINITY;
-    seli[j] = 0;
-    if (j < a.k) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int ee = lane + 32 * i;
-        if (v[i] > bv || (v[i] == bv && ee < bi)) {
-          bv = v[i];
-          bi = ee;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (bi >= a.E) bi = 0;  // only reachable with NaN logits; keeps every index in range
-      selv[j] = bv;
-      seli[j] = bi;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (lane + 32 * i == bi) v[i] = -INFINITY;
-    }
-  }
-  if (lane == 0) {
-    float ex[kMaxTopK];
-    float s = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      ex[j] = (j < a.k) ? expf(selv[j] - selv[0]) : 0.0f;
-      s += ex[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
-      if (j < a.k) {
-        a.sel[j] = seli[j];
-        a.selw[j] = ex[j] / s;
-      }
-    *a.counter = 0u;
-  }
 }
 
-
 // ---------------------------------------------------------------- B: gate / up
-// One warp per (routed slot s, intermediate row f); thread 0 of each CTA
-// prefetches its share of the k chosen down matrices into L2 for kernel C.
+// TMA-fed split of the chosen experts' gate/up rows: tile t covers rows
+// [rb * kRB, (rb + 1) * kRB) of slot s = t / (F / kRB); the CTA streams the
+// tile's gate and up rows through a 4-stage ring of boxes of kRB rows x 512
+// bytes (one box per matrix per stage, no swizzle), warp w (of 8) keeps partial
+// dot products of rows 4w .. 4w+3 in registers across the k-blocks and writes
+// h = silu(g) * u at the end.  Warp 8 lane 0 issues the copies.
+constexpr int kRB = 32;
+constexpr int kBStages = 4;
+constexpr int kBBox = kRB * 512;  // bytes of one box
+
 template <typename T>
-__global__ void __launch_bounds__(256) decode_gateup_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(288, 1)
+    decode_gateup_kernel(const __grid_constant__ CUtensorMap tmG,
+                         const __grid_constant__ CUtensorMap tmU, const DecodeArgs a) {
+  constexpr int KB = 512 / static_cast<int>(sizeof(T));  // elements per box row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *dsm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[kBStages], empty[kBStages];
+  __shared__ int s_sel[kMaxTopK];
+  __shared__ float s_selw[kMaxTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * 8 + warp;
-  const int s = gw / a.F, f = gw - (gw / a.F) * a.F;
-  pdl_wait();
-  pdl_launch_dependents();
+  const int nkb = a.d / KB;
+  const int nrb = a.F / kRB;
+  const int ntile = a.k * nrb;
+  const long long limit = MOE_WAIT_LIMIT_CYCLES;
   if (threadIdx.x == 0) {
-    const long long per = static_cast<long long>(a.d) * a.F * sizeof(T);
-    long long lo, hi;
-    split16(per * a.k, gridDim.x, blockIdx.x, lo, hi);
-    while (lo < hi) {
-      const int j = static_cast<int>(lo / per);
-      const long long off = lo - j * per;
-      const long long n = (hi - lo) < (per - off) ? (hi - lo) : (per - off);
-      prefetch_l2(reinterpret_cast<const char *>(a.wd) + a.sel[j] * per + off,
-                  static_cast<uint32_t>(n));
-      lo += n;
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 8);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tmG);
+    prefetch_tmap(&tmU);
+  }
+  pdl_wait();
+  if (warp == 0) warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
+  uint4 *xs = reinterpret_cast<uint4 *>(dsm + kBStages * 2 * kBBox);
+  const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
+  for (int i = threadIdx.x; i < a.d * static_cast<int>(sizeof(T)) / 16; i += blockDim.x) xs[i] = xg[i];
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == 8) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < ntile; t += gridDim.x) {
+      const int s = t / nrb, rb = t - (t / nrb) * nrb;
+      const int row = s_sel[s] * a.F + rb * kRB;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, limit, nullptr)) {
+          report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_DECODE * 100 + SITE_PRODUCER_EMPTY);
+          return;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        const uint32_t dst = smem_u32(dsm + stage * 2 * kBBox);
+        mbar_arrive_expect_tx(fb, 2 * kBBox);
+        tma_load_2d(dst, &tmG, fb, kb * KB, row, pol);
+        tma_load_2d(dst + kBBox, &tmU, fb, kb * KB, row, pol);
+        if (++stage == kBStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    return;
+  }
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int t = blockIdx.x; t < ntile; t += gridDim.x) {
+    const int s = t / nrb, rb = t - (t / nrb) * nrb;
+    float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kb = 0; kb < nkb; ++kb) {
+      const bool ok = mbar_wait(smem_u32(&full[stage]), phase, limit, nullptr);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_DECODE * 100 + SITE_MMA_FULL);
+        return;
+      }
+      const uint4 *bg = reinterpret_cast<const uint4 *>(dsm + stage * 2 * kBBox);
+      const uint4 *bu = bg + kBBox / 16;
+      const uint4 xv = xs[kb * 32 + lane];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = 4 * warp + q;
+        g[q] += V16<T>::dot(bg[r * 32 + lane], xv);
+        u[q] += V16<T>::dot(bu[r * 32 + lane], xv);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+      if (++stage == kBStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float gg = warp_sum(g[q]), uu = warp_sum(u[q]);
+      if (lane == 0)
+        a.h[static_cast<long long>(s) * a.F + rb * kRB + 4 * warp + q] = gg / (1.0f + __expf(-gg)) * uu;
     }
   }
-  if (s >= a.k) return;
-  const int e = a.sel[s];
-  const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
-  const long long r = (static_cast<long long>(e) * a.F + f) * a.d;
-  const uint4 *rg = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wg) + r);
-  const uint4 *ru = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.wu) + r);
-  RowPre pg, pu;
-  row_prefetch(pg, rg, nvec, lane);
-  row_prefetch(pu, ru, nvec, lane);
-  const uint4 *xv = reinterpret_cast<const uint4 *>(a.x);
-  const float g = warp_sum(row_dot_pre<T>(pg, rg, xv, nvec, lane));
-  const float u = warp_sum(row_dot_pre<T>(pu, ru, xv, nvec, lane));
-  if (lane == 0) a.h[static_cast<long long>(s) * a.F + f] = g / (1.0f + __expf(-g)) * u;
 }
 
 // ---------------------------------------------------------------- C: down
 // One warp per output element i.  The weight vectors of all k + 1 slots (up
 // to 64 per row, two per lane) are requested before the wait for h.
 template <typename T>
-__device__ __forceinline__ const uint4 *down_row(const DecodeArgs &a, int s, int i) {
+__device__ __forceinline__ const uint4 *down_row(const DecodeArgs &a, const int *sel, int s, int i) {
   const T *row = (s < a.k) ? reinterpret_cast<const T *>(a.wd) +
-                                 (static_cast<long long>(a.sel[s]) * a.d + i) * a.F
+                                 (static_cast<long long>(sel[s]) * a.d + i) * a.F
                            : reinterpret_cast<const T *>(a.sd) + static_cast<long long>(i) * a.F;
   return reinterpret_cast<const uint4 *>(row);
 }
@@ -316,11 +385,17 @@ __global__ void __launch_bounds__(256, 2) decode_down_kernel(const DecodeArgs a)
   const int i = blockIdx.x * 8 + warp;
   const int nslot = a.k + a.n_shared;
   const int nvec = a.F / NV;
+  // the next kernel only loads static weights before its own wait
+  pdl_launch_dependents();
+  __shared__ int s_sel[kMaxTopK];
+  __shared__ float s_selw[kMaxTopK];
+  if (warp == 0) warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
+  __syncthreads();
   uint4 wv[kSlots][2];
 #pragma unroll
   for (int s = 0; s < kSlots; ++s) {
     if (s < nslot && i < a.d) {
-      const uint4 *rp = down_row<T>(a, s, i);
+      const uint4 *rp = down_row<T>(a, s_sel, s, i);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int v = q * 32 + lane;
@@ -329,7 +404,7 @@ __global__ void __launch_bounds__(256, 2) decode_down_kernel(const DecodeArgs a)
     }
   }
   pdl_wait();
-  pdl_launch_dependents();
+
   const int total4 = nslot * a.F / 4;
   const float4 *hg = reinterpret_cast<const float4 *>(a.h);
   for (int base = threadIdx.x; base < total4; base += 256 * 8) {
@@ -360,10 +435,10 @@ __global__ void __launch_bounds__(256, 2) decode_down_kernel(const DecodeArgs a)
         if (v < nvec) part += V16<T>::dotf(wv[s][q], hs + v * NV);
       }
       if (nvec > 64) {
-        const uint4 *rp = down_row<T>(a, s, i);
+        const uint4 *rp = down_row<T>(a, s_sel, s, i);
         for (int v = 64 + lane; v < nvec; v += 32) part += V16<T>::dotf(ld_stream16(rp + v), hs + v * NV);
       }
-      acc = fmaf(s < a.k ? a.selw[s] : 1.0f, part, acc);
+      acc = fmaf(s < a.k ? s_selw[s] : 1.0f, part, acc);
     }
   }
   acc = warp_sum(acc);
@@ -394,8 +469,26 @@ cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl)
   return launch_ex(decode_router_kernel<T>, grid, 256, 0, st, pdl, a);
 }
 template <typename T>
-cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  return launch_ex(decode_gateup_kernel<T>, (a.k * a.F + 7) / 8, 256, 0, st, pdl, a);
+cudaError_t launch_decode_gateup(const DecodeArgs &a, const CUtensorMap &tmG, const CUtensorMap &tmU,
+                                 cudaStream_t st, bool pdl) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  const int ntile = a.k * (a.F / kRB);
+  const int grid = ntile < sms ? ntile : sms;
+  const size_t smem = 1024 + kBStages * 2 * kBBox + static_cast<size_t>(a.d) * sizeof(T);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(288);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_gateup_kernel<T>, tmG, tmU, a);
 }
 template <typename T>
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl) {
@@ -407,17 +500,23 @@ cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl) {
 // down kernel keeps h of all slots in shared memory.
 template <typename T>
 cudaError_t decode_set_smem_attr() {
-  return cudaFuncSetAttribute(decode_down_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (kMaxTopK + 1) * 4096 * static_cast<int>(sizeof(float)));
+  const cudaError_t e = cudaFuncSetAttribute(
+      decode_down_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (kMaxTopK + 1) * 4096 * static_cast<int>(sizeof(float)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_gateup_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              1024 + kBStages * 2 * kBBox + 16384 * static_cast<int>(sizeof(T)));
 }
 template cudaError_t decode_set_smem_attr<__nv_bfloat16>();
 template cudaError_t decode_set_smem_attr<float>();
 
 template cudaError_t launch_decode_router<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
-template cudaError_t launch_decode_gateup<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
+template cudaError_t launch_decode_gateup<__nv_bfloat16>(const DecodeArgs &, const CUtensorMap &,
+                                                         const CUtensorMap &, cudaStream_t, bool);
 template cudaError_t launch_decode_down<__nv_bfloat16>(const DecodeArgs &, cudaStream_t, bool);
 template cudaError_t launch_decode_router<float>(const DecodeArgs &, cudaStream_t, bool);
-template cudaError_t launch_decode_gateup<float>(const DecodeArgs &, cudaStream_t, bool);
+template cudaError_t launch_decode_gateup<float>(const DecodeArgs &, const CUtensorMap &,
+                                                 const CUtensorMap &, cudaStream_t, bool);
 template cudaError_t launch_decode_down<float>(const DecodeArgs &, cudaStream_t, bool);
 
 }  // namespace moe

@@ -67,6 +67,10 @@ template <typename T, int EPI>
 cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
+// moe.cu: tensor-map encoding (host only, no allocation)
+bool encode_map_2d(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
 // route.cu
 template <typename T>
 cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T_tok, int d, int E,
@@ -100,8 +104,10 @@ struct DecodeArgs {
 };
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
+// tmG / tmU: w_gate / w_up as [E * F][d] with boxes of (512 bytes) x 32 rows, no swizzle
 template <typename T>
-cudaError_t launch_decode_gateup(const DecodeArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_gateup(const DecodeArgs &a, const CUtensorMap &tmG, const CUtensorMap &tmU,
+                                 cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl);
 // Raise the dynamic shared memory limit of the three decode kernels (once per

@@ -49,22 +49,33 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-// 2D map over a row-major [rows][cols] matrix; box = 128 bytes of columns x
-// box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
-bool make_map(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
-              uint32_t box_rows) {
+}  // namespace
+
+// 2D map over a row-major [rows][cols] matrix with a box of box_cols x
+// box_rows elements; 128-byte swizzle or none; out-of-range elements read as
+// zero.  Host-only (encodes the descriptor, allocates nothing).
+bool moe::encode_map_2d(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
+                        uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return false;
   const CUtensorMapDataType dt =
       esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+// The GEMM operand map: boxes of 128 bytes of columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  return encode_map_2d(m, base, esz, rows, cols, static_cast<uint32_t>(128 / esz), box_rows, true);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -91,6 +102,7 @@ struct moe_handle {
   unsigned *counter = nullptr;
   void *xp = nullptr, *hbuf = nullptr, *yp = nullptr;
   // static tensor maps
+  CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
   CUtensorMap tm_xp, tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
   // profiling
   bool prof = false;
@@ -299,7 +311,7 @@ int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
   }
   {
     ProfScope ps(h, MOE_KERNEL_DECODE_GATE_UP, st);
-    MOE_TRY(launch_decode_gateup<T>(a, st, pdl));
+    MOE_TRY(launch_decode_gateup<T>(a, h->tm_dg, h->tm_du, st, pdl));
   }
   {
     ProfScope ps(h, MOE_KERNEL_DECODE_DOWN, st);
@@ -396,7 +408,11 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
   }
 
   // tensor maps of the weights and the fixed workspace buffers
-  bool ok = make_map(&h->tm_xp, h->xp, esz, A, d, kBM) &&
+  bool ok = encode_map_2d(&h->tm_dg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d,
+                          static_cast<uint32_t>(512 / esz), 32, false) &&
+            encode_map_2d(&h->tm_du, c.w_up, esz, static_cast<uint64_t>(E) * F, d,
+                          static_cast<uint32_t>(512 / esz), 32, false) &&
+            make_map(&h->tm_xp, h->xp, esz, A, d, kBM) &&
             make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
             make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
             make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&

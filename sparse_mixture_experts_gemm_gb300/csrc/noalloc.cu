@@ -119,8 +119,17 @@ extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
   if ((bf16 ? launch_decode_router<__nv_bfloat16>(a, st, false)
             : launch_decode_router<float>(a, st, false)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((bf16 ? launch_decode_gateup<__nv_bfloat16>(a, st, false)
-            : launch_decode_gateup<float>(a, st, false)) != cudaSuccess)
+  // tensor maps of the gate/up weights for the streaming kernel (host-side
+  // descriptors passed by value; nothing is allocated)
+  const size_t esz = bf16 ? 2 : 4;
+  CUtensorMap tmG, tmU;
+  if (!encode_map_2d(&tmG, c->w_gate, esz, static_cast<uint64_t>(c->n_experts) * c->d_ff,
+                     c->d_model, static_cast<uint32_t>(512 / esz), 32, false) ||
+      !encode_map_2d(&tmU, c->w_up, esz, static_cast<uint64_t>(c->n_experts) * c->d_ff,
+                     c->d_model, static_cast<uint32_t>(512 / esz), 32, false))
+    return MOE_ERR_CUDA;
+  if ((bf16 ? launch_decode_gateup<__nv_bfloat16>(a, tmG, tmU, st, false)
+            : launch_decode_gateup<float>(a, tmG, tmU, st, false)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((bf16 ? launch_decode_down<__nv_bfloat16>(a, st, false)
             : launch_decode_down<float>(a, st, false)) != cudaSuccess)
