@@ -375,7 +375,7 @@ def main():
     g1_flops = sum(w_["g1_flops"] for w_ in work) / len(work)
     achieved = g1_bytes / (g1_avg / 1e3) / 1e9
     t_roof = max(flops / (pk["bf16"] * 1e12), bytes_ / (pk["hbm"] * 1e9))
-    launches_per_step = 6 * len(work)
+    launches_per_step = 5 * len(work)  # router, place, gate/up, down, combine per chunk
     line = {
         "metric": METRIC,
         "value": value,

@@ -43,12 +43,16 @@ namespace moe {
 
 namespace {
 
-template <typename T>
+template <typename T, int BN>
 struct Tile {
   static constexpr int BK = 128 / sizeof(T);  // K elements per 128-byte row
   static constexpr int A_BYTES = kBM * 128;
-  static constexpr int B_BYTES = kBN * 128;
+  static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // as many stages as the tile budget holds, at most 8
+  static constexpr int STAGES =
+      (kStageBudget / STAGE_BYTES) < 8 ? (kStageBudget / STAGE_BYTES) : 8;
+  static_assert(STAGES >= 2, "pipeline needs two stages");
 };
 
 
@@ -79,23 +83,21 @@ __device__ __forceinline__ void store32<float>(float *dst, const float (&v)[32])
 
 // Keep the 8 largest (value, index) pairs, sorted descending; a candidate
 // equal to a kept value goes after it, so ties favour the lower index when
-// candidates arrive in increasing index order.
+// candidates arrive in increasing index order.  Branch-free: every slot
+// compares against the candidate independently and takes its own value, the
+// candidate, or its upper neighbour's value.
 __device__ __forceinline__ void topk_insert(float (&bv)[kMaxTopK], int (&bi)[kMaxTopK], float v,
                                             int e) {
-  if (!(v > bv[kMaxTopK - 1])) return;
-  bv[kMaxTopK - 1] = v;
-  bi[kMaxTopK - 1] = e;
+  bool c[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) c[j] = v > bv[j];
 #pragma unroll
   for (int j = kMaxTopK - 1; j > 0; --j) {
-    if (bv[j] > bv[j - 1]) {
-      const float tv = bv[j];
-      bv[j] = bv[j - 1];
-      bv[j - 1] = tv;
-      const int ti = bi[j];
-      bi[j] = bi[j - 1];
-      bi[j - 1] = ti;
-    }
+    bv[j] = c[j] ? (c[j - 1] ? bv[j - 1] : v) : bv[j];
+    bi[j] = c[j] ? (c[j - 1] ? bi[j - 1] : e) : bi[j];
   }
+  bv[0] = c[0] ? v : bv[0];
+  bi[0] = c[0] ? e : bi[0];
 }
 
 // Group table built by every CTA of a grouped GEMM: s_off[g] = first slot of
@@ -136,35 +138,38 @@ __device__ __forceinline__ GemmTile decode_tile(const GroupTable &gt, const Gemm
   return t;
 }
 
-__device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i) {
+// Router tile i: token block i / nq, expert block i % nq (n0 = first expert).
+__device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i, int bn) {
+  const int blk = i / p.nq;
   GemmTile t;
   t.group = 0;
-  t.a_row = i * kBM;
-  t.out_row = i * kBM;
-  t.rows = min(kBM, p.T - i * kBM);
-  t.n0 = 0;
+  t.a_row = blk * kBM;
+  t.out_row = blk * kBM;
+  t.rows = min(kBM, p.T - blk * kBM);
+  t.n0 = (i - blk * p.nq) * bn;
   t.pad[0] = t.pad[1] = t.pad[2] = 0;
   return t;
 }
 
 }  // namespace
 
-template <typename T, int EPI>
+template <typename T, int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const __grid_constant__ CUtensorMap tmB0s,
                 const __grid_constant__ CUtensorMap tmB1s, const GemmParams p) {
-  using C = Tile<T>;
+  using C = Tile<T, BN>;
   constexpr bool kRouter = (EPI == EPI_ROUTER);
   constexpr bool kDual = (EPI == EPI_SWIGLU);  // B = gate rows over up rows
-  constexpr int kOutCols = (EPI == EPI_SWIGLU) ? kBN / 2 : kBN;
+  constexpr int kOutCols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = smem + kStages * C::A_BYTES;
-  uint8_t *ctrl = sB + kStages * C::B_BYTES;
+  uint8_t *sB = smem + C::STAGES * C::A_BYTES;
+  uint8_t *ctrl = sB + C::STAGES * C::B_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
@@ -173,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *s_mt = reinterpret_cast<int *>(ctrl + 1536 + 1040);  // [E + 2]
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * kStages;
-  const uint32_t tfull0 = empty0 + 8 * kStages;
+  const uint32_t empty0 = full0 + 8 * C::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
 
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const GroupTable gt{s_off, s_mt};
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (EPI == EPI_STORE) prefetch_tmap(&tmB0s);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   int ntiles;
@@ -265,12 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
-      const GemmTile tl = kRouter ? router_tile(p, ti) : decode_tile(gt, p, ti, kOutCols, !kDual);
+      const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool sh = !kRouter && tl.group >= p.n_routed;
       const CUtensorMap *ma = sh ? &tmAs : &tmA;
       const CUtensorMap *mb0 = sh ? &tmB0s : &tmB0;
       const CUtensorMap *mb1 = sh ? &tmB1s : &tmB1;
-      const int brow = kRouter ? 0 : (sh ? tl.n0 : tl.group * p.b_rows_per_group + tl.n0);
+      const int brow = kRouter ? tl.n0 : (sh ? tl.n0 : tl.group * p.b_rows_per_group + tl.n0);
       for (int kb = 0; kb < p.num_k_blocks; ++kb) {
         bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pend_mask |= 1u << stage;
         pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
+        if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
         }
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) {
       // copies already issued must land before the CTA's shared memory goes away
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < C::STAGES; ++s)
         if (pend_mask & (1u << s))
           if (!mbar_wait(full0 + 8 * s, (pend_phase >> s) & 1, limit, nullptr))
             report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_DRAIN);
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_make(kBM, kBN, MmaKind<T>::ab_format);
+      constexpr uint32_t idesc = idesc_make(kBM, BN, MmaKind<T>::ab_format);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag)) {
             *abort_flag = 1;
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (kb | kk) != 0 ? 1u : 0u);
           tc_commit(empty0 + 8 * stage);
           issued = true;
-          if (++stage == kStages) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
-      const GemmTile tl = kRouter ? router_tile(p, ti) : decode_tile(gt, p, ti, kOutCols, !kDual);
+      const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, limit, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
@@ -381,16 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb =
-          tmem + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(wq * 32) << 16);
+          tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(wq * 32) << 16);
       const bool valid = r < tl.rows;
 
       if (EPI == EPI_SWIGLU) {
         T *hrow = reinterpret_cast<T *>(p.out) + static_cast<long long>(tl.out_row + r) * p.ldo + tl.n0;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 2; c += 32) {
+        for (int c = 0; c < BN / 2; c += 32) {
           float g[32], u[32];
           tmem_ld32(tb + c, g);
-          tmem_ld32(tb + kBN / 2 + c, u);
+          tmem_ld32(tb + BN / 2 + c, u);
           tmem_ld_wait();
           if (valid) {
 #pragma unroll
@@ -401,13 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (EPI == EPI_STORE) {
         T *yrow = reinterpret_cast<T *>(p.out) + static_cast<long long>(tl.out_row + r) * p.ldo + tl.n0;
 #pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
+        for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
           if (valid) store32<T>(yrow + c, v);
         }
       } else {
+        // top-8 of this tile's BN experts for the thread's token
         float bv[kMaxTopK];
         int bi[kMaxTopK];
 #pragma unroll
@@ -416,40 +422,98 @@ __global__ void __launch_bounds__(kThreads, 1)
           bi[j] = 0;
         }
 #pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
+        for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int e = c + i;
+            const int e = tl.n0 + c + i;
             if (e < p.E) topk_insert(bv, bi, v[i] + (p.bias ? p.bias[e] : 0.0f), e);
           }
         }
+        // the accumulator is free once read
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
         if (valid) {
           const int t = tl.a_row + r;
-          float ex[kMaxTopK];
-          float s = 0.0f;
+          const long long cbase = (static_cast<long long>(t) * p.nq + tl.n0 / BN) * kMaxTopK;
+          float4 *cv = reinterpret_cast<float4 *>(p.cand_v + cbase);
+          int4 *ci = reinterpret_cast<int4 *>(p.cand_i + cbase);
+          cv[0] = make_float4(bv[0], bv[1], bv[2], bv[3]);
+          cv[1] = make_float4(bv[4], bv[5], bv[6], bv[7]);
+          ci[0] = make_int4(bi[0], bi[1], bi[2], bi[3]);
+          ci[1] = make_int4(bi[4], bi[5], bi[6], bi[7]);
+          __threadfence();
+          // the last of the token's nq expert blocks merges the candidates
+          if (atomicAdd(p.tok_cnt + t, 1) == p.nq - 1) {
+            __threadfence();
 #pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            ex[j] = (j < p.k) ? expf(bv[j] - bv[0]) : 0.0f;
-            s += ex[j];
-          }
-          const float inv_s = 1.0f / s;
+            for (int j = 0; j < kMaxTopK; ++j) {
+              bv[j] = -INFINITY;
+              bi[j] = 0;
+            }
+            // expert blocks in increasing order, each list by descending value
+            // with ties in increasing index: equal values keep the lower index
+            const long long tb0 = static_cast<long long>(t) * p.nq * kMaxTopK;
+            for (int q = 0; q < p.nq; ++q) {
+              const float4 *qv = reinterpret_cast<const float4 *>(p.cand_v + tb0 + q * kMaxTopK);
+              const int4 *qi = reinterpret_cast<const int4 *>(p.cand_i + tb0 + q * kMaxTopK);
+              const float4 v0 = __ldcg(qv), v1 = __ldcg(qv + 1);
+              const int4 i0 = __ldcg(qi), i1 = __ldcg(qi + 1);
+              topk_insert(bv, bi, v0.x, i0.x);
+              topk_insert(bv, bi, v0.y, i0.y);
+              topk_insert(bv, bi, v0.z, i0.z);
+              topk_insert(bv, bi, v0.w, i0.w);
+              topk_insert(bv, bi, v1.x, i1.x);
+              topk_insert(bv, bi, v1.y, i1.y);
+              topk_insert(bv, bi, v1.z, i1.z);
+              topk_insert(bv, bi, v1.w, i1.w);
+            }
+            p.tok_cnt[t] = 0;  // ready for the next call
+            float ex[kMaxTopK];
+            float s = 0.0f;
 #pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < p.k) {
-              const long long o = static_cast<long long>(t) * p.k + j;
-              p.idx[o] = bi[j];
-              p.w[o] = ex[j] * inv_s;
-              const int rk = atomicAdd(p.counts + bi[j], 1);
-              if (p.rank) p.rank[o] = rk;
+            for (int j = 0; j < kMaxTopK; ++j) {
+              ex[j] = (j < p.k) ? expf(bv[j] - bv[0]) : 0.0f;
+              s += ex[j];
+            }
+            const float inv_s = 1.0f / s;
+            // ranks inside each expert's group: lanes that chose the same
+            // expert share one atomic on its (line-padded) counter; all k
+            // atomics are issued before any result is used
+            const unsigned act = __activemask();
+            unsigned peers[kMaxTopK];
+            int base[kMaxTopK];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+              base[j] = 0;
+              if (j < p.k) {
+                const long long o = static_cast<long long>(t) * p.k + j;
+                p.idx[o] = bi[j];
+                p.w[o] = ex[j] * inv_s;
+                peers[j] = __match_any_sync(act, bi[j]);
+                if (lane == __ffs(peers[j]) - 1)
+                  base[j] = atomicAdd(p.counts + static_cast<long long>(bi[j]) * kCountStride,
+                                      __popc(peers[j]));
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+              if (j < p.k) {
+                const int b = __shfl_sync(act, base[j], __ffs(peers[j]) - 1);
+                if (p.rank)
+                  p.rank[static_cast<long long>(t) * p.k + j] =
+                      b + __popc(peers[j] & ((1u << lane) - 1u));
+              }
             }
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+      if (!kRouter) {
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -459,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 
-  if (kRouter && p.offsets_out) {
+  if (kRouter && (p.offsets_out || p.counts_out)) {
     // the last CTA to finish turns the histogram into group offsets
     __threadfence();
     __syncthreads();
@@ -474,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sum = 0;
       for (int q = 0; q < per; ++q) {
         const int e = lane * per + q;
-        if (e < E) sum += __ldcg(p.counts + e);
+        if (e < E) sum += __ldcg(p.counts + static_cast<long long>(e) * kCountStride);
       }
       int incl = sum;
 #pragma unroll
@@ -486,44 +550,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < per; ++q) {
         const int e = lane * per + q;
         if (e < E) {
-          p.offsets_out[e] = run;
-          run += __ldcg(p.counts + e);
+          const int ce = __ldcg(p.counts + static_cast<long long>(e) * kCountStride);
+          if (p.offsets_out) p.offsets_out[e] = run;
+          if (p.counts_out) p.counts_out[e] = ce;
+          run += ce;
         }
       }
-      if (lane == 31) p.offsets_out[E] = incl;
+      if (lane == 31 && p.offsets_out) p.offsets_out[E] = incl;
     }
   }
 }
 
-template <typename T, int EPI>
+template <typename T, int EPI, int BN>
 cudaError_t gemm_set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_kernel<T, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_kernel<T, EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kGemmSmem);
 }
 
-template <typename T, int EPI>
+template <typename T, int EPI, int BN>
 cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;
-  gemm_kernel<T, EPI><<<grid, kThreads, kGemmSmem, st>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3],
-                                                          maps.m[4], maps.m[5], p);
+  gemm_kernel<T, EPI, BN><<<grid, kThreads, kGemmSmem, st>>>(maps.m[0], maps.m[1], maps.m[2],
+                                                              maps.m[3], maps.m[4], maps.m[5], p);
   return cudaGetLastError();
 }
 
-template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU>();
-template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_STORE>();
-template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER>();
-template cudaError_t gemm_set_smem_attr<float, EPI_SWIGLU>();
-template cudaError_t gemm_set_smem_attr<float, EPI_STORE>();
-template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU>(const GemmMaps &, const GemmParams &, int,
-                                                             cudaStream_t);
-template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE>(const GemmMaps &, const GemmParams &, int,
-                                                            cudaStream_t);
-template cudaError_t launch_gemm<__nv_bfloat16, EPI_ROUTER>(const GemmMaps &, const GemmParams &, int,
-                                                             cudaStream_t);
-template cudaError_t launch_gemm<float, EPI_SWIGLU>(const GemmMaps &, const GemmParams &, int,
-                                                     cudaStream_t);
-template cudaError_t launch_gemm<float, EPI_STORE>(const GemmMaps &, const GemmParams &, int,
-                                                    cudaStream_t);
+template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN>();
+template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_STORE, kBN>();
+template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>();
+template cudaError_t gemm_set_smem_attr<float, EPI_SWIGLU, kBN>();
+template cudaError_t gemm_set_smem_attr<float, EPI_STORE, kBN>();
+template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &,
+                                                                  int, cudaStream_t);
+template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &,
+                                                                 int, cudaStream_t);
+template cudaError_t launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(const GemmMaps &,
+                                                                        const GemmParams &, int,
+                                                                        cudaStream_t);
+template cudaError_t launch_gemm<float, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &, int,
+                                                          cudaStream_t);
+template cudaError_t launch_gemm<float, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &, int,
+                                                         cudaStream_t);
 
 // ---------------------------------------------------------------- test hook
 // Waits on an mbarrier that nothing signals, with the same bounded wait the

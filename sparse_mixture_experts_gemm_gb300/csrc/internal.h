@@ -21,11 +21,13 @@ static_assert(sizeof(GemmTile) == 32, "tile record is 32 bytes");
 enum Epilogue { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_ROUTER = 2 };
 
 constexpr int kBM = 128;      // rows per tile (TMEM lanes)
-constexpr int kBN = 256;      // MMA N: B rows per tile
-constexpr int kStages = 4;    // smem pipeline depth
+constexpr int kBN = 256;      // MMA N: B rows per tile of the expert GEMMs
+constexpr int kRouterBN = 64; // experts per router tile (E split into E / 64 blocks)
+constexpr int kStageBudget = 4 * (kBM * 128 + kBN * 128);  // smem for the operand stages
 constexpr int kThreads = 192; // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
 constexpr int kGemmCtrl = 4096;  // barriers, TMEM slot, row tokens, group table
-constexpr int kGemmSmem = kStages * (kBM * 128 + kBN * 128) + 1024 + kGemmCtrl;
+constexpr int kGemmSmem = kStageBudget + 1024 + kGemmCtrl;
+constexpr int kCountStride = 32;  // router histogram: one counter per 128-byte line
 constexpr int kMaxTopK = 8;
 
 struct GemmParams {
@@ -49,9 +51,14 @@ struct GemmParams {
   const float *bias;
   int32_t *idx;
   float *w;
-  int32_t *counts;         // [E], zeroed before the launch
+  int32_t *counts;         // [E * kCountStride], zeroed before the launch
+  int32_t *counts_out;     // [E] dense copy written by the last CTA (may be null)
   int32_t *rank;           // [T * k] rank of each assignment inside its group (may be null)
   int32_t *offsets_out;    // [E + 1] written by the last CTA (may be null)
+  int nq;                  // expert blocks per token (ceil(E / kRouterBN))
+  float *cand_v;           // [T][nq][kMaxTopK] per-block top-k candidates
+  int32_t *cand_i;
+  int32_t *tok_cnt;        // [T] blocks finished per token, zero between calls
   unsigned *done;          // CTA completion ticket, zeroed before the launch
 };
 
@@ -61,9 +68,9 @@ struct GemmMaps {
 };
 
 // gemm.cu
-template <typename T, int EPI>
+template <typename T, int EPI, int BN>
 cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
-template <typename T, int EPI>
+template <typename T, int EPI, int BN>
 cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
@@ -84,6 +91,25 @@ template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);
 
+// decode_layer.cu: the fused batch-1 layer kernel's work split and shared
+// memory plan, computed on the host when the handle is created.  Byte offsets
+// are from the kernel's 128-byte aligned dynamic shared memory base.
+constexpr int kLayerThreads = 288;  // warps 0-7 compute, warp 8 issues the copies
+struct DecodePlan {
+  int ok;            // 1 when these dimensions fit the fused kernel
+  int grid;          // CTAs, one per SM
+  int max_rr;        // router rows per CTA (upper bound)
+  int max_sr;        // shared-expert gate/up rows per CTA
+  int max_or;        // output rows per CTA
+  int ring;          // ring slots, one (gate row, up row) pair each
+  int off_x;         // the token [d]
+  int off_u;         // union: router + shared rows, then the ring, then partial sums
+  int off_wd;        // routed down rows [k][max_or][F]
+  int off_sd;        // shared down rows [max_or][F]
+  int smem;          // dynamic shared memory bytes to request
+};
+DecodePlan make_decode_plan(int d, int F, int E, int k, int n_shared, int esz, int sms);
+
 // decode.cu
 struct DecodeArgs {
   const void *x;
@@ -101,7 +127,12 @@ struct DecodeArgs {
   int rows_a;          // kernel A: router rows or shared items per CTA
   int ring;            // kernel B: ring slots per CTA
   int c_rows;          // kernel C: output rows per CTA (upper bound)
+  // fused layer kernel
+  unsigned *gbar;      // [2] grid barrier: arrivals, generation
+  DecodePlan plan;
 };
+template <typename T>
+cudaError_t launch_decode_layer(const DecodeArgs &a, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
 // tmG / tmU: w_gate / w_up as [E * F][d] with boxes of (512 bytes) x 32 rows, no swizzle

@@ -87,6 +87,9 @@ struct ProfRec {
 
 }  // namespace
 
+constexpr int kRouteCtlCounts = 256 * kCountStride;
+constexpr size_t kRouteCtlBytes = sizeof(int32_t) * (kRouteCtlCounts + 4);
+
 struct moe_handle {
   moe_config cfg;
   int device = 0;
@@ -97,9 +100,14 @@ struct moe_handle {
   void *ws = nullptr;
   int32_t *idx = nullptr, *inv = nullptr, *offsets = nullptr, *status = nullptr,
           *sel = nullptr;
-  int32_t *route_ctl = nullptr;  // [256] per-expert counts, then [4] the router's CTA ticket
+  // [256 * kCountStride] per-expert counts (line-padded for the bf16 router,
+  // dense for the fp32 one), then [4] the router's CTA ticket
+  int32_t *route_ctl = nullptr;
   float *w = nullptr, *logits = nullptr, *selw = nullptr, *hdec = nullptr;
   unsigned *counter = nullptr;
+  float *cand_v = nullptr;     // router: per expert block top-k candidates
+  int32_t *cand_i = nullptr;
+  int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
   void *xp = nullptr, *hbuf = nullptr, *yp = nullptr;
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
@@ -110,7 +118,7 @@ struct moe_handle {
   std::vector<cudaEvent_t> pool;
   size_t pool_used = 0;
   int32_t *counts() { return route_ctl; }
-  unsigned *done() { return reinterpret_cast<unsigned *>(route_ctl + 256); }
+  unsigned *done() { return reinterpret_cast<unsigned *>(route_ctl + kRouteCtlCounts); }
 };
 
 namespace {
@@ -177,18 +185,23 @@ struct ProfScope {
 
 // The bf16 router: tcgen05 logits with top-k, weights, ranks and the
 // per-expert histogram in the epilogue; the last CTA writes the offsets.
-int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w, int32_t *counts,
-                     int32_t *rank, int32_t *offsets, cudaStream_t st) {
+int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w, int32_t *rank,
+                     int32_t *offsets, int32_t *counts_out, cudaStream_t st) {
   const moe_config &c = h->cfg;
   CUtensorMap tm_x;
   if (!make_map(&tm_x, x, 2, T, c.d_model, kBM)) return MOE_ERR_CUDA;
   const int nblk = (T + kBM - 1) / kBM;
+  const int nq = (c.n_experts + kRouterBN - 1) / kRouterBN;
   GemmMaps m;
   m.m[0] = m.m[1] = tm_x;
   m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
   GemmParams p = {};
   p.T = T;
-  p.ntiles_host = nblk;
+  p.ntiles_host = nblk * nq;
+  p.nq = nq;
+  p.cand_v = h->cand_v;
+  p.cand_i = h->cand_i;
+  p.tok_cnt = h->tok_cnt;
   p.num_k_blocks = c.d_model / 64;
   p.n_routed = c.n_experts;
   p.status = h->status;
@@ -198,11 +211,15 @@ int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w
   p.bias = c.router_bias;
   p.idx = idx;
   p.w = w;
-  p.counts = counts;
+  p.counts = h->counts();
+  p.counts_out = counts_out;
   p.rank = rank;
   p.offsets_out = offsets;
   p.done = h->done();
-  MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER>(m, p, nblk < h->num_sms ? nblk : h->num_sms, st)));
+  const int tiles = nblk * nq;
+  MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(m, p,
+                                                             tiles < h->num_sms ? tiles : h->num_sms,
+                                                             st)));
   return MOE_OK;
 }
 
@@ -213,11 +230,11 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   const int A = Tc * k;
   const int BK = static_cast<int>(128 / sizeof(T));
 
-  MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, sizeof(int32_t) * 260, st));
+  MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, kRouteCtlBytes, st));
   {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
-      const int rc = launch_router_tc(h, x, Tc, h->idx, h->w, h->counts(), h->inv, h->offsets, st);
+      const int rc = launch_router_tc(h, x, Tc, h->idx, h->w, h->inv, h->offsets, nullptr, st);
       if (rc != MOE_OK) return rc;
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
@@ -254,7 +271,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.out = h->hbuf;
     p.ldo = F;
     p.kid = KID_GEMM_GATE_UP;
-    MOE_TRY((launch_gemm<T, EPI_SWIGLU>(m, p, h->num_sms, st)));
+    MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
   }
   {
     ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
@@ -269,7 +286,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.out = h->yp;
     p.ldo = d;
     p.kid = KID_GEMM_DOWN;
-    MOE_TRY((launch_gemm<T, EPI_STORE>(m, p, h->num_sms, st)));
+    MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st)));
   }
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
@@ -322,8 +339,8 @@ int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
 
 template <typename T>
 int set_attrs(const moe_config &c) {
-  if (gemm_set_smem_attr<T, EPI_SWIGLU>() != cudaSuccess) return MOE_ERR_CUDA;
-  if (gemm_set_smem_attr<T, EPI_STORE>() != cudaSuccess) return MOE_ERR_CUDA;
+  if (gemm_set_smem_attr<T, EPI_SWIGLU, kBN>() != cudaSuccess) return MOE_ERR_CUDA;
+  if (gemm_set_smem_attr<T, EPI_STORE, kBN>() != cudaSuccess) return MOE_ERR_CUDA;
   if (decode_set_smem_attr<T>() != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -367,6 +384,7 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k, Tm = c.max_tokens;
   const size_t A = static_cast<size_t>(Tm) * k;
   const size_t esz = h->esz;
+  const size_t nqk = static_cast<size_t>((E + kRouterBN - 1) / kRouterBN) * kMaxTopK;
 
   // carve the workspace
   struct Part {
@@ -377,7 +395,7 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
       {reinterpret_cast<void **>(&h->idx), sizeof(int32_t) * A},
       {reinterpret_cast<void **>(&h->w), sizeof(float) * A},
       {reinterpret_cast<void **>(&h->inv), sizeof(int32_t) * A},
-      {reinterpret_cast<void **>(&h->route_ctl), sizeof(int32_t) * 260},
+      {reinterpret_cast<void **>(&h->route_ctl), kRouteCtlBytes},
       {reinterpret_cast<void **>(&h->offsets), sizeof(int32_t) * (E + 1)},
       {reinterpret_cast<void **>(&h->status), sizeof(int32_t) * 4},
       {reinterpret_cast<void **>(&h->sel), sizeof(int32_t) * kMaxTopK},
@@ -385,6 +403,9 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
       {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
       {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
       {reinterpret_cast<void **>(&h->counter), sizeof(unsigned) * 4},
+      {reinterpret_cast<void **>(&h->cand_v), sizeof(float) * nqk * Tm},
+      {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
+      {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},
       {&h->xp, esz * A * d},
       {&h->hbuf, esz * (A + Tm) * F},
       {&h->yp, esz * (A + Tm) * d},
@@ -417,7 +438,7 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
             make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
             make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
             make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN) &&
-            make_map(&h->tm_wr, c.w_router, esz, E, d, kBN);
+            make_map(&h->tm_wr, c.w_router, esz, E, d, kRouterBN);
   if (ok && c.n_shared)
     ok = make_map(&h->tm_sg, c.s_gate, esz, F, d, kBM) &&
          make_map(&h->tm_su, c.s_up, esz, F, d, kBM) && make_map(&h->tm_sd, c.s_down, esz, d, F, kBN);
@@ -427,7 +448,7 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
   }
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
-      gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER>() != cudaSuccess)
+      gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess)
     rc = MOE_ERR_CUDA;
   if (rc != MOE_OK) {
     moe_destroy(h);
@@ -456,11 +477,12 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const moe_config &c = h->cfg;
   const int d = c.d_model, E = c.n_experts, k = c.top_k;
-  MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
-  MOE_TRY(cudaMemsetAsync(h->done(), 0, sizeof(unsigned) * 4, st));
   ProfScope ps(h, MOE_KERNEL_ROUTER, st);
-  if (c.dtype == MOE_BF16) return launch_router_tc(h, x, T, topk_idx, topk_w, counts, nullptr,
-                                                   nullptr, st);
+  if (c.dtype == MOE_BF16) {
+    MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, kRouteCtlBytes, st));
+    return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, counts, st);
+  }
+  MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
   MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),
                                     static_cast<const float *>(c.w_router), c.router_bias, T, d, E,
                                     k, topk_idx, topk_w, counts, nullptr, st));
@@ -505,6 +527,10 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
   int s[2] = {0, 0};
   if (cudaMemcpy(s, h->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->status, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
+  // an aborted router leaves per-token arrival counts behind
+  if (s[0] != MOE_OK &&
+      cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (detail) *detail = s[1];
   return s[0];
 }
