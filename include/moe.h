@@ -55,11 +55,10 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
 typedef struct moe_handle moe_handle; /* opaque, owned by the library */
 
 /*
- * Shapes and weights of one MoE layer.  Supported: d_model a multiple of 64 in
- * [64, 16384]; d_ff a multiple of 128 in [128, 4096]; n_experts in [1, 256];
- * top_k in [1, min(n_experts, 16)]; n_shared 0 or 1; max_tokens in
- * [1, 65536].  The prefill kernels of the bf16 path additionally need
- * n_experts <= 256 (the router tile holds all logits of a token).
+ * Shapes and weights of one MoE layer.  Supported: d_model a multiple of 256
+ * in [256, 16384]; d_ff a multiple of 128 in [128, 4096]; n_experts in
+ * [1, 256]; top_k in [1, min(n_experts, 8)]; n_shared 0 or 1; max_tokens in
+ * [1, 65536]; anything else returns MOE_ERR_UNSUPPORTED from moe_create.
  *
  * Weight layouts (all K-contiguous, i.e. the reduction index is innermost):
  *   w_router [E][d]          (the transpose of the mathematical x.Wr shape)

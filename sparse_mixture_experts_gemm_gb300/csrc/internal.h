@@ -91,25 +91,6 @@ template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);
 
-// decode_layer.cu: the fused batch-1 layer kernel's work split and shared
-// memory plan, computed on the host when the handle is created.  Byte offsets
-// are from the kernel's 128-byte aligned dynamic shared memory base.
-constexpr int kLayerThreads = 288;  // warps 0-7 compute, warp 8 issues the copies
-struct DecodePlan {
-  int ok;            // 1 when these dimensions fit the fused kernel
-  int grid;          // CTAs, one per SM
-  int max_rr;        // router rows per CTA (upper bound)
-  int max_sr;        // shared-expert gate/up rows per CTA
-  int max_or;        // output rows per CTA
-  int ring;          // ring slots, one (gate row, up row) pair each
-  int off_x;         // the token [d]
-  int off_u;         // union: router + shared rows, then the ring, then partial sums
-  int off_wd;        // routed down rows [k][max_or][F]
-  int off_sd;        // shared down rows [max_or][F]
-  int smem;          // dynamic shared memory bytes to request
-};
-DecodePlan make_decode_plan(int d, int F, int E, int k, int n_shared, int esz, int sms);
-
 // decode.cu
 struct DecodeArgs {
   const void *x;
@@ -127,12 +108,7 @@ struct DecodeArgs {
   int rows_a;          // kernel A: router rows or shared items per CTA
   int ring;            // kernel B: ring slots per CTA
   int c_rows;          // kernel C: output rows per CTA (upper bound)
-  // fused layer kernel
-  unsigned *gbar;      // [2] grid barrier: arrivals, generation
-  DecodePlan plan;
 };
-template <typename T>
-cudaError_t launch_decode_layer(const DecodeArgs &a, cudaStream_t st, bool pdl);
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
 // tmG / tmU: w_gate / w_up as [E * F][d] with boxes of (512 bytes) x 32 rows, no swizzle

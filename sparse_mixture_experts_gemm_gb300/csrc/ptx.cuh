@@ -216,57 +216,4 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   return v;
 }
 
-// ---------------------------------------------------------------- bulk copies
-// Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses
-// 16-byte aligned) completing `bar`'s transaction count.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- grid barrier
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Barrier over every CTA of the grid (all of them resident): bar[0] counts
-// arrivals, bar[1] is the generation.  The last CTA to arrive resets the
-// count and advances the generation; the others spin on the generation for at
-// most `limit` cycles.  Every CTA arrives, even after an error, so one failing
-// CTA cannot strand the rest.  Returns false (thread 0's view, broadcast
-// through *abort) when the wait ran out.
-__device__ __forceinline__ void grid_sync(unsigned *bar, unsigned nblocks, long long limit,
-                                          volatile int *abort, int *status, int detail) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_gpu(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1u) == nblocks - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      st_release_gpu(bar + 1, gen + 1u);
-    } else {
-      const long long t0 = clock64();
-      while (ld_acquire_gpu(bar + 1) == gen) {
-        if (clock64() - t0 > limit) {
-          *abort = 1;
-          report_error(status, MOE_ERR_DEVICE_TIMEOUT, detail);
-          break;
-        }
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-}
-
 }  // namespace moe

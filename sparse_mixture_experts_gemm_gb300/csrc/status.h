@@ -23,9 +23,6 @@ enum WaitSite {
   SITE_DRAIN = 5,           // final wait for in-flight copies / MMAs
   SITE_INDEX = 6,           // an index check failed
   SITE_DEBUG = 7,           // the test hook's never-signalled barrier
-  SITE_GRID_LOGITS = 8,     // fused decode: grid barrier after the router logits
-  SITE_GRID_H = 9,          // fused decode: grid barrier after the gate/up rows
-  SITE_WEIGHTS = 10,        // fused decode: waiting for preloaded weights
 };
 
 }  // namespace moe
