@@ -180,14 +180,14 @@ int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
  * overlapping.  Result: out = MoE(x), computed by the same decode kernels as
  * moe_forward with T == 1.
  *
- * Scratch: one static device array of 66,048 bytes inside the library, which
+ * Scratch: one static device array of 66,560 bytes inside the library, which
  * every GPU that loads the library holds until the process exits.  It limits
  * (top_k + n_shared) * d_ff to 16384; larger layers return
  * MOE_ERR_UNSUPPORTED, as do the limits of moe_create.  The first call on a
  * device looks up the array's device address (once per device, with that
  * device current), so make that first call before any stream capture.  All
- * calls share the array and it keeps the last call's contents (the call
- * clears what must start at zero itself): calls that overlap on the GPU, on
+ * calls share the array, and every call writes each value it reads (nothing
+ * carries over from the last call): calls that overlap on the GPU, on
  * different streams or from different threads, race on it and must be
  * serialised by the caller.
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.  Asynchronous on

@@ -57,7 +57,7 @@ __device__ __forceinline__ void row_prefetch(RowPre &r, const uint4 *row, int nv
 }
 
 // dot(row, x) for a row whose first 32 * kPre vectors are in r; the rest (rows
-// longer than 256 vectors) are streamed here.
+// longer than 256 vectors) are streamed here.  xv: the token in shared memory.
 template <typename T>
 __device__ __forceinline__ float row_dot_pre(const RowPre &r, const uint4 *row, const uint4 *xv,
                                              int nvec, int lane) {
@@ -65,10 +65,18 @@ __device__ __forceinline__ float row_dot_pre(const RowPre &r, const uint4 *row, 
 #pragma unroll
   for (int u = 0; u < kPre; ++u) {
     const int i = u * 32 + lane;
-    if (i < nvec) acc += V16<T>::dot(r.v[u], __ldg(xv + i));
+    if (i < nvec) acc += V16<T>::dot(r.v[u], xv[i]);
   }
-  for (int i = 32 * kPre + lane; i < nvec; i += 32) acc += V16<T>::dot(ld_stream16(row + i), __ldg(xv + i));
+  for (int i = 32 * kPre + lane; i < nvec; i += 32) acc += V16<T>::dot(ld_stream16(row + i), xv[i]);
   return acc;
+}
+
+// The token into shared memory (all threads; L2 reads, written by the kernel
+// this one waited for), once per CTA rather than once per warp.
+__device__ __forceinline__ void load_token(uint4 *xs, const void *x, int nvec) {
+  const uint4 *xg = static_cast<const uint4 *>(x);
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  __syncthreads();
 }
 
 }  // namespace
@@ -81,7 +89,8 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
   const int n_rt = (a.E + 7) / 8;
-  const uint4 *xv = reinterpret_cast<const uint4 *>(a.x);
+  extern __shared__ uint4 xs_a[];  // the token, one copy per CTA
+  const uint4 *xv = xs_a;
   if (static_cast<int>(blockIdx.x) >= n_rt) {
     const int c = blockIdx.x - n_rt;
     const int f = c * 8 + warp;
@@ -101,6 +110,7 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
     }
     pdl_launch_dependents();  // kernel B reads nothing of ours before its wait
     pdl_wait();
+    load_token(xs_a, a.x, nvec);
     if (f >= a.F) return;
     float g = warp_sum(row_dot_pre<T>(pg, rg, xv, nvec, lane));
     float u = warp_sum(row_dot_pre<T>(pu, ru, xv, nvec, lane));
@@ -114,6 +124,7 @@ __global__ void __launch_bounds__(256) decode_router_kernel(const DecodeArgs a) 
   if (e < a.E) row_prefetch(pr, row, nvec, lane);
   pdl_launch_dependents();  // kernel B reads nothing of ours before its wait
   pdl_wait();
+  load_token(xs_a, a.x, nvec);
   if (e < a.E) {
     const float acc = warp_sum(row_dot_pre<T>(pr, row, xv, nvec, lane));
     if (lane == 0) a.logits[e] = acc + (a.bias ? a.bias[e] : 0.0f);
@@ -162,7 +173,8 @@ __global__ void __launch_bounds__(288, 1)
   if (warp == 0) warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
   uint4 *xs = reinterpret_cast<uint4 *>(dsm + kBStages * 2 * kBBox);
   const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
-  for (int i = threadIdx.x; i < a.d * static_cast<int>(sizeof(T)) / 16; i += blockDim.x) xs[i] = xg[i];
+  for (int i = threadIdx.x; i < a.d * static_cast<int>(sizeof(T)) / 16; i += blockDim.x)
+    xs[i] = __ldcg(xg + i);
   __syncthreads();
   pdl_launch_dependents();
   if (warp == 8) {
@@ -328,7 +340,8 @@ cudaError_t launch_ex(K kern, int grid, int block, size_t smem, cudaStream_t st,
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl) {
   const int grid = (a.E + 7) / 8 + (a.n_shared ? (a.F + 7) / 8 : 0);
-  return launch_ex(decode_router_kernel<T>, grid, 256, 0, st, pdl, a);
+  return launch_ex(decode_router_kernel<T>, grid, 256, static_cast<size_t>(a.d) * sizeof(T), st,
+                   pdl, a);
 }
 template <typename T>
 cudaError_t launch_decode_gateup(const DecodeArgs &a, const CUtensorMap &tmG, const CUtensorMap &tmU,
@@ -362,6 +375,10 @@ cudaError_t launch_decode_down(const DecodeArgs &a, cudaStream_t st, bool pdl) {
 // down kernel keeps h of all slots in shared memory.
 template <typename T>
 cudaError_t decode_set_smem_attr() {
+  const cudaError_t e0 = cudaFuncSetAttribute(decode_router_kernel<T>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              16384 * static_cast<int>(sizeof(T)));
+  if (e0 != cudaSuccess) return e0;
   const cudaError_t e = cudaFuncSetAttribute(
       decode_down_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (kMaxTopK + 1) * 4096 * static_cast<int>(sizeof(float)));

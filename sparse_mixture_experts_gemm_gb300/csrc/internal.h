@@ -98,10 +98,7 @@ struct DecodeArgs {
   const float *bias;
   int d, F, E, k, n_shared;
   float *logits;       // [E]
-  int32_t *sel;        // [k]
-  float *selw;         // [k]
   float *h;            // [(k + 1)][F]
-  unsigned *counter;   // last-block-done ticket, zero between launches
   void *out;           // [d]
   int *status;
   // launch shape, filled in by the launchers

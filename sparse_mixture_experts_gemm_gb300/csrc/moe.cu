@@ -98,13 +98,11 @@ struct moe_handle {
   int nt1 = 0, nt2 = 0;  // N tiles of the gate/up and down GEMMs
   // workspace (one allocation)
   void *ws = nullptr;
-  int32_t *idx = nullptr, *inv = nullptr, *offsets = nullptr, *status = nullptr,
-          *sel = nullptr;
+  int32_t *idx = nullptr, *inv = nullptr, *offsets = nullptr, *status = nullptr;
   // [256 * kCountStride] per-expert counts (line-padded for the bf16 router,
   // dense for the fp32 one), then [4] the router's CTA ticket
   int32_t *route_ctl = nullptr;
-  float *w = nullptr, *logits = nullptr, *selw = nullptr, *hdec = nullptr;
-  unsigned *counter = nullptr;
+  float *w = nullptr, *logits = nullptr, *hdec = nullptr;
   float *cand_v = nullptr;     // router: per expert block top-k candidates
   int32_t *cand_i = nullptr;
   int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
@@ -315,10 +313,7 @@ int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
   a.k = c.top_k;
   a.n_shared = c.n_shared;
   a.logits = h->logits;
-  a.sel = h->sel;
-  a.selw = h->selw;
   a.h = h->hdec;
-  a.counter = h->counter;
   a.out = out;
   a.status = h->status;
   const bool pdl = !h->prof;  // event records between kernels would break the chain
@@ -398,11 +393,8 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
       {reinterpret_cast<void **>(&h->route_ctl), kRouteCtlBytes},
       {reinterpret_cast<void **>(&h->offsets), sizeof(int32_t) * (E + 1)},
       {reinterpret_cast<void **>(&h->status), sizeof(int32_t) * 4},
-      {reinterpret_cast<void **>(&h->sel), sizeof(int32_t) * kMaxTopK},
-      {reinterpret_cast<void **>(&h->selw), sizeof(float) * kMaxTopK},
       {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
       {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
-      {reinterpret_cast<void **>(&h->counter), sizeof(unsigned) * 4},
       {reinterpret_cast<void **>(&h->cand_v), sizeof(float) * nqk * Tm},
       {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
       {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},

@@ -10,11 +10,11 @@
 // in one file-scope device array below that every GPU loading this library
 // holds until the process exits.
 //
-// Scratch layout (floats): [0, 256) router logits, [256, 264) chosen expert
-// ids (as int32), [264, 272) their weights, [272, 276) the router's
-// last-block-done counter (cleared by every call), [512, 512 + kNoAllocMaxH)
-// the intermediate h of the k routed experts and the shared one.  The pages describe no allocation-free mode;
-// this has no counterpart there.
+// Scratch layout (floats): [0, 256) router logits, [256, 256 + kNoAllocMaxH)
+// the intermediate h of the k routed experts and the shared one.  Every
+// value is written before it is read within one call, so nothing needs
+// clearing between calls.  The pages describe no allocation-free mode; this
+// has no counterpart there.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,7 +27,7 @@ namespace moe {
 namespace {
 
 constexpr int kNoAllocMaxH = 16384;                  // (top_k + n_shared) * d_ff at most
-constexpr int kNoAllocFloats = 512 + kNoAllocMaxH;   // 66,048 bytes
+constexpr int kNoAllocFloats = 256 + kNoAllocMaxH;   // 66,560 bytes
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
@@ -107,14 +107,9 @@ extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
   a.k = c->top_k;
   a.n_shared = c->n_shared;
   a.logits = s;
-  a.sel = reinterpret_cast<int32_t *>(s + 256);
-  a.selw = s + 264;
-  a.counter = reinterpret_cast<unsigned *>(s + 272);
-  a.h = s + 512;
+  a.h = s + 256;
   a.out = out;
   a.status = nullptr;
-  // the router's last-block-done counter must start at zero
-  if (cudaMemsetAsync(a.counter, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
   const bool bf16 = c->dtype == MOE_BF16;
   if ((bf16 ? launch_decode_router<__nv_bfloat16>(a, st, false)
             : launch_decode_router<float>(a, st, false)) != cudaSuccess)

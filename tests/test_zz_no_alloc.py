@@ -3,8 +3,8 @@
 It serves callers that cannot allocate device memory (and therefore cannot
 create a handle, since moe_create allocates the workspace): its scratch is a
 static array inside the library.  Its output must match the handle-based
-moe_forward with T == 1 on consecutive calls, since the array keeps the
-previous call's contents and the call must clear what has to start at zero.
+moe_forward with T == 1 on consecutive calls: the array keeps the previous
+call's contents, and no value of one call may leak into the next.
 This file is collected last so that a failure here does not hide the others.
 """
 import ctypes
