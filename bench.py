@@ -117,6 +117,11 @@ def make_layer(cfg: dict, dev, seed: int):
     return layer, w, bias
 
 
+# DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
+# ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
+GEMM1_TRAFFIC_4K = 1_273_021_000 + 24_782_336
+
+
 def algorithmic_prefill(cfg: dict, counts: np.ndarray, T: int) -> dict:
     """Algorithmic work of one prefill pass: FLOPs and the minimum HBM bytes
     (weights of every expert with at least one row + shared + router, x read
@@ -411,7 +416,8 @@ def main():
         "roofline": {
             "kernel": "grouped gate/up GEMM + SiLU (gemm_kernel<bf16, EPI_SWIGLU>)",
             "bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-            "frac": achieved / pk["hbm"], "traffic": None,
+            "frac": achieved / pk["hbm"],
+            "traffic": GEMM1_TRAFFIC_4K if wl_name == "prefill4k" else None,
             "peak_source": f"{pk['src']} hbm_gbs",
             "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_ms": g1_avg,
             "tensor_frac_of_measured_burst": g1_flops / (g1_avg / 1e3) / (pk["bf16"] * 1e12),
@@ -463,7 +469,8 @@ def decode_summary(dec, pk) -> dict:
         "workload": "batch-1 decode: one fresh token per step through 40 distinct layers "
                     "(d=2048, 256 experts top-8 + 1 shared, F=512, bf16), CUDA graph per step",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm"], "traffic": None,
+                     "frac": achieved / pk["hbm"],
+            "traffic": GEMM1_TRAFFIC_4K if wl_name == "prefill4k" else None,
                      "algorithmic_bytes_per_layer": byts,
                      "peak_source": f"{pk['src']} hbm_gbs"},
         "eager_us_per_launch": split,
