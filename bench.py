@@ -117,6 +117,9 @@ def make_layer(cfg: dict, dev, seed: int):
     return layer, w, bias
 
 
+# DRAM bytes of one batch-1 layer (kernels A + B + C, reads; nothing is
+# written back during them), from the ncu capture in profiles/decode_layer.md.
+DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
 # ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
 GEMM1_TRAFFIC_4K = 1_273_021_000 + 24_782_336
@@ -469,8 +472,7 @@ def decode_summary(dec, pk) -> dict:
         "workload": "batch-1 decode: one fresh token per step through 40 distinct layers "
                     "(d=2048, 256 experts top-8 + 1 shared, F=512, bf16), CUDA graph per step",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm"],
-            "traffic": GEMM1_TRAFFIC_4K if wl_name == "prefill4k" else None,
+                     "frac": achieved / pk["hbm"], "traffic": DECODE_TRAFFIC_LAYER,
                      "algorithmic_bytes_per_layer": byts,
                      "peak_source": f"{pk['src']} hbm_gbs"},
         "eager_us_per_launch": split,

@@ -274,25 +274,45 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ yp,
   const int t = static_cast<int>(gid / vpr);
   const int c = static_cast<int>(gid % vpr);
   if (t >= T_tok) return;
+  // every slot and weight first, then every row vector, so all of the
+  // thread's loads are in flight together; the sum keeps the fixed order
+  int slot[kMaxTopK];
+  float wt[kMaxTopK];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    slot[j] = 0;
+    wt[j] = 0.0f;
+    if (j < k) {
+      slot[j] = inv[static_cast<long long>(t) * k + j];
+      wt[j] = w[static_cast<long long>(t) * k + j];
+      bad = bad || slot[j] < 0 || slot[j] >= A_total;
+    }
+  }
+  if (bad) {
+    report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_COMBINE * 100 + SITE_INDEX);
+    return;
+  }
+  uint4 v[kMaxTopK + 1];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) v[j] = ld_stream16(yp + static_cast<long long>(slot[j]) * d + c * NV);
+  if (n_shared) v[kMaxTopK] = ld_stream16(yp + static_cast<long long>(A_total + t) * d + c * NV);
   float acc[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int slot = inv[static_cast<long long>(t) * k + j];
-    if (slot < 0 || slot >= A_total) {
-      report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_COMBINE * 100 + SITE_INDEX);
-      return;
-    }
-    const float wt = w[static_cast<long long>(t) * k + j];
-    float f[NV];
-    Vec<T>::unpack(*reinterpret_cast<const uint4 *>(yp + static_cast<long long>(slot) * d + c * NV), f);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = fmaf(wt, f[i], acc[i]);
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      float f[NV];
+      Vec<T>::unpack(v[j], f);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) acc[i] = fmaf(wt[j], f[i], acc[i]);
+    }
   }
   if (n_shared) {
     float f[NV];
-    Vec<T>::unpack(
-        *reinterpret_cast<const uint4 *>(yp + static_cast<long long>(A_total + t) * d + c * NV), f);
+    Vec<T>::unpack(v[kMaxTopK], f);
 #pragma unroll
     for (int i = 0; i < NV; ++i) acc[i] += f[i];
   }
