@@ -1,11 +1,12 @@
 // gemm.cu -- persistent grouped GEMM on the 5th-generation tensor cores.
 //
 // One kernel template serves the three contractions of the block:
-//   EPI_ROUTER : logits = x . Wr^T for 128 tokens x 256 experts, with the
-//                softmax / top-k / renormalisation fused into the epilogue and
-//                each assignment's rank inside its expert group claimed with an
-//                atomic on the per-expert histogram; the last CTA scans the
-//                histogram into group offsets ("Optimizing on-device inference
+//   EPI_ROUTER : logits = x . Wr^T for 128 tokens x 64 experts per tile, a
+//                top-8 per token and expert block in the epilogue; the last of
+//                a token's expert blocks merges the candidates, takes the
+//                softmax over the chosen logits and claims each assignment's
+//                rank inside its expert group with an atomic on the per-expert
+//                histogram; the last CTA scans the histogram into group offsets ("Optimizing on-device inference
 //                for Apple Silicon", sections "Qwen creates three distinct
 //                workload shapes" and "Keep expert routing on the GPU").
 //   EPI_SWIGLU : for each expert group, gate and up projections of its rows in
@@ -13,8 +14,9 @@
 //                h = silu(gate) * up written once (section "Reduce
 //                intermediate traffic and dispatch traffic": input
 //                projections fused with the gated activation).  Routed A rows
-//                come from the permuted copy Xp (one 128-row TMA box per
-//                stage); the shared expert reads x itself.
+//                are gathered from x by four extra warps (16-byte cp.async
+//                into the swizzled tile, row r from token perm[slot]); the
+//                shared expert's rows (x in order) come by TMA.
 //   EPI_STORE  : the down projection of each group's rows, stored per slot.
 // The tiles of both grouped GEMMs are derived on the device from the group
 // offsets the routing wrote (section "Keep expert routing on the GPU": the
@@ -24,12 +26,13 @@
 // are ordered with m innermost, so the CTAs that share a weight block run side
 // by side and the weight block is read from HBM once.
 //
-// CTA layout: 192 threads.  Warp 0 produces a 4-stage shared-memory ring of
-// 128-byte-swizzled K-major tiles (lane 0 issues the TMA tile loads); warp 1
-// allocates 512
-// TMEM columns (two 128 x 256 fp32 accumulators) and its lane 0 issues
-// tcgen05.mma (M = 128, N = 256, 32 bytes of K per instruction); warps 2-5
-// drain a finished accumulator with tcgen05.ld while the MMA fills the other.
+// CTA layout: 192 threads (320 for the gate/up GEMM).  Warp 0 produces a
+// shared-memory ring of 128-byte-swizzled K-major tiles (lane 0 issues the TMA
+// tile loads; 4 stages at N = 256, 8 at N = 64); warp 1 allocates 2N TMEM
+// columns (two 128 x N fp32 accumulators) and its lane 0 issues tcgen05.mma
+// (M = 128, 32 bytes of K per instruction); warps 2-5 drain a finished
+// accumulator with tcgen05.ld while the MMA fills the other; warps 6-9 of the
+// gate/up GEMM gather its routed A rows.
 // The grid is persistent: CTA c takes tiles c, c + gridDim.x, ...
 // Every wait is bounded; a wait that runs out records a timeout in the status
 // word, raises a CTA-wide abort flag, drains what it issued and returns.
@@ -153,8 +156,13 @@ __device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i, int 
 
 }  // namespace
 
+// Threads of one CTA: the gate/up GEMM adds four warps that gather the routed
+// token rows of its A tiles.
+template <int EPI>
+constexpr int gemm_threads() { return EPI == EPI_SWIGLU ? kThreads + kGatherThreads : kThreads; }
+
 template <typename T, int EPI, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const __grid_constant__ CUtensorMap tmB0s,
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Tile<T, BN>;
   constexpr bool kRouter = (EPI == EPI_ROUTER);
   constexpr bool kDual = (EPI == EPI_SWIGLU);  // B = gate rows over up rows
+  constexpr bool kGather = (EPI == EPI_SWIGLU);  // routed A rows gathered by warps 6-9
   constexpr int kOutCols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
   constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
   extern __shared__ uint8_t smem_raw[];
@@ -190,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      // the TMA producer's expect-tx arrival, plus one per gather thread
+      mbar_init(full0 + 8 * s, kGather ? 1 + kGatherThreads : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -291,8 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
         const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(a_dst, ma, fb, kx, tl.a_row, pol_a);
+          // gate/up: routed A rows come from the gather warps, the shared
+          // expert's (the tokens in order) from TMA like every B tile
+          const bool a_tma = !kGather || sh;
+          mbar_arrive_expect_tx(fb, a_tma ? C::STAGE_BYTES : C::B_BYTES);
+          if (a_tma) tma_load_2d(a_dst, ma, fb, kx, tl.a_row, pol_a);
           if (kDual) {
             tma_load_2d(b_dst, mb0, fb, kx, brow, pol_w);
             tma_load_2d(b_dst + C::B_BYTES / 2, mb1, fb, kx, brow, pol_w);
@@ -341,6 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // gathered A rows were written by cp.async (generic proxy); the
+          // barrier made them visible to this thread, the fence to the
+          // tensor core's reads
+          if (kGather) fence_proxy_async_smem();
           const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
@@ -368,6 +385,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_DRAIN);
       }
     }
+  } else if (kGather && warp >= 6) {
+    // ------------------------------------------------------------ gather
+    // Each routed A tile row (128 bytes of K per k-block, from the token row
+    // perm[slot]) is copied by 8 threads, 16 bytes each, so one warp copies 4
+    // whole rows per instruction; thread g takes chunk g % 8 of rows
+    // g / 8 + 16 i.  Chunk c of row r goes where the 128-byte swizzle the MMA
+    // descriptor expects puts it: c ^ (r % 8).  Rows past the tile's end are
+    // left as they are: the epilogue never stores them.  Every gather thread
+    // arrives on every stage's full barrier through cp.async.mbarrier.arrive,
+    // which fires when the thread's copies so far have landed; the MMA thread
+    // fences the proxy before the tensor core reads them.
+    const int g = threadIdx.x - kThreads;
+    const int c = g & 7, r0 = g >> 3;
+    const int K = p.num_k_blocks * C::BK;
+    const T *xg = static_cast<const T *>(p.x);
+    constexpr int kChunk = 16 / static_cast<int>(sizeof(T));  // elements per 16 bytes
+    constexpr int kRowsPer = kBM / (kGatherThreads / 8);      // rows per thread: 8
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
+      const GemmTile tl = decode_tile(gt, p, ti, kOutCols, !kDual);
+      const bool routed = tl.group < p.n_routed;
+      const T *src[kRowsPer];
+#pragma unroll
+      for (int i = 0; i < kRowsPer; ++i) {
+        const int r = r0 + 16 * i;
+        src[i] = (routed && r < tl.rows)
+                     ? xg + static_cast<long long>(p.perm[tl.a_row + r]) * K + c * kChunk
+                     : nullptr;
+      }
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_PRODUCER_EMPTY);
+          }
+          ok = false;
+          break;
+        }
+        const uint32_t tile_dst = smem_u32(sA + stage * C::A_BYTES);
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+          const int r = r0 + 16 * i;
+          if (src[i] != nullptr)
+            cp_async16(tile_dst + r * 128 + ((c ^ (r & 7)) << 4), src[i] + kb * C::BK);
+        }
+        cp_async_arrive(full0 + 8 * stage);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // copies in flight must land before the CTA's shared memory goes away
+    cp_async_wait_all();
   } else {
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;       // TMEM lane quarter this warp may access
@@ -570,7 +644,7 @@ cudaError_t gemm_set_smem_attr() {
 template <typename T, int EPI, int BN>
 cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;
-  gemm_kernel<T, EPI, BN><<<grid, kThreads, kGemmSmem, st>>>(maps.m[0], maps.m[1], maps.m[2],
+  gemm_kernel<T, EPI, BN><<<grid, gemm_threads<EPI>(), kGemmSmem, st>>>(maps.m[0], maps.m[1], maps.m[2],
                                                               maps.m[3], maps.m[4], maps.m[5], p);
   return cudaGetLastError();
 }

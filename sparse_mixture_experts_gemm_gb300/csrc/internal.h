@@ -10,7 +10,7 @@ namespace moe {
 // Groups 0..E-1 are routed experts; group E is the shared expert.
 struct GemmTile {
   int group;    // expert id, E for the shared expert
-  int a_row;    // first row of the A operand (row of Xp, x or H)
+  int a_row;    // first row of the A operand (first slot, row of x, or row of H)
   int out_row;  // first output row (row of H or Yp)
   int rows;     // valid rows, 1..128
   int n0;       // first output column; also the row offset inside the group's B
@@ -25,6 +25,7 @@ constexpr int kBN = 256;      // MMA N: B rows per tile of the expert GEMMs
 constexpr int kRouterBN = 64; // experts per router tile (E split into E / 64 blocks)
 constexpr int kStageBudget = 4 * (kBM * 128 + kBN * 128);  // smem for the operand stages
 constexpr int kThreads = 192; // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGatherThreads = 128;  // gate/up GEMM: warps 6-9 gather routed token rows
 constexpr int kGemmCtrl = 4096;  // barriers, TMEM slot, row tokens, group table
 constexpr int kGemmSmem = kStageBudget + 1024 + kGemmCtrl;
 constexpr int kCountStride = 32;  // router histogram: one counter per 128-byte line
@@ -59,6 +60,9 @@ struct GemmParams {
   float *cand_v;           // [T][nq][kMaxTopK] per-block top-k candidates
   int32_t *cand_i;
   int32_t *tok_cnt;        // [T] blocks finished per token, zero between calls
+  // gate/up GEMM: routed A rows are gathered from the tokens
+  const int32_t *perm;     // [A] token of each slot
+  const void *x;           // [T][K] the chunk's tokens
   unsigned *done;          // CTA completion ticket, zeroed before the launch
 };
 
@@ -84,9 +88,8 @@ cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T
                                int k, int32_t *idx, float *w, int32_t *counts, int32_t *rank,
                                cudaStream_t st);
 cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaStream_t st);
-template <typename T>
-cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv, const T *x,
-                         T *xp, int A, int k, int E, int d, int *status, cudaStream_t st);
+cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
+                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st);
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);

@@ -6,9 +6,10 @@
 // inference for Apple Silicon", section "Bound temporary memory with request
 // chunking"), all on the caller's stream with no host synchronisation
 // (section "Keep expert routing on the GPU"):
-//   router (tcgen05 for bf16, SIMT + offsets for fp32) -> place (slots and
-//   the permuted row copy Xp) -> grouped gate/up GEMM + SiLU -> grouped down
-//   GEMM -> combine.
+//   router (tcgen05 for bf16, SIMT + offsets for fp32) -> place (slot of
+//   every assignment and token of every slot) -> grouped gate/up GEMM + SiLU
+//   (routed rows gathered from x inside the kernel) -> grouped down GEMM ->
+//   combine.
 // Decode (T == 1, section "Optimise the single-row weight path"):
 //   decode_router -> decode_gateup -> decode_down, chained with programmatic
 //   dependent launch.
@@ -106,10 +107,11 @@ struct moe_handle {
   float *cand_v = nullptr;     // router: per expert block top-k candidates
   int32_t *cand_i = nullptr;
   int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
-  void *xp = nullptr, *hbuf = nullptr, *yp = nullptr;
+  int32_t *perm = nullptr;  // [A] token of each slot
+  void *hbuf = nullptr, *yp = nullptr;
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
-  CUtensorMap tm_xp, tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
   // profiling
   bool prof = false;
   std::vector<ProfRec> recs;
@@ -242,8 +244,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   }
   {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
-    MOE_TRY(launch_place<T>(h->idx, h->offsets, h->inv, x, static_cast<T *>(h->xp), A, k, E, d,
-                               h->status, st));
+    MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st));
   }
   GemmParams base = {};
   base.offsets = h->offsets;
@@ -255,9 +256,10 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   {
     ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
     GemmMaps m;
-    // routed rows from the permuted copy, the shared expert's rows from x
-    m.m[0] = h->tm_xp;
+    // routed rows are gathered from x by the kernel; the shared expert's
+    // rows (x in token order) come through this map
     if (!make_map(&m.m[1], x, sizeof(T), Tc, d, kBM)) return MOE_ERR_CUDA;
+    m.m[0] = m.m[1];
     m.m[2] = h->tm_wg;
     m.m[3] = h->tm_wu;
     m.m[4] = c.n_shared ? h->tm_sg : h->tm_wg;
@@ -269,6 +271,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.out = h->hbuf;
     p.ldo = F;
     p.kid = KID_GEMM_GATE_UP;
+    p.perm = h->perm;
+    p.x = x;
     MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
   }
   {
@@ -398,7 +402,7 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
       {reinterpret_cast<void **>(&h->cand_v), sizeof(float) * nqk * Tm},
       {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
       {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},
-      {&h->xp, esz * A * d},
+      {reinterpret_cast<void **>(&h->perm), sizeof(int32_t) * A},
       {&h->hbuf, esz * (A + Tm) * F},
       {&h->yp, esz * (A + Tm) * d},
   };
@@ -425,7 +429,6 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
                           static_cast<uint32_t>(512 / esz), 32, false) &&
             encode_map_2d(&h->tm_du, c.w_up, esz, static_cast<uint64_t>(E) * F, d,
                           static_cast<uint32_t>(512 / esz), 32, false) &&
-            make_map(&h->tm_xp, h->xp, esz, A, d, kBM) &&
             make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
             make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
             make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&

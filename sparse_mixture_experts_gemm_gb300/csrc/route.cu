@@ -6,7 +6,7 @@
 //                 (the bf16 router does this in its last CTA instead);
 //   place         slot = offset[expert] + rank for every assignment: the
 //                 (token, choice) -> slot map read by the combine, and the
-//                 token's row copied into its group's block of Xp;
+//                 slot -> token map the gate/up GEMM gathers rows with;
 //   combine       out[t] = sum_j w[t][j] * Y[slot(t, j)] + Y_shared[t].
 // Source: "Optimizing on-device inference for Apple Silicon", section "Keep
 // expert routing on the GPU" (histogram, prefix scan into start offsets,
@@ -203,61 +203,35 @@ cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaS
 }
 
 // ---------------------------------------------------------------- place
-// One warp per assignment i = t * k + j: slot = offsets[e] + rank, written
-// over the rank in rank_inv[i]; the token row x[t] is copied to Xp[slot] with
-// 16-byte vectors (all of a lane's loads issued before its stores), so the
-// grouped gate/up GEMM reads each group's rows as one contiguous block.
-template <typename T>
+// One thread per assignment i = t * k + j: slot = offsets[e] + rank, written
+// over the rank in rank_inv[i]; perm[slot] = t names the token whose row the
+// grouped gate/up GEMM gathers into that slot's tile row.
 __global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ idx,
                                                     const int32_t *__restrict__ offsets,
-                                                    int32_t *rank_inv, const T *__restrict__ x,
-                                                    T *xp, int A, int k, int E, int d,
-                                                    int *status) {
-  const int lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+                                                    int32_t *rank_inv, int32_t *perm, int A, int k,
+                                                    int E, int *status) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
   if (i >= A) return;
   const int e = idx[i];
   if (e < 0 || e >= E) {
-    if (lane == 0) report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
+    report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
     return;
   }
   const int lo = offsets[e], hi = offsets[e + 1];
   const int slot = lo + rank_inv[i];
   if (slot < lo || slot >= hi) {
-    if (lane == 0) report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
+    report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
     return;
   }
-  __syncwarp();
-  if (lane == 0) rank_inv[i] = slot;
-  const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<long long>(i / k) * d);
-  uint4 *dst = reinterpret_cast<uint4 *>(xp + static_cast<long long>(slot) * d);
-  const int nvec = d * static_cast<int>(sizeof(T)) / 16;
-  for (int base = 0; base < nvec; base += 32 * 8) {
-    uint4 v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = base + q * 32 + lane;
-      if (j < nvec) v[q] = __ldg(src + j);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = base + q * 32 + lane;
-      if (j < nvec) dst[j] = v[q];
-    }
-  }
+  rank_inv[i] = slot;
+  perm[slot] = i / k;
 }
 
-template <typename T>
-cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv, const T *x,
-                         T *xp, int A, int k, int E, int d, int *status, cudaStream_t st) {
-  place_kernel<T><<<(A + 7) / 8, 256, 0, st>>>(idx, offsets, rank_inv, x, xp, A, k, E, d, status);
+cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
+                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st) {
+  place_kernel<<<(A + 255) / 256, 256, 0, st>>>(idx, offsets, rank_inv, perm, A, k, E, status);
   return cudaGetLastError();
 }
-template cudaError_t launch_place<float>(const int32_t *, const int32_t *, int32_t *, const float *,
-                                         float *, int, int, int, int, int *, cudaStream_t);
-template cudaError_t launch_place<__nv_bfloat16>(const int32_t *, const int32_t *, int32_t *,
-                                                 const __nv_bfloat16 *, __nv_bfloat16 *, int, int,
-                                                 int, int, int *, cudaStream_t);
 
 // ---------------------------------------------------------------- combine
 // One thread per 16-byte chunk of an output row; the k routed contributions
