@@ -5,6 +5,7 @@ The path is three kernels chained with programmatic dependent launch (router
 profile confirms that exactly those ran.  Bars as in the prefill tests: block
 output within 1e-2 row-normwise relative error.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -101,3 +102,49 @@ def test_decode_layer_stack_in_a_cuda_graph(dev):
     finally:
         for layer in layers:
             layer.close()
+
+
+def test_decode_layer_stack_sample_against_oracle(dev):
+    """A sample of the decode workload: fresh tokens fed through a stack of
+    distinct full-size layers (each token is every layer's input), each
+    (step, layer) output against the oracle, with all steps captured in one
+    CUDA graph per step as the benchmark runs them."""
+    d, F, E, k, L, steps = 2048, 512, 256, 8, 4, 12
+    ws = [synth.layer_weights(1000 + l, d, F, E, 1, "bf16", dev) for l in range(L)]
+    layers = [moe.MoELayer(w, k, max_tokens=1) for w in ws]
+    try:
+        xin = torch.empty((1, d), dtype=torch.bfloat16, device=dev)
+        outs = torch.empty((L, d), dtype=torch.bfloat16, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                layers[l].forward(xin, out=outs[l:l + 1], stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                layers[l].forward(xin, out=outs[l:l + 1], stream=stream)
+        # tokens with the routing margin in every layer of the stack
+        cand = synth.tokens(1100, 4 * steps, d, "bf16", dev)
+        keep = np.ones(4 * steps, dtype=bool)
+        for l in range(L):
+            _, _, logits, _ = H.oracle.route(H.np_view(cand), H.np_view(ws[l]["Wr"]), k)
+            keep &= H.kth_gap(logits, k) >= H.MARGIN
+        assert keep.sum() >= steps
+        toks = cand[torch.as_tensor(np.nonzero(keep)[0][:steps], device=dev)].contiguous()
+        got = []
+        for s in range(steps):
+            xin.copy_(toks[s:s + 1])
+            g.replay()
+            torch.cuda.synchronize()
+            got.append(outs.clone())
+        for layer in layers:
+            assert layer.status()[0] == 0
+    finally:
+        for layer in layers:
+            layer.close()
+    for l in range(L):
+        ref, *_ = H.oracle_forward(toks, ws[l], k)
+        out_l = torch.stack([got[s][l] for s in range(steps)])
+        err = H.row_rel_err(out_l, ref)
+        assert err.max() <= H.OUT_TOL, f"layer {l}: max row rel err {err.max():.3e}"

@@ -201,3 +201,31 @@ def test_device_timeout_is_reported_not_trapped(dev):
     torch.cuda.synchronize()
     assert layer.status()[0] == 0
     layer.close()
+
+
+def test_long_prompt_128k_in_8k_chunks(dev):
+    """T=131072 through one layer in 8192-token chunks (the long-prompt
+    workload): routing and per-chunk expert counts exact on all 16 chunks,
+    outputs of two whole chunks (the first and the last) against the oracle."""
+    T, chunk, d, F, E, k = 131072, 8192, 2048, 512, 256, 8
+    w = synth.layer_weights(4, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(1004, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=chunk)
+    try:
+        out = layer.forward(x)
+        routes = [layer.route(x[c0:c0 + chunk]) for c0 in range(0, T, chunk)]
+        torch.cuda.synchronize()
+        rc, detail = layer.status()
+        assert rc == 0, f"device status {rc} detail {detail}"
+    finally:
+        layer.close()
+    wr = H.np_view(w["Wr"])
+    for ci, (idx, wts, counts) in enumerate(routes):
+        xs = x[ci * chunk:(ci + 1) * chunk]
+        ridx, rw, _, rcounts = H.oracle.route(H.np_view(xs), wr, k)
+        H.check_routing(idx, wts, counts, ridx, rw, rcounts)
+    for ci in (0, T // chunk - 1):
+        rows = np.arange(ci * chunk, (ci + 1) * chunk)
+        ref, *_ = H.oracle_forward(x, w, k, rows=rows)
+        err = H.row_rel_err(out[torch.as_tensor(rows, device=dev)], ref)
+        assert err.max() <= H.OUT_TOL, f"chunk {ci}: max row rel err {err.max():.3e}"
