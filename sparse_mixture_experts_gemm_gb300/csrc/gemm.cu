@@ -156,6 +156,44 @@ __device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i, int 
 
 }  // namespace
 
+// Tile sequence of a CTA of the grouped GEMMs: lane 0 of the producer warp
+// claims tiles (its first is blockIdx.x, every later one comes from a global
+// counter, so CTAs that drew cheap tiles take more of them) and publishes each
+// id in a small shared ring; the MMA thread, the epilogue warps and the gather
+// warps read the ids from the ring in the same order.  A claim past the last
+// tile ends every role's loop.  The router keeps the static order (one tile
+// per CTA at most sizes).
+constexpr int kTileRing = 4;
+struct TileRing {
+  uint32_t full0, empty0;  // [kTileRing] mbarriers each
+  volatile int *ids;       // [kTileRing]
+};
+
+// Lane 0 of the producer warp: claim the it-th tile.  False when the slot's
+// readers did not release it in time (the abort flag is then set).
+__device__ __forceinline__ bool claim_tile(const TileRing &r, int it, int *ctr, int ntiles,
+                                           long long limit, volatile int *abort, int &ti) {
+  const int slot = it % kTileRing;
+  if (it >= kTileRing && !mbar_wait(r.empty0 + 8 * slot, ((it / kTileRing) - 1) & 1, limit, abort))
+    return false;
+  ti = it == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(ctr, 1);
+  if (ti > ntiles) ti = ntiles;
+  r.ids[slot] = ti;
+  mbar_arrive(r.full0 + 8 * slot);  // release: the id is visible with the phase
+  return true;
+}
+
+// One thread per reading role: the it-th tile id; false when it did not
+// arrive in time.
+__device__ __forceinline__ bool read_tile(const TileRing &r, int it, long long limit,
+                                          volatile int *abort, int &ti) {
+  const int slot = it % kTileRing;
+  if (!mbar_wait(r.full0 + 8 * slot, (it / kTileRing) & 1, limit, abort)) return false;
+  ti = r.ids[slot];
+  mbar_arrive(r.empty0 + 8 * slot);
+  return true;
+}
+
 // Threads of one CTA: the gate/up GEMM adds four warps that gather the routed
 // token rows of its A tiles.
 template <int EPI>
@@ -185,6 +223,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   int *s_last = reinterpret_cast<int *>(ctrl + 520);
   int *s_off = reinterpret_cast<int *>(ctrl + 1536);        // [E + 1]
   int *s_mt = reinterpret_cast<int *>(ctrl + 1536 + 1040);  // [E + 2]
+  const TileRing ring{smem_u32(ctrl + 1056), smem_u32(ctrl + 1056 + 8 * kTileRing),
+                      reinterpret_cast<volatile int *>(ctrl + 1024)};
+  // readers of the ring: the MMA thread, 4 epilogue warps, 4 gather warps
+  constexpr int kTileReaders = 1 + 4 + (EPI == EPI_SWIGLU ? 4 : 0);
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * C::STAGES;
@@ -208,6 +250,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       mbar_init(tempty0 + 8 * a, 128);
     }
     mbar_init(drain_bar, 1);
+    for (int q = 0; q < kTileRing; ++q) {
+      mbar_init(ring.full0 + 8 * q, 1);
+      mbar_init(ring.empty0 + 8 * q, kTileReaders);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -279,7 +325,22 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
+    for (int it = 0; ok; ++it) {
+      int ti = blockIdx.x + it * gridDim.x;
+      if (!kRouter) {
+        int c_ok = 1;
+        if (lane == 0) c_ok = claim_tile(ring, it, p.tile_ctr, ntiles, limit, abort_flag, ti) ? 1 : 0;
+        ti = __shfl_sync(0xffffffffu, ti, 0);
+        if (!__shfl_sync(0xffffffffu, c_ok, 0)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_PRODUCER_EMPTY);
+          }
+          ok = false;
+          break;
+        }
+      }
+      if (ti >= ntiles) break;
       const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool sh = !kRouter && tl.group >= p.n_routed;
       const CUtensorMap *ma = sh ? &tmAs : &tmA;
@@ -337,7 +398,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
-      for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
+      for (int it = 0; ok; ++it) {
+        int ti = blockIdx.x + it * gridDim.x;
+        if (!kRouter && !read_tile(ring, it, limit, abort_flag, ti)) {
+          *abort_flag = 1;
+          report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
+          ok = false;
+          break;
+        }
+        if (ti >= ntiles) break;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, limit, abort_flag)) {
           *abort_flag = 1;
           report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_TMEM_EMPTY);
@@ -405,7 +474,19 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
+    for (int it = 0; ok; ++it) {
+      int ti = 0, r_ok = 1;
+      if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
+      ti = __shfl_sync(0xffffffffu, ti, 0);
+      if (!__shfl_sync(0xffffffffu, r_ok, 0)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_PRODUCER_EMPTY);
+        }
+        ok = false;
+        break;
+      }
+      if (ti >= ntiles) break;
       const GemmTile tl = decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool routed = tl.group < p.n_routed;
       const T *src[kRowsPer];
@@ -448,7 +529,21 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     const int r = wq * 32 + lane;  // tile row == TMEM lane
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
+    for (int it = 0;; ++it) {
+      int ti = blockIdx.x + it * gridDim.x;
+      if (!kRouter) {
+        int r_ok = 1;
+        if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
+        ti = __shfl_sync(0xffffffffu, ti, 0);
+        if (!__shfl_sync(0xffffffffu, r_ok, 0)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_EPI_TMEM_FULL);
+          }
+          break;
+        }
+      }
+      if (ti >= ntiles) break;
       const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, limit, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {

@@ -60,6 +60,7 @@ struct GemmParams {
   float *cand_v;           // [T][nq][kMaxTopK] per-block top-k candidates
   int32_t *cand_i;
   int32_t *tok_cnt;        // [T] blocks finished per token, zero between calls
+  int *tile_ctr;           // grouped GEMMs: tiles claimed after each CTA's first, zero before the launch
   // gate/up GEMM: routed A rows are gathered from the tokens
   const int32_t *perm;     // [A] token of each slot
   const void *x;           // [T][K] the chunk's tokens

@@ -89,7 +89,9 @@ struct ProfRec {
 }  // namespace
 
 constexpr int kRouteCtlCounts = 256 * kCountStride;
-constexpr size_t kRouteCtlBytes = sizeof(int32_t) * (kRouteCtlCounts + 4);
+// counts, then the router's done ticket, the gate/up and the down GEMM's tile
+// counters, each on its own 128-byte line
+constexpr size_t kRouteCtlBytes = sizeof(int32_t) * (kRouteCtlCounts + 96);
 
 struct moe_handle {
   moe_config cfg;
@@ -101,7 +103,8 @@ struct moe_handle {
   void *ws = nullptr;
   int32_t *idx = nullptr, *inv = nullptr, *offsets = nullptr, *status = nullptr;
   // [256 * kCountStride] per-expert counts (line-padded for the bf16 router,
-  // dense for the fp32 one), then [4] the router's CTA ticket
+  // dense for the fp32 one), then the router's CTA ticket and the grouped
+  // GEMMs' tile counters
   int32_t *route_ctl = nullptr;
   float *w = nullptr, *logits = nullptr, *hdec = nullptr;
   float *cand_v = nullptr;     // router: per expert block top-k candidates
@@ -119,6 +122,7 @@ struct moe_handle {
   size_t pool_used = 0;
   int32_t *counts() { return route_ctl; }
   unsigned *done() { return reinterpret_cast<unsigned *>(route_ctl + kRouteCtlCounts); }
+  int32_t *tile_ctr(int gemm) { return route_ctl + kRouteCtlCounts + 32 * (gemm + 1); }
 };
 
 namespace {
@@ -271,6 +275,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.out = h->hbuf;
     p.ldo = F;
     p.kid = KID_GEMM_GATE_UP;
+    p.tile_ctr = h->tile_ctr(0);
     p.perm = h->perm;
     p.x = x;
     MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
@@ -288,6 +293,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.out = h->yp;
     p.ldo = d;
     p.kid = KID_GEMM_DOWN;
+    p.tile_ctr = h->tile_ctr(1);
     MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st)));
   }
   {
