@@ -723,9 +723,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           if (p.offsets_out) p.offsets_out[e] = run;
           if (p.counts_out) p.counts_out[e] = ce;
           run += ce;
+          // every CTA has added its counts: clear them for the next call
+          p.counts[static_cast<long long>(e) * kCountStride] = 0;
         }
       }
       if (lane == 31 && p.offsets_out) p.offsets_out[E] = incl;
+      if (lane == 0) {
+        *p.done = 0u;
+        for (int q = 0; q < p.n_clear; ++q) p.clear[q * 32] = 0;
+      }
     }
   }
 }

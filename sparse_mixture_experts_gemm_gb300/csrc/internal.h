@@ -52,7 +52,7 @@ struct GemmParams {
   const float *bias;
   int32_t *idx;
   float *w;
-  int32_t *counts;         // [E * kCountStride], zeroed before the launch
+  int32_t *counts;         // [E * kCountStride], zero at the launch; the last CTA clears it again
   int32_t *counts_out;     // [E] dense copy written by the last CTA (may be null)
   int32_t *rank;           // [T * k] rank of each assignment inside its group (may be null)
   int32_t *offsets_out;    // [E + 1] written by the last CTA (may be null)
@@ -64,7 +64,9 @@ struct GemmParams {
   // gate/up GEMM: routed A rows are gathered from the tokens
   const int32_t *perm;     // [A] token of each slot
   const void *x;           // [T][K] the chunk's tokens
-  unsigned *done;          // CTA completion ticket, zeroed before the launch
+  unsigned *done;          // CTA completion ticket, zero at the launch; the last CTA clears it
+  int32_t *clear;          // router: n_clear words (128 bytes apart) the last CTA zeroes
+  int n_clear;
 };
 
 // Tensor maps: A routed, A shared, B0 routed, B1 routed, B0 shared, B1 shared.
@@ -88,7 +90,9 @@ template <typename T>
 cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T_tok, int d, int E,
                                int k, int32_t *idx, float *w, int32_t *counts, int32_t *rank,
                                cudaStream_t st);
-cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaStream_t st);
+// also zeroes counts[0, E) and n_clear words clear[32 q] for the next call
+cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *clear, int n_clear,
+                           cudaStream_t st);
 cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
                          int32_t *perm, int A, int k, int E, int *status, cudaStream_t st);
 template <typename T>

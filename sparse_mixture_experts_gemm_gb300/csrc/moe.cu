@@ -220,6 +220,8 @@ int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w
   p.rank = rank;
   p.offsets_out = offsets;
   p.done = h->done();
+  p.clear = h->tile_ctr(0);
+  p.n_clear = 2;
   const int tiles = nblk * nq;
   MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(m, p,
                                                              tiles < h->num_sms ? tiles : h->num_sms,
@@ -234,7 +236,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   const int A = Tc * k;
   const int BK = static_cast<int>(128 / sizeof(T));
 
-  MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, kRouteCtlBytes, st));
+  // route_ctl is zero here: create cleared it and every router launch clears
+  // what it used (counts, ticket, the GEMMs' tile counters) when it is done
   {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
@@ -243,7 +246,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
                                     k, h->idx, h->w, h->counts(), h->inv, st));
-      MOE_TRY(launch_offsets(h->counts(), E, h->offsets, st));
+      MOE_TRY(launch_offsets(h->counts(), E, h->offsets, h->tile_ctr(0), 2, st));
     }
   }
   {
@@ -480,7 +483,6 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   const int d = c.d_model, E = c.n_experts, k = c.top_k;
   ProfScope ps(h, MOE_KERNEL_ROUTER, st);
   if (c.dtype == MOE_BF16) {
-    MOE_TRY(cudaMemsetAsync(h->route_ctl, 0, kRouteCtlBytes, st));
     return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, counts, st);
   }
   MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
@@ -528,9 +530,11 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
   int s[2] = {0, 0};
   if (cudaMemcpy(s, h->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->status, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
-  // an aborted router leaves per-token arrival counts behind
+  // an aborted launch can leave the router's per-token arrival counts, its
+  // histogram and ticket, or the GEMMs' tile counters behind
   if (s[0] != MOE_OK &&
-      cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) != cudaSuccess)
+      (cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) != cudaSuccess ||
+       cudaMemset(h->route_ctl, 0, kRouteCtlBytes) != cudaSuccess))
     return MOE_ERR_CUDA;
   if (detail) *detail = s[1];
   return s[0];

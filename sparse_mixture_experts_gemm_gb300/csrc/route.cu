@@ -172,7 +172,8 @@ template cudaError_t launch_router_simt<__nv_bfloat16>(const __nv_bfloat16 *, co
 
 // ---------------------------------------------------------------- offsets
 // offsets[e] = sum_{e' < e} counts[e'], offsets[E] = total; one warp.
-__global__ void offsets_kernel(const int32_t *__restrict__ counts, int E, int32_t *offsets) {
+__global__ void offsets_kernel(int32_t *counts, int E, int32_t *offsets, int32_t *clear,
+                               int n_clear) {
   const int lane = threadIdx.x;
   const int per = (E + 31) / 32;
   int sum = 0;
@@ -192,13 +193,17 @@ __global__ void offsets_kernel(const int32_t *__restrict__ counts, int E, int32_
     if (e < E) {
       offsets[e] = run;
       run += counts[e];
+      counts[e] = 0;  // clear for the next call
     }
   }
   if (lane == 31) offsets[E] = incl;
+  if (lane == 0)
+    for (int q = 0; q < n_clear; ++q) clear[q * 32] = 0;
 }
 
-cudaError_t launch_offsets(const int32_t *counts, int E, int32_t *offsets, cudaStream_t st) {
-  offsets_kernel<<<1, 32, 0, st>>>(counts, E, offsets);
+cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *clear, int n_clear,
+                           cudaStream_t st) {
+  offsets_kernel<<<1, 32, 0, st>>>(counts, E, offsets, clear, n_clear);
   return cudaGetLastError();
 }
 
