@@ -122,7 +122,7 @@ def make_layer(cfg: dict, dev, seed: int):
 DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
 # ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
-GEMM1_TRAFFIC_4K = None  # the kernel changed since the last capture
+GEMM1_TRAFFIC_4K = 1_094_968_000 + 8_866_304
 
 
 def algorithmic_prefill(cfg: dict, counts: np.ndarray, T: int) -> dict:
