@@ -27,7 +27,14 @@ _LIBS: dict[int, ctypes.CDLL] = {}
 
 class Dims(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("F", ctypes.c_int), ("E", ctypes.c_int),
-                ("k", ctypes.c_int), ("n_shared", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("k", ctypes.c_int), ("n_shared", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("wdtype", ctypes.c_int)]
+
+
+class Q4(ctypes.Structure):
+    """One expert matrix in the 4-bit group-affine format (codes, scales, biases)."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p)]
 
 
 def lib_path(mutation: int = 0) -> str:
@@ -102,7 +109,7 @@ def route(x, wr, k, bias=None, nthreads=None, mutation=0):
     T, d = x.shape
     E = wr.shape[0]
     bias = _c(bias, np.float32)
-    dims = Dims(d, 1, E, k, 0, dt)
+    dims = Dims(d, 1, E, k, 0, dt, dt)
     idx = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float64)
     logits = np.zeros((T, E), np.float32)
@@ -116,34 +123,51 @@ def route(x, wr, k, bias=None, nthreads=None, mutation=0):
 
 
 def forward(x, wr, wg, wu, wd, k, sg=None, su=None, sd=None, bias=None, nthreads=None,
-            mutation=0):
+            mutation=0, q4=False, F=None):
     """The whole block: returns (out[T][d] f64, idx, w, counts).
 
     wg, wu: [E][F][d] arrays or length-E sequences of [F][d] arrays (None where an
     expert is never selected); wd likewise with [d][F].  sg/su/sd: shared expert
-    ([F][d], [F][d], [d][F]) or all None for no shared expert.
+    ([F][d], [F][d], [d][F]) or all None for no shared expert.  With q4=True
+    every expert matrix is instead a (codes uint8 [rows][cols/2], scales uint16
+    [rows][cols/64], biases uint16 [rows][cols/64]) triple of the 4-bit
+    group-affine format, and F must be given.
     """
     x, wr = _c(x), _c(wr)
     dt = _dtype_code(x)
     T, d = x.shape
     E = wr.shape[0]
+    keep = []  # arrays and records that must outlive the call
+
+    def one(a):
+        """Pointer to one expert matrix (dense array or Q4 record)."""
+        if a is None:
+            return None
+        if q4:
+            c, sc, bi = (_c(a[0], np.uint8), _c(a[1], np.uint16), _c(a[2], np.uint16))
+            rec = Q4(c.ctypes.data, sc.ctypes.data, bi.ctypes.data)
+            keep.extend([c, sc, bi, rec])
+            return ctypes.addressof(rec)
+        arr = _c(a)
+        assert _dtype_code(arr) == dt
+        keep.append(arr)
+        return arr.ctypes.data
 
     def plist(ws):
-        arrs = [None if a is None else _c(a) for a in ws]
-        for a in arrs:
-            if a is not None:
-                assert _dtype_code(a) == dt
-        return arrs, (ctypes.c_void_p * E)(*[None if a is None else a.ctypes.data for a in arrs])
+        return (ctypes.c_void_p * E)(*[one(a) for a in ws])
 
-    wg_a, wg_p = plist(wg)
-    wu_a, wu_p = plist(wu)
-    wd_a, wd_p = plist(wd)
-    F = next(a.shape[0] for a in wg_a if a is not None) if any(a is not None for a in wg_a) else (
-        sg.shape[0])
+    wg_p, wu_p, wd_p = plist(wg), plist(wu), plist(wd)
+    if F is None:
+        F = next(a.shape[0] for a in wg if a is not None) if any(a is not None for a in wg) else (
+            sg.shape[0])
     n_shared = 0 if sg is None else 1
-    sg, su, sd = _c(sg), _c(su), _c(sd)
+    if q4:
+        sgp, sup, sdp = one(sg), one(su), one(sd)
+    else:
+        sg, su, sd = _c(sg), _c(su), _c(sd)
+        sgp, sup, sdp = _ptr(sg), _ptr(su), _ptr(sd)
     bias = _c(bias, np.float32)
-    dims = Dims(d, F, E, k, n_shared, dt)
+    dims = Dims(d, F, E, k, n_shared, dt, 2 if q4 else dt)
     out = np.zeros((T, d), np.float64)
     idx = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float64)
@@ -151,10 +175,9 @@ def forward(x, wr, wg, wu, wd, k, sg=None, su=None, sd=None, bias=None, nthreads
     rc = load(mutation).oracle_forward(
         ctypes.byref(dims), _ptr(x), T, _ptr(wr), _ptr(bias),
         ctypes.cast(wg_p, ctypes.c_void_p), ctypes.cast(wu_p, ctypes.c_void_p),
-        ctypes.cast(wd_p, ctypes.c_void_p), _ptr(sg), _ptr(su), _ptr(sd),
+        ctypes.cast(wd_p, ctypes.c_void_p), sgp, sup, sdp,
         _ptr(out), _ptr(idx), _ptr(w), _ptr(counts), nthreads or _default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_forward failed: {rc}")
-    # keep the pointed-to arrays alive until here
-    del wg_a, wu_a, wd_a
+    del keep  # the pointed-to arrays lived until here
     return out, idx, w, counts

@@ -34,10 +34,17 @@
  * then run in double on those logits.
  *
  * Layouts (row-major):  x[T][d]; Wr[E][d]; Wg_e, Wu_e [F][d]; Wd_e [d][F];
- * Sg, Su [F][d]; Sd [d][F].  Element type of x and weights: dtype 0 = bfloat16
- * bit patterns (uint16), dtype 1 = float32.  Expert weights are passed as an
- * array of E pointers so a caller may hand over only the experts it needs; a
- * selected expert whose pointer is NULL is an error.
+ * Sg, Su [F][d]; Sd [d][F].  Element type of x and the router: dtype 0 =
+ * bfloat16 bit patterns (uint16), dtype 1 = float32.  Expert weights (routed
+ * and shared) have the same type, or, with wdtype 2, the 4-bit group-affine
+ * format of section "Dequantise weights within matrix multiplication": each
+ * matrix is an oracle_q4 record (below) whose element (r, c) is
+ *     w = scale[r][c / 64] * q + bias[r][c / 64],   q = the 4-bit code,
+ * codes packed two per byte along the row, the even column in the low nibble,
+ * scale and bias bfloat16.  The oracle widens scale, bias and q exactly to
+ * double and forms w in double.  Expert weights are passed as an array of E
+ * pointers so a caller may hand over only the experts it needs; a selected
+ * expert whose pointer is NULL is an error.
  *
  * Parity pins live in tests/test_oracle_pins.py (brute force, library
  * cross-checks, closed forms, invariants) and tests/test_oracle_mutations.py,
@@ -59,8 +66,18 @@ typedef struct {
   int E;        /* routed experts */
   int k;        /* experts chosen per token */
   int n_shared; /* 0 or 1 */
-  int dtype;    /* 0 = bf16 bits, 1 = f32 */
+  int dtype;    /* x and router: 0 = bf16 bits, 1 = f32 */
+  int wdtype;   /* expert weights: 0 = bf16 bits, 1 = f32, 2 = 4-bit group-affine */
 } oracle_dims;
+
+/* One matrix in the 4-bit group-affine format (wdtype 2). */
+typedef struct {
+  const uint8_t *codes;   /* [rows][cols / 2] */
+  const uint16_t *scales; /* [rows][cols / 64] bfloat16 bits */
+  const uint16_t *biases; /* [rows][cols / 64] bfloat16 bits */
+} oracle_q4;
+
+#define ORACLE_Q4_GROUP 64
 
 /* Exact widening of one stored element to double. */
 static double elem(const void *base, int dtype, size_t i) {
@@ -71,11 +88,33 @@ static double elem(const void *base, int dtype, size_t i) {
   return (double)f;
 }
 
+static double bf16_bits(uint16_t b) {
+  uint32_t bits = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* Element (r, c) of an R x C expert matrix of type wdtype, in double. */
+static double welem(const void *M, int wdtype, size_t r, size_t c, size_t C) {
+  if (wdtype != 2) return elem(M, wdtype, r * C + c);
+  const oracle_q4 *q = (const oracle_q4 *)M;
+  const size_t i = r * C + c;
+  const uint8_t byte = q->codes[i / 2];
+#if ORACLE_MUTATION == 9
+  const unsigned code = (i & 1) ? (byte & 15u) : (byte >> 4); /* planted: nibbles swapped */
+#else
+  const unsigned code = (i & 1) ? (byte >> 4) : (byte & 15u);
+#endif
+  const size_t g = r * (C / ORACLE_Q4_GROUP) + c / ORACLE_Q4_GROUP;
+  return bf16_bits(q->scales[g]) * (double)code + bf16_bits(q->biases[g]);
+}
+
 /* y[r] = sum_c M[r][c] * v[c] for an R x C row-major matrix, double accumulate. */
 static void matvec(const void *M, int dtype, int R, int C, const double *v, double *y) {
   for (int r = 0; r < R; ++r) {
     double acc = 0.0;
-    for (int c = 0; c < C; ++c) acc += elem(M, dtype, (size_t)r * C + c) * v[c];
+    for (int c = 0; c < C; ++c) acc += welem(M, dtype, (size_t)r, (size_t)c, (size_t)C) * v[c];
     y[r] = acc;
   }
 }
@@ -150,8 +189,8 @@ static void expert_token(const oracle_dims *D, const double *xv, const void *wg,
                          const void *wd, double scale, double *out, double *g, double *u,
                          double *y) {
   const int d = D->d, F = D->F;
-  matvec(wg, D->dtype, F, d, xv, g);
-  matvec(wu, D->dtype, F, d, xv, u);
+  matvec(wg, D->wdtype, F, d, xv, g);
+  matvec(wu, D->wdtype, F, d, xv, u);
   for (int f = 0; f < F; ++f) {
 #if ORACLE_MUTATION == 7
     g[f] = u[f]; /* planted: activation dropped */
@@ -162,11 +201,11 @@ static void expert_token(const oracle_dims *D, const double *xv, const void *wg,
 #if ORACLE_MUTATION == 3
   for (int i = 0; i < d; ++i) { /* planted: output projection read transposed */
     double acc = 0.0;
-    for (int f = 0; f < F; ++f) acc += elem(wd, D->dtype, (size_t)f * d + i) * g[f];
+    for (int f = 0; f < F; ++f) acc += welem(wd, D->wdtype, (size_t)f, (size_t)i, (size_t)d) * g[f];
     y[i] = acc;
   }
 #else
-  matvec(wd, D->dtype, d, F, g, y);
+  matvec(wd, D->wdtype, d, F, g, y);
 #endif
   for (int i = 0; i < d; ++i) out[i] += scale * y[i];
 }
@@ -187,6 +226,8 @@ static int check_dims(const oracle_dims *D) {
   if (!D || D->d <= 0 || D->F <= 0 || D->E <= 0 || D->k <= 0 || D->k > D->E) return -1;
   if (D->n_shared != 0 && D->n_shared != 1) return -1;
   if (D->dtype != 0 && D->dtype != 1) return -1;
+  if (D->wdtype != 0 && D->wdtype != 1 && D->wdtype != 2) return -1;
+  if (D->wdtype == 2 && (D->d % ORACLE_Q4_GROUP || D->F % ORACLE_Q4_GROUP)) return -1;
   return 0;
 }
 

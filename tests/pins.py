@@ -201,7 +201,130 @@ def pin_hand_cases(mutation=0):
         assert counts.tolist() == exp["counts"], case["name"]
 
 
+# ---------------------------------------------------------------- 4-bit weights
+# The 4-bit group-affine format of "Optimizing on-device inference for Apple
+# Silicon", section "Dequantise weights within matrix multiplication": 4-bit
+# codes, one bfloat16 scale and one bfloat16 bias per 64 weights along a row,
+# w = scale * q + bias.  Reading of the pages (silent on the packing): two codes
+# per byte along the row, the even column in the low nibble.
+
+def _bf16(v: float) -> int:
+    """bfloat16 bit pattern of a value exactly representable in bfloat16."""
+    b = np.array([v], np.float32).view(np.uint32)[0]
+    assert b & 0xFFFF == 0, v
+    return int(b >> 16)
+
+
+def _q4(rows, cols, code=0, scale=1.0, bias=0.0):
+    """A rows x cols matrix with every code, scale and bias set to the given values."""
+    codes = np.full((rows, cols // 2), (code & 15) | ((code & 15) << 4), np.uint8)
+    sc = np.full((rows, cols // 64), _bf16(scale), np.uint16)
+    bi = np.full((rows, cols // 64), _bf16(bias), np.uint16)
+    return codes, sc, bi
+
+
+def _q4_probe(wg, x, mutation):
+    """E = 1, k = 1, no shared expert, up = all ones (code 0, bias 1), down =
+    all ones: out[i] = sum_f silu(g_f) with g = Wg x, and silu(0) = 0, so a
+    gate matrix with one non-zero row f0 gives out[i] = silu((Wg x)[f0])."""
+    d, F = x.shape[1], wg[0].shape[0]
+    wr = np.zeros((1, d), np.float32)
+    wu = _q4(F, d, 0, 1.0, 1.0)
+    wd = _q4(d, F, 0, 1.0, 1.0)
+    out, *_ = oracle.forward(x, wr, [wg], [wu], [wd], 1, nthreads=1, mutation=mutation, q4=True,
+                             F=F)
+    return out
+
+
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def pin_q4_nibble_order(mutation=0):
+    """One code byte 0x1F at column pair (2j, 2j + 1) of row 0, scale 1, bias 0:
+    the even column holds 15 (low nibble), the odd column 1 (high nibble)."""
+    d, F, j = 128, 64, 5
+    codes, sc, bi = _q4(F, d, 0, 1.0, 0.0)
+    codes[0, j] = 0x1F
+    x = np.zeros((2, d), np.float32)
+    x[0, 2 * j] = 1.0
+    x[1, 2 * j + 1] = 1.0
+    out = _q4_probe((codes, sc, bi), x, mutation)
+    assert np.allclose(out[0], _silu(15.0), rtol=0, atol=1e-12)
+    assert np.allclose(out[1], _silu(1.0), rtol=0, atol=1e-12)
+
+
+def pin_q4_groups_scale_bias(mutation=0):
+    """Row 0 with code 3 everywhere, scale 1 and bias 0.5 for columns 0..63,
+    scale 2 and bias -1 for columns 64..127: w = 3 s + b = 3.5 then 5 (a swap of
+    scale and bias, or a group of another size, gives other values)."""
+    d, F = 128, 64
+    codes, sc, bi = _q4(F, d, 0, 1.0, 0.0)
+    codes[0, :] = 0x33
+    sc[0, 0], bi[0, 0] = _bf16(1.0), _bf16(0.5)
+    sc[0, 1], bi[0, 1] = _bf16(2.0), _bf16(-1.0)
+    x = np.zeros((4, d), np.float32)
+    for t, c in enumerate((0, 63, 64, 127)):
+        x[t, c] = 1.0
+    out = _q4_probe((codes, sc, bi), x, mutation)
+    for t, w in enumerate((3.5, 3.5, 5.0, 5.0)):
+        assert np.allclose(out[t], _silu(w), rtol=0, atol=1e-12), (t, out[t, 0])
+
+
+def pin_q4_zero_codes_are_bias(mutation=0):
+    """Every code 0: each weight is its group's bias.  A gate row of bias b and
+    x = all ones gives g = d b for that row and 0 (bias 0) for the others; the
+    all-ones up matrix gives u = d for every row, so out[i] = silu(d b) d."""
+    d, F = 128, 64
+    codes, sc, bi = _q4(F, d, 0, 4.0, 0.0)
+    bi[0, :] = _bf16(0.25)
+    x = np.ones((1, d), np.float32)
+    out = _q4_probe((codes, sc, bi), x, mutation)
+    assert np.allclose(out[0], _silu(d * 0.25) * d, rtol=1e-14, atol=0)
+
+
+def pin_q4_matches_dense(mutation=0):
+    """Q4 expert weights whose values are exact in bfloat16 (power-of-two scales,
+    small biases) give the same block output as the same values stored dense."""
+    r = np.random.default_rng(31)
+    T, d, F, E, k = 6, 128, 64, 4, 2
+
+    def rand_q4(rows, cols):
+        codes = r.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+        sc = r.choice([_bf16(v) for v in (0.125, 0.25, 0.5)], (rows, cols // 64)).astype(np.uint16)
+        bi = r.choice([_bf16(v) for v in (-1.0, -0.5, 0.0, 0.5)], (rows, cols // 64)).astype(
+            np.uint16)
+        lo = (codes & 15).astype(np.float64)
+        hi = (codes >> 4).astype(np.float64)
+        q = np.stack([lo, hi], axis=-1).reshape(rows, cols)
+
+        def val(b):
+            return np.array(b, np.uint32).__lshift__(16).view(np.float32).astype(np.float64)
+
+        dense = q * np.repeat(val(sc), 64, axis=1) + np.repeat(val(bi), 64, axis=1)
+        return (codes, sc, bi), dense.astype(np.float32)
+
+    x = r.standard_normal((T, d)).astype(np.float32)
+    wr = (r.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+    q_g, q_u, q_d, d_g, d_u, d_d = [], [], [], [], [], []
+    for _ in range(E):
+        a, b = rand_q4(F, d)
+        q_g.append(a), d_g.append(b)
+        a, b = rand_q4(F, d)
+        q_u.append(a), d_u.append(b)
+        a, b = rand_q4(d, F)
+        q_d.append(a), d_d.append(b)
+    sq = [rand_q4(F, d), rand_q4(F, d), rand_q4(d, F)]
+    out_q, idx_q, *_ = oracle.forward(x, wr, q_g, q_u, q_d, k, sg=sq[0][0], su=sq[1][0],
+                                      sd=sq[2][0], nthreads=2, mutation=mutation, q4=True, F=F)
+    out_d, idx_d, *_ = oracle.forward(x, wr, np.stack(d_g), np.stack(d_u), np.stack(d_d), k,
+                                      sg=sq[0][1], su=sq[1][1], sd=sq[2][1], nthreads=2)
+    assert np.array_equal(idx_q, idx_d)
+    assert np.allclose(out_q, out_d, rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [pin_route_vs_numpy, pin_full_softmax_when_k_equals_E, pin_weights_sum_and_ratio,
             pin_two_expert_logistic, pin_bf16_widening, pin_bias_enters_logits, pin_dense_swiglu,
             pin_dense_plus_shared, pin_all_experts_masked, pin_permutation_equivariance,
-            pin_hand_cases]
+            pin_hand_cases, pin_q4_nibble_order, pin_q4_groups_scale_bias,
+            pin_q4_zero_codes_are_bias, pin_q4_matches_dense]

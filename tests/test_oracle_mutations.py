@@ -15,6 +15,7 @@ MUTATIONS = {
     6: "router weight transposed",
     7: "gated activation dropped",
     8: "histogram counts first choice only",
+    9: "4-bit codes read with the nibbles swapped",
 }
 
 
