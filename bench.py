@@ -4,10 +4,11 @@ Default workload (N=1): prefill of T=4096 tokens through one MoE layer
 (d=2048, 256 experts top-8 + 1 shared, F=512, bf16 weights and activations,
 fp32 accumulation), plus the batch-1 decode path over a stack of 40 distinct
 layers with a fresh token per step.  `value` is prefill tokens/s; the decode
-figures (microseconds per layer) are reported under "decode".
+figures (microseconds per layer) are reported under "decode", and those of the
+same stack with 4-bit group-affine expert weights under "decode_q4".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload prefill4k|skew16k|long128k|decode|tiny]
+                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|tiny]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; a 256 MiB buffer is written between timed
@@ -120,6 +121,8 @@ def make_layer(cfg: dict, dev, seed: int):
 # DRAM bytes of one batch-1 layer (kernels A + B + C, reads; nothing is
 # written back during them), from the ncu capture in profiles/decode_layer.md.
 DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
+# The same for the 4-bit layer: not captured yet.
+DECODE_Q4_TRAFFIC_LAYER = None
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
 # ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
 GEMM1_TRAFFIC_4K = 1_094_968_000 + 8_866_304
@@ -210,11 +213,16 @@ def bench_prefill(cfg, dev, steps, warmup, flush_buf):
     return res
 
 
-def bench_decode(dev, steps, warmup, n_layers=40):
+def bench_decode(dev, steps, warmup, n_layers=40, q4=False):
     cfg = WORKLOADS["prefill4k"]
     layers = []
     for l in range(n_layers):
-        layer, w, _ = make_layer(dict(cfg, chunk=1), dev, 1000 + l)
+        if q4:
+            w = synth.q4_layer_weights(1000 + l, cfg["d"], cfg["F"], cfg["E"], 1, dev)
+            layer = moe.Q4Layer(w, cfg["k"])
+            layer.keep = w
+        else:
+            layer, w, _ = make_layer(dict(cfg, chunk=1), dev, 1000 + l)
         layers.append(layer)
     d = cfg["d"]
     xs = synth.tokens(1, steps + warmup, d, "bf16", dev)
@@ -264,7 +272,7 @@ def bench_decode(dev, steps, warmup, n_layers=40):
     for layer in layers:
         layer.close()
     del g
-    return dict(times=times, clocks=clk.summary(), split=split, n_layers=n_layers)
+    return dict(times=times, clocks=clk.summary(), split=split, n_layers=n_layers, q4=q4)
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -322,7 +330,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill4k",
-                    choices=["prefill4k", "skew16k", "long128k", "tiny", "decode"])
+                    choices=["prefill4k", "skew16k", "long128k", "tiny", "decode", "decode_q4"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-layers", type=int, default=40,
                     help="distinct layers in the decode stack (40 in the benchmark; fewer for profiling)")
@@ -345,7 +353,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    wl_name = "prefill4k" if args.workload == "decode" else args.workload
+    wl_name = "prefill4k" if args.workload.startswith("decode") else args.workload
     cfg = WORKLOADS[wl_name]
     pk = peaks()
 
@@ -365,8 +373,9 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
 
-    if args.workload == "decode":
-        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers)
+    if args.workload.startswith("decode"):
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers,
+                           q4=args.workload == "decode_q4")
         emit_decode_line(args, dec, pk, world)
         return
 
@@ -443,7 +452,10 @@ def main():
     if not args.no_decode and wl_name == "prefill4k":
         dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers)
         line["decode"] = decode_summary(dec, pk)
-        line["gpu_launches"] += 0  # decode launches are counted in its own object
+        dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers,
+                           q4=True)
+        line["decode_q4"] = decode_summary(dec, pk)
+        # decode launches are counted in their own objects
     if rank == 0 and not args.no_cpu:
         nthr = host_threads()
         n_tok = min(args.oracle_tokens, T)
@@ -463,17 +475,23 @@ def decode_summary(dec, pk) -> dict:
     per_layer_us = [t * 1e3 / dec["n_layers"] for t in dec["times"]]
     med = statistics.median(per_layer_us)
     p90 = float(np.percentile(per_layer_us, 90))
-    byts = E * D * 2 + (K + 1) * 3 * F * D * 2
+    q4 = dec.get("q4", False)
+    # router rows (bf16) + the k + 1 experts' three matrices: 2 bytes a weight,
+    # or 4-bit codes plus a bf16 scale and bias per 64 weights (0.5625 bytes)
+    byts = E * D * 2 + (K + 1) * 3 * F * D * (0.5 + 4 / 64 if q4 else 2)
     achieved = byts / (med * 1e-6) / 1e9
     split = {k_: v[0] * 1e3 / max(v[1], 1) for k_, v in dec["split"].items() if v[1] > 0}
     return {
         "us_per_layer_median": med, "us_per_layer_p90": p90,
         "tokens_per_s": 1e6 / (med * dec["n_layers"]),
         "layers": dec["n_layers"], "steps": len(dec["times"]),
-        "workload": "batch-1 decode: one fresh token per step through 40 distinct layers "
-                    "(d=2048, 256 experts top-8 + 1 shared, F=512, bf16), CUDA graph per step",
+        "workload": f"batch-1 decode: one fresh token per step through {dec['n_layers']} "
+                    "distinct layers (d=2048, 256 experts top-8 + 1 shared, F=512, "
+                    + ("4-bit group-affine expert weights, bf16 router and tokens"
+                       if q4 else "bf16") + "), CUDA graph per step",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm"], "traffic": DECODE_TRAFFIC_LAYER,
+                     "frac": achieved / pk["hbm"],
+                     "traffic": DECODE_Q4_TRAFFIC_LAYER if q4 else DECODE_TRAFFIC_LAYER,
                      "algorithmic_bytes_per_layer": byts,
                      "peak_source": f"{pk['src']} hbm_gbs"},
         "eager_us_per_launch": split,

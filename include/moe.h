@@ -96,6 +96,60 @@ typedef struct {
 int moe_create(const moe_config *cfg, moe_handle **out);
 
 /*
+ * 4-bit group-affine expert weights ("Optimizing on-device inference for
+ * Apple Silicon", section "Dequantise weights within matrix multiplication":
+ * 4-bit codes with one scale and one bias per group of 64 weights; the block's
+ * arithmetic is unchanged, only the weights are stored smaller).
+ *
+ * A matrix [rows][cols] (cols a multiple of 64, K-contiguous like the bf16
+ * layouts above) is three device arrays:
+ *   codes  [rows][cols / 2] uint8, two codes per byte along the row, the even
+ *          column in the low nibble;
+ *   scales [rows][cols / 64] bfloat16 bit patterns;
+ *   biases [rows][cols / 64] bfloat16 bit patterns;
+ * and element (r, c) is  w = scale[r][c / 64] * q + bias[r][c / 64]  with q the
+ * 4-bit code (0..15).  All three pointers 16-byte aligned.
+ */
+typedef struct {
+  const uint8_t *codes;
+  const uint16_t *scales;
+  const uint16_t *biases;
+} moe_q4_matrix;
+
+typedef struct {
+  moe_q4_matrix gate;    /* [E * F][d] */
+  moe_q4_matrix up;      /* [E * F][d] */
+  moe_q4_matrix down;    /* [E * d][F] */
+  moe_q4_matrix s_gate;  /* [F][d], all NULL iff n_shared == 0 */
+  moe_q4_matrix s_up;    /* [F][d] */
+  moe_q4_matrix s_down;  /* [d][F] */
+} moe_q4_weights;
+
+/*
+ * moe_create for a layer whose expert weights (routed and shared) are 4-bit
+ * group-affine; the router stays bfloat16.  cfg is as for moe_create with
+ * dtype MOE_BF16 (tokens and outputs are bf16) and w_gate, w_up, w_down,
+ * s_gate, s_up, s_down NULL; w holds the 4-bit matrices instead (kept by
+ * pointer, like the bf16 weights).  Supported: as moe_create; the handle runs
+ * moe_forward with T == 1 (the batch-1 path, which reads 3.6x fewer weight
+ * bytes) and moe_route; moe_forward with T >= 2 returns MOE_ERR_UNSUPPORTED.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, OUT_OF_MEMORY, CUDA.
+ */
+int moe_create_q4(const moe_config *cfg, const moe_q4_weights *w, moe_handle **out);
+
+/*
+ * Quantise a device matrix w[rows][cols] (dtype MOE_BF16 or MOE_F32, cols a
+ * multiple of 64) into the 4-bit group-affine format above: per group of 64
+ * along a row, bias = min rounded to bfloat16, scale = (max - min) / 15 rounded
+ * to bfloat16 (0 for a constant group), q = the nearest integer to
+ * (w - bias) / scale clamped to 0..15 (0 when scale is 0).  Writes codes,
+ * scales and biases (device, 16-byte aligned).  Asynchronous on cuda_stream.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+int moe_quantize_q4(const void *w, moe_dtype dtype, long long rows, int cols, uint8_t *codes,
+                    uint16_t *scales, uint16_t *biases, void *cuda_stream);
+
+/*
  * Routing only (the router and the routing half of the block): for T tokens
  * x[T][d] (device) writes, all device:
  *   topk_idx[T][k] int32   chosen experts of each token, by descending logit,

@@ -181,3 +181,63 @@ def forward(x, wr, wg, wu, wd, k, sg=None, su=None, sd=None, bias=None, nthreads
         raise RuntimeError(f"oracle_forward failed: {rc}")
     del keep  # the pointed-to arrays lived until here
     return out, idx, w, counts
+
+
+def _bf16_bits(v: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _bf16_value(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def quantize_q4(w, mutation: int = 0):
+    """4-bit group-affine quantisation of w[rows][cols] (float32, or bf16 bits as
+    uint16), cols a multiple of 64.  Returns (codes uint8 [rows][cols/2], scales
+    uint16 [rows][cols/64], biases uint16 [rows][cols/64]), bf16 bit patterns.
+
+    "Optimizing on-device inference for Apple Silicon", section "Dequantise
+    weights within matrix multiplication": every weight is a 4-bit code and
+    every group of 64 weights shares one bfloat16 scale and one bias, from which
+    its values are rebuilt as scale * code + bias.  The page does not say how
+    the codes are chosen; the reading taken here is the plain min/max one:
+    bias = the group minimum and scale = (max - min) / 15, each rounded to
+    bfloat16, code = the nearest integer (ties to even) to (w - bias) / scale,
+    clamped to 0..15 (0 where the scale is 0).  Every decision is taken in
+    float32.  Packing: two codes per byte along the row, the even column in the
+    low nibble.
+
+    mutation plants a mistake for the pin tests: 1 packs the odd column in the
+    low nibble, 2 rounds the code down, 3 divides the range by 16.
+    """
+    w = np.asarray(w)
+    v = _bf16_value(w) if w.dtype == np.uint16 else np.asarray(w, np.float32)
+    rows, cols = v.shape
+    assert cols % 64 == 0
+    g = v.reshape(rows, cols // 64, 64)
+    lo = g.min(axis=2)
+    hi = g.max(axis=2)
+    steps = np.float32(16.0 if mutation == 3 else 15.0)
+    scales = _bf16_bits((hi - lo) / steps)
+    biases = _bf16_bits(lo)
+    s = _bf16_value(scales)[:, :, None]
+    b = _bf16_value(biases)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (g - b) / np.where(s > 0, s, np.float32(1.0))
+    q = np.floor(r) if mutation == 2 else np.rint(r)
+    q = np.where(s > 0, np.clip(q, 0, 15), 0).astype(np.uint8).reshape(rows, cols)
+    even, odd = q[:, 0::2], q[:, 1::2]
+    codes = (odd | (even << 4)) if mutation == 1 else (even | (odd << 4))
+    return codes.astype(np.uint8), scales, biases
+
+
+def dequantize_q4(codes, scales, biases) -> np.ndarray:
+    """float64 values scale * code + bias of a 4-bit matrix (layout as quantize_q4)."""
+    codes = np.asarray(codes, np.uint8)
+    rows = codes.shape[0]
+    q = np.stack([codes & 15, codes >> 4], axis=-1).reshape(rows, -1).astype(np.float64)
+    s = np.repeat(_bf16_value(scales).astype(np.float64), 64, axis=1)
+    b = np.repeat(_bf16_value(biases).astype(np.float64), 64, axis=1)
+    return q * s + b

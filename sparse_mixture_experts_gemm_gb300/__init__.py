@@ -37,7 +37,9 @@ KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "de
 
 EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_status", "moe_destroy",
             "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
-            "moe_decode_noalloc"]
+            "moe_decode_noalloc", "moe_create_q4", "moe_quantize_q4"]
+
+Q4_GROUP = 64  # columns per (scale, bias) pair of the 4-bit format
 
 
 class MoeError(RuntimeError):
@@ -54,6 +56,15 @@ class moe_config(ctypes.Structure):
                 ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
                 ("s_down", ctypes.c_void_p), ("router_bias", ctypes.c_void_p)]
+
+
+class moe_q4_matrix(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p)]
+
+
+class moe_q4_weights(ctypes.Structure):
+    _fields_ = [(n, moe_q4_matrix) for n in ("gate", "up", "down", "s_gate", "s_up", "s_down")]
 
 
 _lib = None
@@ -87,6 +98,9 @@ def lib() -> ctypes.CDLL:
                                    ctypes.POINTER(ctypes.c_int64), ip]
     L.moe_debug_wait_timeout.argtypes = [vp, ip, vp]
     L.moe_decode_noalloc.argtypes = [ctypes.POINTER(moe_config), vp, vp, vp]
+    L.moe_create_q4.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_q4_weights),
+                                ctypes.POINTER(vp)]
+    L.moe_quantize_q4.argtypes = [vp, ip, ctypes.c_longlong, ip, vp, vp, vp, vp]
     for name in EXPORTED:
         if name != "moe_strerror":
             getattr(L, name).restype = ip
@@ -179,6 +193,34 @@ def moe_decode_noalloc(cfg: moe_config, x, out, stream=None) -> int:
                                            _stream(stream)), "moe_decode_noalloc")
 
 
+def moe_create_q4(cfg: moe_config, w: moe_q4_weights) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().moe_create_q4(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)),
+           "moe_create_q4")
+    return h.value
+
+
+def moe_quantize_q4(w, dtype: int, rows: int, cols: int, codes, scales, biases,
+                    stream=None) -> int:
+    return _check(lib().moe_quantize_q4(_ptr(w), dtype, rows, cols, _ptr(codes), _ptr(scales),
+                                        _ptr(biases), _stream(stream)), "moe_quantize_q4")
+
+
+def quantize_q4(w, stream=None):
+    """4-bit group-affine copy of a CUDA tensor w[..., cols] (bf16 or f32): returns
+    (codes uint8 [..., cols/2], scales, biases: bf16 bits as int16 [..., cols/64])."""
+    import torch
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    lead = tuple(w.shape[:-1])
+    codes = torch.empty(lead + (cols // 2,), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(lead + (cols // Q4_GROUP,), dtype=torch.int16, device=w.device)
+    biases = torch.empty_like(scales)
+    dt = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}[w.dtype]
+    moe_quantize_q4(w.contiguous(), dt, rows, cols, codes, scales, biases, stream)
+    return codes, scales, biases
+
+
 # ----------------------------------------------------------------- wrapper
 class MoELayer:
     """One layer: owns the handle, keeps the caller's weight tensors alive.
@@ -236,3 +278,37 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+class Q4Layer(MoELayer):
+    """One layer whose expert weights are 4-bit group-affine (moe_create_q4).
+
+    weights: dict with Wr [E][d] bf16 (the router stays bf16), and Wg, Wu, Wd,
+    Sg, Su, Sd as (codes, scales, biases) triples of CUDA tensors in the layouts
+    of the bf16 matrices ([E][F][d] -> codes [E][F][d/2], scales and biases
+    [E][F][d/64]); shared triples None when there is no shared expert.  Runs the
+    batch-1 path (forward with one token) and routing.
+    """
+
+    def __init__(self, weights: dict, top_k: int, bias=None):
+        import torch
+        Wr = weights["Wr"]
+        assert Wr.dtype == torch.bfloat16
+        E, d = Wr.shape
+        F = weights["Wg"][0].shape[1]
+        shared = weights.get("Sg") is not None
+        self.weights = weights
+        self.bias = bias
+        self.dtype = Wr.dtype
+        self.d, self.E, self.F, self.k = d, E, F, top_k
+
+        def mat(t):
+            return moe_q4_matrix(*(None, None, None) if t is None else (_ptr(x) for x in t))
+
+        qw = moe_q4_weights(mat(weights["Wg"]), mat(weights["Wu"]), mat(weights["Wd"]),
+                            mat(weights.get("Sg")), mat(weights.get("Su")),
+                            mat(weights.get("Sd")))
+        cfg = moe_config(d, E, top_k, F, 1 if shared else 0, 1, MOE_BF16, _ptr(Wr), None, None,
+                         None, None, None, None, _ptr(bias))
+        self.cfg, self.qw = cfg, qw
+        self.handle = moe_create_q4(cfg, qw)

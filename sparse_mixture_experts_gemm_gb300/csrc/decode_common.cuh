@@ -149,5 +149,45 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
   }
 }
 
+// Up to kPre 16-byte vectors of one row held in registers per lane: vector
+// u * 32 + lane for u < kPre.  Loads issued before a dependency wait overlap
+// the previous kernel's tail.
+constexpr int kPre = 8;
+
+struct RowPre {
+  uint4 v[kPre];
+};
+
+__device__ __forceinline__ void row_prefetch(RowPre &r, const uint4 *row, int nvec, int lane) {
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = u * 32 + lane;
+    if (i < nvec) r.v[u] = ld_stream16(row + i);
+  }
+}
+
+// dot(row, x) for a row whose first 32 * kPre vectors are in r; the rest (rows
+// longer than 256 vectors) are streamed here.  xv: the token in shared memory.
+template <typename T>
+__device__ __forceinline__ float row_dot_pre(const RowPre &r, const uint4 *row, const uint4 *xv,
+                                             int nvec, int lane) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = u * 32 + lane;
+    if (i < nvec) acc += V16<T>::dot(r.v[u], xv[i]);
+  }
+  for (int i = 32 * kPre + lane; i < nvec; i += 32) acc += V16<T>::dot(ld_stream16(row + i), xv[i]);
+  return acc;
+}
+
+// The token into shared memory (all threads; L2 reads, written by the kernel
+// this one waited for), once per CTA rather than once per warp.
+__device__ __forceinline__ void load_token(uint4 *xs, const void *x, int nvec) {
+  const uint4 *xg = static_cast<const uint4 *>(x);
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  __syncthreads();
+}
+
 }  // namespace
 }  // namespace moe

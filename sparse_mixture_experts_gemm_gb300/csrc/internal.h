@@ -99,6 +99,18 @@ template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);
 
+// 4-bit group-affine matrix (codes two per byte, even column in the low
+// nibble; one bf16 scale and bias per 64 columns of a row)
+constexpr int kQ4Group = 64;
+struct Q4Mat {
+  const uint8_t *c;   // [rows][cols / 2]
+  const uint16_t *s;  // [rows][cols / 64]
+  const uint16_t *b;  // [rows][cols / 64]
+};
+struct Q4Weights {
+  Q4Mat g, u, d, sg, su, sd;
+};
+
 // decode.cu
 struct DecodeArgs {
   const void *x;
@@ -113,7 +125,17 @@ struct DecodeArgs {
   int rows_a;          // kernel A: router rows or shared items per CTA
   int ring;            // kernel B: ring slots per CTA
   int c_rows;          // kernel C: output rows per CTA (upper bound)
+  Q4Weights q;         // 4-bit expert weights (decode_q4.cu), unused by the bf16 kernels
 };
+// decode_q4.cu: the batch-1 kernels for 4-bit expert weights (bf16 tokens,
+// bf16 router) and the quantiser
+cudaError_t launch_decode_router_q4(const DecodeArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_gateup_q4(const DecodeArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_down_q4(const DecodeArgs &a, cudaStream_t st, bool pdl);
+cudaError_t decode_q4_set_smem_attr();
+template <typename T>
+cudaError_t launch_quantize_q4(const T *w, long long rows, int cols, uint8_t *codes,
+                               uint16_t *scales, uint16_t *biases, cudaStream_t st);
 template <typename T>
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t st, bool pdl);
 // tmG / tmU: w_gate / w_up as [E * F][d] with boxes of (512 bytes) x 32 rows, no swizzle

@@ -115,6 +115,9 @@ struct moe_handle {
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
   CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
+  // 4-bit expert weights (moe_create_q4)
+  bool q4 = false;
+  Q4Weights qw = {};
   // profiling
   bool prof = false;
   std::vector<ProfRec> recs;
@@ -127,15 +130,24 @@ struct moe_handle {
 
 namespace {
 
-int check_cfg(const moe_config *c) {
+// q4: the expert weights come as 4-bit matrices (moe_create_q4), so the bf16
+// expert pointers must be NULL.
+int check_cfg(const moe_config *c, bool q4 = false) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
   if (c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0 ||
       c->max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
   if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_INVALID_ARG;
-  if (!c->w_router || !c->w_gate || !c->w_up || !c->w_down) return MOE_ERR_INVALID_ARG;
-  if (c->n_shared && (!c->s_gate || !c->s_up || !c->s_down)) return MOE_ERR_INVALID_ARG;
+  if (!c->w_router) return MOE_ERR_INVALID_ARG;
+  if (q4) {
+    if (c->w_gate || c->w_up || c->w_down || c->s_gate || c->s_up || c->s_down)
+      return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (!c->w_gate || !c->w_up || !c->w_down) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared && (!c->s_gate || !c->s_up || !c->s_down)) return MOE_ERR_INVALID_ARG;
+  }
   if (c->d_model % 256 != 0 || c->d_model > 16384) return MOE_ERR_UNSUPPORTED;
   if (c->d_ff % 128 != 0 || c->d_ff > 4096) return MOE_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
@@ -330,6 +342,22 @@ int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
   a.out = out;
   a.status = h->status;
   const bool pdl = !h->prof;  // event records between kernels would break the chain
+  if (h->q4) {
+    a.q = h->qw;
+    {
+      ProfScope ps(h, MOE_KERNEL_DECODE_ROUTER, st);
+      MOE_TRY(launch_decode_router_q4(a, st, pdl));
+    }
+    {
+      ProfScope ps(h, MOE_KERNEL_DECODE_GATE_UP, st);
+      MOE_TRY(launch_decode_gateup_q4(a, st, pdl));
+    }
+    {
+      ProfScope ps(h, MOE_KERNEL_DECODE_DOWN, st);
+      MOE_TRY(launch_decode_down_q4(a, st, pdl));
+    }
+    return MOE_OK;
+  }
   {
     ProfScope ps(h, MOE_KERNEL_DECODE_ROUTER, st);
     MOE_TRY(launch_decode_router<T>(a, st, pdl));
@@ -371,11 +399,33 @@ const char *moe_strerror(int code) {
   }
 }
 
-int moe_create(const moe_config *cfg, moe_handle **out) {
+}  // extern "C"
+
+namespace {
+
+// Checks of one 4-bit matrix [rows][cols]: present and 16-byte aligned.
+int check_q4(const moe_q4_matrix &m) {
+  if (!m.codes || !m.scales || !m.biases) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(m.codes) || !aligned16(m.scales) || !aligned16(m.biases)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+Q4Mat q4mat(const moe_q4_matrix &m) { return Q4Mat{m.codes, m.scales, m.biases}; }
+
+int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
-  int rc = check_cfg(cfg);
+  int rc = check_cfg(cfg, q4 != nullptr);
   if (rc != MOE_OK) return rc;
+  if (q4) {
+    const moe_q4_matrix *ms[] = {&q4->gate, &q4->up, &q4->down, &q4->s_gate, &q4->s_up,
+                                 &q4->s_down};
+    for (int i = 0; i < (cfg->n_shared ? 6 : 3); ++i)
+      if ((rc = check_q4(*ms[i])) != MOE_OK) return rc;
+    // the batch-1 down kernel spreads the (slot, 64-column group) pairs of a
+    // row over one warp, at most 5 per lane
+    if ((cfg->top_k + cfg->n_shared) * (cfg->d_ff / kQ4Group) > 32 * 5) return MOE_ERR_UNSUPPORTED;
+  }
   moe_handle *h = new (std::nothrow) moe_handle();
   if (!h) return MOE_ERR_OUT_OF_MEMORY;
   h->cfg = *cfg;
@@ -434,18 +484,31 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
   }
 
   // tensor maps of the weights and the fixed workspace buffers
-  bool ok = encode_map_2d(&h->tm_dg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d,
-                          static_cast<uint32_t>(512 / esz), 32, false) &&
-            encode_map_2d(&h->tm_du, c.w_up, esz, static_cast<uint64_t>(E) * F, d,
-                          static_cast<uint32_t>(512 / esz), 32, false) &&
-            make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
-            make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
-            make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
-            make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN) &&
+  bool ok = make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
             make_map(&h->tm_wr, c.w_router, esz, E, d, kRouterBN);
-  if (ok && c.n_shared)
+  if (ok && !q4)
+    ok = encode_map_2d(&h->tm_dg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d,
+                       static_cast<uint32_t>(512 / esz), 32, false) &&
+         encode_map_2d(&h->tm_du, c.w_up, esz, static_cast<uint64_t>(E) * F, d,
+                       static_cast<uint32_t>(512 / esz), 32, false) &&
+         make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
+         make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
+         make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN);
+  if (ok && !q4 && c.n_shared)
     ok = make_map(&h->tm_sg, c.s_gate, esz, F, d, kBM) &&
          make_map(&h->tm_su, c.s_up, esz, F, d, kBM) && make_map(&h->tm_sd, c.s_down, esz, d, F, kBN);
+  if (q4) {
+    h->q4 = true;
+    h->qw.g = q4mat(q4->gate);
+    h->qw.u = q4mat(q4->up);
+    h->qw.d = q4mat(q4->down);
+    if (c.n_shared) {
+      h->qw.sg = q4mat(q4->s_gate);
+      h->qw.su = q4mat(q4->s_up);
+      h->qw.sd = q4mat(q4->s_down);
+    }
+    if (ok && decode_q4_set_smem_attr() != cudaSuccess) ok = false;
+  }
   if (!ok) {
     moe_destroy(h);
     return MOE_ERR_CUDA;
@@ -459,6 +522,37 @@ int moe_create(const moe_config *cfg, moe_handle **out) {
     return rc;
   }
   *out = h;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_create(const moe_config *cfg, moe_handle **out) { return create_impl(cfg, nullptr, out); }
+
+int moe_create_q4(const moe_config *cfg, const moe_q4_weights *w, moe_handle **out) {
+  if (!w) {
+    if (out) *out = nullptr;
+    return MOE_ERR_INVALID_ARG;
+  }
+  return create_impl(cfg, w, out);
+}
+
+int moe_quantize_q4(const void *w, moe_dtype dtype, long long rows, int cols, uint8_t *codes,
+                    uint16_t *scales, uint16_t *biases, void *cuda_stream) {
+  if (rows < 0 || cols <= 0 || cols % kQ4Group) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!w || !codes || !scales || !biases) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(biases))
+    return MOE_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (dtype == MOE_BF16)
+    MOE_TRY(launch_quantize_q4(static_cast<const __nv_bfloat16 *>(w), rows, cols, codes, scales,
+                               biases, st));
+  else
+    MOE_TRY(launch_quantize_q4(static_cast<const float *>(w), rows, cols, codes, scales, biases, st));
   return MOE_OK;
 }
 
@@ -502,6 +596,7 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
   char *ob = static_cast<char *>(out);
   if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (h->q4 && T != 1) return MOE_ERR_UNSUPPORTED;  // 4-bit weights: batch-1 path only
   if (T == 1) {
     return h->cfg.dtype == MOE_BF16
                ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),

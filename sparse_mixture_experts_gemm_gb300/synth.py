@@ -5,7 +5,8 @@ This module only draws random numbers.  It holds none of the block's arithmetic
 their inputs from it.  Every tensor comes from one ``torch.Generator`` on the
 device the tensor is made on, seeded once per call, in a fixed order:
 
-    Wr, Sg, Su, Sd, Wg, Wu, Wd        (layer_weights)
+    Wr, Sg, Su, Sd, Wg, Wu, Wd        (layer_weights, q4_layer_weights; a 4-bit
+                                       matrix draws codes, scales, biases)
     x                                 (tokens)
 
 Distributions follow the workloads the block is measured on: activations
@@ -61,6 +62,45 @@ def layer_weights(seed: int, d: int, F: int, E: int, n_shared: int = 1, dtype="b
     w["Wg"] = _normal((E, F, d), sd_in, g, dtype, device)
     w["Wu"] = _normal((E, F, d), sd_in, g, dtype, device)
     w["Wd"] = _normal((E, d, F), sd_ff, g, dtype, device)
+    return w
+
+
+def _q4_matrix(shape, std, g, device):
+    """Random 4-bit group-affine matrix of logical shape [..., rows, cols]:
+    codes uniform over 0..15 (two per byte), per 64-column group a bfloat16
+    scale ~ std * U(0.27, 0.37) and bias ~ -std * U(2.0, 2.8), about the
+    steps and minima that groups of 64 N(0, std^2) weights give."""
+    *lead, rows, cols = shape
+    codes = torch.randint(0, 256, (*lead, rows, cols // 2), dtype=torch.uint8, device=device,
+                          generator=g)
+    gs = (*lead, rows, cols // 64)
+    sc = torch.empty(gs, dtype=torch.float32, device=device).uniform_(0.27 * std, 0.37 * std,
+                                                                      generator=g)
+    bi = torch.empty(gs, dtype=torch.float32, device=device).uniform_(-2.8 * std, -2.0 * std,
+                                                                      generator=g)
+    return (codes, sc.to(torch.bfloat16).view(torch.int16),
+            bi.to(torch.bfloat16).view(torch.int16))
+
+
+def q4_layer_weights(seed: int, d: int, F: int, E: int, n_shared: int = 1,
+                     device="cpu") -> dict:
+    """One layer with 4-bit expert weights: Wr [E][d] bfloat16 as in
+    layer_weights, and Wg, Wu, Wd, Sg, Su, Sd as (codes uint8, scales int16,
+    biases int16) triples, bfloat16 bits in the int16 tensors, in the layouts
+    of the bf16 matrices (codes [.., rows][cols / 2], scales and biases
+    [.., rows][cols / 64])."""
+    g = _gen(seed, device)
+    sd_in, sd_ff = 1.0 / math.sqrt(d), 1.0 / math.sqrt(F)
+    w = {"Wr": _normal((E, d), sd_in, g, torch.bfloat16, device)}
+    if n_shared:
+        w["Sg"] = _q4_matrix((F, d), sd_in, g, device)
+        w["Su"] = _q4_matrix((F, d), sd_in, g, device)
+        w["Sd"] = _q4_matrix((d, F), sd_ff, g, device)
+    else:
+        w["Sg"] = w["Su"] = w["Sd"] = None
+    w["Wg"] = _q4_matrix((E, F, d), sd_in, g, device)
+    w["Wu"] = _q4_matrix((E, F, d), sd_in, g, device)
+    w["Wd"] = _q4_matrix((E, d, F), sd_ff, g, device)
     return w
 
 

@@ -323,6 +323,63 @@ def pin_q4_matches_dense(mutation=0):
     assert np.allclose(out_q, out_d, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- the quantiser
+# oracle.quantize_q4 (the reading of the pages stated in its docstring) against
+# what the format fixes: values already on a group's grid come back exactly,
+# every value lands within half a step of its code, a constant group has
+# scale 0.
+
+def _grid_matrix(r, rows, cols):
+    """Codes, scales and biases with power-of-two scales and small biases, each
+    group using both code 0 and code 15, and the float32 values they encode."""
+    q = r.integers(0, 16, (rows, cols)).astype(np.uint8)
+    q[:, 0::64] = 0
+    q[:, 1::64] = 15
+    sc = r.choice([0.0078125, 0.015625, 0.03125, 0.0625], (rows, cols // 64)).astype(np.float32)
+    bi = r.choice([-0.25, -0.125, -0.0625, 0.03125], (rows, cols // 64)).astype(np.float32)
+    vals = q * np.repeat(sc, 64, axis=1) + np.repeat(bi, 64, axis=1)
+    # explicit byte layout: column 2j in the low nibble of byte j
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    for j in range(cols // 2):
+        codes[:, j] = q[:, 2 * j] + 16 * q[:, 2 * j + 1]
+    bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)  # exact: few mantissa bits
+    return codes, bits(sc), bits(bi), vals.astype(np.float32)
+
+
+def pin_quantize_recovers_grid(mutation=0):
+    r = np.random.default_rng(41)
+    codes, sc, bi, vals = _grid_matrix(r, 6, 256)
+    c2, s2, b2 = oracle.quantize_q4(vals, mutation=mutation)
+    assert np.array_equal(s2, sc) and np.array_equal(b2, bi)
+    assert np.array_equal(c2, codes)
+    # the same from bfloat16 input (the values are exact in bfloat16)
+    c3, s3, b3 = oracle.quantize_q4(oracle._bf16_bits(vals), mutation=mutation)
+    assert np.array_equal(c3, codes) and np.array_equal(s3, sc) and np.array_equal(b3, bi)
+
+
+def pin_quantize_half_step_bound(mutation=0):
+    """Random N(0, 1/2048) weights: |scale * q + bias - w| <= scale / 2 up to
+    the bfloat16 rounding of scale and bias (2^-8 relative)."""
+    r = np.random.default_rng(43)
+    w = (r.standard_normal((64, 512)) / math.sqrt(2048)).astype(np.float32)
+    c, sc, bi = oracle.quantize_q4(w, mutation=mutation)
+    err = np.abs(oracle.dequantize_q4(c, sc, bi) - w).reshape(64, 8, 64).max(axis=2)
+    s = oracle._bf16_value(sc).astype(np.float64)
+    b = np.abs(oracle._bf16_value(bi).astype(np.float64))
+    assert (err <= s / 2 + 2.0 ** -8 * (b + 15 * s)).all(), (err / s).max()
+
+
+def pin_quantize_constant_group(mutation=0):
+    w = np.full((2, 128), 0.3, np.float32)
+    w[1, 64:] = -2.5
+    c, sc, bi = oracle.quantize_q4(w, mutation=mutation)
+    assert (sc == 0).all() and (c == 0).all()
+    assert np.allclose(oracle._bf16_value(bi), [[0.30078125, 0.30078125], [0.30078125, -2.5]])
+
+
+QUANT_PINS = [pin_quantize_recovers_grid, pin_quantize_half_step_bound,
+              pin_quantize_constant_group]
+
 ALL_PINS = [pin_route_vs_numpy, pin_full_softmax_when_k_equals_E, pin_weights_sum_and_ratio,
             pin_two_expert_logistic, pin_bf16_widening, pin_bias_enters_logits, pin_dense_swiglu,
             pin_dense_plus_shared, pin_all_experts_masked, pin_permutation_equivariance,

@@ -89,3 +89,57 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         moe.lib()
+
+
+def _q4w(**kw):
+    w = moe.moe_q4_weights()
+    for i, name in enumerate(("gate", "up", "down", "s_gate", "s_up", "s_down")):
+        base = 0x10000 * (i + 1)
+        setattr(w, name, moe.moe_q4_matrix(base, base + 0x1000, base + 0x2000))
+    for name, m in kw.items():
+        setattr(w, name, m)
+    return w
+
+
+def _q4cfg(**kw):
+    return _cfg(**{**dict(w_gate=None, w_up=None, w_down=None, s_gate=None, s_up=None,
+                          s_down=None), **kw})
+
+
+@pytest.mark.parametrize("cfg_kw,w_kw,code", [
+    (dict(w_gate=0x2000), {}, moe.MOE_ERR_INVALID_ARG),       # bf16 expert weights given too
+    (dict(s_down=0x7000), {}, moe.MOE_ERR_INVALID_ARG),
+    (dict(dtype=moe.MOE_F32), {}, moe.MOE_ERR_UNSUPPORTED),    # 4-bit layers take bf16 tokens
+    (dict(w_router=None), {}, moe.MOE_ERR_INVALID_ARG),
+    ({}, dict(up=moe.moe_q4_matrix(0x20000, None, 0x22000)), moe.MOE_ERR_INVALID_ARG),
+    ({}, dict(down=moe.moe_q4_matrix(0x30008, 0x31000, 0x32000)), moe.MOE_ERR_ALIGNMENT),
+    ({}, dict(s_gate=moe.moe_q4_matrix(None, None, None)), moe.MOE_ERR_INVALID_ARG),
+    # (top_k + n_shared) * d_ff / 64 = 9 * 32 > 160 pairs per down row
+    (dict(top_k=8, d_ff=2048, n_experts=16), {}, moe.MOE_ERR_UNSUPPORTED),
+    (dict(d_model=520), {}, moe.MOE_ERR_UNSUPPORTED),
+])
+def test_create_q4_rejects_bad_config_on_host(lib, cfg_kw, w_kw, code):
+    h = ctypes.c_void_p()
+    rc = lib.moe_create_q4(ctypes.byref(_q4cfg(**cfg_kw)), ctypes.byref(_q4w(**w_kw)),
+                           ctypes.byref(h))
+    assert rc == code and h.value is None
+
+
+def test_create_q4_null_weights(lib):
+    h = ctypes.c_void_p()
+    assert lib.moe_create_q4(ctypes.byref(_q4cfg()), None, ctypes.byref(h)) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert h.value is None
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0x1000, moe.MOE_BF16, 4, 100, 0x2000, 0x3000, 0x4000), moe.MOE_ERR_INVALID_ARG),  # cols % 64
+    ((0x1000, moe.MOE_BF16, -1, 64, 0x2000, 0x3000, 0x4000), moe.MOE_ERR_INVALID_ARG),
+    ((0x1000, 5, 4, 64, 0x2000, 0x3000, 0x4000), moe.MOE_ERR_INVALID_ARG),              # dtype
+    ((0x1000, moe.MOE_BF16, 4, 64, None, 0x3000, 0x4000), moe.MOE_ERR_INVALID_ARG),
+    ((0x1000, moe.MOE_F32, 4, 64, 0x2008, 0x3000, 0x4000), moe.MOE_ERR_ALIGNMENT),
+    ((0x1002, moe.MOE_BF16, 4, 64, 0x2000, 0x3000, 0x4000), moe.MOE_ERR_ALIGNMENT),
+    ((None, moe.MOE_BF16, 0, 64, None, None, None), moe.MOE_OK),                      # no rows
+])
+def test_quantize_q4_validates_on_host(lib, args, code):
+    assert lib.moe_quantize_q4(*args, None) == code

@@ -1,0 +1,164 @@
+"""4-bit group-affine expert weights on the GPU, through the C ABI.
+
+* moe_quantize_q4 against oracle.quantize_q4 on the same values: codes, scales
+  and biases bit for bit (both sides take every decision in float32).
+* The batch-1 path of a 4-bit handle (moe_create_q4, moe_forward with T == 1)
+  against the oracle's 4-bit forward on the same codes, scales and biases,
+  drawn by the seeded generator: block output within 1e-2 row-normwise
+  relative error, as for the bf16 path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import oracle
+import sparse_mixture_experts_gemm_gb300 as moe
+from sparse_mixture_experts_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+    moe.lib()
+    return torch.device("cuda:0")
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype,shape", [
+    ("bf16", (8, 64)),
+    ("bf16", (256, 2048)),
+    ("bf16", (3, 512, 2048)),      # a stack of expert matrices
+    ("f32", (100, 4096)),
+    ("f32", (17, 192)),
+])
+def test_quantizer_matches_oracle(dev, dtype, shape):
+    g = torch.Generator(device=dev)
+    g.manual_seed(hash(shape) % 1000)
+    w = torch.empty(shape, dtype=synth._dt(dtype), device=dev).normal_(0, 0.02, generator=g)
+    # a few constant groups and one group with a single outlier
+    flat = w.view(-1, shape[-1])
+    flat[0, :64] = 0.375
+    if flat.shape[0] > 2:
+        flat[2, :64] = 0.0
+        flat[2, 7] = 1.0
+    codes, scales, biases = moe.quantize_q4(w)
+    torch.cuda.synchronize()
+    host = H.np_view(flat)
+    rc, rs, rb = oracle.quantize_q4(host)
+    assert np.array_equal(codes.view(-1, shape[-1] // 2).cpu().numpy(), rc)
+    assert np.array_equal(_bits(scales.view(-1, shape[-1] // 64)), rs)
+    assert np.array_equal(_bits(biases.view(-1, shape[-1] // 64)), rb)
+
+
+def _oracle_q4(x, w, k, F):
+    """The oracle's 4-bit forward on the same codes, scales and biases."""
+    E = w["Wr"].shape[0]
+
+    def triple(t):
+        return None if t is None else (t[0].cpu().numpy(), _bits(t[1]), _bits(t[2]))
+
+    per = {n: triple(w[n]) for n in ("Wg", "Wu", "Wd")}
+    experts = {n: [(c[e], s[e], b[e]) for e in range(E)] for n, (c, s, b) in per.items()}
+    return oracle.forward(H.np_view(x), H.np_view(w["Wr"]), experts["Wg"], experts["Wu"],
+                          experts["Wd"], k, sg=triple(w.get("Sg")), su=triple(w.get("Su")),
+                          sd=triple(w.get("Sd")), q4=True, F=F)
+
+
+# (d, F, E, k, n_shared)
+CASES = [
+    (2048, 512, 256, 8, 1),     # the full-size decode layer
+    (2048, 512, 256, 8, 0),     # no shared expert
+    (256, 128, 8, 2, 1),        # few experts, short rows
+    (1024, 256, 64, 8, 1),
+    (8192, 256, 16, 4, 1),      # four 64-column groups per lane
+    (16384, 128, 8, 2, 1),      # the longest rows: eight groups per lane
+    (2048, 4096, 8, 1, 1),      # the widest down rows: 128 (slot, group) pairs
+]
+
+
+@pytest.mark.parametrize("d,F,E,k,n_shared", CASES)
+def test_q4_decode_matches_oracle(dev, d, F, E, k, n_shared):
+    w = synth.q4_layer_weights(150 + d + E, d, F, E, n_shared, dev)
+    n_tok = 4
+    x = H.margined_tokens(160 + d, n_tok, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k)
+    try:
+        moe.moe_profile(layer.handle, True)
+        layer.forward(x[0:1].clone())
+        moe.moe_profile(layer.handle, False)
+        prof = moe.moe_profile_read(layer.handle)
+        kinds = {name for name, (_, n) in prof.items() if n > 0}
+        assert kinds == {"decode_router", "decode_gate_up", "decode_down"}, kinds
+        outs = [layer.forward(x[i:i + 1].clone()) for i in range(n_tok)]
+        torch.cuda.synchronize()
+        rc, detail = layer.status()
+        assert rc == 0, f"device status {rc} detail {detail}"
+    finally:
+        layer.close()
+    out = torch.cat(outs)
+    ref, *_ = _oracle_q4(x, w, k, F)
+    err = H.row_rel_err(out, ref)
+    assert err.max() <= H.OUT_TOL, err
+
+
+def test_q4_handle_routes_and_refuses_batches(dev):
+    d, F, E, k = 2048, 512, 256, 8
+    w = synth.q4_layer_weights(7, d, F, E, 1, dev)
+    x = H.margined_tokens(8, 2, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k)
+    try:
+        idx, wt, counts = layer.route(x[0:1].clone())
+        torch.cuda.synchronize()
+        ri, rw, _, rc = oracle.route(H.np_view(x[0:1]), H.np_view(w["Wr"]), k)
+        H.check_routing(idx, wt, counts, ri, rw, rc)
+        out = torch.empty((2, d), dtype=torch.bfloat16, device=dev)
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward(layer.handle, x, 2, out)
+        assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+
+
+def test_q4_layer_stack_in_a_cuda_graph(dev):
+    """Four chained 4-bit layers captured once; replays equal eager runs bit for
+    bit."""
+    d, F, E, k, L = 2048, 512, 256, 8, 4
+    ws = [synth.q4_layer_weights(170 + l, d, F, E, 1, dev) for l in range(L)]
+    layers = [moe.Q4Layer(w, k) for w in ws]
+    try:
+        xin = torch.empty((1, d), dtype=torch.bfloat16, device=dev)
+        outs = [torch.empty((1, d), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                layers[l].forward(xin if l == 0 else outs[l - 1], out=outs[l], stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                layers[l].forward(xin if l == 0 else outs[l - 1], out=outs[l], stream=stream)
+        toks = synth.tokens(180, 3, d, "bf16", dev)
+        for step in range(3):
+            xin.copy_(toks[step:step + 1])
+            g.replay()
+            torch.cuda.synchronize()
+            got = [o.clone() for o in outs]
+            h = toks[step:step + 1].clone()
+            for l in range(L):
+                h = layers[l].forward(h)
+                torch.cuda.synchronize()
+                assert torch.equal(got[l], h), f"step {step} layer {l}"
+        for layer in layers:
+            assert layer.status()[0] == 0
+    finally:
+        for layer in layers:
+            layer.close()

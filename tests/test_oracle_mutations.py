@@ -28,3 +28,21 @@ def test_mutation_is_caught(m):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"mutation {m} ({MUTATIONS[m]}) passed every pin"
+
+
+QUANT_MUTATIONS = {
+    1: "odd column packed in the low nibble",
+    2: "codes rounded down",
+    3: "range divided into 16 steps",
+}
+
+
+@pytest.mark.parametrize("m", sorted(QUANT_MUTATIONS), ids=lambda m: f"q{m}")
+def test_quantiser_mutation_is_caught(m):
+    failed = []
+    for pin in pins.QUANT_PINS:
+        try:
+            pin(m)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"quantiser mutation {m} ({QUANT_MUTATIONS[m]}) passed every pin"
