@@ -32,114 +32,221 @@ namespace moe {
 
 namespace {
 
-constexpr int kPad = kQ4Group + 1;  // floats per padded group row in shared memory
-constexpr int kMaxGroupsPerLane = 8;  // rows of up to 16384 columns
-
 __device__ __forceinline__ float bf16f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Codes, scale and bias of the groups g = lane + 32 m of one row.
-struct Q4Row {
-  uint4 c[kMaxGroupsPerLane][2];
-  uint16_t s[kMaxGroupsPerLane], b[kMaxGroupsPerLane];
+// Sum over the 8 codes of one 32-bit word (columns c .. c + 7: byte j holds
+// column c + 2j in its low nibble, c + 2j + 1 in its high nibble) of
+// (128 + q) * x.  Each code becomes the float 128 + q with one byte permute:
+// the nibble, isolated in a byte, lands in bits 16..19 under the exponent byte
+// 0x43 (128.0f), which is exact.  The caller removes 128 * sum(x) once per
+// group, so no code is converted with an integer-to-float instruction.
+__device__ __forceinline__ float q4_word_dot(uint32_t w, const float *x, float acc) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t sel = 0x4055u | (static_cast<uint32_t>(j) << 8);
+    acc = fmaf(__uint_as_float(__byte_perm(lo, 0x43u, sel)), x[2 * j], acc);
+    acc = fmaf(__uint_as_float(__byte_perm(hi, 0x43u, sel)), x[2 * j + 1], acc);
+  }
+  return acc;
+}
+
+// s * sum q x + b * sum x for one group's share, given p = sum (128 + q) x and
+// sx = sum x over the same columns.
+__device__ __forceinline__ float q4_finish(float p, float sx, uint16_t s, uint16_t b) {
+  const float sf = bf16f(s);
+  return sf * p + fmaf(-128.0f, sf, bf16f(b)) * sx;
+}
+
+// Warp reduce-scatter of N partial sums (N a power of two, <= 32): returns
+// the warp total of value lane >> (5 - log2 N).  N - 1 + (5 - log2 N)
+// shuffles instead of 5 N.
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+  for (int h = N / 2, o = 16; h >= 1; h >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = up ? v[j] : v[j + h];
+      const float keep = up ? v[j + h] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = 16 / N; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+
+// ---------------------------------------------------------------- gate/up rows
+// Kernel B's items are (slot s, row f), item = s * F + f, over the k routed
+// slots and the shared expert (slot k): h[item] = silu(gate . x) * (up . x).
+// A CTA takes a block of n consecutive items (one slot; F is a multiple of
+// n), whose code bytes, scales and biases are contiguous in both matrices.  A
+// row of d columns is 2G chunks of 32 codes (16 bytes), G = d / 64; a team of
+// ceil(G / 32) warps shares a row and its lane slot q < G owns chunks q and
+// q + G (consecutive lanes read consecutive 16 bytes: no bank conflicts),
+// with the token's 2 x 32 values of those chunks in registers.  Team j takes
+// items kQB j .. kQB j + kQB - 1 of the block, and its rows are one stage of
+// the copy: every thread issues its cp.async share of stage j and arrives on
+// stage j's barrier, so team j starts computing when its own rows landed,
+// while later stages are still in flight.
+constexpr int kQB = 4;
+
+struct XChunks {
+  float a[32], b[32];
+  float sa, sb;
 };
 
-__device__ __forceinline__ void q4_row_load(Q4Row &r, const Q4Mat &m, long long row, int cols,
-                                            int lane) {
-  const int G = cols / kQ4Group;
-  const uint4 *cb = reinterpret_cast<const uint4 *>(m.c + row * (cols / 2));
-  const uint16_t *sb = m.s + row * G, *bb = m.b + row * G;
+// 32 token values (one chunk) from the CTA's shared-memory copy of the token.
+__device__ __forceinline__ void load_x32(float (&x)[32], float &sx, const uint4 *tok, int chunk) {
+  const uint4 *p = tok + chunk * 4;
+  float s = 0.0f;
 #pragma unroll
-  for (int q = 0; q < kMaxGroupsPerLane; ++q) {
-    const int g = lane + 32 * q;
-    if (g < G) {
-      r.c[q][0] = ld_stream16(cb + 2 * g);
-      r.c[q][1] = ld_stream16(cb + 2 * g + 1);
-      r.s[q] = __ldg(sb + g);
-      r.b[q] = __ldg(bb + g);
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = p[j];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[8 * j + 2 * t] = __uint_as_float(u[t] << 16);
+      x[8 * j + 2 * t + 1] = __uint_as_float(u[t] & 0xFFFF0000u);
+      s += x[8 * j + 2 * t] + x[8 * j + 2 * t + 1];
     }
   }
+  sx = s;
 }
 
-// sum over the 64 codes of a group of q_e * v_e (v: 64 floats in shared memory)
-__device__ __forceinline__ float q4_group_dot(const uint4 &c0, const uint4 &c1, const float *v) {
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float acc = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      acc = fmaf(static_cast<float>((w[j] >> (4 * e)) & 15u), v[8 * j + e], acc);
-  return acc;
+__device__ __forceinline__ void load_x_chunks(XChunks &xc, const uint4 *tok, int q, int G) {
+  load_x32(xc.a, xc.sa, tok, q);
+  load_x32(xc.b, xc.sb, tok, q + G);
 }
 
-// dot(row, v) for a row loaded into r; vp: padded groups of v, vs: group sums.
-__device__ __forceinline__ float q4_row_dot(const Q4Row &r, int cols, const float *vp,
-                                            const float *vs, int lane) {
-  const int G = cols / kQ4Group;
-  float acc = 0.0f;
-#pragma unroll
-  for (int q = 0; q < kMaxGroupsPerLane; ++q) {
-    const int g = lane + 32 * q;
-    if (g < G) {
-      const float dq = q4_group_dot(r.c[q][0], r.c[q][1], vp + g * kPad);
-      acc += bf16f(r.s[q]) * dq + bf16f(r.b[q]) * vs[g];
+__device__ __forceinline__ float chunk_dot(const uint4 &c, const float (&x)[32]) {
+  float p0 = q4_word_dot(c.x, x, 0.0f);
+  float p1 = q4_word_dot(c.y, x + 8, 0.0f);
+  p0 = q4_word_dot(c.z, x + 16, p0);
+  p1 = q4_word_dot(c.w, x + 24, p1);
+  return p0 + p1;
+}
+
+// Block of rows of one 4-bit matrix staged in shared memory.
+struct QBlock {
+  const uint4 *c;     // [rows][d / 32] chunks
+  const uint16_t *s;  // [rows][G]
+  const uint16_t *b;
+};
+
+__device__ __forceinline__ float qblock_row_dot(const QBlock &m, int r, int G, int q,
+                                                const XChunks &xc) {
+  const uint4 ca = m.c[r * 2 * G + q], cb = m.c[r * 2 * G + q + G];
+  const int ga = q >> 1, gb = (q + G) >> 1;
+  return q4_finish(chunk_dot(ca, xc.a), xc.sa, m.s[r * G + ga], m.b[r * G + ga]) +
+         q4_finish(chunk_dot(cb, xc.b), xc.sb, m.s[r * G + gb], m.b[r * G + gb]);
+}
+
+// Team geometry of a 256-thread CTA for rows of d columns.
+struct Team {
+  int wt, teams, team, tw, q;
+  bool active;
+  __device__ Team(int d, int warp, int lane) {
+    const int G = d / kQ4Group;
+    wt = (G + 31) / 32;
+    teams = 8 / wt;
+    team = warp / wt;
+    tw = warp - team * wt;
+    q = tw * 32 + lane;
+    active = team < teams && q < G;
+  }
+};
+
+// Shared-memory plan of one block of n rows of a gate and an up matrix:
+// codes, then scales and biases, then the token.
+struct GateUpSmem {
+  QBlock g, u;
+  const uint4 *x;
+  __device__ GateUpSmem(uint8_t *base, int n, int d) {
+    const int G = d / kQ4Group;
+    const int cb = n * d / 2, sb = n * G * 2;
+    g.c = reinterpret_cast<const uint4 *>(base);
+    u.c = reinterpret_cast<const uint4 *>(base + cb);
+    g.s = reinterpret_cast<const uint16_t *>(base + 2 * cb);
+    g.b = reinterpret_cast<const uint16_t *>(base + 2 * cb + sb);
+    u.s = reinterpret_cast<const uint16_t *>(base + 2 * cb + 2 * sb);
+    u.b = reinterpret_cast<const uint16_t *>(base + 2 * cb + 3 * sb);
+    x = reinterpret_cast<const uint4 *>(base + 2 * cb + 4 * sb);
+  }
+};
+
+__host__ __device__ constexpr size_t gateup_smem_bytes(int n, int d) {
+  return static_cast<size_t>(n) * d + static_cast<size_t>(n) * (d / kQ4Group) * 8 +
+         static_cast<size_t>(d) * 2;
+}
+
+// All threads: cp.async of bytes (a multiple of 16) from src to dst.
+__device__ __forceinline__ void cp_async_range(uint8_t *dst, const void *src, int bytes) {
+  const uint8_t *s8 = static_cast<const uint8_t *>(src);
+  const uint32_t d0 = smem_u32(dst);
+  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) cp_async16(d0 + 16 * i, s8 + 16 * i);
+}
+
+// 1D bulk copy (TMA) global -> shared completing on an mbarrier; 16-byte
+// aligned addresses, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Stages of a block (rows row0 .. row0 + n - 1 of mg and mu): stage j holds
+// rows j n / ns .. (j + 1) n / ns - 1.  The code bytes of a stage (16 KB per
+// matrix at d >= 2048) go by one bulk copy per matrix, issued by thread 0
+// with the stage's byte count; the scales and biases by cp.async from every
+// thread, each thread arriving on the stage barrier once its copies landed
+// (barrier count: blockDim.x + 1).  One bulk copy per 16 KB keeps the per-copy
+// cost of the copy engine small against its transfer time, where thread
+// copies of the whole block would stream far below the memory's rate.
+__device__ __forceinline__ void gateup_issue(uint8_t *base, const Q4Mat &mg, const Q4Mat &mu,
+                                             long long row0, int n, int d, int ns,
+                                             uint64_t *bar) {
+  const int G = d / kQ4Group;
+  const int cb = n * d / 2, sb = n * G * 2;
+  const int rows = n / ns;
+  const int scb = rows * d / 2, ssb = rows * G * 2;  // per stage
+  for (int j = 0; j < ns; ++j) {
+    const long long r = row0 + static_cast<long long>(j) * rows;
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(smem_u32(&bar[j]), 2 * scb);
+      bulk_g2s(base + j * scb, mg.c + r * (d / 2), scb, &bar[j]);
+      bulk_g2s(base + cb + j * scb, mu.c + r * (d / 2), scb, &bar[j]);
     }
+    cp_async_range(base + 2 * cb + j * ssb, mg.s + r * G, ssb);
+    cp_async_range(base + 2 * cb + sb + j * ssb, mg.b + r * G, ssb);
+    cp_async_range(base + 2 * cb + 2 * sb + j * ssb, mu.s + r * G, ssb);
+    cp_async_range(base + 2 * cb + 3 * sb + j * ssb, mu.b + r * G, ssb);
+    cp_async_arrive(smem_u32(&bar[j]));
   }
-  return acc;
-}
-
-// The bf16 token into padded float groups vp[G][65] and group sums vs[G]
-// (all threads of the CTA; L2 reads).
-__device__ __forceinline__ void load_token_groups(float *vp, float *vs, const void *x, int d) {
-  const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
-  const uint32_t *xw = reinterpret_cast<const uint32_t *>(xb);
-  for (int i = threadIdx.x; i < d / 2; i += blockDim.x) {
-    const uint32_t v = __ldcg(xw + i);
-    const int c = 2 * i, g = c / kQ4Group, e = c - g * kQ4Group;
-    vp[g * kPad + e] = __uint_as_float(v << 16);
-    vp[g * kPad + e + 1] = __uint_as_float(v & 0xFFFF0000u);
-  }
-  __syncthreads();
-  for (int g = threadIdx.x; g < d / kQ4Group; g += blockDim.x) {
-    float s = 0.0f;
-    for (int e = 0; e < kQ4Group; ++e) s += vp[g * kPad + e];
-    vs[g] = s;
-  }
-  __syncthreads();
 }
 
 }  // namespace
 
-// ---------------------------------------------------------------- A: router + shared gate/up
-// CTAs [0, ceil(E / 8)): one warp per expert logit (bf16 router rows, as in
-// decode.cu).  CTAs after them: one warp per shared-expert row f, its 4-bit
-// gate and up rows loaded before the dependency wait.
+// ---------------------------------------------------------------- A: router + top-k
+// One warp per expert logit (bf16 router rows requested before the
+// dependency wait, the token copied once per CTA).  The last CTA to finish
+// picks the top-k once for the layer (dsel, dselw) and clears the count.
 __global__ void __launch_bounds__(256) decode_router_q4_kernel(const DecodeArgs a) {
-  extern __shared__ uint4 sm4[];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  __shared__ int s_last;
+  __shared__ int s_sel[kMaxTopK];
+  __shared__ float s_selw[kMaxTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d;
   const int nvec = d * 2 / 16;
-  const int n_rt = (a.E + 7) / 8;
-  if (static_cast<int>(blockIdx.x) >= n_rt) {
-    float *vp = reinterpret_cast<float *>(sm4);
-    float *vs = vp + (d / kQ4Group) * kPad;
-    const int f = (blockIdx.x - n_rt) * 8 + warp;
-    Q4Row rg, ru;
-    if (f < a.F) {
-      q4_row_load(rg, a.q.sg, f, d, lane);
-      q4_row_load(ru, a.q.su, f, d, lane);
-    }
-    pdl_launch_dependents();
-    pdl_wait();
-    load_token_groups(vp, vs, a.x, d);
-    if (f >= a.F) return;
-    const float g = warp_sum(q4_row_dot(rg, d, vp, vs, lane));
-    const float u = warp_sum(q4_row_dot(ru, d, vp, vs, lane));
-    if (lane == 0) a.h[static_cast<long long>(a.k) * a.F + f] = g / (1.0f + __expf(-g)) * u;
-    return;
-  }
   const int e = blockIdx.x * 8 + warp;
   const uint4 *row = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.wr) +
                                                      static_cast<long long>(e) * d);
@@ -147,112 +254,233 @@ __global__ void __launch_bounds__(256) decode_router_q4_kernel(const DecodeArgs 
   if (e < a.E) row_prefetch(pr, row, nvec, lane);
   pdl_launch_dependents();
   pdl_wait();
-  load_token(sm4, a.x, nvec);
+  uint4 *xs = reinterpret_cast<uint4 *>(qsm);
+  load_token(xs, a.x, nvec);
   if (e < a.E) {
-    const float acc = warp_sum(row_dot_pre<__nv_bfloat16>(pr, row, sm4, nvec, lane));
+    const float acc = warp_sum(row_dot_pre<__nv_bfloat16>(pr, row, xs, nvec, lane));
     if (lane == 0) a.logits[e] = acc + (a.bias ? a.bias[e] : 0.0f);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.dcnt, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();
+  warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
+  __syncwarp();
+  if (lane < a.k) {
+    a.dsel[lane] = s_sel[lane];
+    a.dselw[lane] = s_selw[lane];
+  }
+  if (lane == 0) *a.dcnt = 0u;
 }
 
-// ---------------------------------------------------------------- B: routed gate/up
-// Tile t: 32 rows of slot s = t / (F / 32); warp w takes rows 4w .. 4w + 3,
-// each a (gate row, up row) pair loaded whole into registers (one group per
-// lane at d = 2048) before any is used.
-constexpr int kQRB = 32;
-
+// ---------------------------------------------------------------- B: gate/up
+// Blocks of the shared expert's items (static rows) are copied before the
+// dependency wait; routed blocks read their expert from dsel after it.
 __global__ void __launch_bounds__(256) decode_gateup_q4_kernel(const DecodeArgs a) {
-  extern __shared__ float smf[];
-  __shared__ int s_sel[kMaxTopK];
-  __shared__ float s_selw[kMaxTopK];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ float red[8][2 * kQB];
+  __shared__ int s_row0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.d, F = a.F;
-  float *vp = smf;
-  float *vs = vp + (d / kQ4Group) * kPad;
-  const int nrb = F / kQRB;
-  const int ntile = a.k * nrb;
+  const int d = a.d, F = a.F, G = d / kQ4Group;
+  const Team tm(d, warp, lane);
+  const int n = tm.teams * kQB;
+  const int ns = tm.teams >= 2 ? 2 : 1;  // copy stages
+  const int it0 = blockIdx.x * n;
+  const int s = it0 / F, f0 = it0 - s * F;
+  const bool shared_blk = s >= a.k;
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&bar[j]), blockDim.x + 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (shared_blk) gateup_issue(qsm, a.q.sg, a.q.su, f0, n, d, ns, bar);
   pdl_wait();
-  if (warp == 0) warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
-  load_token_groups(vp, vs, a.x, d);  // includes the barriers that publish s_sel
+  // kernel A is complete: kernel C may start and stage its down rows (it reads
+  // only the top-k) while this kernel streams
   pdl_launch_dependents();
-  for (int t = blockIdx.x; t < ntile; t += gridDim.x) {
-    const int s = t / nrb, rb = t - (t / nrb) * nrb;
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int f = rb * kQRB + 4 * warp + q;
-      const long long row = static_cast<long long>(s_sel[s]) * F + f;
-      Q4Row rg, ru;
-      q4_row_load(rg, a.q.g, row, d, lane);
-      q4_row_load(ru, a.q.u, row, d, lane);
-      const float g = warp_sum(q4_row_dot(rg, d, vp, vs, lane));
-      const float u = warp_sum(q4_row_dot(ru, d, vp, vs, lane));
-      if (lane == 0) a.h[static_cast<long long>(s) * F + f] = g / (1.0f + __expf(-g)) * u;
+  // the token (the previous layer's output) and this block's expert, in one
+  // round of L2 reads
+  const GateUpSmem sm(qsm, n, d);
+  uint4 *xs = const_cast<uint4 *>(sm.x);
+  if (!shared_blk && threadIdx.x == 0) s_row0 = __ldcg(a.dsel + s) * F + f0;
+  const uint4 *xg = static_cast<const uint4 *>(a.x);
+  for (int i = threadIdx.x; i < d * 2 / 16; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  __syncthreads();
+  if (!shared_blk) gateup_issue(qsm, a.q.g, a.q.u, s_row0, n, d, ns, bar);
+  XChunks xc;
+  if (tm.active) load_x_chunks(xc, sm.x, tm.q, G);
+  // team j takes kQB / ns items of every stage, so all warps compute on each
+  // stage as it lands: item m of the team is st n / ns + j kQB / ns + jj with
+  // (st, jj) = (m / 2, m % 2) for two stages, (0, m) for one.  The loop has no
+  // branch around a row, so the rows' dependent FMA chains interleave;
+  // threads outside a team read row 0 with a zero token.
+  const int per = kQB / ns;
+  const int team_c = tm.team < tm.teams ? tm.team : 0;
+  const int q_c = tm.active ? tm.q : 0;
+  if (!tm.active) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) xc.a[c] = xc.b[c] = 0.0f;
+    xc.sa = xc.sb = 0.0f;
+  }
+  float v[2 * kQB];
+  bool ok = mbar_wait(smem_u32(&bar[0]), 0, MOE_WAIT_LIMIT_CYCLES, nullptr);
+#pragma unroll
+  for (int m = 0; m < kQB; ++m) {
+    if (m == kQB / 2 && ns == 2) ok = mbar_wait(smem_u32(&bar[1]), 0, MOE_WAIT_LIMIT_CYCLES, nullptr) && ok;
+    const int st = ns == 2 ? m / 2 : 0, jj = ns == 2 ? m % 2 : m;
+    const int r = st * (n / ns) + team_c * per + jj;
+    v[2 * m] = qblock_row_dot(sm.g, r, G, q_c, xc);
+    v[2 * m + 1] = qblock_row_dot(sm.u, r, G, q_c, xc);
+  }
+  if (!ok) {
+#pragma unroll
+    for (int m = 0; m < 2 * kQB; ++m) v[m] = 0.0f;
+    if (lane == 0) report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_DECODE * 100 + SITE_STAGE);
+  }
+  const float t = warp_reduce_scatter<2 * kQB>(v, lane);
+  if ((lane & 3) == 0) red[warp][lane >> 2] = t;
+  __syncthreads();
+  const int i = threadIdx.x;
+  if (i < n) {
+    const int st = i / (n / ns), rem = i - st * (n / ns);
+    const int team = rem / per, jj = rem - team * per;
+    const int m = st * (kQB / 2) + jj;  // ns == 1: st = 0, m = jj
+    float g = 0.0f, u = 0.0f;
+    for (int w = 0; w < tm.wt; ++w) {
+      g += red[team * tm.wt + w][2 * m];
+      u += red[team * tm.wt + w][2 * m + 1];
     }
+    a.h[it0 + i] = g / (1.0f + __expf(-g)) * u;
   }
 }
 
 // ---------------------------------------------------------------- C: down + combine
-// One warp per output element i.  The (slot, group) pairs of the row, k + 1
-// slots of F / 64 groups, are spread over the lanes; their codes are loaded
-// before the wait for h.
-constexpr int kMaxPairsPerLane = 5;  // (8 + 1) slots x 16 groups (F = 1024) / 32
+// A CTA computes output rows i0 .. i0 + R - 1.  Their down-matrix rows of
+// every slot (codes, scales, biases) are copied to shared memory with cp.async
+// as soon as the top-k is known, before the wait for h.  Thread t owns CPL
+// consecutive columns of one slot's h (slot t / (F / CPL)), those h values in
+// registers; its partial for row r is weighted by the slot's routing weight,
+// reduce-scattered over the warp and summed over the warps in shared memory.
+constexpr int kQR = 16;  // output rows per CTA, at most
 
-__global__ void __launch_bounds__(256) decode_down_q4_kernel(const DecodeArgs a) {
-  extern __shared__ float smf[];
+// All threads: cp.async of `bytes` from src to dst in pieces of `piece`
+// bytes (4, 8 or 16; both addresses and bytes multiples of it).
+__device__ __forceinline__ void cp_async_pieces(void *dst, const void *src, int bytes, int piece) {
+  const uint8_t *s8 = static_cast<const uint8_t *>(src);
+  const uint32_t d0 = smem_u32(dst);
+  for (int o = threadIdx.x * piece; o < bytes; o += blockDim.x * piece) {
+    if (piece == 16)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d0 + o), "l"(s8 + o)
+                   : "memory");
+    else if (piece == 8)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d0 + o), "l"(s8 + o)
+                   : "memory");
+    else
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d0 + o), "l"(s8 + o)
+                   : "memory");
+  }
+}
+
+__host__ __device__ constexpr size_t down_smem_bytes(int R, int nslot, int F) {
+  return static_cast<size_t>(R) * nslot * (F / 2 + 2 * (F / 32));
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(320) decode_down_q4_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t qsm[];
   __shared__ int s_sel[kMaxTopK];
   __shared__ float s_selw[kMaxTopK];
+  __shared__ float acc_s[10][kQR];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, F = a.F, GF = F / kQ4Group;
+  const int sps = F / CPL;  // slices per slot
   const int nslot = a.k + a.n_shared;
-  const int npair = nslot * GF;
-  const int i = blockIdx.x * 8 + warp;
+  const int slot = threadIdx.x / sps, sl = threadIdx.x - slot * sps;
+  const bool active = slot < nslot;
+  const int R = a.c_rows;
+  const int i0 = blockIdx.x * R;
+  const int nr = (d - i0) < R ? (d - i0) : R;  // rows of this CTA
+  // shared memory: codes [nslot][R][F / 2], scales and biases [nslot][R][GF]
+  // (a slot's rows i0 .. i0 + nr - 1 are consecutive rows of its matrix)
+  uint8_t *cs = qsm;
+  uint16_t *ss = reinterpret_cast<uint16_t *>(qsm + static_cast<size_t>(R) * nslot * (F / 2));
+  uint16_t *bs = ss + R * nslot * GF;
   pdl_launch_dependents();
-  if (warp == 0) warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
+  // the layer's top-k (kernel A finished before kernel B let this kernel start)
+  if (static_cast<int>(threadIdx.x) < a.k) {
+    s_sel[threadIdx.x] = __ldcg(a.dsel + threadIdx.x);
+    s_selw[threadIdx.x] = __ldcg(a.dselw + threadIdx.x);
+  }
   __syncthreads();
-  uint4 c[kMaxPairsPerLane][2];
-  uint16_t sc[kMaxPairsPerLane], bi[kMaxPairsPerLane];
-#pragma unroll
-  for (int m = 0; m < kMaxPairsPerLane; ++m) {
-    const int p = lane + 32 * m;
-    if (p < npair && i < d) {
-      const int s = p / GF, g = p - s * GF;
-      const Q4Mat &mat = s < a.k ? a.q.d : a.q.sd;
-      const long long row = s < a.k ? static_cast<long long>(s_sel[s]) * d + i : i;
-      const uint4 *cb = reinterpret_cast<const uint4 *>(mat.c + row * (F / 2));
-      c[m][0] = ld_stream16(cb + 2 * g);
-      c[m][1] = ld_stream16(cb + 2 * g + 1);
-      sc[m] = __ldg(mat.s + row * GF + g);
-      bi[m] = __ldg(mat.b + row * GF + g);
+  {
+    const int sbp = F / 32 < 16 ? F / 32 : 16;  // scale/bias piece: 4, 8 or 16 bytes
+    for (int sl_ = 0; sl_ < nslot; ++sl_) {
+      const Q4Mat &mat = sl_ < a.k ? a.q.d : a.q.sd;
+      const long long row = (sl_ < a.k ? static_cast<long long>(s_sel[sl_]) * d : 0) + i0;
+      cp_async_pieces(cs + static_cast<size_t>(sl_) * R * (F / 2), mat.c + row * (F / 2),
+                      nr * (F / 2), 16);
+      cp_async_pieces(ss + sl_ * R * GF, mat.s + row * GF, nr * GF * 2, sbp);
+      cp_async_pieces(bs + sl_ * R * GF, mat.b + row * GF, nr * GF * 2, sbp);
     }
+    cp_async_commit();
   }
   pdl_wait();
-  // h of every slot into padded groups, then the group sums
-  float *hp = smf;
-  float *hs = hp + npair * kPad;
-  for (int q = threadIdx.x; q < nslot * F; q += blockDim.x) {
-    const int p = q / kQ4Group, e = q - p * kQ4Group;
-    hp[p * kPad + e] = __ldcg(a.h + q);
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < npair; p += blockDim.x) {
-    float s = 0.0f;
-    for (int e = 0; e < kQ4Group; ++e) s += hp[p * kPad + e];
-    hs[p] = s;
-  }
-  __syncthreads();
-  if (i >= d) return;
-  float acc = 0.0f;
+  float hv[CPL];
 #pragma unroll
-  for (int m = 0; m < kMaxPairsPerLane; ++m) {
-    const int p = lane + 32 * m;
-    if (p < npair) {
-      const int s = p / GF;
-      const float dq = q4_group_dot(c[m][0], c[m][1], hp + p * kPad);
-      const float part = bf16f(sc[m]) * dq + bf16f(bi[m]) * hs[p];
-      acc = fmaf(s < a.k ? s_selw[s] : 1.0f, part, acc);
+  for (int j = 0; j < CPL; ++j) hv[j] = 0.0f;
+  float sh = 0.0f, wslot = 0.0f;
+  if (active) {
+    const float4 *hp = reinterpret_cast<const float4 *>(a.h + slot * F + sl * CPL);
+#pragma unroll
+    for (int j = 0; j < CPL / 4; ++j) {
+      const float4 v = __ldcg(hp + j);
+      hv[4 * j] = v.x;
+      hv[4 * j + 1] = v.y;
+      hv[4 * j + 2] = v.z;
+      hv[4 * j + 3] = v.w;
+      sh += (v.x + v.y) + (v.z + v.w);
     }
+    wslot = slot < a.k ? s_selw[slot] : 1.0f;
   }
-  acc = warp_sum(acc);
-  if (lane == 0) reinterpret_cast<__nv_bfloat16 *>(a.out)[i] = __float2bfloat16_rn(acc);
+  cp_async_wait_all();
+  __syncthreads();
+  const int g = (active ? sl : 0) * CPL / kQ4Group;
+  // Branch-free over the rows, so that their dependent FMA chains interleave:
+  // rows past nr read row 0 and are zeroed; threads past the last slot read
+  // slot 0 with h = 0 and weight 0.
+  const int slot_c = active ? slot : 0, sl_c = active ? sl : 0;
+  const float wuse = active ? wslot : 0.0f;
+  float part[kQR];
+#pragma unroll
+  for (int r = 0; r < kQR; ++r) {
+    const int rsi = slot_c * R + (r < nr ? r : 0);
+    const uint32_t *cw = reinterpret_cast<const uint32_t *>(
+        cs + static_cast<size_t>(rsi) * (F / 2) + sl_c * (CPL / 2));
+    float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) {
+      if (j & 1)
+        p1 = q4_word_dot(cw[j], hv + 8 * j, p1);
+      else
+        p0 = q4_word_dot(cw[j], hv + 8 * j, p0);
+    }
+    const float v = q4_finish(p0 + p1, sh, ss[rsi * GF + g], bs[rsi * GF + g]);
+    part[r] = r < nr ? wuse * v : 0.0f;
+  }
+  const float t = warp_reduce_scatter<kQR>(part, lane);
+  if ((lane & 1) == 0) acc_s[warp][lane >> 1] = t;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  if (static_cast<int>(threadIdx.x) < nr) {
+    float o = 0.0f;
+    for (int w = 0; w < nw; ++w) o += acc_s[w][threadIdx.x];
+    reinterpret_cast<__nv_bfloat16 *>(a.out)[i0 + threadIdx.x] = __float2bfloat16_rn(o);
+  }
 }
 
 // ---------------------------------------------------------------- quantiser
@@ -300,14 +528,12 @@ __global__ void quantize_q4_kernel(const T *__restrict__ w, long long ngroups, i
 
 // ---------------------------------------------------------------- launchers
 namespace {
-size_t tok_smem(int d) { return sizeof(float) * ((d / kQ4Group) * kPad + d / kQ4Group); }
-
 template <typename K>
-cudaError_t launch_q(K kern, int grid, size_t smem, cudaStream_t st, bool pdl,
+cudaError_t launch_q(K kern, int grid, int threads, size_t smem, cudaStream_t st, bool pdl,
                      const DecodeArgs &a) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -317,41 +543,78 @@ cudaError_t launch_q(K kern, int grid, size_t smem, cudaStream_t st, bool pdl,
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
-}  // namespace
 
-cudaError_t launch_decode_router_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  const int grid = (a.E + 7) / 8 + (a.n_shared ? (a.F + 7) / 8 : 0);
-  size_t smem = tok_smem(a.d);
-  if (smem < static_cast<size_t>(a.d) * 2) smem = static_cast<size_t>(a.d) * 2;
-  return launch_q(decode_router_q4_kernel, grid, smem, st, pdl, a);
-}
-cudaError_t launch_decode_gateup_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
+int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return cudaErrorUnknown;
-  const int ntile = a.k * (a.F / kQRB);
-  return launch_q(decode_gateup_q4_kernel, ntile < sms ? ntile : sms, tok_smem(a.d), st, pdl, a);
-}
-cudaError_t launch_decode_down_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  const int npair = (a.k + a.n_shared) * (a.F / kQ4Group);
-  const size_t smem = sizeof(float) * (static_cast<size_t>(npair) * kPad + npair);
-  return launch_q(decode_down_q4_kernel, (a.d + 7) / 8, smem, st, pdl, a);
+    return 0;
+  return sms;
 }
 
-// The shared-memory limits of the three kernels for the largest supported
-// shapes (d = 16384, F * (k + 1) = 4096 * 9 would not fit; the create call
-// rejects layers whose h does not fit, see moe_create_q4).
+int items_per_cta(int d) {
+  const int wt = (d / kQ4Group + 31) / 32;
+  return (8 / wt) * kQB;
+}
+size_t gateup_smem(int d) { return gateup_smem_bytes(items_per_cta(d), d); }
+
+// columns of h per thread in kernel C: the fewest that keep the CTA within
+// 320 threads
+int down_cpl(const DecodeArgs &a) {
+  const int slots = a.k + a.n_shared;
+  for (int cpl : {8, 16, 32})
+    if (slots * (a.F / cpl) <= 320) return cpl;
+  return 0;
+}
+}  // namespace
+
+cudaError_t launch_decode_router_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
+  return launch_q(decode_router_q4_kernel, (a.E + 7) / 8, 256, static_cast<size_t>(a.d) * 2, st,
+                  pdl, a);
+}
+// one CTA per block of items; F is a multiple of the block
+cudaError_t launch_decode_gateup_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
+  const int per = items_per_cta(a.d);
+  const int grid = (a.k + a.n_shared) * a.F / per;
+  return launch_q(decode_gateup_q4_kernel, grid, 256, gateup_smem(a.d), st, pdl, a);
+}
+cudaError_t launch_decode_down_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
+  const int sms = sm_count();
+  const int cpl = down_cpl(a);
+  if (sms == 0 || cpl == 0) return cudaErrorInvalidValue;
+  DecodeArgs b = a;
+  int R = (a.d + sms - 1) / sms;
+  R = R < 1 ? 1 : (R > kQR ? kQR : R);
+  b.c_rows = R;
+  const int nslot = a.k + a.n_shared;
+  const int threads = (nslot * (a.F / cpl) + 31) / 32 * 32;
+  const int grid = (a.d + R - 1) / R;
+  const size_t smem = down_smem_bytes(R, nslot, a.F);
+  if (cpl == 8) return launch_q(decode_down_q4_kernel<8>, grid, threads, smem, st, pdl, b);
+  if (cpl == 16) return launch_q(decode_down_q4_kernel<16>, grid, threads, smem, st, pdl, b);
+  return launch_q(decode_down_q4_kernel<32>, grid, threads, smem, st, pdl, b);
+}
+
+// Kernel B stages a block of gate/up rows and the token: at most 72 KB
+// (n d = 64 K for every supported d, plus the scales and biases) + 32 KB.
+// Kernel C stages at most 16 rows x (k + 1) F / 2 (+ 1/8) bytes: 90 KB.
 cudaError_t decode_q4_set_smem_attr() {
+  const int bytes = 104 * 1024;
   cudaError_t e = cudaFuncSetAttribute(decode_router_q4_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(tok_smem(16384)));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_gateup_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(tok_smem(16384)));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_down_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              200 * 1024);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_gateup_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_down_q4_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_down_q4_kernel<16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_down_q4_kernel<32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
 }
 
 template <typename T>

@@ -126,6 +126,10 @@ struct DecodeArgs {
   int ring;            // kernel B: ring slots per CTA
   int c_rows;          // kernel C: output rows per CTA (upper bound)
   Q4Weights q;         // 4-bit expert weights (decode_q4.cu), unused by the bf16 kernels
+  // decode_q4.cu: the top-k picked once per layer by kernel A's last CTA
+  int *dsel;           // [k] chosen experts
+  float *dselw;        // [k] their routing weights
+  unsigned *dcnt;      // kernel A's CTA arrival count (0 between calls)
 };
 // decode_q4.cu: the batch-1 kernels for 4-bit expert weights (bf16 tokens,
 // bf16 router) and the quantiser

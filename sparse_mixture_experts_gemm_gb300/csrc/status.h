@@ -23,6 +23,7 @@ enum WaitSite {
   SITE_DRAIN = 5,           // final wait for in-flight copies / MMAs
   SITE_INDEX = 6,           // an index check failed
   SITE_DEBUG = 7,           // the test hook's never-signalled barrier
+  SITE_STAGE = 8,           // a 4-bit batch-1 kernel waiting for its staged rows
 };
 
 }  // namespace moe
