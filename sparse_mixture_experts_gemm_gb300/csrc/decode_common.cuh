@@ -96,18 +96,13 @@ __device__ __forceinline__ float fkey_inv(unsigned key) {
   return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
-// One warp: the k largest of E <= 256 logits (ties to the lower index) and
-// their softmax weights, into s_sel / s_selw (shared memory).  Each lane holds
-// experts lane + 32 i; a round takes the warp maximum of the keys, then the
-// lowest expert index holding it, with one redux.sync each.
-__device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int lane, int *s_sel,
-                                          float *s_selw) {
-  unsigned key[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = (e < E) ? fkey(__ldcg(logits + e)) : 0u;
-  }
+// One warp: the k largest of E <= 256 logits given as order-preserving keys
+// (key[i] of expert lane + 32 i, 0 past E), ties to the lower index, and
+// their softmax weights, into s_sel / s_selw (shared memory).  A round takes
+// the warp maximum of the keys, then the lowest expert index holding it, with
+// one redux.sync each.
+__device__ __forceinline__ void topk_from_keys(unsigned (&key)[8], int E, int k, int lane,
+                                               int *s_sel, float *s_selw) {
   float selv[kMaxTopK];
   int seli[kMaxTopK];
 #pragma unroll
@@ -147,6 +142,19 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
         s_selw[j] = ex[j] / sum;
       }
   }
+}
+
+// The same from logits in global memory (L2 reads: written by another kernel
+// or CTA).
+__device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int lane, int *s_sel,
+                                          float *s_selw) {
+  unsigned key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (e < E) ? fkey(__ldcg(logits + e)) : 0u;
+  }
+  topk_from_keys(key, E, k, lane, s_sel, s_selw);
 }
 
 // Up to kPre 16-byte vectors of one row held in registers per lane: vector

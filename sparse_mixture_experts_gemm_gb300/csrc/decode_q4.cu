@@ -84,25 +84,23 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
 // ---------------------------------------------------------------- gate/up rows
 // Kernel B's items are (slot s, row f), item = s * F + f, over the k routed
 // slots and the shared expert (slot k): h[item] = silu(gate . x) * (up . x).
-// A CTA takes a block of n consecutive items (one slot; F is a multiple of
-// n), whose code bytes, scales and biases are contiguous in both matrices.  A
-// row of d columns is 2G chunks of 32 codes (16 bytes), G = d / 64; a team of
-// ceil(G / 32) warps shares a row and its lane slot q < G owns chunks q and
-// q + G (consecutive lanes read consecutive 16 bytes: no bank conflicts),
-// with the token's 2 x 32 values of those chunks in registers.  Team j takes
-// items kQB j .. kQB j + kQB - 1 of the block, and its rows are one stage of
-// the copy: every thread issues its cp.async share of stage j and arrives on
-// stage j's barrier, so team j starts computing when its own rows landed,
-// while later stages are still in flight.
+// A CTA of 16 warps takes a block of n consecutive items (one slot; F is a
+// multiple of n), whose code bytes, scales and biases are contiguous in both
+// matrices.  A row of d columns is 2G chunks of 32 codes (16 bytes), G =
+// d / 64; a team of ceil(2G / 32) warps shares a row, its lane slot q owning
+// chunk q (consecutive lanes read consecutive 16 bytes: no bank conflicts)
+// with the token's 32 values of that chunk in registers.  Each team takes
+// kQB items of the block.
 constexpr int kQB = 4;
+constexpr int kGateUpWarps = 16;
 
-struct XChunks {
-  float a[32], b[32];
-  float sa, sb;
+struct XChunk {
+  float x[32];
+  float sx;
 };
 
 // 32 token values (one chunk) from the CTA's shared-memory copy of the token.
-__device__ __forceinline__ void load_x32(float (&x)[32], float &sx, const uint4 *tok, int chunk) {
+__device__ __forceinline__ void load_x_chunk(XChunk &xc, const uint4 *tok, int chunk) {
   const uint4 *p = tok + chunk * 4;
   float s = 0.0f;
 #pragma unroll
@@ -111,17 +109,12 @@ __device__ __forceinline__ void load_x32(float (&x)[32], float &sx, const uint4 
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      x[8 * j + 2 * t] = __uint_as_float(u[t] << 16);
-      x[8 * j + 2 * t + 1] = __uint_as_float(u[t] & 0xFFFF0000u);
-      s += x[8 * j + 2 * t] + x[8 * j + 2 * t + 1];
+      xc.x[8 * j + 2 * t] = __uint_as_float(u[t] << 16);
+      xc.x[8 * j + 2 * t + 1] = __uint_as_float(u[t] & 0xFFFF0000u);
+      s += xc.x[8 * j + 2 * t] + xc.x[8 * j + 2 * t + 1];
     }
   }
-  sx = s;
-}
-
-__device__ __forceinline__ void load_x_chunks(XChunks &xc, const uint4 *tok, int q, int G) {
-  load_x32(xc.a, xc.sa, tok, q);
-  load_x32(xc.b, xc.sb, tok, q + G);
+  xc.sx = s;
 }
 
 __device__ __forceinline__ float chunk_dot(const uint4 &c, const float (&x)[32]) {
@@ -139,26 +132,27 @@ struct QBlock {
   const uint16_t *b;
 };
 
-__device__ __forceinline__ float qblock_row_dot(const QBlock &m, int r, int G, int q,
-                                                const XChunks &xc) {
-  const uint4 ca = m.c[r * 2 * G + q], cb = m.c[r * 2 * G + q + G];
-  const int ga = q >> 1, gb = (q + G) >> 1;
-  return q4_finish(chunk_dot(ca, xc.a), xc.sa, m.s[r * G + ga], m.b[r * G + ga]) +
-         q4_finish(chunk_dot(cb, xc.b), xc.sb, m.s[r * G + gb], m.b[r * G + gb]);
+// chunk q of row r against its token chunk: that chunk's share of the row's dot
+__device__ __forceinline__ float qblock_chunk_dot(const QBlock &m, int r, int G, int q,
+                                                  const XChunk &xc) {
+  const int g = q >> 1;
+  return q4_finish(chunk_dot(m.c[r * 2 * G + q], xc.x), xc.sx, m.s[r * G + g], m.b[r * G + g]);
 }
 
-// Team geometry of a 256-thread CTA for rows of d columns.
+// Team geometry of a kGateUpWarps-warp CTA for rows of d columns (the team
+// count a power of two, so that the block size divides F).
 struct Team {
   int wt, teams, team, tw, q;
   bool active;
   __device__ Team(int d, int warp, int lane) {
-    const int G = d / kQ4Group;
-    wt = (G + 31) / 32;
-    teams = 8 / wt;
+    const int chunks = 2 * (d / kQ4Group);
+    wt = (chunks + 31) / 32;
+    teams = 1;
+    while (2 * teams * wt <= kGateUpWarps) teams *= 2;
     team = warp / wt;
     tw = warp - team * wt;
     q = tw * 32 + lane;
-    active = team < teams && q < G;
+    active = team < teams && q < chunks;
   }
 };
 
@@ -236,18 +230,39 @@ __device__ __forceinline__ void gateup_issue(uint8_t *base, const Q4Mat &mg, con
 }  // namespace
 
 // ---------------------------------------------------------------- A: router + top-k
-// One warp per expert logit (bf16 router rows requested before the
-// dependency wait, the token copied once per CTA).  The last CTA to finish
-// picks the top-k once for the layer (dsel, dselw) and clears the count.
-__global__ void __launch_bounds__(256) decode_router_q4_kernel(const DecodeArgs a) {
+// One cluster of ceil(E / 16) CTAs of 16 warps, one warp per expert logit
+// (bf16 router rows requested before the dependency wait, the token copied
+// once per CTA).  Every logit goes straight into CTA 0's shared memory; after
+// one cluster barrier CTA 0 picks the layer's top-k (dsel).  No global
+// round trip, fence or arrival counter sits between the logits and the
+// choice.
+constexpr int kRouterWarps = 16;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// st.shared::cluster of one float at a CTA-local shared address, in CTA `rank`
+__device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+__global__ void __launch_bounds__(kRouterWarps * 32) decode_router_q4_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
-  __shared__ int s_last;
+  __shared__ float s_lg[256];  // CTA 0: the layer's logits
   __shared__ int s_sel[kMaxTopK];
   __shared__ float s_selw[kMaxTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d;
   const int nvec = d * 2 / 16;
-  const int e = blockIdx.x * 8 + warp;
+  const int e = blockIdx.x * kRouterWarps + warp;
   const uint4 *row = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.wr) +
                                                      static_cast<long long>(e) * d);
   RowPre pr;
@@ -258,38 +273,41 @@ __global__ void __launch_bounds__(256) decode_router_q4_kernel(const DecodeArgs 
   load_token(xs, a.x, nvec);
   if (e < a.E) {
     const float acc = warp_sum(row_dot_pre<__nv_bfloat16>(pr, row, xs, nvec, lane));
-    if (lane == 0) a.logits[e] = acc + (a.bias ? a.bias[e] : 0.0f);
+    if (lane == 0) st_cluster_f32(&s_lg[e], 0, acc + (a.bias ? a.bias[e] : 0.0f));
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.dcnt, 1u) == gridDim.x - 1;
+  cluster_sync_all();  // every CTA of the cluster reaches this: no return above
+  if (cluster_ctarank() != 0 || warp != 0) return;
+  unsigned key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ee = lane + 32 * i;
+    key[i] = ee < a.E ? fkey(s_lg[ee]) : 0u;
   }
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();
-  warp_topk(a.logits, a.E, a.k, lane, s_sel, s_selw);
+  topk_from_keys(key, a.E, a.k, lane, s_sel, s_selw);
   __syncwarp();
   if (lane < a.k) {
-    a.dsel[lane] = s_sel[lane];
-    a.dselw[lane] = s_selw[lane];
+    for (int r = 0; r < kSelReplicas; ++r) {
+      a.dsel[32 * r + lane] = s_sel[lane];
+      a.dsel[32 * r + 8 + lane] = __float_as_int(s_selw[lane]);
+    }
   }
-  if (lane == 0) *a.dcnt = 0u;
 }
 
 // ---------------------------------------------------------------- B: gate/up
 // Blocks of the shared expert's items (static rows) are copied before the
 // dependency wait; routed blocks read their expert from dsel after it.
-__global__ void __launch_bounds__(256) decode_gateup_q4_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kGateUpWarps * 32) decode_gateup_q4_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   __shared__ __align__(8) uint64_t bar[2];
-  __shared__ float red[8][2 * kQB];
+  __shared__ float red[kGateUpWarps][2 * kQB];
   __shared__ int s_row0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, F = a.F, G = d / kQ4Group;
   const Team tm(d, warp, lane);
   const int n = tm.teams * kQB;
-  const int ns = tm.teams >= 2 ? 2 : 1;  // copy stages
+  // copy stages: the compute left after the last stage lands is 1 / ns of the
+  // block (more stages issue more, smaller copies, and measured slower)
+  const int ns = tm.teams >= 2 ? 2 : 1;
   const int it0 = blockIdx.x * n;
   const int s = it0 / F, f0 = it0 - s * F;
   const bool shared_blk = s >= a.k;
@@ -300,42 +318,41 @@ __global__ void __launch_bounds__(256) decode_gateup_q4_kernel(const DecodeArgs 
   __syncthreads();
   if (shared_blk) gateup_issue(qsm, a.q.sg, a.q.su, f0, n, d, ns, bar);
   pdl_wait();
-  // kernel A is complete: kernel C may start and stage its down rows (it reads
-  // only the top-k) while this kernel streams
+  // kernel A is complete: kernel C may launch (it reads only the top-k)
   pdl_launch_dependents();
   // the token (the previous layer's output) and this block's expert, in one
   // round of L2 reads
   const GateUpSmem sm(qsm, n, d);
   uint4 *xs = const_cast<uint4 *>(sm.x);
-  if (!shared_blk && threadIdx.x == 0) s_row0 = __ldcg(a.dsel + s) * F + f0;
+  if (!shared_blk && threadIdx.x == 0)
+    s_row0 = __ldcg(a.dsel + 32 * (blockIdx.x % kSelReplicas) + s) * F + f0;
   const uint4 *xg = static_cast<const uint4 *>(a.x);
   for (int i = threadIdx.x; i < d * 2 / 16; i += blockDim.x) xs[i] = __ldcg(xg + i);
   __syncthreads();
   if (!shared_blk) gateup_issue(qsm, a.q.g, a.q.u, s_row0, n, d, ns, bar);
-  XChunks xc;
-  if (tm.active) load_x_chunks(xc, sm.x, tm.q, G);
-  // team j takes kQB / ns items of every stage, so all warps compute on each
-  // stage as it lands: item m of the team is st n / ns + j kQB / ns + jj with
-  // (st, jj) = (m / 2, m % 2) for two stages, (0, m) for one.  The loop has no
-  // branch around a row, so the rows' dependent FMA chains interleave;
-  // threads outside a team read row 0 with a zero token.
+  XChunk xc;
+  if (tm.active) load_x_chunk(xc, sm.x, tm.q);
+  // team j takes per = kQB / ns items of every stage, so all warps compute on
+  // each stage as it lands: the team's item m = st per + jj is row
+  // st n / ns + j per + jj of the block.  Threads outside a team read row 0
+  // with a zero token.
   const int per = kQB / ns;
   const int team_c = tm.team < tm.teams ? tm.team : 0;
   const int q_c = tm.active ? tm.q : 0;
   if (!tm.active) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) xc.a[c] = xc.b[c] = 0.0f;
-    xc.sa = xc.sb = 0.0f;
+    for (int c = 0; c < 32; ++c) xc.x[c] = 0.0f;
+    xc.sx = 0.0f;
   }
   float v[2 * kQB];
-  bool ok = mbar_wait(smem_u32(&bar[0]), 0, MOE_WAIT_LIMIT_CYCLES, nullptr);
+  bool ok = true;
 #pragma unroll
   for (int m = 0; m < kQB; ++m) {
-    if (m == kQB / 2 && ns == 2) ok = mbar_wait(smem_u32(&bar[1]), 0, MOE_WAIT_LIMIT_CYCLES, nullptr) && ok;
-    const int st = ns == 2 ? m / 2 : 0, jj = ns == 2 ? m % 2 : m;
+    const int st = m / per, jj = m - st * per;
+    if (jj == 0) ok = mbar_wait(smem_u32(&bar[st]), 0, MOE_WAIT_LIMIT_CYCLES, nullptr) && ok;
     const int r = st * (n / ns) + team_c * per + jj;
-    v[2 * m] = qblock_row_dot(sm.g, r, G, q_c, xc);
-    v[2 * m + 1] = qblock_row_dot(sm.u, r, G, q_c, xc);
+    v[2 * m] = qblock_chunk_dot(sm.g, r, G, q_c, xc);
+    v[2 * m + 1] = qblock_chunk_dot(sm.u, r, G, q_c, xc);
   }
   if (!ok) {
 #pragma unroll
@@ -349,7 +366,7 @@ __global__ void __launch_bounds__(256) decode_gateup_q4_kernel(const DecodeArgs 
   if (i < n) {
     const int st = i / (n / ns), rem = i - st * (n / ns);
     const int team = rem / per, jj = rem - team * per;
-    const int m = st * (kQB / 2) + jj;  // ns == 1: st = 0, m = jj
+    const int m = st * per + jj;
     float g = 0.0f, u = 0.0f;
     for (int w = 0; w < tm.wt; ++w) {
       g += red[team * tm.wt + w][2 * m];
@@ -391,11 +408,11 @@ __host__ __device__ constexpr size_t down_smem_bytes(int R, int nslot, int F) {
 }
 
 template <int CPL>
-__global__ void __launch_bounds__(320) decode_down_q4_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(640) decode_down_q4_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   __shared__ int s_sel[kMaxTopK];
   __shared__ float s_selw[kMaxTopK];
-  __shared__ float acc_s[10][kQR];
+  __shared__ float acc_s[20][kQR];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, F = a.F, GF = F / kQ4Group;
   const int sps = F / CPL;  // slices per slot
@@ -413,8 +430,9 @@ __global__ void __launch_bounds__(320) decode_down_q4_kernel(const DecodeArgs a)
   pdl_launch_dependents();
   // the layer's top-k (kernel A finished before kernel B let this kernel start)
   if (static_cast<int>(threadIdx.x) < a.k) {
-    s_sel[threadIdx.x] = __ldcg(a.dsel + threadIdx.x);
-    s_selw[threadIdx.x] = __ldcg(a.dselw + threadIdx.x);
+    const int *rep = a.dsel + 32 * (blockIdx.x % kSelReplicas);
+    s_sel[threadIdx.x] = __ldcg(rep + threadIdx.x);
+    s_selw[threadIdx.x] = __int_as_float(__ldcg(rep + 8 + threadIdx.x));
   }
   __syncthreads();
   {
@@ -530,17 +548,28 @@ __global__ void quantize_q4_kernel(const T *__restrict__ w, long long ngroups, i
 namespace {
 template <typename K>
 cudaError_t launch_q(K kern, int grid, int threads, size_t smem, cudaStream_t st, bool pdl,
-                     const DecodeArgs &a) {
+                     const DecodeArgs &a, int cluster = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
@@ -552,31 +581,43 @@ int sm_count() {
   return sms;
 }
 
+// Kernels B and C each take more than half of an SM's shared memory, so that
+// no SM holds two CTAs of either: two CTAs of B on one SM share its copy
+// engine and finish last, and the layer waits for them.
+constexpr size_t kOnePerSm = 116 * 1024;
+size_t one_per_sm(size_t bytes) { return bytes > kOnePerSm ? bytes : kOnePerSm; }
+
+// items per kernel-B block: kQB per team, as the Team geometry counts teams
 int items_per_cta(int d) {
-  const int wt = (d / kQ4Group + 31) / 32;
-  return (8 / wt) * kQB;
+  const int wt = (2 * (d / kQ4Group) + 31) / 32;
+  int teams = 1;
+  while (2 * teams * wt <= kGateUpWarps) teams *= 2;
+  return teams * kQB;
 }
 size_t gateup_smem(int d) { return gateup_smem_bytes(items_per_cta(d), d); }
 
 // columns of h per thread in kernel C: the fewest that keep the CTA within
-// 320 threads
+// 640 threads (more warps hide more of the dependent-FMA latency)
 int down_cpl(const DecodeArgs &a) {
   const int slots = a.k + a.n_shared;
-  for (int cpl : {8, 16, 32})
-    if (slots * (a.F / cpl) <= 320) return cpl;
+  for (int cpl : {8, 16})
+    if (slots * (a.F / cpl) <= 640) return cpl;
   return 0;
 }
 }  // namespace
 
+// one cluster: the whole grid (at most 16 CTAs for E <= 256)
 cudaError_t launch_decode_router_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
-  return launch_q(decode_router_q4_kernel, (a.E + 7) / 8, 256, static_cast<size_t>(a.d) * 2, st,
-                  pdl, a);
+  const int ncta = (a.E + kRouterWarps - 1) / kRouterWarps;
+  return launch_q(decode_router_q4_kernel, ncta, kRouterWarps * 32, static_cast<size_t>(a.d) * 2,
+                  st, pdl, a, ncta);
 }
 // one CTA per block of items; F is a multiple of the block
 cudaError_t launch_decode_gateup_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
   const int per = items_per_cta(a.d);
   const int grid = (a.k + a.n_shared) * a.F / per;
-  return launch_q(decode_gateup_q4_kernel, grid, 256, gateup_smem(a.d), st, pdl, a);
+  return launch_q(decode_gateup_q4_kernel, grid, kGateUpWarps * 32, one_per_sm(gateup_smem(a.d)),
+                  st, pdl, a);
 }
 cudaError_t launch_decode_down_q4(const DecodeArgs &a, cudaStream_t st, bool pdl) {
   const int sms = sm_count();
@@ -589,19 +630,23 @@ cudaError_t launch_decode_down_q4(const DecodeArgs &a, cudaStream_t st, bool pdl
   const int nslot = a.k + a.n_shared;
   const int threads = (nslot * (a.F / cpl) + 31) / 32 * 32;
   const int grid = (a.d + R - 1) / R;
-  const size_t smem = down_smem_bytes(R, nslot, a.F);
+  const size_t smem = one_per_sm(down_smem_bytes(R, nslot, a.F));
   if (cpl == 8) return launch_q(decode_down_q4_kernel<8>, grid, threads, smem, st, pdl, b);
-  if (cpl == 16) return launch_q(decode_down_q4_kernel<16>, grid, threads, smem, st, pdl, b);
-  return launch_q(decode_down_q4_kernel<32>, grid, threads, smem, st, pdl, b);
+  return launch_q(decode_down_q4_kernel<16>, grid, threads, smem, st, pdl, b);
 }
 
 // Kernel B stages a block of gate/up rows and the token: at most 72 KB
 // (n d = 64 K for every supported d, plus the scales and biases) + 32 KB.
 // Kernel C stages at most 16 rows x (k + 1) F / 2 (+ 1/8) bytes: 90 KB.
+// Both launch with kOnePerSm (116 KB), above either.  Kernel A runs as one
+// cluster of up to 16 CTAs (above the portable 8).
 cudaError_t decode_q4_set_smem_attr() {
-  const int bytes = 104 * 1024;
+  const int bytes = static_cast<int>(kOnePerSm);
   cudaError_t e = cudaFuncSetAttribute(decode_router_q4_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_router_q4_kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_gateup_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes);
@@ -610,9 +655,6 @@ cudaError_t decode_q4_set_smem_attr() {
                              bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_down_q4_kernel<16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_down_q4_kernel<32>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e;
 }

@@ -102,6 +102,7 @@ cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *o
 // 4-bit group-affine matrix (codes two per byte, even column in the low
 // nibble; one bf16 scale and bias per 64 columns of a row)
 constexpr int kQ4Group = 64;
+constexpr int kSelReplicas = 16;
 struct Q4Mat {
   const uint8_t *c;   // [rows][cols / 2]
   const uint16_t *s;  // [rows][cols / 64]
@@ -126,10 +127,10 @@ struct DecodeArgs {
   int ring;            // kernel B: ring slots per CTA
   int c_rows;          // kernel C: output rows per CTA (upper bound)
   Q4Weights q;         // 4-bit expert weights (decode_q4.cu), unused by the bf16 kernels
-  // decode_q4.cu: the top-k picked once per layer by kernel A's last CTA
-  int *dsel;           // [k] chosen experts
-  float *dselw;        // [k] their routing weights
-  unsigned *dcnt;      // kernel A's CTA arrival count (0 between calls)
+  // decode_q4.cu: the top-k picked once per layer by kernel A, in
+  // kSelReplicas copies of 128 bytes (32 words: [0, 8) experts, [8, 16) their
+  // weights as float bits), so that the many CTAs reading it share no line
+  int *dsel;
 };
 // decode_q4.cu: the batch-1 kernels for 4-bit expert weights (bf16 tokens,
 // bf16 router) and the quantiser

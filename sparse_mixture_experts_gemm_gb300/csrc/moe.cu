@@ -107,7 +107,7 @@ struct moe_handle {
   // GEMMs' tile counters
   int32_t *route_ctl = nullptr;
   float *w = nullptr, *logits = nullptr, *hdec = nullptr;
-  int32_t *dctl = nullptr;  // 4-bit batch-1 path: [0] arrival count, [8, 16) sel, [16, 24) weights
+  int32_t *dctl = nullptr;  // 4-bit batch-1 path: the layer's top-k (DecodeArgs::dsel)
   float *cand_v = nullptr;     // router: per expert block top-k candidates
   int32_t *cand_i = nullptr;
   int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
@@ -345,9 +345,7 @@ int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
   const bool pdl = !h->prof;  // event records between kernels would break the chain
   if (h->q4) {
     a.q = h->qw;
-    a.dcnt = reinterpret_cast<unsigned *>(h->dctl);
-    a.dsel = h->dctl + 8;
-    a.dselw = reinterpret_cast<float *>(h->dctl + 16);
+    a.dsel = h->dctl;
     {
       ProfScope ps(h, MOE_KERNEL_DECODE_ROUTER, st);
       MOE_TRY(launch_decode_router_q4(a, st, pdl));
@@ -426,9 +424,9 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
                                  &q4->s_down};
     for (int i = 0; i < (cfg->n_shared ? 6 : 3); ++i)
       if ((rc = check_q4(*ms[i])) != MOE_OK) return rc;
-    // the batch-1 down kernel gives each thread at most 32 columns of one
-    // slot's h, in a CTA of at most 320 threads
-    if ((cfg->top_k + cfg->n_shared) * cfg->d_ff > 320 * 32) return MOE_ERR_UNSUPPORTED;
+    // the batch-1 down kernel gives each thread at most 16 columns of one
+    // slot's h, in a CTA of at most 640 threads
+    if ((cfg->top_k + cfg->n_shared) * cfg->d_ff > 640 * 16) return MOE_ERR_UNSUPPORTED;
   }
   moe_handle *h = new (std::nothrow) moe_handle();
   if (!h) return MOE_ERR_OUT_OF_MEMORY;
@@ -462,7 +460,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
       {reinterpret_cast<void **>(&h->status), sizeof(int32_t) * 4},
       {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
       {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
-      {reinterpret_cast<void **>(&h->dctl), sizeof(int32_t) * 32},
+      {reinterpret_cast<void **>(&h->dctl), sizeof(int32_t) * 32 * kSelReplicas},
       {reinterpret_cast<void **>(&h->cand_v), sizeof(float) * nqk * Tm},
       {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
       {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},
