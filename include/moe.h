@@ -130,9 +130,14 @@ typedef struct {
  * group-affine; the router stays bfloat16.  cfg is as for moe_create with
  * dtype MOE_BF16 (tokens and outputs are bf16) and w_gate, w_up, w_down,
  * s_gate, s_up, s_down NULL; w holds the 4-bit matrices instead (kept by
- * pointer, like the bf16 weights).  Supported: as moe_create; the handle runs
- * moe_forward with T == 1 (the batch-1 path, which reads 3.6x fewer weight
- * bytes) and moe_route; moe_forward with T >= 2 returns MOE_ERR_UNSUPPORTED.
+ * pointer, like the bf16 weights).  Supported: as moe_create, with
+ * (top_k + n_shared) * d_ff <= 10240.  The handle runs moe_route, moe_forward
+ * with T == 1 (the batch-1 path, which reads 3.6x fewer weight bytes) and,
+ * when d_model and d_ff are multiples of 512, moe_forward with T >= 2: the
+ * grouped GEMMs dequantise each 64-column weight block into bf16 on the chip
+ * (one rounding of s q + b) right before the tensor-core multiplication.  For
+ * other shapes moe_forward with T >= 2 returns MOE_ERR_UNSUPPORTED.
+ * Section "Dequantise weights within matrix multiplication".
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, OUT_OF_MEMORY, CUDA.
  */
 int moe_create_q4(const moe_config *cfg, const moe_q4_weights *w, moe_handle **out);

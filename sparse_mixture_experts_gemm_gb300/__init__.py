@@ -287,10 +287,11 @@ class Q4Layer(MoELayer):
     Sg, Su, Sd as (codes, scales, biases) triples of CUDA tensors in the layouts
     of the bf16 matrices ([E][F][d] -> codes [E][F][d/2], scales and biases
     [E][F][d/64]); shared triples None when there is no shared expert.  Runs the
-    batch-1 path (forward with one token) and routing.
+    batch-1 path (one token), routing, and batches of up to max_tokens tokens
+    when d and F are multiples of 512.
     """
 
-    def __init__(self, weights: dict, top_k: int, bias=None):
+    def __init__(self, weights: dict, top_k: int, max_tokens: int = 1, bias=None):
         import torch
         Wr = weights["Wr"]
         assert Wr.dtype == torch.bfloat16
@@ -308,7 +309,7 @@ class Q4Layer(MoELayer):
         qw = moe_q4_weights(mat(weights["Wg"]), mat(weights["Wu"]), mat(weights["Wd"]),
                             mat(weights.get("Sg")), mat(weights.get("Su")),
                             mat(weights.get("Sd")))
-        cfg = moe_config(d, E, top_k, F, 1 if shared else 0, 1, MOE_BF16, _ptr(Wr), None, None,
-                         None, None, None, None, _ptr(bias))
+        cfg = moe_config(d, E, top_k, F, 1 if shared else 0, max_tokens, MOE_BF16, _ptr(Wr), None,
+                         None, None, None, None, None, _ptr(bias))
         self.cfg, self.qw = cfg, qw
         self.handle = moe_create_q4(cfg, qw)

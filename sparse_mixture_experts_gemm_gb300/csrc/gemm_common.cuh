@@ -1,0 +1,159 @@
+// gemm_common.cuh -- pieces shared by the bf16 and the 4-bit grouped GEMMs:
+// the epilogue's activation and row stores, the device-side group table and
+// tile decoding, and the shared-memory ring that hands claimed tile ids from
+// the producer to the other roles of a CTA.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+// silu(z) = z / (1 + e^-z) with the fast (approximate-reciprocal) division:
+// relative error ~1e-7, far below the bf16 rounding of h; for z -> -inf the
+// denominator overflows to inf and the quotient is 0, the function's limit.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+template <typename T>
+__device__ __forceinline__ void store32(T *dst, const float (&v)[32]);
+template <>
+__device__ __forceinline__ void store32<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&v)[32]) {
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[q * 8 + 2 * j], v[q * 8 + 2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+template <>
+__device__ __forceinline__ void store32<float>(float *dst, const float (&v)[32]) {
+  float4 *d = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+// Group table built by every CTA of a grouped GEMM: s_off[g] = first slot of
+// group g (g <= E), s_mt[g] = first M tile of group g (g <= E + 1; group E is
+// the shared expert).
+struct GroupTable {
+  const int *off;
+  const int *mt;
+};
+
+__device__ __forceinline__ GemmTile decode_tile(const GroupTable &gt, const GemmParams &p, int i,
+                                                int n_cols, bool down) {
+  const int E = p.n_routed;
+  int lo = 0, hi = E;  // largest g with nt * mt[g] <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.nt * gt.mt[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int mtg = gt.mt[g + 1] - gt.mt[g];
+  const int local = i - p.nt * gt.mt[g];
+  const int n = local / mtg, m = local - (local / mtg) * mtg;
+  GemmTile t;
+  t.group = g;
+  t.n0 = n * n_cols;
+  t.pad[0] = t.pad[1] = t.pad[2] = 0;
+  if (g < E) {
+    const int cnt = gt.off[g + 1] - gt.off[g];
+    t.a_row = gt.off[g] + m * kBM;
+    t.out_row = t.a_row;
+    t.rows = min(kBM, cnt - m * kBM);
+  } else {
+    t.rows = min(kBM, p.T - m * kBM);
+    t.out_row = p.A + m * kBM;
+    t.a_row = down ? t.out_row : m * kBM;  // gate/up reads tokens in order
+  }
+  return t;
+}
+
+// Every thread of the CTA: the group table (s_off[g] for g <= E, s_mt[g] =
+// first M tile of group g for g <= E + 1, group E the shared expert), built
+// from the offsets the routing wrote.  Warp 2 runs the exclusive scan.
+__device__ __forceinline__ void build_group_table(const GemmParams &p, int *s_off, int *s_mt,
+                                                  int warp, int lane) {
+  const int E = p.n_routed;
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) s_off[g] = p.offsets[g];
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int rows = g < E ? s_off[g + 1] - s_off[g] : (p.n_shared ? p.T : 0);
+    s_mt[g] = (rows + kBM - 1) / kBM;
+  }
+  __syncthreads();
+  if (warp == 2) {
+    const int n = E + 1;
+    const int per = (n + 31) / 32;
+    int sum = 0;
+    for (int q = 0; q < per; ++q) {
+      const int i = lane * per + q;
+      if (i < n) sum += s_mt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int q = 0; q < per; ++q) {
+      const int i = lane * per + q;
+      if (i < n) {
+        const int v = s_mt[i];
+        s_mt[i] = run;
+        run += v;
+      }
+    }
+    if (lane == 31) s_mt[n] = incl;
+  }
+}
+
+// Tile sequence of a CTA of the grouped GEMMs: lane 0 of the producer warp
+// claims tiles (its first is blockIdx.x, every later one comes from a global
+// counter, so CTAs that drew cheap tiles take more of them) and publishes each
+// id in a small shared ring; the MMA thread, the epilogue warps and the gather
+// warps read the ids from the ring in the same order.  A claim past the last
+// tile ends every role's loop.  The router keeps the static order (one tile
+// per CTA at most sizes).
+constexpr int kTileRing = 4;
+struct TileRing {
+  uint32_t full0, empty0;  // [kTileRing] mbarriers each
+  volatile int *ids;       // [kTileRing]
+};
+
+// Lane 0 of the producer warp: claim the it-th tile.  False when the slot's
+// readers did not release it in time (the abort flag is then set).
+__device__ __forceinline__ bool claim_tile(const TileRing &r, int it, int *ctr, int ntiles,
+                                           long long limit, volatile int *abort, int &ti) {
+  const int slot = it % kTileRing;
+  if (it >= kTileRing && !mbar_wait(r.empty0 + 8 * slot, ((it / kTileRing) - 1) & 1, limit, abort))
+    return false;
+  ti = it == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(ctr, 1);
+  if (ti > ntiles) ti = ntiles;
+  r.ids[slot] = ti;
+  mbar_arrive(r.full0 + 8 * slot);  // release: the id is visible with the phase
+  return true;
+}
+
+// One thread per reading role: the it-th tile id; false when it did not
+// arrive in time.
+__device__ __forceinline__ bool read_tile(const TileRing &r, int it, long long limit,
+                                          volatile int *abort, int &ti) {
+  const int slot = it % kTileRing;
+  if (!mbar_wait(r.full0 + 8 * slot, (it / kTileRing) & 1, limit, abort)) return false;
+  ti = r.ids[slot];
+  mbar_arrive(r.empty0 + 8 * slot);
+  return true;
+}
+
+}  // namespace
+}  // namespace moe

@@ -81,6 +81,23 @@ template <typename T, int EPI, int BN>
 cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
+// gemm_q4.cu: the grouped GEMMs (EPI_SWIGLU, EPI_STORE; bf16 tokens) with
+// 4-bit group-affine weights, dequantised into the MMA's B tiles.  Maps:
+// a = the A operand by TMA (x for the shared expert's gate/up rows, H for the
+// down GEMM); c, s, b = codes [rows][K / 2] u8 (boxes 32 bytes x rows), scales
+// and biases [rows][K / 64] (boxes 8 groups x rows), indexed
+// 2 * shared + half (half 0: gate or down, 1: up).
+struct Q4GemmMaps {
+  CUtensorMap a;
+  CUtensorMap c[4], s[4], b[4];
+};
+constexpr int kQ4GemmSmem = 3 * (kBM * 128 + kBN * 128) + 6 * (kBN * 32) + 2 * (2 * kBN * 8 * 2) +
+                            1024 + kGemmCtrl;
+template <int EPI>
+cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
+template <int EPI>
+cudaError_t gemm_q4_set_smem_attr();
+
 // moe.cu: tensor-map encoding (host only, no allocation)
 bool encode_map_2d(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
                    uint32_t box_cols, uint32_t box_rows, bool swizzle128);

@@ -59,8 +59,11 @@ bool moe::encode_map_2d(CUtensorMap *m, const void *base, size_t esz, uint64_t r
                         uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return false;
-  const CUtensorMapDataType dt =
-      esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  // 2-byte elements travel as bf16 (also the raw bits of 4-bit scales and
+  // biases), 1-byte ones as u8 (4-bit codes, two per byte); TMA copies bits
+  const CUtensorMapDataType dt = esz == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * esz};
   cuuint32_t box[2] = {box_cols, box_rows};
@@ -118,7 +121,9 @@ struct moe_handle {
   CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
+  bool q4_prefill = false;  // the grouped GEMMs support the layer's shape
   Q4Weights qw = {};
+  Q4GemmMaps q4g = {}, q4d = {};  // gate/up and down GEMM maps (a set per call / once)
   // profiling
   bool prof = false;
   std::vector<ProfRec> recs;
@@ -294,7 +299,13 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.tile_ctr = h->tile_ctr(0);
     p.perm = h->perm;
     p.x = x;
-    MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
+    if (h->q4) {  // 4-bit weights (bf16 tokens): dequantised in the GEMM
+      Q4GemmMaps mq = h->q4g;
+      mq.a = m.m[1];
+      MOE_TRY(launch_gemm_q4<EPI_SWIGLU>(mq, p, h->num_sms, st));
+    } else {
+      MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
+    }
   }
   {
     ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
@@ -310,7 +321,11 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.ldo = d;
     p.kid = KID_GEMM_DOWN;
     p.tile_ctr = h->tile_ctr(1);
-    MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st)));
+    if (h->q4) {
+      MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st));
+    } else {
+      MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st)));
+    }
   }
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
@@ -414,6 +429,16 @@ int check_q4(const moe_q4_matrix &m) {
 
 Q4Mat q4mat(const moe_q4_matrix &m) { return Q4Mat{m.codes, m.scales, m.biases}; }
 
+// Grouped-GEMM maps of one 4-bit matrix [rows][K]: codes in boxes of 32
+// bytes (one 64-column K block) x box_rows, scales and biases in boxes of 8
+// groups x box_rows.  K a multiple of 512 (16-byte scale/bias row pitch).
+bool make_q4_maps(Q4GemmMaps &q, int i, const moe_q4_matrix &m, uint64_t rows, int K,
+                  uint32_t box_rows) {
+  return encode_map_2d(&q.c[i], m.codes, 1, rows, K / 2, 32, box_rows, false) &&
+         encode_map_2d(&q.s[i], m.scales, 2, rows, K / kQ4Group, 8, box_rows, false) &&
+         encode_map_2d(&q.b[i], m.biases, 2, rows, K / kQ4Group, 8, box_rows, false);
+}
+
 int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
@@ -511,6 +536,33 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
       h->qw.sd = q4mat(q4->s_down);
     }
     if (ok && decode_q4_set_smem_attr() != cudaSuccess) ok = false;
+    // the grouped GEMMs (T >= 2) take K blocks of 64 columns with scale and
+    // bias rows of 16-byte pitch: d and F multiples of 512
+    h->q4_prefill = d % 512 == 0 && F % 512 == 0;
+    if (ok && h->q4_prefill) {
+      const uint64_t EF = static_cast<uint64_t>(E) * F, Ed = static_cast<uint64_t>(E) * d;
+      ok = make_q4_maps(h->q4g, 0, q4->gate, EF, d, kBN / 2) &&
+           make_q4_maps(h->q4g, 1, q4->up, EF, d, kBN / 2) &&
+           make_q4_maps(h->q4d, 0, q4->down, Ed, F, kBN);
+      if (ok && c.n_shared)
+        ok = make_q4_maps(h->q4g, 2, q4->s_gate, F, d, kBN / 2) &&
+             make_q4_maps(h->q4g, 3, q4->s_up, F, d, kBN / 2) &&
+             make_q4_maps(h->q4d, 2, q4->s_down, d, F, kBN);
+      if (ok && !c.n_shared) {  // never used; valid descriptors all the same
+        h->q4g.c[2] = h->q4g.c[0], h->q4g.s[2] = h->q4g.s[0], h->q4g.b[2] = h->q4g.b[0];
+        h->q4g.c[3] = h->q4g.c[1], h->q4g.s[3] = h->q4g.s[1], h->q4g.b[3] = h->q4g.b[1];
+        h->q4d.c[2] = h->q4d.c[0], h->q4d.s[2] = h->q4d.s[0], h->q4d.b[2] = h->q4d.b[0];
+      }
+      if (ok) {  // the down GEMM has no "up" matrix
+        h->q4d.c[1] = h->q4d.c[0], h->q4d.s[1] = h->q4d.s[0], h->q4d.b[1] = h->q4d.b[0];
+        h->q4d.c[3] = h->q4d.c[2], h->q4d.s[3] = h->q4d.s[2], h->q4d.b[3] = h->q4d.b[2];
+        h->q4d.a = h->tm_h;
+        h->q4g.a = h->tm_h;  // replaced by the tokens' map at every call
+      }
+      if (ok && (gemm_q4_set_smem_attr<EPI_SWIGLU>() != cudaSuccess ||
+                 gemm_q4_set_smem_attr<EPI_STORE>() != cudaSuccess))
+        ok = false;
+    }
   }
   if (!ok) {
     moe_destroy(h);
@@ -599,7 +651,7 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
   char *ob = static_cast<char *>(out);
   if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (h->q4 && T != 1) return MOE_ERR_UNSUPPORTED;  // 4-bit weights: batch-1 path only
+  if (h->q4 && T != 1 && !h->q4_prefill) return MOE_ERR_UNSUPPORTED;
   if (T == 1) {
     return h->cfg.dtype == MOE_BF16
                ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),

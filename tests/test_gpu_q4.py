@@ -58,9 +58,12 @@ def test_quantizer_matches_oracle(dev, dtype, shape):
     assert np.array_equal(_bits(biases.view(-1, shape[-1] // 64)), rb)
 
 
-def _oracle_q4(x, w, k, F):
-    """The oracle's 4-bit forward on the same codes, scales and biases."""
+def _oracle_q4(x, w, k, F, rows=None):
+    """The oracle's 4-bit forward on the same codes, scales and biases (on the
+    given token rows only, when rows is set)."""
     E = w["Wr"].shape[0]
+    if rows is not None:
+        x = x[torch.as_tensor(rows, device=x.device)]
 
     def triple(t):
         return None if t is None else (t[0].cpu().numpy(), _bits(t[1]), _bits(t[2]))
@@ -109,7 +112,7 @@ def test_q4_decode_matches_oracle(dev, d, F, E, k, n_shared):
     assert err.max() <= H.OUT_TOL, err
 
 
-def test_q4_handle_routes_and_refuses_batches(dev):
+def test_q4_handle_routes_and_checks_batches(dev):
     d, F, E, k = 2048, 512, 256, 8
     w = synth.q4_layer_weights(7, d, F, E, 1, dev)
     x = H.margined_tokens(8, 2, w["Wr"], k, "bf16", device=dev)
@@ -119,11 +122,14 @@ def test_q4_handle_routes_and_refuses_batches(dev):
         torch.cuda.synchronize()
         ri, rw, _, rc = oracle.route(H.np_view(x[0:1]), H.np_view(w["Wr"]), k)
         H.check_routing(idx, wt, counts, ri, rw, rc)
+        # a batch on a handle made for one token at a time runs as chunks of
+        # one token through the grouped GEMMs
         out = torch.empty((2, d), dtype=torch.bfloat16, device=dev)
-        with pytest.raises(moe.MoeError) as e:
-            moe.moe_forward(layer.handle, x, 2, out)
-        assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+        moe.moe_forward(layer.handle, x, 2, out)
+        torch.cuda.synchronize()
         assert layer.status()[0] == 0
+        ref, *_ = _oracle_q4(x, w, k, F)
+        assert H.row_rel_err(out, ref).max() <= H.OUT_TOL
     finally:
         layer.close()
 
@@ -162,3 +168,76 @@ def test_q4_layer_stack_in_a_cuda_graph(dev):
     finally:
         for layer in layers:
             layer.close()
+
+
+def test_q4_batches_need_d_and_f_multiples_of_512(dev):
+    """The grouped GEMMs read scale/bias rows of 16-byte pitch: a layer with
+    F = 256 runs one token at a time and refuses batches."""
+    w = synth.q4_layer_weights(9, 1024, 256, 16, 1, dev)
+    x = H.margined_tokens(10, 2, w["Wr"], 4, "bf16", device=dev)
+    layer = moe.Q4Layer(w, 4, max_tokens=8)
+    try:
+        out = torch.empty((2, 1024), dtype=torch.bfloat16, device=dev)
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward(layer.handle, x, 2, out)
+        assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+        layer.forward(x[0:1].clone())
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+
+
+# (d, F, E, k, n_shared, T, max_tokens)
+PREFILL_CASES = [
+    (512, 512, 8, 2, 1, 300, 512),       # ragged tiles, few experts
+    (1024, 512, 16, 4, 0, 130, 256),     # no shared expert
+    (2048, 1024, 32, 8, 1, 520, 1024),   # wider F: 8 gate/up N tiles
+    (2048, 512, 256, 8, 1, 384, 192),    # the full-size layer, in two chunks
+]
+
+
+@pytest.mark.parametrize("d,F,E,k,n_shared,T,max_tokens", PREFILL_CASES)
+def test_q4_prefill_matches_oracle(dev, d, F, E, k, n_shared, T, max_tokens):
+    """Batches through the 4-bit grouped GEMMs (dequantisation in the GEMM,
+    the weights rounded once to bf16) against the oracle's exact 4-bit
+    forward; row-normwise 1e-2 as for the bf16 path."""
+    w = synth.q4_layer_weights(200 + d + E + T, d, F, E, n_shared, dev)
+    x = H.margined_tokens(210 + T, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k, max_tokens=max_tokens)
+    try:
+        moe.moe_profile(layer.handle, True)
+        out = layer.forward(x)
+        moe.moe_profile(layer.handle, False)
+        torch.cuda.synchronize()
+        rc, detail = layer.status()
+        assert rc == 0, f"device status {rc} detail {detail}"
+        kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
+        assert {"gemm_gate_up", "gemm_down"} <= kinds, kinds
+    finally:
+        layer.close()
+    ref, *_ = _oracle_q4(x, w, k, F)
+    err = H.row_rel_err(out, ref)
+    assert err.max() <= H.OUT_TOL, err.max()
+
+
+def test_q4_prefill_4k_sample_against_oracle(dev):
+    """The 4096-token prefill of the full-size layer through the 4-bit GEMMs;
+    64 sampled tokens against the oracle (token rows are independent)."""
+    d, F, E, k, T = 2048, 512, 256, 8, 4096
+    w = synth.q4_layer_weights(300, d, F, E, 1, dev)
+    x = synth.tokens(301, T, d, "bf16", dev)
+    layer = moe.Q4Layer(w, k, max_tokens=T)
+    try:
+        out = layer.forward(x)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+    rows = np.random.default_rng(5).choice(T, 64, replace=False)
+    _, _, logits, _ = oracle.route(H.np_view(x[torch.as_tensor(rows, device=dev)]),
+                                   H.np_view(w["Wr"]), k)
+    keep = rows[H.kth_gap(logits, k) >= H.MARGIN]
+    assert len(keep) >= 48
+    ref, *_ = _oracle_q4(x, w, k, F, rows=keep)
+    err = H.row_rel_err(out[torch.as_tensor(keep, device=dev)], ref)
+    assert err.max() <= H.OUT_TOL, err.max()
