@@ -213,6 +213,66 @@ def bench_prefill(cfg, dev, steps, warmup, flush_buf):
     return res
 
 
+def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
+    """The same prefill with 4-bit group-affine expert weights (seeded random
+    codes, scales and biases; bf16 router and tokens): the grouped GEMMs
+    dequantise each weight block on the chip."""
+    d, F, E, k, T = cfg["d"], cfg["F"], cfg["E"], cfg["k"], cfg["T"]
+    w = synth.q4_layer_weights(cfg["seed"] + 7, d, F, E, 1, dev)
+    layer = moe.Q4Layer(w, k, max_tokens=cfg["chunk"])
+    x = synth.tokens(cfg["seed"] + 1000, T, d, "bf16", dev)
+    out = torch.empty_like(x)
+    st = torch.cuda.current_stream()
+    try:
+        for _ in range(warmup):
+            layer.forward(x, out)
+        torch.cuda.synchronize()
+        _, _, cnt = layer.route(x[:cfg["chunk"]])
+        counts = cnt.cpu().numpy()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        moe.moe_profile(layer.handle, True)
+        with Clocks(dev.index or 0) as clk:
+            for i in range(steps):
+                flush_l2(flush_buf)
+                evs[i][0].record(st)
+                layer.forward(x, out)
+                evs[i][1].record(st)
+            torch.cuda.synchronize()
+        prof = moe.moe_profile_read(layer.handle)
+        moe.moe_profile(layer.handle, False)
+        rc, det = layer.status()
+        if rc != 0:
+            raise RuntimeError(f"4-bit prefill device status {rc} ({det})")
+    finally:
+        layer.close()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    active = int((counts > 0).sum())
+    A = T * k
+    flops = 2 * T * d * E + 6 * (A + T) * d * F
+    q4b = 0.5 + 4 / 64  # bytes per weight: codes, bf16 scale and bias per 64
+    byts = (active + 1) * 3 * F * d * q4b + E * d * 2 + 2 * T * d * 2
+    per = {kk: v[0] / max(v[1], 1) for kk, v in prof.items() if v[1] > 0}
+    g1_ms = per.get("gemm_gate_up", 0.0)
+    g1_flops = 4 * (A + T) * d * F
+    return {
+        "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
+        "workload": f"prefill T={T} (d={d}, {E} experts top-{k} + 1 shared, F={F}), 4-bit "
+                    "group-affine expert weights (64 per group, bf16 scale and bias), bf16 "
+                    "router and tokens, L2 flushed between steps",
+        "flops_per_step": flops, "algorithmic_bytes_per_step": byts,
+        "roofline": {"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
+                     "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / pk["bf16"], "traffic": None,
+                     "kernel": "gemm_gate_up (4-bit weights)",
+                     "peak_source": f"{pk['src']} bf16_tflops"} if g1_ms > 0 else None,
+        "whole_step_floors_us": {"tensor": flops / (pk["bf16"] * 1e12) * 1e6,
+                                 "hbm": byts / (pk["hbm"] * 1e9) * 1e6},
+        "kernels_ms_per_step": per, "clocks": clk.summary(),
+        "gpu_launches": sum(v[1] for v in prof.values()) // max(steps, 1) * steps,
+    }
+
+
 def bench_decode(dev, steps, warmup, n_layers=40, q4=False):
     cfg = WORKLOADS["prefill4k"]
     layers = []
@@ -456,6 +516,8 @@ def main():
                            q4=True)
         line["decode_q4"] = decode_summary(dec, pk)
         # decode launches are counted in their own objects
+    if wl_name == "prefill4k":
+        line["prefill_q4"] = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)
     if rank == 0 and not args.no_cpu:
         nthr = host_threads()
         n_tok = min(args.oracle_tokens, T)

@@ -17,7 +17,7 @@
 //     (BN rows x 32 bytes per K block) into a ring of 6 code stages, and the
 //     scales and biases of 8 K blocks at a time into a ring of 2 chunks, by
 //     TMA;
-//   * 8 dequantising warps turn each code stage into the bf16 B tile of an
+//   * 16 dequantising warps turn each code stage into the bf16 B tile of an
 //     operand stage: w = s q + b with one bf16 rounding (q exact in bf16, one
 //     bf16x2 FMA per pair), written in the 128-byte swizzle the MMA
 //     descriptor expects, then a proxy fence and one arrival per warp;
@@ -42,7 +42,8 @@ constexpr int kOp = 3;            // operand stages
 constexpr int kCode = 6;          // code stages
 constexpr int kSb = 2;            // scale/bias chunks
 constexpr int kSbGroups = 8;      // K blocks per scale/bias chunk
-constexpr int kDqWarps = 8;       // dequantising warps
+constexpr int kDqWarps = 16;      // dequantising warps
+constexpr int kDqRows = kBN / kDqWarps;  // B rows per dequantising warp: 16
 constexpr int kABytes = kBM * 128;
 constexpr int kBBytes = kBN * 128;
 constexpr int kCBytes = kBN * 32;                 // codes of one K block
@@ -60,22 +61,36 @@ constexpr int q4_threads() { return 32 * (6 + gather_warps<EPI>() + kDqWarps + 1
 
 // 8 codes of one 32-bit word (columns c .. c + 7, byte j holding column
 // c + 2j in its low nibble) into 8 bf16 weights s q + b, in column order.
-// ((w >> 4j) & 0x000F000F) | 0x43004300 is the bf16 pair (128 + q_j,
-// 128 + q_{j+4}), exact; subtracting 128 leaves q exactly; one bf16x2 FMA
-// rounds s q + b once; byte permutes restore the column order.
+// With w4 = w >> 4, one byte permute puts byte j of w in byte 0 and byte j of
+// w4 in byte 2; masking to 0x000F000F and setting 0x43004300 makes the bf16
+// pair (128 + q_2j, 128 + q_2j+1), exact; subtracting 128 leaves q exactly;
+// one bf16x2 FMA rounds s q + b once.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) {
   const __nv_bfloat162 c128 = __floats2bfloat162_rn(128.0f, 128.0f);
+  const uint32_t w4 = w >> 4;
   uint32_t r[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t sel = (4u + j) << 12 | (4u + j) << 8 | static_cast<uint32_t>(j) << 4 | j;
+    const uint32_t v = (__byte_perm(w, w4, sel) & 0x000F000Fu) | 0x43004300u;
     const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&v), c128);
     const __nv_bfloat162 o = __hfma2(q, s2, b2);
     r[j] = *reinterpret_cast<const uint32_t *>(&o);
   }
-  // r[j] = (w_j, w_{j+4}); out = (w0 w1 | w2 w3 | w4 w5 | w6 w7)
-  return make_uint4(__byte_perm(r[0], r[1], 0x5410), __byte_perm(r[2], r[3], 0x5410),
-                    __byte_perm(r[0], r[1], 0x7632), __byte_perm(r[2], r[3], 0x7632));
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// 16 floats to 16 bf16 (two 16-byte stores; dst 32-byte aligned)
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16 *dst, const float (&v)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    w[j] = *reinterpret_cast<uint32_t *>(&b);
+  }
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 }  // namespace
@@ -441,12 +456,14 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
     cp_async_wait_all();
   } else if (warp >= kDq0 && warp < kCodeWarp) {
     // ------------------------------------------------------------ dequantise
-    // Warp w writes rows 32 w .. 32 w + 31 of each B tile, 4 rows per pass:
-    // lane (r, c) takes code word c of row r (8 codes, the 16-byte chunk c of
-    // the bf16 row), so a pass reads 128 contiguous code bytes and writes 512
-    // contiguous bytes of the swizzled tile: no bank conflicts either way.
+    // Warp w writes rows kDqRows w .. kDqRows (w + 1) - 1 of each B tile, 8
+    // rows per pass:
+    // lane (r, p) takes code words 2p and 2p + 1 of row r (16 codes, the
+    // 16-byte chunks 2p and 2p + 1 of the bf16 row) with one scale and bias,
+    // so a pass reads 256 contiguous code bytes and each store covers 8 rows
+    // whose chunks land in distinct bank groups (rows in even/odd pairs).
     const int w = warp - kDq0;
-    const int c = lane & 7;
+    const int pr = lane & 3;
     int stage = 0, cs = 0, sb = 0;
     uint32_t phase = 0, cph = 0, sbph = 0;
     bool ok = true;
@@ -482,13 +499,15 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
         uint8_t *bt = sB + stage * kBBytes;
         const int gcol = kb % kSbGroups;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = 32 * w + 4 * i + (lane >> 3);
-          const uint32_t word = *reinterpret_cast<const uint32_t *>(code + row * 32 + c * 4);
-          const __nv_bfloat16 sv = ssc[row * kSbGroups + gcol];
-          const __nv_bfloat16 bv = sbi[row * kSbGroups + gcol];
-          const uint4 o = dequant8(word, __bfloat162bfloat162(sv), __bfloat162bfloat162(bv));
-          *reinterpret_cast<uint4 *>(bt + row * 128 + ((c ^ (row & 7)) << 4)) = o;
+        for (int i = 0; i < kDqRows / 8; ++i) {
+          const int row = kDqRows * w + 8 * i + (lane >> 2);
+          const uint2 words = *reinterpret_cast<const uint2 *>(code + row * 32 + pr * 8);
+          const __nv_bfloat162 s2 = __bfloat162bfloat162(ssc[row * kSbGroups + gcol]);
+          const __nv_bfloat162 b2 = __bfloat162bfloat162(sbi[row * kSbGroups + gcol]);
+          uint8_t *rowp = bt + row * 128;
+          *reinterpret_cast<uint4 *>(rowp + (((2 * pr) ^ (row & 7)) << 4)) = dequant8(words.x, s2, b2);
+          *reinterpret_cast<uint4 *>(rowp + (((2 * pr + 1) ^ (row & 7)) << 4)) =
+              dequant8(words.y, s2, b2);
         }
         // the tile is read by the tensor core (async proxy)
         fence_proxy_async_smem();
@@ -546,26 +565,27 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
       const bool valid = r < tl.rows;
       __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                             static_cast<long long>(tl.out_row + r) * p.ldo + tl.n0;
+      // 16 columns at a time: this CTA runs many warps, registers are few
       if (kDual) {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 2; c += 32) {
-          float g[32], u[32];
-          tmem_ld32(tb + c, g);
-          tmem_ld32(tb + kBN / 2 + c, u);
+        for (int c = 0; c < kBN / 2; c += 16) {
+          float g[16], u[16];
+          tmem_ld16(tb + c, g);
+          tmem_ld16(tb + kBN / 2 + c, u);
           tmem_ld_wait();
           if (valid) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) g[i] = silu(g[i]) * u[i];
-            store32<__nv_bfloat16>(orow + c, g);
+            for (int i = 0; i < 16; ++i) g[i] = silu(g[i]) * u[i];
+            store16_bf16(orow + c, g);
           }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
-          float v[32];
-          tmem_ld32(tb + c, v);
+        for (int c = 0; c < kBN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + c, v);
           tmem_ld_wait();
-          if (valid) store32<__nv_bfloat16>(orow + c, v);
+          if (valid) store16_bf16(orow + c, v);
         }
       }
       tc_fence_before();
