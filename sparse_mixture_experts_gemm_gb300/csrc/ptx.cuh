@@ -51,15 +51,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 #define MOE_WAIT_LIMIT_CYCLES 4000000000LL
 #endif
 
+// try_wait with a suspend-time hint: the thread sleeps in the barrier until
+// the phase completes or about `ns` nanoseconds passed, instead of spinning
+// (spinning warps take issue slots from the warps doing the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of the barrier; false when `limit` cycles passed or
 // *abort (shared flag set by another role of the CTA; may be null) became
-// non-zero.
+// non-zero.  Polls sleep in the barrier for up to 2 us at a time.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit,
                                           const volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
     if (abort != nullptr && *abort) return false;
     if (clock64() - t0 > limit) return false;
   }
