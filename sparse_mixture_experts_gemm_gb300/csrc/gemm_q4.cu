@@ -23,8 +23,10 @@
 //     descriptor expects, then a proxy fence and one arrival per warp;
 //   * A comes as before (TMA for the shared expert's rows and for H, the
 //     gather warps for routed token rows).
-// The operand ring (A 16 KB + B 32 KB per stage) has 3 stages; the deep
-// prefetch is the code ring's, since the codes are what streams from HBM.
+// A and B have rings of their own: 5 stages of A (the gathered token rows
+// arrive from L2 with a latency of several MMA stages, so they need the
+// depth) and 2 of B (dequantised on the chip, a short hop); the deep prefetch
+// from HBM is the code ring's (6 stages).
 // Every wait is bounded; a wait that runs out records a timeout, raises the
 // CTA's abort flag, drains what it issued and returns.
 #include <cuda_bf16.h>
@@ -38,7 +40,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kOp = 3;            // operand stages
+constexpr int kAS = 5;            // A stages (token rows, 16 KB)
+constexpr int kBS = 2;            // B stages (dequantised weights, 32 KB)
 constexpr int kCode = 6;          // code stages
 constexpr int kSb = 2;            // scale/bias chunks
 constexpr int kSbGroups = 8;      // K blocks per scale/bias chunk
@@ -48,7 +51,7 @@ constexpr int kABytes = kBM * 128;
 constexpr int kBBytes = kBN * 128;
 constexpr int kCBytes = kBN * 32;                 // codes of one K block
 constexpr int kSbBytes = 2 * kBN * kSbGroups * 2;  // scales [kBN][8], then biases
-static_assert(kOp * (kABytes + kBBytes) + kCode * kCBytes + kSb * kSbBytes + 1024 + kGemmCtrl ==
+static_assert(kAS * kABytes + kBS * kBBytes + kCode * kCBytes + kSb * kSbBytes + 1024 + kGemmCtrl ==
                   kQ4GemmSmem,
               "shared-memory plan");
 
@@ -108,8 +111,8 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = sA + kOp * kABytes;
-  uint8_t *sC = sB + kOp * kBBytes;
+  uint8_t *sB = sA + kAS * kABytes;
+  uint8_t *sC = sB + kBS * kBBytes;
   uint8_t *sSB = sC + kCode * kCBytes;
   uint8_t *ctrl = sSB + kSb * kSbBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);
@@ -123,9 +126,11 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
   // warps, code producer
   constexpr int kTileReaders = 1 + 4 + gather_warps<EPI>() + kDqWarps + 1;
 
-  const uint32_t full0 = smem_u32(bars);        // operand stage full
-  const uint32_t empty0 = full0 + 8 * kOp;      // operand stage free (MMA commit)
-  const uint32_t cfull0 = empty0 + 8 * kOp;     // code stage landed
+  const uint32_t full0 = smem_u32(bars);        // A stage full
+  const uint32_t empty0 = full0 + 8 * kAS;      // A stage free (MMA commit)
+  const uint32_t bfull0 = empty0 + 8 * kAS;     // B stage dequantised
+  const uint32_t bempty0 = bfull0 + 8 * kBS;    // B stage free (MMA commit)
+  const uint32_t cfull0 = bempty0 + 8 * kBS;    // code stage landed
   const uint32_t cempty0 = cfull0 + 8 * kCode;  // code stage read
   const uint32_t sbfull0 = cempty0 + 8 * kCode;
   const uint32_t sbempty0 = sbfull0 + 8 * kSb;
@@ -140,11 +145,15 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
   const int nkb = p.num_k_blocks;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kOp; ++s) {
-      // the A producer's arrival (with the A bytes when A comes by TMA), one
-      // per gather thread, one per dequantising warp
-      mbar_init(full0 + 8 * s, 1 + (kGather ? kGatherThreads : 0) + kDqWarps);
+    for (int s = 0; s < kAS; ++s) {
+      // the A producer's arrival (with the A bytes when A comes by TMA) and
+      // one per gather thread
+      mbar_init(full0 + 8 * s, 1 + (kGather ? kGatherThreads : 0));
       mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int s = 0; s < kBS; ++s) {
+      mbar_init(bfull0 + 8 * s, kDqWarps);
+      mbar_init(bempty0 + 8 * s, 1);
     }
     for (int s = 0; s < kCode; ++s) {
       mbar_init(cfull0 + 8 * s, 1);
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
           pend_mask |= 1u << stage;
           pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
         }
-        if (++stage == kOp) {
+        if (++stage == kAS) {
           stage = 0;
           phase ^= 1;
         }
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
     }
     if (!ok && lane == 0) {
       // copies already issued must land before the CTA's shared memory goes away
-      for (int s = 0; s < kOp; ++s)
+      for (int s = 0; s < kAS; ++s)
         if (pend_mask & (1u << s))
           if (!mbar_wait(full0 + 8 * s, (pend_phase >> s) & 1, limit, nullptr))
             report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_DRAIN);
@@ -337,8 +346,8 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_make(kBM, kBN, MmaKind<__nv_bfloat16>::ab_format);
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, bstage = 0;
+      uint32_t phase = 0, bphase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
@@ -360,7 +369,8 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag)) {
+          if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag) ||
+              !mbar_wait(bfull0 + 8 * bstage, bphase, limit, abort_flag)) {
             *abort_flag = 1;
             report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
             ok = false;
@@ -372,16 +382,21 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
           // core's reads (the dequantising warps fence their own stores)
           if (kGather) fence_proxy_async_smem();
           const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+          const uint32_t b0 = smem_u32(sB + bstage * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             MmaKind<__nv_bfloat16>::mma(d_tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk),
                                         idesc, (kb | kk) != 0 ? 1u : 0u);
           tc_commit(empty0 + 8 * stage);
+          tc_commit(bempty0 + 8 * bstage);
           issued = true;
-          if (++stage == kOp) {
+          if (++stage == kAS) {
             stage = 0;
             phase ^= 1;
+          }
+          if (++bstage == kBS) {
+            bstage = 0;
+            bphase ^= 1;
           }
         }
         if (!ok) break;
@@ -447,7 +462,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
           if (src[i] != nullptr) cp_async16(tile_dst + r * 128 + ((c ^ (r & 7)) << 4), src[i] + kb * 64);
         }
         cp_async_arrive(full0 + 8 * stage);
-        if (++stage == kOp) {
+        if (++stage == kAS) {
           stage = 0;
           phase ^= 1;
         }
@@ -484,7 +499,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
         bool w_ok = true;
         if (kb % kSbGroups == 0) w_ok = mbar_wait(sbfull0 + 8 * sb, sbph, limit, abort_flag);
         w_ok = w_ok && mbar_wait(cfull0 + 8 * cs, cph, limit, abort_flag);
-        w_ok = w_ok && mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
+        w_ok = w_ok && mbar_wait(bempty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           if (lane == 0) {
             *abort_flag = 1;
@@ -513,11 +528,11 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(full0 + 8 * stage);
+          mbar_arrive(bfull0 + 8 * stage);
           mbar_arrive(cempty0 + 8 * cs);
           if (kb % kSbGroups == kSbGroups - 1 || kb == nkb - 1) mbar_arrive(sbempty0 + 8 * sb);
         }
-        if (++stage == kOp) {
+        if (++stage == kBS) {
           stage = 0;
           phase ^= 1;
         }

@@ -91,8 +91,8 @@ struct Q4GemmMaps {
   CUtensorMap a;
   CUtensorMap c[4], s[4], b[4];
 };
-constexpr int kQ4GemmSmem = 3 * (kBM * 128 + kBN * 128) + 6 * (kBN * 32) + 2 * (2 * kBN * 8 * 2) +
-                            1024 + kGemmCtrl;
+constexpr int kQ4GemmSmem = 5 * (kBM * 128) + 2 * (kBN * 128) + 6 * (kBN * 32) +
+                            2 * (2 * kBN * 8 * 2) + 1024 + kGemmCtrl;
 template <int EPI>
 cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
 template <int EPI>
