@@ -10,16 +10,17 @@
 // once (section "Decode: minimise bytes moved per token"), and this format
 // reads 0.5625 bytes per weight instead of 2.
 //
-// The dequantisation is folded into the dot product: for one group of 64
-// columns,  sum_c (s q_c + b) x_c = s * sum_c q_c x_c + b * sum_c x_c,  and
-// sum_c x_c is computed once per token (per group) in shared memory.  Each
-// lane owns whole groups of a row (32 bytes of codes, one scale, one bias), so
-// it reads the token (or h) from shared memory rows padded to 65 floats per
-// group: lane g reads word g * 65 + e, bank (g + e) % 32, no conflicts.
+// The dequantisation is folded into the dot product: for the columns of one
+// group,  sum_c (s q_c + b) x_c = s * sum_c q_c x_c + b * sum_c x_c,  with the
+// codes turned into the floats 128 + q by byte permutes (no integer-to-float
+// conversion) and 128 * sum_c x_c taken back once per group.  The values x
+// (the token, or h for the down projection) sit in registers; the codes,
+// scales and biases come through shared memory.
 //
-// The three kernels mirror decode.cu (A router + shared gate/up, B routed
-// gate/up, C down + combine), chained with programmatic dependent launch:
-// static weights (the router rows, the shared expert's rows; C's rows once
+// Kernels (chained with programmatic dependent launch): A the router as one
+// thread-block cluster that publishes the layer's top-k once; B the gate/up
+// rows of the k chosen experts and of the shared one; C the down rows and the
+// combine.  Static weights (the shared expert's gate/up blocks, C's rows once
 // the choice is known) are requested before griddepcontrol.wait.
 #include <cuda_bf16.h>
 
