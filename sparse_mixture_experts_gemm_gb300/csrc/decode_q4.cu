@@ -239,22 +239,6 @@ __device__ __forceinline__ void gateup_issue(uint8_t *base, const Q4Mat &mg, con
 // choice.
 constexpr int kRouterWarps = 16;
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// st.shared::cluster of one float at a CTA-local shared address, in CTA `rank`
-__device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
-
 __global__ void __launch_bounds__(kRouterWarps * 32) decode_router_q4_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   __shared__ float s_lg[256];  // CTA 0: the layer's logits

@@ -81,6 +81,16 @@ template <typename T, int EPI, int BN>
 cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
+// route_small.cu: routing of batches of at most kSmallRouteT bf16 tokens
+// (T * d * 2 <= kSmallRouteTokBytes) in one cluster launch: writes idx, w,
+// inv (slots), perm, offsets and zeroes the n_clear words clear[32 q].
+constexpr int kSmallRouteT = 16;
+constexpr int kSmallRouteTokBytes = 65536;
+cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
+                               int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,
+                               int32_t *offsets, int32_t *clear, int n_clear, cudaStream_t st);
+cudaError_t route_small_set_attr();
+
 // gemm_q4.cu: the grouped GEMMs (EPI_SWIGLU, EPI_STORE; bf16 tokens) with
 // 4-bit group-affine weights, dequantised into the MMA's B tiles.  Maps:
 // a = the A operand by TMA (x for the shared expert's gate/up rows, H for the

@@ -256,7 +256,14 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
 
   // route_ctl is zero here: create cleared it and every router launch clears
   // what it used (counts, ticket, the GEMMs' tile counters) when it is done
-  {
+  const bool small = sizeof(T) == 2 && Tc <= kSmallRouteT &&
+                     static_cast<long long>(Tc) * d * 2 <= kSmallRouteTokBytes;
+  if (small) {
+    // a few tokens: routing and placement in one cluster launch
+    ProfScope ps(h, MOE_KERNEL_ROUTER, st);
+    MOE_TRY(launch_route_small(x, c.w_router, c.router_bias, Tc, d, E, k, h->idx, h->w, h->inv,
+                               h->perm, h->offsets, h->tile_ctr(0), 2, st));
+  } else {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
       const int rc = launch_router_tc(h, x, Tc, h->idx, h->w, h->inv, h->offsets, nullptr, st);
@@ -267,7 +274,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
       MOE_TRY(launch_offsets(h->counts(), E, h->offsets, h->tile_ctr(0), 2, st));
     }
   }
-  {
+  if (!small) {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
     MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st));
   }
@@ -570,7 +577,8 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   }
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
-      gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess)
+      (gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess ||
+       route_small_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
   if (rc != MOE_OK) {
     moe_destroy(h);

@@ -1,0 +1,159 @@
+// route_small.cu -- the whole routing step of a small batch (T <= 16 bf16
+// tokens) in one launch: logits, top-k, weights, histogram, group offsets and
+// the slot permutation.
+//
+// "Optimizing on-device inference for Apple Silicon", section "Match tile
+// size to expert load" (the verification batches of speculative decoding,
+// a handful of tokens, want their own path) and section "Keep expert routing
+// on the GPU".  At a few tokens the tensor-core router is all latency (a K
+// loop of 32 steps per tile, then candidate merges and a last-CTA scan across
+// the grid); here one thread-block cluster of ceil(E / 16) CTAs of 16 warps
+// does it: warp e holds expert e's router row in registers (requested before
+// the tokens arrive) and dots it with every token of the batch from shared
+// memory; each logit goes straight into CTA 0's shared memory; after one
+// cluster barrier CTA 0 takes each token's top-k (one warp per token), the
+// rank of every assignment inside its expert's group (the number of earlier
+// assignments, in (token, choice) order, to the same expert), the exclusive
+// scan of the group sizes, and writes idx, w, inv (each assignment's slot),
+// perm (each slot's token) and the offsets: the inputs of the grouped GEMMs
+// and of the combine, with no histogram atomics in memory and no separate
+// placement kernel.
+#include <cuda_bf16.h>
+
+#include "../../include/moe.h"
+#include "decode_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+constexpr int kRouteWarps = 16;
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wr,
+                       const float *__restrict__ bias, int T, int d, int E, int k, int32_t *idx,
+                       float *w, int32_t *inv, int32_t *perm, int32_t *offsets, int32_t *clear,
+                       int n_clear) {
+  extern __shared__ uint4 s_tok[];        // [T][d / 8] the batch's tokens
+  __shared__ float s_lg[kSmallRouteT][256];  // CTA 0: the logits
+  __shared__ int s_idx[kSmallRouteT][kMaxTopK];
+  __shared__ float s_w[kSmallRouteT][kMaxTopK];
+  __shared__ int s_rank[kSmallRouteT * kMaxTopK];
+  __shared__ int s_cnt[256];
+  __shared__ int s_off[257];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = d / 8;
+  const int e = blockIdx.x * kRouteWarps + warp;
+  const uint4 *row = reinterpret_cast<const uint4 *>(wr + static_cast<long long>(e) * d);
+  RowPre pr;
+  if (e < E) row_prefetch(pr, row, nvec, lane);
+  const uint4 *xg = reinterpret_cast<const uint4 *>(x);
+  for (int i = threadIdx.x; i < T * nvec; i += blockDim.x) s_tok[i] = __ldg(xg + i);
+  __syncthreads();
+  if (e < E) {
+    const float b = bias ? bias[e] : 0.0f;
+    for (int t = 0; t < T; ++t) {
+      const float acc = warp_sum(row_dot_pre<__nv_bfloat16>(pr, row, s_tok + t * nvec, nvec, lane));
+      if (lane == 0) st_cluster_f32(&s_lg[t][e], 0, acc + b);
+    }
+  }
+  cluster_sync_all();  // every CTA of the cluster reaches this: no return above
+  if (cluster_ctarank() != 0) return;
+
+  // CTA 0: one warp per token takes its top-k and the softmax over them
+  if (warp < T) {
+    unsigned key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int ee = lane + 32 * i;
+      key[i] = ee < E ? fkey(s_lg[warp][ee]) : 0u;
+    }
+    topk_from_keys(key, E, k, lane, s_idx[warp], s_w[warp]);
+  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  // rank of assignment a = t k + j among the earlier ones with the same expert
+  const int A = T * k;
+  const int a = threadIdx.x;
+  int ea = 0;
+  if (a < A) {
+    const int ta = a / k;
+    ea = s_idx[ta][a - ta * k];
+    // a token's k experts are distinct: only earlier tokens can share ea
+    int r = 0;
+    for (int tq = 0; tq < ta; ++tq)
+      for (int jq = 0; jq < k; ++jq) r += s_idx[tq][jq] == ea;
+    s_rank[a] = r;
+    atomicAdd(&s_cnt[ea], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the group sizes
+    const int per = (E + 31) / 32;
+    int sum = 0;
+    for (int q = 0; q < per; ++q) {
+      const int i = lane * per + q;
+      if (i < E) sum += s_cnt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int q = 0; q < per; ++q) {
+      const int i = lane * per + q;
+      if (i < E) {
+        s_off[i] = run;
+        run += s_cnt[i];
+      }
+    }
+    if (lane == 31) s_off[E] = incl;
+  }
+  __syncthreads();
+  if (a < A) {
+    const int slot = s_off[ea] + s_rank[a];
+    idx[a] = ea;
+    w[a] = s_w[a / k][a % k];
+    inv[a] = slot;
+    perm[slot] = a / k;
+  }
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) offsets[i] = s_off[i];
+  // the grouped GEMMs' tile counters start at zero
+  if (threadIdx.x == 0)
+    for (int q = 0; q < n_clear; ++q) clear[q * 32] = 0;
+}
+
+// one cluster: the whole grid (at most 16 CTAs for E <= 256)
+cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
+                               int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,
+                               int32_t *offsets, int32_t *clear, int n_clear, cudaStream_t st) {
+  const int ncta = (E + kRouteWarps - 1) / kRouteWarps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta);
+  cfg.blockDim = dim3(kRouteWarps * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(T) * d * 2;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_small_kernel, static_cast<const __nv_bfloat16 *>(x),
+                            static_cast<const __nv_bfloat16 *>(wr), bias, T, d, E, k, idx, w, inv,
+                            perm, offsets, clear, n_clear);
+}
+
+cudaError_t route_small_set_attr() {
+  cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmallRouteTokBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+}  // namespace moe

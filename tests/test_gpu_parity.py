@@ -229,3 +229,33 @@ def test_long_prompt_128k_in_8k_chunks(dev):
         ref, *_ = H.oracle_forward(x, w, k, rows=rows)
         err = H.row_rel_err(out[torch.as_tensor(rows, device=dev)], ref)
         assert err.max() <= H.OUT_TOL, f"chunk {ci}: max row rel err {err.max():.3e}"
+
+
+@pytest.mark.parametrize("T", [2, 5, 16])
+def test_small_batch_routing_path(dev, T):
+    """Batches of at most 16 bf16 tokens route through one cluster launch (no
+    placement kernel): the full-size layer against the oracle, every output."""
+    d, F, E, k = 2048, 512, 256, 8
+    w = synth.layer_weights(400 + T, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(410 + T, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=64)
+    try:
+        moe.moe_profile(layer.handle, True)
+        out = layer.forward(x)
+        moe.moe_profile(layer.handle, False)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+        kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
+        assert kinds == {"router", "gemm_gate_up", "gemm_down", "combine"}, kinds
+    finally:
+        layer.close()
+    ref, *_ = H.oracle_forward(x, w, k)
+    err = H.row_rel_err(out, ref)
+    assert err.max() <= H.OUT_TOL, err.max()
+
+
+def test_small_batch_with_router_bias(dev):
+    """The small-batch router adds the per-expert bias before the selection."""
+    E, k = 64, 8
+    bias = synth.zipf_bias(7, E, 1.2)
+    run_case(dev, 44, 9, 512, 128, E, k, bias=bias)
