@@ -5,10 +5,11 @@ Default workload (N=1): prefill of T=4096 tokens through one MoE layer
 fp32 accumulation), plus the batch-1 decode path over a stack of 40 distinct
 layers with a fresh token per step.  `value` is prefill tokens/s; the decode
 figures (microseconds per layer) are reported under "decode", and those of the
-same stack with 4-bit group-affine expert weights under "decode_q4".
+same stack with 4-bit group-affine expert weights under "decode_q4"; batches of
+2..16 tokens through one layer under "small_batch".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|tiny]
+                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|small_batch|tiny]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; a 256 MiB buffer is written between timed
@@ -273,6 +274,40 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
     }
 
 
+def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50) -> dict:
+    """Batches of 2..16 tokens through the same layer (the verification shape
+    of speculative decoding): one routing launch, the grouped GEMV on all SMs,
+    the combine; eager calls as a user makes them, L2 flushed before each."""
+    d, F, E, k = cfg["d"], cfg["F"], cfg["E"], cfg["k"]
+    st = torch.cuda.current_stream()
+    out = {}
+    for T in (2, 4, 8, 16):
+        x = synth.tokens(cfg["seed"] + 5000 + T, T, d, "bf16", dev)
+        for _ in range(5):
+            layer.forward(x)
+        _, _, cnt = layer.route(x)
+        active = int((cnt > 0).sum().item())
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        for a, b in evs:
+            flush_l2(flush_buf)
+            a.record(st)
+            layer.forward(x)
+            b.record(st)
+        torch.cuda.synchronize()
+        rc, det = layer.status()
+        if rc != 0:
+            raise RuntimeError(f"small-batch device status {rc} ({det})")
+        us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+        byts = (active + 1) * 3 * F * d * 2 + E * d * 2
+        out[str(T)] = {"us_per_layer_median": us, "experts_touched": active,
+                       "algorithmic_bytes": byts,
+                       "hbm_frac_of_measured": byts / (us * 1e-6) / (pk["hbm"] * 1e9)}
+    return {"workload": "T = 2, 4, 8, 16 tokens through one layer (d=2048, 256 experts top-8 + "
+                        "1 shared, F=512, bf16), eager calls, L2 flushed before each, median of "
+                        f"{iters}", "by_T": out, "gpu_launches_per_layer": 4}
+
+
 def bench_decode(dev, steps, warmup, n_layers=40, q4=False):
     cfg = WORKLOADS["prefill4k"]
     layers = []
@@ -390,7 +425,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill4k",
-                    choices=["prefill4k", "skew16k", "long128k", "tiny", "decode", "decode_q4"])
+                    choices=["prefill4k", "skew16k", "long128k", "tiny", "decode", "decode_q4",
+                             "small_batch"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-layers", type=int, default=40,
                     help="distinct layers in the decode stack (40 in the benchmark; fewer for profiling)")
@@ -413,7 +449,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    wl_name = "prefill4k" if args.workload.startswith("decode") else args.workload
+    wl_name = ("prefill4k" if args.workload.startswith("decode") or args.workload == "small_batch"
+               else args.workload)
     cfg = WORKLOADS[wl_name]
     pk = peaks()
 
@@ -437,6 +474,21 @@ def main():
         dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers,
                            q4=args.workload == "decode_q4")
         emit_decode_line(args, dec, pk, world)
+        return
+
+    if args.workload == "small_batch":
+        layer, _, _ = make_layer(cfg, dev, cfg["seed"])
+        try:
+            sb = bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=args.steps)
+        finally:
+            layer.close()
+        t16 = sb["by_T"]["16"]
+        print(json.dumps({
+            "metric": "small-batch layer time at T=16", "value": t16["us_per_layer_median"],
+            "unit": "us/layer", "n_gpus": world, "steps": args.steps, "warmup": 5,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)", "config": {"workload": sb["workload"]},
+            "small_batch": sb}))
         return
 
     res = bench_prefill(cfg, dev, args.steps, args.warmup, flush_buf)
@@ -518,6 +570,7 @@ def main():
         # decode launches are counted in their own objects
     if wl_name == "prefill4k":
         line["prefill_q4"] = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)
+        line["small_batch"] = bench_small_batch(res["layer"], cfg, dev, flush_buf, pk)
     if rank == 0 and not args.no_cpu:
         nthr = host_threads()
         n_tok = min(args.oracle_tokens, T)

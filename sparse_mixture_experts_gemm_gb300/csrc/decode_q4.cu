@@ -187,17 +187,6 @@ __device__ __forceinline__ void cp_async_range(uint8_t *dst, const void *src, in
   for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) cp_async16(d0 + 16 * i, s8 + 16 * i);
 }
 
-// 1D bulk copy (TMA) global -> shared completing on an mbarrier; 16-byte
-// aligned addresses, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Stages of a block (rows row0 .. row0 + n - 1 of mg and mu): stage j holds
 // rows j n / ns .. (j + 1) n / ns - 1.  The code bytes of a stage (16 KB per
 // matrix at d >= 2048) go by one bulk copy per matrix, issued by thread 0

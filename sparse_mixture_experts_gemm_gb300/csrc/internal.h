@@ -91,6 +91,27 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
                                int32_t *offsets, int32_t *clear, int n_clear, cudaStream_t st);
 cudaError_t route_small_set_attr();
 
+// gemv_small.cu: gate/up (h = silu(gate) * up as bf16 rows) and down (bf16
+// rows of Y) of a small batch as a grouped GEMV on warp-level MMAs; the units
+// (16 weight rows of one touched expert) are found on the device from the
+// routing step's offsets.  Tokens T <= kSmallRouteT, bf16.
+struct SmallArgs {
+  const __nv_bfloat16 *x;                 // [T][d]
+  const __nv_bfloat16 *wg, *wu, *wd;      // routed experts
+  const __nv_bfloat16 *sg, *su, *sd;      // shared expert (n_shared == 1)
+  const int32_t *offsets, *perm;          // routing step's output
+  __nv_bfloat16 *h;                       // [A + T][F]
+  __nv_bfloat16 *y;                       // [A + T][d]
+  int T, d, F, E, A, n_shared;
+  int *status;
+};
+// whether the kernels' shared memory plans fit (tokens and a ring of at
+// least two stages)
+bool small_gemv_fits(int T, int d, int F);
+cudaError_t launch_small_gateup(const SmallArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_small_down(const SmallArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t small_gemv_set_attr();
+
 // gemm_q4.cu: the grouped GEMMs (EPI_SWIGLU, EPI_STORE; bf16 tokens) with
 // 4-bit group-affine weights, dequantised into the MMA's B tiles.  Maps:
 // a = the A operand by TMA (x for the shared expert's gate/up rows, H for the

@@ -278,6 +278,41 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
     MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st));
   }
+  if (small && !h->q4 && small_gemv_fits(Tc, d, F)) {
+    // every touched expert gets one or two rows: grouped GEMV over all SMs
+    const bool pdl = !h->prof;  // event records between kernels would break the chain
+    SmallArgs sa;
+    sa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    sa.wg = static_cast<const __nv_bfloat16 *>(c.w_gate);
+    sa.wu = static_cast<const __nv_bfloat16 *>(c.w_up);
+    sa.wd = static_cast<const __nv_bfloat16 *>(c.w_down);
+    sa.sg = static_cast<const __nv_bfloat16 *>(c.s_gate);
+    sa.su = static_cast<const __nv_bfloat16 *>(c.s_up);
+    sa.sd = static_cast<const __nv_bfloat16 *>(c.s_down);
+    sa.offsets = h->offsets;
+    sa.perm = h->perm;
+    sa.h = static_cast<__nv_bfloat16 *>(h->hbuf);
+    sa.y = static_cast<__nv_bfloat16 *>(h->yp);
+    sa.T = Tc;
+    sa.d = d;
+    sa.F = F;
+    sa.E = E;
+    sa.A = A;
+    sa.n_shared = c.n_shared;
+    sa.status = h->status;
+    {
+      ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
+      MOE_TRY(launch_small_gateup(sa, h->num_sms, st, pdl));
+    }
+    {
+      ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
+      MOE_TRY(launch_small_down(sa, h->num_sms, st, pdl));
+    }
+    ProfScope ps(h, MOE_KERNEL_COMBINE, st);
+    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
+                              c.n_shared, h->status, st));
+    return MOE_OK;
+  }
   GemmParams base = {};
   base.offsets = h->offsets;
   base.T = Tc;
@@ -578,7 +613,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
       (gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess ||
-       route_small_set_attr() != cudaSuccess))
+       route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
   if (rc != MOE_OK) {
     moe_destroy(h);

@@ -99,6 +99,17 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
+// 1D bulk copy (TMA) global -> shared completing on an mbarrier; 16-byte
+// aligned addresses, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2D tiled load of box (x = inner/column coordinate, y = row) into shared
 // memory, completing `bar`'s transaction count.  x * element size must be a
 // multiple of 16 bytes; callers only pass multiples of the 128-byte K block.

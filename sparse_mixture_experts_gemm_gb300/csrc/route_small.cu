@@ -7,11 +7,12 @@
 // a handful of tokens, want their own path) and section "Keep expert routing
 // on the GPU".  At a few tokens the tensor-core router is all latency (a K
 // loop of 32 steps per tile, then candidate merges and a last-CTA scan across
-// the grid); here one thread-block cluster of ceil(E / 16) CTAs of 16 warps
-// does it: warp e holds expert e's router row in registers (requested before
-// the tokens arrive) and dots it with every token of the batch from shared
-// memory; each logit goes straight into CTA 0's shared memory; after one
-// cluster barrier CTA 0 takes each token's top-k (one warp per token), the
+// the grid); here one thread-block cluster of ceil(E / 16) CTAs does it: CTA
+// c multiplies the router rows of experts 16 c .. 16 c + 15 with the batch's
+// tokens (the small-batch main loop: its 16 warps split d, weights requested
+// before the tokens arrive, warp-level MMAs), and each logit goes straight
+// into CTA 0's shared memory; after one cluster barrier CTA 0 takes each
+// token's top-k (one warp per token), the
 // rank of every assignment inside its expert's group (the number of earlier
 // assignments, in (token, choice) order, to the same expert), the exclusive
 // scan of the group sizes, and writes idx, w, inv (each assignment's slot),
@@ -22,21 +23,65 @@
 
 #include "../../include/moe.h"
 #include "decode_common.cuh"
+#include "gemv_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
-constexpr int kRouteWarps = 16;
-}
+constexpr int kRouteWarps = kGvWarps;
 
-__global__ void __launch_bounds__(kRouteWarps * 32)
+// logits of experts 16 u .. 16 u + 15 for all tokens (one unit per CTA)
+struct RouterOp {
+  const __nv_bfloat16 *x, *wr;
+  const float *bias;
+  uint4 *s_tok;
+  float (*s_lg)[256];
+  int T, d, E, rs, nsteps, first, stride;
+  __device__ void prepare() {
+    first = blockIdx.x;
+    stride = gridDim.x;
+  }
+  __device__ bool early(int u) const { return 16 * u < E; }
+  __device__ void wait() {  // the tokens (no dependency): padded rows
+    const int vr = d / 8;
+    const uint4 *xg = reinterpret_cast<const uint4 *>(x);
+    for (int i = threadIdx.x; i < T * vr; i += blockDim.x) {
+      const int t = i / vr;
+      s_tok[t * rs + (i - t * vr)] = __ldg(xg + i);
+    }
+    __syncthreads();
+  }
+  __device__ int count() const { return early(first) ? 1 : 0; }
+  __device__ void rows(int u, int, const uint4 *&pa, const uint4 *&pb) const {
+    const int g = (threadIdx.x & 31) >> 2, q = threadIdx.x & 3;
+    pa = reinterpret_cast<const uint4 *>(wr + static_cast<long long>(min(16 * u + g, E - 1)) * d) + q;
+    pb = reinterpret_cast<const uint4 *>(wr + static_cast<long long>(min(16 * u + g + 8, E - 1)) * d) + q;
+  }
+  __device__ int ncols(int) const { return T; }
+  __device__ const uint4 *col(int, int nb) const {
+    return s_tok + min(8 * nb + ((threadIdx.x & 31) >> 2), T - 1) * rs + (threadIdx.x & 3);
+  }
+  __device__ void epilogue(int u, const float *red) const {
+    const int t = threadIdx.x;
+    if (t >= 256) return;
+    const int r = t & 15, m = t >> 4, e = 16 * u + r;
+    if (m >= T || e >= E) return;
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kGvWarps; ++w) v += red[w * 256 + gv_part(r, m)];
+    st_cluster_f32(&s_lg[m][e], 0, v + (bias ? bias[e] : 0.0f));
+  }
+};
+}  // namespace
+
+__global__ void __launch_bounds__(kRouteWarps * 32, 1)
     route_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wr,
                        const float *__restrict__ bias, int T, int d, int E, int k, int32_t *idx,
                        float *w, int32_t *inv, int32_t *perm, int32_t *offsets, int32_t *clear,
                        int n_clear) {
-  extern __shared__ uint4 s_tok[];        // [T][d / 8] the batch's tokens
+  extern __shared__ uint4 s_dyn[];  // partial tiles, then [T][d / 8 + 4] tokens
   __shared__ float s_lg[kSmallRouteT][256];  // CTA 0: the logits
   __shared__ int s_idx[kSmallRouteT][kMaxTopK];
   __shared__ float s_w[kSmallRouteT][kMaxTopK];
@@ -44,21 +89,21 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   __shared__ int s_cnt[256];
   __shared__ int s_off[257];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = d / 8;
-  const int e = blockIdx.x * kRouteWarps + warp;
-  const uint4 *row = reinterpret_cast<const uint4 *>(wr + static_cast<long long>(e) * d);
-  RowPre pr;
-  if (e < E) row_prefetch(pr, row, nvec, lane);
-  const uint4 *xg = reinterpret_cast<const uint4 *>(x);
-  for (int i = threadIdx.x; i < T * nvec; i += blockDim.x) s_tok[i] = __ldg(xg + i);
-  __syncthreads();
-  if (e < E) {
-    const float b = bias ? bias[e] : 0.0f;
-    for (int t = 0; t < T; ++t) {
-      const float acc = warp_sum(row_dot_pre<__nv_bfloat16>(pr, row, s_tok + t * nvec, nvec, lane));
-      if (lane == 0) st_cluster_f32(&s_lg[t][e], 0, acc + b);
-    }
-  }
+  // the next launch (the expert gate/up) may start its routing-independent
+  // reads now: it waits for this grid before it reads any of its outputs
+  pdl_launch_dependents();
+  RouterOp op;
+  op.x = x;
+  op.wr = wr;
+  op.bias = bias;
+  op.s_tok = s_dyn + kGvRedBytes / 16;
+  op.s_lg = s_lg;
+  op.T = T;
+  op.d = d;
+  op.E = E;
+  op.rs = d / 8 + 4;
+  op.nsteps = d / 32;
+  gv_run<1>(op, reinterpret_cast<float *>(s_dyn));
   cluster_sync_all();  // every CTA of the cluster reaches this: no return above
   if (cluster_ctarank() != 0) return;
 
@@ -134,7 +179,7 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncta);
   cfg.blockDim = dim3(kRouteWarps * 32);
-  cfg.dynamicSmemBytes = static_cast<size_t>(T) * d * 2;
+  cfg.dynamicSmemBytes = kGvRedBytes + static_cast<size_t>(T) * (d / 8 + 4) * 16;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -150,7 +195,7 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
 
 cudaError_t route_small_set_attr() {
   cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmallRouteTokBytes);
+                                       kGvRedBytes + kSmallRouteTokBytes + kSmallRouteT * 64);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;

@@ -259,3 +259,10 @@ def test_small_batch_with_router_bias(dev):
     E, k = 64, 8
     bias = synth.zipf_bias(7, E, 1.2)
     run_case(dev, 44, 9, 512, 128, E, k, bias=bias)
+
+
+@pytest.mark.parametrize("T,E,k,n_shared", [(16, 4, 2, 1), (13, 8, 3, 0), (9, 2, 1, 1), (3, 8, 2, 0)])
+def test_small_batch_crowded_experts(dev, T, E, k, n_shared):
+    """Small batches whose routed experts get more than 8 tokens (the second
+    column block of the grouped GEMV), with and without the shared expert."""
+    run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=16)
