@@ -241,3 +241,6 @@ def dequantize_q4(codes, scales, biases) -> np.ndarray:
     s = np.repeat(_bf16_value(scales).astype(np.float64), 64, axis=1)
     b = np.repeat(_bf16_value(biases).astype(np.float64), 64, axis=1)
     return q * s + b
+
+
+from .gdn import gdn_scan  # noqa: E402  (the Gated DeltaNet scan, float64)

@@ -385,3 +385,114 @@ ALL_PINS = [pin_route_vs_numpy, pin_full_softmax_when_k_equals_E, pin_weights_su
             pin_dense_plus_shared, pin_all_experts_masked, pin_permutation_equivariance,
             pin_hand_cases, pin_q4_nibble_order, pin_q4_groups_scale_bias,
             pin_q4_zero_codes_are_bias, pin_q4_matches_dense]
+
+
+# ---------------------------------------------------------------- Gated DeltaNet scan
+def _gdn_case(seed, T, Hk, Hv, dk, dv, unit_keys=True, state=True):
+    """Random float32 inputs of the scan (exact float64 values on both sides)."""
+    r = np.random.default_rng(seed)
+    k = r.standard_normal((T, Hk, dk)).astype(np.float32)
+    if unit_keys:
+        k /= np.linalg.norm(k, axis=2, keepdims=True)
+    q = (r.standard_normal((T, Hk, dk)) / np.sqrt(dk)).astype(np.float32)
+    v = r.standard_normal((T, Hv, dv)).astype(np.float32)
+    alpha = r.uniform(0.6, 1.0, (T, Hv)).astype(np.float32)
+    beta = r.uniform(0.05, 1.0, (T, Hv)).astype(np.float32)
+    s0 = r.standard_normal((Hv, dv, dk)).astype(np.float32) if state else None
+    return q, k, v, alpha, beta, s0
+
+
+def pin_gdn_hand_case(mutation=0):
+    """Two tokens worked by hand (tests/golden/gdn_hand.json)."""
+    with open(os.path.join(GOLDEN, "gdn_hand.json")) as f:
+        c = json.load(f)
+    a = {kk: np.asarray(c[kk], np.float32) for kk in ("q", "k", "v", "alpha", "beta", "state_in")}
+    o, s = oracle.gdn_scan(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["state_in"],
+                           mutation=mutation)
+    assert np.array_equal(o, np.asarray(c["o"])), o
+    assert np.array_equal(s, np.asarray(c["state_out"])), s
+
+
+def pin_gdn_delta_invariant(mutation=0):
+    """The delta rule's defining property: after a token, the state recalls
+    alpha r + beta (v - alpha r) |k|^2 at that token's key k, r being the recall
+    before the token (for a unit key: (1 - beta) alpha r + beta v, the value
+    written in); checked step by step through a scan (the state of each prefix
+    continues into the next token)."""
+    q, k, v, alpha, beta, s0 = _gdn_case(11, 6, 2, 4, 8, 8)
+    s = s0.astype(np.float64)
+    for t in range(6):
+        heads = np.arange(4) // 2
+        kt = k[t][heads].astype(np.float64)
+        before = np.einsum("hji,hi->hj", s, kt)
+        _, s = oracle.gdn_scan(q[t:t + 1], k[t:t + 1], v[t:t + 1], alpha[t:t + 1],
+                               beta[t:t + 1], s, mutation=mutation)
+        after = np.einsum("hji,hi->hj", s, kt)
+        a, b = alpha[t][:, None].astype(np.float64), beta[t][:, None].astype(np.float64)
+        kk = np.sum(kt * kt, axis=1)[:, None]
+        want = a * before + b * (v[t].astype(np.float64) - a * before) * kk
+        assert np.allclose(after, want, rtol=1e-12, atol=1e-12)
+
+
+def pin_gdn_pure_decay(mutation=0):
+    """beta = 0 leaves only the gate: S_T = (prod alpha) S_0 and
+    o_t = (prod_{s<=t} alpha_s) S_0 q_t (closed form)."""
+    q, k, v, alpha, beta, s0 = _gdn_case(12, 5, 1, 2, 4, 4)
+    beta[:] = 0
+    o, s = oracle.gdn_scan(q, k, v, alpha, beta, s0, mutation=mutation)
+    g = np.cumprod(alpha.astype(np.float64), axis=0)  # [T][Hv]
+    s64 = s0.astype(np.float64)
+    want_o = g[:, :, None] * np.einsum("hji,ti->thj", s64, q[:, 0].astype(np.float64))
+    assert np.allclose(o, want_o, rtol=1e-12, atol=1e-12)
+    assert np.allclose(s, g[-1][:, None, None] * s64, rtol=1e-12, atol=1e-12)
+
+
+def _gdn_parallel_form(q, k, v, alpha, beta, s0):
+    """The same outputs from the scan's closed form, one value head at a time:
+    S_t = G_t S_0 + sum_{i<=t} g_{t,i} u_i k_i^T with G_t = prod_{s<=t} alpha_s,
+    g_{t,i} = prod_{i<s<=t} alpha_s, and the deltas u the solution of the unit
+    lower-triangular system u_t + beta_t sum_{i<t} g_{t,i} (k_t . k_i) u_i =
+    beta_t (v_t - G_t S_0 k_t) (scipy's triangular solve); o_t = S_t q_t."""
+    import scipy.linalg
+    T, Hk, dk = k.shape
+    _, Hv, dv = v.shape
+    o = np.zeros((T, Hv, dv))
+    s_out = np.zeros((Hv, dv, dk))
+    for h in range(Hv):
+        kk = k[:, h // (Hv // Hk)].astype(np.float64)
+        qq = q[:, h // (Hv // Hk)].astype(np.float64)
+        la = np.cumsum(np.log(alpha[:, h].astype(np.float64)))
+        G = np.exp(la)
+        g = np.tril(np.exp(la[:, None] - la[None, :]))  # g[t, i], i <= t
+        b = beta[:, h].astype(np.float64)
+        S0 = s0[h].astype(np.float64)  # [dv][dk]
+        L = b[:, None] * np.tril(g * (kk @ kk.T), -1)
+        rhs = b[:, None] * (v[:, h].astype(np.float64) - G[:, None] * (kk @ S0.T))
+        U = scipy.linalg.solve_triangular(np.eye(T) + L, rhs, lower=True, unit_diagonal=True)
+        o[:, h] = G[:, None] * (qq @ S0.T) + (g * (qq @ kk.T)) @ U
+        s_out[h] = G[-1] * S0 + (U * g[-1][:, None]).T @ kk
+    return o, s_out
+
+
+def pin_gdn_parallel_form(mutation=0):
+    """Sequential scan == closed form through a triangular solve (another
+    algorithm for the same recurrence), with grouped key heads."""
+    for seed, (T, Hk, Hv, dk, dv) in ((13, (9, 2, 4, 8, 8)), (14, (7, 1, 3, 4, 6))):
+        q, k, v, alpha, beta, s0 = _gdn_case(seed, T, Hk, Hv, dk, dv, unit_keys=seed == 13)
+        o, s = oracle.gdn_scan(q, k, v, alpha, beta, s0, mutation=mutation)
+        wo, ws = _gdn_parallel_form(q, k, v, alpha, beta, s0)
+        assert np.allclose(o, wo, rtol=1e-9, atol=1e-9)
+        assert np.allclose(s, ws, rtol=1e-9, atol=1e-9)
+
+
+def pin_gdn_zero_state_default(mutation=0):
+    """No initial state means a zero state: the first output is
+    beta_1 (k_1 . q_1) v_1."""
+    q, k, v, alpha, beta, _ = _gdn_case(15, 1, 1, 2, 4, 4, state=False)
+    o, _ = oracle.gdn_scan(q, k, v, alpha, beta, None, mutation=mutation)
+    want = beta[0][:, None] * float(k[0, 0] @ q[0, 0]) * v[0]
+    assert np.allclose(o[0], want, rtol=1e-6, atol=1e-7)
+
+
+GDN_PINS = [pin_gdn_hand_case, pin_gdn_delta_invariant, pin_gdn_pure_decay, pin_gdn_parallel_form,
+            pin_gdn_zero_state_default]

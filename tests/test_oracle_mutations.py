@@ -46,3 +46,24 @@ def test_quantiser_mutation_is_caught(m):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"quantiser mutation {m} ({QUANT_MUTATIONS[m]}) passed every pin"
+
+
+GDN_MUTATIONS = {
+    1: "alpha dropped from the recall in the delta",
+    2: "state not decayed",
+    3: "output read before the write",
+    4: "value head h mapped to key head h % H_k",
+    5: "recall with the state transposed",
+    6: "beta scales only the new value",
+}
+
+
+@pytest.mark.parametrize("m", sorted(GDN_MUTATIONS), ids=lambda m: f"g{m}")
+def test_gdn_mutation_is_caught(m):
+    failed = []
+    for pin in pins.GDN_PINS:
+        try:
+            pin(m)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"scan mutation {m} ({GDN_MUTATIONS[m]}) passed every pin"
