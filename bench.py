@@ -6,10 +6,11 @@ fp32 accumulation), plus the batch-1 decode path over a stack of 40 distinct
 layers with a fresh token per step.  `value` is prefill tokens/s; the decode
 figures (microseconds per layer) are reported under "decode", and those of the
 same stack with 4-bit group-affine expert weights under "decode_q4"; batches of
-2..16 tokens through one layer under "small_batch".
+2..16 tokens through one layer under "small_batch"; the Gated DeltaNet scan of
+one layer over a 2K-token prompt under "gdn".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|small_batch|tiny]
+                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|small_batch|gdn2k|tiny]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; a 256 MiB buffer is written between timed
@@ -308,6 +309,65 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50) -> dict:
                         f"{iters}", "by_T": out, "gpu_launches_per_layer": 4}
 
 
+GDN = {"T": 2048, "Hk": 16, "Hv": 32, "dk": 128, "dv": 128, "seed": 31}
+
+
+def bench_gdn(dev, flush_buf, pk, iters=20, cpu_tokens=64) -> dict:
+    """Gated DeltaNet scan of one layer over a 2,048-token prompt (16 key heads,
+    32 value heads, d_k = d_v = 128, fp32 state in registers), L2 flushed
+    before each call; the oracle timed beside it on a bounded sample."""
+    c = GDN
+    inp = synth.gdn_inputs(c["seed"], c["T"], c["Hk"], c["Hv"], c["dk"], c["dv"], dev, state=True)
+    st = torch.cuda.current_stream()
+    o = torch.empty((c["T"], c["Hv"], c["dv"]), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty_like(inp["state"])
+    args = (inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], inp["state"])
+    for _ in range(3):
+        moe.gdn_scan(*args, out=o, state_out=s_out)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    with Clocks(dev.index or 0) as clk:
+        for a, b in evs:
+            flush_l2(flush_buf)
+            a.record(st)
+            moe.gdn_scan(*args, out=o, state_out=s_out)
+            b.record(st)
+        torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+    cols = c["Hv"] * c["dv"]
+    fma = c["T"] * cols * 3 * c["dk"]  # recall, read-out and update per state entry and token
+    byts = (2 * c["T"] * c["Hk"] * c["dk"] * 2 + 2 * c["T"] * cols * 2 + 2 * c["T"] * c["Hv"] * 4
+            + 2 * cols * c["dk"] * 4)
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12  # fp32 lanes x 2 flops x maximum SM clock
+    res = {
+        "workload": f"Gated DeltaNet scan, one layer: T={c['T']} tokens, {c['Hk']} key heads, "
+                    f"{c['Hv']} value heads, d_k=d_v={c['dk']}, bf16 q/k/v, fp32 gate, "
+                    "strength and state, L2 flushed before each call",
+        "us_per_layer_median": us, "tokens_per_s": c["T"] / (us * 1e-6),
+        "us_per_token": us / c["T"],
+        "roofline": {"bound": "alu", "achieved": 2 * fma / (us * 1e-6) / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": 2 * fma / (us * 1e-6) / 1e12 / peak,
+                     "traffic": None, "algorithmic_bytes": byts,
+                     "hbm_frac_of_measured": byts / (us * 1e-6) / (pk["hbm"] * 1e9),
+                     "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (nominal)"},
+        "clocks": clk.summary(), "gpu_launches": iters,
+    }
+    if cpu_tokens:
+        import oracle
+        cpu = {k: (None if v is None else v[:cpu_tokens].cpu()) for k, v in inp.items()
+               if k != "state"}
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        t0 = time.perf_counter()
+        oracle.gdn_scan(bits(cpu["q"]), bits(cpu["k"]), bits(cpu["v"]), cpu["alpha"].numpy(),
+                        cpu["beta"].numpy(), inp["state"].cpu().numpy())
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": cpu_tokens / dt, "unit": "tokens/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"first {cpu_tokens} of the {c['T']} tokens, all heads, "
+                                         f"{dt:.2f} s, numpy float64"}
+    return res
+
+
 def bench_decode(dev, steps, warmup, n_layers=40, q4=False):
     cfg = WORKLOADS["prefill4k"]
     layers = []
@@ -426,7 +486,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill4k",
                     choices=["prefill4k", "skew16k", "long128k", "tiny", "decode", "decode_q4",
-                             "small_batch"])
+                             "small_batch", "gdn2k"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-layers", type=int, default=40,
                     help="distinct layers in the decode stack (40 in the benchmark; fewer for profiling)")
@@ -449,8 +509,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    wl_name = ("prefill4k" if args.workload.startswith("decode") or args.workload == "small_batch"
-               else args.workload)
+    wl_name = ("prefill4k" if args.workload.startswith("decode")
+               or args.workload in ("small_batch", "gdn2k") else args.workload)
     cfg = WORKLOADS[wl_name]
     pk = peaks()
 
@@ -474,6 +534,17 @@ def main():
         dec = bench_decode(dev, args.decode_steps, max(args.warmup, 50), args.decode_layers,
                            q4=args.workload == "decode_q4")
         emit_decode_line(args, dec, pk, world)
+        return
+
+    if args.workload == "gdn2k":
+        g = bench_gdn(dev, flush_buf, pk, iters=args.steps, cpu_tokens=0 if args.no_cpu else 64)
+        print(json.dumps({
+            "metric": "Gated DeltaNet scan time per layer, 2K-token prompt",
+            "value": g["us_per_layer_median"], "unit": "us/layer", "n_gpus": world,
+            "steps": args.steps, "warmup": 3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": g["workload"]}, "roofline": g["roofline"],
+            "clocks": g["clocks"], "gpu_launches": g["gpu_launches"], "gdn": g}))
         return
 
     if args.workload == "small_batch":
@@ -571,6 +642,7 @@ def main():
     if wl_name == "prefill4k":
         line["prefill_q4"] = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)
         line["small_batch"] = bench_small_batch(res["layer"], cfg, dev, flush_buf, pk)
+        line["gdn"] = bench_gdn(dev, flush_buf, pk, cpu_tokens=64 if rank == 0 else 0)
     if rank == 0 and not args.no_cpu:
         nthr = host_threads()
         n_tok = min(args.oracle_tokens, T)

@@ -37,7 +37,7 @@ KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "de
 
 EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_status", "moe_destroy",
             "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
-            "moe_decode_noalloc", "moe_create_q4", "moe_quantize_q4"]
+            "moe_decode_noalloc", "moe_create_q4", "moe_quantize_q4", "gdn_scan"]
 
 Q4_GROUP = 64  # columns per (scale, bias) pair of the 4-bit format
 
@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
     L.moe_create_q4.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_q4_weights),
                                 ctypes.POINTER(vp)]
     L.moe_quantize_q4.argtypes = [vp, ip, ctypes.c_longlong, ip, vp, vp, vp, vp]
+    L.gdn_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp]
     for name in EXPORTED:
         if name != "moe_strerror":
             getattr(L, name).restype = ip
@@ -313,3 +314,36 @@ class Q4Layer(MoELayer):
                          None, None, None, None, None, _ptr(bias))
         self.cfg, self.qw = cfg, qw
         self.handle = moe_create_q4(cfg, qw)
+
+
+def gdn_scan(q, k, v, alpha, beta, state=None, out=None, state_out=None, stream=None):
+    """Gated DeltaNet recurrent scan (include/gdn.h) over device tensors.
+
+    q, k: bf16 [T][H_k][d_k]; v: bf16 [T][H_v][d_v]; alpha, beta: float32
+    [T][H_v]; state: float32 [H_v][d_v][d_k] or None (zeros).  Returns
+    (o bf16 [T][H_v][d_v], final state float32 [H_v][d_v][d_k]); `out` and
+    `state_out` may be given (state_out may be `state`).  Asynchronous on
+    `stream` (default: torch's current stream).
+    """
+    import torch
+    T, Hk, dk = k.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("alpha", alpha, torch.float32),
+                        ("beta", beta, torch.float32)):
+        if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if q.shape != k.shape or v.shape[0] != T or alpha.shape != (T, Hv) or beta.shape != (T, Hv):
+        raise ValueError("shapes of q, k, v, alpha, beta do not agree")
+    if state is not None and (state.dtype != torch.float32 or tuple(state.shape) != (Hv, dv, dk)
+                              or not state.is_contiguous()):
+        raise ValueError("state must be a contiguous float32 [H_v][d_v][d_k] tensor")
+    if out is None:
+        out = torch.empty((T, Hv, dv), dtype=torch.bfloat16, device=v.device)
+    if state_out is None:
+        state_out = torch.empty((Hv, dv, dk), dtype=torch.float32, device=v.device)
+    _check(lib().gdn_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(state),
+                          _ptr(state_out), _ptr(out), T, Hk, Hv, dk, dv, _stream(stream)),
+           "gdn_scan")
+    return out, state_out
+

@@ -1,8 +1,8 @@
-// gemv_common.cuh -- the main loop shared by the small-batch kernels (router
-// logits, expert gate/up, expert down): a weight matrix times at most 16
-// columns on warp-level m16n8k16 MMAs, weights streamed from HBM once.
+// gemv_common.cuh -- warp-level m16n8k16 MMA steps of a weight matrix times
+// at most 16 columns (used by the small-batch kernels), and the block-wide
+// main loop of the small-batch router's logits.
 //
-// Unit of work: one CTA takes a block of kR x 16 weight rows (a "unit") and
+// Main loop.  Unit of work: one CTA takes a block of kR x 16 weight rows (a "unit") and
 // its 16 warps split it: warp w owns row block w / S (S = 16 / kR) and the
 // reduction steps j = w % S + S i (a step is 32 columns).  Lane (g, q) of a
 // warp (g = lane / 4, q = lane % 4) reads, per step, the 16 bytes at column

@@ -8,6 +8,7 @@ device the tensor is made on, seeded once per call, in a fixed order:
     Wr, Sg, Su, Sd, Wg, Wu, Wd        (layer_weights, q4_layer_weights; a 4-bit
                                        matrix draws codes, scales, biases)
     x                                 (tokens)
+    q, k, v, alpha, beta, state       (gdn_inputs, the Gated DeltaNet scan)
 
 Distributions follow the workloads the block is measured on: activations
 x ~ N(0, 1); every projection ~ N(0, 1/fan_in), fan_in = d for the router and
@@ -128,3 +129,30 @@ def zipf_bias(seed: int, E: int, s: float = 1.2) -> torch.Tensor:
     b = torch.empty(E, dtype=torch.float64)
     b[perm] = -s * torch.log(ranks)
     return b.to(torch.float32)
+
+
+def gdn_inputs(seed: int, T: int, Hk: int, Hv: int, dk: int, dv: int, device="cpu",
+               state: bool = False) -> dict:
+    """Inputs of a Gated DeltaNet scan, drawn in the order q, k, v, alpha, beta,
+    state: q and k per head ~ N(0, 1) rescaled to unit length (the model
+    normalises them before the scan), q further by 1/sqrt(d_k) (its query
+    scale), stored bf16; v ~ N(0, 1) bf16; the gate alpha = exp(-softplus(z)),
+    z ~ N(-2.5, 1) (mostly 0.8..1, a long tail toward forgetting) and the write
+    strength beta = sigmoid(N(0, 1)), both float32 [T][H_v]; the initial state
+    (if asked for) ~ N(0, 0.1^2) float32 [H_v][d_v][d_k], else None."""
+    g = _gen(seed, device)
+    f32 = torch.float32
+
+    def unit(shape):
+        t = torch.randn(shape, generator=g, device=device, dtype=f32)
+        return t / t.norm(dim=-1, keepdim=True)
+
+    q = (unit((T, Hk, dk)) / math.sqrt(dk)).to(torch.bfloat16)
+    k = unit((T, Hk, dk)).to(torch.bfloat16)
+    v = torch.randn((T, Hv, dv), generator=g, device=device, dtype=f32).to(torch.bfloat16)
+    z = torch.randn((T, Hv), generator=g, device=device, dtype=f32) - 2.5
+    alpha = torch.exp(-torch.nn.functional.softplus(z))
+    beta = torch.sigmoid(torch.randn((T, Hv), generator=g, device=device, dtype=f32))
+    s0 = (torch.randn((Hv, dv, dk), generator=g, device=device, dtype=f32) * 0.1) if state else None
+    return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta, "state": s0}
+

@@ -1,4 +1,4 @@
-"""The C ABI library builds, loads and exports every function include/moe.h
+"""The C ABI library builds, loads and exports every function include/*.h
 declares; host-side argument validation answers without touching a GPU."""
 import ctypes
 import os
@@ -10,13 +10,21 @@ import sparse_mixture_experts_gemm_gb300 as moe
 from sparse_mixture_experts_gemm_gb300 import buildlib as moe_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("moe.h", "gdn.h")]
 
 
 def header_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+    names = set()
+    for path in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:moe|gdn)_\w+)\s*\(", src,
+                                flags=re.M))
+    return sorted(names)
+
+
+def test_headers_are_all_listed():
+    found = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert found == sorted(os.path.basename(h) for h in HEADERS)
 
 
 @pytest.fixture(scope="module")
@@ -28,13 +36,13 @@ def lib():
 def test_header_declares_the_boundary():
     fns = header_functions()
     for name in ["moe_create", "moe_route", "moe_forward", "moe_destroy", "moe_status",
-                 "moe_strerror"]:
+                 "moe_strerror", "gdn_scan"]:
         assert name in fns
 
 
 def test_every_declared_symbol_is_exported(lib):
     for name in header_functions():
-        assert hasattr(lib, name), f"{name} declared in moe.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
         assert name in moe.EXPORTED
 
 
@@ -143,3 +151,23 @@ def test_create_q4_null_weights(lib):
 ])
 def test_quantize_q4_validates_on_host(lib, args, code):
     assert lib.moe_quantize_q4(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(Hk=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(Hk=3), moe.MOE_ERR_INVALID_ARG),          # 32 value heads over 3 key heads
+    (dict(q=None), moe.MOE_ERR_INVALID_ARG),
+    (dict(alpha=None), moe.MOE_ERR_INVALID_ARG),
+    (dict(dk=64), moe.MOE_ERR_UNSUPPORTED),
+    (dict(dv=24), moe.MOE_ERR_UNSUPPORTED),
+])
+def test_gdn_scan_rejects_before_any_launch(lib, args, code):
+    """Validation happens on the host, before anything touches a GPU."""
+    a = dict(q=0x1000, k=0x2000, v=0x3000, alpha=0x4000, beta=0x5000, s_in=None, s_out=None,
+             o=0x6000, T=16, Hk=16, Hv=32, dk=128, dv=128)
+    a.update(args)
+    rc = lib.gdn_scan(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["s_in"], a["s_out"],
+                      a["o"], a["T"], a["Hk"], a["Hv"], a["dk"], a["dv"], None)
+    assert rc == code
+
