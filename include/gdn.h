@@ -17,9 +17,10 @@
  *
  * Columns are independent, so one call scans any number of heads; a long
  * sequence may be scanned in pieces, passing state_out of one piece as
- * state_in of the next: the state passes in the float32 it is kept in and
- * each token's arithmetic does not depend on where a piece starts, so the
- * result is bit-identical to one scan.
+ * state_in of the next.  Pieces cut at multiples of 8 tokens give results
+ * bit-identical to one scan (the kernel takes tokens 8 at a time and passes
+ * the state in the float32 it keeps it in); other cuts agree up to float
+ * rounding.
  * The caller applies the model's preprocessing (normalising q and k, the
  * query scale, the gate and write-strength activations) before the call.
  */
