@@ -3,41 +3,47 @@
 // "Optimizing on-device inference for Apple Silicon", section "Keep the
 // recurrent state on chip": the state matrix is split by columns, each
 // column's slice loaded into registers once, carried through the whole scan
-// and written back only at its end; partial results are exchanged by lane
-// operations, not through shared memory; state and gate are 32-bit float,
-// the activations bfloat16.
-//
-// Column split.  The pages give each column a whole SIMD group; here a
-// column belongs to L = 8 lanes (16 fp32 entries per lane at d_k = 128, four
-// columns per warp), which keeps the whole state (2 MB for 32 value heads of
-// 128 x 128) in registers on ~7 warps per SM with 3 shuffle rounds per
-// reduction.  Lane s of a column holds the entries 4 s + 32 i + 0..3 (i =
-// 0..3), so the 8 lanes of a column read 128 contiguous bytes of a key per
-// instruction (no shared-memory bank conflicts).
+// and written back only at its end; state and gate are 32-bit float, the
+// activations bfloat16.
 //
 // Token order.  Scanning token by token makes every token wait for a dot
 // product, a cross-lane reduction and the update of the one before (measured
-// ~550 cycles per token on one warp).  The scan therefore takes 8 tokens at a
-// time in the equivalent block form of the same recurrence (S the state
-// before the 8 tokens, A_i the product of the gates alpha_0..alpha_{i-1}
-// inside the block, g(i, l) the product of alpha_{l+1}..alpha_{i-1}):
-//     P_i = k_i . S,  Q_i = q_i . S                  (16 independent reductions)
+// ~550 cycles per token on one warp).  The scan takes 8 tokens at a time in
+// the equivalent block form of the same recurrence (S the state before the 8
+// tokens, A_i the product of the gates alpha_0..alpha_{i-1} inside the block,
+// g(i, l) the product of alpha_{l+1}..alpha_{i-1}):
+//     P_i = k_i . S,  Q_i = q_i . S
 //     r_i = A_i P_i + sum_{l<i} g(i, l) (k_i . k_l) u_l    (what S recalls at k_i)
 //     u_i = beta_i (v_i - alpha_i r_i)
 //     o_i = A_{i+1} Q_i + sum_{l<=i} g(i+1, l) (q_i . k_l) u_l
 //     S  <- A_8 S + sum_l g(8, l) u_l k_l
 // which is the token-by-token rule S <- alpha S + u k, o = S . q written out
-// (no division, no rescaling: a zero gate makes the products zero).  Only
-// the u_i form a chain (two dependent FMAs per token); the dot products, the
-// reductions and the update are independent work.  The coefficient tables
-// come once per CTA from the block's Gram products q_i . k_l and k_i . k_l,
-// computed on warp-level bf16 MMAs (products of bf16 values are exact in
-// fp32; fp32 accumulation).
+// (no division or rescaling: a zero gate makes the products zero).
 //
-// Staging.  A CTA (4 warps, the 16 columns of one value head) copies the bf16
-// q and k of its key head, its v columns and the gates of the next 32 tokens
-// by cp.async while it scans the current 32, then converts q and k to fp32
-// once for all of its columns and builds the four 8-token blocks' tables.
+// Tensor cores.  P, Q and the rank-8 update are matrix products of the state
+// (columns x d_k) with the block's keys and queries, so they run on m16n8k8
+// TF32 MMAs: a warp owns 16 columns and keeps their state in registers in the
+// MMA accumulator layout (lane (g, c) holds columns g and g + 8 at d_k
+// positions 8 n + 2 c, 8 n + 2 c + 1 of each 8-wide chunk n: 64 fp32).  The
+// update accumulates straight into those registers.  As an operand the state
+// is split into two TF32 parts (hi = S rounded to TF32, lo = S - hi rounded
+// to TF32), and the keys and queries, bf16, are exact in TF32, so every
+// product keeps ~21 significant bits and sums in fp32: the 32-bit state the
+// pages ask for, at tensor-core issue rates.  For the products with the
+// state, the MMA's k index is only summed over, so lane (g, c) feeds it the
+// state entries it already holds (k = c and c + 4 from positions 2 c and
+// 2 c + 1) and the key rows are read with the same mapping.
+//
+// The chain.  Only the u_i form a chain; each lane runs it for its two
+// columns (the four lanes of a quad alike, after an all-gather of P and Q),
+// right-looking: once u_l is known it enters every later recall and every
+// output at once.  The coefficient tables come from the block's Gram
+// products q_i . k_l and k_i . k_l on bf16 MMAs (exact products, fp32 sums).
+//
+// Staging.  A CTA is one warp (one value head's 16 columns); it copies the
+// bf16 q and k of its key head, its v columns and the gates of the next 32
+// tokens by cp.async into the second of two buffers while it scans the
+// current 32, and reads q and k for the MMAs straight from the bf16 rows.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -49,16 +55,13 @@
 namespace moe {
 
 namespace {
-constexpr int kDk = 128;                    // d_k supported
-constexpr int kLanes = 8;                   // lanes per column
-constexpr int kEpl = kDk / kLanes;          // state entries per lane
-constexpr int kCols = 16;                   // columns per CTA (one value head's)
-constexpr int kWarpsPerCta = kCols * kLanes / 32;
-constexpr int kTb = 32;                     // tokens per staged block
-constexpr int kB = 8;                       // tokens per block of the recurrence
-constexpr int kSub = kTb / kB;              // blocks of the recurrence per staged block
-constexpr int kRawStride = kDk + 32;        // raw row: 320 B (rows g, g + 1 in other banks)
-static_assert(kB <= 8 && kTb % kB == 0, "the Gram MMA covers at most 8 tokens");
+constexpr int kDk = 128;               // d_k supported
+constexpr int kCols = 16;              // columns per warp (= per CTA)
+constexpr int kChunks = kDk / 8;       // 8-wide d_k chunks of the accumulator layout
+constexpr int kTb = 32;                // tokens per staged block
+constexpr int kB = 8;                  // tokens per block of the recurrence
+constexpr int kSub = kTb / kB;
+constexpr int kRow = kDk + 8;          // staged bf16 row: 272 B (row g on bank 4 g)
 
 struct GdnArgs {
   const __nv_bfloat16 *q, *k, *v;
@@ -78,27 +81,28 @@ struct BlockTab {
   float al[kB], be[kB];
 };
 
-// Every array that cp.async writes 16 bytes at a time, or that is read as
-// float4 / uint4, starts on a 16-byte boundary (checked below).
-struct GdnSmem {
-  alignas(16) float kf[kTb][kDk];           // fp32 activations of the current block
-  alignas(16) float qf[kTb][kDk];
-  alignas(16) BlockTab tab[kSub];
-  alignas(16) __nv_bfloat16 vs[kTb][kCols];   // the current block's v
-  alignas(16) __nv_bfloat16 kr[kTb][kRawStride];  // raw bf16 of the next block
-  alignas(16) __nv_bfloat16 qr[kTb][kRawStride];
-  alignas(16) __nv_bfloat16 vr[kTb][kCols];
-  alignas(16) float ar[kTb];
-  alignas(16) float br[kTb];
+struct Stage {
+  alignas(16) __nv_bfloat16 k[kTb][kRow];
+  alignas(16) __nv_bfloat16 q[kTb][kRow];
+  alignas(16) __nv_bfloat16 v[kTb][kCols];
+  alignas(16) float al[kTb];
+  alignas(16) float be[kTb];
 };
-static_assert(offsetof(GdnSmem, qf) % 16 == 0 && offsetof(GdnSmem, tab) % 16 == 0 &&
-                  offsetof(GdnSmem, kr) % 16 == 0 && offsetof(GdnSmem, qr) % 16 == 0 &&
-                  offsetof(GdnSmem, vr) % 16 == 0 && (kRawStride * 2) % 16 == 0 &&
-                  (kCols * 2) % 16 == 0,
-              "16-byte copies and vector reads need 16-byte aligned rows");
+
+struct GdnSmem {
+  Stage st[2];
+  BlockTab tab[kSub];
+};
+static_assert(offsetof(Stage, q) % 16 == 0 && offsetof(Stage, v) % 16 == 0 &&
+                  sizeof(Stage) % 16 == 0 && (kRow * 2) % 16 == 0,
+              "16-byte copies need 16-byte aligned rows");
 
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -110,74 +114,95 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-// Raw copies of tokens [t0, t0 + n) for this CTA (value head h, columns j0..);
-// the rows of the block past n are zeros with gate 1 and strength 0, so they
-// leave the state unchanged.
-__device__ __forceinline__ void stage_raw(GdnSmem &sm, const GdnArgs &a, int t0, int n, int h,
-                                          int hk, int j0) {
-  for (int i = threadIdx.x; i < kTb * 32; i += blockDim.x) {
+__device__ __forceinline__ float2 f2z() { return make_float2(0.0f, 0.0f); }
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo, both TF32
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+// the two bf16 of a 32-bit word as fp32 bit patterns (exact in TF32)
+__device__ __forceinline__ uint32_t bf16_lo(uint32_t w) { return w << 16; }
+__device__ __forceinline__ uint32_t bf16_hi(uint32_t w) { return w & 0xffff0000u; }
+__device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(x)) << 16;
+}
+
+// Raw copies of tokens [t0, t0 + n) for this CTA (value head h, columns j0..)
+// into stage s; rows past n are zeros with gate 1 and strength 0 (they leave
+// the state unchanged).  One commit group per call.
+__device__ __forceinline__ void stage_block(Stage &s, const GdnArgs &a, int t0, int n, int h,
+                                            int hk, int j0, int lane) {
+  for (int i = lane; i < kTb * 32; i += 32) {
     const int t = i >> 5, p = i & 31, which = p >> 4, piece = p & 15;
-    __nv_bfloat16 *dst = (which ? sm.qr[t] : sm.kr[t]) + piece * 8;
-    if (t < n) {
-      const long long src = (static_cast<long long>(t0 + t) * a.Hk + hk) * kDk + piece * 8;
-      cp_async16(smem_u32(dst), (which ? a.q : a.k) + src);
-    } else {
+    __nv_bfloat16 *dst = (which ? s.q[t] : s.k[t]) + piece * 8;
+    if (t < n)
+      cp_async16(smem_u32(dst), (which ? a.q : a.k) +
+                                    (static_cast<long long>(t0 + t) * a.Hk + hk) * kDk + piece * 8);
+    else
       *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-    }
   }
-  for (int i = threadIdx.x; i < kTb * 4; i += blockDim.x) {
+  for (int i = lane; i < kTb * 4; i += 32) {
     const int t = i >> 2, p = i & 3;
     const long long tv = static_cast<long long>(t0 + t) * a.Hv + h;
     if (t < n) {
       if (p < 2)
-        cp_async16(smem_u32(&sm.vr[t][p * 8]), a.v + tv * a.dv + j0 + p * 8);
+        cp_async16(smem_u32(&s.v[t][p * 8]), a.v + tv * a.dv + j0 + p * 8);
       else if (p == 2)
-        cp_async4(&sm.ar[t], a.alpha + tv);
+        cp_async4(&s.al[t], a.alpha + tv);
       else
-        cp_async4(&sm.br[t], a.beta + tv);
+        cp_async4(&s.be[t], a.beta + tv);
     } else {
       if (p < 2)
-        *reinterpret_cast<uint4 *>(&sm.vr[t][p * 8]) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(&s.v[t][p * 8]) = make_uint4(0, 0, 0, 0);
       else if (p == 2)
-        sm.ar[t] = 1.0f;
+        s.al[t] = 1.0f;
       else
-        sm.br[t] = 0.0f;
+        s.be[t] = 0.0f;
     }
   }
   cp_async_commit();
 }
 
-// Warp w builds the tables of the staged block's 8-token block w.  Gram
-// products on m16n8k16: A rows 0..7 = q_i, rows 8..15 = k_i; B columns =
-// k_l.  The MMA's k index is only summed over, so lane (g, c4) feeds it the
-// 8 columns 32 j + 8 c4 .. of its rows (k = 2 c4, 2 c4 + 1 from +0, +1;
-// 2 c4 + 8, 2 c4 + 9 from +2, +3; the step's second MMA takes +4..+7) and the
+// Tables of 8-token block w of stage s.  Gram products on m16n8k16: A rows
+// 0..7 = q_i, rows 8..15 = k_i; B columns = k_l; lane (g, c) feeds the MMA
+// the 8 columns 32 j + 8 c .. of its rows (k = 2 c, 2 c + 1 from +0, +1;
+// 2 c + 8, 2 c + 9 from +2, +3; the step's second MMA takes +4..+7) and the
 // B side is read with the same mapping.
-__device__ __forceinline__ void block_tables(GdnSmem &sm, int w, int lane) {
-  const int g = lane >> 2, c4 = lane & 3, t = kB * w + min(g, kB - 1);
+__device__ __forceinline__ void block_tables(const Stage &s, BlockTab &tb, int w, int lane) {
+  const int g = lane >> 2, c4 = lane & 3, t = kB * w + g;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kDk / 32; ++j) {
-    const uint4 qv = *reinterpret_cast<const uint4 *>(&sm.qr[t][32 * j + 8 * c4]);
-    const uint4 kv = *reinterpret_cast<const uint4 *>(&sm.kr[t][32 * j + 8 * c4]);
+    const uint4 qv = *reinterpret_cast<const uint4 *>(&s.q[t][32 * j + 8 * c4]);
+    const uint4 kv = *reinterpret_cast<const uint4 *>(&s.k[t][32 * j + 8 * c4]);
     mma_bf16(acc, qv.x, kv.x, qv.y, kv.y, kv.x, kv.y);
     mma_bf16(acc, qv.z, kv.z, qv.w, kv.w, kv.z, kv.w);
   }
-  // acc: (q_g . k_{2 c4}, q_g . k_{2 c4 + 1}, k_g . k_{2 c4}, k_g . k_{2 c4 + 1})
-  BlockTab &tb = sm.tab[w];
-  const float *al = &sm.ar[kB * w];  // this block's gates
+  // acc: (q_g . k_{2 c}, q_g . k_{2 c + 1}, k_g . k_{2 c}, k_g . k_{2 c + 1})
+  const float *al = &s.al[kB * w];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int l = 2 * c4 + e;
-    if (g >= kB || l >= kB) continue;
-    // g(i, l) = alpha_{l+1} .. alpha_{i-1}: for i = g (C) and i = g + 1 (D)
-    float gi = 1.0f;
+    float gi = 1.0f;  // g(g, l) = alpha_{l+1} .. alpha_{g-1}
 #pragma unroll
     for (int m = 0; m < kB; ++m)
       if (m > l && m < g) gi *= al[m];
-    const float gi1 = (g > l) ? gi * sm.ar[t] : 1.0f;  // g(g + 1, l) (l <= g); alpha_g
+    const float gi1 = (g > l) ? gi * al[g] : 1.0f;  // g(g + 1, l), l <= g
     tb.C[l][g] = l < g ? gi * acc[2 + e] : 0.0f;
     tb.D[l][g] = l <= g ? gi1 * acc[e] : 0.0f;
   }
@@ -195,151 +220,172 @@ __device__ __forceinline__ void block_tables(GdnSmem &sm, int w, int lane) {
       if (m > lane) p *= al[m];
     tb.E[lane] = p;
     tb.al[lane] = al[lane];
-    tb.be[lane] = sm.br[kB * w + lane];
+    tb.be[lane] = s.be[kB * w + lane];
   }
-}
-
-// raw block -> fp32 q, k and v for the scan; the tables of its 8-token blocks
-__device__ __forceinline__ void convert_block(GdnSmem &sm) {
-  static_assert(kTb * kDk / 4 % (kWarpsPerCta * 32) == 0, "whole passes");
-#pragma unroll
-  for (int i = threadIdx.x; i < kTb * kDk / 4; i += kWarpsPerCta * 32) {
-    const int t = i / (kDk / 4), e = (i - t * (kDk / 4)) * 4;
-    const uint2 kk = *reinterpret_cast<const uint2 *>(&sm.kr[t][e]);
-    const uint2 qq = *reinterpret_cast<const uint2 *>(&sm.qr[t][e]);
-    const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.x));
-    const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.y));
-    const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq.x));
-    const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq.y));
-    *reinterpret_cast<float4 *>(&sm.kf[t][e]) = make_float4(k0.x, k0.y, k1.x, k1.y);
-    *reinterpret_cast<float4 *>(&sm.qf[t][e]) = make_float4(q0.x, q0.y, q1.x, q1.y);
-  }
-  for (int i = threadIdx.x; i < kTb * kCols; i += blockDim.x)
-    sm.vs[i / kCols][i % kCols] = sm.vr[i / kCols][i % kCols];
-  for (int w = threadIdx.x >> 5; w < kSub; w += kWarpsPerCta) block_tables(sm, w, threadIdx.x & 31);
 }
 }  // namespace
 
-// grid: (H_v * d_v) / kCols CTAs; CTA b scans columns kCols b .. of value head
-// (kCols b) / d_v
-__global__ void __launch_bounds__(kWarpsPerCta * 32) gdn_scan_kernel(GdnArgs a) {
+// grid: (H_v * d_v) / kCols CTAs of one warp; CTA b scans columns kCols b ..
+// of value head (kCols b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) holds
+// columns j0 + g and j0 + g + 8.
+__global__ void __launch_bounds__(32) gdn_scan_kernel(GdnArgs a) {
   extern __shared__ __align__(16) uint8_t s_raw[];
   GdnSmem &sm = *reinterpret_cast<GdnSmem *>(s_raw);
-  const int lane = threadIdx.x & 31, sub = lane % kLanes;
+  const int lane = threadIdx.x, g = lane >> 2, c = lane & 3;
   const int col0 = blockIdx.x * kCols, h = col0 / a.dv, j0 = col0 - h * a.dv;
   const int hk = h / (a.Hv / a.Hk);
-  const int cl = threadIdx.x / kLanes;  // column within the CTA
-  const int j = j0 + cl;
-  // this lane's entries 4 sub + 32 c + 0..3 as pairs: s2[2 c] = (+0, +1), s2[2 c + 1] = (+2, +3)
-  float2 s2[kEpl / 2];
-  const long long sbase = (static_cast<long long>(h) * a.dv + j) * kDk;
-  if (a.s_in) {
+  // st[n] = (S[g][8n + 2c], S[g][8n + 2c + 1], S[g + 8][8n + 2c], S[g + 8][8n + 2c + 1])
+  float st[kChunks][4];
+  const long long sb0 = (static_cast<long long>(h) * a.dv + j0 + g) * kDk + 2 * c;
+  const long long sb8 = sb0 + 8LL * kDk;
 #pragma unroll
-    for (int c = 0; c < kEpl / 4; ++c) {
-      const float4 v4 = reinterpret_cast<const float4 *>(a.s_in + sbase)[sub + kLanes * c];
-      s2[2 * c] = f2(v4.x, v4.y);
-      s2[2 * c + 1] = f2(v4.z, v4.w);
+  for (int n = 0; n < kChunks; ++n) {
+    float2 x = f2z(), y = f2z();
+    if (a.s_in) {
+      x = *reinterpret_cast<const float2 *>(a.s_in + sb0 + 8 * n);
+      y = *reinterpret_cast<const float2 *>(a.s_in + sb8 + 8 * n);
     }
-  } else {
-#pragma unroll
-    for (int c = 0; c < kEpl / 2; ++c) s2[c] = f2(0.0f, 0.0f);
+    st[n][0] = x.x;
+    st[n][1] = x.y;
+    st[n][2] = y.x;
+    st[n][3] = y.y;
   }
   const int nblk = (a.T + kTb - 1) / kTb;
-  if (nblk > 0) {
-    stage_raw(sm, a, 0, min(kTb, a.T), h, hk, j0);
-    cp_async_wait_all();
-    __syncthreads();
-    convert_block(sm);
-    __syncthreads();
-  }
-  __nv_bfloat16 *orow = a.o + static_cast<long long>(h) * a.dv + j;
+  __nv_bfloat16 *ob = a.o + static_cast<long long>(h) * a.dv + j0 + g;
   const long long ostride = static_cast<long long>(a.Hv) * a.dv;
+  if (nblk > 0) stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, lane);
   for (int b = 0; b < nblk; ++b) {
     const int t0 = b * kTb, n = min(kTb, a.T - t0);
-    if (b + 1 < nblk) stage_raw(sm, a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0);
+    if (b + 1 < nblk)
+      stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, lane);
+    else
+      cp_async_commit();  // an empty group keeps the count below uniform
+    cp_async_wait_group<1>();  // this block's copies have landed
+    __syncwarp();
+    const Stage &S = sm.st[b & 1];
+#pragma unroll 1
+    for (int w = 0; w < kSub; ++w) block_tables(S, sm.tab[w], w, lane);
+    __syncwarp();
+#pragma unroll 1
     for (int sb = 0; sb * kB < n; ++sb) {
       const BlockTab &tb = sm.tab[sb];
       const int tb0 = sb * kB;
-      // P_i, Q_i: this lane's part (chunk by chunk, 16 independent
-      // accumulator chains), then one butterfly for all 16
-      float2 pk[kB], pqq[kB], pq[kB];
+      // P = S K^T, Q = S Q^T over the block's 8 tokens (hi and lo parts of
+      // the state, even and odd chunks in separate accumulators)
+      float acc[2][4][4];  // [chunk parity][P hi, P lo, Q hi, Q lo][fragment]
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y)
+#pragma unroll
+          for (int z = 0; z < 4; ++z) acc[x][y][z] = 0.0f;
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_tf32(st[ch][e], hi[e], lo[e]);
+        const uint32_t kw = *reinterpret_cast<const uint32_t *>(&S.k[tb0 + g][8 * ch + 2 * c]);
+        const uint32_t qw = *reinterpret_cast<const uint32_t *>(&S.q[tb0 + g][8 * ch + 2 * c]);
+        float(&A)[4][4] = acc[ch & 1];
+        // a0 = (g, k c) <- entry 2c, a1 = (g + 8, k c), a2 = (g, k c + 4) <- entry 2c + 1, a3 = (g + 8, k c + 4)
+        mma_tf32(A[0], hi[0], hi[2], hi[1], hi[3], bf16_lo(kw), bf16_hi(kw));
+        mma_tf32(A[1], lo[0], lo[2], lo[1], lo[3], bf16_lo(kw), bf16_hi(kw));
+        mma_tf32(A[2], hi[0], hi[2], hi[1], hi[3], bf16_lo(qw), bf16_hi(qw));
+        mma_tf32(A[3], lo[0], lo[2], lo[1], lo[3], bf16_lo(qw), bf16_hi(qw));
+      }
+      // this lane: P, Q of columns g, g + 8 at tokens 2c, 2c + 1
+      float pf[4], qf[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pf[e] = (acc[0][0][e] + acc[0][1][e]) + (acc[1][0][e] + acc[1][1][e]);
+        qf[e] = (acc[0][2][e] + acc[0][3][e]) + (acc[1][2][e] + acc[1][3][e]);
+      }
+      // all 8 tokens for both columns from the quad
+      float p0[kB], p1[kB], q0[kB], q1[kB];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int src = (lane & ~3) | s;
+        p0[2 * s] = __shfl_sync(0xffffffffu, pf[0], src);
+        p0[2 * s + 1] = __shfl_sync(0xffffffffu, pf[1], src);
+        p1[2 * s] = __shfl_sync(0xffffffffu, pf[2], src);
+        p1[2 * s + 1] = __shfl_sync(0xffffffffu, pf[3], src);
+        q0[2 * s] = __shfl_sync(0xffffffffu, qf[0], src);
+        q0[2 * s + 1] = __shfl_sync(0xffffffffu, qf[1], src);
+        q1[2 * s] = __shfl_sync(0xffffffffu, qf[2], src);
+        q1[2 * s + 1] = __shfl_sync(0xffffffffu, qf[3], src);
+      }
+      // the chain, right-looking, for columns g (0) and g + 8 (1)
+      float R0[kB], R1[kB], O0[kB], O1[kB], u0[kB], u1[kB];
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        pk[i] = f2(0.f, 0.f);
-        pqq[i] = f2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int c = 0; c < kEpl / 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < kB; ++i) {
-          const float4 k4 = reinterpret_cast<const float4 *>(sm.kf[tb0 + i])[sub + kLanes * c];
-          const float4 q4 = reinterpret_cast<const float4 *>(sm.qf[tb0 + i])[sub + kLanes * c];
-          pk[i] = __ffma2_rn(s2[2 * c], f2(k4.x, k4.y), pk[i]);
-          pk[i] = __ffma2_rn(s2[2 * c + 1], f2(k4.z, k4.w), pk[i]);
-          pqq[i] = __ffma2_rn(s2[2 * c], f2(q4.x, q4.y), pqq[i]);
-          pqq[i] = __ffma2_rn(s2[2 * c + 1], f2(q4.z, q4.w), pqq[i]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kB; ++i) pq[i] = f2(pk[i].x + pk[i].y, pqq[i].x + pqq[i].y);
-#pragma unroll
-      for (int o = kLanes / 2; o >= 1; o >>= 1) {
-#pragma unroll
-        for (int i = 0; i < kB; ++i)
-          pq[i] = __fadd2_rn(pq[i], f2(__shfl_xor_sync(0xffffffffu, pq[i].x, o),
-                                       __shfl_xor_sync(0xffffffffu, pq[i].y, o)));
-      }
-      // the chain, right-looking: once u_l is known it enters every later
-      // token's recall and every output at once (independent FMAs), so the
-      // chain is the u_l alone
-      float R[kB], O[kB], u[kB];
-#pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        R[i] = tb.A[i] * pq[i].x;
-        O[i] = tb.A[i + 1] * pq[i].y;
+        R0[i] = tb.A[i] * p0[i];
+        R1[i] = tb.A[i] * p1[i];
+        O0[i] = tb.A[i + 1] * q0[i];
+        O1[i] = tb.A[i + 1] * q1[i];
       }
 #pragma unroll
       for (int l = 0; l < kB; ++l) {
-        const float v = __bfloat162float(sm.vs[tb0 + l][cl]);
-        u[l] = tb.be[l] * fmaf(-tb.al[l], R[l], v);
+        const float al = tb.al[l], be = tb.be[l];
+        u0[l] = be * fmaf(-al, R0[l], __bfloat162float(S.v[tb0 + l][g]));
+        u1[l] = be * fmaf(-al, R1[l], __bfloat162float(S.v[tb0 + l][g + 8]));
 #pragma unroll
-        for (int i = l + 1; i < kB; ++i) R[i] = fmaf(tb.C[l][i], u[l], R[i]);
+        for (int i = l + 1; i < kB; ++i) {
+          R0[i] = fmaf(tb.C[l][i], u0[l], R0[i]);
+          R1[i] = fmaf(tb.C[l][i], u1[l], R1[i]);
+        }
 #pragma unroll
-        for (int i = l; i < kB; ++i) O[i] = fmaf(tb.D[l][i], u[l], O[i]);
+        for (int i = l; i < kB; ++i) {
+          O0[i] = fmaf(tb.D[l][i], u0[l], O0[i]);
+          O1[i] = fmaf(tb.D[l][i], u1[l], O1[i]);
+        }
       }
-      if (sub == 0) {
+      // lane c writes tokens 2c, 2c + 1 of both columns
 #pragma unroll
-        for (int i = 0; i < kB; ++i)
-          if (tb0 + i < n) orow[(t0 + tb0 + i) * ostride] = __float2bfloat16_rn(O[i]);
+      for (int i = 0; i < kB; ++i) {
+        if ((i >> 1) == c && tb0 + i < n) {
+          const long long off = (t0 + tb0 + i) * ostride;
+          ob[off] = __float2bfloat16_rn(O0[i]);
+          ob[off + 8] = __float2bfloat16_rn(O1[i]);
+        }
       }
-      // S <- A_8 S + sum_l g(8, l) u_l k_l
+      // S <- A_8 S + W K with W[col][l] = g(8, l) u_l: A operand rows g, g + 8,
+      // k = token c and c + 4
+      float w0 = 0.f, w1 = 0.f, w4 = 0.f, w5 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i == c) {
+          w0 = tb.E[i] * u0[i];
+          w1 = tb.E[i] * u1[i];
+          w4 = tb.E[i + 4] * u0[i + 4];
+          w5 = tb.E[i + 4] * u1[i + 4];
+        }
+      }
+      uint32_t wh[4], wl[4];
+      split_tf32(w0, wh[0], wl[0]);  // a0 = (g, k c)
+      split_tf32(w1, wh[1], wl[1]);  // a1 = (g + 8, k c)
+      split_tf32(w4, wh[2], wl[2]);  // a2 = (g, k c + 4)
+      split_tf32(w5, wh[3], wl[3]);  // a3 = (g + 8, k c + 4)
       const float a8 = tb.A[kB];
 #pragma unroll
-      for (int c = 0; c < kEpl / 2; ++c) s2[c] = __fmul2_rn(f2(a8, a8), s2[c]);
+      for (int ch = 0; ch < kChunks; ++ch) {
 #pragma unroll
-      for (int l = 0; l < kB; ++l) {
-        const float w = tb.E[l] * u[l];
-        const float4 *kr = reinterpret_cast<const float4 *>(sm.kf[tb0 + l]) + sub;
-#pragma unroll
-        for (int c = 0; c < kEpl / 4; ++c) {
-          const float4 k4 = kr[kLanes * c];
-          s2[2 * c] = __ffma2_rn(f2(w, w), f2(k4.x, k4.y), s2[2 * c]);
-          s2[2 * c + 1] = __ffma2_rn(f2(w, w), f2(k4.z, k4.w), s2[2 * c + 1]);
-        }
+        for (int e = 0; e < 4; ++e) st[ch][e] *= a8;
+        // b0 = (k = token c, column g of the chunk), b1 = (token c + 4, column g)
+        const uint32_t b0 = bf16_bits(S.k[tb0 + c][8 * ch + g]);
+        const uint32_t b1 = bf16_bits(S.k[tb0 + c + 4][8 * ch + g]);
+        mma_tf32(st[ch], wh[0], wh[1], wh[2], wh[3], b0, b1);
+        mma_tf32(st[ch], wl[0], wl[1], wl[2], wl[3], b0, b1);
       }
     }
-    if (b + 1 < nblk) {
-      cp_async_wait_all();
-      __syncthreads();  // every warp is done with this block's fp32 data and tables
-      convert_block(sm);
-      __syncthreads();
-    }
+    __syncwarp();  // done with this stage before it is refilled
   }
+  cp_async_wait_group<0>();
   if (a.s_out) {
 #pragma unroll
-    for (int c = 0; c < kEpl / 4; ++c)
-      reinterpret_cast<float4 *>(a.s_out + sbase)[sub + kLanes * c] =
-          make_float4(s2[2 * c].x, s2[2 * c].y, s2[2 * c + 1].x, s2[2 * c + 1].y);
+    for (int n = 0; n < kChunks; ++n) {
+      *reinterpret_cast<float2 *>(a.s_out + sb0 + 8 * n) = make_float2(st[n][0], st[n][1]);
+      *reinterpret_cast<float2 *>(a.s_out + sb8 + 8 * n) = make_float2(st[n][2], st[n][3]);
+    }
   }
 }
 
@@ -371,6 +417,6 @@ extern "C" int gdn_scan(const void *q, const void *k, const void *v, const float
   a.Hv = n_v_heads;
   a.dv = d_v;
   const int grid = n_v_heads * d_v / kCols;
-  gdn_scan_kernel<<<grid, kWarpsPerCta * 32, sizeof(GdnSmem), static_cast<cudaStream_t>(cuda_stream)>>>(a);
+  gdn_scan_kernel<<<grid, 32, sizeof(GdnSmem), static_cast<cudaStream_t>(cuda_stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
