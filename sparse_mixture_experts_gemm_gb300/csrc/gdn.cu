@@ -22,28 +22,30 @@
 //
 // Tensor cores.  P, Q and the rank-8 update are matrix products of the state
 // (columns x d_k) with the block's keys and queries, so they run on m16n8k8
-// TF32 MMAs: a warp owns 16 columns and keeps their state in registers in the
-// MMA accumulator layout (lane (g, c) holds columns g and g + 8 at d_k
-// positions 8 n + 2 c, 8 n + 2 c + 1 of each 8-wide chunk n: 64 fp32).  The
-// update accumulates straight into those registers.  As an operand the state
-// is split into two TF32 parts (hi = S rounded to TF32, lo = S - hi rounded
-// to TF32), and the keys and queries, bf16, are exact in TF32, so every
-// product keeps ~21 significant bits and sums in fp32: the 32-bit state the
-// pages ask for, at tensor-core issue rates.  For the products with the
-// state, the MMA's k index is only summed over, so lane (g, c) feeds it the
-// state entries it already holds (k = c and c + 4 from positions 2 c and
-// 2 c + 1) and the key rows are read with the same mapping.
+// TF32 MMAs.  A CTA owns 16 columns and its 4 warps split d_k: warp w keeps
+// the state of all 16 columns at d_k chunks 4 w .. 4 w + 3 in registers in
+// the MMA accumulator layout (lane (g, c) holds columns g and g + 8 at d_k
+// positions 8 n + 2 c, 8 n + 2 c + 1 of chunk n: 16 fp32).  The update
+// accumulates straight into those registers.  As an operand the state is
+// split into two TF32 parts (hi = the top 11 significant bits of S, lo the
+// top 11 of S - hi), and the keys and queries, bf16, are exact in TF32, so
+// every product keeps ~22 significant bits and sums in fp32: the 32-bit
+// state the pages ask for, at tensor-core issue rates.  For the products
+// with the state, the MMA's k index is only summed over, so lane (g, c) feeds
+// it the state entries it already holds (k = c and c + 4 from positions 2 c
+// and 2 c + 1) and the key rows are read with the same mapping.
 //
-// The chain.  Only the u_i form a chain; each lane runs it for its two
-// columns (the four lanes of a quad alike, after an all-gather of P and Q),
-// right-looking: once u_l is known it enters every later recall and every
-// output at once.  The coefficient tables come from the block's Gram
+// The chain.  The warps' partial P and Q meet in shared memory (one barrier
+// per 8 tokens, two buffers); then every warp runs the chain for all 16
+// columns, one column per lane (lanes 16..31 repeat 0..15), right-looking:
+// once u_l is known it enters every later recall and every output at once.
+// Only the u_i form a chain.  The coefficient tables come from the block's Gram
 // products q_i . k_l and k_i . k_l on bf16 MMAs (exact products, fp32 sums).
 //
-// Staging.  A CTA is one warp (one value head's 16 columns); it copies the
-// bf16 q and k of its key head, its v columns and the gates of the next 32
-// tokens by cp.async into the second of two buffers while it scans the
-// current 32, and reads q and k for the MMAs straight from the bf16 rows.
+// Staging.  The CTA copies the bf16 q and k of its key head, its v columns
+// and the gates of the next 32 tokens by cp.async into the second of two
+// buffers while it scans the current 32, and reads q and k for the MMAs
+// straight from the bf16 rows.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -56,8 +58,10 @@ namespace moe {
 
 namespace {
 constexpr int kDk = 128;               // d_k supported
-constexpr int kCols = 16;              // columns per warp (= per CTA)
-constexpr int kChunks = kDk / 8;       // 8-wide d_k chunks of the accumulator layout
+constexpr int kCols = 16;              // columns per CTA
+constexpr int kWarps = 4;              // warps per CTA, each a quarter of d_k
+constexpr int kGdnThreads = kWarps * 32;
+constexpr int kChunks = kDk / 8 / kWarps;  // 8-wide d_k chunks per warp
 constexpr int kTb = 32;                // tokens per staged block
 constexpr int kB = 8;                  // tokens per block of the recurrence
 constexpr int kSub = kTb / kB;
@@ -92,6 +96,9 @@ struct Stage {
 struct GdnSmem {
   Stage st[2];
   BlockTab tab[kSub];
+  // [buffer][warp][P, Q][column][token] partial sums; rows of 12 floats so
+  // that the 8 columns a quarter-warp reads start in different banks
+  float part[2][kWarps][2][kCols][kB + 4];
 };
 static_assert(offsetof(Stage, q) % 16 == 0 && offsetof(Stage, v) % 16 == 0 &&
                   sizeof(Stage) % 16 == 0 && (kRow * 2) % 16 == 0,
@@ -125,15 +132,13 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ float2 f2z() { return make_float2(0.0f, 0.0f); }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-// x = hi + lo, both TF32
+// x ~ hi + lo, both TF32 (the low 13 bits cleared): hi keeps the top 11
+// significant bits of x, lo = x - hi exactly and then its own top 11, so the
+// pair carries ~22 of x's 24 bits; two integer ops and one FADD, no
+// conversion instruction
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-  hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
 }
 // the two bf16 of a 32-bit word as fp32 bit patterns (exact in TF32)
 __device__ __forceinline__ uint32_t bf16_lo(uint32_t w) { return w << 16; }
@@ -146,8 +151,8 @@ __device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 x) {
 // into stage s; rows past n are zeros with gate 1 and strength 0 (they leave
 // the state unchanged).  One commit group per call.
 __device__ __forceinline__ void stage_block(Stage &s, const GdnArgs &a, int t0, int n, int h,
-                                            int hk, int j0, int lane) {
-  for (int i = lane; i < kTb * 32; i += 32) {
+                                            int hk, int j0, int tid) {
+  for (int i = tid; i < kTb * 32; i += kGdnThreads) {
     const int t = i >> 5, p = i & 31, which = p >> 4, piece = p & 15;
     __nv_bfloat16 *dst = (which ? s.q[t] : s.k[t]) + piece * 8;
     if (t < n)
@@ -156,7 +161,7 @@ __device__ __forceinline__ void stage_block(Stage &s, const GdnArgs &a, int t0, 
     else
       *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
   }
-  for (int i = lane; i < kTb * 4; i += 32) {
+  for (int i = tid; i < kTb * 4; i += kGdnThreads) {
     const int t = i >> 2, p = i & 3;
     const long long tv = static_cast<long long>(t0 + t) * a.Hv + h;
     if (t < n) {
@@ -225,18 +230,20 @@ __device__ __forceinline__ void block_tables(const Stage &s, BlockTab &tb, int w
 }
 }  // namespace
 
-// grid: (H_v * d_v) / kCols CTAs of one warp; CTA b scans columns kCols b ..
-// of value head (kCols b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) holds
-// columns j0 + g and j0 + g + 8.
-__global__ void __launch_bounds__(32) gdn_scan_kernel(GdnArgs a) {
+// grid: (H_v * d_v) / kCols CTAs of 4 warps; CTA b scans columns kCols b ..
+// of value head (kCols b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) of warp w
+// holds columns j0 + g and j0 + g + 8 at d_k chunks 4 w ..
+__global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
   extern __shared__ __align__(16) uint8_t s_raw[];
   GdnSmem &sm = *reinterpret_cast<GdnSmem *>(s_raw);
-  const int lane = threadIdx.x, g = lane >> 2, c = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int jc = lane & 15;  // the column this lane runs the chain for
   const int col0 = blockIdx.x * kCols, h = col0 / a.dv, j0 = col0 - h * a.dv;
   const int hk = h / (a.Hv / a.Hk);
-  // st[n] = (S[g][8n + 2c], S[g][8n + 2c + 1], S[g + 8][8n + 2c], S[g + 8][8n + 2c + 1])
+  const int ch0 = warp * kChunks;  // this warp's first d_k chunk
+  // st[n] = (S[g][8m + 2c], S[g][8m + 2c + 1], S[g + 8][8m + 2c], S[g + 8][8m + 2c + 1]), m = ch0 + n
   float st[kChunks][4];
-  const long long sb0 = (static_cast<long long>(h) * a.dv + j0 + g) * kDk + 2 * c;
+  const long long sb0 = (static_cast<long long>(h) * a.dv + j0 + g) * kDk + 8 * ch0 + 2 * c;
   const long long sb8 = sb0 + 8LL * kDk;
 #pragma unroll
   for (int n = 0; n < kChunks; ++n) {
@@ -251,27 +258,27 @@ __global__ void __launch_bounds__(32) gdn_scan_kernel(GdnArgs a) {
     st[n][3] = y.y;
   }
   const int nblk = (a.T + kTb - 1) / kTb;
-  __nv_bfloat16 *ob = a.o + static_cast<long long>(h) * a.dv + j0 + g;
+  __nv_bfloat16 *ob = a.o + static_cast<long long>(h) * a.dv + j0 + jc;
   const long long ostride = static_cast<long long>(a.Hv) * a.dv;
-  if (nblk > 0) stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, lane);
+  int it = 0;  // 8-token blocks done (selects the partial-sum buffer)
+  if (nblk > 0) stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, tid);
   for (int b = 0; b < nblk; ++b) {
     const int t0 = b * kTb, n = min(kTb, a.T - t0);
     if (b + 1 < nblk)
-      stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, lane);
+      stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, tid);
     else
       cp_async_commit();  // an empty group keeps the count below uniform
     cp_async_wait_group<1>();  // this block's copies have landed
-    __syncwarp();
+    __syncthreads();
     const Stage &S = sm.st[b & 1];
+    block_tables(S, sm.tab[warp], warp, lane);  // one warp per 8-token block
+    __syncthreads();
 #pragma unroll 1
-    for (int w = 0; w < kSub; ++w) block_tables(S, sm.tab[w], w, lane);
-    __syncwarp();
-#pragma unroll 1
-    for (int sb = 0; sb * kB < n; ++sb) {
+    for (int sb = 0; sb * kB < n; ++sb, ++it) {
       const BlockTab &tb = sm.tab[sb];
       const int tb0 = sb * kB;
-      // P = S K^T, Q = S Q^T over the block's 8 tokens (hi and lo parts of
-      // the state, even and odd chunks in separate accumulators)
+      // this warp's part of P = S K^T and Q = S Q^T (hi and lo parts of the
+      // state, even and odd chunks in separate accumulators)
       float acc[2][4][4];  // [chunk parity][P hi, P lo, Q hi, Q lo][fragment]
 #pragma unroll
       for (int x = 0; x < 2; ++x)
@@ -280,84 +287,89 @@ __global__ void __launch_bounds__(32) gdn_scan_kernel(GdnArgs a) {
 #pragma unroll
           for (int z = 0; z < 4; ++z) acc[x][y][z] = 0.0f;
 #pragma unroll
-      for (int ch = 0; ch < kChunks; ++ch) {
+      for (int nn = 0; nn < kChunks; ++nn) {
+        const int m = ch0 + nn;
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_tf32(st[ch][e], hi[e], lo[e]);
-        const uint32_t kw = *reinterpret_cast<const uint32_t *>(&S.k[tb0 + g][8 * ch + 2 * c]);
-        const uint32_t qw = *reinterpret_cast<const uint32_t *>(&S.q[tb0 + g][8 * ch + 2 * c]);
-        float(&A)[4][4] = acc[ch & 1];
+        for (int e = 0; e < 4; ++e) split_tf32(st[nn][e], hi[e], lo[e]);
+        const uint32_t kw = *reinterpret_cast<const uint32_t *>(&S.k[tb0 + g][8 * m + 2 * c]);
+        const uint32_t qw = *reinterpret_cast<const uint32_t *>(&S.q[tb0 + g][8 * m + 2 * c]);
+        float(&A)[4][4] = acc[nn & 1];
         // a0 = (g, k c) <- entry 2c, a1 = (g + 8, k c), a2 = (g, k c + 4) <- entry 2c + 1, a3 = (g + 8, k c + 4)
         mma_tf32(A[0], hi[0], hi[2], hi[1], hi[3], bf16_lo(kw), bf16_hi(kw));
         mma_tf32(A[1], lo[0], lo[2], lo[1], lo[3], bf16_lo(kw), bf16_hi(kw));
         mma_tf32(A[2], hi[0], hi[2], hi[1], hi[3], bf16_lo(qw), bf16_hi(qw));
         mma_tf32(A[3], lo[0], lo[2], lo[1], lo[3], bf16_lo(qw), bf16_hi(qw));
       }
-      // this lane: P, Q of columns g, g + 8 at tokens 2c, 2c + 1
-      float pf[4], qf[4];
+      // partials of columns g, g + 8 at tokens 2c, 2c + 1 into shared memory
+      float(&pt)[kWarps][2][kCols][kB + 4] = sm.part[it & 1];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pf[e] = (acc[0][0][e] + acc[0][1][e]) + (acc[1][0][e] + acc[1][1][e]);
-        qf[e] = (acc[0][2][e] + acc[0][3][e]) + (acc[1][2][e] + acc[1][3][e]);
+      for (int pq = 0; pq < 2; ++pq) {
+        const int y = 2 * pq;
+        *reinterpret_cast<float2 *>(&pt[warp][pq][g][2 * c]) =
+            make_float2((acc[0][y][0] + acc[0][y + 1][0]) + (acc[1][y][0] + acc[1][y + 1][0]),
+                        (acc[0][y][1] + acc[0][y + 1][1]) + (acc[1][y][1] + acc[1][y + 1][1]));
+        *reinterpret_cast<float2 *>(&pt[warp][pq][g + 8][2 * c]) =
+            make_float2((acc[0][y][2] + acc[0][y + 1][2]) + (acc[1][y][2] + acc[1][y + 1][2]),
+                        (acc[0][y][3] + acc[0][y + 1][3]) + (acc[1][y][3] + acc[1][y + 1][3]));
       }
-      // all 8 tokens for both columns from the quad
-      float p0[kB], p1[kB], q0[kB], q1[kB];
+      __syncthreads();
+      // P, Q of column jc at the 8 tokens, summed over the warps in order
+      float p[kB], q[kB];
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int src = (lane & ~3) | s;
-        p0[2 * s] = __shfl_sync(0xffffffffu, pf[0], src);
-        p0[2 * s + 1] = __shfl_sync(0xffffffffu, pf[1], src);
-        p1[2 * s] = __shfl_sync(0xffffffffu, pf[2], src);
-        p1[2 * s + 1] = __shfl_sync(0xffffffffu, pf[3], src);
-        q0[2 * s] = __shfl_sync(0xffffffffu, qf[0], src);
-        q0[2 * s + 1] = __shfl_sync(0xffffffffu, qf[1], src);
-        q1[2 * s] = __shfl_sync(0xffffffffu, qf[2], src);
-        q1[2 * s + 1] = __shfl_sync(0xffffffffu, qf[3], src);
+      for (int i = 0; i < kB; ++i) p[i] = q[i] = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float4 pv = *reinterpret_cast<const float4 *>(&pt[w][0][jc][4 * hf]);
+          const float4 qv = *reinterpret_cast<const float4 *>(&pt[w][1][jc][4 * hf]);
+          p[4 * hf] += pv.x;
+          p[4 * hf + 1] += pv.y;
+          p[4 * hf + 2] += pv.z;
+          p[4 * hf + 3] += pv.w;
+          q[4 * hf] += qv.x;
+          q[4 * hf + 1] += qv.y;
+          q[4 * hf + 2] += qv.z;
+          q[4 * hf + 3] += qv.w;
+        }
       }
-      // the chain, right-looking, for columns g (0) and g + 8 (1)
-      float R0[kB], R1[kB], O0[kB], O1[kB], u0[kB], u1[kB];
+      // the chain, right-looking, for column jc
+      float R[kB], O[kB], u[kB];
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        R0[i] = tb.A[i] * p0[i];
-        R1[i] = tb.A[i] * p1[i];
-        O0[i] = tb.A[i + 1] * q0[i];
-        O1[i] = tb.A[i + 1] * q1[i];
+        R[i] = tb.A[i] * p[i];
+        O[i] = tb.A[i + 1] * q[i];
       }
 #pragma unroll
       for (int l = 0; l < kB; ++l) {
-        const float al = tb.al[l], be = tb.be[l];
-        u0[l] = be * fmaf(-al, R0[l], __bfloat162float(S.v[tb0 + l][g]));
-        u1[l] = be * fmaf(-al, R1[l], __bfloat162float(S.v[tb0 + l][g + 8]));
+        u[l] = tb.be[l] * fmaf(-tb.al[l], R[l], __bfloat162float(S.v[tb0 + l][jc]));
 #pragma unroll
-        for (int i = l + 1; i < kB; ++i) {
-          R0[i] = fmaf(tb.C[l][i], u0[l], R0[i]);
-          R1[i] = fmaf(tb.C[l][i], u1[l], R1[i]);
-        }
+        for (int i = l + 1; i < kB; ++i) R[i] = fmaf(tb.C[l][i], u[l], R[i]);
 #pragma unroll
-        for (int i = l; i < kB; ++i) {
-          O0[i] = fmaf(tb.D[l][i], u0[l], O0[i]);
-          O1[i] = fmaf(tb.D[l][i], u1[l], O1[i]);
-        }
+        for (int i = l; i < kB; ++i) O[i] = fmaf(tb.D[l][i], u[l], O[i]);
       }
-      // lane c writes tokens 2c, 2c + 1 of both columns
+      // warp w writes tokens 2w, 2w + 1 of the 16 columns
+      if (lane < kCols) {
 #pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        if ((i >> 1) == c && tb0 + i < n) {
-          const long long off = (t0 + tb0 + i) * ostride;
-          ob[off] = __float2bfloat16_rn(O0[i]);
-          ob[off + 8] = __float2bfloat16_rn(O1[i]);
-        }
+        for (int i = 0; i < kB; ++i)
+          if ((i >> 1) == warp && tb0 + i < n) ob[(t0 + tb0 + i) * ostride] = __float2bfloat16_rn(O[i]);
       }
       // S <- A_8 S + W K with W[col][l] = g(8, l) u_l: A operand rows g, g + 8,
-      // k = token c and c + 4
+      // k = token c and c + 4 (u of column g from lane g, of g + 8 from lane g + 8)
       float w0 = 0.f, w1 = 0.f, w4 = 0.f, w5 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kB; ++i) {
+        const float eu = tb.E[i] * u[i];
+        const float x = __shfl_sync(0xffffffffu, eu, g);
+        const float y = __shfl_sync(0xffffffffu, eu, g + 8);
         if (i == c) {
-          w0 = tb.E[i] * u0[i];
-          w1 = tb.E[i] * u1[i];
-          w4 = tb.E[i + 4] * u0[i + 4];
-          w5 = tb.E[i + 4] * u1[i + 4];
+          w0 = x;
+          w1 = y;
+        }
+        if (i == c + 4) {
+          w4 = x;
+          w5 = y;
         }
       }
       uint32_t wh[4], wl[4];
@@ -367,17 +379,18 @@ __global__ void __launch_bounds__(32) gdn_scan_kernel(GdnArgs a) {
       split_tf32(w5, wh[3], wl[3]);  // a3 = (g + 8, k c + 4)
       const float a8 = tb.A[kB];
 #pragma unroll
-      for (int ch = 0; ch < kChunks; ++ch) {
+      for (int nn = 0; nn < kChunks; ++nn) {
+        const int m = ch0 + nn;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) st[ch][e] *= a8;
+        for (int e = 0; e < 4; ++e) st[nn][e] *= a8;
         // b0 = (k = token c, column g of the chunk), b1 = (token c + 4, column g)
-        const uint32_t b0 = bf16_bits(S.k[tb0 + c][8 * ch + g]);
-        const uint32_t b1 = bf16_bits(S.k[tb0 + c + 4][8 * ch + g]);
-        mma_tf32(st[ch], wh[0], wh[1], wh[2], wh[3], b0, b1);
-        mma_tf32(st[ch], wl[0], wl[1], wl[2], wl[3], b0, b1);
+        const uint32_t b0 = bf16_bits(S.k[tb0 + c][8 * m + g]);
+        const uint32_t b1 = bf16_bits(S.k[tb0 + c + 4][8 * m + g]);
+        mma_tf32(st[nn], wh[0], wh[1], wh[2], wh[3], b0, b1);
+        mma_tf32(st[nn], wl[0], wl[1], wl[2], wl[3], b0, b1);
       }
     }
-    __syncwarp();  // done with this stage before it is refilled
+    __syncthreads();  // every warp is done with this stage before it is refilled
   }
   cp_async_wait_group<0>();
   if (a.s_out) {
@@ -417,6 +430,6 @@ extern "C" int gdn_scan(const void *q, const void *k, const void *v, const float
   a.Hv = n_v_heads;
   a.dv = d_v;
   const int grid = n_v_heads * d_v / kCols;
-  gdn_scan_kernel<<<grid, 32, sizeof(GdnSmem), static_cast<cudaStream_t>(cuda_stream)>>>(a);
+  gdn_scan_kernel<<<grid, kGdnThreads, sizeof(GdnSmem), static_cast<cudaStream_t>(cuda_stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
