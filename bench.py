@@ -246,6 +246,7 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
         rc, det = layer.status()
         if rc != 0:
             raise RuntimeError(f"4-bit prefill device status {rc} ({det})")
+        small = bench_small_batch(layer, cfg, dev, flush_buf, pk, q4=True)
     finally:
         layer.close()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
@@ -272,13 +273,15 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
                                  "hbm": byts / (pk["hbm"] * 1e9) * 1e6},
         "kernels_ms_per_step": per, "clocks": clk.summary(),
         "gpu_launches": sum(v[1] for v in prof.values()) // max(steps, 1) * steps,
+        "small_batch": small,
     }
 
 
-def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50) -> dict:
+def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dict:
     """Batches of 2..16 tokens through the same layer (the verification shape
     of speculative decoding): one routing launch, the grouped GEMV on all SMs,
-    the combine; eager calls as a user makes them, L2 flushed before each."""
+    the combine; eager calls as a user makes them, L2 flushed before each.
+    q4: the layer has 4-bit expert weights (0.5625 bytes a weight)."""
     d, F, E, k = cfg["d"], cfg["F"], cfg["E"], cfg["k"]
     st = torch.cuda.current_stream()
     out = {}
@@ -300,12 +303,14 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50) -> dict:
         if rc != 0:
             raise RuntimeError(f"small-batch device status {rc} ({det})")
         us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
-        byts = (active + 1) * 3 * F * d * 2 + E * d * 2
+        byts = (active + 1) * 3 * F * d * (0.5 + 4 / 64 if q4 else 2) + E * d * 2
         out[str(T)] = {"us_per_layer_median": us, "experts_touched": active,
                        "algorithmic_bytes": byts,
                        "hbm_frac_of_measured": byts / (us * 1e-6) / (pk["hbm"] * 1e9)}
     return {"workload": "T = 2, 4, 8, 16 tokens through one layer (d=2048, 256 experts top-8 + "
-                        "1 shared, F=512, bf16), eager calls, L2 flushed before each, median of "
+                        "1 shared, F=512, " + ("4-bit group-affine expert weights, bf16 router "
+                                               "and tokens" if q4 else "bf16") +
+                        "), eager calls, L2 flushed before each, median of "
                         f"{iters}", "by_T": out, "gpu_launches_per_layer": 4}
 
 

@@ -20,7 +20,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
 #include "ptx.cuh"
+#include "status.h"
 
 namespace moe {
 namespace {
@@ -72,6 +74,35 @@ __device__ __forceinline__ int gv_part(int r, int m) {
 //                                  valid column: results past ncols are unused)
 //   void epilogue(int u, const float *red)   block-wide, after the barrier;
 //                                  red: [16 warps][32 lanes][8] partials
+// The groups that got rows, in unit order: the shared expert (group E) first,
+// then the routed experts in index order.  Copies the offsets; block-wide.
+// An invalid partition is reported and leaves no groups.
+template <class Args>
+__device__ __forceinline__ void touched_groups(const Args &a, int *s_off, int *s_grp, int *s_ng,
+                                               int kid) {
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldcg(a.offsets + i);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int n = a.n_shared ? 1 : 0;
+    bool bad = s_off[0] != 0 || s_off[a.E] != a.A;
+    for (int base = 0; base < a.E; base += 32) {
+      const int e = base + lane;
+      const int rows = e < a.E ? s_off[e + 1] - s_off[e] : 0;
+      bad = bad || rows < 0;
+      const unsigned m = __ballot_sync(0xffffffffu, rows > 0);
+      if (rows > 0) s_grp[n + __popc(m & ((1u << lane) - 1u))] = e;
+      n += __popc(m);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      if (a.n_shared) s_grp[0] = a.E;
+      *s_ng = bad ? 0 : n;
+      if (bad && blockIdx.x == 0) report_error(a.status, MOE_ERR_DEVICE_BOUNDS, kid * 100 + SITE_INDEX);
+    }
+  }
+  __syncthreads();
+}
 template <int kR, class Op>
 __device__ __forceinline__ void gv_run(Op &op, float *red) {
   constexpr int S = kGvWarps / kR;

@@ -63,34 +63,6 @@ __device__ __forceinline__ void load_rows(uint4 (&ra)[kSteps], uint4 (&rb)[kStep
     }
 }
 
-// The groups that got rows, in unit order: the shared expert (group E) first,
-// then the routed experts in index order.  Copies the offsets; block-wide.
-// An invalid partition is reported and leaves no groups.
-__device__ __forceinline__ void touched_groups(const SmallArgs &a, int *s_off, int *s_grp,
-                                               int *s_ng, int kid) {
-  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldcg(a.offsets + i);
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int n = a.n_shared ? 1 : 0;
-    bool bad = s_off[0] != 0 || s_off[a.E] != a.A;
-    for (int base = 0; base < a.E; base += 32) {
-      const int e = base + lane;
-      const int rows = e < a.E ? s_off[e + 1] - s_off[e] : 0;
-      bad = bad || rows < 0;
-      const unsigned m = __ballot_sync(0xffffffffu, rows > 0);
-      if (rows > 0) s_grp[n + __popc(m & ((1u << lane) - 1u))] = e;
-      n += __popc(m);
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      if (a.n_shared) s_grp[0] = a.E;
-      *s_ng = bad ? 0 : n;
-      if (bad && blockIdx.x == 0) report_error(a.status, MOE_ERR_DEVICE_BOUNDS, kid * 100 + SITE_INDEX);
-    }
-  }
-  __syncthreads();
-}
 }  // namespace
 
 // gate/up: unit u = (touched group u / (F / 8), features 8 (u % (F / 8)) ..);

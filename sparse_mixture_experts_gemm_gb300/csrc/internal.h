@@ -160,6 +160,16 @@ struct Q4Weights {
   Q4Mat g, u, d, sg, su, sd;
 };
 
+// gemv_small_q4.cu: the small-batch grouped GEMV on 4-bit expert weights
+// (same arguments as the bf16 one; the weight pointers of a are unused)
+struct SmallQ4Args {
+  SmallArgs a;
+  Q4Weights w;
+};
+cudaError_t launch_small_gateup_q4(const SmallQ4Args &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_small_down_q4(const SmallQ4Args &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t small_gemv_q4_set_attr();
+
 // decode.cu
 struct DecodeArgs {
   const void *x;

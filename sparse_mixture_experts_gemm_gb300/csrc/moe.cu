@@ -247,6 +247,11 @@ int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w
   return MOE_OK;
 }
 
+// a chunk of Tc bf16 tokens routes in one cluster launch
+bool small_route_ok(int Tc, int d) {
+  return Tc <= kSmallRouteT && static_cast<long long>(Tc) * d * 2 <= kSmallRouteTokBytes;
+}
+
 template <typename T>
 int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st) {
   const moe_config &c = h->cfg;
@@ -256,8 +261,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
 
   // route_ctl is zero here: create cleared it and every router launch clears
   // what it used (counts, ticket, the GEMMs' tile counters) when it is done
-  const bool small = sizeof(T) == 2 && Tc <= kSmallRouteT &&
-                     static_cast<long long>(Tc) * d * 2 <= kSmallRouteTokBytes;
+  const bool small = sizeof(T) == 2 && small_route_ok(Tc, d);
   if (small) {
     // a few tokens: routing and placement in one cluster launch
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
@@ -278,7 +282,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
     MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st));
   }
-  if (small && !h->q4 && small_gemv_fits(Tc, d, F)) {
+  if (small && small_gemv_fits(Tc, d, F)) {
     // every touched expert gets one or two rows: grouped GEMV over all SMs
     const bool pdl = !h->prof;  // event records between kernels would break the chain
     SmallArgs sa;
@@ -300,13 +304,18 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     sa.A = A;
     sa.n_shared = c.n_shared;
     sa.status = h->status;
+    SmallQ4Args qa;
+    qa.a = sa;
+    qa.w = h->qw;
     {
       ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
-      MOE_TRY(launch_small_gateup(sa, h->num_sms, st, pdl));
+      MOE_TRY(h->q4 ? launch_small_gateup_q4(qa, h->num_sms, st, pdl)
+                    : launch_small_gateup(sa, h->num_sms, st, pdl));
     }
     {
       ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
-      MOE_TRY(launch_small_down(sa, h->num_sms, st, pdl));
+      MOE_TRY(h->q4 ? launch_small_down_q4(qa, h->num_sms, st, pdl)
+                    : launch_small_down(sa, h->num_sms, st, pdl));
     }
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
@@ -613,7 +622,8 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
       (gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess ||
-       route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess))
+       route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
+       small_gemv_q4_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
   if (rc != MOE_OK) {
     moe_destroy(h);
@@ -694,7 +704,14 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
   char *ob = static_cast<char *>(out);
   if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (h->q4 && T != 1 && !h->q4_prefill) return MOE_ERR_UNSUPPORTED;
+  // 4-bit layers whose d or F the grouped GEMMs do not take run batches only
+  // where every chunk takes the small-batch kernels
+  if (h->q4 && T != 1 && !h->q4_prefill) {
+    const int c0 = std::min(T, h->cfg.max_tokens);
+    if (T > kSmallRouteT || !small_route_ok(c0, h->cfg.d_model) ||
+        !small_gemv_fits(c0, h->cfg.d_model, h->cfg.d_ff))
+      return MOE_ERR_UNSUPPORTED;
+  }
   if (T == 1) {
     return h->cfg.dtype == MOE_BF16
                ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),

@@ -172,19 +172,23 @@ def test_q4_layer_stack_in_a_cuda_graph(dev):
 
 def test_q4_batches_need_d_and_f_multiples_of_512(dev):
     """The grouped GEMMs read scale/bias rows of 16-byte pitch: a layer with
-    F = 256 runs one token at a time and refuses batches."""
+    F = 256 runs batches only where every chunk takes the small-batch kernels
+    (at most 16 tokens) and refuses larger ones."""
     w = synth.q4_layer_weights(9, 1024, 256, 16, 1, dev)
-    x = H.margined_tokens(10, 2, w["Wr"], 4, "bf16", device=dev)
-    layer = moe.Q4Layer(w, 4, max_tokens=8)
+    x = H.margined_tokens(10, 20, w["Wr"], 4, "bf16", device=dev)
+    layer = moe.Q4Layer(w, 4, max_tokens=32)
     try:
-        out = torch.empty((2, 1024), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((20, 1024), dtype=torch.bfloat16, device=dev)
         with pytest.raises(moe.MoeError) as e:
-            moe.moe_forward(layer.handle, x, 2, out)
+            moe.moe_forward(layer.handle, x, 20, out)
         assert e.value.code == moe.MOE_ERR_UNSUPPORTED
-        layer.forward(x[0:1].clone())
+        got = layer.forward(x[:2].clone())
+        torch.cuda.synchronize()
         assert layer.status()[0] == 0
     finally:
         layer.close()
+    ref, *_ = _oracle_q4(x[:2], w, 4, 256)
+    assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
 
 
 # (d, F, E, k, n_shared, T, max_tokens)
@@ -241,3 +245,44 @@ def test_q4_prefill_4k_sample_against_oracle(dev):
     ref, *_ = _oracle_q4(x, w, k, F, rows=keep)
     err = H.row_rel_err(out[torch.as_tensor(keep, device=dev)], ref)
     assert err.max() <= H.OUT_TOL, err.max()
+
+
+@pytest.mark.parametrize("T", [2, 7, 16])
+def test_q4_small_batch_path(dev, T):
+    """Batches of at most 16 tokens on 4-bit weights take the small-batch
+    kernels (one routing launch, the 4-bit grouped GEMV, the combine): the
+    full-size layer against the oracle, every output, and the kernel kinds."""
+    d, F, E, k = 2048, 512, 256, 8
+    w = synth.q4_layer_weights(60 + T, d, F, E, 1, dev)
+    x = H.margined_tokens(70 + T, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k, max_tokens=64)
+    try:
+        moe.moe_profile(layer.handle, True)
+        got = layer.forward(x)
+        moe.moe_profile(layer.handle, False)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+        kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
+        assert kinds == {"router", "gemm_gate_up", "gemm_down", "combine"}, kinds
+    finally:
+        layer.close()
+    ref, *_ = _oracle_q4(x, w, k, F)
+    assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
+
+
+def test_q4_small_batch_crowded_experts(dev):
+    """4-bit small batch with routed groups of more than 8 tokens and F = 128
+    (one 128-column super-step in the down projection)."""
+    d, F, E, k, T = 256, 128, 4, 2, 16
+    w = synth.q4_layer_weights(80, d, F, E, 1, dev)
+    x = H.margined_tokens(81, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k, max_tokens=16)
+    try:
+        got = layer.forward(x)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+    ref, *_ = _oracle_q4(x, w, k, F)
+    assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
+
