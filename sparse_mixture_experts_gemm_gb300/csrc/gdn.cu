@@ -76,14 +76,25 @@ struct GdnArgs {
 };
 
 // Tables of one 8-token block (tokens i, l = 0..7 of the block), stored by
-// l so that the chain reads one contiguous row per token.
-struct BlockTab {
+// l so that the chain reads whole rows (16-byte vectors; the zeros outside
+// the triangles make the full-row updates exact).
+struct alignas(16) BlockTab {
   float C[kB][kB];   // [l][i] = g(i, l) (k_i . k_l), l < i (0 elsewhere)
   float D[kB][kB];   // [l][i] = g(i + 1, l) (q_i . k_l), l <= i (0 elsewhere)
-  float A[kB + 1];   // A_i = alpha_0 .. alpha_{i-1}
+  float A[kB + 4];   // A_i = alpha_0 .. alpha_{i-1}, i = 0..8 (then padding)
   float E[kB];       // g(8, l)
   float al[kB], be[kB];
 };
+static_assert(sizeof(BlockTab) % 16 == 0 && offsetof(BlockTab, A) % 16 == 0 &&
+                  offsetof(BlockTab, E) % 16 == 0 && offsetof(BlockTab, al) % 16 == 0 &&
+                  offsetof(BlockTab, be) % 16 == 0,
+              "the chain reads the tables as 16-byte vectors");
+
+__device__ __forceinline__ void ld8(const float *p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
 struct Stage {
   alignas(16) __nv_bfloat16 k[kTb][kRow];
@@ -335,19 +346,26 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
         }
       }
       // the chain, right-looking, for column jc
-      float R[kB], O[kB], u[kB];
+      float R[kB], O[kB], u[kB], Av[kB], alv[kB], bev[kB];
+      ld8(tb.A, Av);  // A_0 .. A_7
+      const float a8 = reinterpret_cast<const float4 *>(tb.A + kB)->x;  // A_8 (16-byte aligned)
+      ld8(tb.al, alv);
+      ld8(tb.be, bev);
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        R[i] = tb.A[i] * p[i];
-        O[i] = tb.A[i + 1] * q[i];
+        R[i] = Av[i] * p[i];
+        O[i] = (i + 1 < kB ? Av[i + 1] : a8) * q[i];
       }
 #pragma unroll
       for (int l = 0; l < kB; ++l) {
-        u[l] = tb.be[l] * fmaf(-tb.al[l], R[l], __bfloat162float(S.v[tb0 + l][jc]));
+        u[l] = bev[l] * fmaf(-alv[l], R[l], __bfloat162float(S.v[tb0 + l][jc]));
+        float cr[kB], dr[kB];
+        ld8(tb.C[l], cr);
+        ld8(tb.D[l], dr);
 #pragma unroll
-        for (int i = l + 1; i < kB; ++i) R[i] = fmaf(tb.C[l][i], u[l], R[i]);
+        for (int i = l + 1; i < kB; ++i) R[i] = fmaf(cr[i], u[l], R[i]);
 #pragma unroll
-        for (int i = l; i < kB; ++i) O[i] = fmaf(tb.D[l][i], u[l], O[i]);
+        for (int i = l; i < kB; ++i) O[i] = fmaf(dr[i], u[l], O[i]);
       }
       // warp w writes tokens 2w, 2w + 1 of the 16 columns
       if (lane < kCols) {
@@ -377,7 +395,6 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
       split_tf32(w1, wh[1], wl[1]);  // a1 = (g + 8, k c)
       split_tf32(w4, wh[2], wl[2]);  // a2 = (g, k c + 4)
       split_tf32(w5, wh[3], wl[3]);  // a3 = (g + 8, k c + 4)
-      const float a8 = tb.A[kB];
 #pragma unroll
       for (int nn = 0; nn < kChunks; ++nn) {
         const int m = ch0 + nn;
