@@ -123,8 +123,8 @@ def make_layer(cfg: dict, dev, seed: int):
 # DRAM bytes of one batch-1 layer (kernels A + B + C, reads; nothing is
 # written back during them), from the ncu capture in profiles/decode_layer.md.
 DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
-# The same for the 4-bit layer: not captured yet.
-DECODE_Q4_TRAFFIC_LAYER = None
+# The same for the 4-bit layer, from profiles/decode_q4_layer.md.
+DECODE_Q4_TRAFFIC_LAYER = 1_081_344 + 10_664_960 + 5_347_584
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
 # ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
 GEMM1_TRAFFIC_4K = 1_094_968_000 + 8_866_304
