@@ -135,3 +135,9 @@ def test_state_in_place_and_empty_scan(dev):
     _, z = moe.gdn_scan(e["q"], e["k"], e["v"], e["alpha"], e["beta"], None)
     torch.cuda.synchronize()
     assert torch.equal(s0, inp["state"]) and not z.any()
+
+
+@pytest.mark.parametrize("Hk,Hv,dv", [(2, 16, 32), (8, 8, 16)])
+def test_scan_head_groupings(dev, Hk, Hv, dv):
+    """Eight value heads per key head, and one per key head with eight heads."""
+    run(dev, 200 + Hv, 77, Hk, Hv, dv, state=True)

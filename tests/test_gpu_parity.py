@@ -266,3 +266,31 @@ def test_small_batch_crowded_experts(dev, T, E, k, n_shared):
     """Small batches whose routed experts get more than 8 tokens (the second
     column block of the grouped GEMV), with and without the shared expert."""
     run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=16)
+
+
+def test_chunked_prefill_with_a_small_tail(dev):
+    """A 1,000-token batch on a 248-token handle: four full chunks on the
+    grouped GEMMs, then an 8-token tail on the small-batch kernels; every
+    output against the oracle."""
+    run_case(dev, 91, 1000, 512, 128, 32, 4, max_tokens=248)
+
+
+def test_small_batch_beyond_the_router_limit(dev):
+    """16 tokens of d = 8192 (256 KB of tokens) do not fit the small router's
+    shared memory: the batch takes the tensor-core router and grouped GEMMs."""
+    d, F, E, k, T = 8192, 128, 16, 2, 16
+    w = synth.layer_weights(92, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(93, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=T)
+    try:
+        moe.moe_profile(layer.handle, True)
+        out = layer.forward(x)
+        moe.moe_profile(layer.handle, False)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+        kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
+        assert "permute" in kinds, kinds
+    finally:
+        layer.close()
+    ref, *_ = H.oracle_forward(x, w, k)
+    assert H.row_rel_err(out, ref).max() <= H.OUT_TOL
