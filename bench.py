@@ -315,6 +315,9 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dic
 
 
 GDN = {"T": 2048, "Hk": 16, "Hv": 32, "dk": 128, "dv": 128, "seed": 31}
+# DRAM bytes (read + write) of one scan launch on that workload, from the ncu
+# capture summarised in profiles/gdn_scan_2k.md (same kernel build)
+GDN_TRAFFIC_2K = 36_199_168 + 222_720
 
 
 def bench_gdn(dev, flush_buf, pk, iters=20, cpu_tokens=64) -> dict:
@@ -352,7 +355,7 @@ def bench_gdn(dev, flush_buf, pk, iters=20, cpu_tokens=64) -> dict:
         "us_per_token": us / c["T"],
         "roofline": {"bound": "alu", "achieved": 2 * fma / (us * 1e-6) / 1e12, "peak": peak,
                      "unit": "TFLOP/s", "frac": 2 * fma / (us * 1e-6) / 1e12 / peak,
-                     "traffic": None, "algorithmic_bytes": byts,
+                     "traffic": GDN_TRAFFIC_2K, "algorithmic_bytes": byts,
                      "hbm_frac_of_measured": byts / (us * 1e-6) / (pk["hbm"] * 1e9),
                      "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (nominal)"},
         "clocks": clk.summary(), "gpu_launches": iters,
