@@ -277,6 +277,23 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
     }
 
 
+def slowest_rank_ms(total_ms: float, steps: int, world: int, device=None) -> float:
+    """Mean step time of the slowest rank: each rank passes the sum of its
+    timed steps, the MAX over ranks (all_reduce on the default process group)
+    is divided by the step count.  One rank: its own mean."""
+    if world <= 1:
+        return total_ms / steps
+    import torch.distributed as dist
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item() / steps
+
+
+def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Units all ranks process per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dict:
     """Batches of 2..16 tokens through the same layer (the verification shape
     of speculative decoding): one routing launch, the grouped GEMV on all SMs,
@@ -573,14 +590,9 @@ def main():
     res = bench_prefill(cfg, dev, args.steps, args.warmup, flush_buf)
     T = cfg["T"]
     ms = statistics.mean(res["times"])
-    ms_max = ms
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([sum(res["times"])], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = tt.item() / len(res["times"])
-    value = world * T / (ms_max / 1e3)
-    e2e_ms = statistics.mean(res["e2e_times"])
+    ms_max = slowest_rank_ms(sum(res["times"]), len(res["times"]), world, dev)
+    value = whole_job_rate(T, ms_max, world)
+    e2e_ms = slowest_rank_ms(sum(res["e2e_times"]), len(res["e2e_times"]), world, dev)
 
     counts = np.sum(res["counts"], axis=0) if len(res["counts"]) == 1 else None
     work = [algorithmic_prefill(cfg, c, min(cfg["chunk"], T - i * cfg["chunk"]))
@@ -635,7 +647,7 @@ def main():
         },
         "kernels_ms_per_step": {k_: v[0] / max(args.steps, 1) for k_, v in res["prof"].items()
                                 if v[1] > 0},
-        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(T, e2e_ms, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": res["clocks"],
