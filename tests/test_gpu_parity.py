@@ -294,3 +294,9 @@ def test_small_batch_beyond_the_router_limit(dev):
         layer.close()
     ref, *_ = H.oracle_forward(x, w, k)
     assert H.row_rel_err(out, ref).max() <= H.OUT_TOL
+
+
+def test_small_batch_partial_router_cluster(dev):
+    """40 experts: a cluster of three router CTAs, the last one holding only
+    8 experts (its other warps clamp to a valid row and write nothing)."""
+    run_case(dev, 94, 11, 512, 128, 40, 6, n_shared=1, max_tokens=16)

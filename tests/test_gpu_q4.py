@@ -286,3 +286,19 @@ def test_q4_small_batch_crowded_experts(dev):
     ref, *_ = _oracle_q4(x, w, k, F)
     assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
 
+
+
+def test_q4_small_batch_without_shared_expert(dev):
+    """4-bit small batch with no shared expert and 40 experts (a partial router CTA)."""
+    d, F, E, k, T = 512, 256, 40, 4, 9
+    w = synth.q4_layer_weights(82, d, F, E, 0, dev)
+    x = H.margined_tokens(83, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.Q4Layer(w, k, max_tokens=16)
+    try:
+        got = layer.forward(x)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+    ref, *_ = _oracle_q4(x, w, k, F)
+    assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
