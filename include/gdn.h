@@ -45,11 +45,13 @@ extern "C" {
  *              state_in (each column is read before it is written)
  *   o          bf16 [T][n_v_heads][d_v], round-to-nearest of the fp32 result
  * Supported: d_k == 128, d_v a multiple of 16, n_v_heads a multiple of
- * n_k_heads, T >= 0 (T == 0 copies state_in to state_out); q, k, v, state
- * pointers 16-byte aligned.
+ * n_k_heads, T >= 0 (T == 0 copies state_in to state_out).
  * Returns MOE_OK; MOE_ERR_INVALID_ARG for NULL required pointers, negative
  * sizes or a head count that does not divide; MOE_ERR_UNSUPPORTED for other
- * dimensions; MOE_ERR_CUDA if a launch fails (nothing is written then).
+ * dimensions; MOE_ERR_ALIGNMENT unless q, k, v are 16-byte aligned, the
+ * state pointers 8-byte, alpha and beta 4-byte and o 2-byte aligned;
+ * MOE_ERR_CUDA if a launch fails (nothing is written then).  All checks are
+ * made on the host before anything is launched.
  * Device-side faults are not produced by this kernel (it waits on nothing
  * but block barriers). */
 int gdn_scan(const void *q, const void *k, const void *v, const float *alpha, const float *beta,

@@ -429,6 +429,13 @@ extern "C" int gdn_scan(const void *q, const void *k, const void *v, const float
   if (n_v_heads % n_k_heads != 0) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!q || !k || !v || !alpha || !beta || !o)) return MOE_ERR_INVALID_ARG;
   if (d_k != kDk || d_v % kCols != 0) return MOE_ERR_UNSUPPORTED;
+  // 16-byte copies of q, k, v rows; 8-byte state reads and writes; 4-byte gates
+  auto misaligned = [](const void *ptr, uintptr_t n) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) % n) != 0;
+  };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(state_in, 8) ||
+      misaligned(state_out, 8) || misaligned(alpha, 4) || misaligned(beta, 4) || misaligned(o, 2))
+    return MOE_ERR_ALIGNMENT;
   if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sizeof(GdnSmem))) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -161,6 +161,9 @@ def test_quantize_q4_validates_on_host(lib, args, code):
     (dict(alpha=None), moe.MOE_ERR_INVALID_ARG),
     (dict(dk=64), moe.MOE_ERR_UNSUPPORTED),
     (dict(dv=24), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=0x2008), moe.MOE_ERR_ALIGNMENT),
+    (dict(s_in=0x7004), moe.MOE_ERR_ALIGNMENT),
+    (dict(beta=0x5002), moe.MOE_ERR_ALIGNMENT),
 ])
 def test_gdn_scan_rejects_before_any_launch(lib, args, code):
     """Validation happens on the host, before anything touches a GPU."""
