@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
     cp_async_wait_group<1>();  // this block's copies have landed
     __syncthreads();
     const Stage &S = sm.st[b & 1];
-    block_tables(S, sm.tab[warp], warp, lane);  // one warp per 8-token block
+    if (warp < kSub) block_tables(S, sm.tab[warp], warp, lane);  // one warp per 8-token block
     __syncthreads();
 #pragma unroll 1
     for (int sb = 0; sb * kB < n; ++sb, ++it) {
