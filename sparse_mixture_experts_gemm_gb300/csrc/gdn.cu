@@ -35,12 +35,13 @@
 // it the state entries it already holds (k = c and c + 4 from positions 2 c
 // and 2 c + 1) and the key rows are read with the same mapping.
 //
-// The chain.  The warps' partial P and Q meet in shared memory (one barrier
-// per 8 tokens, two buffers); then every warp runs the chain for all 16
-// columns, one column per lane (lanes 16..31 repeat 0..15), right-looking:
-// once u_l is known it enters every later recall and every output at once.
-// Only the u_i form a chain.  The coefficient tables come from the block's Gram
-// products q_i . k_l and k_i . k_l on bf16 MMAs (exact products, fp32 sums).
+// The chain.  The warps' partial P and Q meet in shared memory (two buffers);
+// warp 0 alone sums them, runs the chain for the 16 columns, one column per
+// lane (right-looking: once u_l is known it enters every later recall and
+// every output at once; only the u_i form a chain), writes the outputs and
+// leaves g(8, l) u_l in shared memory for the update, which all four warps
+// then apply to their quarters (two barriers per 8 tokens).  Running the
+// chain in one warp instead of four halves the instructions the CTA issues.
 //
 // Staging.  The CTA copies the bf16 q and k of its key head, its v columns
 // and the gates of the next 32 tokens by cp.async into the second of two
@@ -110,6 +111,7 @@ struct GdnSmem {
   // [buffer][warp][P, Q][column][token] partial sums; rows of 12 floats so
   // that the 8 columns a quarter-warp reads start in different banks
   float part[2][kWarps][2][kCols][kB + 4];
+  alignas(16) float wu[kCols][kB + 4];  // g(8, l) u_l of the 16 columns (rows padded as part)
 };
 static_assert(offsetof(Stage, q) % 16 == 0 && offsetof(Stage, v) % 16 == 0 &&
                   sizeof(Stage) % 16 == 0 && (kRow * 2) % 16 == 0,
@@ -244,7 +246,7 @@ __device__ __forceinline__ void block_tables(const Stage &s, BlockTab &tb, int w
 // grid: (H_v * d_v) / kCols CTAs of 4 warps; CTA b scans columns kCols b ..
 // of value head (kCols b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) of warp w
 // holds columns j0 + g and j0 + g + 8 at d_k chunks 4 w ..
-__global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
+__global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
   extern __shared__ __align__(16) uint8_t s_raw[];
   GdnSmem &sm = *reinterpret_cast<GdnSmem *>(s_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
@@ -325,71 +327,64 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(GdnArgs a) {
                         (acc[0][y][3] + acc[0][y + 1][3]) + (acc[1][y][3] + acc[1][y + 1][3]));
       }
       __syncthreads();
-      // P, Q of column jc at the 8 tokens, summed over the warps in order
-      float p[kB], q[kB];
+      if (warp == 0) {
+        // P, Q of column jc at the 8 tokens, summed over the warps in order
+        float p[kB], q[kB];
 #pragma unroll
-      for (int i = 0; i < kB; ++i) p[i] = q[i] = 0.0f;
+        for (int i = 0; i < kB; ++i) p[i] = q[i] = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const float4 pv = *reinterpret_cast<const float4 *>(&pt[w][0][jc][4 * hf]);
-          const float4 qv = *reinterpret_cast<const float4 *>(&pt[w][1][jc][4 * hf]);
-          p[4 * hf] += pv.x;
-          p[4 * hf + 1] += pv.y;
-          p[4 * hf + 2] += pv.z;
-          p[4 * hf + 3] += pv.w;
-          q[4 * hf] += qv.x;
-          q[4 * hf + 1] += qv.y;
-          q[4 * hf + 2] += qv.z;
-          q[4 * hf + 3] += qv.w;
+          for (int hf = 0; hf < 2; ++hf) {
+            const float4 pv = *reinterpret_cast<const float4 *>(&pt[w][0][jc][4 * hf]);
+            const float4 qv = *reinterpret_cast<const float4 *>(&pt[w][1][jc][4 * hf]);
+            p[4 * hf] += pv.x;
+            p[4 * hf + 1] += pv.y;
+            p[4 * hf + 2] += pv.z;
+            p[4 * hf + 3] += pv.w;
+            q[4 * hf] += qv.x;
+            q[4 * hf + 1] += qv.y;
+            q[4 * hf + 2] += qv.z;
+            q[4 * hf + 3] += qv.w;
+          }
+        }
+        // the chain, right-looking, for column jc
+        float R[kB], O[kB], u[kB], Av[kB], alv[kB], bev[kB], ev[kB];
+        ld8(tb.A, Av);  // A_0 .. A_7
+        const float a8v = reinterpret_cast<const float4 *>(tb.A + kB)->x;  // A_8 (16-byte aligned)
+        ld8(tb.al, alv);
+        ld8(tb.be, bev);
+        ld8(tb.E, ev);
+#pragma unroll
+        for (int i = 0; i < kB; ++i) {
+          R[i] = Av[i] * p[i];
+          O[i] = (i + 1 < kB ? Av[i + 1] : a8v) * q[i];
+        }
+#pragma unroll
+        for (int l = 0; l < kB; ++l) {
+          u[l] = bev[l] * fmaf(-alv[l], R[l], __bfloat162float(S.v[tb0 + l][jc]));
+          float cr[kB], dr[kB];
+          ld8(tb.C[l], cr);
+          ld8(tb.D[l], dr);
+#pragma unroll
+          for (int i = l + 1; i < kB; ++i) R[i] = fmaf(cr[i], u[l], R[i]);
+#pragma unroll
+          for (int i = l; i < kB; ++i) O[i] = fmaf(dr[i], u[l], O[i]);
+        }
+        if (lane < kCols) {
+#pragma unroll
+          for (int i = 0; i < kB; ++i)
+            if (tb0 + i < n) ob[(t0 + tb0 + i) * ostride] = __float2bfloat16_rn(O[i]);
+          float4 *dst = reinterpret_cast<float4 *>(&sm.wu[jc][0]);
+          dst[0] = make_float4(ev[0] * u[0], ev[1] * u[1], ev[2] * u[2], ev[3] * u[3]);
+          dst[1] = make_float4(ev[4] * u[4], ev[5] * u[5], ev[6] * u[6], ev[7] * u[7]);
         }
       }
-      // the chain, right-looking, for column jc
-      float R[kB], O[kB], u[kB], Av[kB], alv[kB], bev[kB];
-      ld8(tb.A, Av);  // A_0 .. A_7
-      const float a8 = reinterpret_cast<const float4 *>(tb.A + kB)->x;  // A_8 (16-byte aligned)
-      ld8(tb.al, alv);
-      ld8(tb.be, bev);
-#pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        R[i] = Av[i] * p[i];
-        O[i] = (i + 1 < kB ? Av[i + 1] : a8) * q[i];
-      }
-#pragma unroll
-      for (int l = 0; l < kB; ++l) {
-        u[l] = bev[l] * fmaf(-alv[l], R[l], __bfloat162float(S.v[tb0 + l][jc]));
-        float cr[kB], dr[kB];
-        ld8(tb.C[l], cr);
-        ld8(tb.D[l], dr);
-#pragma unroll
-        for (int i = l + 1; i < kB; ++i) R[i] = fmaf(cr[i], u[l], R[i]);
-#pragma unroll
-        for (int i = l; i < kB; ++i) O[i] = fmaf(dr[i], u[l], O[i]);
-      }
-      // warp w writes tokens 2w, 2w + 1 of the 16 columns
-      if (lane < kCols) {
-#pragma unroll
-        for (int i = 0; i < kB; ++i)
-          if ((i >> 1) == warp && tb0 + i < n) ob[(t0 + tb0 + i) * ostride] = __float2bfloat16_rn(O[i]);
-      }
+      __syncthreads();  // the scaled deltas are in shared memory
       // S <- A_8 S + W K with W[col][l] = g(8, l) u_l: A operand rows g, g + 8,
-      // k = token c and c + 4 (u of column g from lane g, of g + 8 from lane g + 8)
-      float w0 = 0.f, w1 = 0.f, w4 = 0.f, w5 = 0.f;
-#pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        const float eu = tb.E[i] * u[i];
-        const float x = __shfl_sync(0xffffffffu, eu, g);
-        const float y = __shfl_sync(0xffffffffu, eu, g + 8);
-        if (i == c) {
-          w0 = x;
-          w1 = y;
-        }
-        if (i == c + 4) {
-          w4 = x;
-          w5 = y;
-        }
-      }
+      // k = token c and c + 4
+      const float w0 = sm.wu[g][c], w1 = sm.wu[g + 8][c], w4 = sm.wu[g][c + 4], w5 = sm.wu[g + 8][c + 4];
+      const float a8 = reinterpret_cast<const float4 *>(tb.A + kB)->x;
       uint32_t wh[4], wl[4];
       split_tf32(w0, wh[0], wl[0]);  // a0 = (g, k c)
       split_tf32(w1, wh[1], wl[1]);  // a1 = (g + 8, k c)
