@@ -107,7 +107,7 @@ struct Stage {
 
 struct GdnSmem {
   Stage st[2];
-  BlockTab tab[kSub];
+  BlockTab tab[2][kSub];  // by staged-block parity
   // [buffer][warp][P, Q][column][token] partial sums; rows of 12 floats so
   // that the 8 columns a quarter-warp reads start in different banks
   float part[2][kWarps][2][kCols][kB + 4];
@@ -274,21 +274,26 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
   __nv_bfloat16 *ob = a.o + static_cast<long long>(h) * a.dv + j0 + jc;
   const long long ostride = static_cast<long long>(a.Hv) * a.dv;
   int it = 0;  // 8-token blocks done (selects the partial-sum buffer)
-  if (nblk > 0) stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, tid);
+  // The first staged block's copies and tables up front; those of block b + 1
+  // during block b: its copies are issued at b's start, every thread waits
+  // for its own before the first barrier of b's third 8-token block (every
+  // block but the last is whole), and warps 1..3 build the tables while warp
+  // 0 runs the chains of b's third and fourth 8-token blocks.
+  if (nblk > 0) {
+    stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, tid);
+    cp_async_wait_group<0>();
+    __syncthreads();
+    if (warp < kSub) block_tables(sm.st[0], sm.tab[0][warp], warp, lane);
+    __syncthreads();
+  }
   for (int b = 0; b < nblk; ++b) {
     const int t0 = b * kTb, n = min(kTb, a.T - t0);
-    if (b + 1 < nblk)
-      stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, tid);
-    else
-      cp_async_commit();  // an empty group keeps the count below uniform
-    cp_async_wait_group<1>();  // this block's copies have landed
-    __syncthreads();
+    const bool next = b + 1 < nblk;
+    if (next) stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, tid);
     const Stage &S = sm.st[b & 1];
-    if (warp < kSub) block_tables(S, sm.tab[warp], warp, lane);  // one warp per 8-token block
-    __syncthreads();
 #pragma unroll 1
     for (int sb = 0; sb * kB < n; ++sb, ++it) {
-      const BlockTab &tb = sm.tab[sb];
+      const BlockTab &tb = sm.tab[b & 1][sb];
       const int tb0 = sb * kB;
       // this warp's part of P = S K^T and Q = S Q^T (hi and lo parts of the
       // state, even and odd chunks in separate accumulators)
@@ -326,7 +331,15 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
             make_float2((acc[0][y][2] + acc[0][y + 1][2]) + (acc[1][y][2] + acc[1][y + 1][2]),
                         (acc[0][y][3] + acc[0][y + 1][3]) + (acc[1][y][3] + acc[1][y + 1][3]));
       }
+      // (a block with a successor is whole: it has 8-token blocks 0..3)
+      if (next && sb == 2) cp_async_wait_group<0>();  // block b + 1's copies, this thread's
       __syncthreads();
+      if (next && sb >= 2 && warp > 0) {
+        // the next block's tables, one per warp and 8-token block, while warp
+        // 0 runs this block's chain: tables 0..2 now, table 3 in the next one
+        const int w = sb == 2 ? warp - 1 : (warp == 1 ? 3 : -1);
+        if (w >= 0) block_tables(sm.st[(b + 1) & 1], sm.tab[(b + 1) & 1][w], w, lane);
+      }
       if (warp == 0) {
         // P, Q of column jc at the 8 tokens, summed over the warps in order
         float p[kB], q[kB];
