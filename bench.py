@@ -334,7 +334,7 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dic
 GDN = {"T": 2048, "Hk": 16, "Hv": 32, "dk": 128, "dv": 128, "seed": 31}
 # DRAM bytes (read + write) of one scan launch on that workload, from the ncu
 # capture summarised in profiles/gdn_scan_2k.md (same kernel build)
-GDN_TRAFFIC_2K = 36_199_168 + 222_720
+GDN_TRAFFIC_2K = 36_200_448 + 293_888
 
 
 def bench_gdn(dev, flush_buf, pk, iters=20, cpu_tokens=64) -> dict:
