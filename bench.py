@@ -14,7 +14,11 @@ one layer over a 2K-token prompt under "gdn".
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; a 256 MiB buffer is written between timed
-steps to flush L2 (outside the events).  Multi-GPU (torchrun): every rank runs
+steps to flush L2 (outside the events).  The per-kernel split (and the
+roofline's kernel duration) comes from a second pass of K steps with events
+around every kernel.  End to end ("e2e"): K steps through the host-buffer call
+issued back to back, each copying its batch in from pinned host memory and its
+result out, with one event pair around all of them.  Multi-GPU (torchrun): every rank runs
 its own replica (tokens are independent; no collective on the data path),
 value = all ranks' tokens / the slowest rank's time ("scaling": "weak").
 The reference arm (--impl reference) times the CPU oracle on the host cores on
@@ -153,6 +157,31 @@ def flush_l2(buf):
 
 
 # ------------------------------------------------------------------ our arm
+def timed_steps(layer, x, out, steps, flush_buf, st, profile=False):
+    """Per-step milliseconds of `steps` forwards, L2 flushed before each
+    (outside the events).  profile: also time every kernel with the library's
+    events on the launching stream and return {kind: (ms, launches)} as well.
+    Those events make the front end drain before each next launch, so a
+    profiled step runs longer than a plain one; the plain times are the step
+    times, the profiled ones give the per-kernel split."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    if profile:
+        moe.moe_profile(layer.handle, True)
+    for i in range(steps):
+        flush_l2(flush_buf)
+        evs[i][0].record(st)
+        layer.forward(x, out)
+        evs[i][1].record(st)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    if not profile:
+        return times
+    prof = moe.moe_profile_read(layer.handle)
+    moe.moe_profile(layer.handle, False)
+    return times, prof
+
+
 def bench_prefill(cfg, dev, steps, warmup, flush_buf):
     layer, w, bias = make_layer(cfg, dev, cfg["seed"])
     T = cfg["T"]
@@ -171,47 +200,71 @@ def bench_prefill(cfg, dev, steps, warmup, flush_buf):
         chunk_counts.append(cnt.cpu().numpy())
     torch.cuda.synchronize()
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    moe.moe_profile(layer.handle, True)
     with Clocks(dev.index or 0) as clk:
-        for i in range(steps):
-            flush_l2(flush_buf)
-            evs[i][0].record(st)
-            layer.forward(x, out)
-            evs[i][1].record(st)
-        torch.cuda.synchronize()
-    prof = moe.moe_profile_read(layer.handle)
-    moe.moe_profile(layer.handle, False)
+        times = timed_steps(layer, x, out, steps, flush_buf, st)
+    times_prof, prof = timed_steps(layer, x, out, steps, flush_buf, st, profile=True)
     rc, det = layer.status()
     if rc != 0:
         raise RuntimeError(f"device status {rc} ({det}) in timed region")
-    times = [a.elapsed_time(b) for a, b in evs]
 
-    # end to end through the public call with host buffers
-    xh = x.cpu().pin_memory()
-    oh = torch.empty_like(xh).pin_memory()
+    # end to end through the host-buffer call (moe_forward_host): every step
+    # copies its batch in from pinned host memory and its result back out, and
+    # the handle overlaps one batch's copies with its neighbours' forwards.
+    # Two batches (the tokens and a permutation of them) alternate.
+    xh = [x.cpu().pin_memory(), x.roll(1, 0).cpu().pin_memory()]
+    oh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
+    for i in range(max(3, warmup)):
+        layer.forward_host(xh[i % 2], oh[i % 2])
+    layer.host_join()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(steps):
+        layer.forward_host(xh[i % 2], oh[i % 2])
+    layer.host_join()
+    b.record(st)
+    torch.cuda.synchronize()
+    e2e_times = [a.elapsed_time(b) / steps] * steps
+    rc, det = layer.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} ({det}) in the end-to-end steps")
+
+    # the copies alone, for comparison with the step time
+    c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    xd_ = torch.empty_like(x)
+    for _ in range(2):
+        c_ev[0].record(st)
+        xd_.copy_(xh[0], non_blocking=True)
+        c_ev[1].record(st)
+        oh[0].copy_(xd_, non_blocking=True)
+        c_ev[2].record(st)
+        torch.cuda.synchronize()
+    copy_ms = {"h2d": c_ev[0].elapsed_time(c_ev[1]), "d2h": c_ev[1].elapsed_time(c_ev[2])}
+
+    # the same one step at a time: copy in, forward, copy out, L2 flushed between
     xd = torch.empty_like(x)
     od = torch.empty_like(x)
     for _ in range(max(1, warmup)):
-        xd.copy_(xh, non_blocking=True)
+        xd.copy_(xh[0], non_blocking=True)
         layer.forward(xd, od)
-        oh.copy_(od, non_blocking=True)
+        oh[0].copy_(od, non_blocking=True)
     torch.cuda.synchronize()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    ser_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
     for i in range(steps):
         flush_l2(flush_buf)
-        e2e_ev[i][0].record(st)
-        xd.copy_(xh, non_blocking=True)
+        ser_ev[i][0].record(st)
+        xd.copy_(xh[0], non_blocking=True)
         layer.forward(xd, od)
-        oh.copy_(od, non_blocking=True)
-        e2e_ev[i][1].record(st)
+        oh[0].copy_(od, non_blocking=True)
+        ser_ev[i][1].record(st)
     torch.cuda.synchronize()
-    e2e_times = [a.elapsed_time(b) for a, b in e2e_ev]
-    res = dict(times=times, prof=prof, clocks=clk.summary(), e2e_times=e2e_times,
-               counts=chunk_counts, h2d=xh.numel() * xh.element_size(),
-               d2h=oh.numel() * oh.element_size(), layer=layer, w=w, bias=bias, x=x)
+    serial_times = [a_.elapsed_time(b_) for a_, b_ in ser_ev]
+    res = dict(times=times, times_prof=times_prof, prof=prof, clocks=clk.summary(),
+               e2e_times=e2e_times,
+               serial_times=serial_times, copy_ms=copy_ms,
+               counts=chunk_counts, h2d=xh[0].numel() * xh[0].element_size(),
+               d2h=oh[0].numel() * oh[0].element_size(), layer=layer, w=w, bias=bias, x=x)
     return res
 
 
@@ -231,25 +284,16 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
         torch.cuda.synchronize()
         _, _, cnt = layer.route(x[:cfg["chunk"]])
         counts = cnt.cpu().numpy()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        moe.moe_profile(layer.handle, True)
         with Clocks(dev.index or 0) as clk:
-            for i in range(steps):
-                flush_l2(flush_buf)
-                evs[i][0].record(st)
-                layer.forward(x, out)
-                evs[i][1].record(st)
-            torch.cuda.synchronize()
-        prof = moe.moe_profile_read(layer.handle)
-        moe.moe_profile(layer.handle, False)
+            times = timed_steps(layer, x, out, steps, flush_buf, st)
+        times_prof, prof = timed_steps(layer, x, out, steps, flush_buf, st, profile=True)
         rc, det = layer.status()
         if rc != 0:
             raise RuntimeError(f"4-bit prefill device status {rc} ({det})")
         small = bench_small_batch(layer, cfg, dev, flush_buf, pk, q4=True)
     finally:
         layer.close()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = statistics.mean(times)
     active = int((counts > 0).sum())
     A = T * k
     flops = 2 * T * d * E + 6 * (A + T) * d * F
@@ -260,6 +304,7 @@ def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
     g1_flops = 4 * (A + T) * d * F
     return {
         "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
+        "ms_per_step_with_kernel_events": statistics.mean(times_prof),
         "workload": f"prefill T={T} (d={d}, {E} experts top-{k} + 1 shared, F={F}), 4-bit "
                     "group-affine expert weights (64 per group, bf16 scale and bias), bf16 "
                     "router and tokens, L2 flushed between steps",
@@ -593,6 +638,7 @@ def main():
     ms_max = slowest_rank_ms(sum(res["times"]), len(res["times"]), world, dev)
     value = whole_job_rate(T, ms_max, world)
     e2e_ms = slowest_rank_ms(sum(res["e2e_times"]), len(res["e2e_times"]), world, dev)
+    serial_ms = slowest_rank_ms(sum(res["serial_times"]), len(res["serial_times"]), world, dev)
 
     counts = np.sum(res["counts"], axis=0) if len(res["counts"]) == 1 else None
     work = [algorithmic_prefill(cfg, c, min(cfg["chunk"], T - i * cfg["chunk"]))
@@ -647,8 +693,21 @@ def main():
         },
         "kernels_ms_per_step": {k_: v[0] / max(args.steps, 1) for k_, v in res["prof"].items()
                                 if v[1] > 0},
+        "kernel_times_from": "a second pass of the same steps with an event pair around every "
+                             "kernel on the launching stream (the events cost the step "
+                             "launch overlap: see ms_per_step_with_kernel_events)",
+        "ms_per_step_with_kernel_events": slowest_rank_ms(sum(res["times_prof"]),
+                                                          len(res["times_prof"]), world, dev),
         "e2e": {"value": whole_job_rate(T, e2e_ms, world), "unit": "tokens/s",
-                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": e2e_ms, "copies_alone_ms": res["copy_ms"],
+                "how": "moe_forward_host on pinned host buffers, steps issued back to back, "
+                       "one moe_host_join, events around all steps; each batch's copies "
+                       "overlap the neighbouring batches' forwards; no L2 flush (each "
+                       f"step reads {bytes_ / 1e9:.3f} GB; L2 holds 0.13 GB)",
+                "serial": {"value": whole_job_rate(T, serial_ms, world), "ms_per_step": serial_ms,
+                           "how": "copy in, moe_forward, copy out per step, L2 flushed "
+                                  "between steps outside the events"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": res["clocks"],
     }

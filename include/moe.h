@@ -183,6 +183,41 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
 int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream);
 
 /*
+ * The whole block on host buffers: out_host[T][d] = MoE(x_host[T][d]), the
+ * same result as moe_forward on device copies of x, bit for bit.  Like
+ * moe_forward it enqueues the work and returns (section "Keep expert routing
+ * on the GPU": no host synchronisation inside the block).  The handle stages
+ * batches through two device slots, used by alternate calls: the copy of
+ * x_host into a slot runs on a copy-in stream of the handle's, the forward on
+ * cuda_stream, the copy into out_host on a copy-out stream of the handle's.
+ * A call's copy-in waits only for the forward two calls back (the slot's
+ * previous user), so the copies of one batch overlap the forward of the
+ * batches next to it.
+ *   x_host, out_host: host, [T][d] in the handle's dtype, not overlapping.
+ *     Page-locked memory (cudaHostAlloc, cudaHostRegister) gives asynchronous
+ *     copies; pageable memory works, but the copies then hold up the host.
+ *   The caller keeps x_host unchanged and out_host untouched until the work
+ *   of a later moe_host_join on some stream has completed.
+ * The first call, and any call with a larger T than all before it, allocates
+ * the slots (2 x 2 x T x d elements of device memory) after draining the copy
+ * streams and cuda_stream.  Calls on one handle must come from one host
+ * thread and use one cuda_stream (the forward's workspace is the handle's).
+ * Errors: INVALID_ARG, UNSUPPORTED (as moe_forward, checked before any copy),
+ * OUT_OF_MEMORY (the slots), CUDA.  T == 0 is a no-op returning MOE_OK.
+ */
+int moe_forward_host(moe_handle *h, const void *x_host, int T, void *out_host,
+                     void *cuda_stream);
+
+/*
+ * Make cuda_stream wait for every copy into a host buffer that
+ * moe_forward_host has issued on this handle; once that stream's work has
+ * completed (cudaStreamSynchronize, an event), all those results are in host
+ * memory.  Asynchronous; a no-op before the first moe_forward_host.
+ * Errors: INVALID_ARG, CUDA.
+ */
+int moe_host_join(moe_handle *h, void *cuda_stream);
+
+/*
  * Synchronise cuda_stream, then return and clear the handle's device status
  * word: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  If
  * detail != NULL it receives a library-defined code naming the kernel and the

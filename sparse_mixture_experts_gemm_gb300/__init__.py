@@ -35,7 +35,8 @@ MOE_F32 = 1
 KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
                 "decode_gate_up", "decode_down"]
 
-EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_status", "moe_destroy",
+EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_host_join",
+            "moe_status", "moe_destroy",
             "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
             "moe_decode_noalloc", "moe_create_q4", "moe_quantize_q4", "gdn_scan"]
 
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
     L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(vp)]
     L.moe_route.argtypes = [vp, vp, ip, vp, vp, vp, vp]
     L.moe_forward.argtypes = [vp, vp, ip, vp, vp]
+    L.moe_forward_host.argtypes = [vp, vp, ip, vp, vp]
+    L.moe_host_join.argtypes = [vp, vp]
     L.moe_status.argtypes = [vp, vp, ctypes.POINTER(ip)]
     L.moe_destroy.argtypes = [vp]
     L.moe_strerror.argtypes = [ip]
@@ -153,6 +156,15 @@ def moe_route(h: int, x, T: int, topk_idx, topk_w, counts, stream=None) -> int:
 
 def moe_forward(h: int, x, T: int, out, stream=None) -> int:
     return _check(lib().moe_forward(h, _ptr(x), T, _ptr(out), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(h: int, x_host, T: int, out_host, stream=None) -> int:
+    return _check(lib().moe_forward_host(h, _ptr(x_host), T, _ptr(out_host), _stream(stream)),
+                  "moe_forward_host")
+
+
+def moe_host_join(h: int, stream=None) -> int:
+    return _check(lib().moe_host_join(h, _stream(stream)), "moe_host_join")
 
 
 def moe_status(h: int, stream=None) -> tuple[int, int]:
@@ -256,6 +268,19 @@ class MoELayer:
             out = torch.empty((T, self.d), dtype=self.dtype, device=x.device)
         moe_forward(self.handle, x, T, out, stream)
         return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        """moe_forward_host: x_host and out_host are CPU tensors (pinned for
+        overlap); the result is there after host_join's stream work is done."""
+        assert x_host.device.type == "cpu" and out_host.device.type == "cpu"
+        assert x_host.is_contiguous() and out_host.is_contiguous()
+        assert x_host.shape == out_host.shape and x_host.shape[1] == self.d
+        assert x_host.dtype == self.dtype and out_host.dtype == self.dtype
+        moe_forward_host(self.handle, x_host, x_host.shape[0], out_host, stream)
+        return out_host
+
+    def host_join(self, stream=None):
+        moe_host_join(self.handle, stream)
 
     def route(self, x, stream=None):
         import torch

@@ -124,6 +124,18 @@ struct moe_handle {
   bool q4_prefill = false;  // the grouped GEMMs support the layer's shape
   Q4Weights qw = {};
   Q4GemmMaps q4g = {}, q4d = {};  // gate/up and down GEMM maps (a set per call / once)
+  // host-buffer calls (moe_forward_host): two device slots, each an input and
+  // an output region of cap tokens, a copy-in and a copy-out stream, and per
+  // slot the events that order the copies against the forward on the caller's
+  // stream
+  struct HostStage {
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t in_done[2] = {}, fwd_done[2] = {}, out_done[2] = {};
+    bool used[2] = {false, false};
+    char *buf = nullptr;
+    size_t cap = 0;
+    int next = 0, last = -1;
+  } hs;
   // profiling
   bool prof = false;
   std::vector<ProfRec> recs;
@@ -668,6 +680,15 @@ int moe_destroy(moe_handle *h) {
   if (!h) return MOE_OK;
   for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
   int rc = MOE_OK;
+  moe_handle::HostStage &hs = h->hs;
+  for (cudaStream_t s : {hs.cin, hs.cout})
+    if (s && cudaStreamSynchronize(s) != cudaSuccess) rc = MOE_ERR_CUDA;
+  for (int i = 0; i < 2; ++i)
+    for (cudaEvent_t e : {hs.in_done[i], hs.fwd_done[i], hs.out_done[i]})
+      if (e) cudaEventDestroy(e);
+  for (cudaStream_t s : {hs.cin, hs.cout})
+    if (s) cudaStreamDestroy(s);
+  if (hs.buf && cudaFree(hs.buf) != cudaSuccess) rc = MOE_ERR_CUDA;
   if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = MOE_ERR_CUDA;
   delete h;
   return rc;
@@ -694,6 +715,56 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   return MOE_OK;
 }
 
+namespace {
+
+// 4-bit layers whose d or F the grouped GEMMs do not take run batches only
+// where every chunk takes the small-batch kernels
+int forward_shape_ok(const moe_handle *h, int T) {
+  if (h->q4 && T != 1 && !h->q4_prefill) {
+    const int c0 = std::min(T, h->cfg.max_tokens);
+    if (T > kSmallRouteT || !small_route_ok(c0, h->cfg.d_model) ||
+        !small_gemv_fits(c0, h->cfg.d_model, h->cfg.d_ff))
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// The copy streams and events of the host-buffer calls, made on first use.
+int host_stage_init(moe_handle *h) {
+  moe_handle::HostStage &s = h->hs;
+  if (s.cout) return MOE_OK;
+  for (int i = 0; i < 2; ++i)
+    for (cudaEvent_t *e : {&s.in_done[i], &s.fwd_done[i], &s.out_done[i]})
+      if (!*e) MOE_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+  if (!s.cin) MOE_TRY(cudaStreamCreateWithFlags(&s.cin, cudaStreamNonBlocking));
+  MOE_TRY(cudaStreamCreateWithFlags(&s.cout, cudaStreamNonBlocking));
+  return MOE_OK;
+}
+
+// Grows both slots to T tokens.  Earlier calls may still be using them, so
+// the copy streams and the caller's stream are drained before the old
+// buffer is freed.
+int host_stage_reserve(moe_handle *h, size_t T, cudaStream_t st) {
+  moe_handle::HostStage &s = h->hs;
+  if (T <= s.cap) return MOE_OK;
+  MOE_TRY(cudaStreamSynchronize(s.cin));
+  MOE_TRY(cudaStreamSynchronize(s.cout));
+  MOE_TRY(cudaStreamSynchronize(st));
+  if (s.buf) MOE_TRY(cudaFree(s.buf));
+  s.buf = nullptr;
+  s.cap = 0;
+  const size_t row = h->esz * h->cfg.d_model;
+  if (cudaMalloc(&s.buf, 4 * T * row) != cudaSuccess) {
+    s.buf = nullptr;
+    cudaGetLastError();
+    return MOE_ERR_OUT_OF_MEMORY;
+  }
+  s.cap = T;
+  return MOE_OK;
+}
+
+}  // namespace
+
 int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream) {
   if (!h || T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -704,14 +775,7 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
   char *ob = static_cast<char *>(out);
   if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  // 4-bit layers whose d or F the grouped GEMMs do not take run batches only
-  // where every chunk takes the small-batch kernels
-  if (h->q4 && T != 1 && !h->q4_prefill) {
-    const int c0 = std::min(T, h->cfg.max_tokens);
-    if (T > kSmallRouteT || !small_route_ok(c0, h->cfg.d_model) ||
-        !small_gemv_fits(c0, h->cfg.d_model, h->cfg.d_ff))
-      return MOE_ERR_UNSUPPORTED;
-  }
+  if (const int rc = forward_shape_ok(h, T); rc != MOE_OK) return rc;
   if (T == 1) {
     return h->cfg.dtype == MOE_BF16
                ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),
@@ -730,6 +794,50 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
                                     reinterpret_cast<float *>(ob + row * c0), st);
     if (rc != MOE_OK) return rc;
   }
+  return MOE_OK;
+}
+
+int moe_forward_host(moe_handle *h, const void *x_host, int T, void *out_host,
+                     void *cuda_stream) {
+  if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  const size_t row = h->esz * h->cfg.d_model, bytes = row * T;
+  const char *xb = static_cast<const char *>(x_host);
+  char *ob = static_cast<char *>(out_host);
+  if (xb < ob + bytes && ob < xb + bytes) return MOE_ERR_INVALID_ARG;  // overlap
+  if (const int rc = forward_shape_ok(h, T); rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (const int rc = host_stage_init(h); rc != MOE_OK) return rc;
+  if (const int rc = host_stage_reserve(h, T, st); rc != MOE_OK) return rc;
+  moe_handle::HostStage &s = h->hs;
+  const int k = s.next;
+  char *xs = s.buf + (2 * k) * s.cap * row, *os = s.buf + (2 * k + 1) * s.cap * row;
+  // copy-in: the slot's input is free once the forward two calls back is done
+  if (s.used[k]) MOE_TRY(cudaStreamWaitEvent(s.cin, s.fwd_done[k], 0));
+  MOE_TRY(cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, s.cin));
+  MOE_TRY(cudaEventRecord(s.in_done[k], s.cin));
+  // forward: after its input arrived and the slot's previous result left
+  MOE_TRY(cudaStreamWaitEvent(st, s.in_done[k], 0));
+  if (s.used[k]) MOE_TRY(cudaStreamWaitEvent(st, s.out_done[k], 0));
+  if (const int rc = moe_forward(h, xs, T, os, cuda_stream); rc != MOE_OK) return rc;
+  MOE_TRY(cudaEventRecord(s.fwd_done[k], st));
+  // copy-out
+  MOE_TRY(cudaStreamWaitEvent(s.cout, s.fwd_done[k], 0));
+  MOE_TRY(cudaMemcpyAsync(out_host, os, bytes, cudaMemcpyDeviceToHost, s.cout));
+  MOE_TRY(cudaEventRecord(s.out_done[k], s.cout));
+  s.used[k] = true;
+  s.last = k;
+  s.next = k ^ 1;
+  return MOE_OK;
+}
+
+int moe_host_join(moe_handle *h, void *cuda_stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  // the copy-out stream runs in order: its last event covers every copy-out
+  if (h->hs.last >= 0)
+    MOE_TRY(cudaStreamWaitEvent(static_cast<cudaStream_t>(cuda_stream),
+                                h->hs.out_done[h->hs.last], 0));
   return MOE_OK;
 }
 

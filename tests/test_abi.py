@@ -35,8 +35,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     fns = header_functions()
-    for name in ["moe_create", "moe_route", "moe_forward", "moe_destroy", "moe_status",
-                 "moe_strerror", "gdn_scan"]:
+    for name in ["moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_host_join",
+                 "moe_destroy", "moe_status", "moe_strerror", "gdn_scan"]:
         assert name in fns
 
 
@@ -87,6 +87,8 @@ def test_create_rejects_bad_config_on_host(lib, kw, code):
 
 def test_null_handle_calls(lib):
     assert lib.moe_forward(None, None, 4, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_host(None, None, 4, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_join(None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_route(None, None, 4, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == moe.MOE_OK
     assert lib.moe_create(None, None) == moe.MOE_ERR_INVALID_ARG
