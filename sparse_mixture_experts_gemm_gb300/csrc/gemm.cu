@@ -172,6 +172,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // Launched as a programmatic dependent, everything above overlaps the tail
+  // of the previous kernel: none of it touches global memory.  The wait
+  // returns once that kernel has completed and its writes are visible; the
+  // next kernel may then be scheduled (its CTAs run their own prologue and
+  // wait in turn).  Both are no-ops in an ordinary launch.
+  pdl_wait();
+  pdl_launch_dependents();
   int ntiles;
   if (kRouter) {
     ntiles = p.ntiles_host;
@@ -610,11 +617,21 @@ cudaError_t gemm_set_smem_attr() {
 }
 
 template <typename T, int EPI, int BN>
-cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st) {
+cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
+                        bool pdl) {
   if (grid <= 0) return cudaSuccess;
-  gemm_kernel<T, EPI, BN><<<grid, gemm_threads<EPI>(), kGemmSmem, st>>>(maps.m[0], maps.m[1], maps.m[2],
-                                                              maps.m[3], maps.m[4], maps.m[5], p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(gemm_threads<EPI>());
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<T, EPI, BN>, maps.m[0], maps.m[1], maps.m[2],
+                            maps.m[3], maps.m[4], maps.m[5], p);
 }
 
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN>();
@@ -623,16 +640,16 @@ template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_SWIGLU, kBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_STORE, kBN>();
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &,
-                                                                  int, cudaStream_t);
+                                                                  int, cudaStream_t, bool);
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &,
-                                                                 int, cudaStream_t);
+                                                                 int, cudaStream_t, bool);
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(const GemmMaps &,
                                                                         const GemmParams &, int,
-                                                                        cudaStream_t);
+                                                                        cudaStream_t, bool);
 template cudaError_t launch_gemm<float, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &, int,
-                                                          cudaStream_t);
+                                                          cudaStream_t, bool);
 template cudaError_t launch_gemm<float, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &, int,
-                                                         cudaStream_t);
+                                                         cudaStream_t, bool);
 
 // ---------------------------------------------------------------- test hook
 // Waits on an mbarrier that nothing signals, with the same bounded wait the

@@ -187,6 +187,10 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // programmatic dependent launch: as in the bf16 GEMM, the prologue above
+  // overlaps the previous kernel; its outputs are read only after the wait
+  pdl_wait();
+  pdl_launch_dependents();
   build_group_table(p, s_off, s_mt, warp, lane);
   tc_fence_before();
   __syncthreads();
@@ -624,17 +628,27 @@ cudaError_t gemm_q4_set_smem_attr() {
 }
 
 template <int EPI>
-cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st) {
+cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
+                           bool pdl) {
   if (grid <= 0) return cudaSuccess;
-  gemm_q4_kernel<EPI><<<grid, q4_threads<EPI>(), kQ4GemmSmem, st>>>(maps, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(q4_threads<EPI>());
+  cfg.dynamicSmemBytes = kQ4GemmSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_q4_kernel<EPI>, maps, p);
 }
 
 template cudaError_t gemm_q4_set_smem_attr<EPI_SWIGLU>();
 template cudaError_t gemm_q4_set_smem_attr<EPI_STORE>();
 template cudaError_t launch_gemm_q4<EPI_SWIGLU>(const Q4GemmMaps &, const GemmParams &, int,
-                                                cudaStream_t);
+                                                cudaStream_t, bool);
 template cudaError_t launch_gemm_q4<EPI_STORE>(const Q4GemmMaps &, const GemmParams &, int,
-                                               cudaStream_t);
+                                               cudaStream_t, bool);
 
 }  // namespace moe

@@ -76,7 +76,9 @@ struct GemmMaps {
 
 // gemm.cu
 template <typename T, int EPI, int BN>
-cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
+// pdl: launched as a programmatic dependent of the previous kernel on st
+cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
+                        bool pdl = false);
 template <typename T, int EPI, int BN>
 cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
@@ -125,7 +127,8 @@ struct Q4GemmMaps {
 constexpr int kQ4GemmSmem = 5 * (kBM * 128) + 2 * (kBN * 128) + 6 * (kBN * 32) +
                             2 * (2 * kBN * 8 * 2) + 1024 + kGemmCtrl;
 template <int EPI>
-cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
+                           bool pdl = false);
 template <int EPI>
 cudaError_t gemm_q4_set_smem_attr();
 
@@ -142,10 +145,12 @@ cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T
 cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *clear, int n_clear,
                            cudaStream_t st);
 cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
-                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st);
+                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st,
+                         bool pdl = false);
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
-                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st);
+                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
+                           bool pdl = false);
 
 // 4-bit group-affine matrix (codes two per byte, even column in the low
 // nibble; one bf16 scale and bias per 64 columns of a row)

@@ -290,13 +290,16 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
       MOE_TRY(launch_offsets(h->counts(), E, h->offsets, h->tile_ctr(0), 2, st));
     }
   }
+  // the kernels after the router run as programmatic dependents, each
+  // waiting for its predecessor inside (event records between kernels would
+  // break the chain, so not while profiling)
+  const bool pdl = !h->prof;
   if (!small) {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
-    MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st));
+    MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
   }
   if (small && small_gemv_fits(Tc, d, F)) {
     // every touched expert gets one or two rows: grouped GEMV over all SMs
-    const bool pdl = !h->prof;  // event records between kernels would break the chain
     SmallArgs sa;
     sa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
     sa.wg = static_cast<const __nv_bfloat16 *>(c.w_gate);
@@ -331,7 +334,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     }
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
-                              c.n_shared, h->status, st));
+                              c.n_shared, h->status, st, pdl));
     return MOE_OK;
   }
   GemmParams base = {};
@@ -365,9 +368,9 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     if (h->q4) {  // 4-bit weights (bf16 tokens): dequantised in the GEMM
       Q4GemmMaps mq = h->q4g;
       mq.a = m.m[1];
-      MOE_TRY(launch_gemm_q4<EPI_SWIGLU>(mq, p, h->num_sms, st));
+      MOE_TRY(launch_gemm_q4<EPI_SWIGLU>(mq, p, h->num_sms, st, pdl));
     } else {
-      MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st)));
+      MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st, pdl)));
     }
   }
   {
@@ -385,15 +388,15 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
     p.kid = KID_GEMM_DOWN;
     p.tile_ctr = h->tile_ctr(1);
     if (h->q4) {
-      MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st));
+      MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st, pdl));
     } else {
-      MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st)));
+      MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st, pdl)));
     }
   }
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
-                              c.n_shared, h->status, st));
+                              c.n_shared, h->status, st, pdl));
   }
   return MOE_OK;
 }

@@ -215,6 +215,10 @@ __global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ 
                                                     const int32_t *__restrict__ offsets,
                                                     int32_t *rank_inv, int32_t *perm, int A, int k,
                                                     int E, int *status) {
+  // a programmatic dependent of the router: its outputs are read after the
+  // wait; the grouped GEMM after it may then be scheduled
+  pdl_wait();
+  pdl_launch_dependents();
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i >= A) return;
   const int e = idx[i];
@@ -232,10 +236,27 @@ __global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ 
   perm[slot] = i / k;
 }
 
+namespace {
+cudaLaunchConfig_t pdl_config(int grid, int block, cudaStream_t st, bool pdl,
+                              cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+}  // namespace
+
 cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
-                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st) {
-  place_kernel<<<(A + 255) / 256, 256, 0, st>>>(idx, offsets, rank_inv, perm, A, k, E, status);
-  return cudaGetLastError();
+                         int32_t *perm, int A, int k, int E, int *status, cudaStream_t st,
+                         bool pdl) {
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_config((A + 255) / 256, 256, st, pdl, &attr);
+  return cudaLaunchKernelEx(&cfg, place_kernel, idx, offsets, rank_inv, perm, A, k, E, status);
 }
 
 // ---------------------------------------------------------------- combine
@@ -247,6 +268,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ yp,
                                                       const float *__restrict__ w, T *out, int T_tok,
                                                       int k, int d, int A_total, int n_shared,
                                                       int *status) {
+  // a programmatic dependent of the down GEMM (or GEMV): yp is read after
+  // the wait
+  pdl_wait();
   constexpr int NV = Vec<T>::N;
   const int vpr = d / NV;  // vectors per row
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -300,16 +324,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ yp,
 
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
-                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st) {
+                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
+                           bool pdl) {
   const long long threads = static_cast<long long>(T_tok) * (d / Vec<T>::N);
   const int grid = static_cast<int>((threads + 255) / 256);
-  combine_kernel<T><<<grid, 256, 0, st>>>(yp, inv, w, out, T_tok, k, d, A_total, n_shared, status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_config(grid, 256, st, pdl, &attr);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<T>, yp, inv, w, out, T_tok, k, d, A_total,
+                            n_shared, status);
 }
 template cudaError_t launch_combine<float>(const float *, const int32_t *, const float *, float *, int,
-                                           int, int, int, int, int *, cudaStream_t);
+                                           int, int, int, int, int *, cudaStream_t, bool);
 template cudaError_t launch_combine<__nv_bfloat16>(const __nv_bfloat16 *, const int32_t *,
                                                    const float *, __nv_bfloat16 *, int, int, int, int,
-                                                   int, int *, cudaStream_t);
+                                                   int, int *, cudaStream_t, bool);
 
 }  // namespace moe
