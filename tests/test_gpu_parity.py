@@ -107,6 +107,38 @@ def test_chunking_does_not_change_output(dev):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("dtype,q4", [("bf16", False), ("bf16", True), ("f32", False)])
+def test_back_to_back_calls_equal_isolated_calls(dev, dtype, q4):
+    """The kernels after the router start as programmatic dependents of their
+    predecessor and wait for it inside: twelve forwards issued without a host
+    synchronisation (alternating batches, chunked and unchunked, a small tail
+    chunk, one-token calls between them) must equal the same forwards run
+    one at a time with a synchronisation after each, bit for bit."""
+    d, F, E, k = (512, 512, 32, 4) if q4 else (512, 256, 32, 4)
+    if q4:
+        w = synth.q4_layer_weights(50, d, F, E, 1, dev)
+        layer = moe.Q4Layer(w, k, max_tokens=400)
+    else:
+        w = to_dev(synth.layer_weights(50, d, F, E, 1, dtype, "cpu"), dev)
+        layer = moe.MoELayer(w, k, max_tokens=400)
+    try:
+        sizes = [1000, 1, 333, 1000, 5, 800, 1, 1000, 333, 2, 800, 1000]
+        xs = [synth.tokens(51 + (i % 4), T, d, dtype, "cpu").to(dev)
+              for i, T in enumerate(sizes)]
+        outs = [torch.full_like(x, float("nan")) for x in xs]
+        for x, o in zip(xs, outs):
+            layer.forward(x, o)
+        torch.cuda.synchronize()
+        assert layer.status()[0] == 0
+        for i, x in enumerate(xs):
+            want = layer.forward(x)
+            torch.cuda.synchronize()
+            assert torch.equal(outs[i], want), f"call {i} (T={sizes[i]}) differs"
+        assert layer.status()[0] == 0
+    finally:
+        layer.close()
+
+
 def test_token_permutation_equivariance(dev):
     d, F, E, k, T = 512, 128, 32, 4, 257
     w = to_dev(synth.layer_weights(32, d, F, E, 1, "bf16", "cpu"), dev)
