@@ -156,6 +156,21 @@ def flush_l2(buf):
     buf.fill_(1)
 
 
+def workload_config(cfg: dict, wl_name: str, world: int) -> dict:
+    """The line's `config` object: the same for both arms of one workload."""
+    T = cfg["T"]
+    return {
+        "workload": f"{wl_name}: T={T} tokens through one MoE layer, d={cfg['d']}, "
+                    f"{cfg['E']} experts top-{cfg['k']} + 1 shared, F={cfg['F']}"
+                    + (", Zipf(1.2) router bias" if cfg["zipf"] else "")
+                    + (f", chunks of {cfg['chunk']}" if cfg["chunk"] < T else ""),
+        "tokens_per_step": T, "chunk": cfg["chunk"], "d_model": cfg["d"],
+        "n_experts": cfg["E"], "top_k": cfg["k"], "d_ff": cfg["F"], "n_shared": 1,
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "l2": "flushed between timed steps (256 MiB write outside the events)",
+    }
+
+
 # ------------------------------------------------------------------ our arm
 def timed_steps(layer, x, out, steps, flush_buf, st, profile=False):
     """Per-step milliseconds of `steps` forwards, L2 flushed before each
@@ -266,6 +281,66 @@ def bench_prefill(cfg, dev, steps, warmup, flush_buf):
                counts=chunk_counts, h2d=xh[0].numel() * xh[0].element_size(),
                d2h=oh[0].numel() * oh[0].element_size(), layer=layer, w=w, bias=bias, x=x)
     return res
+
+
+def bench_prefill_side(name, dev, steps, warmup, flush_buf, pk) -> dict:
+    """Another prefill configuration through the same kernels as the main
+    line (skewed 16K, 128K in 8K chunks): step time, whole-step roofline and
+    the per-kernel split from a second, event-profiled pass."""
+    cfg = WORKLOADS[name]
+    layer, w, bias = make_layer(cfg, dev, cfg["seed"])
+    T = cfg["T"]
+    x = synth.tokens(cfg["seed"] + 1000, T, cfg["d"], cfg["dtype"], dev)
+    out = torch.empty_like(x)
+    st = torch.cuda.current_stream()
+    try:
+        for _ in range(warmup):
+            layer.forward(x, out)
+        torch.cuda.synchronize()
+        counts = [layer.route(x[c0:c0 + cfg["chunk"]])[2].cpu().numpy()
+                  for c0 in range(0, T, cfg["chunk"])]
+        with Clocks(dev.index or 0) as clk:
+            times = timed_steps(layer, x, out, steps, flush_buf, st)
+        times_prof, prof = timed_steps(layer, x, out, steps, flush_buf, st, profile=True)
+        rc, det = layer.status()
+        if rc != 0:
+            raise RuntimeError(f"{name} device status {rc} ({det})")
+    finally:
+        layer.close()
+    ms = statistics.mean(times)
+    work = [algorithmic_prefill(cfg, c, min(cfg["chunk"], T - i * cfg["chunk"]))
+            for i, c in enumerate(counts)]
+    flops = sum(w_["flops"] for w_ in work)
+    byts = sum(w_["bytes"] for w_ in work)
+    t_tensor, t_hbm = flops / (pk["bf16"] * 1e12), byts / (pk["hbm"] * 1e9)
+    per_step = {k_: v[0] / max(steps, 1) for k_, v in prof.items() if v[1] > 0}
+    g1_ms = prof["gemm_gate_up"][0] / max(prof["gemm_gate_up"][1], 1)
+    g2_ms = prof["gemm_down"][0] / max(prof["gemm_down"][1], 1)
+    g1_flops = sum(w_["g1_flops"] for w_ in work) / len(work)
+    g2_flops = g1_flops / 2  # the down projection: half the gate/up multiply-adds
+    return {
+        "workload": workload_config(cfg, name, 1)["workload"],
+        "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
+        "ms_per_step_with_kernel_events": statistics.mean(times_prof),
+        "flops_per_step": flops, "algorithmic_bytes_per_step": byts,
+        "experts_with_rows_per_chunk": [int((c > 0).sum()) for c in counts],
+        "largest_group_rows": int(max(c.max() for c in counts)),
+        "block_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                           "t_roof_ms": max(t_tensor, t_hbm) * 1e3,
+                           "frac": max(t_tensor, t_hbm) * 1e3 / ms,
+                           "tensor_frac_of_measured_burst": t_tensor * 1e3 / ms,
+                           "tensor_frac_of_measured_sustained":
+                               flops / (ms * 1e-3) / (pk["bf16_sus"] * 1e12),
+                           "hbm_frac_of_measured": t_hbm * 1e3 / ms},
+        "gemm_tensor_frac_of_measured_burst": {
+            "gate_up": g1_flops / (g1_ms * 1e-3) / (pk["bf16"] * 1e12),
+            "down": g2_flops / (g2_ms * 1e-3) / (pk["bf16"] * 1e12)},
+        "kernels_ms_per_step": per_step,
+        "kernel_times_from": "event pair around every kernel on the launching stream "
+                             "(second pass of the same steps)",
+        "gpu_launches": sum(v[1] for v in prof.values()),
+        "clocks": clk.summary(),
+    }
 
 
 def bench_prefill_q4(cfg, dev, steps, warmup, flush_buf, pk) -> dict:
@@ -665,16 +740,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
-        "config": {
-            "workload": f"{wl_name}: T={T} tokens through one MoE layer, d={cfg['d']}, "
-                        f"{cfg['E']} experts top-{cfg['k']} + 1 shared, F={cfg['F']}"
-                        + (", Zipf(1.2) router bias" if cfg["zipf"] else "")
-                        + (f", chunks of {cfg['chunk']}" if cfg["chunk"] < T else ""),
-            "tokens_per_step": T, "chunk": cfg["chunk"], "d_model": cfg["d"],
-            "n_experts": cfg["E"], "top_k": cfg["k"], "d_ff": cfg["F"], "n_shared": 1,
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "flushed between timed steps (256 MiB write outside the events)",
-        },
+        "config": workload_config(cfg, wl_name, world),
         "roofline": {
             "kernel": "grouped gate/up GEMM + SiLU (gemm_kernel<bf16, EPI_SWIGLU>)",
             "bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
@@ -719,6 +785,8 @@ def main():
         line["decode_q4"] = decode_summary(dec, pk)
         # decode launches are counted in their own objects
     if wl_name == "prefill4k":
+        for side in ("skew16k", "long128k"):
+            line[side] = bench_prefill_side(side, dev, args.steps, args.warmup, flush_buf, pk)
         line["prefill_q4"] = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)
         line["small_batch"] = bench_small_batch(res["layer"], cfg, dev, flush_buf, pk)
         line["gdn"] = bench_gdn(dev, flush_buf, pk, cpu_tokens=64 if rank == 0 else 0)
@@ -733,8 +801,41 @@ def main():
                                 "sample": f"{what}, {passes} pass(es) in {dt:.1f} s, "
                                           f"{cpu_model()}"}
     res["layer"].close()
+    line["summary"] = summary_of(line)  # last key: the record keeps the line's tail
     if rank == 0:
         print(json.dumps(line))
+
+
+def summary_of(line: dict) -> dict:
+    """The headline figures of every object of the line, in a few hundred
+    bytes: prefill 4K, decode, the other prefill configurations, 4-bit
+    weights, small batches and the scan."""
+    r3 = lambda v: None if v is None else round(v, 3)  # noqa: E731
+    out = {"prefill4k": {"Mtok_s": r3(line["value"] / 1e6), "ms": r3(line["ms_per_step"]),
+                         "block_frac": r3(line["block_roofline"]["frac"]),
+                         "gate_up_hbm_frac": r3(line["roofline"]["frac"]),
+                         "e2e_Mtok_s": r3(line["e2e"]["value"] / 1e6)}}
+    for key in ("decode", "decode_q4"):
+        if key in line:
+            dsum = line[key]
+            out[key] = {"us_per_layer": r3(dsum["us_per_layer_median"]),
+                        "hbm_frac": r3(dsum["roofline"]["frac"])}
+    for key in ("skew16k", "long128k"):
+        if key in line:
+            o = line[key]
+            out[key] = {"Mtok_s": r3(o["tokens_per_s"] / 1e6), "ms": r3(o["ms_per_step"]),
+                        "block_frac": r3(o["block_roofline"]["frac"]),
+                        "bound": o["block_roofline"]["bound"],
+                        "gate_up_tensor_frac": r3(o["gemm_tensor_frac_of_measured_burst"]["gate_up"])}
+    if "prefill_q4" in line:
+        out["prefill_q4"] = {"ms": r3(line["prefill_q4"]["ms_per_step"])}
+    for key in ("small_batch",):
+        if key in line:
+            out[key] = {T: {"us": r3(v["us_per_layer_median"]), "hbm_frac": r3(v["hbm_frac_of_measured"])}
+                        for T, v in line[key]["by_T"].items()}
+    if "gdn" in line:
+        out["gdn_us"] = r3(line["gdn"]["us_per_layer_median"])
+    return out
 
 
 def decode_summary(dec, pk) -> dict:
@@ -781,7 +882,11 @@ def emit_decode_line(args, dec, pk, world):
 
 
 def run_reference(args, cfg, wl_name):
-    """The CPU oracle on the host cores, same metric and config, bounded sample."""
+    """The CPU oracle on the host cores, same metric and config as our arm.
+    Each step is a bounded sample of the workload (the first
+    --reference-tokens tokens of the same batch, through the same layer):
+    `ms_per_step` is the time of that sample, `value` the tokens it processed
+    per second; --warmup untimed steps come first."""
     import oracle
     oracle.build()
     T = cfg["T"]
@@ -790,22 +895,23 @@ def run_reference(args, cfg, wl_name):
     bias = synth.zipf_bias(cfg["seed"], cfg["E"], 1.2) if cfg["zipf"] else None
     nthr = host_threads()
     n_tok = min(args.reference_tokens, T)
-    for _ in range(1):
-        oracle_prefill_rate(cfg, w, x, bias, min(8, T), nthr)
-    rates, dts = [], []
+    for _ in range(args.warmup):
+        oracle_prefill_rate(cfg, w, x, bias, n_tok, nthr)
+    dts = []
     for _ in range(args.steps):
-        r, dt, _ = oracle_prefill_rate(cfg, w, x, bias, n_tok, nthr)
-        rates.append(r)
+        _, dt, _ = oracle_prefill_rate(cfg, w, x, bias, n_tok, nthr)
         dts.append(dt)
-    rate = statistics.mean(rates)
-    ms = statistics.mean(dts) * 1e3 * T / n_tok
-    sample = (f"first {n_tok} of the {T} tokens per step, {statistics.mean(dts):.2f} s per step, "
-              f"{cpu_model()}")
+    ms = statistics.mean(dts) * 1e3
+    rate = n_tok / (ms / 1e3)
+    sample = (f"first {n_tok} of the {T} tokens of the same batch per step "
+              f"({ms / 1e3:.2f} s per step), {nthr} threads, {cpu_model()}")
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": f"{wl_name}: T={T}, oracle on host"},
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": workload_config(cfg, wl_name, 1),
+        "tokens_timed_per_step": n_tok,
         "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -183,6 +183,25 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
 int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream);
 
 /*
+ * moe_forward that also hands back the routing its own kernels computed and
+ * used for this call (section "Keep expert routing on the GPU": the top-8,
+ * the histogram of assignments per expert, all on the GPU).  Every path
+ * writes what it actually used, not a second computation: the batch-1
+ * kernels (T == 1), the small-batch router (chunks of at most 16 bf16
+ * tokens) and the tensor-core or fp32 router of larger chunks.
+ *   topk_idx [T][k] int32  device, the chosen experts of each token, by
+ *                          descending logit, ties to the lower index;
+ *   topk_w   [T][k] float  device, their routing weights (sum 1 per token);
+ *   counts   [E]    int32  device, tokens that chose each expert, summed over
+ *                          all chunks of the call (zeroed on the stream first).
+ * Each of the three may be NULL; with all three NULL this is moe_forward.
+ * out and the other arguments as for moe_forward; asynchronous, no
+ * allocation, no host synchronisation.  Errors: as moe_forward.
+ */
+int moe_forward_routed(moe_handle *h, const void *x, int T, void *out, int32_t *topk_idx,
+                       float *topk_w, int32_t *counts, void *cuda_stream);
+
+/*
  * The whole block on host buffers: out_host[T][d] = MoE(x_host[T][d]), the
  * same result as moe_forward on device copies of x, bit for bit.  Like
  * moe_forward it enqueues the work and returns (section "Keep expert routing
@@ -258,7 +277,9 @@ int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n);
  * a barrier nothing will ever signal, giving up after about wait_us
  * microseconds (1 <= wait_us <= 2000000).  The kernel then records
  * MOE_ERR_DEVICE_TIMEOUT in the handle's status word and returns; the context
- * stays usable.  Read the result with moe_status.
+ * stays usable.  Read the result with moe_status.  With h == NULL the kernel
+ * records it in the status word of moe_decode_noalloc on the current device
+ * instead (read it with moe_noalloc_status).
  */
 int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
 
@@ -274,20 +295,34 @@ int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
  * overlapping.  Result: out = MoE(x), computed by the same decode kernels as
  * moe_forward with T == 1.
  *
- * Scratch: one static device array of 66,560 bytes inside the library, which
+ * Scratch: one static device array of 66,576 bytes inside the library, which
  * every GPU that loads the library holds until the process exits.  It limits
  * (top_k + n_shared) * d_ff to 16384; larger layers return
  * MOE_ERR_UNSUPPORTED, as do the limits of moe_create.  The first call on a
  * device looks up the array's device address (once per device, with that
  * device current), so make that first call before any stream capture.  All
- * calls share the array, and every call writes each value it reads (nothing
- * carries over from the last call): calls that overlap on the GPU, on
- * different streams or from different threads, race on it and must be
- * serialised by the caller.
+ * calls share the array: calls that overlap on the GPU, on different streams
+ * or from different threads, race on it and must be serialised by the caller.
+ * Within a call every scratch value is written before it is read, unless a
+ * device-side failure cuts the call short: a bounded wait in the kernels
+ * that runs out leaves out unspecified and records MOE_ERR_DEVICE_TIMEOUT in
+ * a status word kept in the same array (the first failure wins until it is
+ * read), which moe_noalloc_status returns.
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.  Asynchronous on
  * cuda_stream; no host synchronisation.
  */
 int moe_decode_noalloc(const moe_config *cfg, const void *x, void *out, void *cuda_stream);
+
+/*
+ * Synchronise cuda_stream, then return and clear the device status word of
+ * moe_decode_noalloc on the current device: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or
+ * MOE_ERR_DEVICE_BOUNDS, the first device-side failure of any call since the
+ * last read.  If detail != NULL it receives the library-defined code of the
+ * kernel and wait that failed (0 when none).  Allocates nothing; like
+ * moe_decode_noalloc, its first use on a device looks the array up.
+ * Errors: CUDA.
+ */
+int moe_noalloc_status(void *cuda_stream, int *detail);
 
 #ifdef __cplusplus
 }

@@ -35,10 +35,11 @@ MOE_F32 = 1
 KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
                 "decode_gate_up", "decode_down"]
 
-EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_host_join",
-            "moe_status", "moe_destroy",
+EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_forward_routed", "moe_forward_host",
+            "moe_host_join", "moe_status", "moe_destroy",
             "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
-            "moe_decode_noalloc", "moe_create_q4", "moe_quantize_q4", "gdn_scan"]
+            "moe_decode_noalloc", "moe_noalloc_status", "moe_create_q4", "moe_quantize_q4",
+            "gdn_scan"]
 
 Q4_GROUP = 64  # columns per (scale, bias) pair of the 4-bit format
 
@@ -90,6 +91,7 @@ def lib() -> ctypes.CDLL:
     L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(vp)]
     L.moe_route.argtypes = [vp, vp, ip, vp, vp, vp, vp]
     L.moe_forward.argtypes = [vp, vp, ip, vp, vp]
+    L.moe_forward_routed.argtypes = [vp, vp, ip, vp, vp, vp, vp, vp]
     L.moe_forward_host.argtypes = [vp, vp, ip, vp, vp]
     L.moe_host_join.argtypes = [vp, vp]
     L.moe_status.argtypes = [vp, vp, ctypes.POINTER(ip)]
@@ -101,6 +103,7 @@ def lib() -> ctypes.CDLL:
                                    ctypes.POINTER(ctypes.c_int64), ip]
     L.moe_debug_wait_timeout.argtypes = [vp, ip, vp]
     L.moe_decode_noalloc.argtypes = [ctypes.POINTER(moe_config), vp, vp, vp]
+    L.moe_noalloc_status.argtypes = [vp, ctypes.POINTER(ip)]
     L.moe_create_q4.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_q4_weights),
                                 ctypes.POINTER(vp)]
     L.moe_quantize_q4.argtypes = [vp, ip, ctypes.c_longlong, ip, vp, vp, vp, vp]
@@ -158,6 +161,13 @@ def moe_forward(h: int, x, T: int, out, stream=None) -> int:
     return _check(lib().moe_forward(h, _ptr(x), T, _ptr(out), _stream(stream)), "moe_forward")
 
 
+def moe_forward_routed(h: int, x, T: int, out, topk_idx=None, topk_w=None, counts=None,
+                       stream=None) -> int:
+    return _check(lib().moe_forward_routed(h, _ptr(x), T, _ptr(out), _ptr(topk_idx),
+                                           _ptr(topk_w), _ptr(counts), _stream(stream)),
+                  "moe_forward_routed")
+
+
 def moe_forward_host(h: int, x_host, T: int, out_host, stream=None) -> int:
     return _check(lib().moe_forward_host(h, _ptr(x_host), T, _ptr(out_host), _stream(stream)),
                   "moe_forward_host")
@@ -204,6 +214,14 @@ def moe_decode_noalloc(cfg: moe_config, x, out, stream=None) -> int:
     callers that cannot allocate device memory and so cannot create a handle."""
     return _check(lib().moe_decode_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(out),
                                            _stream(stream)), "moe_decode_noalloc")
+
+
+def moe_noalloc_status(stream=None) -> tuple[int, int]:
+    """(code, detail) of moe_decode_noalloc's device status word on the current
+    device; synchronises the stream and clears the word."""
+    detail = ctypes.c_int(0)
+    rc = lib().moe_noalloc_status(_stream(stream), ctypes.byref(detail))
+    return rc, detail.value
 
 
 def moe_create_q4(cfg: moe_config, w: moe_q4_weights) -> int:
@@ -268,6 +286,19 @@ class MoELayer:
             out = torch.empty((T, self.d), dtype=self.dtype, device=x.device)
         moe_forward(self.handle, x, T, out, stream)
         return out
+
+    def forward_routed(self, x, out=None, stream=None):
+        """moe_forward_routed: (out, idx [T][k], w [T][k], counts [E]) -- the
+        routing the forward's own kernels used."""
+        import torch
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.d), dtype=self.dtype, device=x.device)
+        idx = torch.empty((T, self.k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, self.k), dtype=torch.float32, device=x.device)
+        counts = torch.empty((self.E,), dtype=torch.int32, device=x.device)
+        moe_forward_routed(self.handle, x, T, out, idx, w, counts, stream)
+        return out, idx, w, counts
 
     def forward_host(self, x_host, out_host, stream=None):
         """moe_forward_host: x_host and out_host are CPU tensors (pinned for

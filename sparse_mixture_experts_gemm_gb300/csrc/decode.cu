@@ -130,9 +130,10 @@ __global__ void __launch_bounds__(288, 1)
   uint4 *xs = reinterpret_cast<uint4 *>(dsm + kBStages * 2 * kBBox);
   const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
   for (int i = threadIdx.x; i < a.d * static_cast<int>(sizeof(T)) / 16; i += blockDim.x)
-    xs[i] = __ldcg(xg + i);
+    xs[i] = ld_cg16(xg + i);
   __syncthreads();
   pdl_launch_dependents();
+  if (blockIdx.x == 0) write_routing(a, s_sel, s_selw, threadIdx.x);
   if (warp == 8) {
     if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
@@ -236,13 +237,12 @@ __global__ void __launch_bounds__(256, 2) decode_down_kernel(const DecodeArgs a)
   pdl_wait();
 
   const int total4 = nslot * a.F / 4;
-  const float4 *hg = reinterpret_cast<const float4 *>(a.h);
   for (int base = threadIdx.x; base < total4; base += 256 * 8) {
     float4 t[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int q = base + u * 256;
-      if (q < total4) t[u] = __ldcg(hg + q);
+      if (q < total4) t[u] = ld_cg_f32x4(a.h + 4 * q);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {

@@ -152,9 +152,20 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    key[i] = (e < E) ? fkey(__ldcg(logits + e)) : 0u;
+    key[i] = (e < E) ? fkey(ld_cg_f32(logits + e)) : 0u;
   }
   topk_from_keys(key, E, k, lane, s_sel, s_selw);
+}
+
+// Thread j < k: entry j of the layer's routing (the choice the kernels use)
+// into the caller's buffers, if it asked for them.  The k experts are
+// distinct, so no two threads touch the same count.
+__device__ __forceinline__ void write_routing(const DecodeArgs &a, const int *sel,
+                                              const float *selw, int j) {
+  if (j >= a.k) return;
+  if (a.sel_idx) a.sel_idx[j] = sel[j];
+  if (a.sel_w) a.sel_w[j] = selw[j];
+  if (a.sel_counts) a.sel_counts[sel[j]] += 1;
 }
 
 // Up to kPre 16-byte vectors of one row held in registers per lane: vector
@@ -193,7 +204,7 @@ __device__ __forceinline__ float row_dot_pre(const RowPre &r, const uint4 *row, 
 // this one waited for), once per CTA rather than once per warp.
 __device__ __forceinline__ void load_token(uint4 *xs, const void *x, int nvec) {
   const uint4 *xg = static_cast<const uint4 *>(x);
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) xs[i] = ld_cg16(xg + i);
   __syncthreads();
 }
 

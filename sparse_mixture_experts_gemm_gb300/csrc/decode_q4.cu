@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) decode_router_q4_kernel(con
       a.dsel[32 * r + 8 + lane] = __float_as_int(s_selw[lane]);
     }
   }
+  write_routing(a, s_sel, s_selw, lane);
 }
 
 // ---------------------------------------------------------------- B: gate/up
@@ -299,9 +300,9 @@ __global__ void __launch_bounds__(kGateUpWarps * 32) decode_gateup_q4_kernel(con
   const GateUpSmem sm(qsm, n, d);
   uint4 *xs = const_cast<uint4 *>(sm.x);
   if (!shared_blk && threadIdx.x == 0)
-    s_row0 = __ldcg(a.dsel + 32 * (blockIdx.x % kSelReplicas) + s) * F + f0;
+    s_row0 = ld_cg_s32(a.dsel + 32 * (blockIdx.x % kSelReplicas) + s) * F + f0;
   const uint4 *xg = static_cast<const uint4 *>(a.x);
-  for (int i = threadIdx.x; i < d * 2 / 16; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  for (int i = threadIdx.x; i < d * 2 / 16; i += blockDim.x) xs[i] = ld_cg16(xg + i);
   __syncthreads();
   if (!shared_blk) gateup_issue(qsm, a.q.g, a.q.u, s_row0, n, d, ns, bar);
   XChunk xc;
@@ -405,8 +406,8 @@ __global__ void __launch_bounds__(640) decode_down_q4_kernel(const DecodeArgs a)
   // the layer's top-k (kernel A finished before kernel B let this kernel start)
   if (static_cast<int>(threadIdx.x) < a.k) {
     const int *rep = a.dsel + 32 * (blockIdx.x % kSelReplicas);
-    s_sel[threadIdx.x] = __ldcg(rep + threadIdx.x);
-    s_selw[threadIdx.x] = __int_as_float(__ldcg(rep + 8 + threadIdx.x));
+    s_sel[threadIdx.x] = ld_cg_s32(rep + threadIdx.x);
+    s_selw[threadIdx.x] = __int_as_float(ld_cg_s32(rep + 8 + threadIdx.x));
   }
   __syncthreads();
   {
@@ -427,10 +428,10 @@ __global__ void __launch_bounds__(640) decode_down_q4_kernel(const DecodeArgs a)
   for (int j = 0; j < CPL; ++j) hv[j] = 0.0f;
   float sh = 0.0f, wslot = 0.0f;
   if (active) {
-    const float4 *hp = reinterpret_cast<const float4 *>(a.h + slot * F + sl * CPL);
+    const float *hp = a.h + slot * F + sl * CPL;
 #pragma unroll
     for (int j = 0; j < CPL / 4; ++j) {
-      const float4 v = __ldcg(hp + j);
+      const float4 v = ld_cg_f32x4(hp + 4 * j);
       hv[4 * j] = v.x;
       hv[4 * j + 1] = v.y;
       hv[4 * j + 2] = v.z;

@@ -437,9 +437,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           float g[32], u[32];
-          tmem_ld32(tb + c, g);
-          tmem_ld32(tb + BN / 2 + c, u);
-          tmem_ld_wait();
+          tmem_ld32x2_sync(tb + c, tb + BN / 2 + c, g, u);
           if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) g[i] = silu(g[i]) * u[i];
@@ -451,8 +449,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
-          tmem_ld32(tb + c, v);
-          tmem_ld_wait();
+          tmem_ld32_sync(tb + c, v);
           if (valid) store32<T>(yrow + c, v);
         }
       } else {
@@ -467,8 +464,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
-          tmem_ld32(tb + c, v);
-          tmem_ld_wait();
+          tmem_ld32_sync(tb + c, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int e = tl.n0 + c + i;
@@ -500,10 +496,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             // with ties in increasing index: equal values keep the lower index
             const long long tb0 = static_cast<long long>(t) * p.nq * kMaxTopK;
             for (int q = 0; q < p.nq; ++q) {
-              const float4 *qv = reinterpret_cast<const float4 *>(p.cand_v + tb0 + q * kMaxTopK);
-              const int4 *qi = reinterpret_cast<const int4 *>(p.cand_i + tb0 + q * kMaxTopK);
-              const float4 v0 = __ldcg(qv), v1 = __ldcg(qv + 1);
-              const int4 i0 = __ldcg(qi), i1 = __ldcg(qi + 1);
+              // written by other CTAs before their fence and arrival:
+              // strong loads, ordered after this thread's fence
+              const float *qv = p.cand_v + tb0 + q * kMaxTopK;
+              const int *qi = p.cand_i + tb0 + q * kMaxTopK;
+              const float4 v0 = ld_relaxed_f32x4(qv), v1 = ld_relaxed_f32x4(qv + 4);
+              const int4 i0 = ld_relaxed_s32x4(qi), i1 = ld_relaxed_s32x4(qi + 4);
               topk_insert(bv, bi, v0.x, i0.x);
               topk_insert(bv, bi, v0.y, i0.y);
               topk_insert(bv, bi, v0.z, i0.z);
@@ -581,7 +579,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       int sum = 0;
       for (int q = 0; q < per; ++q) {
         const int e = lane * per + q;
-        if (e < E) sum += __ldcg(p.counts + static_cast<long long>(e) * kCountStride);
+        if (e < E) sum += ld_relaxed_s32(p.counts + static_cast<long long>(e) * kCountStride);
       }
       int incl = sum;
 #pragma unroll
@@ -593,9 +591,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       for (int q = 0; q < per; ++q) {
         const int e = lane * per + q;
         if (e < E) {
-          const int ce = __ldcg(p.counts + static_cast<long long>(e) * kCountStride);
+          const int ce = ld_relaxed_s32(p.counts + static_cast<long long>(e) * kCountStride);
           if (p.offsets_out) p.offsets_out[e] = run;
-          if (p.counts_out) p.counts_out[e] = ce;
+          if (p.counts_out) p.counts_out[e] += ce;  // summed over the chunks of a call
           run += ce;
           // every CTA has added its counts: clear them for the next call
           p.counts[static_cast<long long>(e) * kCountStride] = 0;

@@ -589,9 +589,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
 #pragma unroll 1
         for (int c = 0; c < kBN / 2; c += 16) {
           float g[16], u[16];
-          tmem_ld16(tb + c, g);
-          tmem_ld16(tb + kBN / 2 + c, u);
-          tmem_ld_wait();
+          tmem_ld16x2_sync(tb + c, tb + kBN / 2 + c, g, u);
           if (valid) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) g[i] = silu(g[i]) * u[i];
@@ -602,8 +600,7 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
 #pragma unroll 1
         for (int c = 0; c < kBN; c += 16) {
           float v[16];
-          tmem_ld16(tb + c, v);
-          tmem_ld_wait();
+          tmem_ld16_sync(tb + c, v);
           if (valid) store16_bf16(orow + c, v);
         }
       }

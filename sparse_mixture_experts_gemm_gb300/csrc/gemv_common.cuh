@@ -80,7 +80,7 @@ __device__ __forceinline__ int gv_part(int r, int m) {
 template <class Args>
 __device__ __forceinline__ void touched_groups(const Args &a, int *s_off, int *s_grp, int *s_ng,
                                                int kid) {
-  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldcg(a.offsets + i);
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = ld_cg_s32(a.offsets + i);
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;

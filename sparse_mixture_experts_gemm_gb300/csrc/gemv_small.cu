@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_kernel(SmallArgs 
   pdl_launch_dependents();
   touched_groups(a, s_off, s_grp, &s_ng, KID_GEMM_GATE_UP);
   for (int i = threadIdx.x; i < a.A; i += blockDim.x) {
-    int t = __ldcg(a.perm + i);
+    int t = ld_cg_s32(a.perm + i);
     if (t < 0 || t >= a.T) {
       report_error(a.status, MOE_ERR_DEVICE_BOUNDS, KID_GEMM_GATE_UP * 100 + SITE_INDEX);
       t = 0;
@@ -203,13 +203,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_down_kernel(SmallArgs a)
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int j0 = 0; j0 < nsteps; j0 += kSteps) {
       if (!(pre && j0 == 0)) load_rows(ra, rb, pa, pb, j0, nsteps);
+      // h was written by the gate/up kernel: coherent loads, all issued
+      // before the first MMA that uses them
+      uint4 hv[kSteps];
 #pragma unroll
       for (int s = 0; s < kSteps; ++s)
-        if (j0 + s < nsteps) gv_step(c0, ra[s], rb[s], __ldcg(hq0 + 4 * (j0 + s)));
+        if (j0 + s < nsteps) hv[s] = ld_cg16(hq0 + 4 * (j0 + s));
+#pragma unroll
+      for (int s = 0; s < kSteps; ++s)
+        if (j0 + s < nsteps) gv_step(c0, ra[s], rb[s], hv[s]);
       if (n > 8) {
 #pragma unroll
         for (int s = 0; s < kSteps; ++s)
-          if (j0 + s < nsteps) gv_step(c1, ra[s], rb[s], __ldcg(hq1 + 4 * (j0 + s)));
+          if (j0 + s < nsteps) hv[s] = ld_cg16(hq1 + 4 * (j0 + s));
+#pragma unroll
+        for (int s = 0; s < kSteps; ++s)
+          if (j0 + s < nsteps) gv_step(c1, ra[s], rb[s], hv[s]);
       }
     }
     __nv_bfloat16 *yp = a.y + static_cast<long long>(slot0) * d + r0 + g;

@@ -91,11 +91,19 @@ __device__ __forceinline__ void superstep(float (&c0)[4], float (&c1)[4], const 
   const __nv_bfloat162 sb = bcast(rb.s[i]), bb = bcast(rb.b[i]);
   const uint32_t wa[4] = {ra.c[i].x, ra.c[i].y, ra.c[i].z, ra.c[i].w};
   const uint32_t wb[4] = {rb.c[i].x, rb.c[i].y, rb.c[i].z, rb.c[i].w};
+  // h from global memory was written by the gate/up kernel: coherent loads,
+  // all issued before the first MMA that uses them
+  uint4 v0[4], v1[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    v0[s] = kGlobal ? ld_cg16(x0 + s) : x0[s];
+    if (two) v1[s] = kGlobal ? ld_cg16(x1 + s) : x1[s];
+  }
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const uint4 a = dq8(wa[s], sa, ba), b = dq8(wb[s], sb, bb);
-    gv_step(c0, a, b, kGlobal ? __ldcg(x0 + s) : x0[s]);
-    if (two) gv_step(c1, a, b, kGlobal ? __ldcg(x1 + s) : x1[s]);
+    gv_step(c0, a, b, v0[s]);
+    if (two) gv_step(c1, a, b, v1[s]);
   }
 }
 }  // namespace
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_q4_kernel(SmallQ4
   pdl_launch_dependents();
   touched_groups(a, s_off, s_grp, &s_ng, KID_GEMM_GATE_UP);
   for (int i = threadIdx.x; i < a.A; i += blockDim.x) {
-    int t = __ldcg(a.perm + i);
+    int t = ld_cg_s32(a.perm + i);
     if (t < 0 || t >= a.T) {
       report_error(a.status, MOE_ERR_DEVICE_BOUNDS, KID_GEMM_GATE_UP * 100 + SITE_INDEX);
       t = 0;

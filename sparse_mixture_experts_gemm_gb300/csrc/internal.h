@@ -53,7 +53,7 @@ struct GemmParams {
   int32_t *idx;
   float *w;
   int32_t *counts;         // [E * kCountStride], zero at the launch; the last CTA clears it again
-  int32_t *counts_out;     // [E] dense copy written by the last CTA (may be null)
+  int32_t *counts_out;     // [E] the last CTA adds each count to it (may be null)
   int32_t *rank;           // [T * k] rank of each assignment inside its group (may be null)
   int32_t *offsets_out;    // [E + 1] written by the last CTA (may be null)
   int nq;                  // expert blocks per token (ceil(E / kRouterBN))
@@ -88,9 +88,11 @@ cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t 
 // inv (slots), perm, offsets and zeroes the n_clear words clear[32 q].
 constexpr int kSmallRouteT = 16;
 constexpr int kSmallRouteTokBytes = 65536;
+// counts_out (may be null): each expert's group size is added to it.
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,
-                               int32_t *offsets, int32_t *clear, int n_clear, cudaStream_t st);
+                               int32_t *offsets, int32_t *counts_out, int32_t *clear, int n_clear,
+                               cudaStream_t st);
 cudaError_t route_small_set_attr();
 
 // gemv_small.cu: gate/up (h = silu(gate) * up as bf16 rows) and down (bf16
@@ -132,6 +134,10 @@ cudaError_t launch_gemm_q4(const Q4GemmMaps &maps, const GemmParams &p, int grid
 template <int EPI>
 cudaError_t gemm_q4_set_smem_attr();
 
+// noalloc.cu: device address of moe_decode_noalloc's status word on the
+// current device (null if the lookup failed)
+int *noalloc_status_word();
+
 // moe.cu: tensor-map encoding (host only, no allocation)
 bool encode_map_2d(CUtensorMap *m, const void *base, size_t esz, uint64_t rows, uint64_t cols,
                    uint32_t box_cols, uint32_t box_rows, bool swizzle128);
@@ -142,8 +148,9 @@ cudaError_t launch_router_simt(const T *x, const T *wr, const float *bias, int T
                                int k, int32_t *idx, float *w, int32_t *counts, int32_t *rank,
                                cudaStream_t st);
 // also zeroes counts[0, E) and n_clear words clear[32 q] for the next call
-cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *clear, int n_clear,
-                           cudaStream_t st);
+// counts_out (may be null) accumulates the counts
+cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *counts_out,
+                           int32_t *clear, int n_clear, cudaStream_t st);
 cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
                          int32_t *perm, int A, int k, int E, int *status, cudaStream_t st,
                          bool pdl = false);
@@ -194,6 +201,11 @@ struct DecodeArgs {
   // kSelReplicas copies of 128 bytes (32 words: [0, 8) experts, [8, 16) their
   // weights as float bits), so that the many CTAs reading it share no line
   int *dsel;
+  // the routing the kernels use, for a caller that asked for it (each may be
+  // null): the k experts, their weights, and +1 on each chosen expert's count
+  int32_t *sel_idx;
+  float *sel_w;
+  int32_t *sel_counts;
 };
 // decode_q4.cu: the batch-1 kernels for 4-bit expert weights (bf16 tokens,
 // bf16 router) and the quantiser

@@ -259,17 +259,31 @@ int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w
   return MOE_OK;
 }
 
+// Where a forward puts the routing its kernels compute: idx [Tc][k] and
+// w [Tc][k] of this chunk (null: the handle's workspace) and the per-expert
+// counts of the call (null: not wanted; otherwise zeroed at the call's start
+// and summed over its chunks).
+struct RouteOut {
+  int32_t *idx = nullptr;
+  float *w = nullptr;
+  int32_t *counts = nullptr;
+};
+
 // a chunk of Tc bf16 tokens routes in one cluster launch
 bool small_route_ok(int Tc, int d) {
   return Tc <= kSmallRouteT && static_cast<long long>(Tc) * d * 2 <= kSmallRouteTokBytes;
 }
 
 template <typename T>
-int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st) {
+int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut &ro,
+                      cudaStream_t st) {
   const moe_config &c = h->cfg;
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k;
   const int A = Tc * k;
   const int BK = static_cast<int>(128 / sizeof(T));
+  // the chunk's routing: written by the router, read by place and combine
+  int32_t *idx = ro.idx ? ro.idx : h->idx;
+  float *wts = ro.w ? ro.w : h->w;
 
   // route_ctl is zero here: create cleared it and every router launch clears
   // what it used (counts, ticket, the GEMMs' tile counters) when it is done
@@ -277,17 +291,17 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   if (small) {
     // a few tokens: routing and placement in one cluster launch
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
-    MOE_TRY(launch_route_small(x, c.w_router, c.router_bias, Tc, d, E, k, h->idx, h->w, h->inv,
-                               h->perm, h->offsets, h->tile_ctr(0), 2, st));
+    MOE_TRY(launch_route_small(x, c.w_router, c.router_bias, Tc, d, E, k, idx, wts, h->inv,
+                               h->perm, h->offsets, ro.counts, h->tile_ctr(0), 2, st));
   } else {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
-      const int rc = launch_router_tc(h, x, Tc, h->idx, h->w, h->inv, h->offsets, nullptr, st);
+      const int rc = launch_router_tc(h, x, Tc, idx, wts, h->inv, h->offsets, ro.counts, st);
       if (rc != MOE_OK) return rc;
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
-                                    k, h->idx, h->w, h->counts(), h->inv, st));
-      MOE_TRY(launch_offsets(h->counts(), E, h->offsets, h->tile_ctr(0), 2, st));
+                                    k, idx, wts, h->counts(), h->inv, st));
+      MOE_TRY(launch_offsets(h->counts(), E, h->offsets, ro.counts, h->tile_ctr(0), 2, st));
     }
   }
   // the kernels after the router run as programmatic dependents, each
@@ -296,7 +310,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   const bool pdl = !h->prof;
   if (!small) {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
-    MOE_TRY(launch_place(h->idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
+    MOE_TRY(launch_place(idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
   }
   if (small && small_gemv_fits(Tc, d, F)) {
     // every touched expert gets one or two rows: grouped GEMV over all SMs
@@ -333,7 +347,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
                     : launch_small_down(sa, h->num_sms, st, pdl));
     }
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
-    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
+    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
                               c.n_shared, h->status, st, pdl));
     return MOE_OK;
   }
@@ -395,16 +409,19 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, cudaStream_t st
   }
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
-    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, h->w, out, Tc, k, d, A,
+    MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
                               c.n_shared, h->status, st, pdl));
   }
   return MOE_OK;
 }
 
 template <typename T>
-int run_decode(moe_handle *h, const T *x, T *out, cudaStream_t st) {
+int run_decode(moe_handle *h, const T *x, T *out, const RouteOut &ro, cudaStream_t st) {
   const moe_config &c = h->cfg;
-  DecodeArgs a;
+  DecodeArgs a = {};
+  a.sel_idx = ro.idx;
+  a.sel_w = ro.w;
+  a.sel_counts = ro.counts;
   a.x = x;
   a.wr = c.w_router;
   a.wg = c.w_gate;
@@ -709,6 +726,8 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   const int d = c.d_model, E = c.n_experts, k = c.top_k;
   ProfScope ps(h, MOE_KERNEL_ROUTER, st);
   if (c.dtype == MOE_BF16) {
+    // the router's last CTA adds the histogram to counts
+    MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
     return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, counts, st);
   }
   MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
@@ -768,7 +787,14 @@ int host_stage_reserve(moe_handle *h, size_t T, cudaStream_t st) {
 
 }  // namespace
 
-int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// moe_forward and moe_forward_routed: validation, then the batch-1 path or
+// the chunk loop; idx / w / counts as for moe_forward_routed (each may be null).
+int forward_impl(moe_handle *h, const void *x, int T, void *out, int32_t *idx, float *w,
+                 int32_t *counts, void *cuda_stream) {
   if (!h || T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !out) return MOE_ERR_INVALID_ARG;
@@ -779,25 +805,46 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
   if (xb < ob + row * T && ob < xb + row * T) return MOE_ERR_INVALID_ARG;  // overlap
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (const int rc = forward_shape_ok(h, T); rc != MOE_OK) return rc;
+  // the kernels add to the counts
+  if (counts)
+    MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * h->cfg.n_experts, st));
+  const int k = h->cfg.top_k;
   if (T == 1) {
+    const RouteOut ro{idx, w, counts};
     return h->cfg.dtype == MOE_BF16
                ? run_decode<__nv_bfloat16>(h, static_cast<const __nv_bfloat16 *>(x),
-                                           static_cast<__nv_bfloat16 *>(out), st)
-               : run_decode<float>(h, static_cast<const float *>(x), static_cast<float *>(out), st);
+                                           static_cast<__nv_bfloat16 *>(out), ro, st)
+               : run_decode<float>(h, static_cast<const float *>(x), static_cast<float *>(out),
+                                   ro, st);
   }
   for (int c0 = 0; c0 < T; c0 += h->cfg.max_tokens) {
     const int Tc = (T - c0) < h->cfg.max_tokens ? (T - c0) : h->cfg.max_tokens;
+    const long long o = static_cast<long long>(c0) * k;
+    const RouteOut ro{idx ? idx + o : nullptr, w ? w + o : nullptr, counts};
     int rc;
     if (h->cfg.dtype == MOE_BF16)
       rc = run_prefill_chunk<__nv_bfloat16>(
           h, reinterpret_cast<const __nv_bfloat16 *>(xb + row * c0), Tc,
-          reinterpret_cast<__nv_bfloat16 *>(ob + row * c0), st);
+          reinterpret_cast<__nv_bfloat16 *>(ob + row * c0), ro, st);
     else
       rc = run_prefill_chunk<float>(h, reinterpret_cast<const float *>(xb + row * c0), Tc,
-                                    reinterpret_cast<float *>(ob + row * c0), st);
+                                    reinterpret_cast<float *>(ob + row * c0), ro, st);
     if (rc != MOE_OK) return rc;
   }
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_stream) {
+  return forward_impl(h, x, T, out, nullptr, nullptr, nullptr, cuda_stream);
+}
+
+int moe_forward_routed(moe_handle *h, const void *x, int T, void *out, int32_t *topk_idx,
+                       float *topk_w, int32_t *counts, void *cuda_stream) {
+  return forward_impl(h, x, T, out, topk_idx, topk_w, counts, cuda_stream);
 }
 
 int moe_forward_host(moe_handle *h, const void *x_host, int T, void *out_host,
@@ -890,12 +937,21 @@ int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n) {
 }
 
 int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream) {
-  if (!h || wait_us < 1 || wait_us > 2000000) return MOE_ERR_INVALID_ARG;
+  if (wait_us < 1 || wait_us > 2000000) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (h) {
+    dev = h->device;
+  } else if (cudaGetDevice(&dev) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
+  // no handle: the status word of the allocation-free entry point
+  int *status = h ? h->status : noalloc_status_word();
+  if (!status) return MOE_ERR_CUDA;
   int clk_khz = 0;
-  if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, h->device) != cudaSuccess)
+  if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   const long long cycles = static_cast<long long>(clk_khz) * wait_us / 1000;
-  MOE_TRY(launch_debug_wait(h->status, cycles, static_cast<cudaStream_t>(cuda_stream)));
+  MOE_TRY(launch_debug_wait(status, cycles, static_cast<cudaStream_t>(cuda_stream)));
   return MOE_OK;
 }
 

@@ -10,11 +10,14 @@
 // in one file-scope device array below that every GPU loading this library
 // holds until the process exits.
 //
-// Scratch layout (floats): [0, 256) router logits, [256, 256 + kNoAllocMaxH)
-// the intermediate h of the k routed experts and the shared one.  Every
-// value is written before it is read within one call, so nothing needs
-// clearing between calls.  The pages describe no allocation-free mode; this
-// has no counterpart there.
+// Scratch layout (4-byte words): [0, 256) router logits, [256, 256 +
+// kNoAllocMaxH) the intermediate h of the k routed experts and the shared
+// one, then 4 ints: the status word (first error code, detail) that the
+// kernels' bounded waits report into.  Within a call every logit and h value
+// is written before it is read, so they need no clearing between calls; the
+// status word starts at zero (static storage) and is cleared when
+// moe_noalloc_status reads it.  The pages describe no allocation-free mode;
+// this has no counterpart there.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,7 +30,8 @@ namespace moe {
 namespace {
 
 constexpr int kNoAllocMaxH = 16384;                  // (top_k + n_shared) * d_ff at most
-constexpr int kNoAllocFloats = 256 + kNoAllocMaxH;   // 66,560 bytes
+constexpr int kNoAllocStatus = 256 + kNoAllocMaxH;   // first word of the status
+constexpr int kNoAllocFloats = kNoAllocStatus + 4;   // 66,576 bytes
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
@@ -57,9 +61,31 @@ int setup_device(int dev, float **out) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// The status word inside the scratch array of the current device (device
+// address), for the failure-path test hook; null when the lookup failed.
+int *noalloc_status_word() {
+  int dev = 0;
+  float *s = nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || setup_device(dev, &s) != MOE_OK) return nullptr;
+  return reinterpret_cast<int *>(s + kNoAllocStatus);
+}
+
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" int moe_noalloc_status(void *cuda_stream, int *detail) {
+  int *w = noalloc_status_word();
+  if (!w) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int s[2] = {0, 0};
+  if (cudaMemcpy(s, w, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(w, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = s[1];
+  return s[0];
+}
 
 extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
                                   void *cuda_stream) {
@@ -91,7 +117,7 @@ extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
   if (rc != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
 
-  DecodeArgs a;
+  DecodeArgs a = {};
   a.x = x;
   a.wr = c->w_router;
   a.wg = c->w_gate;
@@ -109,7 +135,7 @@ extern "C" int moe_decode_noalloc(const moe_config *c, const void *x, void *out,
   a.logits = s;
   a.h = s + 256;
   a.out = out;
-  a.status = nullptr;
+  a.status = reinterpret_cast<int *>(s + kNoAllocStatus);
   const bool bf16 = c->dtype == MOE_BF16;
   if ((bf16 ? launch_decode_router<__nv_bfloat16>(a, st, false)
             : launch_decode_router<float>(a, st, false)) != cudaSuccess)

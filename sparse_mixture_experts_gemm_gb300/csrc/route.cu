@@ -172,8 +172,10 @@ template cudaError_t launch_router_simt<__nv_bfloat16>(const __nv_bfloat16 *, co
 
 // ---------------------------------------------------------------- offsets
 // offsets[e] = sum_{e' < e} counts[e'], offsets[E] = total; one warp.
-__global__ void offsets_kernel(int32_t *counts, int E, int32_t *offsets, int32_t *clear,
-                               int n_clear) {
+// counts_out (may be null): each expert's count is added to it (the counts of
+// a call's chunks sum up there).
+__global__ void offsets_kernel(int32_t *counts, int E, int32_t *offsets, int32_t *counts_out,
+                               int32_t *clear, int n_clear) {
   const int lane = threadIdx.x;
   const int per = (E + 31) / 32;
   int sum = 0;
@@ -193,6 +195,7 @@ __global__ void offsets_kernel(int32_t *counts, int E, int32_t *offsets, int32_t
     if (e < E) {
       offsets[e] = run;
       run += counts[e];
+      if (counts_out) counts_out[e] += counts[e];
       counts[e] = 0;  // clear for the next call
     }
   }
@@ -201,9 +204,9 @@ __global__ void offsets_kernel(int32_t *counts, int E, int32_t *offsets, int32_t
     for (int q = 0; q < n_clear; ++q) clear[q * 32] = 0;
 }
 
-cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *clear, int n_clear,
-                           cudaStream_t st) {
-  offsets_kernel<<<1, 32, 0, st>>>(counts, E, offsets, clear, n_clear);
+cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *counts_out,
+                           int32_t *clear, int n_clear, cudaStream_t st) {
+  offsets_kernel<<<1, 32, 0, st>>>(counts, E, offsets, counts_out, clear, n_clear);
   return cudaGetLastError();
 }
 
@@ -211,8 +214,9 @@ cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *cl
 // One thread per assignment i = t * k + j: slot = offsets[e] + rank, written
 // over the rank in rank_inv[i]; perm[slot] = t names the token whose row the
 // grouped gate/up GEMM gathers into that slot's tile row.
-__global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ idx,
-                                                    const int32_t *__restrict__ offsets,
+// idx, offsets and the ranks come from the router, the kernel this one
+// waits for: read through L2 after the wait, never the non-coherent path.
+__global__ void __launch_bounds__(256) place_kernel(const int32_t *idx, const int32_t *offsets,
                                                     int32_t *rank_inv, int32_t *perm, int A, int k,
                                                     int E, int *status) {
   // a programmatic dependent of the router: its outputs are read after the
@@ -221,13 +225,14 @@ __global__ void __launch_bounds__(256) place_kernel(const int32_t *__restrict__ 
   pdl_launch_dependents();
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i >= A) return;
-  const int e = idx[i];
+  const int e = ld_cg_s32(idx + i);
+  const int rank = ld_cg_s32(rank_inv + i);  // issued before e is used
   if (e < 0 || e >= E) {
     report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
     return;
   }
-  const int lo = offsets[e], hi = offsets[e + 1];
-  const int slot = lo + rank_inv[i];
+  const int lo = ld_cg_s32(offsets + e), hi = ld_cg_s32(offsets + e + 1);
+  const int slot = lo + rank;
   if (slot < lo || slot >= hi) {
     report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_PERMUTE * 100 + SITE_INDEX);
     return;
@@ -262,35 +267,40 @@ cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *ra
 // ---------------------------------------------------------------- combine
 // One thread per 16-byte chunk of an output row; the k routed contributions
 // are added in choice order (deterministic), then the shared expert's row.
+// Y, the slots and the weights were written by kernels earlier in the launch
+// chain (Y by the one this kernel waits for): all are read through L2 after
+// the wait, never through the non-coherent path.
 template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ yp,
-                                                      const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ w, T *out, int T_tok,
-                                                      int k, int d, int A_total, int n_shared,
+__global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t *inv,
+                                                      const float *w, T *out, int T_tok, int k,
+                                                      int d, int A_total, int n_shared,
                                                       int *status) {
   // a programmatic dependent of the down GEMM (or GEMV): yp is read after
   // the wait
   pdl_wait();
   constexpr int NV = Vec<T>::N;
-  const int vpr = d / NV;  // vectors per row
+  const int vpr = d / NV;  // vectors per row (a multiple of 32: a warp serves one token)
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int t = static_cast<int>(gid / vpr);
   const int c = static_cast<int>(gid % vpr);
-  if (t >= T_tok) return;
-  // every slot and weight first, then every row vector, so all of the
-  // thread's loads are in flight together; the sum keeps the fixed order
+  if (t >= T_tok) return;  // whole warps
+  // the token's slots and weights: lanes j < k load slot j, lanes 16 + j its
+  // weight, once per warp, and hand them to every lane; then every row
+  // vector is requested, so all of the thread's loads are in flight
+  // together; the sum keeps the fixed order
+  const int lane = threadIdx.x & 31;
+  int my_slot = 0;
+  float my_w = 0.0f;
+  if (lane < k) my_slot = ld_cg_s32(inv + static_cast<long long>(t) * k + lane);
+  if (lane >= 16 && lane - 16 < k) my_w = ld_cg_f32(w + static_cast<long long>(t) * k + lane - 16);
   int slot[kMaxTopK];
   float wt[kMaxTopK];
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
-    slot[j] = 0;
-    wt[j] = 0.0f;
-    if (j < k) {
-      slot[j] = inv[static_cast<long long>(t) * k + j];
-      wt[j] = w[static_cast<long long>(t) * k + j];
-      bad = bad || slot[j] < 0 || slot[j] >= A_total;
-    }
+    slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
+    wt[j] = __shfl_sync(0xffffffffu, my_w, 16 + j);
+    if (j < k) bad = bad || slot[j] < 0 || slot[j] >= A_total;
   }
   if (bad) {
     report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_COMBINE * 100 + SITE_INDEX);
@@ -299,8 +309,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ yp,
   uint4 v[kMaxTopK + 1];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) v[j] = ld_stream16(yp + static_cast<long long>(slot[j]) * d + c * NV);
-  if (n_shared) v[kMaxTopK] = ld_stream16(yp + static_cast<long long>(A_total + t) * d + c * NV);
+    if (j < k) v[j] = ld_cg16(yp + static_cast<long long>(slot[j]) * d + c * NV);
+  if (n_shared) v[kMaxTopK] = ld_cg16(yp + static_cast<long long>(A_total + t) * d + c * NV);
   float acc[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) acc[i] = 0.0f;

@@ -79,8 +79,8 @@ struct RouterOp {
 __global__ void __launch_bounds__(kRouteWarps * 32, 1)
     route_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wr,
                        const float *__restrict__ bias, int T, int d, int E, int k, int32_t *idx,
-                       float *w, int32_t *inv, int32_t *perm, int32_t *offsets, int32_t *clear,
-                       int n_clear) {
+                       float *w, int32_t *inv, int32_t *perm, int32_t *offsets,
+                       int32_t *counts_out, int32_t *clear, int n_clear) {
   extern __shared__ uint4 s_dyn[];  // partial tiles, then [T][d / 8 + 4] tokens
   __shared__ float s_lg[kSmallRouteT][256];  // CTA 0: the logits
   __shared__ int s_idx[kSmallRouteT][kMaxTopK];
@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32, 1)
     perm[slot] = a / k;
   }
   for (int i = threadIdx.x; i <= E; i += blockDim.x) offsets[i] = s_off[i];
+  if (counts_out)  // summed over the chunks of a call
+    for (int i = threadIdx.x; i < E; i += blockDim.x) counts_out[i] += s_cnt[i];
   // the grouped GEMMs' tile counters start at zero
   if (threadIdx.x == 0)
     for (int q = 0; q < n_clear; ++q) clear[q * 32] = 0;
@@ -174,7 +176,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32, 1)
 // one cluster: the whole grid (at most 16 CTAs for E <= 256)
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,
-                               int32_t *offsets, int32_t *clear, int n_clear, cudaStream_t st) {
+                               int32_t *offsets, int32_t *counts_out, int32_t *clear, int n_clear,
+                               cudaStream_t st) {
   const int ncta = (E + kRouteWarps - 1) / kRouteWarps;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncta);
@@ -190,7 +193,7 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_small_kernel, static_cast<const __nv_bfloat16 *>(x),
                             static_cast<const __nv_bfloat16 *>(wr), bias, T, d, E, k, idx, w, inv,
-                            perm, offsets, clear, n_clear);
+                            perm, offsets, counts_out, clear, n_clear);
 }
 
 cudaError_t route_small_set_attr() {

@@ -2,9 +2,11 @@
 
 Bars: expert index sets and per-expert counts bit-exact; routing weights
 within 1e-5; block output within 1e-2 row-normwise relative error (bf16 data,
-fp32 accumulation, bf16 intermediates).  Small cases compare every output;
-full-size cases compare routing on every token and outputs on a seeded sample
-of tokens, in the launch configuration the benchmark uses.
+fp32 accumulation, bf16 intermediates).  Routing is checked twice: the
+standalone routing call (moe_route) and the routing the forward's own kernels
+used (moe_forward_routed).  Every output row is compared, the full-size
+4,096- and 16,384-token cases included, in the launch configuration the
+benchmark uses; the 128K case compares two whole chunks.
 """
 import numpy as np
 import pytest
@@ -41,13 +43,15 @@ def run_case(dev, seed, T, d, F, E, k, dtype="bf16", n_shared=1, max_tokens=None
     try:
         if T <= layer.cfg.max_tokens:
             idx, wts, counts = layer.route(xd)
-        out = layer.forward(xd)
+        out, f_idx, f_w, f_counts = layer.forward_routed(xd)
         torch.cuda.synchronize()
         rc, detail = layer.status()
         assert rc == 0, f"device status {rc} detail {detail}"
+        ridx, rw, _, rcounts = H.oracle.route(H.np_view(x), H.np_view(w["Wr"]), k,
+                                              bias=None if bias is None else bias.numpy())
+        # the routing the forward's kernels used (counts summed over chunks)
+        H.check_routing(f_idx, f_w, f_counts, ridx, rw, rcounts)
         if T <= layer.cfg.max_tokens:
-            ridx, rw, _, rcounts = H.oracle.route(H.np_view(x), H.np_view(w["Wr"]), k,
-                                                  bias=None if bias is None else bias.numpy())
             H.check_routing(idx, wts, counts, ridx, rw, rcounts)
         ref, oidx, ow, _ = H.oracle_forward(x, w, k, bias=bias, rows=rows)
         got = out if rows is None else out[torch.as_tensor(rows, device=dev)]
@@ -172,27 +176,20 @@ def test_decode_full_size_layer(dev):
     assert err_pre.max() <= H.OUT_TOL, err_pre
 
 
-def _sample_rows(T, n, seed):
-    r = np.random.default_rng(seed)
-    rows = np.unique(np.concatenate([[0, T - 1], r.choice(T, n, replace=False)]))
-    return rows
-
-
 def test_prefill_4k_full_size(dev):
     """T=4096, d=2048, 256 experts top-8 + shared, F=512, bf16: routing exact on
-    every token, outputs on 48 sampled tokens."""
+    every token, every output row against the oracle."""
     T = 4096
-    run_case(dev, 2, T, 2048, 512, 256, 8, max_tokens=T, rows=_sample_rows(T, 46, 2),
-             gen_device=dev)
+    run_case(dev, 2, T, 2048, 512, 256, 8, max_tokens=T, gen_device=dev)
 
 
 def test_skewed_16k_full_size(dev):
     """T=16384 with a Zipf(1.2) router bias: a few experts take thousands of
-    rows, many take none; routing exact on every token, outputs sampled."""
+    rows (the giant groups of the grouped GEMMs), many take none; routing
+    exact on every token, every output row against the oracle."""
     T = 16384
     bias = synth.zipf_bias(3, 256, 1.2)
-    out, err = run_case(dev, 3, T, 2048, 512, 256, 8, max_tokens=T, bias=bias,
-                        rows=_sample_rows(T, 46, 3), gen_device=dev)
+    _, err = run_case(dev, 3, T, 2048, 512, 256, 8, max_tokens=T, bias=bias, gen_device=dev)
 
 
 def test_edge_calls(dev):
@@ -244,7 +241,7 @@ def test_long_prompt_128k_in_8k_chunks(dev):
     x = H.margined_tokens(1004, T, w["Wr"], k, "bf16", device=dev)
     layer = moe.MoELayer(w, k, max_tokens=chunk)
     try:
-        out = layer.forward(x)
+        out, f_idx, f_w, f_counts = layer.forward_routed(x)
         routes = [layer.route(x[c0:c0 + chunk]) for c0 in range(0, T, chunk)]
         torch.cuda.synchronize()
         rc, detail = layer.status()
@@ -252,10 +249,16 @@ def test_long_prompt_128k_in_8k_chunks(dev):
     finally:
         layer.close()
     wr = H.np_view(w["Wr"])
+    rcount_sum = np.zeros(E, dtype=np.int64)
     for ci, (idx, wts, counts) in enumerate(routes):
         xs = x[ci * chunk:(ci + 1) * chunk]
         ridx, rw, _, rcounts = H.oracle.route(H.np_view(xs), wr, k)
         H.check_routing(idx, wts, counts, ridx, rw, rcounts)
+        # the forward's own routing of this chunk is the same
+        sl = slice(ci * chunk, (ci + 1) * chunk)
+        H.check_routing(f_idx[sl], f_w[sl], None, ridx, rw, None)
+        rcount_sum += rcounts
+    assert np.array_equal(f_counts.cpu().numpy(), rcount_sum), "call counts over 16 chunks"
     for ci in (0, T // chunk - 1):
         rows = np.arange(ci * chunk, (ci + 1) * chunk)
         ref, *_ = H.oracle_forward(x, w, k, rows=rows)
