@@ -6,11 +6,14 @@ fp32 accumulation), plus the batch-1 decode path over a stack of 40 distinct
 layers with a fresh token per step.  `value` is prefill tokens/s; the decode
 figures (microseconds per layer) are reported under "decode", and those of the
 same stack with 4-bit group-affine expert weights under "decode_q4"; batches of
-2..16 tokens through one layer under "small_batch"; the Gated DeltaNet scan of
-one layer over a 2K-token prompt under "gdn".
+2..64 tokens through one layer under "small_batch"; the Gated DeltaNet scan of
+one layer over a 2K-token prompt under "gdn".  `--no-side` leaves out every
+object but the 4K prefill (for profiling); `--workload prefill_q4` prints the
+4-bit prefill alone.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|small_batch|gdn2k|tiny]
+                    [--workload prefill4k|skew16k|long128k|decode|decode_q4|small_batch|gdn2k|prefill_q4|tiny]
+                    [--no-decode] [--no-side] [--no-cpu]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; a 256 MiB buffer is written between timed
@@ -415,14 +418,15 @@ def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> flo
 
 
 def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dict:
-    """Batches of 2..16 tokens through the same layer (the verification shape
-    of speculative decoding): one routing launch, the grouped GEMV on all SMs,
-    the combine; eager calls as a user makes them, L2 flushed before each.
-    q4: the layer has 4-bit expert weights (0.5625 bytes a weight)."""
+    """Batches of 2..64 tokens through the same layer (the verification shape
+    of speculative decoding): one routing launch, then the grouped GEMV on all
+    SMs (at most 32 tokens) or the grouped GEMMs, the combine; eager calls as
+    a user makes them, L2 flushed before each.  q4: the layer has 4-bit expert
+    weights (0.5625 bytes a weight)."""
     d, F, E, k = cfg["d"], cfg["F"], cfg["E"], cfg["k"]
     st = torch.cuda.current_stream()
     out = {}
-    for T in (2, 4, 8, 16):
+    for T in (2, 4, 8, 16, 32, 64):
         x = synth.tokens(cfg["seed"] + 5000 + T, T, d, "bf16", dev)
         for _ in range(5):
             layer.forward(x)
@@ -444,7 +448,7 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dic
         out[str(T)] = {"us_per_layer_median": us, "experts_touched": active,
                        "algorithmic_bytes": byts,
                        "hbm_frac_of_measured": byts / (us * 1e-6) / (pk["hbm"] * 1e9)}
-    return {"workload": "T = 2, 4, 8, 16 tokens through one layer (d=2048, 256 experts top-8 + "
+    return {"workload": "T = 2, 4, 8, 16, 32, 64 tokens through one layer (d=2048, 256 experts top-8 + "
                         "1 shared, F=512, " + ("4-bit group-affine expert weights, bf16 router "
                                                "and tokens" if q4 else "bf16") +
                         "), eager calls, L2 flushed before each, median of "
@@ -631,11 +635,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill4k",
                     choices=["prefill4k", "skew16k", "long128k", "tiny", "decode", "decode_q4",
-                             "small_batch", "gdn2k"])
+                             "small_batch", "gdn2k", "prefill_q4"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-layers", type=int, default=40,
                     help="distinct layers in the decode stack (40 in the benchmark; fewer for profiling)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="only the 4K prefill: no 16K/128K, 4-bit, small-batch or scan objects")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--oracle-seconds", type=float, default=10.0,
                     help="minimum host seconds of the oracle baseline (whole passes)")
@@ -655,7 +661,7 @@ def main():
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
     wl_name = ("prefill4k" if args.workload.startswith("decode")
-               or args.workload in ("small_batch", "gdn2k") else args.workload)
+               or args.workload in ("small_batch", "gdn2k", "prefill_q4") else args.workload)
     cfg = WORKLOADS[wl_name]
     pk = peaks()
 
@@ -692,6 +698,17 @@ def main():
             "clocks": g["clocks"], "gpu_launches": g["gpu_launches"], "gdn": g}))
         return
 
+    if args.workload == "prefill_q4":
+        q = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)
+        print(json.dumps({
+            "metric": "prefill tokens/s, 4-bit expert weights", "value": q["tokens_per_s"],
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": q["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": q["workload"]}, "roofline": q["roofline"],
+            "clocks": q["clocks"], "gpu_launches": q["gpu_launches"], "prefill_q4": q}))
+        return
+
     if args.workload == "small_batch":
         layer, _, _ = make_layer(cfg, dev, cfg["seed"])
         try:
@@ -726,7 +743,7 @@ def main():
     g1_flops = sum(w_["g1_flops"] for w_ in work) / len(work)
     achieved = g1_bytes / (g1_avg / 1e3) / 1e9
     t_roof = max(flops / (pk["bf16"] * 1e12), bytes_ / (pk["hbm"] * 1e9))
-    launches_per_step = 5 * len(work)  # router, place, gate/up, down, combine per chunk
+    launches_per_step = 4 * len(work)  # router, gate/up, down, combine per chunk
     line = {
         "metric": METRIC,
         "value": value,
@@ -784,7 +801,7 @@ def main():
                            q4=True)
         line["decode_q4"] = decode_summary(dec, pk)
         # decode launches are counted in their own objects
-    if wl_name == "prefill4k":
+    if wl_name == "prefill4k" and not args.no_side:
         for side in ("skew16k", "long128k"):
             line[side] = bench_prefill_side(side, dev, args.steps, args.warmup, flush_buf, pk)
         line["prefill_q4"] = bench_prefill_q4(cfg, dev, args.steps, args.warmup, flush_buf, pk)

@@ -187,7 +187,7 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
  * used for this call (section "Keep expert routing on the GPU": the top-8,
  * the histogram of assignments per expert, all on the GPU).  Every path
  * writes what it actually used, not a second computation: the batch-1
- * kernels (T == 1), the small-batch router (chunks of at most 16 bf16
+ * kernels (T == 1), the small-batch router (chunks of at most 64 bf16
  * tokens) and the tensor-core or fp32 router of larger chunks.
  *   topk_idx [T][k] int32  device, the chosen experts of each token, by
  *                          descending logit, ties to the lower index;
@@ -267,7 +267,9 @@ const char *moe_strerror(int code);
 #define MOE_KERNEL_DECODE_ROUTER 5
 #define MOE_KERNEL_DECODE_GATE_UP 6
 #define MOE_KERNEL_DECODE_DOWN 7
-#define MOE_KERNEL_KINDS 8
+#define MOE_KERNEL_GEMV_GATE_UP 8 /* small batches: the grouped GEMVs */
+#define MOE_KERNEL_GEMV_DOWN 9
+#define MOE_KERNEL_KINDS 10
 int moe_profile(moe_handle *h, int enable);
 int moe_profile_read(moe_handle *h, float *ms, int64_t *launches, int n);
 
@@ -293,7 +295,7 @@ int moe_debug_wait_timeout(moe_handle *h, int wait_us, void *cuda_stream);
  * cfg describes the layer exactly as for moe_create (max_tokens is ignored);
  * x[d] and out[d] are device rows of cfg->dtype, 16-byte aligned, not
  * overlapping.  Result: out = MoE(x), computed by the same decode kernels as
- * moe_forward with T == 1.
+ * moe_forward with T == 1 (bit for bit the same result).
  *
  * Scratch: one static device array of 66,576 bytes inside the library, which
  * every GPU that loads the library holds until the process exits.  It limits

@@ -33,7 +33,7 @@ MOE_BF16 = 0
 MOE_F32 = 1
 
 KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
-                "decode_gate_up", "decode_down"]
+                "decode_gate_up", "decode_down", "gemv_gate_up", "gemv_down"]
 
 EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_forward_routed", "moe_forward_host",
             "moe_host_join", "moe_status", "moe_destroy",

@@ -6,8 +6,12 @@
 //                a token's expert blocks merges the candidates, takes the
 //                softmax over the chosen logits and claims each assignment's
 //                rank inside its expert group with an atomic on the per-expert
-//                histogram; the last CTA scans the histogram into group offsets ("Optimizing on-device inference
-//                for Apple Silicon", sections "Qwen creates three distinct
+//                histogram, and puts the assignment at that rank of the
+//                expert's list (the rows the gate/up GEMM gathers, which also
+//                records each assignment's slot for the combine, so no
+//                separate placement step is needed); the last CTA scans the histogram
+//                into group offsets ("Optimizing on-device inference for
+//                Apple Silicon", sections "Qwen creates three distinct
 //                workload shapes" and "Keep expert routing on the GPU").
 //   EPI_SWIGLU : for each expert group, gate and up projections of its rows in
 //                one MMA (B tile = 128 gate rows over 128 up rows), epilogue
@@ -364,13 +368,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       const GemmTile tl = decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool routed = tl.group < p.n_routed;
       const T *src[kRowsPer];
+      int tok[kRowsPer];
+      if (routed) gather_tokens<kRowsPer>(p, gt, tl, r0, tok);
 #pragma unroll
-      for (int i = 0; i < kRowsPer; ++i) {
-        const int r = r0 + 16 * i;
-        src[i] = (routed && r < tl.rows)
-                     ? xg + static_cast<long long>(p.perm[tl.a_row + r]) * K + c * kChunk
+      for (int i = 0; i < kRowsPer; ++i)
+        src[i] = (routed && r0 + 16 * i < tl.rows)
+                     ? xg + static_cast<long long>(tok[i]) * K + c * kChunk
                      : nullptr;
-      }
       for (int kb = 0; kb < p.num_k_blocks; ++kb) {
         const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -542,10 +546,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j) {
               if (j < p.k) {
-                const int b = __shfl_sync(act, base[j], __ffs(peers[j]) - 1);
-                if (p.rank)
-                  p.rank[static_cast<long long>(t) * p.k + j] =
-                      b + __popc(peers[j] & ((1u << lane) - 1u));
+                const int rk = __shfl_sync(act, base[j], __ffs(peers[j]) - 1) +
+                               __popc(peers[j] & ((1u << lane) - 1u));
+                if (p.rank) p.rank[static_cast<long long>(t) * p.k + j] = rk;
+                // the token goes to place rk of its expert's list
+                if (p.list) p.list[static_cast<long long>(bi[j]) * p.list_stride + rk] = t;
               }
             }
           }

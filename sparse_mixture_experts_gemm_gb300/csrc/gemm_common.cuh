@@ -47,6 +47,27 @@ struct GroupTable {
   const int *mt;
 };
 
+// Tokens of the rows of routed tile tl that a gather thread copies: rows
+// r0 + 16 i (i < kRows) that exist, -1 for the others.  The token comes from
+// the router's per-expert list (tokens in rank order) or, without lists, from
+// the slot permutation.  Both were written by kernels the GEMM waited for at
+// griddepcontrol.wait (an asm with a memory clobber: no load moves above
+// it): ordinary loads, so the 8 threads that share a row hit in L1, all
+// issued together.
+template <int kRows>
+__device__ __forceinline__ void gather_tokens(const GemmParams &p, const GroupTable &gt,
+                                              const GemmTile &tl, int r0, int (&tok)[kRows]) {
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int r = r0 + 16 * i;
+    tok[i] = -1;
+    if (r < tl.rows)
+      tok[i] = p.list ? p.list[static_cast<long long>(tl.group) * p.list_stride +
+                               (tl.a_row - gt.off[tl.group]) + r]
+                      : p.perm[tl.a_row + r];
+  }
+}
+
 __device__ __forceinline__ GemmTile decode_tile(const GroupTable &gt, const GemmParams &p, int i,
                                                 int n_cols, bool down) {
   const int E = p.n_routed;

@@ -442,13 +442,12 @@ __global__ void __launch_bounds__(q4_threads<EPI>(), 1)
       const GemmTile tl = decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool routed = tl.group < p.n_routed;
       const __nv_bfloat16 *src[kRowsPer];
+      int tok[kRowsPer];
+      if (routed) gather_tokens<kRowsPer>(p, gt, tl, r0, tok);
 #pragma unroll
-      for (int i = 0; i < kRowsPer; ++i) {
-        const int r = r0 + 16 * i;
-        src[i] = (routed && r < tl.rows)
-                     ? xg + static_cast<long long>(p.perm[tl.a_row + r]) * K + c * 8
-                     : nullptr;
-      }
+      for (int i = 0; i < kRowsPer; ++i)
+        src[i] = (routed && r0 + 16 * i < tl.rows) ? xg + static_cast<long long>(tok[i]) * K + c * 8
+                                                   : nullptr;
       for (int kb = 0; kb < nkb; ++kb) {
         const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {

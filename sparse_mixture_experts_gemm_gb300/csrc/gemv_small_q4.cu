@@ -1,4 +1,4 @@
-// gemv_small_q4.cu -- the small-batch grouped GEMV (T <= 16 bf16 tokens) on
+// gemv_small_q4.cu -- the small-batch grouped GEMV (T <= 32 bf16 tokens) on
 // 4-bit group-affine expert weights.
 //
 // The same units and warps as the bf16 small-batch GEMV (gemv_small.cu: 16
@@ -36,8 +36,16 @@ namespace moe {
 namespace {
 constexpr int kWarps = 16;
 constexpr int kPairs = kWarps / 2;
-constexpr int kPre = 4;  // super-steps of codes in flight per row
-constexpr int kPairBytes = 2 * kPairs * 8 * 32 * 4;
+// super-steps in flight with NB 8-column blocks: fewer with more blocks
+// (their accumulators take the registers)
+template <int NB>
+constexpr int pre_for() { return NB <= 2 ? 4 : 2; }
+// the down kernel, whose N side (h) comes from global memory, holds two
+template <int NB>
+constexpr int pre_down() { return 2; }
+// two buffers of [pair][4 NB values][32 lanes]
+template <int NB>
+constexpr int pair_bytes() { return 2 * kPairs * 4 * NB * 32 * 4; }
 
 // 8 codes -> the 4 bf16x2 weight pairs of columns (0, 1), (2, 3), (4, 5), (6, 7)
 __device__ __forceinline__ uint4 dq8(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) {
@@ -60,18 +68,20 @@ __device__ __forceinline__ __nv_bfloat162 bcast(uint16_t bits) {
   return __halves2bfloat162(v, v);
 }
 
-// One row's codes and (scale, bias) for super-steps [J0, J0 + kPre).
+// One row's codes and (scale, bias) for super-steps [J0, J0 + P).
+template <int P>
 struct RowQ {
-  uint4 c[kPre];
-  uint16_t s[kPre], b[kPre];
+  uint4 c[P];
+  uint16_t s[P], b[P];
 };
 // codes: the row's codes offset to this lane's first super-step (uint4 index
 // 4 J per super-step); sb: the row's scales / biases at this lane's group of
 // super-step 0 (2 groups per super-step)
-__device__ __forceinline__ void load_rowq(RowQ &r, const uint4 *codes, const uint16_t *s,
+template <int P>
+__device__ __forceinline__ void load_rowq(RowQ<P> &r, const uint4 *codes, const uint16_t *s,
                                           const uint16_t *b, int J0, int J1) {
 #pragma unroll
-  for (int i = 0; i < kPre; ++i)
+  for (int i = 0; i < P; ++i)
     if (J0 + i < J1) {
       r.c[i] = ld_stream16(codes + 4 * (J0 + i));
       r.s[i] = __ldg(s + 2 * (J0 + i));
@@ -80,42 +90,72 @@ __device__ __forceinline__ void load_rowq(RowQ &r, const uint4 *codes, const uin
 }
 
 // MMA steps of one super-step: rows g (ra) and g + 8 (rb) against the 32
-// columns' N-side values x (uint4 per 8 columns, stride 1) for column
-// blocks 0 and (if two) 1; kGlobal: x in global memory (read through L2),
-// else in shared memory
-template <bool kGlobal>
-__device__ __forceinline__ void superstep(float (&c0)[4], float (&c1)[4], const RowQ &ra,
-                                          const RowQ &rb, int i, const uint4 *x0, const uint4 *x1,
-                                          bool two) {
+// columns' N-side values x[nb] (uint4 per 8 columns, stride 1) of the
+// column blocks nb < nblk; kGlobal: x in global memory (read through L2),
+// else in shared memory.  The weights are rebuilt once for all blocks.
+// the N-side pointers of a unit's column blocks
+template <int NB>
+struct Cols {
+  const uint4 *p[NB];
+};
+
+template <bool kGlobal, int NB, int P>
+__device__ __forceinline__ void superstep(float (&c)[NB][4], const RowQ<P> &ra, const RowQ<P> &rb,
+                                          int i, const Cols<NB> xb, int off, int nblk) {
   const __nv_bfloat162 sa = bcast(ra.s[i]), ba = bcast(ra.b[i]);
   const __nv_bfloat162 sb = bcast(rb.s[i]), bb = bcast(rb.b[i]);
   const uint32_t wa[4] = {ra.c[i].x, ra.c[i].y, ra.c[i].z, ra.c[i].w};
   const uint32_t wb[4] = {rb.c[i].x, rb.c[i].y, rb.c[i].z, rb.c[i].w};
-  // h from global memory was written by the gate/up kernel: coherent loads,
-  // all issued before the first MMA that uses them
-  uint4 v0[4], v1[4];
+  if constexpr (NB <= 2) {
+    // every N-side value first (h from global memory was written by the
+    // gate/up kernel: coherent loads, all issued before the first MMA that
+    // uses them), then the weights of each step, rebuilt once for the blocks
+    uint4 v[NB][4];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    v0[s] = kGlobal ? ld_cg16(x0 + s) : x0[s];
-    if (two) v1[s] = kGlobal ? ld_cg16(x1 + s) : x1[s];
-  }
+    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const uint4 a = dq8(wa[s], sa, ba), b = dq8(wb[s], sb, bb);
-    gv_step(c0, a, b, v0[s]);
-    if (two) gv_step(c1, a, b, v1[s]);
+      for (int s = 0; s < 4; ++s)
+        if (nb < nblk) v[nb][s] = kGlobal ? ld_cg16(xb.p[nb] + off + s) : xb.p[nb][off + s];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint4 a = dq8(wa[s], sa, ba), b = dq8(wb[s], sb, bb);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        if (nb < nblk) gv_step(c[nb], a, b, v[nb][s]);
+    }
+  } else {
+    // the weights of the super-step rebuilt once, then block by block its N
+    // side (four loads issued together) and MMAs
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      a[s] = dq8(wa[s], sa, ba);
+      b[s] = dq8(wb[s], sb, bb);
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      if (nb < nblk) {
+        uint4 v[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) v[s] = kGlobal ? ld_cg16(xb.p[nb] + off + s) : xb.p[nb][off + s];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) gv_step(c[nb], a[s], b[s], v[s]);
+      }
+    }
   }
 }
 }  // namespace
 
 // gate/up: unit u = (touched group u / (F / 8), features 8 (u % (F / 8)) ..);
 // pair p of CTA b takes units b + grid (p + 8 i); warp p takes the first half
-// of d, warp p + 8 the second.
+// of d, warp p + 8 the second.  NB: 8-column blocks of a group, at most 4.
+template <int NB>
 __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_q4_kernel(SmallQ4Args qa) {
+  constexpr int P = pre_for<NB>();
   const SmallArgs &a = qa.a;
   extern __shared__ uint4 s_dyn[];  // pair partials, then the tokens [T][d / 8 + 4]
   __shared__ int s_off[257], s_grp[257], s_ng;
-  __shared__ int s_perm[kSmallRouteT * kMaxTopK];
+  __shared__ int s_perm[kSmallGemvT * kMaxTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int pair = warp % kPairs, half = warp / kPairs;
   const int d = a.d, F = a.F, vr = d / 8, rs = vr + 4;
@@ -123,7 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_q4_kernel(SmallQ4
   const int col0 = half * (d / 2) + 32 * c;  // this lane's first column
   const int stride = gridDim.x * kPairs;
   float *s_part = reinterpret_cast<float *>(s_dyn);
-  uint4 *s_tok = s_dyn + kPairBytes / 16;
+  uint4 *s_tok = s_dyn + pair_bytes<NB>() / 16;
   const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
   for (int i = threadIdx.x; i < a.T * vr; i += blockDim.x) {
     const int t = i / vr;
@@ -153,37 +193,44 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_q4_kernel(SmallQ4
     const uint4 *cg = reinterpret_cast<const uint4 *>(mg.c + row * (d / 2) + col0 / 2);
     const uint4 *cu = reinterpret_cast<const uint4 *>(mu.c + row * (d / 2) + col0 / 2);
     const long long sbo = row * (d / 64) + col0 / 64;
-    const int m0 = min(g, n - 1), m1 = min(8 + g, n - 1);
-    const uint4 *x0 = s_tok + (sh ? m0 : s_perm[slot0 + m0]) * rs + col0 / 8;
-    const uint4 *x1 = s_tok + (sh ? m1 : s_perm[slot0 + m1]) * rs + col0 / 8;
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int J0 = 0; J0 < nss; J0 += kPre) {
-      RowQ ra, rb;
-      load_rowq(ra, cg, mg.s + sbo, mg.b + sbo, J0, nss);
-      load_rowq(rb, cu, mu.s + sbo, mu.b + sbo, J0, nss);
+    Cols<NB> xc;
 #pragma unroll
-      for (int i = 0; i < kPre; ++i)
-        if (J0 + i < nss) superstep<false>(c0, c1, ra, rb, i, x0 + 16 * (J0 + i), x1 + 16 * (J0 + i), n > 8);
+    for (int nb = 0; nb < NB; ++nb) {
+      const int m = min(8 * nb + g, n - 1);
+      xc.p[nb] = s_tok + (sh ? m : s_perm[slot0 + m]) * rs + col0 / 8;
     }
-    float *buf = s_part + ((it & 1) * kPairs + pair) * 256 + lane;
+    const int nblk = (n + 7) / 8;
+    float cacc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cacc[nb][i] = 0.f;
+    for (int J0 = 0; J0 < nss; J0 += P) {
+      RowQ<P> ra, rb;
+      load_rowq<P>(ra, cg, mg.s + sbo, mg.b + sbo, J0, nss);
+      load_rowq<P>(rb, cu, mu.s + sbo, mu.b + sbo, J0, nss);
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        if (J0 + i < nss) superstep<false, NB, P>(cacc, ra, rb, i, xc, 16 * (J0 + i), nblk);
+      }
+    }
+    float *buf = s_part + ((it & 1) * kPairs + pair) * (4 * NB * 32) + lane;
     if (half == 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        buf[32 * i] = c0[i];
-        buf[32 * (4 + i)] = c1[i];
-      }
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) buf[32 * (4 * nb + i)] = cacc[nb][i];
     }
     named_bar_sync(1 + pair, 64);
     if (half == 1) continue;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      c0[i] += buf[32 * i];
-      c1[i] += buf[32 * (4 + i)];
-    }
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cacc[nb][i] += buf[32 * (4 * nb + i)];
     __nv_bfloat16 *hp = a.h + static_cast<long long>(slot0) * F + f0 + g;
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      const float *cc = nb ? c1 : c0;
+    for (int nb = 0; nb < NB; ++nb) {
+      const float *cc = cacc[nb];
       const int m = 8 * nb + 2 * c;
       if (m < n) hp[static_cast<long long>(m) * F] = __float2bfloat16_rn(silu(cc[0]) * cc[2]);
       if (m + 1 < n) hp[static_cast<long long>(m + 1) * F] = __float2bfloat16_rn(silu(cc[1]) * cc[3]);
@@ -193,7 +240,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_gateup_q4_kernel(SmallQ4
 
 // down: unit u = (touched group u / (d / 16), rows 16 (u % (d / 16)) ..);
 // warp w of CTA b takes units b + grid (w + 16 i), each over the whole of F.
+// NB: 8-column blocks of a group, at most 4.
+template <int NB>
 __global__ void __launch_bounds__(kWarps * 32, 1) small_down_q4_kernel(SmallQ4Args qa) {
+  constexpr int P = pre_down<NB>();
   const SmallArgs &a = qa.a;
   __shared__ int s_off[257], s_grp[257], s_ng;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -215,21 +265,31 @@ __global__ void __launch_bounds__(kWarps * 32, 1) small_down_q4_kernel(SmallQ4Ar
     const uint4 *ca = reinterpret_cast<const uint4 *>(md.c + ra0 * (F / 2)) + c;
     const uint4 *cb = reinterpret_cast<const uint4 *>(md.c + (ra0 + 8) * (F / 2)) + c;
     const long long sa = ra0 * (F / 64) + c / 2, sb = (ra0 + 8) * (F / 64) + c / 2;
-    const uint4 *h0 = reinterpret_cast<const uint4 *>(a.h + static_cast<long long>(slot0 + min(g, n - 1)) * F) + 4 * c;
-    const uint4 *h1 = reinterpret_cast<const uint4 *>(a.h + static_cast<long long>(slot0 + min(8 + g, n - 1)) * F) + 4 * c;
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int J0 = 0; J0 < nss; J0 += kPre) {
-      RowQ qa0, qb0;
-      load_rowq(qa0, ca, md.s + sa, md.b + sa, J0, nss);
-      load_rowq(qb0, cb, md.s + sb, md.b + sb, J0, nss);
+    Cols<NB> hc;
 #pragma unroll
-      for (int i = 0; i < kPre; ++i)
-        if (J0 + i < nss) superstep<true>(c0, c1, qa0, qb0, i, h0 + 16 * (J0 + i), h1 + 16 * (J0 + i), n > 8);
+    for (int nb = 0; nb < NB; ++nb)
+      hc.p[nb] = reinterpret_cast<const uint4 *>(
+                   a.h + static_cast<long long>(slot0 + min(8 * nb + g, n - 1)) * F) +
+               4 * c;
+    const int nblk = (n + 7) / 8;
+    float cacc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cacc[nb][i] = 0.f;
+    for (int J0 = 0; J0 < nss; J0 += P) {
+      RowQ<P> qa0, qb0;
+      load_rowq<P>(qa0, ca, md.s + sa, md.b + sa, J0, nss);
+      load_rowq<P>(qb0, cb, md.s + sb, md.b + sb, J0, nss);
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        if (J0 + i < nss) superstep<true, NB, P>(cacc, qa0, qb0, i, hc, 16 * (J0 + i), nblk);
+      }
     }
     __nv_bfloat16 *yp = a.y + static_cast<long long>(slot0) * d + r0 + g;
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      const float *cc = nb ? c1 : c0;
+    for (int nb = 0; nb < NB; ++nb) {
+      const float *cc = cacc[nb];
       const int m = 8 * nb + 2 * c;
       if (m < n) {
         yp[static_cast<long long>(m) * d] = __float2bfloat16_rn(cc[0]);
@@ -258,21 +318,34 @@ cudaError_t launch_q4(K kern, int grid, size_t smem, cudaStream_t st, bool pdl, 
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
-constexpr size_t kGateUpSmemMax = kPairBytes + kSmallRouteTokBytes + kSmallRouteT * 64;
+// the tokens of at most 16 (32) rows of d = 2048 and the pair partials of 2
+// (4) column blocks (the bf16 small-batch GEMV's plan: small_gemv_fits
+// decides for both)
+constexpr size_t kTokBytes16 = 16 * (2048 / 8 + 4) * 16;
+constexpr size_t kGateUpSmemMax2 = pair_bytes<2>() + kTokBytes16;
+constexpr size_t kGateUpSmemMax4 = pair_bytes<4>() + 2 * kTokBytes16;
 }  // namespace
 
 cudaError_t launch_small_gateup_q4(const SmallQ4Args &a, int grid, cudaStream_t st, bool pdl) {
-  const size_t smem = kPairBytes + static_cast<size_t>(a.a.T) * (a.a.d / 8 + 4) * 16;
-  return launch_q4(small_gateup_q4_kernel, grid, smem, st, pdl, a);
+  const int T = a.a.T;
+  const size_t tok = static_cast<size_t>(T) * (a.a.d / 8 + 4) * 16;
+  return T <= 16 ? launch_q4(small_gateup_q4_kernel<2>, grid, pair_bytes<2>() + tok, st, pdl, a)
+                 : launch_q4(small_gateup_q4_kernel<4>, grid, pair_bytes<4>() + tok, st, pdl, a);
 }
 
 cudaError_t launch_small_down_q4(const SmallQ4Args &a, int grid, cudaStream_t st, bool pdl) {
-  return launch_q4(small_down_q4_kernel, grid, 0, st, pdl, a);
+  return a.a.T <= 16 ? launch_q4(small_down_q4_kernel<2>, grid, 0, st, pdl, a)
+                     : launch_q4(small_down_q4_kernel<4>, grid, 0, st, pdl, a);
 }
 
 cudaError_t small_gemv_q4_set_attr() {
-  return cudaFuncSetAttribute(small_gateup_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kGateUpSmemMax);
+  cudaError_t e = cudaFuncSetAttribute(small_gateup_q4_kernel<2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kGateUpSmemMax2));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(small_gateup_q4_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGateUpSmemMax4));
+  return e;
 }
 
 }  // namespace moe

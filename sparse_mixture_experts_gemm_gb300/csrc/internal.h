@@ -61,8 +61,12 @@ struct GemmParams {
   int32_t *cand_i;
   int32_t *tok_cnt;        // [T] blocks finished per token, zero between calls
   int *tile_ctr;           // grouped GEMMs: tiles claimed after each CTA's first, zero before the launch
-  // gate/up GEMM: routed A rows are gathered from the tokens
+  // gate/up GEMM: routed A rows are gathered from the tokens, row r of group
+  // g's M tile m from token list[g * list_stride + m * 128 + r] (the router's
+  // per-expert token lists) or, with list null, perm[slot]
   const int32_t *perm;     // [A] token of each slot
+  int32_t *list;           // [E][list_stride] tokens of each group in rank order
+  long long list_stride;
   const void *x;           // [T][K] the chunk's tokens
   unsigned *done;          // CTA completion ticket, zero at the launch; the last CTA clears it
   int32_t *clear;          // router: n_clear words (128 bytes apart) the last CTA zeroes
@@ -84,10 +88,14 @@ cudaError_t gemm_set_smem_attr();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
 // route_small.cu: routing of batches of at most kSmallRouteT bf16 tokens
-// (T * d * 2 <= kSmallRouteTokBytes) in one cluster launch: writes idx, w,
+// (tokens in passes of kSmallRoutePass, a pass's tokens within
+// kSmallRouteTokBytes) in one cluster launch: writes idx, w,
 // inv (slots), perm, offsets and zeroes the n_clear words clear[32 q].
-constexpr int kSmallRouteT = 16;
+constexpr int kSmallRouteT = 64;
+constexpr int kSmallRoutePass = 16;
 constexpr int kSmallRouteTokBytes = 65536;
+// gemv_small.cu: the grouped GEMVs take batches of at most kSmallGemvT tokens
+constexpr int kSmallGemvT = 32;
 // counts_out (may be null): each expert's group size is added to it.
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,
@@ -98,7 +106,7 @@ cudaError_t route_small_set_attr();
 // gemv_small.cu: gate/up (h = silu(gate) * up as bf16 rows) and down (bf16
 // rows of Y) of a small batch as a grouped GEMV on warp-level MMAs; the units
 // (16 weight rows of one touched expert) are found on the device from the
-// routing step's offsets.  Tokens T <= kSmallRouteT, bf16.
+// routing step's offsets.  Tokens T <= kSmallGemvT, bf16.
 struct SmallArgs {
   const __nv_bfloat16 *x;                 // [T][d]
   const __nv_bfloat16 *wg, *wu, *wd;      // routed experts
@@ -154,10 +162,13 @@ cudaError_t launch_offsets(int32_t *counts, int E, int32_t *offsets, int32_t *co
 cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *rank_inv,
                          int32_t *perm, int A, int k, int E, int *status, cudaStream_t st,
                          bool pdl = false);
+// inv[t][j]: the slot (row of Y) of assignment (t, j); with offsets given,
+// its rank inside the group of expert idx[t][j] (slot = offsets[e] + rank)
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
-                           bool pdl = false);
+                           bool pdl = false, const int32_t *idx = nullptr,
+                           const int32_t *offsets = nullptr, int E = 0);
 
 // 4-bit group-affine matrix (codes two per byte, even column in the low
 // nibble; one bf16 scale and bias per 64 columns of a row)
@@ -207,6 +218,7 @@ struct DecodeArgs {
   float *sel_w;
   int32_t *sel_counts;
 };
+
 // decode_q4.cu: the batch-1 kernels for 4-bit expert weights (bf16 tokens,
 // bf16 router) and the quantiser
 cudaError_t launch_decode_router_q4(const DecodeArgs &a, cudaStream_t st, bool pdl);

@@ -115,6 +115,7 @@ struct moe_handle {
   int32_t *cand_i = nullptr;
   int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
   int32_t *perm = nullptr;  // [A] token of each slot
+  int32_t *list = nullptr;  // [E][max_tokens] tokens of each expert group in rank order
   void *hbuf = nullptr, *yp = nullptr;
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
@@ -217,10 +218,11 @@ struct ProfScope {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-// The bf16 router: tcgen05 logits with top-k, weights, ranks and the
-// per-expert histogram in the epilogue; the last CTA writes the offsets.
+// The bf16 router: tcgen05 logits with top-k, weights, ranks, the
+// per-expert token lists (when list is given) and the histogram in the
+// epilogue; the last CTA writes the offsets.
 int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w, int32_t *rank,
-                     int32_t *offsets, int32_t *counts_out, cudaStream_t st) {
+                     int32_t *list, int32_t *offsets, int32_t *counts_out, cudaStream_t st) {
   const moe_config &c = h->cfg;
   CUtensorMap tm_x;
   if (!make_map(&tm_x, x, 2, T, c.d_model, kBM)) return MOE_ERR_CUDA;
@@ -248,6 +250,8 @@ int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w
   p.counts = h->counts();
   p.counts_out = counts_out;
   p.rank = rank;
+  p.list = list;
+  p.list_stride = c.max_tokens;
   p.offsets_out = offsets;
   p.done = h->done();
   p.clear = h->tile_ctr(0);
@@ -269,9 +273,11 @@ struct RouteOut {
   int32_t *counts = nullptr;
 };
 
-// a chunk of Tc bf16 tokens routes in one cluster launch
+// a chunk of Tc bf16 tokens routes in one cluster launch (tokens in passes
+// of kSmallRoutePass, each pass staged in shared memory)
 bool small_route_ok(int Tc, int d) {
-  return Tc <= kSmallRouteT && static_cast<long long>(Tc) * d * 2 <= kSmallRouteTokBytes;
+  const int pass = Tc < kSmallRoutePass ? Tc : kSmallRoutePass;
+  return Tc <= kSmallRouteT && static_cast<long long>(pass) * d * 2 <= kSmallRouteTokBytes;
 }
 
 template <typename T>
@@ -296,7 +302,10 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   } else {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
-      const int rc = launch_router_tc(h, x, Tc, idx, wts, h->inv, h->offsets, ro.counts, st);
+      // tokens into per-expert lists, ranks into inv: no placement step (the
+      // combine adds each assignment's group offset to its rank)
+      const int rc =
+          launch_router_tc(h, x, Tc, idx, wts, h->inv, h->list, h->offsets, ro.counts, st);
       if (rc != MOE_OK) return rc;
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
@@ -308,12 +317,19 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   // waiting for its predecessor inside (event records between kernels would
   // break the chain, so not while profiling)
   const bool pdl = !h->prof;
-  if (!small) {
+  // the tensor-core router writes per-expert token lists, from which the
+  // gate/up GEMM gathers its rows; the fp32 router's ranks become slots and
+  // a slot permutation in a placement step
+  const bool lists = sizeof(T) == 2 && !small;
+  if (!small && !lists) {
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
     MOE_TRY(launch_place(idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
   }
   if (small && small_gemv_fits(Tc, d, F)) {
-    // every touched expert gets one or two rows: grouped GEMV over all SMs
+    // at most 32 tokens: every touched expert gets a few rows, grouped GEMV
+    // over all SMs (the tensor-core tiles of 128 rows would stay mostly empty
+    // and leave most SMs idle); up to 64 tokens the routing is still the
+    // cluster launch and the grouped GEMMs follow
     SmallArgs sa;
     sa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
     sa.wg = static_cast<const __nv_bfloat16 *>(c.w_gate);
@@ -337,12 +353,12 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     qa.a = sa;
     qa.w = h->qw;
     {
-      ProfScope ps(h, MOE_KERNEL_GEMM_GATE_UP, st);
+      ProfScope ps(h, MOE_KERNEL_GEMV_GATE_UP, st);
       MOE_TRY(h->q4 ? launch_small_gateup_q4(qa, h->num_sms, st, pdl)
                     : launch_small_gateup(sa, h->num_sms, st, pdl));
     }
     {
-      ProfScope ps(h, MOE_KERNEL_GEMM_DOWN, st);
+      ProfScope ps(h, MOE_KERNEL_GEMV_DOWN, st);
       MOE_TRY(h->q4 ? launch_small_down_q4(qa, h->num_sms, st, pdl)
                     : launch_small_down(sa, h->num_sms, st, pdl));
     }
@@ -378,6 +394,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.kid = KID_GEMM_GATE_UP;
     p.tile_ctr = h->tile_ctr(0);
     p.perm = h->perm;
+    p.list = lists ? h->list : nullptr;
+    p.list_stride = c.max_tokens;
     p.x = x;
     if (h->q4) {  // 4-bit weights (bf16 tokens): dequantised in the GEMM
       Q4GemmMaps mq = h->q4g;
@@ -410,7 +428,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
-                              c.n_shared, h->status, st, pdl));
+                              c.n_shared, h->status, st, pdl, lists ? idx : nullptr,
+                              lists ? h->offsets : nullptr, E));
   }
   return MOE_OK;
 }
@@ -573,6 +592,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
       {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
       {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},
       {reinterpret_cast<void **>(&h->perm), sizeof(int32_t) * A},
+      {reinterpret_cast<void **>(&h->list), sizeof(int32_t) * E * static_cast<size_t>(Tm)},
       {&h->hbuf, esz * (A + Tm) * F},
       {&h->yp, esz * (A + Tm) * d},
   };
@@ -728,7 +748,7 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   if (c.dtype == MOE_BF16) {
     // the router's last CTA adds the histogram to counts
     MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
-    return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, counts, st);
+    return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, nullptr, counts, st);
   }
   MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
   MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),
@@ -743,10 +763,13 @@ namespace {
 // where every chunk takes the small-batch kernels
 int forward_shape_ok(const moe_handle *h, int T) {
   if (h->q4 && T != 1 && !h->q4_prefill) {
-    const int c0 = std::min(T, h->cfg.max_tokens);
-    if (T > kSmallRouteT || !small_route_ok(c0, h->cfg.d_model) ||
-        !small_gemv_fits(c0, h->cfg.d_model, h->cfg.d_ff))
-      return MOE_ERR_UNSUPPORTED;
+    // 4-bit shapes the grouped GEMMs do not take: every chunk (full ones of
+    // max_tokens, then the rest) must run on the small-batch kernels
+    const int d = h->cfg.d_model, F = h->cfg.d_ff;
+    const int c0 = std::min(T, h->cfg.max_tokens), rest = T % c0;
+    for (const int Tc : {c0, rest})
+      if (Tc > 0 && !(small_route_ok(Tc, d) && small_gemv_fits(Tc, d, F)))
+        return MOE_ERR_UNSUPPORTED;
   }
   return MOE_OK;
 }
@@ -899,10 +922,10 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
   if (cudaMemcpy(s, h->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->status, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
   // an aborted launch can leave the router's per-token arrival counts, its
-  // histogram and ticket, or the GEMMs' tile counters behind
-  if (s[0] != MOE_OK &&
-      (cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) != cudaSuccess ||
-       cudaMemset(h->route_ctl, 0, kRouteCtlBytes) != cudaSuccess))
+  // histogram and ticket or the GEMMs' tile counters behind
+  if (s[0] != MOE_OK && (cudaMemset(h->route_ctl, 0, kRouteCtlBytes) != cudaSuccess ||
+                         cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) !=
+                             cudaSuccess))
     return MOE_ERR_CUDA;
   if (detail) *detail = s[1];
   return s[0];

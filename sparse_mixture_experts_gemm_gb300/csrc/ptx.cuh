@@ -379,6 +379,16 @@ __device__ __forceinline__ uint4 ld_cg16(const void *p) {
                : "memory");
   return v;
 }
+// 16-byte load of data a completed predecessor grid wrote, read once after
+// griddepcontrol.wait: the coherent path, without allocating in L1.
+__device__ __forceinline__ uint4 ld_na16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 ld_cg_f32x4(const float *p) {
   float4 v;
   asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -267,14 +267,18 @@ cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *ra
 // ---------------------------------------------------------------- combine
 // One thread per 16-byte chunk of an output row; the k routed contributions
 // are added in choice order (deterministic), then the shared expert's row.
-// Y, the slots and the weights were written by kernels earlier in the launch
-// chain (Y by the one this kernel waits for): all are read through L2 after
-// the wait, never through the non-coherent path.
+// inv holds each assignment's slot (row of Y) or, when offsets is given, its
+// rank inside its expert's group, to which the group's offset is added (the
+// expert is idx's entry).  Y, the slots, ranks, offsets and weights were
+// written by kernels earlier in the launch chain (Y by the one this kernel
+// waits for): all are read after the wait (an asm with a memory clobber),
+// never through the non-coherent path; Y without allocating in L1.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t *inv,
                                                       const float *w, T *out, int T_tok, int k,
                                                       int d, int A_total, int n_shared,
-                                                      int *status) {
+                                                      int *status, const int32_t *idx,
+                                                      const int32_t *offsets, int E) {
   // a programmatic dependent of the down GEMM (or GEMV): yp is read after
   // the wait
   pdl_wait();
@@ -291,11 +295,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
   const int lane = threadIdx.x & 31;
   int my_slot = 0;
   float my_w = 0.0f;
-  if (lane < k) my_slot = ld_cg_s32(inv + static_cast<long long>(t) * k + lane);
-  if (lane >= 16 && lane - 16 < k) my_w = ld_cg_f32(w + static_cast<long long>(t) * k + lane - 16);
+  bool bad = false;
+  if (lane < k) {
+    const long long o = static_cast<long long>(t) * k + lane;
+    my_slot = inv[o];
+    if (offsets) {
+      const int e = idx[o];
+      if (e < 0 || e >= E) bad = true;
+      else my_slot += offsets[e];
+    }
+  }
+  if (lane >= 16 && lane - 16 < k) my_w = w[static_cast<long long>(t) * k + lane - 16];
   int slot[kMaxTopK];
   float wt[kMaxTopK];
-  bool bad = false;
+  bad = __any_sync(0xffffffffu, bad);
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
@@ -309,8 +322,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
   uint4 v[kMaxTopK + 1];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) v[j] = ld_cg16(yp + static_cast<long long>(slot[j]) * d + c * NV);
-  if (n_shared) v[kMaxTopK] = ld_cg16(yp + static_cast<long long>(A_total + t) * d + c * NV);
+    if (j < k) v[j] = ld_na16(yp + static_cast<long long>(slot[j]) * d + c * NV);
+  if (n_shared) v[kMaxTopK] = ld_na16(yp + static_cast<long long>(A_total + t) * d + c * NV);
   float acc[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
@@ -335,18 +348,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
-                           bool pdl) {
+                           bool pdl, const int32_t *idx, const int32_t *offsets, int E) {
   const long long threads = static_cast<long long>(T_tok) * (d / Vec<T>::N);
   const int grid = static_cast<int>((threads + 255) / 256);
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_config(grid, 256, st, pdl, &attr);
   return cudaLaunchKernelEx(&cfg, combine_kernel<T>, yp, inv, w, out, T_tok, k, d, A_total,
-                            n_shared, status);
+                            n_shared, status, idx, offsets, E);
 }
 template cudaError_t launch_combine<float>(const float *, const int32_t *, const float *, float *, int,
-                                           int, int, int, int, int *, cudaStream_t, bool);
+                                           int, int, int, int, int *, cudaStream_t, bool,
+                                           const int32_t *, const int32_t *, int);
 template cudaError_t launch_combine<__nv_bfloat16>(const __nv_bfloat16 *, const int32_t *,
                                                    const float *, __nv_bfloat16 *, int, int, int, int,
-                                                   int, int *, cudaStream_t, bool);
+                                                   int, int *, cudaStream_t, bool, const int32_t *,
+                                                   const int32_t *, int);
 
 }  // namespace moe

@@ -1,4 +1,4 @@
-// route_small.cu -- the whole routing step of a small batch (T <= 16 bf16
+// route_small.cu -- the whole routing step of a small batch (T <= 64 bf16
 // tokens) in one launch: logits, top-k, weights, histogram, group offsets and
 // the slot permutation.
 //
@@ -10,8 +10,9 @@
 // the grid); here one thread-block cluster of ceil(E / 16) CTAs does it: CTA
 // c multiplies the router rows of experts 16 c .. 16 c + 15 with the batch's
 // tokens (the small-batch main loop: its 16 warps split d, weights requested
-// before the tokens arrive, warp-level MMAs), and each logit goes straight
-// into CTA 0's shared memory; after one cluster barrier CTA 0 takes each
+// before the tokens arrive, warp-level MMAs; the tokens in passes of 16, the
+// router rows coming from L2 after the first pass), and each logit goes
+// straight into CTA 0's shared memory; after one cluster barrier CTA 0 takes each
 // token's top-k (one warp per token), the
 // rank of every assignment inside its expert's group (the number of earlier
 // assignments, in (token, choice) order, to the same expert), the exclusive
@@ -32,13 +33,14 @@ namespace moe {
 namespace {
 constexpr int kRouteWarps = kGvWarps;
 
-// logits of experts 16 u .. 16 u + 15 for all tokens (one unit per CTA)
+// logits of experts 16 u .. 16 u + 15 for the pass's tokens t0 .. t0 + T - 1
+// (one unit per CTA)
 struct RouterOp {
   const __nv_bfloat16 *x, *wr;
   const float *bias;
   uint4 *s_tok;
   float (*s_lg)[256];
-  int T, d, E, rs, nsteps, first, stride;
+  int T, t0, d, E, rs, nsteps, first, stride;
   __device__ void prepare() {
     first = blockIdx.x;
     stride = gridDim.x;
@@ -71,7 +73,7 @@ struct RouterOp {
     float v = 0.0f;
 #pragma unroll
     for (int w = 0; w < kGvWarps; ++w) v += red[w * 256 + gv_part(r, m)];
-    st_cluster_f32(&s_lg[m][e], 0, v + (bias ? bias[e] : 0.0f));
+    st_cluster_f32(&s_lg[t0 + m][e], 0, v + (bias ? bias[e] : 0.0f));
   }
 };
 }  // namespace
@@ -81,8 +83,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32, 1)
                        const float *__restrict__ bias, int T, int d, int E, int k, int32_t *idx,
                        float *w, int32_t *inv, int32_t *perm, int32_t *offsets,
                        int32_t *counts_out, int32_t *clear, int n_clear) {
-  extern __shared__ uint4 s_dyn[];  // partial tiles, then [T][d / 8 + 4] tokens
-  __shared__ float s_lg[kSmallRouteT][256];  // CTA 0: the logits
+  // partial tiles, then [kSmallRoutePass][d / 8 + 4] tokens, then (read in
+  // CTA 0) the logits [T][256]
+  extern __shared__ uint4 s_dyn[];
   __shared__ int s_idx[kSmallRouteT][kMaxTopK];
   __shared__ float s_w[kSmallRouteT][kMaxTopK];
   __shared__ int s_rank[kSmallRouteT * kMaxTopK];
@@ -92,34 +95,41 @@ __global__ void __launch_bounds__(kRouteWarps * 32, 1)
   // the next launch (the expert gate/up) may start its routing-independent
   // reads now: it waits for this grid before it reads any of its outputs
   pdl_launch_dependents();
-  RouterOp op;
-  op.x = x;
-  op.wr = wr;
-  op.bias = bias;
-  op.s_tok = s_dyn + kGvRedBytes / 16;
-  op.s_lg = s_lg;
-  op.T = T;
-  op.d = d;
-  op.E = E;
-  op.rs = d / 8 + 4;
-  op.nsteps = d / 32;
-  gv_run<1>(op, reinterpret_cast<float *>(s_dyn));
+  const int rs = d / 8 + 4;
+  float(*s_lg)[256] =
+      reinterpret_cast<float(*)[256]>(s_dyn + kGvRedBytes / 16 + kSmallRoutePass * rs);
+  for (int t0 = 0; t0 < T; t0 += kSmallRoutePass) {
+    RouterOp op;
+    op.x = x + static_cast<long long>(t0) * d;
+    op.wr = wr;
+    op.bias = bias;
+    op.s_tok = s_dyn + kGvRedBytes / 16;
+    op.s_lg = s_lg;
+    op.T = min(kSmallRoutePass, T - t0);
+    op.t0 = t0;
+    op.d = d;
+    op.E = E;
+    op.rs = rs;
+    op.nsteps = d / 32;
+    gv_run<1>(op, reinterpret_cast<float *>(s_dyn));
+  }
   cluster_sync_all();  // every CTA of the cluster reaches this: no return above
   if (cluster_ctarank() != 0) return;
 
   // CTA 0: one warp per token takes its top-k and the softmax over them
-  if (warp < T) {
+  for (int t = warp; t < T; t += kRouteWarps) {
     unsigned key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int ee = lane + 32 * i;
-      key[i] = ee < E ? fkey(s_lg[warp][ee]) : 0u;
+      key[i] = ee < E ? fkey(s_lg[t][ee]) : 0u;
     }
-    topk_from_keys(key, E, k, lane, s_idx[warp], s_w[warp]);
+    topk_from_keys(key, E, k, lane, s_idx[t], s_w[t]);
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   // rank of assignment a = t k + j among the earlier ones with the same expert
+  // (A = T k <= 512, the CTA's threads)
   const int A = T * k;
   const int a = threadIdx.x;
   int ea = 0;
@@ -182,7 +192,8 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncta);
   cfg.blockDim = dim3(kRouteWarps * 32);
-  cfg.dynamicSmemBytes = kGvRedBytes + static_cast<size_t>(T) * (d / 8 + 4) * 16;
+  cfg.dynamicSmemBytes = kGvRedBytes + static_cast<size_t>(kSmallRoutePass) * (d / 8 + 4) * 16 +
+                         static_cast<size_t>(T) * 256 * 4;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -198,7 +209,8 @@ cudaError_t launch_route_small(const void *x, const void *wr, const float *bias,
 
 cudaError_t route_small_set_attr() {
   cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kGvRedBytes + kSmallRouteTokBytes + kSmallRouteT * 64);
+                                       kGvRedBytes + kSmallRouteTokBytes + kSmallRoutePass * 64 +
+                                           kSmallRouteT * 256 * 4);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;

@@ -93,12 +93,12 @@ def test_pageable_host_buffers(dev):
 
 
 def test_unsupported_batch_is_refused_before_any_copy(dev):
-    """A 4-bit layer with F = 256 runs at most 16 tokens per batch: a 20-token
+    """A 4-bit layer with F = 256 runs at most 32 tokens per batch: a 40-token
     host call returns MOE_ERR_UNSUPPORTED and leaves the output untouched."""
     w = synth.q4_layer_weights(9, 1024, 256, 16, 1, dev)
-    layer = moe.Q4Layer(w, 4, max_tokens=32)
+    layer = moe.Q4Layer(w, 4, max_tokens=64)
     try:
-        x = _pinned(synth.tokens(46, 20, 1024, "bf16", "cpu"))
+        x = _pinned(synth.tokens(46, 40, 1024, "bf16", "cpu"))
         y = torch.zeros_like(x).pin_memory()
         with pytest.raises(moe.MoeError) as e:
             layer.forward_host(x, y)
@@ -106,7 +106,7 @@ def test_unsupported_batch_is_refused_before_any_copy(dev):
         layer.host_join()
         torch.cuda.synchronize()
         assert not y.any()
-        _issue_and_compare(layer, [x[:2].clone(), x[2:18].clone()])
+        _issue_and_compare(layer, [x[:2].clone(), x[2:34].clone()])
     finally:
         layer.close()
 

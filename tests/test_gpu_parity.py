@@ -97,12 +97,14 @@ def test_fp32_multi_tile(dev):
 
 def test_chunking_does_not_change_output(dev):
     """Tokens are independent, so the chunk size must not change a single bit
-    ("Bound temporary memory with request chunking")."""
+    ("Bound temporary memory with request chunking") among chunks that take
+    the same router: every chunk here holds more than 64 tokens (700 = 7 x
+    100 = 2 x 350 = 1 x 700)."""
     d, F, E, k, T = 512, 128, 32, 4, 700
     w = to_dev(synth.layer_weights(30, d, F, E, 1, "bf16", "cpu"), dev)
     x = synth.tokens(31, T, d, "bf16", "cpu").to(dev)
     outs = []
-    for mt in (128, 333, 1024):
+    for mt in (100, 350, 1024):
         layer = moe.MoELayer(w, k, max_tokens=mt)
         outs.append(layer.forward(x))
         torch.cuda.synchronize()
@@ -266,10 +268,12 @@ def test_long_prompt_128k_in_8k_chunks(dev):
         assert err.max() <= H.OUT_TOL, f"chunk {ci}: max row rel err {err.max():.3e}"
 
 
-@pytest.mark.parametrize("T", [2, 5, 16])
+@pytest.mark.parametrize("T", [2, 5, 16, 17, 32, 33, 64])
 def test_small_batch_routing_path(dev, T):
-    """Batches of at most 16 bf16 tokens route through one cluster launch (no
-    placement kernel): the full-size layer against the oracle, every output."""
+    """Batches of at most 64 bf16 tokens route through one cluster launch (no
+    placement kernel); at most 32 then take the grouped GEMV (two column
+    blocks up to 16 tokens, four beyond), larger ones the grouped GEMMs: the
+    full-size layer against the oracle, every output, and the kernel kinds."""
     d, F, E, k = 2048, 512, 256, 8
     w = synth.layer_weights(400 + T, d, F, E, 1, "bf16", dev)
     x = H.margined_tokens(410 + T, T, w["Wr"], k, "bf16", device=dev)
@@ -281,7 +285,9 @@ def test_small_batch_routing_path(dev, T):
         torch.cuda.synchronize()
         assert layer.status()[0] == 0
         kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
-        assert kinds == {"router", "gemm_gate_up", "gemm_down", "combine"}, kinds
+        want = ({"router", "gemv_gate_up", "gemv_down", "combine"} if T <= 32
+                else {"router", "gemm_gate_up", "gemm_down", "combine"})
+        assert kinds == want, kinds
     finally:
         layer.close()
     ref, *_ = H.oracle_forward(x, w, k)
@@ -296,11 +302,22 @@ def test_small_batch_with_router_bias(dev):
     run_case(dev, 44, 9, 512, 128, E, k, bias=bias)
 
 
-@pytest.mark.parametrize("T,E,k,n_shared", [(16, 4, 2, 1), (13, 8, 3, 0), (9, 2, 1, 1), (3, 8, 2, 0)])
+@pytest.mark.parametrize("T,E,k,n_shared", [(16, 4, 2, 1), (13, 8, 3, 0), (9, 2, 1, 1), (3, 8, 2, 0),
+                                            (32, 4, 2, 1), (29, 2, 1, 0), (24, 3, 2, 1)])
 def test_small_batch_crowded_experts(dev, T, E, k, n_shared):
-    """Small batches whose routed experts get more than 8 tokens (the second
-    column block of the grouped GEMV), with and without the shared expert."""
-    run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=16)
+    """Small batches whose routed experts get more than 8 (up to 32) tokens:
+    the second to fourth column blocks of the grouped GEMV, with and without
+    the shared expert."""
+    run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=32)
+
+
+def test_chunks_of_up_to_64_tokens_mix_paths(dev):
+    """130 tokens on a 48-token handle: chunks of 48 (cluster routing, grouped
+    GEMMs), 48 and 34 (the same), every output against the oracle; and 60
+    tokens on a 40-token handle: 40 (cluster routing, grouped GEMMs) then 20
+    (cluster routing, four-block grouped GEMV)."""
+    run_case(dev, 95, 130, 512, 128, 32, 4, max_tokens=48)
+    run_case(dev, 96, 60, 512, 128, 32, 4, max_tokens=40)
 
 
 def test_chunked_prefill_with_a_small_tail(dev):
@@ -324,7 +341,7 @@ def test_small_batch_beyond_the_router_limit(dev):
         torch.cuda.synchronize()
         assert layer.status()[0] == 0
         kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
-        assert "permute" in kinds, kinds
+        assert kinds == {"router", "gemm_gate_up", "gemm_down", "combine"}, kinds
     finally:
         layer.close()
     ref, *_ = H.oracle_forward(x, w, k)

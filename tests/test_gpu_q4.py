@@ -173,22 +173,34 @@ def test_q4_layer_stack_in_a_cuda_graph(dev):
 def test_q4_batches_need_d_and_f_multiples_of_512(dev):
     """The grouped GEMMs read scale/bias rows of 16-byte pitch: a layer with
     F = 256 runs batches only where every chunk takes the small-batch kernels
-    (at most 16 tokens) and refuses larger ones."""
+    (at most 32 tokens) and refuses larger ones; 2 and 20 tokens run (two and
+    four column blocks of the grouped GEMV) and match the oracle, and so do 40
+    tokens through a handle with 16-token chunks (16 + 16 + 8)."""
     w = synth.q4_layer_weights(9, 1024, 256, 16, 1, dev)
-    x = H.margined_tokens(10, 20, w["Wr"], 4, "bf16", device=dev)
-    layer = moe.Q4Layer(w, 4, max_tokens=32)
+    x = H.margined_tokens(10, 40, w["Wr"], 4, "bf16", device=dev)
+    layer = moe.Q4Layer(w, 4, max_tokens=64)
     try:
-        out = torch.empty((20, 1024), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((40, 1024), dtype=torch.bfloat16, device=dev)
         with pytest.raises(moe.MoeError) as e:
-            moe.moe_forward(layer.handle, x, 20, out)
+            moe.moe_forward(layer.handle, x, 40, out)
         assert e.value.code == moe.MOE_ERR_UNSUPPORTED
-        got = layer.forward(x[:2].clone())
+        got2 = layer.forward(x[:2].clone())
+        got20 = layer.forward(x[:20].clone())
         torch.cuda.synchronize()
         assert layer.status()[0] == 0
     finally:
         layer.close()
-    ref, *_ = _oracle_q4(x[:2], w, 4, 256)
-    assert H.row_rel_err(got, ref).max() <= H.OUT_TOL
+    chunked = moe.Q4Layer(w, 4, max_tokens=16)
+    try:
+        got40 = chunked.forward(x)
+        torch.cuda.synchronize()
+        assert chunked.status()[0] == 0
+    finally:
+        chunked.close()
+    ref, *_ = _oracle_q4(x, w, 4, 256)
+    assert H.row_rel_err(got2, ref[:2]).max() <= H.OUT_TOL
+    assert H.row_rel_err(got20, ref[:20]).max() <= H.OUT_TOL
+    assert H.row_rel_err(got40, ref).max() <= H.OUT_TOL
 
 
 # (d, F, E, k, n_shared, T, max_tokens)
@@ -247,11 +259,12 @@ def test_q4_prefill_4k_sample_against_oracle(dev):
     assert err.max() <= H.OUT_TOL, err.max()
 
 
-@pytest.mark.parametrize("T", [2, 7, 16])
+@pytest.mark.parametrize("T", [2, 7, 16, 17, 32, 33, 64])
 def test_q4_small_batch_path(dev, T):
-    """Batches of at most 16 tokens on 4-bit weights take the small-batch
-    kernels (one routing launch, the 4-bit grouped GEMV, the combine): the
-    full-size layer against the oracle, every output, and the kernel kinds."""
+    """Batches of at most 32 tokens on 4-bit weights take the small-batch
+    kernels (one routing launch, the 4-bit grouped GEMV, the combine), and up
+    to 64 the same routing launch before the grouped GEMMs: the full-size
+    layer against the oracle, every output, and the kernel kinds."""
     d, F, E, k = 2048, 512, 256, 8
     w = synth.q4_layer_weights(60 + T, d, F, E, 1, dev)
     x = H.margined_tokens(70 + T, T, w["Wr"], k, "bf16", device=dev)
@@ -263,7 +276,9 @@ def test_q4_small_batch_path(dev, T):
         torch.cuda.synchronize()
         assert layer.status()[0] == 0
         kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
-        assert kinds == {"router", "gemm_gate_up", "gemm_down", "combine"}, kinds
+        want = ({"router", "gemv_gate_up", "gemv_down", "combine"} if T <= 32
+                else {"router", "gemm_gate_up", "gemm_down", "combine"})
+        assert kinds == want, kinds
     finally:
         layer.close()
     ref, *_ = _oracle_q4(x, w, k, F)
