@@ -134,6 +134,17 @@ def test_q4_handle_routes_and_checks_batches(dev):
         layer.close()
 
 
+def _diff_report(a, b):
+    """Where two bf16 tensors differ bit-wise: count, first indices, NaNs,
+    largest difference."""
+    ne = a.view(torch.int16) != b.view(torch.int16)
+    idx = ne.nonzero()[:8].tolist()
+    diff = (a.float() - b.float()).abs().nan_to_num(0.0)
+    return (f"{int(ne.sum())} differing of {a.numel()} at {idx}, NaN {int(a.isnan().sum())}"
+            f"/{int(b.isnan().sum())}, max |diff| {diff.max().item():.4g}, "
+            f"max |a| {a.float().abs().nan_to_num(0.0).max().item():.4g}")
+
+
 def test_q4_layer_stack_in_a_cuda_graph(dev):
     """Four chained 4-bit layers captured once; replays equal eager runs bit for
     bit."""
@@ -162,7 +173,9 @@ def test_q4_layer_stack_in_a_cuda_graph(dev):
             for l in range(L):
                 h = layers[l].forward(h)
                 torch.cuda.synchronize()
-                assert torch.equal(got[l], h), f"step {step} layer {l}"
+                assert torch.equal(got[l].view(torch.int16), h.view(torch.int16)), (
+                    f"step {step} layer {l}: {_diff_report(got[l], h)}; "
+                    f"status {[lay.status() for lay in layers]}")
         for layer in layers:
             assert layer.status()[0] == 0
     finally:
