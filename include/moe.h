@@ -244,6 +244,24 @@ int moe_host_join(moe_handle *h, void *cuda_stream);
  */
 int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 
+/*
+ * Tuning options of a handle; each keeps its default until set, and no
+ * option changes a result bit (the same tiles are multiplied in the same
+ * order either way).
+ *   MOE_OPT_PAIR_MIN_TOKENS: chunks of at least this many tokens through a
+ *     bf16 handle run the grouped GEMMs on thread-block clusters of two CTAs
+ *     that multiply consecutive 128-row tiles of one expert group with the
+ *     same weight tile, each CTA loading half of the tile into both (section
+ *     "Match tile size to expert load": large groups share weight traffic).
+ *     Default 8192; 0 for every chunk, a value above max_tokens for none.
+ *     Ignored where the device cannot run such clusters.
+ * Host-side only, takes effect at the next call; not to be changed while
+ * a forward on the handle is being captured into a CUDA graph.
+ * Errors: INVALID_ARG (null handle, unknown option, negative value).
+ */
+#define MOE_OPT_PAIR_MIN_TOKENS 1
+int moe_set_option(moe_handle *h, int option, long long value);
+
 /* Free the workspace and the handle.  NULL is accepted.  The caller must make
  * sure no work using the handle is still running. */
 int moe_destroy(moe_handle *h);

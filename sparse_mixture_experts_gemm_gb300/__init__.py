@@ -32,11 +32,13 @@ MOE_ERR_OUT_OF_MEMORY = -7
 MOE_BF16 = 0
 MOE_F32 = 1
 
+MOE_OPT_PAIR_MIN_TOKENS = 1
+
 KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
                 "decode_gate_up", "decode_down", "gemv_gate_up", "gemv_down"]
 
 EXPORTED = ["moe_create", "moe_route", "moe_forward", "moe_forward_routed", "moe_forward_host",
-            "moe_host_join", "moe_status", "moe_destroy",
+            "moe_host_join", "moe_status", "moe_set_option", "moe_destroy",
             "moe_strerror", "moe_profile", "moe_profile_read", "moe_debug_wait_timeout",
             "moe_decode_noalloc", "moe_noalloc_status", "moe_create_q4", "moe_quantize_q4",
             "gdn_scan"]
@@ -95,6 +97,7 @@ def lib() -> ctypes.CDLL:
     L.moe_forward_host.argtypes = [vp, vp, ip, vp, vp]
     L.moe_host_join.argtypes = [vp, vp]
     L.moe_status.argtypes = [vp, vp, ctypes.POINTER(ip)]
+    L.moe_set_option.argtypes = [vp, ip, ctypes.c_longlong]
     L.moe_destroy.argtypes = [vp]
     L.moe_strerror.argtypes = [ip]
     L.moe_strerror.restype = ctypes.c_char_p
@@ -190,6 +193,10 @@ def moe_destroy(h: int) -> int:
 
 def moe_strerror(code: int) -> str:
     return strerror(code)
+
+
+def moe_set_option(h: int, option: int, value: int) -> int:
+    return _check(lib().moe_set_option(h, option, value), "moe_set_option")
 
 
 def moe_profile(h: int, enable: bool) -> int:
@@ -324,6 +331,9 @@ class MoELayer:
 
     def status(self, stream=None):
         return moe_status(self.handle, stream)
+
+    def set_option(self, option: int, value: int) -> None:
+        moe_set_option(self.handle, option, value)
 
     def close(self):
         if getattr(self, "handle", None):

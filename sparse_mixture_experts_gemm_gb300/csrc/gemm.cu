@@ -103,7 +103,7 @@ __device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i, int 
 template <int EPI>
 constexpr int gemm_threads() { return EPI == EPI_SWIGLU ? kThreads + kGatherThreads : kThreads; }
 
-template <typename T, int EPI, int BN>
+template <typename T, int EPI, int BN, bool kPair>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   constexpr bool kGather = (EPI == EPI_SWIGLU);  // routed A rows gathered by warps 6-9
   constexpr int kOutCols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
   constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  static_assert(!(kPair && kRouter), "the router runs one CTA per tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   int *s_last = reinterpret_cast<int *>(ctrl + 520);
   int *s_off = reinterpret_cast<int *>(ctrl + 1536);        // [E + 1]
   int *s_mt = reinterpret_cast<int *>(ctrl + 1536 + 1040);  // [E + 2]
+  int *s_it = reinterpret_cast<int *>(ctrl + 1536 + 2080);  // [E + 2], pair mode
   const TileRing ring{smem_u32(ctrl + 1056), smem_u32(ctrl + 1056 + 8 * kTileRing),
                       reinterpret_cast<volatile int *>(ctrl + 1024)};
   // readers of the ring: the MMA thread, 4 epilogue warps, 4 gather warps
@@ -142,12 +144,21 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   const int lane = threadIdx.x & 31;
   const long long limit = MOE_WAIT_LIMIT_CYCLES;
   const GroupTable gt{s_off, s_mt};
+  // pair mode: this CTA's rank in its cluster of two, the cluster's index
+  // and count (items are taken in a fixed order: cluster c runs items
+  // c, c + ncl, ...)
+  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cl = kPair ? static_cast<int>(blockIdx.x >> 1) : 0;
+  const int ncl = kPair ? static_cast<int>(gridDim.x >> 1) : 1;
+  constexpr uint16_t kBoth = 3;  // cluster mask of both CTAs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       // the TMA producer's expect-tx arrival, plus one per gather thread
       mbar_init(full0 + 8 * s, kGather ? 1 + kGatherThreads : 1);
-      mbar_init(empty0 + 8 * s, 1);
+      // pair mode: a stage is free when the MMAs of both CTAs are done with it
+      // (the partner's producer writes half of the weight tile into it)
+      mbar_init(empty0 + 8 * s, kPair ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -170,12 +181,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       prefetch_tmap(&tmB0s);
       prefetch_tmap(&tmB1s);
     }
-    if (EPI == EPI_STORE) prefetch_tmap(&tmB0s);
+    if (EPI == EPI_STORE) prefetch_tmap(kPair ? &tmB1s : &tmB0s);
+    if (EPI == EPI_STORE && kPair) prefetch_tmap(&tmB1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // pair mode: both CTAs' barriers exist before either writes into the other
+  if (kPair) cluster_sync_all();
   // Launched as a programmatic dependent, everything above overlaps the tail
   // of the previous kernel: none of it touches global memory.  The wait
   // returns once that kernel has completed and its writes are visible; the
@@ -194,6 +208,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (!kRouter) ntiles = p.nt * s_mt[p.n_routed + 1];
+  if (kPair) {
+    build_item_table(p, s_mt, s_it, warp, lane);
+    __syncthreads();
+    ntiles = s_it[p.n_routed + 1];
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -204,8 +223,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
-      int ti = blockIdx.x + it * gridDim.x;
-      if (!kRouter) {
+      int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
+      if (!kRouter && !kPair) {
         int c_ok = 1;
         if (lane == 0) c_ok = claim_tile(ring, it, p.tile_ctr, ntiles, limit, abort_flag, ti) ? 1 : 0;
         ti = __shfl_sync(0xffffffffu, ti, 0);
@@ -219,7 +238,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         }
       }
       if (ti >= ntiles) break;
-      const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
+      bool mc = false;
+      const GemmTile tl = kRouter ? router_tile(p, ti, BN)
+                          : kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
+                                  : decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool sh = !kRouter && tl.group >= p.n_routed;
       const CUtensorMap *ma = sh ? &tmAs : &tmA;
       const CUtensorMap *mb0 = sh ? &tmB0s : &tmB0;
@@ -245,15 +267,43 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           const bool a_tma = !kGather || sh;
           mbar_arrive_expect_tx(fb, a_tma ? C::STAGE_BYTES : C::B_BYTES);
           if (a_tma) tma_load_2d(a_dst, ma, fb, kx, tl.a_row, pol_a);
-          if (kDual) {
+          if (kPair && mc) {
+            // both CTAs multiply this weight tile: each loads one half into
+            // both (gate/up: the gate rows or the up rows; down: 128 of the
+            // 256 rows through the half-height map)
+            const uint32_t hb = b_dst + rank * (C::B_BYTES / 2);
+            if (kDual) tma_load_2d_mc(hb, rank ? mb1 : mb0, fb, kx, brow, kBoth, pol_w);
+            else tma_load_2d_mc(hb, mb1, fb, kx, brow + rank * (BN / 2), kBoth, pol_w);
+          } else if (kDual) {
             tma_load_2d(b_dst, mb0, fb, kx, brow, pol_w);
             tma_load_2d(b_dst + C::B_BYTES / 2, mb1, fb, kx, brow, pol_w);
+          } else if (kPair) {
+            tma_load_2d(b_dst, mb1, fb, kx, brow, pol_w);
+            tma_load_2d(b_dst + C::B_BYTES / 2, mb1, fb, kx, brow + BN / 2, pol_w);
           } else {
             tma_load_2d(b_dst, mb0, fb, kx, brow, kRouter ? pol_a : pol_w);
           }
         }
         pend_mask |= 1u << stage;
         pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (kPair && ok) {
+      // the partner's MMA arrives on this CTA's stages: wait for its last
+      // arrival on each, so none lands after the CTA has ended
+      for (int j = 0; j < C::STAGES; ++j) {
+        const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_DRAIN);
+          }
+          break;
+        }
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
@@ -277,8 +327,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int it = 0; ok; ++it) {
-        int ti = blockIdx.x + it * gridDim.x;
-        if (!kRouter && !read_tile(ring, it, limit, abort_flag, ti)) {
+        int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
+        if (!kRouter && !kPair && !read_tile(ring, it, limit, abort_flag, ti)) {
           *abort_flag = 1;
           report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
           ok = false;
@@ -311,7 +361,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           for (int kk = 0; kk < 4; ++kk)
             MmaKind<T>::mma(d_tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk), idesc,
                             (kb | kk) != 0 ? 1u : 0u);
-          tc_commit(empty0 + 8 * stage);
+          // pair mode: the stage is released in both CTAs (the partner's
+          // producer fills half of this CTA's weight tile)
+          if (kPair) tc_commit_mc(empty0 + 8 * stage, kBoth);
+          else tc_commit(empty0 + 8 * stage);
           issued = true;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -353,9 +406,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
-      int ti = 0, r_ok = 1;
-      if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
-      ti = __shfl_sync(0xffffffffu, ti, 0);
+      int ti = cl + it * ncl, r_ok = 1;
+      if (!kPair) {
+        if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
+        ti = __shfl_sync(0xffffffffu, ti, 0);
+      }
       if (!__shfl_sync(0xffffffffu, r_ok, 0)) {
         if (lane == 0) {
           *abort_flag = 1;
@@ -365,7 +420,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         break;
       }
       if (ti >= ntiles) break;
-      const GemmTile tl = decode_tile(gt, p, ti, kOutCols, !kDual);
+      bool mc = false;
+      const GemmTile tl = kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
+                                : decode_tile(gt, p, ti, kOutCols, !kDual);
       const bool routed = tl.group < p.n_routed;
       const T *src[kRowsPer];
       int tok[kRowsPer];
@@ -408,8 +465,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = 0;; ++it) {
-      int ti = blockIdx.x + it * gridDim.x;
-      if (!kRouter) {
+      int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
+      if (!kRouter && !kPair) {
         int r_ok = 1;
         if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
         ti = __shfl_sync(0xffffffffu, ti, 0);
@@ -422,7 +479,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         }
       }
       if (ti >= ntiles) break;
-      const GemmTile tl = kRouter ? router_tile(p, ti, BN) : decode_tile(gt, p, ti, kOutCols, !kDual);
+      bool mc = false;
+      const GemmTile tl = kRouter ? router_tile(p, ti, BN)
+                          : kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
+                                  : decode_tile(gt, p, ti, kOutCols, !kDual);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, limit, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
@@ -570,6 +630,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (kPair) {
+    // neither CTA ends while its partner may still write into it; after an
+    // abort, copies the partner issued before it stopped get time to land
+    cluster_sync_all();
+    if (*abort_flag)
+      for (int i = 0; i < 200; ++i) __nanosleep(1000);
+  }
 
   if (kRouter && (p.offsets_out || p.counts_out)) {
     // the last CTA to finish turns the histogram into group offsets
@@ -613,28 +680,66 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   }
 }
 
-template <typename T, int EPI, int BN>
+template <typename T, int EPI, int BN, bool kPair>
 cudaError_t gemm_set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_kernel<T, EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kGemmSmem);
+  return cudaFuncSetAttribute(gemm_kernel<T, EPI, BN, kPair>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
 }
 
-template <typename T, int EPI, int BN>
+template <typename T, int EPI, int BN, bool kPair>
 cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
                         bool pdl) {
   if (grid <= 0) return cudaSuccess;
+  if (kPair && (grid & 1)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(gemm_threads<EPI>());
   cfg.dynamicSmemBytes = kGemmSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (kPair) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<T, EPI, BN>, maps.m[0], maps.m[1], maps.m[2],
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<T, EPI, BN, kPair>, maps.m[0], maps.m[1], maps.m[2],
                             maps.m[3], maps.m[4], maps.m[5], p);
+}
+
+int gemm_pair_clusters() {
+  int best = 0;
+  for (int e = 0; e < 2; ++e) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(e == 0 ? gemm_threads<EPI_SWIGLU>() : gemm_threads<EPI_STORE>());
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t err =
+        e == 0 ? cudaOccupancyMaxActiveClusters(&n, gemm_kernel<__nv_bfloat16, EPI_SWIGLU, kBN, true>,
+                                                &cfg)
+               : cudaOccupancyMaxActiveClusters(&n, gemm_kernel<__nv_bfloat16, EPI_STORE, kBN, true>,
+                                                &cfg);
+    if (err != cudaSuccess) return 0;
+    best = e == 0 ? n : (n < best ? n : best);
+  }
+  return best;
 }
 
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN>();
@@ -642,6 +747,14 @@ template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_STORE, kBN>();
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_SWIGLU, kBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_STORE, kBN>();
+template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN, true>();
+template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_STORE, kBN, true>();
+template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN, true>(const GemmMaps &,
+                                                                        const GemmParams &, int,
+                                                                        cudaStream_t, bool);
+template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE, kBN, true>(const GemmMaps &,
+                                                                       const GemmParams &, int,
+                                                                       cudaStream_t, bool);
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &,
                                                                   int, cudaStream_t, bool);
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &,

@@ -138,6 +138,98 @@ __device__ __forceinline__ void build_group_table(const GemmParams &p, int *s_of
   }
 }
 
+// Work items of the grouped GEMMs in cluster-pair mode (two CTAs of a
+// thread-block cluster run each item side by side, their stages in lockstep).
+// Group g with mt M tiles and nt N tiles has nt * floor(mt / 2) pair items --
+// M tiles 2q and 2q + 1 of one N tile, so both CTAs multiply the same weight
+// tile, each loading half of it for both -- then, when mt is odd, ceil(nt / 2)
+// items of its last M tile, N tiles 2q and 2q + 1 (each CTA its own weight
+// tile).  s_it[g] = first item of group g (g <= E + 1).  Warp 2 runs the
+// scan over the finished s_mt prefix.
+__device__ __forceinline__ void build_item_table(const GemmParams &p, const int *s_mt, int *s_it,
+                                                 int warp, int lane) {
+  if (warp != 2) return;
+  const int n = p.n_routed + 1;
+  const int per = (n + 31) / 32;
+  auto items = [&](int g) {
+    const int mt = s_mt[g + 1] - s_mt[g];
+    return p.nt * (mt >> 1) + (mt & 1) * ((p.nt + 1) >> 1);
+  };
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int i = lane * per + q;
+    if (i < n) sum += items(i);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - sum;
+  for (int q = 0; q < per; ++q) {
+    const int i = lane * per + q;
+    if (i < n) {
+      s_it[i] = run;
+      run += items(i);
+    }
+  }
+  if (lane == 31) s_it[n] = incl;
+}
+
+// The tile of cluster CTA `rank` (0 or 1) in pair-mode item i; mc is set when
+// both CTAs share the weight tile (a pair item).  In the last-M-tile items of
+// a group with an odd number of N tiles, rank 1 may have no N tile left: it
+// then runs the previous N tile with no rows, so every stage still fills and
+// empties in step with its partner but nothing is stored.
+__device__ __forceinline__ GemmTile decode_pair_item(const GroupTable &gt, const int *s_it,
+                                                     const GemmParams &p, int i, int rank,
+                                                     int n_cols, bool down, bool &mc) {
+  const int E = p.n_routed;
+  int lo = 0, hi = E;  // largest g with s_it[g] <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_it[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int mtg = gt.mt[g + 1] - gt.mt[g];
+  const int pairs = mtg >> 1;
+  int local = i - s_it[g];
+  int m, n;
+  bool idle = false;
+  if (local < p.nt * pairs) {
+    n = local / pairs;
+    m = 2 * (local - n * pairs) + rank;
+    mc = true;
+  } else {
+    local -= p.nt * pairs;
+    n = 2 * local + rank;
+    m = mtg - 1;
+    mc = false;
+    if (n >= p.nt) {
+      n = p.nt - 1;
+      idle = true;
+    }
+  }
+  GemmTile t;
+  t.group = g;
+  t.n0 = n * n_cols;
+  t.pad[0] = t.pad[1] = t.pad[2] = 0;
+  if (g < E) {
+    const int cnt = gt.off[g + 1] - gt.off[g];
+    t.a_row = gt.off[g] + m * kBM;
+    t.out_row = t.a_row;
+    t.rows = min(kBM, cnt - m * kBM);
+  } else {
+    t.rows = min(kBM, p.T - m * kBM);
+    t.out_row = p.A + m * kBM;
+    t.a_row = down ? t.out_row : m * kBM;
+  }
+  if (idle) t.rows = 0;
+  return t;
+}
+
 // Tile sequence of a CTA of the grouped GEMMs: lane 0 of the producer warp
 // claims tiles (its first is blockIdx.x, every later one comes from a global
 // counter, so CTAs that drew cheap tiles take more of them) and publishes each

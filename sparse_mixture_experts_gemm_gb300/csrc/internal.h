@@ -12,7 +12,7 @@ struct GemmTile {
   int group;    // expert id, E for the shared expert
   int a_row;    // first row of the A operand (first slot, row of x, or row of H)
   int out_row;  // first output row (row of H or Yp)
-  int rows;     // valid rows, 1..128
+  int rows;     // valid rows, 0..128 (0: a cluster-pair CTA that stores nothing)
   int n0;       // first output column; also the row offset inside the group's B
   int pad[3];
 };
@@ -26,7 +26,7 @@ constexpr int kRouterBN = 64; // experts per router tile (E split into E / 64 bl
 constexpr int kStageBudget = 4 * (kBM * 128 + kBN * 128);  // smem for the operand stages
 constexpr int kThreads = 192; // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
 constexpr int kGatherThreads = 128;  // gate/up GEMM: warps 6-9 gather routed token rows
-constexpr int kGemmCtrl = 4096;  // barriers, TMEM slot, row tokens, group table
+constexpr int kGemmCtrl = 5120;  // barriers, TMEM slot, tile ring, group and item tables
 constexpr int kGemmSmem = kStageBudget + 1024 + kGemmCtrl;
 constexpr int kCountStride = 32;  // router histogram: one counter per 128-byte line
 constexpr int kMaxTopK = 8;
@@ -79,12 +79,17 @@ struct GemmMaps {
 };
 
 // gemm.cu
-template <typename T, int EPI, int BN>
-// pdl: launched as a programmatic dependent of the previous kernel on st
+// pdl: launched as a programmatic dependent of the previous kernel on st.
+// kPair (grouped GEMMs): thread-block clusters of two CTAs that run the
+// pair-mode work items (gemm_common.cuh) in lockstep; grid even.  For
+// EPI_STORE the B1 maps then hold 128-row boxes of the down weights.
+template <typename T, int EPI, int BN, bool kPair = false>
 cudaError_t launch_gemm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
                         bool pdl = false);
-template <typename T, int EPI, int BN>
+template <typename T, int EPI, int BN, bool kPair = false>
 cudaError_t gemm_set_smem_attr();
+// Clusters of two pair-mode CTAs that can be resident at once (0 on error).
+int gemm_pair_clusters();
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
 // route_small.cu: routing of batches of at most kSmallRouteT bf16 tokens
@@ -96,6 +101,9 @@ constexpr int kSmallRoutePass = 16;
 constexpr int kSmallRouteTokBytes = 65536;
 // gemv_small.cu: the grouped GEMVs take batches of at most kSmallGemvT tokens
 constexpr int kSmallGemvT = 32;
+// chunks of at least this many tokens run the bf16 grouped GEMMs on clusters
+// of two CTAs (moe_set_option(MOE_OPT_PAIR_MIN_TOKENS) changes it)
+constexpr long long kPairMinTokens = 8192;
 // counts_out (may be null): each expert's group size is added to it.
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,

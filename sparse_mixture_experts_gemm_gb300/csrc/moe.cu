@@ -120,6 +120,12 @@ struct moe_handle {
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
   CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
+  // cluster-pair grouped GEMMs (bf16): the down weights in 128-row boxes,
+  // the grid (two CTAs per cluster, 0: not available) and the smallest
+  // chunk that takes them
+  CUtensorMap tm_wd2, tm_sd2;
+  int pair_grid = 0;
+  long long pair_min_tokens = kPairMinTokens;
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
   bool q4_prefill = false;  // the grouped GEMMs support the layer's shape
@@ -367,6 +373,9 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
                               c.n_shared, h->status, st, pdl));
     return MOE_OK;
   }
+  // large chunks: the grouped GEMMs on clusters of two CTAs that share each
+  // weight tile of a group's consecutive M tiles
+  const bool pair = sizeof(T) == 2 && !h->q4 && h->pair_grid > 0 && Tc >= h->pair_min_tokens;
   GemmParams base = {};
   base.offsets = h->offsets;
   base.T = Tc;
@@ -401,6 +410,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
       Q4GemmMaps mq = h->q4g;
       mq.a = m.m[1];
       MOE_TRY(launch_gemm_q4<EPI_SWIGLU>(mq, p, h->num_sms, st, pdl));
+    } else if (pair) {
+      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN, true>(m, p, h->pair_grid, st, pdl)));
     } else {
       MOE_TRY((launch_gemm<T, EPI_SWIGLU, kBN>(m, p, h->num_sms, st, pdl)));
     }
@@ -421,6 +432,10 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.tile_ctr = h->tile_ctr(1);
     if (h->q4) {
       MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st, pdl));
+    } else if (pair) {
+      m.m[3] = h->tm_wd2;
+      m.m[5] = c.n_shared ? h->tm_sd2 : h->tm_wd2;
+      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_STORE, kBN, true>(m, p, h->pair_grid, st, pdl)));
     } else {
       MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st, pdl)));
     }
@@ -624,10 +639,12 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
                        static_cast<uint32_t>(512 / esz), 32, false) &&
          make_map(&h->tm_wg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
          make_map(&h->tm_wu, c.w_up, esz, static_cast<uint64_t>(E) * F, d, kBM) &&
-         make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN);
+         make_map(&h->tm_wd, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN) &&
+         make_map(&h->tm_wd2, c.w_down, esz, static_cast<uint64_t>(E) * d, F, kBN / 2);
   if (ok && !q4 && c.n_shared)
     ok = make_map(&h->tm_sg, c.s_gate, esz, F, d, kBM) &&
-         make_map(&h->tm_su, c.s_up, esz, F, d, kBM) && make_map(&h->tm_sd, c.s_down, esz, d, F, kBN);
+         make_map(&h->tm_su, c.s_up, esz, F, d, kBM) && make_map(&h->tm_sd, c.s_down, esz, d, F, kBN) &&
+         make_map(&h->tm_sd2, c.s_down, esz, d, F, kBN / 2);
   if (q4) {
     h->q4 = true;
     h->qw.g = q4mat(q4->gate);
@@ -677,6 +694,15 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
        route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
        small_gemv_q4_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
+  if (rc == MOE_OK && c.dtype == MOE_BF16 && !q4) {
+    // cluster-pair grouped GEMMs: as many clusters of two as fit at once
+    if (gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN, true>() != cudaSuccess ||
+        gemm_set_smem_attr<__nv_bfloat16, EPI_STORE, kBN, true>() != cudaSuccess)
+      rc = MOE_ERR_CUDA;
+    const int ncl = rc == MOE_OK ? gemm_pair_clusters() : 0;
+    cudaGetLastError();
+    h->pair_grid = 2 * std::min(ncl, h->num_sms / 2);
+  }
   if (rc != MOE_OK) {
     moe_destroy(h);
     return rc;
@@ -929,6 +955,14 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
     return MOE_ERR_CUDA;
   if (detail) *detail = s[1];
   return s[0];
+}
+
+int moe_set_option(moe_handle *h, int option, long long value) {
+  if (!h || value < 0) return MOE_ERR_INVALID_ARG;
+  switch (option) {
+    case MOE_OPT_PAIR_MIN_TOKENS: h->pair_min_tokens = value; return MOE_OK;
+    default: return MOE_ERR_INVALID_ARG;
+  }
 }
 
 int moe_profile(moe_handle *h, int enable) {

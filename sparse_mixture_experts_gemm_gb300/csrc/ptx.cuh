@@ -122,6 +122,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// The same box written to the same shared-memory offset of every CTA of the
+// thread-block cluster in `mask`, each copy completing the barrier at offset
+// `bar` of its own CTA (one read of the box from L2 for all of them).  The
+// source is this GPU's own memory.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                               int x, int y, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask), "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 // rank of this CTA in its thread-block cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -163,6 +176,15 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// The same arrival on the barrier at offset `bar` of every cluster CTA in
+// `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 

@@ -176,3 +176,10 @@ def test_gdn_scan_rejects_before_any_launch(lib, args, code):
                       a["o"], a["T"], a["Hk"], a["Hv"], a["dk"], a["dv"], None)
     assert rc == code
 
+
+
+def test_set_option_rejects_null_handle_and_bad_values(lib):
+    """moe_set_option validates on the host: a null handle is refused before
+    any CUDA call."""
+    assert lib.moe_set_option(None, moe.MOE_OPT_PAIR_MIN_TOKENS, 0) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_option(None, 99, 0) == moe.MOE_ERR_INVALID_ARG

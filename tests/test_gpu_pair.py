@@ -1,0 +1,100 @@
+"""Grouped GEMMs on clusters of two CTAs (MOE_OPT_PAIR_MIN_TOKENS), through the
+C ABI.
+
+In that mode two CTAs of a thread-block cluster multiply consecutive 128-row
+tiles of one expert group with the same weight tile, each loading half of it
+into both; a group's last tile (odd tile counts) runs beside the next N tile
+of the same rows, and with an odd number of N tiles one CTA of the last item
+runs without rows.  Every tile is the same MMA sequence as in the one-CTA
+mode, so the outputs must be equal bit for bit; each case is also checked
+against the oracle on every row (1e-2 row-normwise).
+"""
+import pytest
+import torch
+
+import helpers as H
+import sparse_mixture_experts_gemm_gb300 as moe
+from sparse_mixture_experts_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+OFF = 1 << 40  # no chunk is that large
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+    moe.lib()
+    return torch.device("cuda:0")
+
+
+def both_modes(layer, x):
+    layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, OFF)
+    one = layer.forward(x)
+    layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, 0)
+    pair = layer.forward(x)
+    torch.cuda.synchronize()
+    rc, detail = layer.status()
+    assert rc == 0, f"device status {rc} detail {detail}"
+    return one, pair
+
+
+# (seed, T, d, F, E, k, n_shared, max_tokens, skew)
+CASES = [
+    (50, 700, 768, 384, 16, 4, 1, 700, False),   # 3 N tiles in both GEMMs: idle CTAs
+    (51, 1000, 512, 256, 8, 2, 0, 1000, False),  # no shared expert, several M tiles per group
+    (52, 129, 512, 256, 16, 4, 1, 129, False),   # single-tile groups only
+    (53, 300, 512, 128, 64, 8, 1, 300, True),    # 8 groups of 300 rows (3 M tiles each)
+    (54, 3000, 512, 256, 32, 4, 1, 1024, False),  # chunks of 1024, 1024, 952
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"T{c[1]}_d{c[2]}_F{c[3]}_E{c[4]}")
+def test_pair_mode_equals_one_cta_mode_and_oracle(dev, case):
+    seed, T, d, F, E, k, n_shared, max_tokens, skew = case
+    bias = None
+    if skew:
+        bias = torch.zeros(E)
+        bias[:k] = 20.0
+    w = synth.layer_weights(seed, d, F, E, n_shared, "bf16", "cpu")
+    x = H.margined_tokens(seed + 1000, T, w["Wr"], k, "bf16", bias=bias, device="cpu")
+    wd = {kk: (None if v is None else v.to(dev)) for kk, v in w.items()}
+    layer = moe.MoELayer(wd, k, max_tokens=max_tokens, bias=None if bias is None else bias.to(dev))
+    try:
+        one, pair = both_modes(layer, x.to(dev))
+    finally:
+        layer.close()
+    assert torch.equal(one, pair)
+    ref, *_ = H.oracle_forward(x, w, k, bias=bias)
+    err = H.row_rel_err(pair, ref)
+    assert err.max() <= H.OUT_TOL, f"max row rel err {err.max():.3e} at row {err.argmax()}"
+
+
+def test_pair_mode_full_size_4k_bit_equal(dev):
+    """T=4096, d=2048, 256 experts top-8 + shared, F=512 (the one-CTA result is
+    checked against the oracle on every row in test_gpu_parity)."""
+    d, F, E, k, T = 2048, 512, 256, 8, 4096
+    w = synth.layer_weights(2, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(1002, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=T)
+    try:
+        one, pair = both_modes(layer, x)
+    finally:
+        layer.close()
+    assert torch.equal(one, pair)
+
+
+def test_pair_mode_full_size_16k_skewed_bit_equal(dev):
+    """T=16384 with the Zipf(1.2) router bias: giant groups of many M tiles."""
+    d, F, E, k, T = 2048, 512, 256, 8, 16384
+    bias = synth.zipf_bias(3, E, 1.2)
+    w = synth.layer_weights(3, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(1003, T, w["Wr"], k, "bf16", bias=bias, device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=T, bias=bias.to(dev))
+    try:
+        one, pair = both_modes(layer, x)
+    finally:
+        layer.close()
+    assert torch.equal(one, pair)
