@@ -104,8 +104,50 @@ __device__ __forceinline__ GemmTile decode_tile(const GroupTable &gt, const Gemm
 __device__ __forceinline__ void build_group_table(const GemmParams &p, int *s_off, int *s_mt,
                                                   int warp, int lane) {
   const int E = p.n_routed;
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) s_off[g] = p.offsets[g];
-  __syncthreads();
+  if (p.counts_in) {
+    // the cluster router left only the histogram: scan it here
+    for (int g = threadIdx.x; g < E; g += blockDim.x)
+      s_off[g] = p.counts_in[static_cast<long long>(g) * kCountStride];
+    __syncthreads();
+    if (warp == 2) {
+      const int per = (E + 31) / 32;
+      int sum = 0;
+      for (int q = 0; q < per; ++q) {
+        const int i = lane * per + q;
+        if (i < E) sum += s_off[i];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - sum;
+      for (int q = 0; q < per; ++q) {
+        const int i = lane * per + q;
+        if (i < E) {
+          const int c = s_off[i];
+          if (blockIdx.x == 0 && p.counts_out) p.counts_out[i] += c;  // summed over a call's chunks
+          s_off[i] = run;
+          run += c;
+        }
+      }
+      if (lane == 31) s_off[E] = incl;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && p.offsets_out)
+      for (int g = threadIdx.x; g <= E; g += blockDim.x) p.offsets_out[g] = s_off[g];
+  } else {
+    for (int g = threadIdx.x; g <= E; g += blockDim.x) s_off[g] = p.offsets[g];
+    __syncthreads();
+  }
+  if (blockIdx.x == 0) {
+    // the gate/up GEMM that read them has finished (this kernel waited for it)
+    if (p.clear_counts)
+      for (int g = threadIdx.x; g < E; g += blockDim.x)
+        p.clear_counts[static_cast<long long>(g) * kCountStride] = 0;
+    if (p.clear_ctr && threadIdx.x == 0) *p.clear_ctr = 0;
+  }
   for (int g = threadIdx.x; g <= E; g += blockDim.x) {
     const int rows = g < E ? s_off[g + 1] - s_off[g] : (p.n_shared ? p.T : 0);
     s_mt[g] = (rows + kBM - 1) / kBM;

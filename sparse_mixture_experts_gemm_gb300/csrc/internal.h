@@ -71,6 +71,14 @@ struct GemmParams {
   unsigned *done;          // CTA completion ticket, zero at the launch; the last CTA clears it
   int32_t *clear;          // router: n_clear words (128 bytes apart) the last CTA zeroes
   int n_clear;
+  // grouped GEMMs after the cluster router: the group offsets come from its
+  // line-padded histogram counts_in (CTA 0 also writes them to offsets_out
+  // and adds the counts into counts_out, when given); the down GEMM's CTA 0
+  // zeroes clear_counts (that histogram) and *clear_ctr (the gate/up GEMM's
+  // tile counter) for the next call, both read only by the finished gate/up
+  const int32_t *counts_in;
+  int32_t *clear_counts;
+  int *clear_ctr;
 };
 
 // Tensor maps: A routed, A shared, B0 routed, B1 routed, B0 shared, B1 shared.
@@ -90,6 +98,28 @@ template <typename T, int EPI, int BN, bool kPair = false>
 cudaError_t gemm_set_smem_attr();
 // Clusters of two pair-mode CTAs that can be resident at once (0 on error).
 int gemm_pair_clusters();
+
+// router.cu: the router of chunks of more than kSmallRouteT bf16 tokens.
+// One cluster of four CTAs per 128 tokens (each a quarter of d, all experts).
+// Writes idx [T][k], w [T][k]; then either adds each expert's count into
+// counts_direct [E] (routing only) or claims ranks on the line-padded
+// histogram counts [E * kCountStride] (zero before the launch), writing each
+// assignment's rank into rank [T][k] and the token into list[e][rank].
+struct RouterArgs {
+  int T, d, E, k;
+  const float *bias;       // [E] or null
+  int32_t *idx;
+  float *w;
+  int32_t *counts;         // line-padded histogram (ranks)
+  int32_t *counts_direct;  // [E] per-expert counts (no ranks, no lists)
+  int32_t *rank;
+  int32_t *list;
+  long long list_stride;
+  int *status;
+};
+cudaError_t router_set_attr();
+cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const RouterArgs &a,
+                          cudaStream_t st);
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
 // route_small.cu: routing of batches of at most kSmallRouteT bf16 tokens
@@ -176,7 +206,8 @@ template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
                            bool pdl = false, const int32_t *idx = nullptr,
-                           const int32_t *offsets = nullptr, int E = 0);
+                           const int32_t *offsets = nullptr, int E = 0,
+                           int *clear_ctr = nullptr);
 
 // 4-bit group-affine matrix (codes two per byte, even column in the low
 // nibble; one bf16 scale and bias per 64 columns of a row)

@@ -124,6 +124,7 @@ struct moe_handle {
   // the grid (two CTAs per cluster, 0: not available) and the smallest
   // chunk that takes them
   CUtensorMap tm_wd2, tm_sd2;
+  CUtensorMap tm_wr256;  // router rows in boxes of 256 rows (the cluster router)
   int pair_grid = 0;
   long long pair_min_tokens = kPairMinTokens;
   // 4-bit expert weights (moe_create_q4)
@@ -224,48 +225,30 @@ struct ProfScope {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-// The bf16 router: tcgen05 logits with top-k, weights, ranks, the
-// per-expert token lists (when list is given) and the histogram in the
-// epilogue; the last CTA writes the offsets.
-int launch_router_tc(moe_handle *h, const void *x, int T, int32_t *idx, float *w, int32_t *rank,
-                     int32_t *list, int32_t *offsets, int32_t *counts_out, cudaStream_t st) {
+// The bf16 router of chunks above the small-batch size: one cluster of four
+// CTAs per 128 tokens (router.cu).  With counts_direct it writes the
+// per-expert counts for the caller; otherwise it claims ranks on the
+// handle's histogram and fills the per-expert token lists.
+int launch_router_bf16(moe_handle *h, const void *x, int T, int32_t *idx, float *w,
+                       int32_t *counts_direct, cudaStream_t st) {
   const moe_config &c = h->cfg;
   CUtensorMap tm_x;
   if (!make_map(&tm_x, x, 2, T, c.d_model, kBM)) return MOE_ERR_CUDA;
-  const int nblk = (T + kBM - 1) / kBM;
-  const int nq = (c.n_experts + kRouterBN - 1) / kRouterBN;
-  GemmMaps m;
-  m.m[0] = m.m[1] = tm_x;
-  m.m[2] = m.m[3] = m.m[4] = m.m[5] = h->tm_wr;
-  GemmParams p = {};
-  p.T = T;
-  p.ntiles_host = nblk * nq;
-  p.nq = nq;
-  p.cand_v = h->cand_v;
-  p.cand_i = h->cand_i;
-  p.tok_cnt = h->tok_cnt;
-  p.num_k_blocks = c.d_model / 64;
-  p.n_routed = c.n_experts;
-  p.status = h->status;
-  p.kid = KID_ROUTER;
-  p.k = c.top_k;
-  p.E = c.n_experts;
-  p.bias = c.router_bias;
-  p.idx = idx;
-  p.w = w;
-  p.counts = h->counts();
-  p.counts_out = counts_out;
-  p.rank = rank;
-  p.list = list;
-  p.list_stride = c.max_tokens;
-  p.offsets_out = offsets;
-  p.done = h->done();
-  p.clear = h->tile_ctr(0);
-  p.n_clear = 2;
-  const int tiles = nblk * nq;
-  MOE_TRY((launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(m, p,
-                                                             tiles < h->num_sms ? tiles : h->num_sms,
-                                                             st)));
+  RouterArgs a = {};
+  a.T = T;
+  a.d = c.d_model;
+  a.E = c.n_experts;
+  a.k = c.top_k;
+  a.bias = c.router_bias;
+  a.idx = idx;
+  a.w = w;
+  a.counts = h->counts();
+  a.counts_direct = counts_direct;
+  a.rank = h->inv;
+  a.list = h->list;
+  a.list_stride = c.max_tokens;
+  a.status = h->status;
+  MOE_TRY(launch_router(tm_x, h->tm_wr256, a, st));
   return MOE_OK;
 }
 
@@ -297,8 +280,10 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   int32_t *idx = ro.idx ? ro.idx : h->idx;
   float *wts = ro.w ? ro.w : h->w;
 
-  // route_ctl is zero here: create cleared it and every router launch clears
-  // what it used (counts, ticket, the GEMMs' tile counters) when it is done
+  // route_ctl is zero here: create cleared it; the small-batch and fp32
+  // routers clear the GEMMs' tile counters when they are done, and after the
+  // bf16 cluster router the down GEMM clears its histogram and the gate/up
+  // tile counter, the combine the down tile counter
   const bool small = sizeof(T) == 2 && small_route_ok(Tc, d);
   if (small) {
     // a few tokens: routing and placement in one cluster launch
@@ -308,10 +293,10 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   } else {
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
     if (sizeof(T) == 2) {
-      // tokens into per-expert lists, ranks into inv: no placement step (the
-      // combine adds each assignment's group offset to its rank)
-      const int rc =
-          launch_router_tc(h, x, Tc, idx, wts, h->inv, h->list, h->offsets, ro.counts, st);
+      // tokens into per-expert lists, ranks into inv, the histogram: no
+      // placement step (the gate/up GEMM scans the histogram into the group
+      // offsets, the combine adds each assignment's group offset to its rank)
+      const int rc = launch_router_bf16(h, x, Tc, idx, wts, nullptr, st);
       if (rc != MOE_OK) return rc;
     } else {
       MOE_TRY(launch_router_simt<T>(x, static_cast<const T *>(c.w_router), c.router_bias, Tc, d, E,
@@ -406,6 +391,14 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.list = lists ? h->list : nullptr;
     p.list_stride = c.max_tokens;
     p.x = x;
+    if (lists) {
+      // the cluster router left the histogram: this GEMM scans it into the
+      // group offsets (for itself, the down GEMM and the combine) and adds it
+      // to the caller's counts
+      p.counts_in = h->counts();
+      p.offsets_out = h->offsets;
+      p.counts_out = ro.counts;
+    }
     if (h->q4) {  // 4-bit weights (bf16 tokens): dequantised in the GEMM
       Q4GemmMaps mq = h->q4g;
       mq.a = m.m[1];
@@ -430,6 +423,9 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.ldo = d;
     p.kid = KID_GEMM_DOWN;
     p.tile_ctr = h->tile_ctr(1);
+    // the finished gate/up GEMM read these: clear them for the next call
+    p.clear_counts = lists ? h->counts() : nullptr;
+    p.clear_ctr = h->tile_ctr(0);
     if (h->q4) {
       MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st, pdl));
     } else if (pair) {
@@ -444,7 +440,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
                               c.n_shared, h->status, st, pdl, lists ? idx : nullptr,
-                              lists ? h->offsets : nullptr, E));
+                              lists ? h->offsets : nullptr, E, h->tile_ctr(1)));
   }
   return MOE_OK;
 }
@@ -631,7 +627,8 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
 
   // tensor maps of the weights and the fixed workspace buffers
   bool ok = make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
-            make_map(&h->tm_wr, c.w_router, esz, E, d, kRouterBN);
+            make_map(&h->tm_wr, c.w_router, esz, E, d, kRouterBN) &&
+            make_map(&h->tm_wr256, c.w_router, esz, E, d, 256);
   if (ok && !q4)
     ok = encode_map_2d(&h->tm_dg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d,
                        static_cast<uint32_t>(512 / esz), 32, false) &&
@@ -691,7 +688,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
       (gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess ||
-       route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
+       router_set_attr() != cudaSuccess || route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
        small_gemv_q4_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
   if (rc == MOE_OK && c.dtype == MOE_BF16 && !q4) {
@@ -772,9 +769,14 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   const int d = c.d_model, E = c.n_experts, k = c.top_k;
   ProfScope ps(h, MOE_KERNEL_ROUTER, st);
   if (c.dtype == MOE_BF16) {
-    // the router's last CTA adds the histogram to counts
+    // the router adds each expert's assignments to counts
     MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
-    return launch_router_tc(h, x, T, topk_idx, topk_w, nullptr, nullptr, nullptr, counts, st);
+    if (small_route_ok(T, d))
+      return launch_route_small(x, c.w_router, c.router_bias, T, d, E, k, topk_idx, topk_w, h->inv,
+                                h->perm, h->offsets, counts, h->tile_ctr(0), 2, st) == cudaSuccess
+                 ? MOE_OK
+                 : MOE_ERR_CUDA;
+    return launch_router_bf16(h, x, T, topk_idx, topk_w, counts, st);
   }
   MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
   MOE_TRY(launch_router_simt<float>(static_cast<const float *>(x),

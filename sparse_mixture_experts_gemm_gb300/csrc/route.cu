@@ -278,10 +278,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
                                                       const float *w, T *out, int T_tok, int k,
                                                       int d, int A_total, int n_shared,
                                                       int *status, const int32_t *idx,
-                                                      const int32_t *offsets, int E) {
+                                                      const int32_t *offsets, int E,
+                                                      int *clear_ctr) {
   // a programmatic dependent of the down GEMM (or GEMV): yp is read after
   // the wait
   pdl_wait();
+  // the down GEMM has finished: its tile counter is free for the next call
+  if (clear_ctr && blockIdx.x == 0 && threadIdx.x == 0) *clear_ctr = 0;
   constexpr int NV = Vec<T>::N;
   const int vpr = d / NV;  // vectors per row (a multiple of 32: a warp serves one token)
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -348,20 +351,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
                            int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
-                           bool pdl, const int32_t *idx, const int32_t *offsets, int E) {
+                           bool pdl, const int32_t *idx, const int32_t *offsets, int E,
+                           int *clear_ctr) {
   const long long threads = static_cast<long long>(T_tok) * (d / Vec<T>::N);
   const int grid = static_cast<int>((threads + 255) / 256);
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_config(grid, 256, st, pdl, &attr);
   return cudaLaunchKernelEx(&cfg, combine_kernel<T>, yp, inv, w, out, T_tok, k, d, A_total,
-                            n_shared, status, idx, offsets, E);
+                            n_shared, status, idx, offsets, E, clear_ctr);
 }
 template cudaError_t launch_combine<float>(const float *, const int32_t *, const float *, float *, int,
                                            int, int, int, int, int *, cudaStream_t, bool,
-                                           const int32_t *, const int32_t *, int);
+                                           const int32_t *, const int32_t *, int, int *);
 template cudaError_t launch_combine<__nv_bfloat16>(const __nv_bfloat16 *, const int32_t *,
                                                    const float *, __nv_bfloat16 *, int, int, int, int,
                                                    int, int *, cudaStream_t, bool, const int32_t *,
-                                                   const int32_t *, int);
+                                                   const int32_t *, int, int *);
 
 }  // namespace moe

@@ -1,0 +1,369 @@
+// router.cu -- the router of the grouped path for bf16 tokens: logits, top-k,
+// routing weights, ranks, per-expert token lists and histogram in one launch
+// ("Optimizing on-device inference for Apple Silicon", sections "Qwen
+// creates three distinct workload shapes": 256 experts, eight kept per
+// token, and "Keep expert routing on the GPU": selection and the per-expert
+// histogram stay on the device).
+//
+// One thread-block cluster of four CTAs per tile of 128 tokens.  CTA r
+// multiplies the tokens' columns [r d/4, (r+1) d/4) with the same columns of
+// all router rows on the tensor cores (M = 128 tokens, N = 256 experts, fp32
+// accumulator in TMEM), so each CTA streams a quarter of the tile's tokens
+// and of the router weights.  The four partial logit blocks are then
+// exchanged through distributed shared memory: CTA r receives the partials
+// of tokens 32 r .. 32 r + 31 from all four CTAs into its (now idle) operand
+// ring, sums them in a fixed order (deterministic), adds the router bias and
+// takes each token's top-k with eight threads per token (32 experts each,
+// then three pairwise merges).  The thread that ends with a token's list
+// writes its experts and weights and claims each assignment's rank inside
+// its expert group with one atomic per expert among the lanes of a warp.
+//
+// Warp 0 issues the TMA loads, warp 1 the MMAs, warps 2-9 drain TMEM into the
+// owners' partial buffers and then select.  Every wait is bounded; a CTA that
+// gave up tells the other CTAs of its cluster before the exchange, and then
+// none of them exchanges or writes, but all still meet at both cluster
+// barriers.
+#include <cuda_bf16.h>
+
+#include "../../include/moe.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRSplit = 4;                    // CTAs per cluster: quarters of d
+constexpr int kRN = 256;                      // experts per MMA (E <= 256)
+constexpr int kRStages = 4;
+constexpr int kRABytes = kBM * 128;           // 128 tokens x 64 columns
+constexpr int kRBBytes = kRN * 128;           // 256 router rows x 64 columns
+constexpr int kRStageBytes = kRABytes + kRBBytes;
+constexpr int kRRows = kBM / kRSplit;         // tokens finished per CTA
+constexpr int kRRowFloats = kRN + 4;          // 1040-byte rows of the partial buffer
+constexpr int kRRedBytes = kRSplit * kRRows * kRRowFloats * 4;
+static_assert(kRRedBytes <= kRStages * kRStageBytes, "the partials reuse the operand ring");
+constexpr int kRThreads = 320;
+constexpr int kREpiWarps = 8;
+constexpr int kRCtrl = 2048;
+constexpr int kRSmem = kRStages * kRStageBytes + 1024 + kRCtrl;
+
+// 16-byte chunk q (of 64) of a row of partials is kept at chunk q ^ (q / 8 %
+// 8): the eight threads that read one token's row take chunks 8 s + u with
+// s = 0..7, which this spreads over all 32 banks.
+__device__ __forceinline__ int red_chunk(int q) { return q ^ ((q >> 3) & 7); }
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t local, uint32_t rank, int v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
+// Keep the 8 largest (value, index) pairs, sorted by descending value; a
+// candidate equal to a kept value goes after it (callers insert in
+// increasing index order, so ties keep the lower index first).  The
+// candidate is carried down the list: at each place it swaps with a smaller
+// kept pair, so value and index always move together.
+__device__ __forceinline__ void top8_insert(float (&bv)[kMaxTopK], int (&bi)[kMaxTopK], float v,
+                                            int e) {
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const bool gt = v > bv[j];
+    const float kv = bv[j];
+    const int ki = bi[j];
+    bv[j] = gt ? v : kv;
+    bi[j] = gt ? e : ki;
+    v = gt ? kv : v;
+    e = gt ? ki : e;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    router_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  const RouterArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kRStages * kRABytes;
+  float *red = reinterpret_cast<float *>(smem);  // after the MMAs: [4 src][32 rows][260]
+  uint8_t *ctrl = smem + kRStages * kRStageBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 256);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 260);
+  volatile int *s_err = reinterpret_cast<volatile int *>(ctrl + 264);  // set by any cluster CTA
+  float *s_bias = reinterpret_cast<float *>(ctrl + 1024);               // [256]
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kRStages;
+  const uint32_t tfull = empty0 + 8 * kRStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int tile = static_cast<int>(blockIdx.x) / kRSplit;
+  const int nkb = a.d / (kRSplit * 64);  // K blocks of 64 columns per CTA
+  const int kx0 = static_cast<int>(rank) * (a.d / kRSplit);
+  const long long limit = MOE_WAIT_LIMIT_CYCLES;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    *s_err = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kRN);
+    tmem_relinquish();
+  }
+  if (threadIdx.x >= 64)
+    for (int e = threadIdx.x - 64; e < kRN; e += kRThreads - 64)
+      s_bias[e] = e < a.E ? (a.bias ? a.bias[e] : 0.0f) : -INFINITY;
+  // the tokens may be the previous kernel's output
+  pdl_wait();
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  // every CTA's error flag is initialised before any CTA may set it
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();  // tokens and router rows are read again
+      uint32_t pend = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kRStages;
+        if (kb >= kRStages && !mbar_wait(empty0 + 8 * s, ((kb / kRStages) - 1) & 1, limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * s;
+        const int kx = kx0 + kb * 64;
+        mbar_arrive_expect_tx(fb, kRStageBytes);
+        tma_load_2d(smem_u32(sA + s * kRABytes), &tmX, fb, kx, tile * kBM, pol);
+        tma_load_2d(smem_u32(sB + s * kRBBytes), &tmW, fb, kx, 0, pol);
+        pend = kb;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_ROUTER * 100 + SITE_PRODUCER_EMPTY);
+        // copies already issued must land before the ring is reused
+        for (int kb = pend > kRStages ? pend - kRStages + 1 : 0; kb <= static_cast<int>(pend); ++kb)
+          if (!mbar_wait(full0 + 8 * (kb % kRStages), (kb / kRStages) & 1, limit, nullptr))
+            report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_ROUTER * 100 + SITE_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_make(kBM, kRN, MmaKind<__nv_bfloat16>::ab_format);
+      bool issued = false;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kRStages;
+        if (!mbar_wait(full0 + 8 * s, (kb / kRStages) & 1, limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * kRABytes);
+        const uint32_t b0 = smem_u32(sB + s * kRBBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          MmaKind<__nv_bfloat16>::mma(tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk),
+                                      idesc, (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(empty0 + 8 * s);
+        issued = true;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_ROUTER * 100 + SITE_MMA_FULL);
+      }
+      // the epilogue waits for this arrival; after an abort it still comes
+      // once the MMAs issued so far are done
+      if (issued || ok) tc_commit(tfull);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const bool w_ok = mbar_wait(tfull, 0, limit, abort_flag);
+    if (!__all_sync(0xffffffffu, w_ok)) {
+      ok = false;
+      if (lane == 0) report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_ROUTER * 100 + SITE_EPI_TMEM_FULL);
+    }
+    tc_fence_after();
+  }
+  // a CTA that gave up tells every CTA of the cluster (its partials would be
+  // missing or its ring still filling); the barrier also orders each CTA's
+  // last MMA before any partial lands in its ring
+  if (!ok || *abort_flag)
+    for (uint32_t r = 0; r < kRSplit; ++r) st_cluster_s32(smem_u32(const_cast<int *>(s_err)), r, 1);
+  __syncwarp();
+  cluster_sync_all();
+  const bool go = *s_err == 0;
+
+  if (go && warp >= 2) {
+    // TMEM lanes 32 (warp % 4) .. + 31 (tokens) belong to owner CTA warp % 4;
+    // warps 2-5 send columns 0-127, warps 6-9 columns 128-255
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t rbase = smem_u32(red) + ((rank * kRRows + lane) * kRRowFloats) * 4;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int col0 = h * 128 + c * 32;
+      float v[32];
+      tmem_ld32_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int chunk = red_chunk((col0 >> 2) + u);
+        st_cluster_v4(rbase + chunk * 16, q,
+                      make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  // every partial has landed in its owner's buffer
+  cluster_sync_all();
+
+  if (go && warp >= 2) {
+    // ------------------------------------------------------------ select
+    // thread (j, s): token j of this CTA's 32, experts 32 s .. 32 s + 31
+    const int t_loc = (warp - 2) * 32 + lane;
+    const int j = t_loc >> 3, s = t_loc & 7;
+    float bv[kMaxTopK];
+    int bi[kMaxTopK];
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i) {
+      bv[i] = -INFINITY;
+      bi[i] = 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int off = (j * kRRowFloats + (8 * s + (u ^ s)) * 4);
+      float4 acc = *reinterpret_cast<const float4 *>(red + off);
+#pragma unroll
+      for (int src = 1; src < kRSplit; ++src) {
+        const float4 p = *reinterpret_cast<const float4 *>(red + src * kRRows * kRRowFloats + off);
+        acc.x += p.x;
+        acc.y += p.y;
+        acc.z += p.z;
+        acc.w += p.w;
+      }
+      const int e0 = 32 * s + 4 * u;
+      top8_insert(bv, bi, acc.x + s_bias[e0], e0);
+      top8_insert(bv, bi, acc.y + s_bias[e0 + 1], e0 + 1);
+      top8_insert(bv, bi, acc.z + s_bias[e0 + 2], e0 + 2);
+      top8_insert(bv, bi, acc.w + s_bias[e0 + 3], e0 + 3);
+    }
+    // merge the eight lists of a token: at each step the thread with the
+    // lower experts takes its partner's list (all of whose experts are
+    // higher, so equal values keep the lower expert first)
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+      float pv[kMaxTopK];
+      int pi[kMaxTopK];
+#pragma unroll
+      for (int i = 0; i < kMaxTopK; ++i) {
+        pv[i] = __shfl_xor_sync(0xffffffffu, bv[i], m);
+        pi[i] = __shfl_xor_sync(0xffffffffu, bi[i], m);
+      }
+      if ((s & m) == 0) {
+#pragma unroll
+        for (int i = 0; i < kMaxTopK; ++i) top8_insert(bv, bi, pv[i], pi[i]);
+      }
+    }
+    const int t = tile * kBM + static_cast<int>(rank) * kRRows + j;
+    if (s == 0 && t < a.T) {
+      float ex[kMaxTopK];
+      float sum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kMaxTopK; ++i) {
+        ex[i] = (i < a.k) ? expf(bv[i] - bv[0]) : 0.0f;
+        sum += ex[i];
+      }
+      const float inv_s = 1.0f / sum;
+      // lanes of this warp that chose the same expert share one atomic on
+      // its counter; all k atomics are issued before any result is used
+      const unsigned act = __activemask();
+      unsigned peers[kMaxTopK];
+      int base[kMaxTopK];
+#pragma unroll
+      for (int i = 0; i < kMaxTopK; ++i) {
+        base[i] = 0;
+        peers[i] = 0;
+        if (i < a.k) {
+          const long long o = static_cast<long long>(t) * a.k + i;
+          a.idx[o] = bi[i];
+          a.w[o] = ex[i] * inv_s;
+          peers[i] = __match_any_sync(act, bi[i]);
+          if (lane == __ffs(peers[i]) - 1) {
+            if (a.counts_direct) atomicAdd(a.counts_direct + bi[i], __popc(peers[i]));
+            else base[i] = atomicAdd(a.counts + static_cast<long long>(bi[i]) * kCountStride,
+                                     __popc(peers[i]));
+          }
+        }
+      }
+      if (!a.counts_direct) {
+#pragma unroll
+        for (int i = 0; i < kMaxTopK; ++i) {
+          if (i < a.k) {
+            const int rk = __shfl_sync(act, base[i], __ffs(peers[i]) - 1) +
+                           __popc(peers[i] & ((1u << lane) - 1u));
+            a.rank[static_cast<long long>(t) * a.k + i] = rk;
+            // the token goes to place rk of its expert's list
+            a.list[static_cast<long long>(bi[i]) * a.list_stride + rk] = t;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kRN);
+}
+
+cudaError_t router_set_attr() {
+  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+}
+
+cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const RouterArgs &a,
+                          cudaStream_t st) {
+  if (a.T <= 0) return cudaSuccess;
+  const int ntiles = (a.T + kBM - 1) / kBM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kRSplit * ntiles);
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = kRSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kRSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_kernel, tm_x, tm_w, a);
+}
+
+}  // namespace moe
