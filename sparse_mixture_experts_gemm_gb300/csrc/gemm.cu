@@ -1,29 +1,18 @@
 // gemm.cu -- persistent grouped GEMM on the 5th-generation tensor cores.
 //
-// One kernel template serves the three contractions of the block:
-//   EPI_ROUTER : logits = x . Wr^T for 128 tokens x 64 experts per tile, a
-//                top-8 per token and expert block in the epilogue; the last of
-//                a token's expert blocks merges the candidates, takes the
-//                softmax over the chosen logits and claims each assignment's
-//                rank inside its expert group with an atomic on the per-expert
-//                histogram, and puts the assignment at that rank of the
-//                expert's list (the rows the gate/up GEMM gathers, which also
-//                records each assignment's slot for the combine, so no
-//                separate placement step is needed); the last CTA scans the histogram
-//                into group offsets ("Optimizing on-device inference for
-//                Apple Silicon", sections "Qwen creates three distinct
-//                workload shapes" and "Keep expert routing on the GPU").
+// One kernel template serves the two grouped contractions of the block:
 //   EPI_SWIGLU : for each expert group, gate and up projections of its rows in
 //                one MMA (B tile = 128 gate rows over 128 up rows), epilogue
 //                h = silu(gate) * up written once (section "Reduce
 //                intermediate traffic and dispatch traffic": input
 //                projections fused with the gated activation).  Routed A rows
 //                are gathered from x by four extra warps (16-byte cp.async
-//                into the swizzled tile, row r from token perm[slot]); the
+//                into the swizzled tile, the token of each row from the
+//                router's per-expert list or the slot permutation); the
 //                shared expert's rows (x in order) come by TMA.
 //   EPI_STORE  : the down projection of each group's rows, stored per slot.
 // The tiles of both grouped GEMMs are derived on the device from the group
-// offsets the routing wrote (section "Keep expert routing on the GPU": the
+// sizes the routing left (section "Keep expert routing on the GPU": the
 // block map of fixed-size blocks the grouped GEMM processes), so no host
 // synchronisation is needed: every CTA scans ceil(rows / 128) over the groups
 // and maps a tile index to (group, m, n) by binary search.  Tiles of one group
@@ -32,12 +21,13 @@
 //
 // CTA layout: 192 threads (320 for the gate/up GEMM).  Warp 0 produces a
 // shared-memory ring of 128-byte-swizzled K-major tiles (lane 0 issues the TMA
-// tile loads; 4 stages at N = 256, 8 at N = 64); warp 1 allocates 2N TMEM
+// tile loads; 4 stages); warp 1 allocates 2N TMEM
 // columns (two 128 x N fp32 accumulators) and its lane 0 issues tcgen05.mma
 // (M = 128, 32 bytes of K per instruction); warps 2-5 drain a finished
 // accumulator with tcgen05.ld while the MMA fills the other; warps 6-9 of the
 // gate/up GEMM gather its routed A rows.
-// The grid is persistent: CTA c takes tiles c, c + gridDim.x, ...
+// The grid is persistent: CTA c takes tile c, then claims tiles from a
+// counter; in cluster-pair mode the clusters take work items in a fixed order.
 // Every wait is bounded; a wait that runs out records a timeout in the status
 // word, raises a CTA-wide abort flag, drains what it issued and returns.
 #include <cuda_bf16.h>
@@ -64,38 +54,6 @@ struct Tile {
 };
 
 
-// Keep the 8 largest (value, index) pairs, sorted descending; a candidate
-// equal to a kept value goes after it, so ties favour the lower index when
-// candidates arrive in increasing index order.  Branch-free: every slot
-// compares against the candidate independently and takes its own value, the
-// candidate, or its upper neighbour's value.
-__device__ __forceinline__ void topk_insert(float (&bv)[kMaxTopK], int (&bi)[kMaxTopK], float v,
-                                            int e) {
-  bool c[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) c[j] = v > bv[j];
-#pragma unroll
-  for (int j = kMaxTopK - 1; j > 0; --j) {
-    bv[j] = c[j] ? (c[j - 1] ? bv[j - 1] : v) : bv[j];
-    bi[j] = c[j] ? (c[j - 1] ? bi[j - 1] : e) : bi[j];
-  }
-  bv[0] = c[0] ? v : bv[0];
-  bi[0] = c[0] ? e : bi[0];
-}
-
-// Router tile i: token block i / nq, expert block i % nq (n0 = first expert).
-__device__ __forceinline__ GemmTile router_tile(const GemmParams &p, int i, int bn) {
-  const int blk = i / p.nq;
-  GemmTile t;
-  t.group = 0;
-  t.a_row = blk * kBM;
-  t.out_row = blk * kBM;
-  t.rows = min(kBM, p.T - blk * kBM);
-  t.n0 = (i - blk * p.nq) * bn;
-  t.pad[0] = t.pad[1] = t.pad[2] = 0;
-  return t;
-}
-
 }  // namespace
 
 // Threads of one CTA: the gate/up GEMM adds four warps that gather the routed
@@ -110,12 +68,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                 const __grid_constant__ CUtensorMap tmB0s,
                 const __grid_constant__ CUtensorMap tmB1s, const GemmParams p) {
   using C = Tile<T, BN>;
-  constexpr bool kRouter = (EPI == EPI_ROUTER);
   constexpr bool kDual = (EPI == EPI_SWIGLU);  // B = gate rows over up rows
   constexpr bool kGather = (EPI == EPI_SWIGLU);  // routed A rows gathered by warps 6-9
   constexpr int kOutCols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
   constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
-  static_assert(!(kPair && kRouter), "the router runs one CTA per tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -125,7 +81,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
-  int *s_last = reinterpret_cast<int *>(ctrl + 520);
   int *s_off = reinterpret_cast<int *>(ctrl + 1536);        // [E + 1]
   int *s_mt = reinterpret_cast<int *>(ctrl + 1536 + 1040);  // [E + 2]
   int *s_it = reinterpret_cast<int *>(ctrl + 1536 + 2080);  // [E + 2], pair mode
@@ -175,7 +130,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmB0);
     prefetch_tmap(&tmA);
-    if (!kRouter) prefetch_tmap(&tmAs);
+    prefetch_tmap(&tmAs);
     if (EPI == EPI_SWIGLU) {
       prefetch_tmap(&tmB1);
       prefetch_tmap(&tmB0s);
@@ -197,17 +152,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   // wait in turn).  Both are no-ops in an ordinary launch.
   pdl_wait();
   pdl_launch_dependents();
-  int ntiles;
-  if (kRouter) {
-    ntiles = p.ntiles_host;
-  } else {
-    build_group_table(p, s_off, s_mt, warp, lane);
-  }
+  build_group_table(p, s_off, s_mt, warp, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (!kRouter) ntiles = p.nt * s_mt[p.n_routed + 1];
+  int ntiles = p.nt * s_mt[p.n_routed + 1];
   if (kPair) {
     build_item_table(p, s_mt, s_it, warp, lane);
     __syncthreads();
@@ -224,7 +174,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     bool ok = true;
     for (int it = 0; ok; ++it) {
       int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
-      if (!kRouter && !kPair) {
+      if (!kPair) {
         int c_ok = 1;
         if (lane == 0) c_ok = claim_tile(ring, it, p.tile_ctr, ntiles, limit, abort_flag, ti) ? 1 : 0;
         ti = __shfl_sync(0xffffffffu, ti, 0);
@@ -239,14 +189,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       }
       if (ti >= ntiles) break;
       bool mc = false;
-      const GemmTile tl = kRouter ? router_tile(p, ti, BN)
-                          : kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
-                                  : decode_tile(gt, p, ti, kOutCols, !kDual);
-      const bool sh = !kRouter && tl.group >= p.n_routed;
+      const GemmTile tl = kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
+                                : decode_tile(gt, p, ti, kOutCols, !kDual);
+      const bool sh = tl.group >= p.n_routed;
       const CUtensorMap *ma = sh ? &tmAs : &tmA;
       const CUtensorMap *mb0 = sh ? &tmB0s : &tmB0;
       const CUtensorMap *mb1 = sh ? &tmB1s : &tmB1;
-      const int brow = kRouter ? tl.n0 : (sh ? tl.n0 : tl.group * p.b_rows_per_group + tl.n0);
+      const int brow = sh ? tl.n0 : tl.group * p.b_rows_per_group + tl.n0;
       for (int kb = 0; kb < p.num_k_blocks; ++kb) {
         bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -281,7 +230,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             tma_load_2d(b_dst, mb1, fb, kx, brow, pol_w);
             tma_load_2d(b_dst + C::B_BYTES / 2, mb1, fb, kx, brow + BN / 2, pol_w);
           } else {
-            tma_load_2d(b_dst, mb0, fb, kx, brow, kRouter ? pol_a : pol_w);
+            tma_load_2d(b_dst, mb0, fb, kx, brow, pol_w);
           }
         }
         pend_mask |= 1u << stage;
@@ -328,7 +277,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       bool ok = true, issued = false;
       for (int it = 0; ok; ++it) {
         int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
-        if (!kRouter && !kPair && !read_tile(ring, it, limit, abort_flag, ti)) {
+        if (!kPair && !read_tile(ring, it, limit, abort_flag, ti)) {
           *abort_flag = 1;
           report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
           ok = false;
@@ -466,7 +415,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     uint32_t acc_phase = 0;
     for (int it = 0;; ++it) {
       int ti = kPair ? cl + it * ncl : blockIdx.x + it * gridDim.x;
-      if (!kRouter && !kPair) {
+      if (!kPair) {
         int r_ok = 1;
         if (lane == 0) r_ok = read_tile(ring, it, limit, abort_flag, ti) ? 1 : 0;
         ti = __shfl_sync(0xffffffffu, ti, 0);
@@ -480,9 +429,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       }
       if (ti >= ntiles) break;
       bool mc = false;
-      const GemmTile tl = kRouter ? router_tile(p, ti, BN)
-                          : kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
-                                  : decode_tile(gt, p, ti, kOutCols, !kDual);
+      const GemmTile tl = kPair ? decode_pair_item(gt, s_it, p, ti, rank, kOutCols, !kDual, mc)
+                                : decode_tile(gt, p, ti, kOutCols, !kDual);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, limit, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
@@ -516,110 +464,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           tmem_ld32_sync(tb + c, v);
           if (valid) store32<T>(yrow + c, v);
         }
-      } else {
-        // top-8 of this tile's BN experts for the thread's token
-        float bv[kMaxTopK];
-        int bi[kMaxTopK];
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-          bv[j] = -INFINITY;
-          bi[j] = 0;
-        }
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32_sync(tb + c, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = tl.n0 + c + i;
-            if (e < p.E) topk_insert(bv, bi, v[i] + (p.bias ? p.bias[e] : 0.0f), e);
-          }
-        }
-        // the accumulator is free once read
-        tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
-        if (valid) {
-          const int t = tl.a_row + r;
-          const long long cbase = (static_cast<long long>(t) * p.nq + tl.n0 / BN) * kMaxTopK;
-          float4 *cv = reinterpret_cast<float4 *>(p.cand_v + cbase);
-          int4 *ci = reinterpret_cast<int4 *>(p.cand_i + cbase);
-          cv[0] = make_float4(bv[0], bv[1], bv[2], bv[3]);
-          cv[1] = make_float4(bv[4], bv[5], bv[6], bv[7]);
-          ci[0] = make_int4(bi[0], bi[1], bi[2], bi[3]);
-          ci[1] = make_int4(bi[4], bi[5], bi[6], bi[7]);
-          __threadfence();
-          // the last of the token's nq expert blocks merges the candidates
-          if (atomicAdd(p.tok_cnt + t, 1) == p.nq - 1) {
-            __threadfence();
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-              bv[j] = -INFINITY;
-              bi[j] = 0;
-            }
-            // expert blocks in increasing order, each list by descending value
-            // with ties in increasing index: equal values keep the lower index
-            const long long tb0 = static_cast<long long>(t) * p.nq * kMaxTopK;
-            for (int q = 0; q < p.nq; ++q) {
-              // written by other CTAs before their fence and arrival:
-              // strong loads, ordered after this thread's fence
-              const float *qv = p.cand_v + tb0 + q * kMaxTopK;
-              const int *qi = p.cand_i + tb0 + q * kMaxTopK;
-              const float4 v0 = ld_relaxed_f32x4(qv), v1 = ld_relaxed_f32x4(qv + 4);
-              const int4 i0 = ld_relaxed_s32x4(qi), i1 = ld_relaxed_s32x4(qi + 4);
-              topk_insert(bv, bi, v0.x, i0.x);
-              topk_insert(bv, bi, v0.y, i0.y);
-              topk_insert(bv, bi, v0.z, i0.z);
-              topk_insert(bv, bi, v0.w, i0.w);
-              topk_insert(bv, bi, v1.x, i1.x);
-              topk_insert(bv, bi, v1.y, i1.y);
-              topk_insert(bv, bi, v1.z, i1.z);
-              topk_insert(bv, bi, v1.w, i1.w);
-            }
-            p.tok_cnt[t] = 0;  // ready for the next call
-            float ex[kMaxTopK];
-            float s = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-              ex[j] = (j < p.k) ? expf(bv[j] - bv[0]) : 0.0f;
-              s += ex[j];
-            }
-            const float inv_s = 1.0f / s;
-            // ranks inside each expert's group: lanes that chose the same
-            // expert share one atomic on its (line-padded) counter; all k
-            // atomics are issued before any result is used
-            const unsigned act = __activemask();
-            unsigned peers[kMaxTopK];
-            int base[kMaxTopK];
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-              base[j] = 0;
-              if (j < p.k) {
-                const long long o = static_cast<long long>(t) * p.k + j;
-                p.idx[o] = bi[j];
-                p.w[o] = ex[j] * inv_s;
-                peers[j] = __match_any_sync(act, bi[j]);
-                if (lane == __ffs(peers[j]) - 1)
-                  base[j] = atomicAdd(p.counts + static_cast<long long>(bi[j]) * kCountStride,
-                                      __popc(peers[j]));
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-              if (j < p.k) {
-                const int rk = __shfl_sync(act, base[j], __ffs(peers[j]) - 1) +
-                               __popc(peers[j] & ((1u << lane) - 1u));
-                if (p.rank) p.rank[static_cast<long long>(t) * p.k + j] = rk;
-                // the token goes to place rk of its expert's list
-                if (p.list) p.list[static_cast<long long>(bi[j]) * p.list_stride + rk] = t;
-              }
-            }
-          }
-        }
       }
-      if (!kRouter) {
-        tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
-      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -636,47 +483,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     cluster_sync_all();
     if (*abort_flag)
       for (int i = 0; i < 200; ++i) __nanosleep(1000);
-  }
-
-  if (kRouter && (p.offsets_out || p.counts_out)) {
-    // the last CTA to finish turns the histogram into group offsets
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-    __syncthreads();
-    if (*s_last && warp == 0) {
-      __threadfence();
-      const int E = p.E;
-      const int per = (E + 31) / 32;
-      int sum = 0;
-      for (int q = 0; q < per; ++q) {
-        const int e = lane * per + q;
-        if (e < E) sum += ld_relaxed_s32(p.counts + static_cast<long long>(e) * kCountStride);
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int run = incl - sum;
-      for (int q = 0; q < per; ++q) {
-        const int e = lane * per + q;
-        if (e < E) {
-          const int ce = ld_relaxed_s32(p.counts + static_cast<long long>(e) * kCountStride);
-          if (p.offsets_out) p.offsets_out[e] = run;
-          if (p.counts_out) p.counts_out[e] += ce;  // summed over the chunks of a call
-          run += ce;
-          // every CTA has added its counts: clear them for the next call
-          p.counts[static_cast<long long>(e) * kCountStride] = 0;
-        }
-      }
-      if (lane == 31 && p.offsets_out) p.offsets_out[E] = incl;
-      if (lane == 0) {
-        *p.done = 0u;
-        for (int q = 0; q < p.n_clear; ++q) p.clear[q * 32] = 0;
-      }
-    }
   }
 }
 
@@ -744,7 +550,6 @@ int gemm_pair_clusters() {
 
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN>();
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_STORE, kBN>();
-template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_SWIGLU, kBN>();
 template cudaError_t gemm_set_smem_attr<float, EPI_STORE, kBN>();
 template cudaError_t gemm_set_smem_attr<__nv_bfloat16, EPI_SWIGLU, kBN, true>();
@@ -759,9 +564,6 @@ template cudaError_t launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN>(const GemmMaps 
                                                                   int, cudaStream_t, bool);
 template cudaError_t launch_gemm<__nv_bfloat16, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &,
                                                                  int, cudaStream_t, bool);
-template cudaError_t launch_gemm<__nv_bfloat16, EPI_ROUTER, kRouterBN>(const GemmMaps &,
-                                                                        const GemmParams &, int,
-                                                                        cudaStream_t, bool);
 template cudaError_t launch_gemm<float, EPI_SWIGLU, kBN>(const GemmMaps &, const GemmParams &, int,
                                                           cudaStream_t, bool);
 template cudaError_t launch_gemm<float, EPI_STORE, kBN>(const GemmMaps &, const GemmParams &, int,

@@ -18,11 +18,10 @@ struct GemmTile {
 };
 static_assert(sizeof(GemmTile) == 32, "tile record is 32 bytes");
 
-enum Epilogue { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_ROUTER = 2 };
+enum Epilogue { EPI_SWIGLU = 0, EPI_STORE = 1 };
 
 constexpr int kBM = 128;      // rows per tile (TMEM lanes)
 constexpr int kBN = 256;      // MMA N: B rows per tile of the expert GEMMs
-constexpr int kRouterBN = 64; // experts per router tile (E split into E / 64 blocks)
 constexpr int kStageBudget = 4 * (kBM * 128 + kBN * 128);  // smem for the operand stages
 constexpr int kThreads = 192; // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
 constexpr int kGatherThreads = 128;  // gate/up GEMM: warps 6-9 gather routed token rows
@@ -38,7 +37,6 @@ struct GemmParams {
   int A;                   // T * k routed assignments
   int n_shared;            // 0 or 1: group E = the shared expert over all T tokens
   int nt;                  // N tiles per group
-  int ntiles_host;         // router: number of 128-token tiles
   int num_k_blocks;        // K / (128 bytes / element size)
   int n_routed;            // E
   int b_rows_per_group;    // rows of one routed group's B matrix (F or d)
@@ -47,19 +45,6 @@ struct GemmParams {
   long long ldo;           // elements per output row
   int *status;             // device status word
   int kid;                 // KernelId for failure details
-  // router epilogue
-  int k, E;
-  const float *bias;
-  int32_t *idx;
-  float *w;
-  int32_t *counts;         // [E * kCountStride], zero at the launch; the last CTA clears it again
-  int32_t *counts_out;     // [E] the last CTA adds each count to it (may be null)
-  int32_t *rank;           // [T * k] rank of each assignment inside its group (may be null)
-  int32_t *offsets_out;    // [E + 1] written by the last CTA (may be null)
-  int nq;                  // expert blocks per token (ceil(E / kRouterBN))
-  float *cand_v;           // [T][nq][kMaxTopK] per-block top-k candidates
-  int32_t *cand_i;
-  int32_t *tok_cnt;        // [T] blocks finished per token, zero between calls
   int *tile_ctr;           // grouped GEMMs: tiles claimed after each CTA's first, zero before the launch
   // gate/up GEMM: routed A rows are gathered from the tokens, row r of group
   // g's M tile m from token list[g * list_stride + m * 128 + r] (the router's
@@ -68,15 +53,14 @@ struct GemmParams {
   int32_t *list;           // [E][list_stride] tokens of each group in rank order
   long long list_stride;
   const void *x;           // [T][K] the chunk's tokens
-  unsigned *done;          // CTA completion ticket, zero at the launch; the last CTA clears it
-  int32_t *clear;          // router: n_clear words (128 bytes apart) the last CTA zeroes
-  int n_clear;
   // grouped GEMMs after the cluster router: the group offsets come from its
   // line-padded histogram counts_in (CTA 0 also writes them to offsets_out
   // and adds the counts into counts_out, when given); the down GEMM's CTA 0
   // zeroes clear_counts (that histogram) and *clear_ctr (the gate/up GEMM's
   // tile counter) for the next call, both read only by the finished gate/up
   const int32_t *counts_in;
+  int32_t *offsets_out;    // [E + 1]
+  int32_t *counts_out;     // [E], summed over a call's chunks (may be null)
   int32_t *clear_counts;
   int *clear_ctr;
 };
@@ -118,8 +102,9 @@ struct RouterArgs {
   int *status;
 };
 cudaError_t router_set_attr();
+// pdl: launched as a programmatic dependent of the previous kernel on st
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const RouterArgs &a,
-                          cudaStream_t st);
+                          cudaStream_t st, bool pdl = false);
 cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t st);
 
 // route_small.cu: routing of batches of at most kSmallRouteT bf16 tokens

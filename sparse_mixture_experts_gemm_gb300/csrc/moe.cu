@@ -92,8 +92,8 @@ struct ProfRec {
 }  // namespace
 
 constexpr int kRouteCtlCounts = 256 * kCountStride;
-// counts, then the router's done ticket, the gate/up and the down GEMM's tile
-// counters, each on its own 128-byte line
+// the router's histogram (one counter per 128-byte line), then a spare line,
+// the gate/up and the down GEMM's tile counters, each on its own line
 constexpr size_t kRouteCtlBytes = sizeof(int32_t) * (kRouteCtlCounts + 96);
 
 struct moe_handle {
@@ -111,15 +111,12 @@ struct moe_handle {
   int32_t *route_ctl = nullptr;
   float *w = nullptr, *logits = nullptr, *hdec = nullptr;
   int32_t *dctl = nullptr;  // 4-bit batch-1 path: the layer's top-k (DecodeArgs::dsel)
-  float *cand_v = nullptr;     // router: per expert block top-k candidates
-  int32_t *cand_i = nullptr;
-  int32_t *tok_cnt = nullptr;  // router: expert blocks finished per token
   int32_t *perm = nullptr;  // [A] token of each slot
   int32_t *list = nullptr;  // [E][max_tokens] tokens of each expert group in rank order
   void *hbuf = nullptr, *yp = nullptr;
   // static tensor maps
   CUtensorMap tm_dg, tm_du;  // decode gate/up GEMV boxes
-  CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_wr;
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd;
   // cluster-pair grouped GEMMs (bf16): the down weights in 128-row boxes,
   // the grid (two CTAs per cluster, 0: not available) and the smallest
   // chunk that takes them
@@ -150,7 +147,6 @@ struct moe_handle {
   std::vector<cudaEvent_t> pool;
   size_t pool_used = 0;
   int32_t *counts() { return route_ctl; }
-  unsigned *done() { return reinterpret_cast<unsigned *>(route_ctl + kRouteCtlCounts); }
   int32_t *tile_ctr(int gemm) { return route_ctl + kRouteCtlCounts + 32 * (gemm + 1); }
 };
 
@@ -248,7 +244,7 @@ int launch_router_bf16(moe_handle *h, const void *x, int T, int32_t *idx, float 
   a.list = h->list;
   a.list_stride = c.max_tokens;
   a.status = h->status;
-  MOE_TRY(launch_router(tm_x, h->tm_wr256, a, st));
+  MOE_TRY(launch_router(tm_x, h->tm_wr256, a, st, !h->prof));
   return MOE_OK;
 }
 
@@ -582,7 +578,6 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k, Tm = c.max_tokens;
   const size_t A = static_cast<size_t>(Tm) * k;
   const size_t esz = h->esz;
-  const size_t nqk = static_cast<size_t>((E + kRouterBN - 1) / kRouterBN) * kMaxTopK;
 
   // carve the workspace
   struct Part {
@@ -599,9 +594,6 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
       {reinterpret_cast<void **>(&h->logits), sizeof(float) * E},
       {reinterpret_cast<void **>(&h->hdec), sizeof(float) * (k + 1) * F},
       {reinterpret_cast<void **>(&h->dctl), sizeof(int32_t) * 32 * kSelReplicas},
-      {reinterpret_cast<void **>(&h->cand_v), sizeof(float) * nqk * Tm},
-      {reinterpret_cast<void **>(&h->cand_i), sizeof(int32_t) * nqk * Tm},
-      {reinterpret_cast<void **>(&h->tok_cnt), sizeof(int32_t) * Tm},
       {reinterpret_cast<void **>(&h->perm), sizeof(int32_t) * A},
       {reinterpret_cast<void **>(&h->list), sizeof(int32_t) * E * static_cast<size_t>(Tm)},
       {&h->hbuf, esz * (A + Tm) * F},
@@ -627,7 +619,6 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
 
   // tensor maps of the weights and the fixed workspace buffers
   bool ok = make_map(&h->tm_h, h->hbuf, esz, A + Tm, F, kBM) &&
-            make_map(&h->tm_wr, c.w_router, esz, E, d, kRouterBN) &&
             make_map(&h->tm_wr256, c.w_router, esz, E, d, 256);
   if (ok && !q4)
     ok = encode_map_2d(&h->tm_dg, c.w_gate, esz, static_cast<uint64_t>(E) * F, d,
@@ -687,8 +678,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
   }
   rc = c.dtype == MOE_BF16 ? set_attrs<__nv_bfloat16>(c) : set_attrs<float>(c);
   if (rc == MOE_OK && c.dtype == MOE_BF16 &&
-      (gemm_set_smem_attr<__nv_bfloat16, EPI_ROUTER, kRouterBN>() != cudaSuccess ||
-       router_set_attr() != cudaSuccess || route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
+      (router_set_attr() != cudaSuccess || route_small_set_attr() != cudaSuccess || small_gemv_set_attr() != cudaSuccess ||
        small_gemv_q4_set_attr() != cudaSuccess))
     rc = MOE_ERR_CUDA;
   if (rc == MOE_OK && c.dtype == MOE_BF16 && !q4) {
@@ -949,11 +939,9 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail) {
   int s[2] = {0, 0};
   if (cudaMemcpy(s, h->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->status, 0, sizeof s) != cudaSuccess) return MOE_ERR_CUDA;
-  // an aborted launch can leave the router's per-token arrival counts, its
-  // histogram and ticket or the GEMMs' tile counters behind
-  if (s[0] != MOE_OK && (cudaMemset(h->route_ctl, 0, kRouteCtlBytes) != cudaSuccess ||
-                         cudaMemset(h->tok_cnt, 0, sizeof(int32_t) * h->cfg.max_tokens) !=
-                             cudaSuccess))
+  // an aborted launch can leave the router's histogram or the GEMMs' tile
+  // counters behind
+  if (s[0] != MOE_OK && cudaMemset(h->route_ctl, 0, kRouteCtlBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (detail) *detail = s[1];
   return s[0];

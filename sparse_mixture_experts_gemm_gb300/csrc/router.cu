@@ -11,8 +11,10 @@
 // accumulator in TMEM), so each CTA streams a quarter of the tile's tokens
 // and of the router weights.  The four partial logit blocks are then
 // exchanged through distributed shared memory: CTA r receives the partials
-// of tokens 32 r .. 32 r + 31 from all four CTAs into its (now idle) operand
-// ring, sums them in a fixed order (deterministic), adds the router bias and
+// of tokens 32 r .. 32 r + 31 from the other three CTAs into its (now idle)
+// operand ring, each 4 KB block staged by the sending warp and moved by one
+// bulk copy that completes a byte-counting barrier of the receiver; it sums
+// the four partials in a fixed order (deterministic), adds the router bias and
 // takes each token's top-k with eight threads per token (32 experts each,
 // then three pairwise merges).  The thread that ends with a token's list
 // writes its experts and weights and claims each assignment's rank inside
@@ -20,9 +22,8 @@
 //
 // Warp 0 issues the TMA loads, warp 1 the MMAs, warps 2-9 drain TMEM into the
 // owners' partial buffers and then select.  Every wait is bounded; a CTA that
-// gave up tells the other CTAs of its cluster before the exchange, and then
-// none of them exchanges or writes, but all still meet at both cluster
-// barriers.
+// gave up tells the other CTAs of its cluster at the cluster barrier before
+// the exchange, and then none of them exchanges or writes.
 #include <cuda_bf16.h>
 
 #include "../../include/moe.h"
@@ -40,26 +41,48 @@ constexpr int kRABytes = kBM * 128;           // 128 tokens x 64 columns
 constexpr int kRBBytes = kRN * 128;           // 256 router rows x 64 columns
 constexpr int kRStageBytes = kRABytes + kRBBytes;
 constexpr int kRRows = kBM / kRSplit;         // tokens finished per CTA
-constexpr int kRRowFloats = kRN + 4;          // 1040-byte rows of the partial buffer
-constexpr int kRRedBytes = kRSplit * kRRows * kRRowFloats * 4;
-static_assert(kRRedBytes <= kRStages * kRStageBytes, "the partials reuse the operand ring");
+// partial logits of one source CTA and 32 columns for the 32 tokens a CTA
+// finishes: [32 rows][32 floats], 4 KB, the unit of the exchange
+constexpr int kRBlock = kRRows * 32 * 4;
+constexpr int kRRecvBytes = kRSplit * (kRN / 32) * kRBlock;  // [4 src][8 column blocks]
+constexpr int kRStageSlot = kRBlock;                          // two per epilogue warp
+static_assert(kRRecvBytes + 16 * kRStageSlot <= kRStages * kRStageBytes,
+              "the exchange reuses the operand ring");
 constexpr int kRThreads = 320;
 constexpr int kREpiWarps = 8;
 constexpr int kRCtrl = 2048;
 constexpr int kRSmem = kRStages * kRStageBytes + 1024 + kRCtrl;
 
-// 16-byte chunk q (of 64) of a row of partials is kept at chunk q ^ (q / 8 %
-// 8): the eight threads that read one token's row take chunks 8 s + u with
-// s = 0..7, which this spreads over all 32 banks.
-__device__ __forceinline__ int red_chunk(int q) { return q ^ ((q >> 3) & 7); }
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t rank, float4 v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
+// Inside a block [32 rows][32 floats] of column block c, 16-byte chunk u of
+// row j is kept at chunk u ^ ((j ^ c) % 8): a warp writing one chunk of all
+// its rows, and the eight threads of a token reading chunk u of blocks
+// c = 0..7, both spread over all 32 banks.
+__device__ __forceinline__ int blk_off(int c, int j, int u) {
+  return c * kRBlock + j * 128 + ((u ^ ((j ^ c) & 7)) << 4);
 }
+
+// Bulk copy of `bytes` of this CTA's shared memory into cluster CTA `rank`
+// at the offset of `dst`, completing its barrier at the offset of `bar`.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar,
+                                         uint32_t rank) {
+  uint32_t rdst, rbar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(dst), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar), "r"(rank));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(rdst), "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the bulk copies this thread issued have read their source (all, or all
+// but the last one)
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_but1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void st_cluster_s32(uint32_t local, uint32_t rank, int v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
@@ -95,7 +118,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + kRStages * kRABytes;
-  float *red = reinterpret_cast<float *>(smem);  // after the MMAs: [4 src][32 rows][260]
+  // after the MMAs: partials received [4 src][8 column blocks] at the
+  // ring's start, then one staging block per epilogue warp
+  uint8_t *recv = smem;
+  uint8_t *stage_blk = smem + kRRecvBytes;
   uint8_t *ctrl = smem + kRStages * kRStageBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 256);
@@ -106,6 +132,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kRStages;
   const uint32_t tfull = empty0 + 8 * kRStages;
+  const uint32_t rbar = tfull + 8;  // the other CTAs' partials have landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -120,9 +147,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(tfull, 1);
+    mbar_init(rbar, 1);
     *abort_flag = 0;
     *s_err = 0;
     fence_mbar_init();
+    // three CTAs each send this CTA 8 blocks
+    mbar_arrive_expect_tx(rbar, (kRSplit - 1) * (kRN / 32) * kRBlock);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
@@ -220,31 +250,51 @@ __global__ void __launch_bounds__(kRThreads, 1)
   cluster_sync_all();
   const bool go = *s_err == 0;
 
+  bool have = go;
   if (go && warp >= 2) {
     // TMEM lanes 32 (warp % 4) .. + 31 (tokens) belong to owner CTA warp % 4;
-    // warps 2-5 send columns 0-127, warps 6-9 columns 128-255
+    // warps 2-5 hold column blocks 0-3, warps 6-9 blocks 4-7.  A block for
+    // this CTA goes straight into its receive buffer; one for another CTA is
+    // staged and sent by one bulk copy into that CTA's buffer.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    const uint32_t rbase = smem_u32(red) + ((rank * kRRows + lane) * kRRowFloats) * 4;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      const int col0 = h * 128 + c * 32;
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c = 4 * h + cc;
       float v[32];
-      tmem_ld32_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
+      tmem_ld32_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * c, v);
+      const bool mine = q == static_cast<int>(rank);
+      // two staging slots per warp, used in turn
+      uint8_t *slot = stage_blk + ((warp - 2) * 2 + (cc & 1)) * kRStageSlot;
+      uint8_t *dst = mine ? recv + rank * (kRN / 32) * kRBlock : slot - c * kRBlock;
+      if (!mine && cc >= 2) {
+        // the copy that used this slot two blocks ago has read it
+        if (lane == 0) bulk_wait_read_but1();
+        __syncwarp();
+      }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int chunk = red_chunk((col0 >> 2) + u);
-        st_cluster_v4(rbase + chunk * 16, q,
-                      make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<float4 *>(dst + blk_off(c, lane, u)) =
+            make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      if (!mine) {
+        fence_proxy_async_smem();  // the copy engine reads what the threads wrote
+        __syncwarp();
+        if (lane == 0)
+          bulk_s2s(smem_u32(recv + (rank * (kRN / 32) + c) * kRBlock), smem_u32(slot), kRBlock,
+                   rbar, q);
       }
     }
+    if (lane == 0) bulk_wait_read();
+    // this CTA's own blocks, written by all eight warps, then the others'
+    named_bar_sync(1, kREpiWarps * 32);
+    const bool r_ok = mbar_wait(rbar, 0, limit, nullptr);
+    if (!__all_sync(0xffffffffu, r_ok)) {
+      have = false;
+      if (lane == 0) report_error(a.status, MOE_ERR_DEVICE_TIMEOUT, KID_ROUTER * 100 + SITE_DRAIN);
+    }
   }
-  tc_fence_before();
-  __syncwarp();
-  // every partial has landed in its owner's buffer
-  cluster_sync_all();
 
-  if (go && warp >= 2) {
+  if (have && warp >= 2) {
     // ------------------------------------------------------------ select
     // thread (j, s): token j of this CTA's 32, experts 32 s .. 32 s + 31
     const int t_loc = (warp - 2) * 32 + lane;
@@ -258,11 +308,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int off = (j * kRRowFloats + (8 * s + (u ^ s)) * 4);
-      float4 acc = *reinterpret_cast<const float4 *>(red + off);
+      const int off = blk_off(s, j, u);
+      float4 acc = *reinterpret_cast<const float4 *>(recv + off);
 #pragma unroll
       for (int src = 1; src < kRSplit; ++src) {
-        const float4 p = *reinterpret_cast<const float4 *>(red + src * kRRows * kRRowFloats + off);
+        const float4 p =
+            *reinterpret_cast<const float4 *>(recv + src * (kRN / 32) * kRBlock + off);
         acc.x += p.x;
         acc.y += p.y;
         acc.z += p.z;
@@ -348,7 +399,7 @@ cudaError_t router_set_attr() {
 }
 
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const RouterArgs &a,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
   const int ntiles = (a.T + kBM - 1) / kBM;
   cudaLaunchConfig_t cfg = {};
@@ -356,13 +407,17 @@ cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, cons
   cfg.blockDim = dim3(kRThreads);
   cfg.dynamicSmemBytes = kRSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kRSplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of whatever ran before: the prologue (barriers,
+  // TMEM, the bias) overlaps it, the tokens are read after the wait
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, router_kernel, tm_x, tm_w, a);
 }
 
