@@ -15,8 +15,9 @@
 // operand ring, each 4 KB block staged by the sending warp and moved by one
 // bulk copy that completes a byte-counting barrier of the receiver; it sums
 // the four partials in a fixed order (deterministic), adds the router bias and
-// takes each token's top-k with eight threads per token (32 experts each,
-// then three pairwise merges).  The thread that ends with a token's list
+// takes each token's top-k with eight threads per token: each sorts its 32
+// experts' (logit, expert) keys in groups of 8 with bitonic networks and
+// keeps the best 8, then three pairwise exchanges merge the lists.  The thread that ends with a token's list
 // writes its experts and weights and claims each assignment's rank inside
 // its expert group with one atomic per expert among the lanes of a warp.
 //
@@ -89,23 +90,61 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t local, uint32_t rank, in
   asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
-// Keep the 8 largest (value, index) pairs, sorted by descending value; a
-// candidate equal to a kept value goes after it (callers insert in
-// increasing index order, so ties keep the lower index first).  The
-// candidate is carried down the list: at each place it swaps with a smaller
-// kept pair, so value and index always move together.
-__device__ __forceinline__ void top8_insert(float (&bv)[kMaxTopK], int (&bi)[kMaxTopK], float v,
-                                            int e) {
+// A logit and its expert as one 64-bit key whose unsigned order is the
+// selection order: larger logit first, then (for equal logits) the lower
+// expert.  The float is mapped to an unsigned integer of the same order
+// (sign bit set: all bits flipped; clear: sign bit set) above 255 - e, so a
+// logit and its expert always move together.  Adding +0 first turns -0 into
+// +0 (they compare equal as floats).
+__device__ __forceinline__ unsigned long long logit_key(float v, int e) {
+  const unsigned u = __float_as_uint(v + 0.0f);
+  const unsigned o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | static_cast<unsigned>(255 - e);
+}
+__device__ __forceinline__ float key_logit(unsigned long long k) {
+  const unsigned o = static_cast<unsigned>(k >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ int key_expert(unsigned long long k) {
+  return 255 - static_cast<int>(k & 0xFFu);
+}
+
+// a >= b afterwards
+__device__ __forceinline__ void cx(unsigned long long &a, unsigned long long &b) {
+  const bool sw = a < b;
+  const unsigned long long hi = sw ? b : a, lo = sw ? a : b;
+  a = hi;
+  b = lo;
+}
+// Sort 8 keys descending (bitonic network: 24 independent-per-stage
+// compare-exchanges).
+__device__ __forceinline__ void sort8(unsigned long long (&a)[8]) {
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    const bool gt = v > bv[j];
-    const float kv = bv[j];
-    const int ki = bi[j];
-    bv[j] = gt ? v : kv;
-    bi[j] = gt ? e : ki;
-    v = gt ? kv : v;
-    e = gt ? ki : e;
-  }
+  for (int k = 2; k <= 8; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0) cx(a[i], a[l]);
+          else cx(a[l], a[i]);
+        }
+      }
+}
+// a := the 8 largest of a and b (both sorted descending), sorted descending:
+// the element-wise larger of a[i] and b[7 - i] are those 8 (a bitonic
+// sequence), which three stages of compare-exchanges sort.
+__device__ __forceinline__ void merge8(unsigned long long (&a)[8], const unsigned long long (&b)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = a[i] > b[7 - i] ? a[i] : b[7 - i];
+#pragma unroll
+  for (int j = 4; j > 0; j >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int l = i ^ j;
+      if (l > i) cx(a[i], a[l]);
+    }
 }
 
 }  // namespace
@@ -299,48 +338,54 @@ __global__ void __launch_bounds__(kRThreads, 1)
     // thread (j, s): token j of this CTA's 32, experts 32 s .. 32 s + 31
     const int t_loc = (warp - 2) * 32 + lane;
     const int j = t_loc >> 3, s = t_loc & 7;
+    // each thread: the sorted top 8 of its 32 experts, in four groups of 8
+    unsigned long long top[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      unsigned long long grp[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int u = 2 * g + h;
+        const int off = blk_off(s, j, u);
+        float4 acc = *reinterpret_cast<const float4 *>(recv + off);
+#pragma unroll
+        for (int src = 1; src < kRSplit; ++src) {
+          const float4 p =
+              *reinterpret_cast<const float4 *>(recv + src * (kRN / 32) * kRBlock + off);
+          acc.x += p.x;
+          acc.y += p.y;
+          acc.z += p.z;
+          acc.w += p.w;
+        }
+        const int e0 = 32 * s + 4 * u;
+        grp[4 * h] = logit_key(acc.x + s_bias[e0], e0);
+        grp[4 * h + 1] = logit_key(acc.y + s_bias[e0 + 1], e0 + 1);
+        grp[4 * h + 2] = logit_key(acc.z + s_bias[e0 + 2], e0 + 2);
+        grp[4 * h + 3] = logit_key(acc.w + s_bias[e0 + 3], e0 + 3);
+      }
+      sort8(grp);
+      if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) top[i] = grp[i];
+      } else {
+        merge8(top, grp);
+      }
+    }
+    // the eight threads of a token exchange and merge their lists pairwise;
+    // both threads of a pair end with the same list
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+      unsigned long long other[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) other[i] = __shfl_xor_sync(0xffffffffu, top[i], m);
+      merge8(top, other);
+    }
     float bv[kMaxTopK];
     int bi[kMaxTopK];
 #pragma unroll
     for (int i = 0; i < kMaxTopK; ++i) {
-      bv[i] = -INFINITY;
-      bi[i] = 0;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int off = blk_off(s, j, u);
-      float4 acc = *reinterpret_cast<const float4 *>(recv + off);
-#pragma unroll
-      for (int src = 1; src < kRSplit; ++src) {
-        const float4 p =
-            *reinterpret_cast<const float4 *>(recv + src * (kRN / 32) * kRBlock + off);
-        acc.x += p.x;
-        acc.y += p.y;
-        acc.z += p.z;
-        acc.w += p.w;
-      }
-      const int e0 = 32 * s + 4 * u;
-      top8_insert(bv, bi, acc.x + s_bias[e0], e0);
-      top8_insert(bv, bi, acc.y + s_bias[e0 + 1], e0 + 1);
-      top8_insert(bv, bi, acc.z + s_bias[e0 + 2], e0 + 2);
-      top8_insert(bv, bi, acc.w + s_bias[e0 + 3], e0 + 3);
-    }
-    // merge the eight lists of a token: at each step the thread with the
-    // lower experts takes its partner's list (all of whose experts are
-    // higher, so equal values keep the lower expert first)
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
-      float pv[kMaxTopK];
-      int pi[kMaxTopK];
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        pv[i] = __shfl_xor_sync(0xffffffffu, bv[i], m);
-        pi[i] = __shfl_xor_sync(0xffffffffu, bi[i], m);
-      }
-      if ((s & m) == 0) {
-#pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i) top8_insert(bv, bi, pv[i], pi[i]);
-      }
+      bv[i] = key_logit(top[i]);
+      bi[i] = key_expert(top[i]);
     }
     const int t = tile * kBM + static_cast<int>(rank) * kRRows + j;
     if (s == 0 && t < a.T) {
