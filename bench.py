@@ -134,7 +134,7 @@ DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
 DECODE_Q4_TRAFFIC_LAYER = 1_081_344 + 10_664_960 + 5_347_584
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
 # ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
-GEMM1_TRAFFIC_4K = 1_095_102_720 + 8_815_104
+GEMM1_TRAFFIC_4K = 1_095_047_424 + 8_568_576
 
 
 def algorithmic_prefill(cfg: dict, counts: np.ndarray, T: int) -> dict:

@@ -363,36 +363,12 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   return v;
 }
 
-// Loads of data that another CTA or a preceding kernel wrote (routing
-// results, candidates, histograms, h, Y, tokens handed down a launch chain).
-// Each is one volatile asm statement with a memory clobber, so the compiler
-// neither moves it above the fence, atomic or dependency wait that made the
-// data visible nor merges it with an earlier read of the same address.
-// ld.relaxed.gpu is a strong load at GPU scope (it bypasses the SM's L1):
-// the form for data published by a fence and an atomic inside one grid.
-// ld.global.cg (L2 only) is the form for data a completed predecessor grid
-// wrote, read after griddepcontrol.wait.
-__device__ __forceinline__ int ld_relaxed_s32(const int *p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_relaxed_f32x4(const float *p) {
-  float4 v;
-  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ int4 ld_relaxed_s32x4(const int *p) {
-  int4 v;
-  asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
+// Loads of data that a preceding kernel wrote (routing results, h, Y,
+// tokens handed down a launch chain), read after griddepcontrol.wait.  Each
+// is one volatile asm statement with a memory clobber, so the compiler
+// neither moves it above the dependency wait that made the data visible nor
+// merges it with an earlier read of the same address.  ld.global.cg reads
+// through L2 only.
 __device__ __forceinline__ uint4 ld_cg16(const void *p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
