@@ -16,27 +16,39 @@ namespace {
 // denominator overflows to inf and the quotient is 0, the function's limit.
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// 32 consecutive bytes from eight words (dst 32-byte aligned): a thread's
+// store covers whole 32-byte sectors, so none reaches L2 as two halves
+__device__ __forceinline__ void st_global_32b(void *dst, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// 32 floats of one output row (dst 64-byte aligned for bf16, 128 for fp32)
 template <typename T>
 __device__ __forceinline__ void store32(T *dst, const float (&v)[32]);
 template <>
 __device__ __forceinline__ void store32<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&v)[32]) {
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t w[4];
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[q * 8 + 2 * j], v[q * 8 + 2 * j + 1]);
+    for (int j = 0; j < 8; ++j) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[q * 16 + 2 * j], v[q * 16 + 2 * j + 1]);
       w[j] = *reinterpret_cast<uint32_t *>(&b);
     }
-    d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    st_global_32b(dst + q * 16, w);
   }
 }
 template <>
 __device__ __forceinline__ void store32<float>(float *dst, const float (&v)[32]) {
-  float4 *d = reinterpret_cast<float4 *>(dst);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(v[q * 8 + j]);
+    st_global_32b(dst + q * 8, w);
+  }
 }
 
 // Group table built by every CTA of a grouped GEMM: s_off[g] = first slot of

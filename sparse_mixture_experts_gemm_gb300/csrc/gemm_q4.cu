@@ -83,7 +83,7 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 s2, __nv_bf
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// 16 floats to 16 bf16 (two 16-byte stores; dst 32-byte aligned)
+// 16 floats to 16 bf16 (one 32-byte store; dst 32-byte aligned)
 __device__ __forceinline__ void store16_bf16(__nv_bfloat16 *dst, const float (&v)[16]) {
   uint32_t w[8];
 #pragma unroll
@@ -91,9 +91,7 @@ __device__ __forceinline__ void store16_bf16(__nv_bfloat16 *dst, const float (&v
     __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
     w[j] = *reinterpret_cast<uint32_t *>(&b);
   }
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
-  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  st_global_32b(dst, w);
 }
 
 }  // namespace

@@ -1,13 +1,14 @@
-"""Grouped GEMMs on clusters of two CTAs (MOE_OPT_PAIR_MIN_TOKENS), through the
-C ABI.
+"""Launch options that must not change a result bit, through the C ABI.
 
-In that mode two CTAs of a thread-block cluster multiply consecutive 128-row
-tiles of one expert group with the same weight tile, each loading half of it
-into both; a group's last tile (odd tile counts) runs beside the next N tile
-of the same rows, and with an odd number of N tiles one CTA of the last item
-runs without rows.  Every tile is the same MMA sequence as in the one-CTA
-mode, so the outputs must be equal bit for bit; each case is also checked
-against the oracle on every row (1e-2 row-normwise).
+* MOE_OPT_PAIR_MIN_TOKENS: grouped GEMMs on clusters of two CTAs.  Two CTAs
+  of a thread-block cluster multiply consecutive 128-row tiles of one expert
+  group with the same weight tile, each loading half of it into both; a
+  group's last tile (odd tile counts) runs beside the next N tile of the same
+  rows, and with an odd number of N tiles one CTA of the last item runs
+  without rows.  Every tile is the same MMA sequence as in the one-CTA mode.
+
+Outputs must be equal bit for bit across the settings; each case is also
+checked against the oracle on every row (1e-2 row-normwise).
 """
 import pytest
 import torch
