@@ -128,13 +128,13 @@ def make_layer(cfg: dict, dev, seed: int):
 
 
 # DRAM bytes of one batch-1 layer (kernels A + B + C, reads; nothing is
-# written back during them), from the ncu capture in profiles/decode_layer.md.
+# written back during them), from one ncu capture of the same kernel build.
 DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
-# The same for the 4-bit layer, from profiles/decode_q4_layer.md.
+# The same for the 4-bit layer.
 DECODE_Q4_TRAFFIC_LAYER = 1_081_344 + 10_664_960 + 5_347_584
-# DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from the
-# ncu capture summarised in profiles/gemm_prefill4k.md (same kernel build).
-GEMM1_TRAFFIC_4K = 1_095_047_424 + 8_568_576
+# DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from one
+# ncu capture of the same kernel build.
+GEMM1_TRAFFIC_4K = 1_095_424_512 + 7_973_888
 
 
 def algorithmic_prefill(cfg: dict, counts: np.ndarray, T: int) -> dict:
@@ -456,8 +456,8 @@ def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dic
 
 
 GDN = {"T": 2048, "Hk": 16, "Hv": 32, "dk": 128, "dv": 128, "seed": 31}
-# DRAM bytes (read + write) of one scan launch on that workload, from the ncu
-# capture summarised in profiles/gdn_scan_2k.md (same kernel build)
+# DRAM bytes (read + write) of one scan launch on that workload, from one ncu
+# capture of the same kernel build
 GDN_TRAFFIC_2K = 36_200_448 + 293_888
 
 
