@@ -129,9 +129,9 @@ def make_layer(cfg: dict, dev, seed: int):
 
 # DRAM bytes of one batch-1 layer (kernels A + B + C, reads; nothing is
 # written back during them), from one ncu capture of the same kernel build.
-DECODE_TRAFFIC_LAYER = 7_378_432 + 33_592_064 + 18_956_800
+DECODE_TRAFFIC_LAYER = 7_378_688 + 33_601_536 + 18_958_848
 # The same for the 4-bit layer.
-DECODE_Q4_TRAFFIC_LAYER = 1_081_344 + 10_664_960 + 5_347_584
+DECODE_Q4_TRAFFIC_LAYER = 1_082_368 + 10_668_032 + 5_349_632
 # DRAM bytes (read + write) of one gate/up GEMM launch at T = 4096, from one
 # ncu capture of the same kernel build.
 GEMM1_TRAFFIC_4K = 1_095_424_512 + 7_973_888
@@ -420,7 +420,8 @@ def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> flo
 def bench_small_batch(layer, cfg, dev, flush_buf, pk, iters=50, q4=False) -> dict:
     """Batches of 2..64 tokens through the same layer (the verification shape
     of speculative decoding): one routing launch, then the grouped GEMV on all
-    SMs (at most 32 tokens) or the grouped GEMMs, the combine; eager calls as
+    SMs (at most 16 tokens with bf16 weights, 32 with 4-bit ones) or the
+    grouped GEMMs, the combine; eager calls as
     a user makes them, L2 flushed before each.  q4: the layer has 4-bit expert
     weights (0.5625 bytes a weight)."""
     d, F, E, k = cfg["d"], cfg["F"], cfg["E"], cfg["k"]

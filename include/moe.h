@@ -245,9 +245,11 @@ int moe_host_join(moe_handle *h, void *cuda_stream);
 int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 
 /*
- * Tuning options of a handle; each keeps its default until set, and no
- * option changes a result bit (the same tiles are multiplied in the same
- * order either way).
+ * Tuning options of a handle; each keeps its default until set.
+ * MOE_OPT_PAIR_MIN_TOKENS changes no result bit (the same tiles are
+ * multiplied in the same order either way); MOE_OPT_GEMV_MAX_TOKENS picks
+ * between two kernels that sum in different orders (both fp32, both within
+ * the block's tolerance).
  *   MOE_OPT_PAIR_MIN_TOKENS: chunks of at least this many tokens through a
  *     bf16 handle run the grouped GEMMs on thread-block clusters of two CTAs
  *     that multiply consecutive 128-row tiles of one expert group with the
@@ -255,11 +257,18 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
  *     "Match tile size to expert load": large groups share weight traffic).
  *     Default 8192; 0 for every chunk, a value above max_tokens for none.
  *     Ignored where the device cannot run such clusters.
+ *   MOE_OPT_GEMV_MAX_TOKENS: chunks of at most this many tokens (0..32)
+ *     that route on the small-batch router run the experts as grouped GEMVs
+ *     (warp-level MMAs over all SMs) instead of the grouped GEMMs.  Default
+ *     16 for bf16 weights and 32 for 4-bit ones (where the GEMMs dequantise
+ *     every weight tile for few rows).  4-bit layers whose shapes the 4-bit
+ *     GEMMs do not take use the GEMVs whatever the value.
  * Host-side only, takes effect at the next call; not to be changed while
  * a forward on the handle is being captured into a CUDA graph.
- * Errors: INVALID_ARG (null handle, unknown option, negative value).
+ * Errors: INVALID_ARG (null handle, unknown option, value out of range).
  */
 #define MOE_OPT_PAIR_MIN_TOKENS 1
+#define MOE_OPT_GEMV_MAX_TOKENS 3
 int moe_set_option(moe_handle *h, int option, long long value);
 
 /* Free the workspace and the handle.  NULL is accepted.  The caller must make

@@ -114,8 +114,12 @@ cudaError_t launch_debug_wait(int *status, long long limit_cycles, cudaStream_t 
 constexpr int kSmallRouteT = 64;
 constexpr int kSmallRoutePass = 16;
 constexpr int kSmallRouteTokBytes = 65536;
-// gemv_small.cu: the grouped GEMVs take batches of at most kSmallGemvT tokens
+// gemv_small.cu: the grouped GEMVs take batches of at most kSmallGemvT tokens;
+// by default bf16 layers use them up to kSmallGemvTBf16 tokens (the grouped
+// GEMMs are as fast above), 4-bit layers up to kSmallGemvT
+// (moe_set_option(MOE_OPT_GEMV_MAX_TOKENS) changes the limit)
 constexpr int kSmallGemvT = 32;
+constexpr int kSmallGemvTBf16 = 16;
 // chunks of at least this many tokens run the bf16 grouped GEMMs on clusters
 // of two CTAs (moe_set_option(MOE_OPT_PAIR_MIN_TOKENS) changes it)
 constexpr long long kPairMinTokens = 8192;

@@ -124,6 +124,7 @@ struct moe_handle {
   CUtensorMap tm_wr256;  // router rows in boxes of 256 rows (the cluster router)
   int pair_grid = 0;
   long long pair_min_tokens = kPairMinTokens;
+  int gemv_max_tokens = -1;  // -1: by weight type (kSmallGemvTBf16 / kSmallGemvT)
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
   bool q4_prefill = false;  // the grouped GEMMs support the layer's shape
@@ -312,11 +313,15 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     ProfScope ps(h, MOE_KERNEL_PERMUTE, st);
     MOE_TRY(launch_place(idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
   }
-  if (small && small_gemv_fits(Tc, d, F)) {
-    // at most 32 tokens: every touched expert gets a few rows, grouped GEMV
-    // over all SMs (the tensor-core tiles of 128 rows would stay mostly empty
-    // and leave most SMs idle); up to 64 tokens the routing is still the
-    // cluster launch and the grouped GEMMs follow
+  // grouped GEMV up to the handle's limit; 4-bit shapes the 4-bit GEMMs do
+  // not take always (forward_shape_ok admitted only chunks that fit it)
+  const int gemv_max = h->gemv_max_tokens >= 0 ? h->gemv_max_tokens
+                                                : (h->q4 ? kSmallGemvT : kSmallGemvTBf16);
+  if (small && small_gemv_fits(Tc, d, F) && (Tc <= gemv_max || (h->q4 && !h->q4_prefill))) {
+    // a few tokens: every touched expert gets a few rows, grouped GEMV over
+    // all SMs (the tensor-core tiles of 128 rows would stay mostly empty and
+    // leave most SMs idle); above the limit and up to 64 tokens the routing
+    // is still the cluster launch and the grouped GEMMs follow
     SmallArgs sa;
     sa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
     sa.wg = static_cast<const __nv_bfloat16 *>(c.w_gate);
@@ -951,6 +956,10 @@ int moe_set_option(moe_handle *h, int option, long long value) {
   if (!h || value < 0) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PAIR_MIN_TOKENS: h->pair_min_tokens = value; return MOE_OK;
+    case MOE_OPT_GEMV_MAX_TOKENS:
+      if (value > kSmallGemvT) return MOE_ERR_INVALID_ARG;
+      h->gemv_max_tokens = static_cast<int>(value);
+      return MOE_OK;
     default: return MOE_ERR_INVALID_ARG;
   }
 }

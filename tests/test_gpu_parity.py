@@ -33,13 +33,15 @@ def to_dev(w, dev):
 
 
 def run_case(dev, seed, T, d, F, E, k, dtype="bf16", n_shared=1, max_tokens=None, bias=None,
-             rows=None, gen_device="cpu"):
+             rows=None, gen_device="cpu", gemv_max=None):
     w = synth.layer_weights(seed, d, F, E, n_shared, dtype, gen_device)
     x = H.margined_tokens(seed + 1000, T, w["Wr"], k, dtype, bias=bias, device=gen_device)
     wd = to_dev(w, dev)
     xd = x.to(dev)
     bd = None if bias is None else bias.to(dev)
     layer = moe.MoELayer(wd, k, max_tokens=max_tokens or max(T, 1), bias=bd)
+    if gemv_max is not None:
+        layer.set_option(moe.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
     try:
         if T <= layer.cfg.max_tokens:
             idx, wts, counts = layer.route(xd)
@@ -268,16 +270,21 @@ def test_long_prompt_128k_in_8k_chunks(dev):
         assert err.max() <= H.OUT_TOL, f"chunk {ci}: max row rel err {err.max():.3e}"
 
 
-@pytest.mark.parametrize("T", [2, 5, 16, 17, 32, 33, 64])
-def test_small_batch_routing_path(dev, T):
+@pytest.mark.parametrize("T,gemv_max", [(2, None), (5, None), (16, None), (17, None), (32, None),
+                                        (33, None), (64, None), (17, 32), (32, 32), (8, 0)])
+def test_small_batch_routing_path(dev, T, gemv_max):
     """Batches of at most 64 bf16 tokens route through one cluster launch (no
-    placement kernel); at most 32 then take the grouped GEMV (two column
-    blocks up to 16 tokens, four beyond), larger ones the grouped GEMMs: the
-    full-size layer against the oracle, every output, and the kernel kinds."""
+    placement kernel); up to the GEMV limit (16 by default, set here to 32
+    or 0 as well) they then take the grouped GEMV (two column blocks up to
+    16 tokens, four beyond), larger ones the grouped GEMMs: the full-size
+    layer against the oracle, every output, and the kernel kinds."""
     d, F, E, k = 2048, 512, 256, 8
     w = synth.layer_weights(400 + T, d, F, E, 1, "bf16", dev)
     x = H.margined_tokens(410 + T, T, w["Wr"], k, "bf16", device=dev)
     layer = moe.MoELayer(w, k, max_tokens=64)
+    if gemv_max is not None:
+        layer.set_option(moe.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
+    limit = 16 if gemv_max is None else gemv_max
     try:
         moe.moe_profile(layer.handle, True)
         out = layer.forward(x)
@@ -285,7 +292,7 @@ def test_small_batch_routing_path(dev, T):
         torch.cuda.synchronize()
         assert layer.status()[0] == 0
         kinds = {name for name, (_, n) in moe.moe_profile_read(layer.handle).items() if n > 0}
-        want = ({"router", "gemv_gate_up", "gemv_down", "combine"} if T <= 32
+        want = ({"router", "gemv_gate_up", "gemv_down", "combine"} if T <= limit
                 else {"router", "gemm_gate_up", "gemm_down", "combine"})
         assert kinds == want, kinds
     finally:
@@ -306,18 +313,18 @@ def test_small_batch_with_router_bias(dev):
                                             (32, 4, 2, 1), (29, 2, 1, 0), (24, 3, 2, 1)])
 def test_small_batch_crowded_experts(dev, T, E, k, n_shared):
     """Small batches whose routed experts get more than 8 (up to 32) tokens:
-    the second to fourth column blocks of the grouped GEMV, with and without
-    the shared expert."""
-    run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=32)
+    the second to fourth column blocks of the grouped GEMV (its limit set to
+    32 tokens), with and without the shared expert."""
+    run_case(dev, 50 + T, T, 256, 128, E, k, n_shared=n_shared, max_tokens=32, gemv_max=32)
 
 
 def test_chunks_of_up_to_64_tokens_mix_paths(dev):
     """130 tokens on a 48-token handle: chunks of 48 (cluster routing, grouped
     GEMMs), 48 and 34 (the same), every output against the oracle; and 60
     tokens on a 40-token handle: 40 (cluster routing, grouped GEMMs) then 20
-    (cluster routing, four-block grouped GEMV)."""
+    (cluster routing, four-block grouped GEMV with its limit at 32)."""
     run_case(dev, 95, 130, 512, 128, 32, 4, max_tokens=48)
-    run_case(dev, 96, 60, 512, 128, 32, 4, max_tokens=40)
+    run_case(dev, 96, 60, 512, 128, 32, 4, max_tokens=40, gemv_max=32)
 
 
 def test_chunked_prefill_with_a_small_tail(dev):

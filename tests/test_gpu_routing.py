@@ -106,14 +106,14 @@ def test_q4_decode_kernels_routing(dev):
 @pytest.mark.parametrize("T", [2, 5, 16, 17, 32, 33, 64])
 def test_small_batch_router_routing(dev, T):
     """2..64 bf16 tokens: the cluster router's choice, weights and group sizes
-    (tokens in passes of 16), before the grouped GEMV (at most 32 tokens) or
-    the grouped GEMMs."""
+    (tokens in passes of 16), before the grouped GEMV (at most 16 tokens of a
+    bf16 layer) or the grouped GEMMs."""
     d, F, E, k = 2048, 512, 256, 8
     w = synth.layer_weights(640 + T, d, F, E, 1, "bf16", dev)
     x = H.margined_tokens(650 + T, T, w["Wr"], k, "bf16", device=dev)
     layer = moe.MoELayer(w, k, max_tokens=64)
     try:
-        _routed(layer, x, w["Wr"], k, kinds=SMALL if T <= 32 else PREFILL)
+        _routed(layer, x, w["Wr"], k, kinds=SMALL if T <= 16 else PREFILL)
     finally:
         layer.close()
 
