@@ -829,7 +829,8 @@ def summary_of(line: dict) -> dict:
     bytes: prefill 4K, decode, the other prefill configurations, 4-bit
     weights, small batches and the scan."""
     r3 = lambda v: None if v is None else round(v, 3)  # noqa: E731
-    out = {"prefill4k": {"Mtok_s": r3(line["value"] / 1e6), "ms": r3(line["ms_per_step"]),
+    main = line["config"]["workload"].split(":")[0]
+    out = {main: {"Mtok_s": r3(line["value"] / 1e6), "ms": r3(line["ms_per_step"]),
                          "block_frac": r3(line["block_roofline"]["frac"]),
                          "gate_up_hbm_frac": r3(line["roofline"]["frac"]),
                          "e2e_Mtok_s": r3(line["e2e"]["value"] / 1e6)}}
