@@ -198,16 +198,19 @@ __device__ __forceinline__ void build_group_table(const GemmParams &p, int *s_of
 // M tiles 2q and 2q + 1 of one N tile, so both CTAs multiply the same weight
 // tile, each loading half of it for both -- then, when mt is odd, ceil(nt / 2)
 // items of its last M tile, N tiles 2q and 2q + 1 (each CTA its own weight
-// tile).  s_it[g] = first item of group g (g <= E + 1).  Warp 2 runs the
-// scan over the finished s_mt prefix.
+// tile).  With the two-CTA MMA (two_cta) every item is two consecutive M
+// tiles of one N tile, the second possibly empty: nt * ceil(mt / 2) items.
+// s_it[g] = first item of group g (g <= E + 1).  Warp 2 runs the scan over
+// the finished s_mt prefix.
 __device__ __forceinline__ void build_item_table(const GemmParams &p, const int *s_mt, int *s_it,
-                                                 int warp, int lane) {
+                                                 int warp, int lane, bool two_cta = false) {
   if (warp != 2) return;
   const int n = p.n_routed + 1;
   const int per = (n + 31) / 32;
   auto items = [&](int g) {
     const int mt = s_mt[g + 1] - s_mt[g];
-    return p.nt * (mt >> 1) + (mt & 1) * ((p.nt + 1) >> 1);
+    return two_cta ? p.nt * ((mt + 1) >> 1)
+                   : p.nt * (mt >> 1) + (mt & 1) * ((p.nt + 1) >> 1);
   };
   int sum = 0;
   for (int q = 0; q < per; ++q) {
@@ -281,6 +284,42 @@ __device__ __forceinline__ GemmTile decode_pair_item(const GroupTable &gt, const
     t.a_row = down ? t.out_row : m * kBM;
   }
   if (idle) t.rows = 0;
+  return t;
+}
+
+// Two-CTA-MMA work item i (two_cta items of build_item_table): group g,
+// N tile n and pair q of its M tiles, m innermost (the clusters that share a
+// weight tile run side by side); CTA `rank` of the cluster takes M tile
+// 2 q + rank, with no rows when that tile is past the group's end.
+__device__ __forceinline__ GemmTile decode_2cta_item(const GroupTable &gt, const int *s_it,
+                                                     const GemmParams &p, int i, int rank,
+                                                     int n_cols, bool down) {
+  const int E = p.n_routed;
+  int lo = 0, hi = E;  // largest g with s_it[g] <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_it[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int pairs = (gt.mt[g + 1] - gt.mt[g] + 1) >> 1;
+  const int local = i - s_it[g];
+  const int n = local / pairs;
+  const int m = 2 * (local - n * pairs) + rank;
+  GemmTile t;
+  t.group = g;
+  t.n0 = n * n_cols;
+  t.pad[0] = t.pad[1] = t.pad[2] = 0;
+  if (g < E) {
+    const int cnt = gt.off[g + 1] - gt.off[g];
+    t.a_row = gt.off[g] + m * kBM;
+    t.out_row = t.a_row;
+    t.rows = max(0, min(kBM, cnt - m * kBM));
+  } else {
+    t.rows = max(0, min(kBM, p.T - m * kBM));
+    t.out_row = p.A + m * kBM;
+    t.a_row = down ? t.out_row : m * kBM;
+  }
   return t;
 }
 

@@ -83,6 +83,15 @@ cudaError_t gemm_set_smem_attr();
 // Clusters of two pair-mode CTAs that can be resident at once (0 on error).
 int gemm_pair_clusters();
 
+// gemm2sm.cu: the bf16 grouped GEMMs on the two-CTA MMA (clusters of two,
+// grid even; the maps as for the pair mode of launch_gemm).
+template <int EPI>
+cudaError_t launch_gemm2sm(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t st,
+                           bool pdl = false);
+template <int EPI>
+cudaError_t gemm2sm_set_smem_attr();
+int gemm2sm_clusters();
+
 // router.cu: the router of chunks of more than kSmallRouteT bf16 tokens.
 // One cluster of four CTAs per 128 tokens (each a quarter of d, all experts).
 // Writes idx [T][k], w [T][k]; then either adds each expert's count into
@@ -123,6 +132,9 @@ constexpr int kSmallGemvTBf16 = 16;
 // chunks of at least this many tokens run the bf16 grouped GEMMs on clusters
 // of two CTAs (moe_set_option(MOE_OPT_PAIR_MIN_TOKENS) changes it)
 constexpr long long kPairMinTokens = 8192;
+// chunks of at least this many tokens run them on the two-CTA MMA instead
+// (moe_set_option(MOE_OPT_MMA2_MIN_TOKENS) changes it)
+constexpr long long kMma2MinTokens = 1LL << 62;
 // counts_out (may be null): each expert's group size is added to it.
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,

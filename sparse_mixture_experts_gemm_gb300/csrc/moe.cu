@@ -124,6 +124,9 @@ struct moe_handle {
   CUtensorMap tm_wr256;  // router rows in boxes of 256 rows (the cluster router)
   int pair_grid = 0;
   long long pair_min_tokens = kPairMinTokens;
+  // two-CTA-MMA grouped GEMMs (bf16): grid and smallest chunk
+  int mma2_grid = 0;
+  long long mma2_min_tokens = kMma2MinTokens;
   int gemv_max_tokens = -1;  // -1: by weight type (kSmallGemvTBf16 / kSmallGemvT)
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
@@ -361,7 +364,9 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   }
   // large chunks: the grouped GEMMs on clusters of two CTAs that share each
   // weight tile of a group's consecutive M tiles
-  const bool pair = sizeof(T) == 2 && !h->q4 && h->pair_grid > 0 && Tc >= h->pair_min_tokens;
+  const bool mma2 = sizeof(T) == 2 && !h->q4 && h->mma2_grid > 0 && Tc >= h->mma2_min_tokens;
+  const bool pair =
+      !mma2 && sizeof(T) == 2 && !h->q4 && h->pair_grid > 0 && Tc >= h->pair_min_tokens;
   GemmParams base = {};
   base.offsets = h->offsets;
   base.T = Tc;
@@ -404,6 +409,8 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
       Q4GemmMaps mq = h->q4g;
       mq.a = m.m[1];
       MOE_TRY(launch_gemm_q4<EPI_SWIGLU>(mq, p, h->num_sms, st, pdl));
+    } else if (mma2) {
+      MOE_TRY(launch_gemm2sm<EPI_SWIGLU>(m, p, h->mma2_grid, st, pdl));
     } else if (pair) {
       MOE_TRY((launch_gemm<__nv_bfloat16, EPI_SWIGLU, kBN, true>(m, p, h->pair_grid, st, pdl)));
     } else {
@@ -429,10 +436,12 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.clear_ctr = h->tile_ctr(0);
     if (h->q4) {
       MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st, pdl));
-    } else if (pair) {
+    } else if (pair || mma2) {
+      // 128-row boxes of the down weights
       m.m[3] = h->tm_wd2;
       m.m[5] = c.n_shared ? h->tm_sd2 : h->tm_wd2;
-      MOE_TRY((launch_gemm<__nv_bfloat16, EPI_STORE, kBN, true>(m, p, h->pair_grid, st, pdl)));
+      if (mma2) MOE_TRY(launch_gemm2sm<EPI_STORE>(m, p, h->mma2_grid, st, pdl));
+      else MOE_TRY((launch_gemm<__nv_bfloat16, EPI_STORE, kBN, true>(m, p, h->pair_grid, st, pdl)));
     } else {
       MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st, pdl)));
     }
@@ -694,6 +703,13 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
     const int ncl = rc == MOE_OK ? gemm_pair_clusters() : 0;
     cudaGetLastError();
     h->pair_grid = 2 * std::min(ncl, h->num_sms / 2);
+    // the same for the two-CTA MMA
+    if (rc == MOE_OK && (gemm2sm_set_smem_attr<EPI_SWIGLU>() != cudaSuccess ||
+                         gemm2sm_set_smem_attr<EPI_STORE>() != cudaSuccess))
+      rc = MOE_ERR_CUDA;
+    const int ncl2 = rc == MOE_OK ? gemm2sm_clusters() : 0;
+    cudaGetLastError();
+    h->mma2_grid = 2 * std::min(ncl2, h->num_sms / 2);
   }
   if (rc != MOE_OK) {
     moe_destroy(h);
@@ -956,6 +972,7 @@ int moe_set_option(moe_handle *h, int option, long long value) {
   if (!h || value < 0) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PAIR_MIN_TOKENS: h->pair_min_tokens = value; return MOE_OK;
+    case MOE_OPT_MMA2_MIN_TOKENS: h->mma2_min_tokens = value; return MOE_OK;
     case MOE_OPT_GEMV_MAX_TOKENS:
       if (value > kSmallGemvT) return MOE_ERR_INVALID_ARG;
       h->gemv_max_tokens = static_cast<int>(value);

@@ -6,6 +6,10 @@
   group's last tile (odd tile counts) runs beside the next N tile of the same
   rows, and with an odd number of N tiles one CTA of the last item runs
   without rows.  Every tile is the same MMA sequence as in the one-CTA mode.
+* MOE_OPT_MMA2_MIN_TOKENS: grouped GEMMs on the two-CTA MMA.  A cluster of
+  two CTAs computes 256 x 256 tiles (M tiles 2q and 2q + 1 of a group; with
+  an odd tile count the second CTA of a group's last items has no rows), each
+  CTA staging half of the weight tile; the MMA runs over K in the same order.
 
 Outputs must be equal bit for bit across the settings; each case is also
 checked against the oracle on every row (1e-2 row-normwise).
@@ -32,6 +36,8 @@ def dev():
 
 
 def both_modes(layer, x):
+    """Outputs of the one-CTA, cluster-pair and two-CTA-MMA grouped GEMMs."""
+    layer.set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, OFF)
     layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, OFF)
     one = layer.forward(x)
     layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, 0)
@@ -39,7 +45,20 @@ def both_modes(layer, x):
     torch.cuda.synchronize()
     rc, detail = layer.status()
     assert rc == 0, f"device status {rc} detail {detail}"
-    return one, pair
+    layer.set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, 0)
+    mma2 = layer.forward(x)
+    torch.cuda.synchronize()
+    rc, detail = layer.status()
+    assert rc == 0, f"device status {rc} detail {detail} (two-CTA MMA)"
+    return one, pair, mma2
+
+
+def assert_bit_equal(one, other, what):
+    if not torch.equal(one, other):
+        diff = (one.float() - other.float()).abs()
+        rows = torch.nonzero(diff.amax(dim=1) > 0).flatten()
+        raise AssertionError(f"{what}: {rows.numel()} rows differ (first {rows[:8].tolist()}), "
+                             f"max abs diff {diff.max().item():.3e}")
 
 
 # (seed, T, d, F, E, k, n_shared, max_tokens, skew)
@@ -53,7 +72,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"T{c[1]}_d{c[2]}_F{c[3]}_E{c[4]}")
-def test_pair_mode_equals_one_cta_mode_and_oracle(dev, case):
+def test_cluster_modes_equal_one_cta_mode_and_oracle(dev, case):
     seed, T, d, F, E, k, n_shared, max_tokens, skew = case
     bias = None
     if skew:
@@ -64,16 +83,18 @@ def test_pair_mode_equals_one_cta_mode_and_oracle(dev, case):
     wd = {kk: (None if v is None else v.to(dev)) for kk, v in w.items()}
     layer = moe.MoELayer(wd, k, max_tokens=max_tokens, bias=None if bias is None else bias.to(dev))
     try:
-        one, pair = both_modes(layer, x.to(dev))
+        one, pair, mma2 = both_modes(layer, x.to(dev))
     finally:
         layer.close()
-    assert torch.equal(one, pair)
+    assert_bit_equal(one, pair, "cluster pair")
     ref, *_ = H.oracle_forward(x, w, k, bias=bias)
-    err = H.row_rel_err(pair, ref)
-    assert err.max() <= H.OUT_TOL, f"max row rel err {err.max():.3e} at row {err.argmax()}"
+    for name, out in (("cluster pair", pair), ("two-CTA MMA", mma2)):
+        err = H.row_rel_err(out, ref)
+        assert err.max() <= H.OUT_TOL, f"{name}: max row rel err {err.max():.3e} at row {err.argmax()}"
+    assert_bit_equal(one, mma2, "two-CTA MMA")
 
 
-def test_pair_mode_full_size_4k_bit_equal(dev):
+def test_cluster_modes_full_size_4k_bit_equal(dev):
     """T=4096, d=2048, 256 experts top-8 + shared, F=512 (the one-CTA result is
     checked against the oracle on every row in test_gpu_parity)."""
     d, F, E, k, T = 2048, 512, 256, 8, 4096
@@ -81,13 +102,14 @@ def test_pair_mode_full_size_4k_bit_equal(dev):
     x = H.margined_tokens(1002, T, w["Wr"], k, "bf16", device=dev)
     layer = moe.MoELayer(w, k, max_tokens=T)
     try:
-        one, pair = both_modes(layer, x)
+        one, pair, mma2 = both_modes(layer, x)
     finally:
         layer.close()
-    assert torch.equal(one, pair)
+    assert_bit_equal(one, pair, "cluster pair")
+    assert_bit_equal(one, mma2, "two-CTA MMA")
 
 
-def test_pair_mode_full_size_16k_skewed_bit_equal(dev):
+def test_cluster_modes_full_size_16k_skewed_bit_equal(dev):
     """T=16384 with the Zipf(1.2) router bias: giant groups of many M tiles."""
     d, F, E, k, T = 2048, 512, 256, 8, 16384
     bias = synth.zipf_bias(3, E, 1.2)
@@ -95,7 +117,8 @@ def test_pair_mode_full_size_16k_skewed_bit_equal(dev):
     x = H.margined_tokens(1003, T, w["Wr"], k, "bf16", bias=bias, device=dev)
     layer = moe.MoELayer(w, k, max_tokens=T, bias=bias.to(dev))
     try:
-        one, pair = both_modes(layer, x)
+        one, pair, mma2 = both_modes(layer, x)
     finally:
         layer.close()
-    assert torch.equal(one, pair)
+    assert_bit_equal(one, pair, "cluster pair")
+    assert_bit_equal(one, mma2, "two-CTA MMA")
