@@ -246,8 +246,9 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 
 /*
  * Tuning options of a handle; each keeps its default until set.
- * MOE_OPT_PAIR_MIN_TOKENS and MOE_OPT_MMA2_MIN_TOKENS change no result bit
- * (the same tiles are multiplied in the same order either way);
+ * MOE_OPT_PAIR_MIN_TOKENS, MOE_OPT_MMA2_MIN_TOKENS and
+ * MOE_OPT_MMA2_DOWN_MIN_TOKENS change no result bit (the same tiles are
+ * multiplied in the same order either way);
  * MOE_OPT_GEMV_MAX_TOKENS picks
  * between two kernels that sum in different orders (both fp32, both within
  * the block's tolerance).
@@ -259,12 +260,15 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
  *     Default 8192; 0 for every chunk, a value above max_tokens for none.
  *     Ignored where the device cannot run such clusters.
  *   MOE_OPT_MMA2_MIN_TOKENS: chunks of at least this many tokens through a
- *     bf16 handle run the grouped GEMMs on the two-CTA tensor-core MMA: a
+ *     bf16 handle run the gate/up GEMM on the two-CTA tensor-core MMA: a
  *     cluster of two CTAs computes a 256 x 256 tile of one expert group, each
  *     CTA staging its own 128 rows and half of the weight tile.  Takes
- *     precedence over MOE_OPT_PAIR_MIN_TOKENS.  0 for every chunk, a value
- *     above max_tokens for none (the default).  Ignored where the device
+ *     precedence over MOE_OPT_PAIR_MIN_TOKENS.  Default 8192; 0 for every
+ *     chunk, a value above max_tokens for none.  Ignored where the device
  *     cannot run such clusters.
+ *   MOE_OPT_MMA2_DOWN_MIN_TOKENS: the same for the down GEMM (default
+ *     16384: with groups of a few hundred rows the down GEMM's short K does
+ *     not repay the half-empty tile pairs).
  *   MOE_OPT_GEMV_MAX_TOKENS: chunks of at most this many tokens (0..32)
  *     that route on the small-batch router run the experts as grouped GEMVs
  *     (warp-level MMAs over all SMs) instead of the grouped GEMMs.  Default
@@ -278,6 +282,7 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 #define MOE_OPT_PAIR_MIN_TOKENS 1
 #define MOE_OPT_GEMV_MAX_TOKENS 3
 #define MOE_OPT_MMA2_MIN_TOKENS 4
+#define MOE_OPT_MMA2_DOWN_MIN_TOKENS 5
 int moe_set_option(moe_handle *h, int option, long long value);
 
 /* Free the workspace and the handle.  NULL is accepted.  The caller must make

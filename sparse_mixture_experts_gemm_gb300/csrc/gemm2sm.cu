@@ -23,12 +23,15 @@
 // Roles (both CTAs unless noted): warp 0 lane 0 issues the TMA loads of the
 // CTA's A rows (shared expert, down projection) and B half; warp 1 allocates
 // 512 TMEM columns in both CTAs (two accumulators); in CTA 0 its lane 0
-// issues the MMAs, in CTA 1 it forwards each loaded stage to CTA 0; warps 2-5
+// issues the MMAs, in CTA 1 (gate/up) it tells CTA 0 when the rows gathered
+// into a stage have landed; warps 2-5
 // drain the CTA's accumulator rows; warps 6-9 of the gate/up GEMM gather its
-// routed A rows.  Barriers: full[s] (local: the TMA bytes and the gather
-// arrivals), pfull[s] (CTA 0 only: the partner's stage s is loaded, signalled
-// by an asynchronous remote store: a thread's remote mbarrier.arrive waits
-// for a round trip of about 1,500 cycles, longer than the stage's MMAs), empty[s]
+// routed A rows.  Barriers: full[s] in CTA 0 counts every byte of stage s in
+// both CTAs (the TMA copies of both complete it directly) and the gather
+// arrivals of CTA 0; CTA 1's gathered rows complete a local full[s], and its
+// forwarder then adds 4 bytes to CTA 0's full[s] with an asynchronous remote
+// store (a thread's remote mbarrier.arrive holds it for a round trip of about
+// 1,500 cycles, longer than a stage's MMAs).  empty[s]
 // and tfull[a] (both CTAs, arrived on by the MMA's multicast commit),
 // tempty[a] (CTA 0 only: the four epilogue warps of each CTA have drained
 // accumulator a).  Every wait is bounded; a wait that runs out records a
@@ -47,10 +50,19 @@ namespace moe {
 
 namespace {
 
-constexpr int kA2 = kBM * 128;                          // this CTA's A rows of a k-block
-constexpr int kB2 = (kBN / 2) * 128;                    // this CTA's half of the B rows
-constexpr int kStages2 = kStageBudget / (kA2 + kB2);  // 6
-constexpr int kBK2 = 64;                                // bf16 K elements per 128-byte row
+// A stage holds 128 elements of K: two 128-byte column blocks of the CTA's
+// 128 A rows and of its 128 B rows, each block a 16 KB tile in the 128-byte
+// swizzle.  One barrier wait and one commit then cover 8 MMAs: the wait
+// (about 90 cycles), the commit and the issue of each two-CTA MMA (about 80)
+// are paid by one thread, and with 64-element stages that thread needed
+// more cycles per stage than the MMAs took.
+constexpr int kBK2 = 64;                                // bf16 K elements per 128-byte block
+constexpr int kCB = 2;                                  // column blocks per stage
+constexpr int kKS = kCB * kBK2;                         // K elements per stage
+constexpr int kBlk = kBM * 128;                         // one 128-row column block: 16 KB
+constexpr int kA2 = kCB * kBlk;                         // this CTA's A rows of a stage
+constexpr int kB2 = kCB * kBlk;                         // this CTA's half of the B rows
+constexpr int kStages2 = kStageBudget / (kA2 + kB2);  // 3
 constexpr uint32_t kTmemCols2 = 2 * kBN;                // two accumulators
 static_assert(kStages2 >= 2 && kStages2 <= 8, "stage count");
 
@@ -81,12 +93,11 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
   int *s_off = reinterpret_cast<int *>(ctrl + 1536);        // [E + 1]
   int *s_mt = reinterpret_cast<int *>(ctrl + 1536 + 1040);  // [E + 2]
   int *s_it = reinterpret_cast<int *>(ctrl + 1536 + 2080);  // [E + 2]
-  uint32_t *s_pf = reinterpret_cast<uint32_t *>(ctrl + 1024);  // [kStages2] CTA 1's stage signals
+  uint32_t *s_pf = reinterpret_cast<uint32_t *>(ctrl + 1024);  // [kStages2] CTA 1's forwards
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages2;
-  const uint32_t pfull0 = empty0 + 8 * kStages2;
-  const uint32_t tfull0 = pfull0 + 8 * kStages2;
+  const uint32_t tfull0 = empty0 + 8 * kStages2;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
 
@@ -101,11 +112,11 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages2; ++s) {
-      // the TMA producer's expect-tx arrival, plus one per gather thread
-      mbar_init(full0 + 8 * s, kGather ? 1 + kGatherThreads : 1);
+      // CTA 0: its producer's expect-tx arrival and one per gather thread;
+      // CTA 1: one per gather thread (gate/up; the down GEMM does not use it)
+      mbar_init(full0 + 8 * s, rank == 0 ? 1 + (kGather ? kGatherThreads : 0)
+                                         : (kGather ? kGatherThreads : 1));
       mbar_init(empty0 + 8 * s, 1);  // CTA 0's multicast commit
-      // CTA 0's MMA thread expects 4 bytes; CTA 1's forward stores them
-      mbar_init(pfull0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -163,10 +174,14 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
       const CUtensorMap *mb = (kDual && rank == 0) ? (sh ? &tmB0s : &tmB0) : (sh ? &tmB1s : &tmB1);
       const int brow =
           (sh ? tl.n0 : tl.group * p.b_rows_per_group + tl.n0) + (kDual ? 0 : rank * (kBN / 2));
-      // gate/up: the shared expert's rows by TMA, routed rows by the gather
-      // warps; down: always (rows past the group's end are never stored)
-      const bool a_tma = !kGather || (sh && tl.rows > 0);
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      // A rows by TMA for the down GEMM and the gate/up GEMM's shared expert
+      // (also in a CTA whose tile has no rows: the box is read as zeros or
+      // ignored), otherwise by the gather warps.  CTA 0's full barrier
+      // expects the bytes of both CTAs, plus the forward for gate/up.
+      const bool a_tma = !kGather || sh;
+      const uint32_t tx = 2 * (kB2 + (a_tma ? kA2 : 0)) + (kGather ? 4 : 0);
+      const int nks = p.num_k_blocks / kCB;
+      for (int ks = 0; ks < nks; ++ks) {
         const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           if (lane == 0) {
@@ -177,20 +192,15 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
           break;
         }
         const uint32_t fb = full0 + 8 * stage;
-        const int kx = kb * kBK2;
         if (lane == 0) {
-          if (kGather) {
-            // the stage completes locally; CTA 1's forwarder hands it on
-            mbar_arrive_expect_tx(fb, (a_tma ? kA2 : 0) + kB2);
-            if (a_tma) tma_load_2d(smem_u32(sA + stage * kA2), ma, fb, kx, tl.a_row, pol_a);
-            tma_load_2d(smem_u32(sB + stage * kB2), mb, fb, kx, brow, pol_w);
-          } else {
-            // both CTAs' copies complete CTA 0's full barrier, which expects
-            // the bytes of both
-            const uint32_t fb0 = cluster_map(fb, 0);
-            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (kA2 + kB2));
-            tma_load_2d_pair(smem_u32(sA + stage * kA2), ma, fb0, kx, tl.a_row, pol_a);
-            tma_load_2d_pair(smem_u32(sB + stage * kB2), mb, fb0, kx, brow, pol_w);
+          const uint32_t fb0 = cluster_map(fb, 0);
+          if (rank == 0) mbar_arrive_expect_tx(fb, tx);
+#pragma unroll
+          for (int h = 0; h < kCB; ++h) {
+            const int kx = ks * kKS + h * kBK2;
+            if (a_tma)
+              tma_load_2d_pair(smem_u32(sA + stage * kA2 + h * kBlk), ma, fb0, kx, tl.a_row, pol_a);
+            tma_load_2d_pair(smem_u32(sB + stage * kB2 + h * kBlk), mb, fb0, kx, brow, pol_w);
           }
         }
         pend_mask |= 1u << stage;
@@ -219,10 +229,10 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
         }
       }
     }
-    if (!ok && lane == 0 && (kGather || rank == 0)) {
+    if (!ok && lane == 0 && rank == 0) {
       // copies already issued must land before the CTA's shared memory goes
-      // away (CTA 1's copies of the down GEMM complete on CTA 0, which waits
-      // for them; the CTAs meet at the final cluster barrier)
+      // away (CTA 1's copies complete on CTA 0, which waits for them; the
+      // CTAs meet at the final cluster barrier)
       for (int s = 0; s < kStages2; ++s)
         if (pend_mask & (1u << s))
           if (!mbar_wait(full0 + 8 * s, (pend_phase >> s) & 1, limit, nullptr))
@@ -248,10 +258,9 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (kGather) mbar_arrive_expect_tx(pfull0 + 8 * stage, 4);
-          if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag) ||
-              (kGather && !mbar_wait(pfull0 + 8 * stage, phase, limit, abort_flag))) {
+        const int nks = p.num_k_blocks / kCB;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag)) {
             *abort_flag = 1;
             report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
             ok = false;
@@ -268,9 +277,11 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
           const uint32_t a0 = smem_u32(sA + stage * kA2);
           const uint32_t b0 = smem_u32(sB + stage * kB2);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma2_bf16(d_tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4 * kCB; ++kk) {
+            const uint32_t off = (kk >> 2) * kBlk + 32 * (kk & 3);
+            mma2_bf16(d_tmem, sdesc_sw128(a0 + off), sdesc_sw128(b0 + off), idesc,
+                      (ks | kk) != 0 ? 1u : 0u);
+          }
           tc_commit2_mc(empty0 + 8 * stage, kBoth);
           issued = true;
           if (++stage == kStages2) {
@@ -294,10 +305,11 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
     }
   } else if (kGather && warp == 1) {
     // ------------------------------------------------------------ forwarder
-    // CTA 1: each stage this CTA loaded is handed to CTA 0's MMA issuer by
-    // an asynchronous 4-byte store that completes CTA 0's pfull barrier
+    // CTA 1: the rows its gather warps copied into stage s are handed to
+    // CTA 0's MMA issuer by an asynchronous 4-byte store that completes
+    // CTA 0's full[s]
     if (lane == 0) {
-      const uint32_t pfull_r = cluster_map(pfull0, 0);
+      const uint32_t full_r = cluster_map(full0, 0);
       const uint32_t pf_r = cluster_map(smem_u32(s_pf), 0);
       int stage = 0;
       uint32_t phase = 0;
@@ -305,7 +317,8 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
       for (int it = 0; ok; ++it) {
         const int ti = cl + it * ncl;
         if (ti >= nitems) break;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        const int nks = p.num_k_blocks / kCB;
+        for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(full0 + 8 * stage, phase, limit, abort_flag)) {
             *abort_flag = 1;
             report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, p.kid * 100 + SITE_MMA_FULL);
@@ -314,7 +327,7 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
           }
           // the gathered rows (generic proxy) before the partner's MMA reads
           fence_proxy_async_smem();
-          st_async_tx4(pf_r + 4 * stage, static_cast<uint32_t>(kb), pfull_r + 8 * stage);
+          st_async_tx4(pf_r + 4 * stage, static_cast<uint32_t>(ks), full_r + 8 * stage);
           if (++stage == kStages2) {
             stage = 0;
             phase ^= 1;
@@ -350,7 +363,8 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
         src[i] = (routed && r0 + 16 * i < tl.rows)
                      ? xg + static_cast<long long>(tok[i]) * K + c * kChunk
                      : nullptr;
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      const int nks = p.num_k_blocks / kCB;
+      for (int ks = 0; ks < nks; ++ks) {
         const bool w_ok = mbar_wait(empty0 + 8 * stage, phase ^ 1, limit, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           if (lane == 0) {
@@ -362,11 +376,14 @@ __global__ void __launch_bounds__(gemm2sm_threads<EPI>(), 1)
         }
         const uint32_t tile_dst = smem_u32(sA + stage * kA2);
 #pragma unroll
-        for (int i = 0; i < kRowsPer; ++i) {
-          const int r = r0 + 16 * i;
-          if (src[i] != nullptr)
-            cp_async16(tile_dst + r * 128 + ((c ^ (r & 7)) << 4), src[i] + kb * kBK2);
-        }
+        for (int h = 0; h < kCB; ++h)
+#pragma unroll
+          for (int i = 0; i < kRowsPer; ++i) {
+            const int r = r0 + 16 * i;
+            if (src[i] != nullptr)
+              cp_async16(tile_dst + h * kBlk + r * 128 + ((c ^ (r & 7)) << 4),
+                         src[i] + ks * kKS + h * kBK2);
+          }
         cp_async_arrive(full0 + 8 * stage);
         if (++stage == kStages2) {
           stage = 0;

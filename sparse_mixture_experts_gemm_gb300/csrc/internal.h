@@ -132,9 +132,11 @@ constexpr int kSmallGemvTBf16 = 16;
 // chunks of at least this many tokens run the bf16 grouped GEMMs on clusters
 // of two CTAs (moe_set_option(MOE_OPT_PAIR_MIN_TOKENS) changes it)
 constexpr long long kPairMinTokens = 8192;
-// chunks of at least this many tokens run them on the two-CTA MMA instead
-// (moe_set_option(MOE_OPT_MMA2_MIN_TOKENS) changes it)
-constexpr long long kMma2MinTokens = 1LL << 62;
+// chunks of at least this many tokens run the gate/up GEMM, and of at least
+// kMma2DownMinTokens the down GEMM, on the two-CTA MMA instead
+// (moe_set_option(MOE_OPT_MMA2_MIN_TOKENS / MOE_OPT_MMA2_DOWN_MIN_TOKENS))
+constexpr long long kMma2MinTokens = 8192;
+constexpr long long kMma2DownMinTokens = 16384;
 // counts_out (may be null): each expert's group size is added to it.
 cudaError_t launch_route_small(const void *x, const void *wr, const float *bias, int T, int d,
                                int E, int k, int32_t *idx, float *w, int32_t *inv, int32_t *perm,

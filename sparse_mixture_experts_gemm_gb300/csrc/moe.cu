@@ -124,9 +124,10 @@ struct moe_handle {
   CUtensorMap tm_wr256;  // router rows in boxes of 256 rows (the cluster router)
   int pair_grid = 0;
   long long pair_min_tokens = kPairMinTokens;
-  // two-CTA-MMA grouped GEMMs (bf16): grid and smallest chunk
+  // two-CTA-MMA grouped GEMMs (bf16): grid and the smallest chunk for each
   int mma2_grid = 0;
   long long mma2_min_tokens = kMma2MinTokens;
+  long long mma2_down_min_tokens = kMma2DownMinTokens;
   int gemv_max_tokens = -1;  // -1: by weight type (kSmallGemvTBf16 / kSmallGemvT)
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
@@ -362,11 +363,16 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
                               c.n_shared, h->status, st, pdl));
     return MOE_OK;
   }
-  // large chunks: the grouped GEMMs on clusters of two CTAs that share each
-  // weight tile of a group's consecutive M tiles
-  const bool mma2 = sizeof(T) == 2 && !h->q4 && h->mma2_grid > 0 && Tc >= h->mma2_min_tokens;
-  const bool pair =
-      !mma2 && sizeof(T) == 2 && !h->q4 && h->pair_grid > 0 && Tc >= h->pair_min_tokens;
+  // large chunks: the grouped GEMMs on clusters of two CTAs, either on the
+  // two-CTA MMA (256 x 256 tiles) or as pairs of one-CTA MMAs that share each
+  // weight tile of a group's consecutive M tiles; the gate/up and the down
+  // GEMM choose independently (every mode produces the same bits)
+  const bool bf16 = sizeof(T) == 2 && !h->q4;
+  const bool mma2 = bf16 && h->mma2_grid > 0 && Tc >= h->mma2_min_tokens;
+  const bool mma2_down = bf16 && h->mma2_grid > 0 && Tc >= h->mma2_down_min_tokens;
+  const bool pair_ok = bf16 && h->pair_grid > 0 && Tc >= h->pair_min_tokens;
+  const bool pair = !mma2 && pair_ok;
+  const bool pair_down = !mma2_down && pair_ok;
   GemmParams base = {};
   base.offsets = h->offsets;
   base.T = Tc;
@@ -436,11 +442,11 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     p.clear_ctr = h->tile_ctr(0);
     if (h->q4) {
       MOE_TRY(launch_gemm_q4<EPI_STORE>(h->q4d, p, h->num_sms, st, pdl));
-    } else if (pair || mma2) {
+    } else if (pair_down || mma2_down) {
       // 128-row boxes of the down weights
       m.m[3] = h->tm_wd2;
       m.m[5] = c.n_shared ? h->tm_sd2 : h->tm_wd2;
-      if (mma2) MOE_TRY(launch_gemm2sm<EPI_STORE>(m, p, h->mma2_grid, st, pdl));
+      if (mma2_down) MOE_TRY(launch_gemm2sm<EPI_STORE>(m, p, h->mma2_grid, st, pdl));
       else MOE_TRY((launch_gemm<__nv_bfloat16, EPI_STORE, kBN, true>(m, p, h->pair_grid, st, pdl)));
     } else {
       MOE_TRY((launch_gemm<T, EPI_STORE, kBN>(m, p, h->num_sms, st, pdl)));
@@ -973,6 +979,7 @@ int moe_set_option(moe_handle *h, int option, long long value) {
   switch (option) {
     case MOE_OPT_PAIR_MIN_TOKENS: h->pair_min_tokens = value; return MOE_OK;
     case MOE_OPT_MMA2_MIN_TOKENS: h->mma2_min_tokens = value; return MOE_OK;
+    case MOE_OPT_MMA2_DOWN_MIN_TOKENS: h->mma2_down_min_tokens = value; return MOE_OK;
     case MOE_OPT_GEMV_MAX_TOKENS:
       if (value > kSmallGemvT) return MOE_ERR_INVALID_ARG;
       h->gemv_max_tokens = static_cast<int>(value);

@@ -4,9 +4,10 @@ Every forward launch is asynchronous and allocation-free, and the kernels of a
 chunk are chained by programmatic dependent launch (the router too, after the
 previous kernel on the stream).  A stack of chained layers captured once must
 give, at every replay with new tokens, the same bits as the same calls made
-eagerly: at 1,024 tokens (cluster router, grouped GEMMs, one layer on the
-cluster-pair GEMMs), at 20 tokens (small-batch router and grouped GEMMs) and
-at 12 tokens (small-batch router and grouped GEMVs).
+eagerly: at 1,024 tokens (cluster router, grouped GEMMs; the second layer on
+the cluster-pair GEMMs, the third on the two-CTA-MMA GEMMs), at 20 tokens
+(small-batch router and grouped GEMMs in the same three modes) and at 12
+tokens (small-batch router and grouped GEMVs).
 """
 import pytest
 import torch
@@ -32,6 +33,8 @@ def test_prefill_stack_in_a_cuda_graph(dev, T):
     layers = [moe.MoELayer(synth.layer_weights(700 + l, d, F, E, 1, "bf16", dev), k, max_tokens=T)
               for l in range(L)]
     layers[1].set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, 0)
+    layers[2].set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, 0)
+    layers[2].set_option(moe.MOE_OPT_MMA2_DOWN_MIN_TOKENS, 0)
     try:
         x_in = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         outs = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(L)]

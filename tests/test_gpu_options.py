@@ -6,10 +6,11 @@
   group's last tile (odd tile counts) runs beside the next N tile of the same
   rows, and with an odd number of N tiles one CTA of the last item runs
   without rows.  Every tile is the same MMA sequence as in the one-CTA mode.
-* MOE_OPT_MMA2_MIN_TOKENS: grouped GEMMs on the two-CTA MMA.  A cluster of
-  two CTAs computes 256 x 256 tiles (M tiles 2q and 2q + 1 of a group; with
-  an odd tile count the second CTA of a group's last items has no rows), each
-  CTA staging half of the weight tile; the MMA runs over K in the same order.
+* MOE_OPT_MMA2_MIN_TOKENS / MOE_OPT_MMA2_DOWN_MIN_TOKENS: the gate/up and
+  the down GEMM on the two-CTA MMA.  A cluster of two CTAs computes 256 x 256
+  tiles (M tiles 2q and 2q + 1 of a group; with an odd tile count the second
+  CTA of a group's last items has no rows), each CTA staging half of the
+  weight tile; the MMA runs over K in the same order.
 
 Outputs must be equal bit for bit across the settings; each case is also
 checked against the oracle on every row (1e-2 row-normwise).
@@ -35,21 +36,25 @@ def dev():
     return torch.device("cuda:0")
 
 
+def run_mode(layer, x, pair, mma2, mma2_down):
+    layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, pair)
+    layer.set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, mma2)
+    layer.set_option(moe.MOE_OPT_MMA2_DOWN_MIN_TOKENS, mma2_down)
+    out = layer.forward(x)
+    torch.cuda.synchronize()
+    rc, detail = layer.status()
+    assert rc == 0, f"device status {rc} detail {detail} (options {pair}, {mma2}, {mma2_down})"
+    return out
+
+
 def both_modes(layer, x):
-    """Outputs of the one-CTA, cluster-pair and two-CTA-MMA grouped GEMMs."""
-    layer.set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, OFF)
-    layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, OFF)
-    one = layer.forward(x)
-    layer.set_option(moe.MOE_OPT_PAIR_MIN_TOKENS, 0)
-    pair = layer.forward(x)
-    torch.cuda.synchronize()
-    rc, detail = layer.status()
-    assert rc == 0, f"device status {rc} detail {detail}"
-    layer.set_option(moe.MOE_OPT_MMA2_MIN_TOKENS, 0)
-    mma2 = layer.forward(x)
-    torch.cuda.synchronize()
-    rc, detail = layer.status()
-    assert rc == 0, f"device status {rc} detail {detail} (two-CTA MMA)"
+    """Outputs of the one-CTA, cluster-pair and two-CTA-MMA grouped GEMMs
+    (the last also checked with a one-CTA down GEMM after it)."""
+    one = run_mode(layer, x, OFF, OFF, OFF)
+    pair = run_mode(layer, x, 0, OFF, OFF)
+    mma2 = run_mode(layer, x, OFF, 0, 0)
+    mixed = run_mode(layer, x, OFF, 0, OFF)
+    assert_bit_equal(mma2, mixed, "two-CTA gate/up + one-CTA down")
     return one, pair, mma2
 
 
