@@ -286,6 +286,22 @@ def bench_prefill(cfg, dev, steps, warmup, flush_buf):
     return res
 
 
+def gemm_kernels(chunk: int) -> dict:
+    """The grouped-GEMM kernels that bf16 chunks of `chunk` tokens run on under
+    the library's default options (two-CTA MMA for the gate/up GEMM from 8,192
+    tokens and for the down GEMM from 16,384; cluster pairs of one-CTA MMAs
+    for the down GEMM from 8,192; one CTA per tile below)."""
+    gu = ("gemm2sm_kernel<EPI_SWIGLU> (two-CTA MMA, 256 x 256 tiles)" if chunk >= 8192
+          else "gemm_kernel<bf16, EPI_SWIGLU, 256> (one CTA per 128 x 256 tile)")
+    if chunk >= 16384:
+        dn = "gemm2sm_kernel<EPI_STORE> (two-CTA MMA, 256 x 256 tiles)"
+    elif chunk >= 8192:
+        dn = "gemm_kernel<bf16, EPI_STORE, 256, pair> (cluster pairs sharing weight tiles)"
+    else:
+        dn = "gemm_kernel<bf16, EPI_STORE, 256> (one CTA per 128 x 256 tile)"
+    return {"gate_up": gu, "down": dn}
+
+
 def bench_prefill_side(name, dev, steps, warmup, flush_buf, pk) -> dict:
     """Another prefill configuration through the same kernels as the main
     line (skewed 16K, 128K in 8K chunks): step time, whole-step roofline and
@@ -326,6 +342,7 @@ def bench_prefill_side(name, dev, steps, warmup, flush_buf, pk) -> dict:
         "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
         "ms_per_step_with_kernel_events": statistics.mean(times_prof),
         "flops_per_step": flops, "algorithmic_bytes_per_step": byts,
+        "gemm_kernels": gemm_kernels(cfg["chunk"]),
         "experts_with_rows_per_chunk": [int((c > 0).sum()) for c in counts],
         "largest_group_rows": int(max(c.max() for c in counts)),
         "block_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
@@ -760,7 +777,7 @@ def main():
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": workload_config(cfg, wl_name, world),
         "roofline": {
-            "kernel": "grouped gate/up GEMM + SiLU (gemm_kernel<bf16, EPI_SWIGLU>)",
+            "kernel": "grouped gate/up GEMM + SiLU: " + gemm_kernels(cfg["chunk"])["gate_up"],
             "bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
             "frac": achieved / pk["hbm"],
             "traffic": GEMM1_TRAFFIC_4K if wl_name == "prefill4k" and GEMM1_TRAFFIC_4K else None,
