@@ -73,6 +73,9 @@ CASES = [
     (52, 129, 512, 256, 16, 4, 1, 129, False),   # single-tile groups only
     (53, 300, 512, 128, 64, 8, 1, 300, True),    # 8 groups of 300 rows (3 M tiles each)
     (54, 3000, 512, 256, 32, 4, 1, 1024, False),  # chunks of 1024, 1024, 952
+    (55, 128, 512, 256, 16, 4, 1, 128, True),    # 4 groups of exactly 128 rows, 12 empty
+    (56, 256, 512, 256, 16, 4, 1, 256, True),    # 4 groups of exactly 256 rows: full pairs
+    (57, 384, 768, 128, 16, 4, 0, 384, True),    # 3 M tiles per group, no shared expert
 ]
 
 
