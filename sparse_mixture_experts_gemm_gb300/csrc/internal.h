@@ -207,8 +207,8 @@ cudaError_t launch_place(const int32_t *idx, const int32_t *offsets, int32_t *ra
 // its rank inside the group of expert idx[t][j] (slot = offsets[e] + rank)
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
-                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
-                           bool pdl = false, const int32_t *idx = nullptr,
+                           int k, int d, int A_total, int n_shared, int *status, int num_sms,
+                           cudaStream_t st, bool pdl = false, const int32_t *idx = nullptr,
                            const int32_t *offsets = nullptr, int E = 0,
                            int *clear_ctr = nullptr);
 

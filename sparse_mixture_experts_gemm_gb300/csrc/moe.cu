@@ -360,7 +360,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     }
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
-                              c.n_shared, h->status, st, pdl));
+                              c.n_shared, h->status, h->num_sms, st, pdl));
     return MOE_OK;
   }
   // large chunks: the grouped GEMMs on clusters of two CTAs, either on the
@@ -455,7 +455,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   {
     ProfScope ps(h, MOE_KERNEL_COMBINE, st);
     MOE_TRY(launch_combine<T>(static_cast<const T *>(h->yp), h->inv, wts, out, Tc, k, d, A,
-                              c.n_shared, h->status, st, pdl, lists ? idx : nullptr,
+                              c.n_shared, h->status, h->num_sms, st, pdl, lists ? idx : nullptr,
                               lists ? h->offsets : nullptr, E, h->tile_ctr(1)));
   }
   return MOE_OK;

@@ -287,85 +287,93 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *yp, const int32_t
   if (clear_ctr && blockIdx.x == 0 && threadIdx.x == 0) *clear_ctr = 0;
   constexpr int NV = Vec<T>::N;
   const int vpr = d / NV;  // vectors per row (a multiple of 32: a warp serves one token)
-  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int t = static_cast<int>(gid / vpr);
-  const int c = static_cast<int>(gid % vpr);
-  if (t >= T_tok) return;  // whole warps
-  // the token's slots and weights: lanes j < k load slot j, lanes 16 + j its
-  // weight, once per warp, and hand them to every lane; then every row
-  // vector is requested, so all of the thread's loads are in flight
-  // together; the sum keeps the fixed order
+  // Grid-stride over the (token, vector) units: the grid is a few blocks per
+  // SM (a ragged last wave of one-token blocks cost ~1 % of the step), and a
+  // warp's 32 units always belong to one token.
+  const long long total = static_cast<long long>(T_tok) * vpr;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31;
-  int my_slot = 0;
-  float my_w = 0.0f;
-  bool bad = false;
-  if (lane < k) {
-    const long long o = static_cast<long long>(t) * k + lane;
-    my_slot = inv[o];
-    if (offsets) {
-      const int e = idx[o];
-      if (e < 0 || e >= E) bad = true;
-      else my_slot += offsets[e];
+  for (long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; gid < total;
+       gid += stride) {
+    const int t = static_cast<int>(gid / vpr);
+    const int c = static_cast<int>(gid % vpr);
+    // the token's slots and weights: lanes j < k load slot j, lanes 16 + j
+    // its weight, once per warp, and hand them to every lane; then every row
+    // vector is requested, so all of the thread's loads are in flight
+    // together; the sum keeps the fixed order
+    int my_slot = 0;
+    float my_w = 0.0f;
+    bool bad = false;
+    if (lane < k) {
+      const long long o = static_cast<long long>(t) * k + lane;
+      my_slot = inv[o];
+      if (offsets) {
+        const int e = idx[o];
+        if (e < 0 || e >= E) bad = true;
+        else my_slot += offsets[e];
+      }
     }
-  }
-  if (lane >= 16 && lane - 16 < k) my_w = w[static_cast<long long>(t) * k + lane - 16];
-  int slot[kMaxTopK];
-  float wt[kMaxTopK];
-  bad = __any_sync(0xffffffffu, bad);
+    if (lane >= 16 && lane - 16 < k) my_w = w[static_cast<long long>(t) * k + lane - 16];
+    int slot[kMaxTopK];
+    float wt[kMaxTopK];
+    bad = __any_sync(0xffffffffu, bad);
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
-    wt[j] = __shfl_sync(0xffffffffu, my_w, 16 + j);
-    if (j < k) bad = bad || slot[j] < 0 || slot[j] >= A_total;
-  }
-  if (bad) {
-    report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_COMBINE * 100 + SITE_INDEX);
-    return;
-  }
-  uint4 v[kMaxTopK + 1];
+    for (int j = 0; j < kMaxTopK; ++j) {
+      slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
+      wt[j] = __shfl_sync(0xffffffffu, my_w, 16 + j);
+      if (j < k) bad = bad || slot[j] < 0 || slot[j] >= A_total;
+    }
+    if (bad) {  // warp-uniform
+      report_error(status, MOE_ERR_DEVICE_BOUNDS, KID_COMBINE * 100 + SITE_INDEX);
+      continue;
+    }
+    uint4 v[kMaxTopK + 1];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) v[j] = ld_na16(yp + static_cast<long long>(slot[j]) * d + c * NV);
-  if (n_shared) v[kMaxTopK] = ld_na16(yp + static_cast<long long>(A_total + t) * d + c * NV);
-  float acc[NV];
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) v[j] = ld_na16(yp + static_cast<long long>(slot[j]) * d + c * NV);
+    if (n_shared) v[kMaxTopK] = ld_na16(yp + static_cast<long long>(A_total + t) * d + c * NV);
+    float acc[NV];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j < k) {
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        float f[NV];
+        Vec<T>::unpack(v[j], f);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = fmaf(wt[j], f[i], acc[i]);
+      }
+    }
+    if (n_shared) {
       float f[NV];
-      Vec<T>::unpack(v[j], f);
+      Vec<T>::unpack(v[kMaxTopK], f);
 #pragma unroll
-      for (int i = 0; i < NV; ++i) acc[i] = fmaf(wt[j], f[i], acc[i]);
+      for (int i = 0; i < NV; ++i) acc[i] += f[i];
     }
+    *reinterpret_cast<uint4 *>(out + static_cast<long long>(t) * d + c * NV) = Vec<T>::pack(acc);
   }
-  if (n_shared) {
-    float f[NV];
-    Vec<T>::unpack(v[kMaxTopK], f);
-#pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] += f[i];
-  }
-  *reinterpret_cast<uint4 *>(out + static_cast<long long>(t) * d + c * NV) = Vec<T>::pack(acc);
 }
 
 template <typename T>
 cudaError_t launch_combine(const T *yp, const int32_t *inv, const float *w, T *out, int T_tok,
-                           int k, int d, int A_total, int n_shared, int *status, cudaStream_t st,
-                           bool pdl, const int32_t *idx, const int32_t *offsets, int E,
-                           int *clear_ctr) {
+                           int k, int d, int A_total, int n_shared, int *status, int num_sms,
+                           cudaStream_t st, bool pdl, const int32_t *idx, const int32_t *offsets,
+                           int E, int *clear_ctr) {
+  constexpr long long kBlocksPerSm = 4;  // 1,024 threads per SM, 8 loads of 16 bytes each in flight
   const long long threads = static_cast<long long>(T_tok) * (d / Vec<T>::N);
-  const int grid = static_cast<int>((threads + 255) / 256);
+  const long long want = (threads + 255) / 256;
+  const int grid = static_cast<int>(want < kBlocksPerSm * num_sms ? want : kBlocksPerSm * num_sms);
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_config(grid, 256, st, pdl, &attr);
   return cudaLaunchKernelEx(&cfg, combine_kernel<T>, yp, inv, w, out, T_tok, k, d, A_total,
                             n_shared, status, idx, offsets, E, clear_ctr);
 }
 template cudaError_t launch_combine<float>(const float *, const int32_t *, const float *, float *, int,
-                                           int, int, int, int, int *, cudaStream_t, bool,
+                                           int, int, int, int, int *, int, cudaStream_t, bool,
                                            const int32_t *, const int32_t *, int, int *);
 template cudaError_t launch_combine<__nv_bfloat16>(const __nv_bfloat16 *, const int32_t *,
                                                    const float *, __nv_bfloat16 *, int, int, int, int,
-                                                   int, int *, cudaStream_t, bool, const int32_t *,
-                                                   const int32_t *, int, int *);
+                                                   int, int *, int, cudaStream_t, bool,
+                                                   const int32_t *, const int32_t *, int, int *);
 
 }  // namespace moe
