@@ -246,9 +246,10 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 
 /*
  * Tuning options of a handle; each keeps its default until set.
- * MOE_OPT_PAIR_MIN_TOKENS, MOE_OPT_MMA2_MIN_TOKENS and
- * MOE_OPT_MMA2_DOWN_MIN_TOKENS change no result bit (the same tiles are
- * multiplied in the same order either way);
+ * MOE_OPT_PAIR_MIN_TOKENS, MOE_OPT_MMA2_MIN_TOKENS,
+ * MOE_OPT_MMA2_DOWN_MIN_TOKENS and MOE_OPT_ROUTER_PAIR_MIN_TOKENS change no
+ * result bit (the same tiles are multiplied, and the same partial sums
+ * added, in the same order either way);
  * MOE_OPT_GEMV_MAX_TOKENS picks
  * between two kernels that sum in different orders (both fp32, both within
  * the block's tolerance).
@@ -269,6 +270,12 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
  *   MOE_OPT_MMA2_DOWN_MIN_TOKENS: the same for the down GEMM (default
  *     16384: with groups of a few hundred rows the down GEMM's short K does
  *     not repay the half-empty tile pairs).
+ *   MOE_OPT_ROUTER_PAIR_MIN_TOKENS: chunks of at least this many bf16 tokens
+ *     that take the cluster router run it on clusters of two CTAs per 128
+ *     tokens (each multiplying half of d) instead of four.  Default: the
+ *     smallest chunk whose four-CTA clusters would not all be resident at
+ *     once (128 * floor(SMs / 4) + 1 tokens).  0 for every such chunk, a
+ *     value above max_tokens for none.
  *   MOE_OPT_GEMV_MAX_TOKENS: chunks of at most this many tokens (0..32)
  *     that route on the small-batch router run the experts as grouped GEMVs
  *     (warp-level MMAs over all SMs) instead of the grouped GEMMs.  Default
@@ -283,6 +290,7 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
 #define MOE_OPT_GEMV_MAX_TOKENS 3
 #define MOE_OPT_MMA2_MIN_TOKENS 4
 #define MOE_OPT_MMA2_DOWN_MIN_TOKENS 5
+#define MOE_OPT_ROUTER_PAIR_MIN_TOKENS 6
 int moe_set_option(moe_handle *h, int option, long long value);
 
 /* Free the workspace and the handle.  NULL is accepted.  The caller must make

@@ -36,6 +36,7 @@ MOE_OPT_PAIR_MIN_TOKENS = 1
 MOE_OPT_GEMV_MAX_TOKENS = 3
 MOE_OPT_MMA2_MIN_TOKENS = 4
 MOE_OPT_MMA2_DOWN_MIN_TOKENS = 5
+MOE_OPT_ROUTER_PAIR_MIN_TOKENS = 6
 
 KERNEL_KINDS = ["router", "permute", "gemm_gate_up", "gemm_down", "combine", "decode_router",
                 "decode_gate_up", "decode_down", "gemv_gate_up", "gemv_down"]

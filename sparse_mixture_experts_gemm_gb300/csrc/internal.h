@@ -93,7 +93,9 @@ cudaError_t gemm2sm_set_smem_attr();
 int gemm2sm_clusters();
 
 // router.cu: the router of chunks of more than kSmallRouteT bf16 tokens.
-// One cluster of four CTAs per 128 tokens (each a quarter of d, all experts).
+// One cluster of `split` CTAs per 128 tokens (each 4 / split quarters of d,
+// all experts; split 4, or 2 when four CTAs per tile would not all be
+// resident at once).
 // Writes idx [T][k], w [T][k]; then either adds each expert's count into
 // counts_direct [E] (routing only) or claims ranks on the line-padded
 // histogram counts [E * kCountStride] (zero before the launch), writing each
@@ -109,6 +111,7 @@ struct RouterArgs {
   int32_t *list;
   long long list_stride;
   int *status;
+  int split;  // CTAs per cluster: 4 or 2 (the same results either way)
 };
 cudaError_t router_set_attr();
 // pdl: launched as a programmatic dependent of the previous kernel on st

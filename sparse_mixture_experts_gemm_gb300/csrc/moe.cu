@@ -128,6 +128,9 @@ struct moe_handle {
   int mma2_grid = 0;
   long long mma2_min_tokens = kMma2MinTokens;
   long long mma2_down_min_tokens = kMma2DownMinTokens;
+  // the router's clusters of two CTAs: from the smallest chunk whose clusters
+  // of four (4 CTAs of one SM each per 128 tokens) would not all be resident
+  long long router_pair_min_tokens = 0;
   int gemv_max_tokens = -1;  // -1: by weight type (kSmallGemvTBf16 / kSmallGemvT)
   // 4-bit expert weights (moe_create_q4)
   bool q4 = false;
@@ -227,7 +230,8 @@ struct ProfScope {
   } while (0)
 
 // The bf16 router of chunks above the small-batch size: one cluster of four
-// CTAs per 128 tokens (router.cu).  With counts_direct it writes the
+// CTAs per 128 tokens, or of two CTAs from router_pair_min_tokens on
+// (router.cu; the same results either way).  With counts_direct it writes the
 // per-expert counts for the caller; otherwise it claims ranks on the
 // handle's histogram and fills the per-expert token lists.
 int launch_router_bf16(moe_handle *h, const void *x, int T, int32_t *idx, float *w,
@@ -249,6 +253,7 @@ int launch_router_bf16(moe_handle *h, const void *x, int T, int32_t *idx, float 
   a.list = h->list;
   a.list_stride = c.max_tokens;
   a.status = h->status;
+  a.split = T >= h->router_pair_min_tokens ? 2 : 4;
   MOE_TRY(launch_router(tm_x, h->tm_wr256, a, st, !h->prof));
   return MOE_OK;
 }
@@ -595,6 +600,7 @@ int create_impl(const moe_config *cfg, const moe_q4_weights *q4, moe_handle **ou
     delete h;
     return MOE_ERR_CUDA;
   }
+  h->router_pair_min_tokens = static_cast<long long>(kBM) * (h->num_sms / 4) + 1;
   const int d = c.d_model, F = c.d_ff, E = c.n_experts, k = c.top_k, Tm = c.max_tokens;
   const size_t A = static_cast<size_t>(Tm) * k;
   const size_t esz = h->esz;
@@ -980,6 +986,7 @@ int moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_PAIR_MIN_TOKENS: h->pair_min_tokens = value; return MOE_OK;
     case MOE_OPT_MMA2_MIN_TOKENS: h->mma2_min_tokens = value; return MOE_OK;
     case MOE_OPT_MMA2_DOWN_MIN_TOKENS: h->mma2_down_min_tokens = value; return MOE_OK;
+    case MOE_OPT_ROUTER_PAIR_MIN_TOKENS: h->router_pair_min_tokens = value; return MOE_OK;
     case MOE_OPT_GEMV_MAX_TOKENS:
       if (value > kSmallGemvT) return MOE_ERR_INVALID_ARG;
       h->gemv_max_tokens = static_cast<int>(value);

@@ -5,17 +5,22 @@
 // token, and "Keep expert routing on the GPU": selection and the per-expert
 // histogram stay on the device).
 //
-// One thread-block cluster of four CTAs per tile of 128 tokens.  CTA r
-// multiplies the tokens' columns [r d/4, (r+1) d/4) with the same columns of
-// all router rows on the tensor cores (M = 128 tokens, N = 256 experts, fp32
-// accumulator in TMEM), so each CTA streams a quarter of the tile's tokens
-// and of the router weights.  The four partial logit blocks are then
-// exchanged through distributed shared memory: CTA r receives the partials
-// of tokens 32 r .. 32 r + 31 from the other three CTAs into its (now idle)
+// One thread-block cluster of S CTAs per tile of 128 tokens (S = 4, or 2 for
+// chunks whose 4-CTA clusters would not all be resident at once).  The
+// tokens' columns are cut into quarters of d; CTA r multiplies quarters
+// r 4/S .. (r + 1) 4/S - 1 with the same columns of all router rows on the
+// tensor cores (M = 128 tokens, N = 256 experts), one fp32 accumulator per
+// quarter in TMEM, so each CTA streams 1/S of the tile's tokens and of the
+// router weights.  The partial logit blocks are then exchanged through
+// distributed shared memory: CTA r receives the partials of tokens
+// 128 r / S .. 128 (r + 1) / S - 1 from the other CTAs into its (now idle)
 // operand ring, each 4 KB block staged by the sending warp and moved by one
-// bulk copy that completes a byte-counting barrier of the receiver; it sums
-// the four partials in a fixed order (deterministic), adds the router bias and
-// takes each token's top-k with eight threads per token: each sorts its 32
+// bulk copy that completes a byte-counting barrier of the receiver.  The
+// logit is (q0 + q1) + (q2 + q3) over the quarter partials q, in fp32 and in
+// this order with either S (with S = 2 each CTA adds its two quarters before
+// sending), so the result does not depend on S; the receiver adds the
+// router bias and takes each token's top-k with eight threads per token
+// (32 tokens at a time): each sorts its 32
 // experts' (logit, expert) keys in groups of 8 with bitonic networks and
 // keeps the best 8, then three pairwise exchanges merge the lists.  The thread that ends with a token's list
 // writes its experts and weights and claims each assignment's rank inside
@@ -35,17 +40,16 @@ namespace moe {
 
 namespace {
 
-constexpr int kRSplit = 4;                    // CTAs per cluster: quarters of d
 constexpr int kRN = 256;                      // experts per MMA (E <= 256)
 constexpr int kRStages = 4;
 constexpr int kRABytes = kBM * 128;           // 128 tokens x 64 columns
 constexpr int kRBBytes = kRN * 128;           // 256 router rows x 64 columns
 constexpr int kRStageBytes = kRABytes + kRBBytes;
-constexpr int kRRows = kBM / kRSplit;         // tokens finished per CTA
-// partial logits of one source CTA and 32 columns for the 32 tokens a CTA
-// finishes: [32 rows][32 floats], 4 KB, the unit of the exchange
-constexpr int kRBlock = kRRows * 32 * 4;
-constexpr int kRRecvBytes = kRSplit * (kRN / 32) * kRBlock;  // [4 src][8 column blocks]
+// partial logits of one source CTA and 32 columns for 32 of the tokens a
+// CTA finishes: [32 rows][32 floats], 4 KB, the unit of the exchange
+constexpr int kRBlock = 32 * 32 * 4;
+// [S sources][128 / S / 32 row blocks][8 column blocks]: 128 KB for either S
+constexpr int kRRecvBytes = (kBM / 32) * (kRN / 32) * kRBlock;
 constexpr int kRStageSlot = kRBlock;                          // two per epilogue warp
 static_assert(kRRecvBytes + 16 * kRStageSlot <= kRStages * kRStageBytes,
               "the exchange reuses the operand ring");
@@ -149,16 +153,22 @@ __device__ __forceinline__ void merge8(unsigned long long (&a)[8], const unsigne
 
 }  // namespace
 
+template <int S>
 __global__ void __launch_bounds__(kRThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const RouterArgs a) {
+  constexpr int kRows = kBM / S;            // tokens this CTA finishes
+  constexpr int kRB = kRows / 32;           // in row blocks of 32
+  constexpr int kQ = 4 / S;                 // quarters of d this CTA multiplies
+  constexpr uint32_t kCols = kQ * kRN;      // one accumulator per quarter
+  static_assert(S == 2 || S == 4, "clusters of two or four CTAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + kRStages * kRABytes;
-  // after the MMAs: partials received [4 src][8 column blocks] at the
-  // ring's start, then one staging block per epilogue warp
+  // after the MMAs: partials received [S src][kRB row blocks][8 column
+  // blocks] at the ring's start, then two staging blocks per epilogue warp
   uint8_t *recv = smem;
   uint8_t *stage_blk = smem + kRRecvBytes;
   uint8_t *ctrl = smem + kRStages * kRStageBytes;
@@ -175,9 +185,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int tile = static_cast<int>(blockIdx.x) / kRSplit;
-  const int nkb = a.d / (kRSplit * 64);  // K blocks of 64 columns per CTA
-  const int kx0 = static_cast<int>(rank) * (a.d / kRSplit);
+  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int nkb = a.d / (S * 64);  // K blocks of 64 columns per CTA
+  const int nkq = a.d / (4 * 64);  // K blocks per quarter of d
+  const int kx0 = static_cast<int>(rank) * (a.d / S);
   const long long limit = MOE_WAIT_LIMIT_CYCLES;
 
   if (threadIdx.x == 0) {
@@ -190,15 +201,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
     *abort_flag = 0;
     *s_err = 0;
     fence_mbar_init();
-    // three CTAs each send this CTA 8 blocks
-    mbar_arrive_expect_tx(rbar, (kRSplit - 1) * (kRN / 32) * kRBlock);
+    // every other CTA sends this CTA 8 column blocks per row block
+    mbar_arrive_expect_tx(rbar, (S - 1) * kRB * (kRN / 32) * kRBlock);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kRN);
+    tmem_alloc(smem_u32(tmem_slot), kCols);
     tmem_relinquish();
   }
   if (threadIdx.x >= 64)
@@ -256,10 +267,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + s * kRABytes);
         const uint32_t b0 = smem_u32(sB + s * kRBBytes);
+        // quarter kb / nkq of d goes to its own accumulator
+        const int qk = kb % nkq;
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>((kb / nkq) * kRN);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          MmaKind<__nv_bfloat16>::mma(tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk),
-                                      idesc, (kb | kk) != 0 ? 1u : 0u);
+          MmaKind<__nv_bfloat16>::mma(d_tmem, sdesc_sw128(a0 + 32 * kk), sdesc_sw128(b0 + 32 * kk),
+                                      idesc, (qk | kk) != 0 ? 1u : 0u);
         tc_commit(empty0 + 8 * s);
         issued = true;
       }
@@ -284,28 +298,40 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // missing or its ring still filling); the barrier also orders each CTA's
   // last MMA before any partial lands in its ring
   if (!ok || *abort_flag)
-    for (uint32_t r = 0; r < kRSplit; ++r) st_cluster_s32(smem_u32(const_cast<int *>(s_err)), r, 1);
+    for (uint32_t r = 0; r < S; ++r) st_cluster_s32(smem_u32(const_cast<int *>(s_err)), r, 1);
   __syncwarp();
   cluster_sync_all();
   const bool go = *s_err == 0;
 
   bool have = go;
   if (go && warp >= 2) {
-    // TMEM lanes 32 (warp % 4) .. + 31 (tokens) belong to owner CTA warp % 4;
-    // warps 2-5 hold column blocks 0-3, warps 6-9 blocks 4-7.  A block for
-    // this CTA goes straight into its receive buffer; one for another CTA is
-    // staged and sent by one bulk copy into that CTA's buffer.
+    // TMEM lanes 32 (warp % 4) .. + 31 (tokens) are row block rb of owner
+    // CTA (warp % 4) / kRB; warps 2-5 hold column blocks 0-3, warps 6-9
+    // blocks 4-7.  With two quarters per CTA their partials are added here
+    // (q0 + q1, or q2 + q3).  A block for this CTA goes straight into its
+    // receive buffer; one for another CTA is staged and sent by one bulk copy
+    // into that CTA's buffer, at [source = this CTA][rb][column block].
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
+    const int owner = q / kRB, rb = q % kRB;
+    uint8_t *const my_blocks = recv + (rank * kRB + rb) * (kRN / 32) * kRBlock;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int c = 4 * h + cc;
+      const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * c;
       float v[32];
-      tmem_ld32_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * c, v);
-      const bool mine = q == static_cast<int>(rank);
+      if (kQ == 2) {
+        float v1[32];
+        tmem_ld32x2_sync(ta, ta + kRN, v, v1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += v1[i];
+      } else {
+        tmem_ld32_sync(ta, v);
+      }
+      const bool mine = owner == static_cast<int>(rank);
       // two staging slots per warp, used in turn
       uint8_t *slot = stage_blk + ((warp - 2) * 2 + (cc & 1)) * kRStageSlot;
-      uint8_t *dst = mine ? recv + rank * (kRN / 32) * kRBlock : slot - c * kRBlock;
+      uint8_t *dst = mine ? my_blocks : slot - c * kRBlock;
       if (!mine && cc >= 2) {
         // the copy that used this slot two blocks ago has read it
         if (lane == 0) bulk_wait_read_but1();
@@ -319,8 +345,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         fence_proxy_async_smem();  // the copy engine reads what the threads wrote
         __syncwarp();
         if (lane == 0)
-          bulk_s2s(smem_u32(recv + (rank * (kRN / 32) + c) * kRBlock), smem_u32(slot), kRBlock,
-                   rbar, q);
+          bulk_s2s(smem_u32(my_blocks + c * kRBlock), smem_u32(slot), kRBlock, rbar,
+                   static_cast<uint32_t>(owner));
       }
     }
     if (lane == 0) bulk_wait_read();
@@ -333,11 +359,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   }
 
-  if (have && warp >= 2) {
-    // ------------------------------------------------------------ select
-    // thread (j, s): token j of this CTA's 32, experts 32 s .. 32 s + 31
+  // ------------------------------------------------------------ select
+  // thread (j, s): token j of row block rb of this CTA's tokens, experts
+  // 32 s .. 32 s + 31
+#pragma unroll 1
+  for (int rb = 0; rb < kRB && have && warp >= 2; ++rb) {
     const int t_loc = (warp - 2) * 32 + lane;
     const int j = t_loc >> 3, s = t_loc & 7;
+    // the partials of source CTA src for row block rb
+    auto part = [&](int src, int off) {
+      return *reinterpret_cast<const float4 *>(recv + (src * kRB + rb) * (kRN / 32) * kRBlock + off);
+    };
     // each thread: the sorted top 8 of its 32 experts, in four groups of 8
     unsigned long long top[8];
 #pragma unroll
@@ -347,15 +379,25 @@ __global__ void __launch_bounds__(kRThreads, 1)
       for (int h = 0; h < 2; ++h) {
         const int u = 2 * g + h;
         const int off = blk_off(s, j, u);
-        float4 acc = *reinterpret_cast<const float4 *>(recv + off);
-#pragma unroll
-        for (int src = 1; src < kRSplit; ++src) {
-          const float4 p =
-              *reinterpret_cast<const float4 *>(recv + src * (kRN / 32) * kRBlock + off);
-          acc.x += p.x;
-          acc.y += p.y;
-          acc.z += p.z;
-          acc.w += p.w;
+        // (q0 + q1) + (q2 + q3): with S = 4 the sources are the quarters,
+        // with S = 2 each source already holds its two quarters' sum
+        float4 acc = part(0, off);
+        const float4 p1 = part(1, off);
+        acc.x += p1.x;
+        acc.y += p1.y;
+        acc.z += p1.z;
+        acc.w += p1.w;
+        if (S == 4) {
+          float4 p23 = part(2, off);
+          const float4 p3 = part(3, off);
+          p23.x += p3.x;
+          p23.y += p3.y;
+          p23.z += p3.z;
+          p23.w += p3.w;
+          acc.x += p23.x;
+          acc.y += p23.y;
+          acc.z += p23.z;
+          acc.w += p23.w;
         }
         const int e0 = 32 * s + 4 * u;
         grp[4 * h] = logit_key(acc.x + s_bias[e0], e0);
@@ -387,7 +429,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       bv[i] = key_logit(top[i]);
       bi[i] = key_expert(top[i]);
     }
-    const int t = tile * kBM + static_cast<int>(rank) * kRRows + j;
+    const int t = tile * kBM + static_cast<int>(rank) * kRows + rb * 32 + j;
     if (s == 0 && t < a.T) {
       float ex[kMaxTopK];
       float sum = 0.0f;
@@ -436,25 +478,29 @@ __global__ void __launch_bounds__(kRThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kRN);
+  if (warp == 1) tmem_dealloc(tmem, kCols);
 }
 
 cudaError_t router_set_attr() {
-  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+  const cudaError_t e =
+      cudaFuncSetAttribute(router_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
 }
 
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const RouterArgs &a,
                           cudaStream_t st, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
+  if (a.split != 2 && a.split != 4) return cudaErrorInvalidValue;
   const int ntiles = (a.T + kBM - 1) / kBM;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kRSplit * ntiles);
+  cfg.gridDim = dim3(a.split * ntiles);
   cfg.blockDim = dim3(kRThreads);
   cfg.dynamicSmemBytes = kRSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kRSplit;
+  attr[0].val.clusterDim.x = a.split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // a programmatic dependent of whatever ran before: the prologue (barriers,
@@ -463,7 +509,8 @@ cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, cons
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, router_kernel, tm_x, tm_w, a);
+  return a.split == 2 ? cudaLaunchKernelEx(&cfg, router_kernel<2>, tm_x, tm_w, a)
+                      : cudaLaunchKernelEx(&cfg, router_kernel<4>, tm_x, tm_w, a);
 }
 
 }  // namespace moe

@@ -189,6 +189,6 @@ def test_gemv_limit_option_is_declared():
     """The option numbers of the binding match the header's."""
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     for name in ("MOE_OPT_PAIR_MIN_TOKENS", "MOE_OPT_GEMV_MAX_TOKENS", "MOE_OPT_MMA2_MIN_TOKENS",
-                 "MOE_OPT_MMA2_DOWN_MIN_TOKENS"):
+                 "MOE_OPT_MMA2_DOWN_MIN_TOKENS", "MOE_OPT_ROUTER_PAIR_MIN_TOKENS"):
         m = re.search(r"#define\s+" + name + r"\s+(\d+)", src)
         assert m and int(m.group(1)) == getattr(moe, name)

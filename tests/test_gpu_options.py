@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import helpers as H
+import oracle
 import sparse_mixture_experts_gemm_gb300 as moe
 from sparse_mixture_experts_gemm_gb300 import synth
 
@@ -130,3 +131,33 @@ def test_cluster_modes_full_size_16k_skewed_bit_equal(dev):
         layer.close()
     assert_bit_equal(one, pair, "cluster pair")
     assert_bit_equal(one, mma2, "two-CTA MMA")
+
+
+@pytest.mark.parametrize("T,d,E,k", [(300, 2048, 256, 8), (4096, 2048, 256, 8), (1000, 768, 64, 4)],
+                         ids=lambda v: str(v))
+def test_router_clusters_of_two_equal_clusters_of_four(dev, T, d, E, k):
+    """MOE_OPT_ROUTER_PAIR_MIN_TOKENS: the cluster router on clusters of two
+    CTAs (each half of d, its two quarter partials added before the
+    exchange) against clusters of four (one quarter each): the logits are
+    (q0 + q1) + (q2 + q3) either way, so indices, weights, counts and the
+    layer's output must be equal bit for bit; routing also against the oracle."""
+    F = 256
+    w = synth.layer_weights(60 + T, d, F, E, 1, "bf16", dev)
+    x = H.margined_tokens(1060 + T, T, w["Wr"], k, "bf16", device=dev)
+    layer = moe.MoELayer(w, k, max_tokens=T)
+    res = {}
+    try:
+        for name, v in (("four", OFF), ("two", 0)):
+            layer.set_option(moe.MOE_OPT_ROUTER_PAIR_MIN_TOKENS, v)
+            idx, wt, counts = layer.route(x)
+            out = layer.forward(x)
+            torch.cuda.synchronize()
+            rc, detail = layer.status()
+            assert rc == 0, f"device status {rc} detail {detail} ({name})"
+            res[name] = (idx, wt, counts, out)
+    finally:
+        layer.close()
+    for a, b, what in zip(res["four"], res["two"], ("indices", "weights", "counts", "output")):
+        assert_bit_equal(a.reshape(a.shape[0], -1), b.reshape(b.shape[0], -1), f"router clusters: {what}")
+    idx_ref, w_ref, _, counts_ref = oracle.route(H.np_view(x), H.np_view(w["Wr"]), k)
+    H.check_routing(*res["two"][:3], idx_ref, w_ref, counts_ref)
