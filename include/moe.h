@@ -187,8 +187,9 @@ int moe_forward(moe_handle *h, const void *x, int T, void *out, void *cuda_strea
  * used for this call (section "Keep expert routing on the GPU": the top-8,
  * the histogram of assignments per expert, all on the GPU).  Every path
  * writes what it actually used, not a second computation: the batch-1
- * kernels (T == 1), the small-batch router (chunks of at most 64 bf16
- * tokens) and the tensor-core or fp32 router of larger chunks.
+ * kernels (T == 1), the small-batch router (the bf16 chunks that run the
+ * grouped GEMVs, see MOE_OPT_GEMV_MAX_TOKENS) and the tensor-core or fp32
+ * router of the others.
  *   topk_idx [T][k] int32  device, the chosen experts of each token, by
  *                          descending logit, ties to the lower index;
  *   topk_w   [T][k] float  device, their routing weights (sum 1 per token);
@@ -277,8 +278,9 @@ int moe_status(moe_handle *h, void *cuda_stream, int *detail);
  *     once (128 * floor(SMs / 4) + 1 tokens).  0 for every such chunk, a
  *     value above max_tokens for none.
  *   MOE_OPT_GEMV_MAX_TOKENS: chunks of at most this many tokens (0..32)
- *     that route on the small-batch router run the experts as grouped GEMVs
- *     (warp-level MMAs over all SMs) instead of the grouped GEMMs.  Default
+ *     route on the small-batch router and run the experts as grouped GEMVs
+ *     (warp-level MMAs over all SMs); larger chunks take the cluster router
+ *     and the grouped GEMMs.  Default
  *     16 for bf16 weights and 32 for 4-bit ones (where the GEMMs dequantise
  *     every weight tile for few rows).  4-bit layers whose shapes the 4-bit
  *     GEMMs do not take use the GEMVs whatever the value.

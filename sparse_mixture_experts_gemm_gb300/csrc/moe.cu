@@ -275,6 +275,21 @@ bool small_route_ok(int Tc, int d) {
   return Tc <= kSmallRouteT && static_cast<long long>(pass) * d * 2 <= kSmallRouteTokBytes;
 }
 
+// The small-batch router (routing and placement in one cluster launch, 16
+// tokens per pass) serves the chunks that run the grouped GEMVs; every other
+// bf16 chunk takes the cluster router, whose per-expert token lists feed the
+// grouped GEMMs (at 32 and 64 tokens the small router's passes took 25 and
+// 42 us, the cluster router ~20).
+bool use_small_route(const moe_handle *h, int Tc) {
+  const moe_config &c = h->cfg;
+  if (c.dtype != MOE_BF16 || !small_route_ok(Tc, c.d_model) ||
+      !small_gemv_fits(Tc, c.d_model, c.d_ff))
+    return false;
+  const int gemv_max = h->gemv_max_tokens >= 0 ? h->gemv_max_tokens
+                                                : (h->q4 ? kSmallGemvT : kSmallGemvTBf16);
+  return Tc <= gemv_max || (h->q4 && !h->q4_prefill);
+}
+
 template <typename T>
 int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut &ro,
                       cudaStream_t st) {
@@ -290,7 +305,7 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
   // routers clear the GEMMs' tile counters when they are done, and after the
   // bf16 cluster router the down GEMM clears its histogram and the gate/up
   // tile counter, the combine the down tile counter
-  const bool small = sizeof(T) == 2 && small_route_ok(Tc, d);
+  const bool small = sizeof(T) == 2 && use_small_route(h, Tc);
   if (small) {
     // a few tokens: routing and placement in one cluster launch
     ProfScope ps(h, MOE_KERNEL_ROUTER, st);
@@ -323,14 +338,12 @@ int run_prefill_chunk(moe_handle *h, const T *x, int Tc, T *out, const RouteOut 
     MOE_TRY(launch_place(idx, h->offsets, h->inv, h->perm, A, k, E, h->status, st, pdl));
   }
   // grouped GEMV up to the handle's limit; 4-bit shapes the 4-bit GEMMs do
-  // not take always (forward_shape_ok admitted only chunks that fit it)
-  const int gemv_max = h->gemv_max_tokens >= 0 ? h->gemv_max_tokens
-                                                : (h->q4 ? kSmallGemvT : kSmallGemvTBf16);
-  if (small && small_gemv_fits(Tc, d, F) && (Tc <= gemv_max || (h->q4 && !h->q4_prefill))) {
+  // not take always (forward_shape_ok admitted only chunks that fit it):
+  // exactly the chunks use_small_route sent to the small-batch router
+  if (small) {
     // a few tokens: every touched expert gets a few rows, grouped GEMV over
     // all SMs (the tensor-core tiles of 128 rows would stay mostly empty and
-    // leave most SMs idle); above the limit and up to 64 tokens the routing
-    // is still the cluster launch and the grouped GEMMs follow
+    // leave most SMs idle)
     SmallArgs sa;
     sa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
     sa.wg = static_cast<const __nv_bfloat16 *>(c.w_gate);
@@ -794,7 +807,7 @@ int moe_route(moe_handle *h, const void *x, int T, int32_t *topk_idx, float *top
   if (c.dtype == MOE_BF16) {
     // the router adds each expert's assignments to counts
     MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st));
-    if (small_route_ok(T, d))
+    if (use_small_route(h, T))
       return launch_route_small(x, c.w_router, c.router_bias, T, d, E, k, topk_idx, topk_w, h->inv,
                                 h->perm, h->offsets, counts, h->tile_ctr(0), 2, st) == cudaSuccess
                  ? MOE_OK

@@ -6,7 +6,7 @@ previous kernel on the stream).  A stack of chained layers captured once must
 give, at every replay with new tokens, the same bits as the same calls made
 eagerly: at 1,024 tokens (cluster router, grouped GEMMs; the second layer on
 the cluster-pair GEMMs, the third on the two-CTA-MMA GEMMs), at 20 tokens
-(small-batch router and grouped GEMMs in the same three modes) and at 12
+(cluster router and grouped GEMMs in the same three modes) and at 12
 tokens (small-batch router and grouped GEMVs).
 """
 import pytest
