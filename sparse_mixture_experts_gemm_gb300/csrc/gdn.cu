@@ -22,10 +22,12 @@
 //
 // Tensor cores.  P, Q and the rank-8 update are matrix products of the state
 // (columns x d_k) with the block's keys and queries, so they run on m16n8k8
-// TF32 MMAs.  A CTA owns 16 columns and its 4 warps split d_k: warp w keeps
-// the state of all 16 columns at d_k chunks 4 w .. 4 w + 3 in registers in
-// the MMA accumulator layout (lane (g, c) holds columns g and g + 8 at d_k
-// positions 8 n + 2 c, 8 n + 2 c + 1 of chunk n: 16 fp32).  The update
+// TF32 MMAs.  A group of 16 columns is held by 4 warps that split d_k: warp
+// w keeps the state of all 16 columns at d_k chunks 4 w .. 4 w + 3 in
+// registers in the MMA accumulator layout (lane (g, c) holds columns g and
+// g + 8 at d_k positions 8 n + 2 c, 8 n + 2 c + 1 of chunk n: 16 fp32).  A
+// CTA owns one group, or two (8 warps) when one group per CTA would leave
+// two CTAs on some SM.  The update
 // accumulates straight into those registers.  As an operand the state is
 // split into two TF32 parts (hi = the top 11 significant bits of S, lo the
 // top 11 of S - hi), and the keys and queries, bf16, are exact in TF32, so
@@ -59,9 +61,9 @@ namespace moe {
 
 namespace {
 constexpr int kDk = 128;               // d_k supported
-constexpr int kCols = 16;              // columns per CTA
-constexpr int kWarps = 4;              // warps per CTA, each a quarter of d_k
-constexpr int kGdnThreads = kWarps * 32;
+constexpr int kCols = 16;              // columns per group (the MMAs' M)
+constexpr int kGMax = 2;               // column groups per CTA: 2, or 1 where d_v is not a multiple of 32
+constexpr int kWarps = 4;              // warps per column group, each a quarter of d_k
 constexpr int kChunks = kDk / 8 / kWarps;  // 8-wide d_k chunks per warp
 constexpr int kTb = 32;                // tokens per staged block
 constexpr int kB = 8;                  // tokens per block of the recurrence
@@ -100,7 +102,7 @@ __device__ __forceinline__ void ld8(const float *p, float (&v)[8]) {
 struct Stage {
   alignas(16) __nv_bfloat16 k[kTb][kRow];
   alignas(16) __nv_bfloat16 q[kTb][kRow];
-  alignas(16) __nv_bfloat16 v[kTb][kCols];
+  alignas(16) __nv_bfloat16 v[kTb][kGMax * kCols];
   alignas(16) float al[kTb];
   alignas(16) float be[kTb];
 };
@@ -110,8 +112,8 @@ struct GdnSmem {
   BlockTab tab[2][kSub];  // by staged-block parity
   // [buffer][warp][P, Q][column][token] partial sums; rows of 12 floats so
   // that the 8 columns a quarter-warp reads start in different banks
-  float part[2][kWarps][2][kCols][kB + 4];
-  alignas(16) float wu[kCols][kB + 4];  // g(8, l) u_l of the 16 columns (rows padded as part)
+  float part[2][kGMax * kWarps][2][kCols][kB + 4];
+  alignas(16) float wu[kGMax * kCols][kB + 4];  // g(8, l) u_l of the CTA's columns (rows padded as part)
 };
 static_assert(offsetof(Stage, q) % 16 == 0 && offsetof(Stage, v) % 16 == 0 &&
                   sizeof(Stage) % 16 == 0 && (kRow * 2) % 16 == 0,
@@ -160,12 +162,15 @@ __device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 x) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(x)) << 16;
 }
 
-// Raw copies of tokens [t0, t0 + n) for this CTA (value head h, columns j0..)
-// into stage s; rows past n are zeros with gate 1 and strength 0 (they leave
-// the state unchanged).  One commit group per call.
+// Raw copies of tokens [t0, t0 + n) for this CTA (value head h, G groups of
+// 16 columns from j0) into stage s by the CTA's G * 128 threads; rows past n
+// are zeros with gate 1 and strength 0 (they leave the state unchanged).  One
+// commit group per call.
+template <int G>
 __device__ __forceinline__ void stage_block(Stage &s, const GdnArgs &a, int t0, int n, int h,
                                             int hk, int j0, int tid) {
-  for (int i = tid; i < kTb * 32; i += kGdnThreads) {
+  constexpr int nt = G * kWarps * 32, pv = 2 * G;  // threads; 16-byte pieces of v per token
+  for (int i = tid; i < kTb * 32; i += nt) {
     const int t = i >> 5, p = i & 31, which = p >> 4, piece = p & 15;
     __nv_bfloat16 *dst = (which ? s.q[t] : s.k[t]) + piece * 8;
     if (t < n)
@@ -174,20 +179,20 @@ __device__ __forceinline__ void stage_block(Stage &s, const GdnArgs &a, int t0, 
     else
       *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
   }
-  for (int i = tid; i < kTb * 4; i += kGdnThreads) {
-    const int t = i >> 2, p = i & 3;
+  for (int i = tid; i < kTb * (pv + 2); i += nt) {
+    const int t = i / (pv + 2), p = i - t * (pv + 2);
     const long long tv = static_cast<long long>(t0 + t) * a.Hv + h;
     if (t < n) {
-      if (p < 2)
+      if (p < pv)
         cp_async16(smem_u32(&s.v[t][p * 8]), a.v + tv * a.dv + j0 + p * 8);
-      else if (p == 2)
+      else if (p == pv)
         cp_async4(&s.al[t], a.alpha + tv);
       else
         cp_async4(&s.be[t], a.beta + tv);
     } else {
-      if (p < 2)
+      if (p < pv)
         *reinterpret_cast<uint4 *>(&s.v[t][p * 8]) = make_uint4(0, 0, 0, 0);
-      else if (p == 2)
+      else if (p == pv)
         s.al[t] = 1.0f;
       else
         s.be[t] = 0.0f;
@@ -243,20 +248,28 @@ __device__ __forceinline__ void block_tables(const Stage &s, BlockTab &tb, int w
 }
 }  // namespace
 
-// grid: (H_v * d_v) / kCols CTAs of 4 warps; CTA b scans columns kCols b ..
-// of value head (kCols b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) of warp w
-// holds columns j0 + g and j0 + g + 8 at d_k chunks 4 w ..
-__global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
+// grid: (H_v * d_v) / (16 G) CTAs of 4 G warps; CTA b scans columns 16 G b ..
+// of value head (16 G b) / d_v.  Lane (g, c) = (lane / 4, lane % 4) of warp w
+// holds columns j0 + 16 (w / 4) + g and + 8 at d_k chunks 4 (w % 4) ..; lane
+// l of warp 0 runs the chain of column j0 + l (with G = 1, lanes 16..31 repeat
+// lanes 0..15).  Two groups per CTA give every lane of the chain warp a column
+// of its own, and with d_v = 128 one CTA per SM for 32 value heads.
+template <int G>
+__global__ void __launch_bounds__(G * kWarps * 32, 1) gdn_scan_kernel(GdnArgs a) {
+  constexpr int kColsCta = G * kCols;
   extern __shared__ __align__(16) uint8_t s_raw[];
   GdnSmem &sm = *reinterpret_cast<GdnSmem *>(s_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-  const int jc = lane & 15;  // the column this lane runs the chain for
-  const int col0 = blockIdx.x * kCols, h = col0 / a.dv, j0 = col0 - h * a.dv;
+  const int jc = lane & (kColsCta - 1);  // the column this lane runs the chain for
+  const int jg = jc >> 4, jl = jc & 15;  // its group and place in the group
+  const int col0 = blockIdx.x * kColsCta, h = col0 / a.dv, j0 = col0 - h * a.dv;
   const int hk = h / (a.Hv / a.Hk);
-  const int ch0 = warp * kChunks;  // this warp's first d_k chunk
+  const int cg = warp / kWarps;               // this warp's column group
+  const int ch0 = (warp % kWarps) * kChunks;  // this warp's first d_k chunk
   // st[n] = (S[g][8m + 2c], S[g][8m + 2c + 1], S[g + 8][8m + 2c], S[g + 8][8m + 2c + 1]), m = ch0 + n
   float st[kChunks][4];
-  const long long sb0 = (static_cast<long long>(h) * a.dv + j0 + g) * kDk + 8 * ch0 + 2 * c;
+  const long long sb0 =
+      (static_cast<long long>(h) * a.dv + j0 + kCols * cg + g) * kDk + 8 * ch0 + 2 * c;
   const long long sb8 = sb0 + 8LL * kDk;
 #pragma unroll
   for (int n = 0; n < kChunks; ++n) {
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
   // block but the last is whole), and warps 1..3 build the tables while warp
   // 0 runs the chains of b's third and fourth 8-token blocks.
   if (nblk > 0) {
-    stage_block(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, tid);
+    stage_block<G>(sm.st[0], a, 0, min(kTb, a.T), h, hk, j0, tid);
     cp_async_wait_group<0>();
     __syncthreads();
     if (warp < kSub) block_tables(sm.st[0], sm.tab[0][warp], warp, lane);
@@ -289,7 +302,8 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
   for (int b = 0; b < nblk; ++b) {
     const int t0 = b * kTb, n = min(kTb, a.T - t0);
     const bool next = b + 1 < nblk;
-    if (next) stage_block(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, tid);
+    if (next)
+      stage_block<G>(sm.st[(b + 1) & 1], a, t0 + kTb, min(kTb, a.T - t0 - kTb), h, hk, j0, tid);
     const Stage &S = sm.st[b & 1];
 #pragma unroll 1
     for (int sb = 0; sb * kB < n; ++sb, ++it) {
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
         mma_tf32(A[3], lo[0], lo[2], lo[1], lo[3], bf16_lo(qw), bf16_hi(qw));
       }
       // partials of columns g, g + 8 at tokens 2c, 2c + 1 into shared memory
-      float(&pt)[kWarps][2][kCols][kB + 4] = sm.part[it & 1];
+      float(&pt)[kGMax * kWarps][2][kCols][kB + 4] = sm.part[it & 1];
 #pragma unroll
       for (int pq = 0; pq < 2; ++pq) {
         const int y = 2 * pq;
@@ -336,8 +350,9 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
       __syncthreads();
       if (next && sb >= 2 && warp > 0) {
         // the next block's tables, one per warp and 8-token block, while warp
-        // 0 runs this block's chain: tables 0..2 now, table 3 in the next one
-        const int w = sb == 2 ? warp - 1 : (warp == 1 ? 3 : -1);
+        // 0 runs this block's chain: tables 0..3 now with two column groups,
+        // else 0..2 now and 3 in the next one
+        const int w = sb == 2 ? (warp <= kSub ? warp - 1 : -1) : (G == 1 && warp == 1 ? 3 : -1);
         if (w >= 0) block_tables(sm.st[(b + 1) & 1], sm.tab[(b + 1) & 1][w], w, lane);
       }
       if (warp == 0) {
@@ -349,8 +364,8 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
         for (int w = 0; w < kWarps; ++w) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            const float4 pv = *reinterpret_cast<const float4 *>(&pt[w][0][jc][4 * hf]);
-            const float4 qv = *reinterpret_cast<const float4 *>(&pt[w][1][jc][4 * hf]);
+            const float4 pv = *reinterpret_cast<const float4 *>(&pt[kWarps * jg + w][0][jl][4 * hf]);
+            const float4 qv = *reinterpret_cast<const float4 *>(&pt[kWarps * jg + w][1][jl][4 * hf]);
             p[4 * hf] += pv.x;
             p[4 * hf + 1] += pv.y;
             p[4 * hf + 2] += pv.z;
@@ -384,7 +399,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
 #pragma unroll
           for (int i = l; i < kB; ++i) O[i] = fmaf(dr[i], u[l], O[i]);
         }
-        if (lane < kCols) {
+        if (lane < kColsCta) {
 #pragma unroll
           for (int i = 0; i < kB; ++i)
             if (tb0 + i < n) ob[(t0 + tb0 + i) * ostride] = __float2bfloat16_rn(O[i]);
@@ -396,7 +411,8 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_scan_kernel(GdnArgs a) {
       __syncthreads();  // the scaled deltas are in shared memory
       // S <- A_8 S + W K with W[col][l] = g(8, l) u_l: A operand rows g, g + 8,
       // k = token c and c + 4
-      const float w0 = sm.wu[g][c], w1 = sm.wu[g + 8][c], w4 = sm.wu[g][c + 4], w5 = sm.wu[g + 8][c + 4];
+      const int wr = kCols * cg + g;  // this lane's rows of W: columns wr, wr + 8
+      const float w0 = sm.wu[wr][c], w1 = sm.wu[wr + 8][c], w4 = sm.wu[wr][c + 4], w5 = sm.wu[wr + 8][c + 4];
       const float a8 = reinterpret_cast<const float4 *>(tb.A + kB)->x;
       uint32_t wh[4], wl[4];
       split_tf32(w0, wh[0], wl[0]);  // a0 = (g, k c)
@@ -444,7 +460,9 @@ extern "C" int gdn_scan(const void *q, const void *k, const void *v, const float
   if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(state_in, 8) ||
       misaligned(state_out, 8) || misaligned(alpha, 4) || misaligned(beta, 4) || misaligned(o, 2))
     return MOE_ERR_ALIGNMENT;
-  if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gdn_scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(GdnSmem))) != cudaSuccess ||
+      cudaFuncSetAttribute(gdn_scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sizeof(GdnSmem))) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!state_out && T == 0) return MOE_OK;
@@ -461,7 +479,20 @@ extern "C" int gdn_scan(const void *q, const void *k, const void *v, const float
   a.Hk = n_k_heads;
   a.Hv = n_v_heads;
   a.dv = d_v;
-  const int grid = n_v_heads * d_v / kCols;
-  gdn_scan_kernel<<<grid, kGdnThreads, sizeof(GdnSmem), static_cast<cudaStream_t>(cuda_stream)>>>(a);
+  // Two groups of 16 columns per CTA where a head's columns split into them
+  // and one group per CTA would put two CTAs on some SM: the two groups'
+  // state products then share an SM's tensor issue inside one CTA instead of
+  // two CTAs' (measured 249 vs 257 us for 32 heads of 128 columns), while
+  // with fewer columns one group per CTA keeps each CTA's chain shortest
+  // (212 vs 262 us for a single head).
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (d_v % (kGMax * kCols) == 0 && static_cast<long long>(n_v_heads) * d_v / kCols > sms)
+    gdn_scan_kernel<kGMax><<<n_v_heads * d_v / (kGMax * kCols), kGMax * kWarps * 32, sizeof(GdnSmem), st>>>(a);
+  else
+    gdn_scan_kernel<1><<<n_v_heads * d_v / kCols, kWarps * 32, sizeof(GdnSmem), st>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -66,6 +66,7 @@ def run(dev, seed, T, Hk, Hv, dv, state=True):
     (1, 1, 1, 16, False),     # a single token from a zero state
     (64, 1, 3, 48, True),     # three value heads on one key head, exactly two blocks
     (300, 4, 4, 16, True),    # one value head per key head
+    (37, 4, 80, 32, True),    # 160 groups of 16 columns: two groups per CTA, ragged blocks
 ])
 def test_scan_matches_oracle(dev, T, Hk, Hv, dv, state):
     run(dev, 100 + T, T, Hk, Hv, dv, state)
