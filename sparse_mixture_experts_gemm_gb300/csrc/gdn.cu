@@ -38,12 +38,12 @@
 // and 2 c + 1) and the key rows are read with the same mapping.
 //
 // The chain.  The warps' partial P and Q meet in shared memory (two buffers);
-// warp 0 alone sums them, runs the chain for the 16 columns, one column per
-// lane (right-looking: once u_l is known it enters every later recall and
+// warp 0 alone sums them, runs the chain for the CTA's columns, one column
+// per lane (right-looking: once u_l is known it enters every later recall and
 // every output at once; only the u_i form a chain), writes the outputs and
-// leaves g(8, l) u_l in shared memory for the update, which all four warps
-// then apply to their quarters (two barriers per 8 tokens).  Running the
-// chain in one warp instead of four halves the instructions the CTA issues.
+// leaves g(8, l) u_l in shared memory for the update, which every warp then
+// applies to its quarter (two barriers per 8 tokens).  Running the chain in
+// one warp instead of four halves the instructions the CTA issues.
 //
 // Staging.  The CTA copies the bf16 q and k of its key head, its v columns
 // and the gates of the next 32 tokens by cp.async into the second of two
